@@ -1,0 +1,262 @@
+/*
+ * coli_oracle.c -- plain, slow, obviously-correct CPU oracle of the routed-MoE
+ * layer forward over int4-grouped expert weights.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the library (the CUDA path) includes,
+ * links or calls this file; only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark do.  It shares no code with the CUDA path.
+ *
+ * Sources (pages about the "colibri" pure-C MoE engine):
+ *   [P1] "Colibrì 深度解析:用 12 万行纯 C 把 744B MoE 塞进 25GB 笔记本"
+ *   [P2] "从源码开始colibri纯C引擎的编译、权重转换与.bin直映射实战"
+ *   [P4] "colibrì 路由遥测全解析.coli_usage专家历史、ROUTE_TRACE追踪流与route_trace.h统一格式"
+ *
+ * Precision: the quantiser works in f32 because the format fixes those bits
+ * (the converter divides float32 weights by a float32 scale and rounds with
+ * np.rint, which the engine mirrors with lrintf: [P2] §权重转换).  Everything
+ * else accumulates in double.  Expert ranking is decided on logits rounded to
+ * f32, the precision the GPU router decides in; gates are computed in double.
+ *
+ * Readings where the pages are silent (each listed in the design notes):
+ *   - scale rule s = max|w| / 7 per group (f32 division), elided on [P2];
+ *   - an all-zero group stores s = 0 and q = 0 (nibble 8);
+ *   - a NaN weight is ignored by the max and stored as q = 0;
+ *   - odd column count: the high nibble of the last byte is 0;
+ *   - routing = softmax over E, top-k (ties to the lower id), renormalise;
+ *   - NaN logits rank below every number; if all are NaN the slots take
+ *     experts 0..k-1 with gates 1/k ([P4] §测试与 CI, rt_router_pick);
+ *   - activation SwiGLU, silu(z) = z / (1 + e^-z); the shared expert is added
+ *     with weight 1 and is not counted.
+ *
+ * Build: cc -std=c11 -O2 -ffp-contract=off -fPIC -shared (no fast-math).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_GROUP 64
+
+/* ---------------------------------------------------------------------- */
+/* Format geometry: uint8[rows][ceil(cols/2)] nibbles, f32[rows][ceil(cols/64)]. */
+
+int64_t orc_packed_row_bytes(int64_t cols) { return (cols + 1) / 2; }
+int64_t orc_scales_per_row(int64_t cols) { return (cols + ORC_GROUP - 1) / ORC_GROUP; }
+
+/* ---------------------------------------------------------------------- */
+/* quant_int4_grouped ([P2] §权重转换): per row, per group of 64 columns along
+ * the row, s = max|w| / 7; q = clip(rint(w / s), -8, 7); stored unsigned as
+ * q + 8; even column -> low nibble, odd column -> high nibble. */
+void orc_quant_i4g(const float *w, int64_t rows, int64_t cols,
+                   uint8_t *packed, float *scales)
+{
+    const int64_t rb = orc_packed_row_bytes(cols);
+    const int64_t ng = orc_scales_per_row(cols);
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *wr = w + r * cols;
+        uint8_t *pr = packed + r * rb;
+        memset(pr, 0, (size_t)rb);
+        for (int64_t g = 0; g < ng; ++g) {
+            const int64_t c0 = g * ORC_GROUP;
+            const int64_t c1 = (c0 + ORC_GROUP < cols) ? c0 + ORC_GROUP : cols;
+            float m = 0.0f;
+            for (int64_t c = c0; c < c1; ++c) {
+                float a = fabsf(wr[c]);
+                if (a > m) m = a;              /* NaN never compares greater */
+            }
+            const float s = m / 7.0f;          /* IEEE f32 division */
+            scales[r * ng + g] = s;
+            for (int64_t c = c0; c < c1; ++c) {
+                int q;
+                if (s == 0.0f) {
+                    q = 0;
+                } else {
+                    float v = rintf(wr[c] / s); /* f32 divide, round half to even */
+                    if (v != v) q = 0;           /* NaN weight */
+                    else if (v < -8.0f) q = -8;
+                    else if (v > 7.0f) q = 7;
+                    else q = (int)v;
+                }
+                const uint8_t u = (uint8_t)(q + 8);
+                if ((c & 1) == 0) pr[c >> 1] |= u;
+                else pr[c >> 1] |= (uint8_t)(u << 4);
+            }
+        }
+    }
+}
+
+/* The engine consumes the packed rows directly (matmul_i4_grouped, [P2]):
+ * element (r, c) is s[r][c/64] * (u - 8). */
+static double orc_elem(const uint8_t *packed, const float *scales,
+                       int64_t rb, int64_t ng, int64_t r, int64_t c)
+{
+    const uint8_t b = packed[r * rb + (c >> 1)];
+    const int u = (c & 1) ? (b >> 4) : (b & 0x0F);
+    return (double)scales[r * ng + c / ORC_GROUP] * (double)(u - 8);
+}
+
+void orc_dequant_i4g(const uint8_t *packed, const float *scales,
+                     int64_t rows, int64_t cols, double *w)
+{
+    const int64_t rb = orc_packed_row_bytes(cols);
+    const int64_t ng = orc_scales_per_row(cols);
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c)
+            w[r * cols + c] = orc_elem(packed, scales, rb, ng, r, c);
+}
+
+/* y[r] = sum_c W[r][c] x[c] with W the dequantised matrix. */
+void orc_matvec_i4g(const uint8_t *packed, const float *scales,
+                    int64_t rows, int64_t cols, const double *x, double *y)
+{
+    const int64_t rb = orc_packed_row_bytes(cols);
+    const int64_t ng = orc_scales_per_row(cols);
+    for (int64_t r = 0; r < rows; ++r) {
+        double acc = 0.0;
+        for (int64_t c = 0; c < cols; ++c)
+            acc += orc_elem(packed, scales, rb, ng, r, c) * x[c];
+        y[r] = acc;
+    }
+}
+
+/* ---------------------------------------------------------------------- */
+/* Router GEMV: logits[t][e] = sum_h Wr[e][h] x[t][h]. */
+void orc_router_logits(const double *x, const double *wr, int64_t T, int64_t H,
+                       int64_t E, double *logits)
+{
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int64_t h = 0; h < H; ++h) acc += wr[e * H + h] * x[t * H + h];
+            logits[t * E + e] = acc;
+        }
+}
+
+/* Ranking key: the f32 logit; NaN below every number; equal keys -> lower id. */
+static int orc_ranks_before(float a, int64_t ia, float b, int64_t ib)
+{
+    const int na = (a != a), nb = (b != b);
+    if (na != nb) return nb;        /* the number ranks before the NaN */
+    if (!na && a != b) return a > b;
+    return ia < ib;
+}
+
+/* Top-k with renormalised softmax gates for one token.
+ * Softmax over all E followed by renormalisation over the k picked equals
+ * exp(l_j - l_0) / sum_{j'<k} exp(l_j' - l_0), l_0 the top logit.
+ * Returns 1 if any logit of the token is NaN, else 0. */
+int orc_topk(const double *logits, int64_t E, int k, int32_t *idx, double *gates)
+{
+    int64_t *ord = (int64_t *)malloc((size_t)E * sizeof(int64_t));
+    float *key = (float *)malloc((size_t)E * sizeof(float));
+    int any_nan = 0;
+    for (int64_t e = 0; e < E; ++e) {
+        ord[e] = e;
+        key[e] = (float)logits[e];
+        if (logits[e] != logits[e]) any_nan = 1;
+    }
+    /* insertion sort: slow, stable, plain */
+    for (int64_t i = 1; i < E; ++i) {
+        int64_t v = ord[i], j = i - 1;
+        while (j >= 0 && orc_ranks_before(key[v], v, key[ord[j]], ord[j])) {
+            ord[j + 1] = ord[j];
+            --j;
+        }
+        ord[j + 1] = v;
+    }
+    for (int j = 0; j < k; ++j) idx[j] = (int32_t)ord[j];
+    const double l0 = logits[ord[0]];
+    if (l0 != l0) {                  /* every logit NaN */
+        for (int j = 0; j < k; ++j) gates[j] = 1.0 / (double)k;
+    } else {
+        double den = 0.0;
+        for (int j = 0; j < k; ++j) {
+            const double lj = logits[ord[j]];
+            gates[j] = (lj != lj) ? 0.0 : exp(lj - l0);
+            den += gates[j];
+        }
+        for (int j = 0; j < k; ++j) gates[j] /= den;
+    }
+    free(ord);
+    free(key);
+    return any_nan;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Expert record: gate[F][H] | up[F][H] | down[H][F], each matrix in the
+ * packed format, stored adjacently ([P1] §四: the three matrices of an expert
+ * are stored next to each other and read in one go). */
+
+int64_t orc_expert_packed_bytes(int64_t H, int64_t F)
+{
+    return 2 * F * orc_packed_row_bytes(H) + H * orc_packed_row_bytes(F);
+}
+
+int64_t orc_expert_scales(int64_t H, int64_t F)
+{
+    return 2 * F * orc_scales_per_row(H) + H * orc_scales_per_row(F);
+}
+
+static double orc_silu(double z) { return z / (1.0 + exp(-z)); }
+
+/* y = Wd (silu(Wg x) * (Wu x)) */
+void orc_expert(const uint8_t *pe, const float *se, int64_t H, int64_t F,
+                const double *x, double *y)
+{
+    const uint8_t *pg = pe;
+    const uint8_t *pu = pg + F * orc_packed_row_bytes(H);
+    const uint8_t *pd = pu + F * orc_packed_row_bytes(H);
+    const float *sg = se;
+    const float *su = sg + F * orc_scales_per_row(H);
+    const float *sd = su + F * orc_scales_per_row(H);
+    double *g = (double *)malloc((size_t)F * sizeof(double));
+    double *u = (double *)malloc((size_t)F * sizeof(double));
+    orc_matvec_i4g(pg, sg, F, H, x, g);
+    orc_matvec_i4g(pu, su, F, H, x, u);
+    for (int64_t f = 0; f < F; ++f) g[f] = orc_silu(g[f]) * u[f];
+    orc_matvec_i4g(pd, sd, H, F, g, y);
+    free(g);
+    free(u);
+}
+
+/* One routed-MoE layer for T tokens ([P1] §十一 route -> union -> compute;
+ * [P4] route counts, one per routing decision).
+ *   x       [T][H]              layer input
+ *   wr      [E][H]              router weights
+ *   packed  experts 0..E+S-1    S = n_shared shared experts after the routed
+ *   out     [T][H]              sum_j gates[t][j] E_idx(x) + sum_s E_shared(x)
+ *   idx     [T][k], gates [T][k]
+ *   counts  [E]                 += 1 per (token, slot); may be NULL
+ * Returns the number of tokens that saw a NaN logit. */
+int orc_moe_forward(const double *x, int64_t T, int64_t H, int64_t F, int64_t E,
+                    int64_t n_shared, const double *wr, const uint8_t *packed,
+                    const float *scales, int k, double *out, int32_t *idx,
+                    double *gates, uint32_t *counts)
+{
+    const int64_t eb = orc_expert_packed_bytes(H, F);
+    const int64_t es = orc_expert_scales(H, F);
+    double *logits = (double *)malloc((size_t)(T * E) * sizeof(double));
+    double *y = (double *)malloc((size_t)H * sizeof(double));
+    int nan_tokens = 0;
+    orc_router_logits(x, wr, T, H, E, logits);
+    for (int64_t t = 0; t < T; ++t) {
+        nan_tokens += orc_topk(logits + t * E, E, k, idx + t * k, gates + t * k);
+        if (counts)
+            for (int j = 0; j < k; ++j) counts[idx[t * k + j]] += 1u;
+        double *o = out + t * H;
+        for (int64_t h = 0; h < H; ++h) o[h] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            const int64_t e = idx[t * k + j];
+            orc_expert(packed + e * eb, scales + e * es, H, F, x + t * H, y);
+            for (int64_t h = 0; h < H; ++h) o[h] += gates[t * k + j] * y[h];
+        }
+        for (int64_t s = 0; s < n_shared; ++s) {
+            const int64_t e = E + s;
+            orc_expert(packed + e * eb, scales + e * es, H, F, x + t * H, y);
+            for (int64_t h = 0; h < H; ++h) o[h] += y[h];
+        }
+    }
+    free(logits);
+    free(y);
+    return nan_tokens;
+}

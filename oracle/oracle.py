@@ -1,0 +1,175 @@
+"""ctypes shim over the plain-C oracle (``coli_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).  Takes and returns numpy
+arrays; all conversions here are exact widenings (bf16/f32 -> f32/f64).
+"""
+import ctypes as C
+
+import numpy as np
+
+from .build import build_oracle
+
+__all__ = [
+    "GROUP", "packed_row_bytes", "scales_per_row", "expert_packed_bytes",
+    "expert_scales", "quant_i4g", "dequant_i4g", "matvec_i4g", "router_logits",
+    "topk", "expert", "moe_forward", "moe_stack_forward", "lib",
+]
+
+GROUP = 64
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        L = C.CDLL(build_oracle())
+        i64, f32p, f64p = C.c_int64, C.POINTER(C.c_float), C.POINTER(C.c_double)
+        u8p, i32p, u32p = C.POINTER(C.c_uint8), C.POINTER(C.c_int32), C.POINTER(C.c_uint32)
+        L.orc_packed_row_bytes.argtypes = [i64]
+        L.orc_packed_row_bytes.restype = i64
+        L.orc_scales_per_row.argtypes = [i64]
+        L.orc_scales_per_row.restype = i64
+        L.orc_expert_packed_bytes.argtypes = [i64, i64]
+        L.orc_expert_packed_bytes.restype = i64
+        L.orc_expert_scales.argtypes = [i64, i64]
+        L.orc_expert_scales.restype = i64
+        L.orc_quant_i4g.argtypes = [f32p, i64, i64, u8p, f32p]
+        L.orc_quant_i4g.restype = None
+        L.orc_dequant_i4g.argtypes = [u8p, f32p, i64, i64, f64p]
+        L.orc_dequant_i4g.restype = None
+        L.orc_matvec_i4g.argtypes = [u8p, f32p, i64, i64, f64p, f64p]
+        L.orc_matvec_i4g.restype = None
+        L.orc_router_logits.argtypes = [f64p, f64p, i64, i64, i64, f64p]
+        L.orc_router_logits.restype = None
+        L.orc_topk.argtypes = [f64p, i64, C.c_int, i32p, f64p]
+        L.orc_topk.restype = C.c_int
+        L.orc_expert.argtypes = [u8p, f32p, i64, i64, f64p, f64p]
+        L.orc_expert.restype = None
+        L.orc_moe_forward.argtypes = [f64p, i64, i64, i64, i64, i64, f64p, u8p, f32p,
+                                      C.c_int, f64p, i32p, f64p, u32p]
+        L.orc_moe_forward.restype = C.c_int
+        _lib = L
+    return _lib
+
+
+def _p(a, ctype):
+    return a.ctypes.data_as(C.POINTER(ctype))
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def packed_row_bytes(cols):
+    return int(lib().orc_packed_row_bytes(cols))
+
+
+def scales_per_row(cols):
+    return int(lib().orc_scales_per_row(cols))
+
+
+def expert_packed_bytes(H, F):
+    return int(lib().orc_expert_packed_bytes(H, F))
+
+
+def expert_scales(H, F):
+    return int(lib().orc_expert_scales(H, F))
+
+
+def quant_i4g(w):
+    """w: [rows, cols] float32 (bf16 widened exactly).  -> (packed u8, scales f32)."""
+    w = _c(w, np.float32)
+    rows, cols = w.shape
+    packed = np.zeros((rows, packed_row_bytes(cols)), np.uint8)
+    scales = np.zeros((rows, scales_per_row(cols)), np.float32)
+    lib().orc_quant_i4g(_p(w, C.c_float), rows, cols, _p(packed, C.c_uint8),
+                        _p(scales, C.c_float))
+    return packed, scales
+
+
+def dequant_i4g(packed, scales, cols):
+    packed, scales = _c(packed, np.uint8), _c(scales, np.float32)
+    rows = packed.shape[0]
+    w = np.zeros((rows, cols), np.float64)
+    lib().orc_dequant_i4g(_p(packed, C.c_uint8), _p(scales, C.c_float), rows, cols,
+                          _p(w, C.c_double))
+    return w
+
+
+def matvec_i4g(packed, scales, cols, x):
+    packed, scales, x = _c(packed, np.uint8), _c(scales, np.float32), _c(x, np.float64)
+    rows = packed.shape[0]
+    y = np.zeros(rows, np.float64)
+    lib().orc_matvec_i4g(_p(packed, C.c_uint8), _p(scales, C.c_float), rows, cols,
+                         _p(x, C.c_double), _p(y, C.c_double))
+    return y
+
+
+def router_logits(x, wr):
+    """x [T, H], wr [E, H] -> logits [T, E] (float64)."""
+    x, wr = _c(x, np.float64), _c(wr, np.float64)
+    T, H = x.shape
+    E = wr.shape[0]
+    out = np.zeros((T, E), np.float64)
+    lib().orc_router_logits(_p(x, C.c_double), _p(wr, C.c_double), T, H, E,
+                            _p(out, C.c_double))
+    return out
+
+
+def topk(logits, k):
+    """logits [E] (float64) -> (idx int32 [k], gates float64 [k], any_nan)."""
+    logits = _c(logits, np.float64)
+    idx = np.zeros(k, np.int32)
+    gates = np.zeros(k, np.float64)
+    nan = lib().orc_topk(_p(logits, C.c_double), logits.shape[0], k,
+                         _p(idx, C.c_int32), _p(gates, C.c_double))
+    return idx, gates, bool(nan)
+
+
+def expert(packed_e, scales_e, H, F, x):
+    packed_e, scales_e, x = _c(packed_e, np.uint8), _c(scales_e, np.float32), _c(x, np.float64)
+    y = np.zeros(H, np.float64)
+    lib().orc_expert(_p(packed_e, C.c_uint8), _p(scales_e, C.c_float), H, F,
+                     _p(x, C.c_double), _p(y, C.c_double))
+    return y
+
+
+def moe_forward(x, wr, packed, scales, H, F, E, n_shared, k, counts=None):
+    """One routed-MoE layer.
+
+    x [T, H]; wr [E, H]; packed / scales: flat arrays holding experts 0..E+S-1
+    in the library layout.  Returns (out [T,H] f64, idx [T,k] i32, gates [T,k]
+    f64, nan_tokens).  ``counts`` (uint32 [E]) is accumulated in place.
+    """
+    x, wr = _c(x, np.float64), _c(wr, np.float64)
+    packed, scales = _c(packed.reshape(-1), np.uint8), _c(scales.reshape(-1), np.float32)
+    T = x.shape[0]
+    out = np.zeros((T, H), np.float64)
+    idx = np.zeros((T, k), np.int32)
+    gates = np.zeros((T, k), np.float64)
+    cp = None
+    if counts is not None:
+        assert counts.dtype == np.uint32 and counts.flags.c_contiguous
+        cp = _p(counts, C.c_uint32)
+    nan = lib().orc_moe_forward(_p(x, C.c_double), T, H, F, E, n_shared,
+                                _p(wr, C.c_double), _p(packed, C.c_uint8),
+                                _p(scales, C.c_float), k, _p(out, C.c_double),
+                                _p(idx, C.c_int32), _p(gates, C.c_double), cp)
+    return out, idx, gates, int(nan)
+
+
+def moe_stack_forward(x0, layers, H, F, E, n_shared, k, counts=None):
+    """Decode stack: x_{l+1} = x_l + MoE_l(x_l) (residual chain, no attention or norm).
+
+    ``layers`` is a list of (wr, packed, scales) per layer.  Returns
+    (x_L, per-layer outputs, per-layer idx).  ``counts`` is uint32 [L, E].
+    """
+    x = np.asarray(x0, np.float64)
+    outs, idxs = [], []
+    for l, (wr, packed, scales) in enumerate(layers):
+        c = None if counts is None else counts[l]
+        out, idx, _, _ = moe_forward(x, wr, packed, scales, H, F, E, n_shared, k, c)
+        outs.append(out)
+        idxs.append(idx)
+        x = x + out
+    return x, outs, idxs
