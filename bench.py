@@ -1,0 +1,452 @@
+"""Benchmark of the routed-MoE decode forward over int4-grouped experts on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl coli|reference]
+                    [--workload olmoe_decode|glm_decode_b1|glm_decode_b8|quant]
+
+Default workload: the OLMoE-like decode stack -- 16 MoE layers, hidden 2048, 64
+experts of FFN width 1024, top-8, no shared expert, int4-grouped g64 experts
+quantised from N(0, 0.02) bf16, bf16 router, batch 1 token of fresh N(0,1)
+input per step.  One step = one token through all 16 layers (router, top-k,
+route counts, batch union, gate/up + SwiGLU, down, combine, residual).
+
+Prints one JSON line (rank 0).  With torchrun (N > 1) every rank runs an
+independent replica on its own GPU (the decode path has no exchange step);
+`value` sums the ranks' tokens over the slowest rank's time.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "MoE decode tokens/s and int4 expert-weight GB/s vs GB300 HBM peak"
+
+# DRAM traffic per launch of the dominant kernel from an ncu capture of the
+# same kernel build (dram__bytes_read.sum + dram__bytes_write.sum); None until
+# a capture of the current kernel exists.  Source file named beside each value.
+NCU_TRAFFIC = {}
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1900.0)), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index, interval_ms=50):
+        self.gpu = gpu_index
+        self.interval = interval_ms
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [s.strip() for s in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        win = [s for t, s in self.samples if t0 <= t <= t1]
+        note = None
+        if len(win) < 3:  # timed region shorter than a few sampling intervals
+            mid = 0.5 * (t0 + t1)
+            win = [s for t, s in sorted(self.samples, key=lambda ts: abs(ts[0] - mid))[:5]]
+            note = "timed region shorter than 3 samples; nearest 5 samples used"
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(s[1]) for s in win if num(s[1]) is not None]
+        mx = [num(s[2]) for s in win if num(s[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in win for i in range(4)
+                          if len(s) > 5 + i and s[5 + i].lower().startswith("active")})
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(win)}
+        if note:
+            out["note"] = note
+        return out
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(v, world, dev):
+    if world == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# decode workloads
+
+
+class DecodeWorkload:
+    """A decode stack resident in HBM: weights, routers, per-step inputs."""
+
+    def __init__(self, shape, steps_total, dev, seed=0):
+        import int4_expert_ffn_gb300 as pkg
+        from int4_expert_ffn_gb300 import synth
+        self.coli = pkg.binding
+        self.synth = synth
+        self.shape = shape
+        self.dev = dev
+        c = self.coli
+        L, H, F, E, S, T = (shape.layers, shape.hidden, shape.ffn, shape.experts, shape.shared,
+                            shape.tokens)
+        self.eb = c.coli_expert_packed_bytes(H, F)
+        self.es = c.coli_expert_scale_count(H, F)
+        n = E + S
+        self.packed = torch.empty(L * n * self.eb, dtype=torch.uint8, device=dev)
+        self.scales = torch.empty(L * n * self.es, dtype=torch.float32, device=dev)
+        wrs = []
+        for l in range(L):
+            p0, s0 = l * n * self.eb, l * n * self.es
+            for e in range(n):
+                for m in range(3):
+                    w = synth.expert_matrix(shape, l, e, m, seed, device=dev)
+                    rows, cols = w.shape
+                    nb, ns = rows * cols // 2, rows * cols // 64
+                    c.coli_quant_i4g(w, self.packed[p0:p0 + nb].view(rows, -1),
+                                     self.scales[s0:s0 + ns].view(rows, -1))
+                    p0 += nb
+                    s0 += ns
+            wrs.append(synth.router_weights(shape, l, seed, device=dev))
+        self.router = torch.stack(wrs).contiguous()
+        self.x = torch.stack([synth.tokens(shape, seed, i, device=dev)
+                              for i in range(steps_total)]).contiguous()
+        self.out = torch.empty((steps_total, T, H), dtype=torch.float32, device=dev)
+        self.counts = torch.zeros((steps_total, L, E), dtype=torch.int32, device=dev)
+        self.desc = c.MoEDesc(H, F, E, S, T, c.COLI_F32,
+                              c.COLI_BF16 if shape.router_dtype == "bf16" else c.COLI_F32)
+        self.ws = c.new_workspace(self.desc, shape.top_k)
+        torch.cuda.synchronize()
+
+    def step(self, i, stream=None, x=None, out=None):
+        c = self.coli
+        c.coli_moe_stack_forward(self.desc, self.shape.top_k, self.shape.layers,
+                                 self.x[i] if x is None else x, self.router, self.packed,
+                                 self.scales, self.ws,
+                                 x_out=self.out[i] if out is None else out,
+                                 route_counts=self.counts[i], stream=stream)
+
+    def kernels_per_step(self):
+        passes = (self.shape.tokens + 15) // 16
+        return self.shape.layers * passes * 3
+
+    def algorithmic_bytes(self, steps):
+        """Bytes the method must move for the given steps: packed nibbles and
+        scales of every distinct expert each layer routed to, the shared
+        experts, the router weights, x in and out."""
+        sh = self.shape
+        per_expert = self.eb + 4 * self.es
+        cnt = self.counts[steps].cpu().numpy()             # [K, L, E]
+        unique = (cnt > 0).sum()
+        router_b = sh.experts * sh.hidden * (2 if sh.router_dtype == "bf16" else 4)
+        per_step_fixed = sh.layers * (sh.shared * per_expert + router_b + 2 * sh.tokens * sh.hidden * 4)
+        return int(unique * per_expert + len(steps) * per_step_fixed), int(unique)
+
+
+def capture_graphs(wl, idxs, stream):
+    graphs = []
+    for i in idxs:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            wl.step(i, stream=stream)
+        graphs.append(g)
+    return graphs
+
+
+def run_decode(args, shape, dev, world, rank):
+    steps, warmup = args.steps, args.warmup
+    wl = DecodeWorkload(shape, warmup + steps, dev)
+    stream = torch.cuda.Stream(device=dev)
+    # eager warm-up (first launches, module load), then graphs of each step
+    with torch.cuda.stream(stream):
+        wl.step(0, stream=stream)
+    stream.synchronize()
+    graphs = capture_graphs(wl, range(warmup + steps), stream)
+    wl.counts.zero_()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            graphs[i].replay()
+        # soak: keep the GPU at its steady clock before timing (untimed)
+        t_soak = time.time()
+        while time.time() - t_soak < 0.3:
+            for i in range(warmup):
+                graphs[i].replay()
+            stream.synchronize()
+    wl.counts.zero_()
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[0]))
+    sampler.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(warmup, warmup + steps):
+            graphs[i].replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    time.sleep(0.15)
+    sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(ms, world, dev)
+    tokens = steps * shape.tokens
+    alg_bytes, n_unique = wl.algorithmic_bytes(list(range(warmup, warmup + steps)))
+    res = {
+        "tokens_per_rank": tokens,
+        "ms": ms_max,
+        "alg_bytes": alg_bytes,
+        "unique_experts": n_unique,
+        "clocks": sampler.summary(t0, t1),
+        "launches": steps * wl.kernels_per_step(),
+    }
+    res["e2e"] = run_e2e(wl, args, dev, world, stream)
+    del graphs
+    return wl, res
+
+
+def run_e2e(wl, args, dev, world, stream):
+    """Same metric through the public API with host buffers: each step copies its
+    input from pinned host memory, runs the stack, and reads the output back."""
+    sh = wl.shape
+    steps, warmup = args.steps, args.warmup
+    n = warmup + steps
+    host_x = wl.x.cpu().pin_memory()
+    host_out = torch.empty((n, sh.tokens, sh.hidden), dtype=torch.float32).pin_memory()
+    dx = torch.empty((sh.tokens, sh.hidden), dtype=torch.float32, device=dev)
+    dout = torch.empty((sh.tokens, sh.hidden), dtype=torch.float32, device=dev)
+    graphs = []
+    for i in range(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            dx.copy_(host_x[i], non_blocking=True)
+            wl.step(i, stream=stream, x=dx, out=dout)
+            host_out[i].copy_(dout, non_blocking=True)
+        graphs.append(g)
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            graphs[i].replay()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(warmup, n):
+            graphs[i].replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+    assert torch.equal(host_out[warmup:n], wl.out[warmup:n].cpu()), "e2e output mismatch"
+    bi = sh.tokens * sh.hidden * 4
+    return {"value": world * steps * sh.tokens / (ms / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bi}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample of the same workload
+
+
+def oracle_baseline(shape, dev, budget_s=15.0, seed=0):
+    """Time the oracle on layer 0 of the stack for as many fresh tokens as fit
+    in ~budget_s of CPU work; scale to tokens/s of the full stack."""
+    import oracle as orc
+    from int4_expert_ffn_gb300 import synth
+    H, F, E, S, k = shape.hidden, shape.ffn, shape.experts, shape.shared, shape.top_k
+    wr = synth.router_weights(shape, 0, seed, device=dev).double().cpu().numpy()
+    eb = orc.expert_packed_bytes(H, F)
+    es = orc.expert_scales(H, F)
+    packed = np.zeros((E + S) * eb, np.uint8)
+    scales = np.zeros((E + S) * es, np.float32)
+    done = set()
+
+    def materialise(experts):
+        for e in experts:
+            if e in done:
+                continue
+            ps, ss = [], []
+            for m in range(3):
+                w = synth.expert_matrix(shape, 0, e, m, seed, device=dev).float().cpu().numpy()
+                p, s = orc.quant_i4g(w)
+                ps.append(p.reshape(-1))
+                ss.append(s.reshape(-1))
+            packed[e * eb:(e + 1) * eb] = np.concatenate(ps)
+            scales[e * es:(e + 1) * es] = np.concatenate(ss)
+            done.add(e)
+
+    materialise(range(E, E + S))
+    n_tok, spent = 0, 0.0
+    while spent < budget_s and n_tok < 64:
+        x = synth.tokens(shape, seed, 10_000 + n_tok, device=dev).double().cpu().numpy()
+        lg = orc.router_logits(x, wr)
+        materialise(sorted({int(e) for row in lg for e in np.argsort(-row)[:k + 2]}))
+        t = time.perf_counter()
+        orc.moe_forward(x, wr, packed, scales, H, F, E, S, k)
+        spent += time.perf_counter() - t
+        n_tok += shape.tokens
+    per_token_layer = spent / n_tok
+    value = 1.0 / (per_token_layer * shape.layers)
+    return {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": "%d fresh tokens through layer 0 of the %d-layer stack (%.1f s of "
+                      "single-thread oracle time), scaled x%d layers"
+                      % (n_tok, shape.layers, spent, shape.layers)}
+
+
+# ---------------------------------------------------------------------------
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="coli", choices=["coli", "reference"])
+    ap.add_argument("--workload", default="olmoe_decode",
+                    choices=["olmoe_decode", "glm_decode_b1", "glm_decode_b8"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+
+    from int4_expert_ffn_gb300 import synth
+    shape = synth.SHAPES[args.workload]
+    config = {"workload": "%s: %d MoE layers, hidden %d, %d experts of FFN width %d, top-%d, "
+                          "%d shared, batch %d, int4-grouped g64 f32 scales, %s router"
+                          % (shape.name, shape.layers, shape.hidden, shape.experts, shape.ffn,
+                             shape.top_k, shape.shared, shape.tokens, shape.router_dtype),
+              "layers": shape.layers, "hidden": shape.hidden, "experts": shape.experts,
+              "ffn": shape.ffn, "top_k": shape.top_k, "shared": shape.shared,
+              "batch": shape.tokens, "parallelism": "replicas" if world > 1 else "single",
+              "l2": "inputs larger than L2: %.2f GB of experts resident, fresh routing each step"}
+
+    if args.impl == "reference":
+        if rank == 0:
+            base = oracle_baseline(shape, dev)
+            line = {"metric": METRIC, "value": base["value"], "unit": "tokens/s",
+                    "impl": "reference", "n_gpus": args.gpus, "steps": args.steps,
+                    "warmup": args.warmup, "higher_is_better": True, "dtype": "f64",
+                    "data": "synthetic", "config": dict(config, l2="n/a (CPU)"),
+                    "cpu_baseline": base,
+                    "e2e": {"value": base["value"], "unit": "tokens/s",
+                            "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    from int4_expert_ffn_gb300 import build as b
+    if rank == 0:
+        b.build()
+    barrier(world)
+    wl, res = run_decode(args, shape, dev, world, rank)
+    resident = wl.packed.numel() + 4 * wl.scales.numel()
+    config["l2"] = config["l2"] % (resident / 1e9)
+    hbm_peak, _, peak_kind = read_peaks()
+    sec = res["ms"] / 1e3
+    value = world * res["tokens_per_rank"] / sec
+    gbs = res["alg_bytes"] / sec / 1e9
+    kernel = "decode step (router + gate/up + down per layer, CUDA graph)"
+    traffic = NCU_TRAFFIC.get(args.workload)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"] / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; weights N(0,0.02) bf16 quantised on the GPU)",
+        "config": config,
+        "gbs": gbs,
+        "roofline": {"bound": "hbm", "kernel": kernel, "achieved": gbs, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": gbs / hbm_peak, "peak_kind": peak_kind,
+                     "traffic": traffic,
+                     "alg_bytes_per_step": res["alg_bytes"] / args.steps},
+        "clocks": res["clocks"],
+        "e2e": res["e2e"],
+        "gpu_launches": res["launches"],
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_baseline(shape, dev)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

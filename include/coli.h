@@ -1,0 +1,171 @@
+/*
+ * coli.h -- C ABI of the GB300 (sm_103a) routed-MoE forward over int4-grouped
+ * expert weights.
+ *
+ * What it computes (pages about the "colibri" pure-C MoE engine):
+ *   [P1] "Colibrì 深度解析:用 12 万行纯 C 把 744B MoE 塞进 25GB 笔记本"
+ *   [P2] "从源码开始colibri纯C引擎的编译、权重转换与.bin直映射实战"
+ *   [P4] "colibrì 路由遥测全解析.coli_usage专家历史、ROUTE_TRACE追踪流与route_trace.h统一格式"
+ *
+ * Weight format ([P2] §权重转换, quant_int4_grouped / matmul_i4_grouped):
+ * a matrix W[O][I] is stored as
+ *   packed  uint8 [O][ceil(I/2)]   element (o,i) is nibble u = q + 8 of byte
+ *                                  i/2, low nibble for even i, high for odd i
+ *   scales  f32   [O][ceil(I/64)]  one scale per 64 consecutive columns
+ * and W[o][i] = scales[o][i/64] * (u - 8).
+ *
+ * Expert record ([P1] §四: an expert's three matrices sit next to each other):
+ *   packed_experts = for e in 0 .. E+S-1:  gate[F][H/2] | up[F][H/2] | down[H][F/2]
+ *   scales         = for e in 0 .. E+S-1:  gate[F][H/64] | up[F][H/64] | down[H][F/64]
+ * experts 0..E-1 are routed, E..E+S-1 are the S shared experts.
+ *
+ * Conventions of every entry point:
+ *   - all array arguments are DEVICE pointers owned by the caller; the library
+ *     allocates no memory on any call (scratch lives in the caller's workspace);
+ *   - work is enqueued on `stream` and is asynchronous; COLI_OK means the
+ *     arguments were valid and the launches were accepted;
+ *   - arguments are validated on the host before anything is launched; a
+ *     rejected call has no side effect;
+ *   - device-side conditions (NaN router logits) are recorded as flag bits
+ *     in the workspace and read back with coli_moe_check().
+ */
+#ifndef COLI_H
+#define COLI_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    COLI_OK = 0,
+    COLI_EINVAL = -1,        /* null pointer, bad size or dtype */
+    COLI_EALIGN = -2,        /* a pointer is not 16-byte aligned */
+    COLI_ECUDA = -3,         /* a CUDA launch or query failed */
+    COLI_ETIMEOUT = -4,      /* a bounded device-side wait gave up */
+    COLI_ENOMEM = -5,        /* the caller's workspace is too small */
+    COLI_EUNSUPPORTED = -6   /* valid, but outside what this build handles */
+} coli_status;
+
+typedef enum { COLI_F32 = 0, COLI_BF16 = 1 } coli_dtype;
+
+/* Device-side flag bits (coli_moe_check). */
+#define COLI_FLAG_NAN_LOGITS 0x1u   /* a token had a NaN router logit */
+#define COLI_FLAG_TIMEOUT    0x2u   /* a bounded wait gave up */
+
+/* Shape of one MoE layer call. */
+typedef struct {
+    int32_t hidden;        /* H: multiple of 64, 64 .. 16384 */
+    int32_t ffn;           /* F: multiple of 64, 64 .. 16384 */
+    int32_t n_experts;     /* E routed experts, 1 .. 1024 */
+    int32_t n_shared;      /* S shared experts, 0 .. 8 */
+    int32_t n_tokens;      /* T tokens in this call, >= 0 (0 is a no-op) */
+    coli_dtype x_dtype;    /* activations x: COLI_F32 or COLI_BF16 */
+    coli_dtype router_dtype; /* router weights: COLI_F32 or COLI_BF16 */
+} coli_moe_desc;
+
+const char *coli_status_str(int status);
+
+/* Size helpers of the packed format (bytes / element counts). */
+int64_t coli_packed_row_bytes(int64_t cols);            /* ceil(cols/2) */
+int64_t coli_scales_per_row(int64_t cols);              /* ceil(cols/64) */
+int64_t coli_expert_packed_bytes(int64_t H, int64_t F); /* 2 F ceil(H/2) + H ceil(F/2) */
+int64_t coli_expert_scale_count(int64_t H, int64_t F);  /* 2 F ceil(H/64) + H ceil(F/64) */
+
+/*
+ * coli_quant_i4g -- quantise W[rows][cols] into the int4-grouped format
+ * ([P2] §权重转换, quant_int4_grouped).  Per row and per group of 64 columns:
+ *   s = max|w| / 7            (f32 division, round to nearest even)
+ *   q = clip(rint(w / s), -8, 7)  (f32 division; rint rounds half to even)
+ *   u = q + 8; byte j of a row = u[2j] | u[2j+1] << 4
+ * A group whose max is 0 stores s = 0 and u = 8; a NaN weight stores u = 8;
+ * with an odd column count the high nibble of the last byte is 0.
+ *   w        [rows][cols] row-major, dtype w_dtype (COLI_BF16 or COLI_F32)
+ *   packed   [rows][ceil(cols/2)]  written
+ *   scales   [rows][ceil(cols/64)] written
+ * rows >= 0, cols >= 1.  Any alignment is accepted; 16-byte aligned pointers
+ * with cols % 64 == 0 take the vectorised path.  Result is bit-identical to
+ * the definition above for every finite input.
+ */
+int coli_quant_i4g(const void *w, coli_dtype w_dtype, int64_t rows, int64_t cols,
+                   uint8_t *packed, float *scales, cudaStream_t stream);
+
+/*
+ * Workspace: every routed call needs caller-owned device scratch of at least
+ * the returned size, 256-byte aligned.  It must be zero-filled once before its
+ * first use (cudaMemset); each call leaves it ready for the next.  Calls that
+ * share one workspace must be ordered (same stream or events).
+ */
+size_t coli_router_workspace_size(const coli_moe_desc *d, int top_k);
+size_t coli_moe_workspace_size(const coli_moe_desc *d, int top_k);
+
+/*
+ * coli_router_topk -- router GEMV, top-k selection and route counts
+ * ([P1] §十一 "route"; [P4] §追踪流: gates are the normalised values the
+ * layer applies; §从新引擎接入: one count per routing decision).
+ *   logits[t][e] = sum_h router_w[e][h] x[t][h]      (f32 accumulation)
+ *   idx[t][0..k-1]  the k largest logits, descending; equal logits -> lower e;
+ *                   NaN ranks below every number
+ *   gates[t][j]     softmax over all E renormalised over the k picked
+ *                   = exp(l_j - l_0) / sum_{j'<k} exp(l_j' - l_0);
+ *                   a picked NaN logit gets gate 0; if every logit of a
+ *                   token is NaN, idx = 0..k-1 and gates = 1/k
+ *                   ([P4] §测试与 CI, the rt_router_pick fallback), and
+ *                   COLI_FLAG_NAN_LOGITS is set in the workspace
+ *   route_counts[e] += number of (t, j) with idx[t][j] == e  (may be NULL;
+ *                   never zeroed by the library: counts accumulate)
+ *   x [T][H] (d->x_dtype), router_w [E][H] (d->router_dtype),
+ *   idx int32 [T][k], gates f32 [T][k].   1 <= top_k <= min(E, 64).
+ */
+int coli_router_topk(const coli_moe_desc *d, int top_k, const void *x,
+                     const void *router_w, int32_t *idx, float *gates,
+                     uint32_t *route_counts, void *workspace, size_t ws_bytes,
+                     cudaStream_t stream);
+
+/*
+ * coli_moe_forward -- one routed-MoE layer ([P1] §十一: route, union of the
+ * batch's experts, expert FFNs, combine).
+ *   out[t] = sum_j gates[t][j] * E_{idx[t][j]}(x[t]) + sum_s E_{E+s}(x[t])
+ *   E_e(x) = Wd_e (silu(Wg_e x) * (Wu_e x)),  silu(z) = z / (1 + e^-z)
+ * with routing as in coli_router_topk (route_counts updated the same way; the
+ * shared experts are not counted).  Each expert used by the batch is read
+ * once (batch union).  The per-token sum runs in a fixed order, so results
+ * are deterministic.
+ *   x [T][H] (d->x_dtype), router_w [E][H], packed_experts / scales in the
+ *   expert record layout above, out f32 [T][H].
+ */
+int coli_moe_forward(const coli_moe_desc *d, int top_k, const void *x,
+                     const void *router_w, const uint8_t *packed_experts,
+                     const float *scales, float *out, uint32_t *route_counts,
+                     void *workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * coli_moe_stack_forward -- n_layers MoE layers chained through a residual
+ * stream (decode stack without attention or norms):
+ *   x_0 = x;  x_{l+1} = x_l + MoE_l(x_l);  x_out = x_{n_layers}
+ * Layer l uses router_w + l*E*H elements, packed_experts + l*(E+S)*
+ * coli_expert_packed_bytes(H,F), scales + l*(E+S)*coli_expert_scale_count(H,F),
+ * route_counts + l*E.  x is d->x_dtype; x_out f32 [T][H]; layer_out (may be
+ * NULL) receives MoE_l(x_l) as f32 [n_layers][T][H].  Same workspace size as
+ * coli_moe_forward.
+ */
+int coli_moe_stack_forward(const coli_moe_desc *d, int top_k, int n_layers,
+                           const void *x, const void *router_w,
+                           const uint8_t *packed_experts, const float *scales,
+                           float *x_out, float *layer_out, uint32_t *route_counts,
+                           void *workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * coli_moe_check -- read (and optionally clear) the device-side flag word of a
+ * workspace.  Synchronises `stream`.  *flags receives COLI_FLAG_* bits.
+ * Returns COLI_ETIMEOUT if COLI_FLAG_TIMEOUT is set, else COLI_OK.
+ */
+int coli_moe_check(void *workspace, int clear, uint32_t *flags, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* COLI_H */

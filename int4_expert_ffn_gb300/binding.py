@@ -1,0 +1,224 @@
+"""Python binding of libcoli, the GB300 routed-MoE forward over int4-grouped experts.
+
+Argument marshalling only: every function forwards torch tensors' device
+pointers and the current CUDA stream to the C ABI in ``include/coli.h`` under
+the same name.  All computation runs in the library's CUDA kernels; there is
+no CPU or PyTorch fallback -- importing this package fails loudly when
+``libcoli.so`` is missing, and calls fail when no GPU is present.
+"""
+import ctypes as C
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libcoli.so")
+
+COLI_OK, COLI_EINVAL, COLI_EALIGN, COLI_ECUDA, COLI_ETIMEOUT, COLI_ENOMEM, COLI_EUNSUPPORTED = (
+    0, -1, -2, -3, -4, -5, -6)
+COLI_F32, COLI_BF16 = 0, 1
+COLI_FLAG_NAN_LOGITS, COLI_FLAG_TIMEOUT = 0x1, 0x2
+GROUP = 64
+
+# every symbol include/coli.h declares
+EXPORTS = (
+    "coli_status_str", "coli_packed_row_bytes", "coli_scales_per_row",
+    "coli_expert_packed_bytes", "coli_expert_scale_count", "coli_quant_i4g",
+    "coli_router_workspace_size", "coli_moe_workspace_size", "coli_router_topk",
+    "coli_moe_forward", "coli_moe_stack_forward", "coli_moe_check",
+)
+
+
+class ColiError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__("%s failed: %s (%d)" % (fn, _status_str(status), status))
+
+
+class coli_moe_desc(C.Structure):
+    _fields_ = [("hidden", C.c_int32), ("ffn", C.c_int32), ("n_experts", C.c_int32),
+                ("n_shared", C.c_int32), ("n_tokens", C.c_int32), ("x_dtype", C.c_int),
+                ("router_dtype", C.c_int)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            "libcoli.so is not built (expected at %s); run "
+            "`python -c 'import __graft_entry__ as g; g.build()'`" % LIB_PATH)
+    L = C.CDLL(LIB_PATH)
+    vp, i64, sz = C.c_void_p, C.c_int64, C.c_size_t
+    dp = C.POINTER(coli_moe_desc)
+    L.coli_status_str.argtypes = [C.c_int]
+    L.coli_status_str.restype = C.c_char_p
+    for f in ("coli_packed_row_bytes", "coli_scales_per_row"):
+        getattr(L, f).argtypes = [i64]
+        getattr(L, f).restype = i64
+    for f in ("coli_expert_packed_bytes", "coli_expert_scale_count"):
+        getattr(L, f).argtypes = [i64, i64]
+        getattr(L, f).restype = i64
+    L.coli_quant_i4g.argtypes = [vp, C.c_int, i64, i64, vp, vp, vp]
+    L.coli_quant_i4g.restype = C.c_int
+    for f in ("coli_router_workspace_size", "coli_moe_workspace_size"):
+        getattr(L, f).argtypes = [dp, C.c_int]
+        getattr(L, f).restype = sz
+    L.coli_router_topk.argtypes = [dp, C.c_int, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.coli_router_topk.restype = C.c_int
+    L.coli_moe_forward.argtypes = [dp, C.c_int, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.coli_moe_forward.restype = C.c_int
+    L.coli_moe_stack_forward.argtypes = [dp, C.c_int, C.c_int, vp, vp, vp, vp, vp, vp, vp,
+                                         vp, sz, vp]
+    L.coli_moe_stack_forward.restype = C.c_int
+    L.coli_moe_check.argtypes = [vp, C.c_int, C.POINTER(C.c_uint32), vp]
+    L.coli_moe_check.restype = C.c_int
+    return L
+
+
+lib = _load()
+
+
+def _status_str(status):
+    return lib.coli_status_str(status).decode()
+
+
+def _check(fn, status):
+    if status != COLI_OK:
+        raise ColiError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _dt(t):
+    if t.dtype == torch.float32:
+        return COLI_F32
+    if t.dtype == torch.bfloat16:
+        return COLI_BF16
+    raise TypeError("expected float32 or bfloat16, got %s" % t.dtype)
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+@dataclass(frozen=True)
+class MoEDesc:
+    hidden: int
+    ffn: int
+    n_experts: int
+    n_shared: int
+    n_tokens: int
+    x_dtype: int = COLI_F32
+    router_dtype: int = COLI_BF16
+
+    def c(self):
+        return coli_moe_desc(self.hidden, self.ffn, self.n_experts, self.n_shared,
+                             self.n_tokens, self.x_dtype, self.router_dtype)
+
+
+def coli_packed_row_bytes(cols):
+    return lib.coli_packed_row_bytes(cols)
+
+
+def coli_scales_per_row(cols):
+    return lib.coli_scales_per_row(cols)
+
+
+def coli_expert_packed_bytes(H, F):
+    return lib.coli_expert_packed_bytes(H, F)
+
+
+def coli_expert_scale_count(H, F):
+    return lib.coli_expert_scale_count(H, F)
+
+
+def coli_quant_i4g(w, packed=None, scales=None, stream=None):
+    """Quantise w [rows, cols] (bf16 or f32, CUDA) -> (packed u8, scales f32)."""
+    _cuda(w)
+    rows, cols = w.shape
+    if packed is None:
+        packed = torch.empty((rows, coli_packed_row_bytes(cols)), dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty((rows, coli_scales_per_row(cols)), dtype=torch.float32, device=w.device)
+    _cuda(packed, scales)
+    _check("coli_quant_i4g", lib.coli_quant_i4g(_ptr(w), _dt(w), rows, cols, _ptr(packed),
+                                                 _ptr(scales), _stream(stream)))
+    return packed, scales
+
+
+def coli_moe_workspace_size(desc: MoEDesc, top_k):
+    d = desc.c()
+    return lib.coli_moe_workspace_size(C.byref(d), top_k)
+
+
+def coli_router_workspace_size(desc: MoEDesc, top_k):
+    d = desc.c()
+    return lib.coli_router_workspace_size(C.byref(d), top_k)
+
+
+def new_workspace(desc: MoEDesc, top_k, device="cuda"):
+    """Zero-filled workspace of the size the library asks for."""
+    n = coli_moe_workspace_size(desc, top_k)
+    if n == 0:
+        raise ColiError("coli_moe_workspace_size", COLI_EINVAL)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def coli_router_topk(desc: MoEDesc, top_k, x, router_w, workspace, idx=None, gates=None,
+                     route_counts=None, stream=None):
+    _cuda(x, router_w, workspace, route_counts)
+    T = desc.n_tokens
+    if idx is None:
+        idx = torch.empty((T, top_k), dtype=torch.int32, device=x.device)
+    if gates is None:
+        gates = torch.empty((T, top_k), dtype=torch.float32, device=x.device)
+    d = desc.c()
+    _check("coli_router_topk", lib.coli_router_topk(
+        C.byref(d), top_k, _ptr(x), _ptr(router_w), _ptr(idx), _ptr(gates),
+        _ptr(route_counts), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return idx, gates
+
+
+def coli_moe_forward(desc: MoEDesc, top_k, x, router_w, packed_experts, scales, workspace,
+                     out=None, route_counts=None, stream=None):
+    _cuda(x, router_w, packed_experts, scales, workspace, out, route_counts)
+    if out is None:
+        out = torch.empty((desc.n_tokens, desc.hidden), dtype=torch.float32, device=x.device)
+    d = desc.c()
+    _check("coli_moe_forward", lib.coli_moe_forward(
+        C.byref(d), top_k, _ptr(x), _ptr(router_w), _ptr(packed_experts), _ptr(scales),
+        _ptr(out), _ptr(route_counts), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def coli_moe_stack_forward(desc: MoEDesc, top_k, n_layers, x, router_w, packed_experts, scales,
+                           workspace, x_out=None, layer_out=None, route_counts=None,
+                           stream=None):
+    _cuda(x, router_w, packed_experts, scales, workspace, x_out, layer_out, route_counts)
+    if x_out is None:
+        x_out = torch.empty((desc.n_tokens, desc.hidden), dtype=torch.float32, device=x.device)
+    d = desc.c()
+    _check("coli_moe_stack_forward", lib.coli_moe_stack_forward(
+        C.byref(d), top_k, n_layers, _ptr(x), _ptr(router_w), _ptr(packed_experts),
+        _ptr(scales), _ptr(x_out), _ptr(layer_out), _ptr(route_counts), _ptr(workspace),
+        workspace.numel(), _stream(stream)))
+    return x_out
+
+
+def coli_moe_check(workspace, clear=True, stream=None):
+    """Return the device-side flag word (COLI_FLAG_*) of a workspace; clears it by default."""
+    flags = C.c_uint32(0)
+    st = lib.coli_moe_check(_ptr(workspace), 1 if clear else 0, C.byref(flags), _stream(stream))
+    if st not in (COLI_OK, COLI_ETIMEOUT):
+        raise ColiError("coli_moe_check", st)
+    return flags.value

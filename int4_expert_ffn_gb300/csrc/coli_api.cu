@@ -1,0 +1,230 @@
+// C ABI entry points of libcoli: host-side validation, workspace layout and
+// dispatch.  Declarations and the meaning of every argument are in coli.h.
+#include <limits.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "coli_internal.cuh"
+
+namespace coli {
+
+static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+WsLayout ws_layout(int T, int H, int F, int E, int S, int k) {
+  WsLayout L{};
+  size_t o = 0;
+  const size_t KS = (size_t)k + S;
+  L.ctrl = o;      o = align256(o + kCtrlWords * sizeof(uint32_t));
+  L.logits = o;    o = align256(o + (size_t)T * E * sizeof(float));
+  L.idx = o;       o = align256(o + (size_t)T * k * sizeof(int32_t));
+  L.gates = o;     o = align256(o + (size_t)T * k * sizeof(float));
+  L.act = o;       o = align256(o + (size_t)(2 * (E + S) + 2) * sizeof(int32_t));
+  L.routes = o;    o = align256(o + (size_t)T * KS * sizeof(int32_t));
+  L.slot_gate = o; o = align256(o + (size_t)T * KS * sizeof(float));
+  L.h = o;         o = align256(o + (size_t)T * KS * F * sizeof(float));
+  L.total = o;
+  (void)H;
+  return L;
+}
+
+int num_sms() {
+  static int sms = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0)
+      sms = 148;
+  });
+  return sms;
+}
+
+}  // namespace coli
+
+using namespace coli;
+
+namespace {
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+int check_desc(const coli_moe_desc *d, int top_k) {
+  if (!d) return COLI_EINVAL;
+  if (d->hidden < 64 || d->hidden > 16384 || d->hidden % kGroup) return COLI_EINVAL;
+  if (d->ffn < 64 || d->ffn > 16384 || d->ffn % kGroup) return COLI_EINVAL;
+  if (d->n_experts < 1 || d->n_experts > kMaxExperts) return COLI_EINVAL;
+  if (d->n_shared < 0 || d->n_shared > kMaxShared) return COLI_EINVAL;
+  if (d->n_tokens < 0) return COLI_EINVAL;
+  if (top_k < 1 || top_k > d->n_experts || top_k > kMaxTopK) return COLI_EINVAL;
+  if ((d->x_dtype != COLI_F32 && d->x_dtype != COLI_BF16) ||
+      (d->router_dtype != COLI_F32 && d->router_dtype != COLI_BF16))
+    return COLI_EINVAL;
+  return COLI_OK;
+}
+
+// Tokens per internal pass of the GEMV path; larger calls run in passes.
+int pass_tokens(int T) { return T < kDecodeMaxT ? T : kDecodeMaxT; }
+
+int map_err(cudaError_t e) { return e == cudaSuccess ? COLI_OK : COLI_ECUDA; }
+
+size_t xsize(coli_dtype t) { return t == COLI_BF16 ? 2 : 4; }
+
+}  // namespace
+
+extern "C" {
+
+const char *coli_status_str(int status) {
+  switch (status) {
+    case COLI_OK: return "ok";
+    case COLI_EINVAL: return "invalid argument";
+    case COLI_EALIGN: return "pointer not 16-byte aligned";
+    case COLI_ECUDA: return "CUDA error";
+    case COLI_ETIMEOUT: return "device-side wait timed out";
+    case COLI_ENOMEM: return "workspace too small";
+    case COLI_EUNSUPPORTED: return "unsupported configuration";
+    default: return "unknown status";
+  }
+}
+
+int64_t coli_packed_row_bytes(int64_t cols) { return cols < 0 ? 0 : (cols + 1) / 2; }
+int64_t coli_scales_per_row(int64_t cols) { return cols < 0 ? 0 : (cols + kGroup - 1) / kGroup; }
+int64_t coli_expert_packed_bytes(int64_t H, int64_t F) {
+  return 2 * F * coli_packed_row_bytes(H) + H * coli_packed_row_bytes(F);
+}
+int64_t coli_expert_scale_count(int64_t H, int64_t F) {
+  return 2 * F * coli_scales_per_row(H) + H * coli_scales_per_row(F);
+}
+
+int coli_quant_i4g(const void *w, coli_dtype w_dtype, int64_t rows, int64_t cols,
+                   uint8_t *packed, float *scales, cudaStream_t stream) {
+  if (rows < 0 || cols < 1) return COLI_EINVAL;
+  if (w_dtype != COLI_F32 && w_dtype != COLI_BF16) return COLI_EINVAL;
+  if (rows > 0 && (!w || !packed || !scales)) return COLI_EINVAL;
+  if (rows > 0 && cols > INT64_MAX / rows) return COLI_EINVAL;
+  return map_err(launch_quant_i4g(w, w_dtype, rows, cols, packed, scales, stream));
+}
+
+size_t coli_router_workspace_size(const coli_moe_desc *d, int top_k) {
+  return coli_moe_workspace_size(d, top_k);
+}
+
+size_t coli_moe_workspace_size(const coli_moe_desc *d, int top_k) {
+  if (check_desc(d, top_k) != COLI_OK) return 0;
+  const int T = pass_tokens(d->n_tokens);
+  return ws_layout(T > 0 ? T : 1, d->hidden, d->ffn, d->n_experts, d->n_shared, top_k).total;
+}
+
+int coli_router_topk(const coli_moe_desc *d, int top_k, const void *x, const void *router_w,
+                     int32_t *idx, float *gates, uint32_t *route_counts, void *workspace,
+                     size_t ws_bytes, cudaStream_t stream) {
+  int st = check_desc(d, top_k);
+  if (st) return st;
+  const int T = d->n_tokens;
+  if (T == 0) return COLI_OK;
+  if (!x || !router_w || !idx || !gates || !workspace) return COLI_EINVAL;
+  if (!aligned16(x) || !aligned16(router_w) || ((uintptr_t)workspace & 255u)) return COLI_EALIGN;
+  if (ws_bytes < coli_router_workspace_size(d, top_k)) return COLI_ENOMEM;
+  const int H = d->hidden, E = d->n_experts, k = top_k;
+  const int TP = pass_tokens(T);
+  const WsLayout L = ws_layout(TP, H, d->ffn, E, d->n_shared, k);
+  for (int t0 = 0; t0 < T; t0 += TP) {
+    const int tn = T - t0 < TP ? T - t0 : TP;
+    const void *xp = (const char *)x + (size_t)t0 * H * xsize(d->x_dtype);
+    cudaError_t e = launch_router_topk(xp, d->x_dtype, router_w, d->router_dtype, tn, H, E,
+                                       d->n_shared, k, (uint8_t *)workspace, L,
+                                       idx + (size_t)t0 * k, gates + (size_t)t0 * k,
+                                       route_counts, false, stream);
+    if (e != cudaSuccess) return COLI_ECUDA;
+  }
+  return COLI_OK;
+}
+
+static int moe_layer(const coli_moe_desc *d, int top_k, const void *x, coli_dtype x_dtype,
+                     const void *router_w, const uint8_t *packed, const float *scales,
+                     float *out, const float *residual, float *layer_out,
+                     uint32_t *route_counts, void *workspace, cudaStream_t stream) {
+  const int T = d->n_tokens, H = d->hidden, F = d->ffn, E = d->n_experts, S = d->n_shared;
+  const int k = top_k;
+  const int TP = pass_tokens(T);
+  const WsLayout L = ws_layout(TP, H, F, E, S, k);
+  uint8_t *ws = (uint8_t *)workspace;
+  for (int t0 = 0; t0 < T; t0 += TP) {
+    const int tn = T - t0 < TP ? T - t0 : TP;
+    const size_t xo = (size_t)t0 * H;
+    const void *xp = (const char *)x + xo * xsize(x_dtype);
+    cudaError_t e = launch_router_topk(xp, x_dtype, router_w, d->router_dtype, tn, H, E, S, k,
+                                       ws, L, nullptr, nullptr, route_counts, true, stream);
+    if (e != cudaSuccess) return COLI_ECUDA;
+    e = launch_moe_decode(xp, x_dtype, tn, H, F, E, S, k, packed, scales, ws, L, out + xo,
+                          residual ? residual + xo : nullptr,
+                          layer_out ? layer_out + xo : nullptr, stream);
+    if (e != cudaSuccess) return COLI_ECUDA;
+  }
+  return COLI_OK;
+}
+
+int coli_moe_forward(const coli_moe_desc *d, int top_k, const void *x, const void *router_w,
+                     const uint8_t *packed_experts, const float *scales, float *out,
+                     uint32_t *route_counts, void *workspace, size_t ws_bytes,
+                     cudaStream_t stream) {
+  int st = check_desc(d, top_k);
+  if (st) return st;
+  if (d->n_tokens == 0) return COLI_OK;
+  if (!x || !router_w || !packed_experts || !scales || !out || !workspace) return COLI_EINVAL;
+  if (!aligned16(x) || !aligned16(router_w) || !aligned16(packed_experts) ||
+      !aligned16(scales) || !aligned16(out) || ((uintptr_t)workspace & 255u))
+    return COLI_EALIGN;
+  if (ws_bytes < coli_moe_workspace_size(d, top_k)) return COLI_ENOMEM;
+  return moe_layer(d, top_k, x, d->x_dtype, router_w, packed_experts, scales, out, nullptr,
+                   nullptr, route_counts, workspace, stream);
+}
+
+int coli_moe_stack_forward(const coli_moe_desc *d, int top_k, int n_layers, const void *x,
+                           const void *router_w, const uint8_t *packed_experts,
+                           const float *scales, float *x_out, float *layer_out,
+                           uint32_t *route_counts, void *workspace, size_t ws_bytes,
+                           cudaStream_t stream) {
+  int st = check_desc(d, top_k);
+  if (st) return st;
+  if (n_layers < 1) return COLI_EINVAL;
+  if (d->n_tokens == 0) return COLI_OK;
+  if (!x || !router_w || !packed_experts || !scales || !x_out || !workspace)
+    return COLI_EINVAL;
+  if (!aligned16(x) || !aligned16(router_w) || !aligned16(packed_experts) ||
+      !aligned16(scales) || !aligned16(x_out) || (layer_out && !aligned16(layer_out)) ||
+      ((uintptr_t)workspace & 255u))
+    return COLI_EALIGN;
+  if (ws_bytes < coli_moe_workspace_size(d, top_k)) return COLI_ENOMEM;
+  const int T = d->n_tokens, H = d->hidden, F = d->ffn, E = d->n_experts, S = d->n_shared;
+  const size_t wr_stride = (size_t)E * H * xsize(d->router_dtype);
+  const size_t pk_stride = (size_t)(E + S) * coli_expert_packed_bytes(H, F);
+  const size_t sc_stride = (size_t)(E + S) * coli_expert_scale_count(H, F);
+  // The residual stream is f32: the stack takes an f32 input.
+  if (d->x_dtype != COLI_F32) return COLI_EUNSUPPORTED;
+  for (int l = 0; l < n_layers; ++l) {
+    const void *xin = (l == 0) ? x : (const void *)x_out;
+    const float *res = (const float *)xin;
+    st = moe_layer(d, top_k, xin, COLI_F32, (const char *)router_w + l * wr_stride,
+                   packed_experts + l * pk_stride, scales + l * sc_stride, x_out, res,
+                   layer_out ? layer_out + (size_t)l * T * H : nullptr,
+                   route_counts ? route_counts + (size_t)l * E : nullptr, workspace, stream);
+    if (st) return st;
+  }
+  return COLI_OK;
+}
+
+int coli_moe_check(void *workspace, int clear, uint32_t *flags, cudaStream_t stream) {
+  if (!workspace || !flags) return COLI_EINVAL;
+  uint32_t v = 0;
+  uint32_t *dev = (uint32_t *)workspace + kCtrlFlags;
+  if (cudaMemcpyAsync(&v, dev, sizeof(v), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return COLI_ECUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return COLI_ECUDA;
+  if (clear && v && cudaMemsetAsync(dev, 0, sizeof(uint32_t), stream) != cudaSuccess)
+    return COLI_ECUDA;
+  *flags = v;
+  return (v & COLI_FLAG_TIMEOUT) ? COLI_ETIMEOUT : COLI_OK;
+}
+
+}  // extern "C"
