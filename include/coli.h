@@ -143,6 +143,30 @@ int coli_moe_forward(const coli_moe_desc *d, int top_k, const void *x,
                      void *workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * coli_moe_forward_noalloc -- coli_moe_forward without a workspace argument,
+ * for callers that cannot allocate device memory: hosts that hand the whole
+ * device-memory budget out up front, or latency-critical loops that must
+ * never reach cudaMalloc (it can synchronise the device).  The pages have no
+ * counterpart of this entry point; it only changes where the scratch lives.
+ *   Scratch: a 4 MiB array in the library's device image, which every GPU
+ *   that loads the library holds until the process exits.  Calls whose
+ *   coli_moe_workspace_size(d, top_k) exceeds 4 MiB return COLI_ENOMEM and
+ *   launch nothing.  The array's device address is looked up on the first
+ *   call on each device (with that device current), so make that first call
+ *   before any stream capture.
+ *   All calls share the one array: calls that overlap on the GPU (different
+ *   streams, or several host threads) race and give wrong results; order them.
+ *   Each call clears the array's control words first, so the NaN-logit flag
+ *   of coli_moe_check is not available through this entry point.
+ *   Allocates nothing (no cudaMalloc, no allocating library routine); the
+ *   caller still provides x, the weights, out and route_counts.
+ */
+int coli_moe_forward_noalloc(const coli_moe_desc *d, int top_k, const void *x,
+                             const void *router_w, const uint8_t *packed_experts,
+                             const float *scales, float *out, uint32_t *route_counts,
+                             cudaStream_t stream);
+
+/*
  * coli_moe_stack_forward -- n_layers MoE layers chained through a residual
  * stream (decode stack without attention or norms):
  *   x_0 = x;  x_{l+1} = x_l + MoE_l(x_l);  x_out = x_{n_layers}

@@ -26,7 +26,8 @@ EXPORTS = (
     "coli_status_str", "coli_packed_row_bytes", "coli_scales_per_row",
     "coli_expert_packed_bytes", "coli_expert_scale_count", "coli_quant_i4g",
     "coli_router_workspace_size", "coli_moe_workspace_size", "coli_router_topk",
-    "coli_moe_forward", "coli_moe_stack_forward", "coli_moe_check",
+    "coli_moe_forward", "coli_moe_forward_noalloc", "coli_moe_stack_forward",
+    "coli_moe_check",
 )
 
 
@@ -67,6 +68,8 @@ def _load():
     L.coli_router_topk.restype = C.c_int
     L.coli_moe_forward.argtypes = [dp, C.c_int, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.coli_moe_forward.restype = C.c_int
+    L.coli_moe_forward_noalloc.argtypes = [dp, C.c_int, vp, vp, vp, vp, vp, vp, vp]
+    L.coli_moe_forward_noalloc.restype = C.c_int
     L.coli_moe_stack_forward.argtypes = [dp, C.c_int, C.c_int, vp, vp, vp, vp, vp, vp, vp,
                                          vp, sz, vp]
     L.coli_moe_stack_forward.restype = C.c_int
@@ -198,6 +201,20 @@ def coli_moe_forward(desc: MoEDesc, top_k, x, router_w, packed_experts, scales, 
     _check("coli_moe_forward", lib.coli_moe_forward(
         C.byref(d), top_k, _ptr(x), _ptr(router_w), _ptr(packed_experts), _ptr(scales),
         _ptr(out), _ptr(route_counts), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def coli_moe_forward_noalloc(desc: MoEDesc, top_k, x, router_w, packed_experts, scales,
+                             out=None, route_counts=None, stream=None):
+    """coli_moe_forward with the library's fixed device scratch instead of a
+    workspace, for callers that cannot allocate device memory (see coli.h)."""
+    _cuda(x, router_w, packed_experts, scales, out, route_counts)
+    if out is None:
+        out = torch.empty((desc.n_tokens, desc.hidden), dtype=torch.float32, device=x.device)
+    d = desc.c()
+    _check("coli_moe_forward_noalloc", lib.coli_moe_forward_noalloc(
+        C.byref(d), top_k, _ptr(x), _ptr(router_w), _ptr(packed_experts), _ptr(scales),
+        _ptr(out), _ptr(route_counts), _stream(stream)))
     return out
 
 
