@@ -15,8 +15,9 @@ WsLayout ws_layout(int T, int H, int F, int E, int S, int k) {
   WsLayout L{};
   size_t o = 0;
   const size_t KS = (size_t)k + S;
+  L.n_part = num_sms() < H / 4 ? num_sms() : H / 4;
   L.ctrl = o;      o = align256(o + kCtrlWords * sizeof(uint32_t));
-  L.logits = o;    o = align256(o + (size_t)T * E * sizeof(float));
+  L.partials = o;  o = align256(o + (size_t)L.n_part * T * E * sizeof(float));
   L.idx = o;       o = align256(o + (size_t)T * k * sizeof(int32_t));
   L.gates = o;     o = align256(o + (size_t)T * k * sizeof(float));
   L.act = o;       o = align256(o + (size_t)(2 * (E + S) + 2) * sizeof(int32_t));
@@ -24,7 +25,6 @@ WsLayout ws_layout(int T, int H, int F, int E, int S, int k) {
   L.slot_gate = o; o = align256(o + (size_t)T * KS * sizeof(float));
   L.h = o;         o = align256(o + (size_t)T * KS * F * sizeof(float));
   L.total = o;
-  (void)H;
   return L;
 }
 
@@ -69,6 +69,28 @@ int pass_tokens(int T) { return T < kDecodeMaxT ? T : kDecodeMaxT; }
 int map_err(cudaError_t e) { return e == cudaSuccess ? COLI_OK : COLI_ECUDA; }
 
 size_t xsize(coli_dtype t) { return t == COLI_BF16 ? 2 : 4; }
+
+Dec2Args make_args(const coli_moe_desc *d, int k, int tn, uint8_t *ws, const WsLayout &L) {
+  Dec2Args a{};
+  a.T = tn;
+  a.H = d->hidden;
+  a.F = d->ffn;
+  a.E = d->n_experts;
+  a.S = d->n_shared;
+  a.k = k;
+  a.eb = coli_expert_packed_bytes(a.H, a.F);
+  a.es = coli_expert_scale_count(a.H, a.F);
+  a.n_part = L.n_part;
+  a.partials = (float *)(ws + L.partials);
+  a.g_idx = (int32_t *)(ws + L.idx);
+  a.g_gates = (float *)(ws + L.gates);
+  a.g_act = (int32_t *)(ws + L.act);
+  a.g_routes = (int32_t *)(ws + L.routes);
+  a.g_slot_gate = (float *)(ws + L.slot_gate);
+  a.h = (float *)(ws + L.h);
+  a.ctrl = (uint32_t *)(ws + L.ctrl);
+  return a;
+}
 
 }  // namespace
 
@@ -128,38 +150,78 @@ int coli_router_topk(const coli_moe_desc *d, int top_k, const void *x, const voi
   const int H = d->hidden, E = d->n_experts, k = top_k;
   const int TP = pass_tokens(T);
   const WsLayout L = ws_layout(TP, H, d->ffn, E, d->n_shared, k);
+  uint8_t *ws = (uint8_t *)workspace;
   for (int t0 = 0; t0 < T; t0 += TP) {
     const int tn = T - t0 < TP ? T - t0 : TP;
-    const void *xp = (const char *)x + (size_t)t0 * H * xsize(d->x_dtype);
-    cudaError_t e = launch_router_topk(xp, d->x_dtype, router_w, d->router_dtype, tn, H, E,
-                                       d->n_shared, k, (uint8_t *)workspace, L,
-                                       idx + (size_t)t0 * k, gates + (size_t)t0 * k,
-                                       route_counts, false, stream);
+    Dec2Args a = make_args(d, k, tn, ws, L);
+    a.x = (const char *)x + (size_t)t0 * H * xsize(d->x_dtype);
+    a.wr = router_w;
+    a.counts = route_counts;
+    a.idx_out = idx + (size_t)t0 * k;
+    a.gates_out = gates + (size_t)t0 * k;
+    cudaError_t e = launch_route_partials(a, d->x_dtype == COLI_BF16,
+                                          d->router_dtype == COLI_BF16, stream, true);
+    if (e == cudaSuccess) e = launch_topk(a, stream, true);
     if (e != cudaSuccess) return COLI_ECUDA;
   }
   return COLI_OK;
 }
 
-static int moe_layer(const coli_moe_desc *d, int top_k, const void *x, coli_dtype x_dtype,
-                     const void *router_w, const uint8_t *packed, const float *scales,
-                     float *out, const float *residual, float *layer_out,
-                     uint32_t *route_counts, void *workspace, cudaStream_t stream) {
-  const int T = d->n_tokens, H = d->hidden, F = d->ffn, E = d->n_experts, S = d->n_shared;
-  const int k = top_k;
+// One token pass (<= kDecodeMaxT tokens) through n_layers layers.  Layer l reads
+// x (l = 0, dtype x_dtype) or out (l > 0, f32); with a residual the output of
+// layer l is x_l + MoE_l(x_l), else MoE_l(x_l) (single layer only).
+static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const void *x,
+                    coli_dtype x_dtype, const void *router_w, const uint8_t *packed,
+                    const float *scales, float *out, bool residual, float *layer_out,
+                    uint32_t *route_counts, void *workspace, const WsLayout &L,
+                    cudaStream_t stream) {
+  const int H = d->hidden, F = d->ffn, E = d->n_experts, S = d->n_shared;
+  const size_t wr_stride = (size_t)E * H * xsize(d->router_dtype);
+  const size_t pk_stride = (size_t)(E + S) * coli_expert_packed_bytes(H, F);
+  const size_t sc_stride = (size_t)(E + S) * coli_expert_scale_count(H, F);
+  const size_t T_H = (size_t)d->n_tokens * H;
+  Dec2Args a = make_args(d, k, tn, (uint8_t *)workspace, L);
+  if (plan_decode(a, L.n_part) != cudaSuccess) return COLI_EUNSUPPORTED;
+  const int wr_bf16 = d->router_dtype == COLI_BF16;
+  cudaError_t e = cudaSuccess;
+  for (int l = 0; l < n_layers && e == cudaSuccess; ++l) {
+    const void *xin = (l == 0) ? x : (const void *)out;
+    const int x_bf16 = (l == 0) ? (x_dtype == COLI_BF16) : 0;
+    a.x = xin;
+    a.packed = packed + l * pk_stride;
+    a.scales = scales + l * sc_stride;
+    a.counts = route_counts ? route_counts + (size_t)l * E : nullptr;
+    if (l == 0) {
+      a.wr = router_w;
+      e = launch_route_partials(a, x_bf16, wr_bf16, stream, true);
+      if (e != cudaSuccess) break;
+    }
+    e = launch_gateup(a, x_bf16, num_sms(), stream, true);
+    if (e != cudaSuccess) break;
+    a.wr = (l + 1 < n_layers) ? (const void *)((const char *)router_w + (l + 1) * wr_stride)
+                              : nullptr;
+    a.residual = residual ? (const float *)xin : nullptr;
+    a.out = out;
+    a.layer_out = layer_out ? layer_out + (size_t)l * T_H : nullptr;
+    e = launch_down(a, wr_bf16, stream, true);
+  }
+  return e == cudaSuccess ? COLI_OK : COLI_ECUDA;
+}
+
+static int moe_run(const coli_moe_desc *d, int k, int n_layers, const void *x, const void *router_w,
+                   const uint8_t *packed, const float *scales, float *out, bool residual,
+                   float *layer_out, uint32_t *route_counts, void *workspace, cudaStream_t stream) {
+  const int T = d->n_tokens, H = d->hidden;
   const int TP = pass_tokens(T);
-  const WsLayout L = ws_layout(TP, H, F, E, S, k);
-  uint8_t *ws = (uint8_t *)workspace;
+  const WsLayout L = ws_layout(TP, H, d->ffn, d->n_experts, d->n_shared, k);
   for (int t0 = 0; t0 < T; t0 += TP) {
     const int tn = T - t0 < TP ? T - t0 : TP;
     const size_t xo = (size_t)t0 * H;
-    const void *xp = (const char *)x + xo * xsize(x_dtype);
-    cudaError_t e = launch_router_topk(xp, x_dtype, router_w, d->router_dtype, tn, H, E, S, k,
-                                       ws, L, nullptr, nullptr, route_counts, true, stream);
-    if (e != cudaSuccess) return COLI_ECUDA;
-    e = launch_moe_decode(xp, x_dtype, tn, H, F, E, S, k, packed, scales, ws, L, out + xo,
-                          residual ? residual + xo : nullptr,
-                          layer_out ? layer_out + xo : nullptr, stream);
-    if (e != cudaSuccess) return COLI_ECUDA;
+    const int st = moe_pass(d, k, n_layers, tn, (const char *)x + xo * xsize(d->x_dtype),
+                            d->x_dtype, router_w, packed, scales, out + xo, residual,
+                            layer_out ? layer_out + xo : nullptr, route_counts, workspace, L,
+                            stream);
+    if (st != COLI_OK) return st;
   }
   return COLI_OK;
 }
@@ -176,8 +238,8 @@ int coli_moe_forward(const coli_moe_desc *d, int top_k, const void *x, const voi
       !aligned16(scales) || !aligned16(out) || ((uintptr_t)workspace & 255u))
     return COLI_EALIGN;
   if (ws_bytes < coli_moe_workspace_size(d, top_k)) return COLI_ENOMEM;
-  return moe_layer(d, top_k, x, d->x_dtype, router_w, packed_experts, scales, out, nullptr,
-                   nullptr, route_counts, workspace, stream);
+  return moe_run(d, top_k, 1, x, router_w, packed_experts, scales, out, false, nullptr,
+                 route_counts, workspace, stream);
 }
 
 int coli_moe_stack_forward(const coli_moe_desc *d, int top_k, int n_layers, const void *x,
@@ -196,22 +258,10 @@ int coli_moe_stack_forward(const coli_moe_desc *d, int top_k, int n_layers, cons
       ((uintptr_t)workspace & 255u))
     return COLI_EALIGN;
   if (ws_bytes < coli_moe_workspace_size(d, top_k)) return COLI_ENOMEM;
-  const int T = d->n_tokens, H = d->hidden, F = d->ffn, E = d->n_experts, S = d->n_shared;
-  const size_t wr_stride = (size_t)E * H * xsize(d->router_dtype);
-  const size_t pk_stride = (size_t)(E + S) * coli_expert_packed_bytes(H, F);
-  const size_t sc_stride = (size_t)(E + S) * coli_expert_scale_count(H, F);
   // The residual stream is f32: the stack takes an f32 input.
   if (d->x_dtype != COLI_F32) return COLI_EUNSUPPORTED;
-  for (int l = 0; l < n_layers; ++l) {
-    const void *xin = (l == 0) ? x : (const void *)x_out;
-    const float *res = (const float *)xin;
-    st = moe_layer(d, top_k, xin, COLI_F32, (const char *)router_w + l * wr_stride,
-                   packed_experts + l * pk_stride, scales + l * sc_stride, x_out, res,
-                   layer_out ? layer_out + (size_t)l * T * H : nullptr,
-                   route_counts ? route_counts + (size_t)l * E : nullptr, workspace, stream);
-    if (st) return st;
-  }
-  return COLI_OK;
+  return moe_run(d, top_k, n_layers, x, router_w, packed_experts, scales, x_out, true, layer_out,
+                 route_counts, workspace, stream);
 }
 
 int coli_moe_check(void *workspace, int clear, uint32_t *flags, cudaStream_t stream) {

@@ -25,30 +25,64 @@ enum CtrlWord : int {
 // Byte offsets of the scratch arrays inside a workspace (all 256-aligned).
 struct WsLayout {
   size_t ctrl;       // uint32[kCtrlWords]
-  size_t logits;     // f32 [T][E]
+  size_t partials;   // f32 [n_part][T][E] router partial logits
   size_t idx;        // i32 [T][k]
   size_t gates;      // f32 [T][k]
   size_t act;        // i32: n_active, act_expert[E+S], act_off[E+S+1]
-  size_t routes;     // i32 [T*(k+S)] slot ids grouped by active expert
+  size_t routes;     // i32 [T*(k+S)] slot ids grouped by used expert
   size_t slot_gate;  // f32 [T*(k+S)]
   size_t h;          // f32 [T*(k+S)][F]
   size_t total;
+  int n_part;
 };
 
 WsLayout ws_layout(int T, int H, int F, int E, int S, int k);
 
-// Router + top-k + union (router.cu).  x_dtype / w_dtype are coli_dtype.
-// Writes logits, idx, gates, union lists into ws; optional user copies.
-cudaError_t launch_router_topk(const void *x, int x_dtype, const void *wr, int w_dtype,
-                               int T, int H, int E, int S, int k, uint8_t *ws,
-                               const WsLayout &L, int32_t *idx_out, float *gates_out,
-                               uint32_t *counts, bool build_union, cudaStream_t s);
+constexpr int kDec2MaxThreads = 640;
 
-// Expert FFN over the union lists (moe_decode.cu).
-cudaError_t launch_moe_decode(const void *x, int x_dtype, int T, int H, int F, int E, int S,
-                              int k, const uint8_t *packed, const float *scales,
-                              uint8_t *ws, const WsLayout &L, float *out,
-                              const float *residual, float *layer_out, cudaStream_t s);
+// Shared-memory plan of k_gateup (byte offsets into dynamic smem).
+struct GuSmem {
+  size_t logits, idx, gates, park, scratch, act, routes, slot_gate, ring, red, bar, total;
+};
+// Shared-memory plan of k_down.
+struct DnSmem {
+  size_t act, routes, acc, xn, wr, h, ring, red, bar, total;
+};
+
+// Arguments of the decode kernels (one layer, T <= kDecodeMaxT tokens).
+struct Dec2Args {
+  int T, H, F, E, S, k;
+  const void *x;            // layer input [T][H], f32 or bf16
+  const void *wr;           // k_route: this layer's router; k_down: next layer's (or null)
+  const float *residual;    // k_down: added to the layer output (or null)
+  const uint8_t *packed;    // this layer's expert records
+  const float *scales;
+  int64_t eb, es;           // packed bytes / scales per expert
+  float *partials;          // [n_part][T][E]
+  int n_part;
+  int32_t *g_idx;
+  float *g_gates;
+  int32_t *g_act, *g_routes;
+  float *g_slot_gate;
+  float *h;
+  uint32_t *ctrl;
+  uint32_t *counts;         // route counts [E] (or null)
+  float *out;               // k_down output [T][H]
+  float *layer_out;         // or null
+  int32_t *idx_out;         // k_topk user outputs (or null)
+  float *gates_out;
+  int gu_ncg, gu_nrg, gu_rs, gu_ns;
+  int dn_ncg, dn_nrg, dn_rs, dn_ns, dn_h_smem;
+  GuSmem gu;
+  DnSmem dn;
+};
+
+cudaError_t plan_decode(Dec2Args &a, int n_part);
+cudaError_t launch_route_partials(const Dec2Args &a, int x_bf16, int w_bf16, cudaStream_t s,
+                                  bool pdl);
+cudaError_t launch_topk(const Dec2Args &a, cudaStream_t s, bool pdl);
+cudaError_t launch_gateup(const Dec2Args &a, int x_bf16, int grid, cudaStream_t s, bool pdl);
+cudaError_t launch_down(const Dec2Args &a, int wr_bf16, cudaStream_t s, bool pdl);
 
 // Quantiser (quant.cu).
 cudaError_t launch_quant_i4g(const void *w, int w_dtype, int64_t rows, int64_t cols,
