@@ -193,8 +193,10 @@ class DecodeWorkload:
                                  route_counts=self.counts[i], stream=stream)
 
     def kernels_per_step(self):
+        # per 16-token pass: the first layer's router partials, then gate/up
+        # and down for every layer
         passes = (self.shape.tokens + 15) // 16
-        return self.shape.layers * passes * 3
+        return passes * (1 + 2 * self.shape.layers)
 
     def algorithmic_bytes(self, steps):
         """Bytes the method must move for the given steps: packed nibbles and

@@ -16,14 +16,20 @@ WsLayout ws_layout(int T, int H, int F, int E, int S, int k) {
   size_t o = 0;
   const size_t KS = (size_t)k + S;
   L.n_part = num_sms() < H / 4 ? num_sms() : H / 4;
+  // replica strides: whole 256-byte units plus one, so replicas start at
+  // different offsets modulo any power of two
+  L.part_stride = (align256((size_t)L.n_part * T * E * 4) + 256) / 4;
+  L.h_stride = (align256((size_t)T * KS * F * 4) + 256) / 4;
+  L.x_stride = (align256((size_t)T * H * 4) + 256) / 4;
   L.ctrl = o;      o = align256(o + kCtrlWords * sizeof(uint32_t));
-  L.partials = o;  o = align256(o + (size_t)L.n_part * T * E * sizeof(float));
+  L.partials = o;  o = align256(o + kReplicas * L.part_stride * 4);
   L.idx = o;       o = align256(o + (size_t)T * k * sizeof(int32_t));
   L.gates = o;     o = align256(o + (size_t)T * k * sizeof(float));
   L.act = o;       o = align256(o + (size_t)(2 * (E + S) + 2) * sizeof(int32_t));
   L.routes = o;    o = align256(o + (size_t)T * KS * sizeof(int32_t));
   L.slot_gate = o; o = align256(o + (size_t)T * KS * sizeof(float));
-  L.h = o;         o = align256(o + (size_t)T * KS * F * sizeof(float));
+  L.h = o;         o = align256(o + kReplicas * L.h_stride * 4);
+  L.xrep = o;      o = align256(o + kReplicas * L.x_stride * 4);
   L.total = o;
   return L;
 }
@@ -81,7 +87,12 @@ Dec2Args make_args(const coli_moe_desc *d, int k, int tn, uint8_t *ws, const WsL
   a.eb = coli_expert_packed_bytes(a.H, a.F);
   a.es = coli_expert_scale_count(a.H, a.F);
   a.n_part = L.n_part;
+  a.n_rep = kReplicas;
   a.partials = (float *)(ws + L.partials);
+  a.part_stride = L.part_stride;
+  a.h_stride = L.h_stride;
+  a.xrep = (float *)(ws + L.xrep);
+  a.x_stride = L.x_stride;
   a.g_idx = (int32_t *)(ws + L.idx);
   a.g_gates = (float *)(ws + L.gates);
   a.g_act = (int32_t *)(ws + L.act);
@@ -196,7 +207,7 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
       e = launch_route_partials(a, x_bf16, wr_bf16, stream, true);
       if (e != cudaSuccess) break;
     }
-    e = launch_gateup(a, x_bf16, num_sms(), stream, true);
+    e = launch_gateup(a, num_sms(), stream, true);
     if (e != cudaSuccess) break;
     a.wr = (l + 1 < n_layers) ? (const void *)((const char *)router_w + (l + 1) * wr_stride)
                               : nullptr;

@@ -14,6 +14,10 @@ constexpr int kDecodeMaxT = 16;     // tokens per call served by the GEMV path
 constexpr int kMaxTopK = 64;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxShared = 8;
+// Buffers that every CTA of a kernel reads (layer input, h, router partials)
+// are written in this many copies, each read by 1/kReplicas of the CTAs, so
+// that no single L2 slice serves the whole grid.
+constexpr int kReplicas = 8;
 
 // Control words at the head of every workspace.
 enum CtrlWord : int {
@@ -25,15 +29,17 @@ enum CtrlWord : int {
 // Byte offsets of the scratch arrays inside a workspace (all 256-aligned).
 struct WsLayout {
   size_t ctrl;       // uint32[kCtrlWords]
-  size_t partials;   // f32 [n_part][T][E] router partial logits
+  size_t partials;   // f32 [kReplicas][n_part][T][E] router partial logits
   size_t idx;        // i32 [T][k]
   size_t gates;      // f32 [T][k]
   size_t act;        // i32: n_active, act_expert[E+S], act_off[E+S+1]
   size_t routes;     // i32 [T*(k+S)] slot ids grouped by used expert
   size_t slot_gate;  // f32 [T*(k+S)]
-  size_t h;          // f32 [T*(k+S)][F]
+  size_t h;          // f32 [kReplicas][T*(k+S)][F]
+  size_t xrep;       // f32 [kReplicas][T][H]
   size_t total;
   int n_part;
+  size_t part_stride, h_stride, x_stride;   // replica strides (floats)
 };
 
 WsLayout ws_layout(int T, int H, int F, int E, int S, int k);
@@ -42,11 +48,11 @@ constexpr int kDec2MaxThreads = 640;
 
 // Shared-memory plan of k_gateup (byte offsets into dynamic smem).
 struct GuSmem {
-  size_t logits, idx, gates, park, scratch, act, routes, slot_gate, ring, red, bar, total;
+  size_t logits, idx, gates, vals, rank, scratch, act, routes, slot_gate, desc, ring, red, bar, total;
 };
 // Shared-memory plan of k_down.
 struct DnSmem {
-  size_t act, routes, acc, xn, wr, h, ring, red, bar, total;
+  size_t act, routes, acc, xn, wr, desc, planes, ring, red, bar, total;
 };
 
 // Arguments of the decode kernels (one layer, T <= kDecodeMaxT tokens).
@@ -58,21 +64,26 @@ struct Dec2Args {
   const uint8_t *packed;    // this layer's expert records
   const float *scales;
   int64_t eb, es;           // packed bytes / scales per expert
-  float *partials;          // [n_part][T][E]
+  float *partials;          // [n_rep][n_part][T][E]: replica r at partials + r * part_stride
+  size_t part_stride;
   int n_part;
+  int n_rep;                // replicas of the buffers every CTA reads
+  float *xrep;              // [n_rep][T][H] f32 layer input (or null)
+  size_t x_stride;
+  size_t h_stride;          // h replica stride (floats)
   int32_t *g_idx;
   float *g_gates;
   int32_t *g_act, *g_routes;
   float *g_slot_gate;
-  float *h;
+  float *h;                 // [n_rep][T*(k+S)][F]
   uint32_t *ctrl;
   uint32_t *counts;         // route counts [E] (or null)
   float *out;               // k_down output [T][H]
   float *layer_out;         // or null
   int32_t *idx_out;         // k_topk user outputs (or null)
   float *gates_out;
-  int gu_ncg, gu_nrg, gu_rs, gu_ns;
-  int dn_ncg, dn_nrg, dn_rs, dn_ns, dn_h_smem;
+  int gu_ncg, gu_nrg, gu_rs, gu_ns, gu_stage_partials;
+  int dn_ncg, dn_nrg, dn_rs, dn_ns, dn_planes, dn_nbp;
   GuSmem gu;
   DnSmem dn;
 };
@@ -81,7 +92,7 @@ cudaError_t plan_decode(Dec2Args &a, int n_part);
 cudaError_t launch_route_partials(const Dec2Args &a, int x_bf16, int w_bf16, cudaStream_t s,
                                   bool pdl);
 cudaError_t launch_topk(const Dec2Args &a, cudaStream_t s, bool pdl);
-cudaError_t launch_gateup(const Dec2Args &a, int x_bf16, int grid, cudaStream_t s, bool pdl);
+cudaError_t launch_gateup(const Dec2Args &a, int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_down(const Dec2Args &a, int wr_bf16, cudaStream_t s, bool pdl);
 
 // Quantiser (quant.cu).

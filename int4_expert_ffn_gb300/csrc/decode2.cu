@@ -28,6 +28,7 @@
 #include "coli_internal.cuh"
 #include "ptx.cuh"
 #include "topk.cuh"
+#include "trace.cuh"
 
 namespace coli {
 
@@ -153,6 +154,84 @@ __device__ __forceinline__ float reduce8(float (&v)[8]) {
   return d;
 }
 
+// Quantise n_vec f32 vectors of length F (global, row-major [n_vec][F]) into
+// activation planes in shared memory, transposed for conflict-free reads:
+// word w (0..15 planes, 16 = sq, 17 = sx bits) of 32-column block b of vector v
+// is at planes[(v * 18 + w) * nbp + b].  One warp handles 4 blocks at a time;
+// lane q of a block's 8 lanes holds its columns 4q..4q+3.
+__device__ void build_planes(const float *src, int n_vec, int F, uint32_t *planes, int nbp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int groups_per_vec = (F + 127) / 128;
+  const int n_groups = n_vec * groups_per_vec;
+  const int q = lane & 7;
+  for (int g = warp; g < n_groups; g += nw) {
+    const int v = g / groups_per_vec, gc = g - v * groups_per_vec;
+    const int col = gc * 128 + 4 * lane;
+    const bool act = col < F;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (act) x = __ldcg((const float4 *)(src + (int64_t)v * F + col));
+    float m = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+    bool bad = (x.x != x.x) | (x.y != x.y) | (x.z != x.z) | (x.w != x.w);
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) {
+      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+      bad |= __shfl_xor_sync(0xFFFFFFFFu, (int)bad, off) != 0;
+    }
+    const float inv = m > 0.0f ? (float)kQ / m : 0.0f;
+    const float sx = bad ? __int_as_float(0x7FC00000) : m / (float)kQ;
+    int qv[4];
+    const float xv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      qv[i] = (int)fminf(fmaxf(rintf(xv[i] * inv), -(float)kQ), (float)kQ);
+    int hv[4], lv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      hv[i] = (qv[i] + 64) >> 7;
+      lv[i] = qv[i] - (hv[i] << 7);
+    }
+    // 16-bit halves of the plane words: even columns are elements 0, 2; odd 1, 3
+    const uint32_t eh = (uint32_t)(hv[0] & 0xFF) | ((uint32_t)(hv[2] & 0xFF) << 8);
+    const uint32_t el = (uint32_t)(lv[0] & 0xFF) | ((uint32_t)(lv[2] & 0xFF) << 8);
+    const uint32_t oh = (uint32_t)(hv[1] & 0xFF) | ((uint32_t)(hv[3] & 0xFF) << 8);
+    const uint32_t ol = (uint32_t)(lv[1] & 0xFF) | ((uint32_t)(lv[3] & 0xFF) << 8);
+    const uint32_t eh2 = __shfl_down_sync(0xFFFFFFFFu, eh, 1);
+    const uint32_t el2 = __shfl_down_sync(0xFFFFFFFFu, el, 1);
+    const uint32_t oh2 = __shfl_down_sync(0xFFFFFFFFu, oh, 1);
+    const uint32_t ol2 = __shfl_down_sync(0xFFFFFFFFu, ol, 1);
+    int sq = qv[0] + qv[1] + qv[2] + qv[3];
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, off);
+    const int b = (gc * 128 + 32 * (lane >> 3)) / 32;   // block index within the vector
+    if (act && (q & 1) == 0) {
+      const int i = q >> 1;
+      uint32_t *pv = planes + (size_t)v * 18 * nbp + b;
+      pv[(size_t)i * nbp] = eh | (eh2 << 16);
+      pv[(size_t)(4 + i) * nbp] = el | (el2 << 16);
+      pv[(size_t)(8 + i) * nbp] = oh | (oh2 << 16);
+      pv[(size_t)(12 + i) * nbp] = ol | (ol2 << 16);
+      if (q == 0) {
+        pv[(size_t)16 * nbp] = (uint32_t)sq;
+        pv[(size_t)17 * nbp] = __float_as_uint(sx);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void load_planes(const uint32_t *planes, int v, int b, int nbp,
+                                            Planes &p) {
+  const uint32_t *pv = planes + (size_t)v * 18 * nbp + b;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    p.eh[i] = pv[(size_t)i * nbp];
+    p.el[i] = pv[(size_t)(4 + i) * nbp];
+    p.oh[i] = pv[(size_t)(8 + i) * nbp];
+    p.ol[i] = pv[(size_t)(12 + i) * nbp];
+  }
+  p.sq = (int)pv[(size_t)16 * nbp];
+  p.sx = __uint_as_float(pv[(size_t)17 * nbp]);
+}
+
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 __device__ __forceinline__ int part_lo(int c, int n, int parts) {
@@ -200,8 +279,19 @@ __global__ void __launch_bounds__(256) k_route(Dec2Args a) {
   for (int o = threadIdx.x; o < a.T * a.E; o += blockDim.x) {
     const int t = o / a.E, e = o - t * a.E;
     float s = 0.0f;
-    for (int h = h0; h < h1; ++h) s = fmaf(to_f32(wr[(size_t)e * a.H + h]), to_f32(x[(size_t)t * a.H + h]), s);
-    a.partials[(size_t)c * a.T * a.E + o] = s;
+    for (int h = h0; h < h1; ++h)
+      s = fmaf(to_f32(wr[(size_t)e * a.H + h]), to_f32(x[(size_t)t * a.H + h]), s);
+    for (int r = 0; r < a.n_rep; ++r)
+      a.partials[r * a.part_stride + (size_t)c * a.T * a.E + o] = s;
+  }
+  // the layer input, widened to f32, in every replica (read by all gate/up CTAs)
+  if (a.xrep) {
+    const int nr = h1 - h0;
+    for (int i = threadIdx.x; i < a.T * nr; i += blockDim.x) {
+      const int t = i / nr, h = h0 + (i - t * nr);
+      const float v = to_f32(x[(size_t)t * a.H + h]);
+      for (int r = 0; r < a.n_rep; ++r) a.xrep[r * a.x_stride + (size_t)t * a.H + h] = v;
+    }
   }
 }
 
@@ -210,28 +300,50 @@ __global__ void __launch_bounds__(256) k_route(Dec2Args a) {
 // order), top-k per token by warps, NaN flag.
 
 __device__ void route_block(const Dec2Args &a, float *s_logits, int *s_idx, float *s_gates,
-                            float *s_park, float *s_scratch, bool publish) {
+                            float *s_vals, int *s_rank, float *s_scratch, float *s_stage,
+                            uint64_t *pbar, bool publish) {
   const int T = a.T, E = a.E, k = a.k;
   const int TE = T * E;
   const int nthr = blockDim.x;
+  const float *src = a.partials + (size_t)(blockIdx.x % a.n_rep) * a.part_stride;
+  if (s_stage) {
+    // one bulk copy of all partials into shared memory, then reduce there
+    if (threadIdx.x == 0) {
+      const uint32_t bytes = (uint32_t)((size_t)a.n_part * TE * 4);
+      mbar_arrive_expect_tx(pbar, bytes);
+      bulk_g2s(s_stage, src, bytes, pbar);
+    }
+    if (!mbar_wait(pbar, 0)) set_flag(a.ctrl, COLI_FLAG_TIMEOUT);
+    src = s_stage;
+  }
   int nsplit = nthr / TE;
   if (nsplit > 8) nsplit = 8;
   if (nsplit <= 1) {
     for (int o = threadIdx.x; o < TE; o += nthr) {
-      float s = 0.0f;
-#pragma unroll 4
-      for (int p = 0; p < a.n_part; ++p) s += __ldcg(a.partials + (size_t)p * TE + o);
-      s_logits[o] = s;
+      float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+      int p = 0;
+      for (; p + 4 <= a.n_part; p += 4) {
+        s0 += src[(size_t)p * TE + o];
+        s1 += src[(size_t)(p + 1) * TE + o];
+        s2 += src[(size_t)(p + 2) * TE + o];
+        s3 += src[(size_t)(p + 3) * TE + o];
+      }
+      for (; p < a.n_part; ++p) s0 += src[(size_t)p * TE + o];
+      s_logits[o] = (s0 + s1) + (s2 + s3);
     }
   } else {
     // nsplit * TE <= nthr: one partial sum per thread, combined in fixed order
     for (int i = threadIdx.x; i < TE * nsplit; i += nthr) {
       const int o = i % TE, part = i / TE;
       const int p0 = part_lo(part, a.n_part, nsplit), p1 = part_lo(part + 1, a.n_part, nsplit);
-      float s = 0.0f;
-#pragma unroll 4
-      for (int p = p0; p < p1; ++p) s += __ldcg(a.partials + (size_t)p * TE + o);
-      s_scratch[part * TE + o] = s;
+      float s0 = 0.0f, s1 = 0.0f;
+      int p = p0;
+      for (; p + 2 <= p1; p += 2) {
+        s0 += src[(size_t)p * TE + o];
+        s1 += src[(size_t)(p + 1) * TE + o];
+      }
+      if (p < p1) s0 += src[(size_t)p * TE + o];
+      s_scratch[part * TE + o] = s0 + s1;
     }
     __syncthreads();
     for (int o = threadIdx.x; o < TE; o += nthr) {
@@ -241,13 +353,10 @@ __device__ void route_block(const Dec2Args &a, float *s_logits, int *s_idx, floa
     }
   }
   __syncthreads();
-  const int warp = threadIdx.x >> 5, nw = nthr >> 5, lane = threadIdx.x & 31;
-  bool nan = false;
-  for (int t = warp; t < T; t += nw)
-    nan |= warp_topk(s_logits + t * E, E, k, s_idx + t * k, s_gates + t * k, s_park + warp * k);
-  if (publish && lane == 0 && nan) set_flag(a.ctrl, COLI_FLAG_NAN_LOGITS);
-  __syncthreads();
+  const bool nan = block_topk(s_logits, T, E, k, s_idx, s_gates, s_vals, s_rank,
+                              (int *)s_scratch);
   if (publish) {
+    if (threadIdx.x == 0 && nan) set_flag(a.ctrl, COLI_FLAG_NAN_LOGITS);
     for (int i = threadIdx.x; i < T * k; i += nthr) {
       a.g_idx[i] = s_idx[i];
       a.g_gates[i] = s_gates[i];
@@ -257,17 +366,27 @@ __device__ void route_block(const Dec2Args &a, float *s_logits, int *s_idx, floa
 }
 
 __global__ void __launch_bounds__(256) k_topk(Dec2Args a) {
-  extern __shared__ __align__(16) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem[];
   grid_dependents_launch();
-  grid_dependency_wait();
-  float *s_logits = (float *)smem;
-  int *s_idx = (int *)(s_logits + a.T * a.E);
-  float *s_gates = (float *)(s_idx + a.T * a.k);
-  float *s_park = s_gates + a.T * a.k;
-  float *s_scratch = s_park + 8 * a.k;
-  route_block(a, s_logits, s_idx, s_gates, s_park, s_scratch, true);
+  uint64_t *pbar = (uint64_t *)smem;
+  if (threadIdx.x == 0) {
+    mbar_init(pbar, 1);
+    fence_mbar_init();
+  }
   __syncthreads();
-  for (int i = threadIdx.x; i < a.T * a.k; i += blockDim.x) {
+  grid_dependency_wait();
+  const int T = a.T, E = a.E, k = a.k;
+  float *s_stage = (float *)(smem + 128);
+  float *s_logits = s_stage + (a.gu_stage_partials ? (size_t)a.n_part * T * E : 0);
+  int *s_rank = (int *)(s_logits + T * E);
+  int *s_idx = s_rank + T * E;
+  float *s_gates = (float *)(s_idx + T * k);
+  float *s_vals = s_gates + T * k;
+  float *s_scratch = s_vals + T * k;
+  route_block(a, s_logits, s_idx, s_gates, s_vals, s_rank, s_scratch,
+              a.gu_stage_partials ? s_stage : nullptr, pbar, true);
+  __syncthreads();
+  for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
     if (a.idx_out) a.idx_out[i] = s_idx[i];
     if (a.gates_out) a.gates_out[i] = s_gates[i];
   }
@@ -276,31 +395,38 @@ __global__ void __launch_bounds__(256) k_topk(Dec2Args a) {
 // ---------------------------------------------------------------------------
 // gate/up
 
-template <typename XT>
 __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const GuSmem &L = a.gu;
   const int T = a.T, H = a.H, F = a.F, E = a.E, S = a.S, k = a.k, KS = k + S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nwc = a.gu_ncg * a.gu_nrg;   // compute warps; warp nwc is the producer
+  const int ns = a.gu_ns;
   uint64_t *full = (uint64_t *)(smem + L.bar);
-  uint64_t *done = full + a.gu_ns;
-  int *s_abort = (int *)(done + a.gu_ns);
+  uint64_t *done = full + ns;
+  uint64_t *pbar = done + ns;
+  int *s_abort = (int *)(pbar + 1);
+  int *s_desc = (int *)(smem + L.desc);   // [3][16]: segment, first row, rows per slot
   if (tid == 0) {
-    for (int i = 0; i < a.gu_ns; ++i) {
+    for (int i = 0; i < ns; ++i) {
       mbar_init(full + i, 1);
       mbar_init(done + i, nwc);
     }
+    mbar_init(pbar, 1);
     *s_abort = 0;
     fence_mbar_init();
   }
+  __syncthreads();
   grid_dependents_launch();
+  if (tid == 0) COLI_TRACE_POINT(0, 0);
   grid_dependency_wait();
+  if (tid == 0) COLI_TRACE_POINT(0, 1);
 
   float *s_logits = (float *)(smem + L.logits);
   int *s_idx = (int *)(smem + L.idx);
   float *s_gates = (float *)(smem + L.gates);
-  float *s_park = (float *)(smem + L.park);
+  float *s_vals = (float *)(smem + L.vals);
+  int *s_rank = (int *)(smem + L.rank);
   float *s_scratch = (float *)(smem + L.scratch);
   int *s_act = (int *)(smem + L.act);          // [0] n_active, act_expert, act_off
   int *s_act_expert = s_act + 1;
@@ -309,14 +435,13 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
   float *s_slot_gate = (float *)(smem + L.slot_gate);
   const bool cta0 = blockIdx.x == 0;
 
-  route_block(a, s_logits, s_idx, s_gates, s_park, s_scratch, cta0);
-  if (warp == 0) {
-    const int na = warp_union(s_idx, s_gates, T, k, S, E, s_act_expert, s_act_off, s_routes,
-                              s_slot_gate);
-    if (lane == 0) s_act[0] = na;
-  }
-  __syncthreads();
-  const int n_active = s_act[0];
+  // partials are staged in the (not yet used) weight ring
+  route_block(a, s_logits, s_idx, s_gates, s_vals, s_rank, s_scratch,
+              a.gu_stage_partials ? (float *)(smem + L.ring) : nullptr, pbar, cta0);
+  if (tid == 0) COLI_TRACE_POINT(0, 2);
+  const int n_active = block_union(s_idx, s_gates, T, k, S, E, s_act, s_act_expert, s_act_off,
+                                   s_routes, s_slot_gate, s_rank);
+  if (tid == 0) COLI_TRACE_POINT(0, 3);
   if (cta0) {
     for (int i = tid; i < 1 + 2 * (E + S) + 1; i += blockDim.x) a.g_act[i] = s_act[i];
     for (int i = tid; i < T * KS; i += blockDim.x) {
@@ -330,56 +455,51 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
   const int F4 = F / 4;
   const int U = n_active * F4;
   const int u0 = part_lo(c, U, G), u1 = part_lo(c + 1, U, G);
-  const int rs4 = a.gu_rs / 4, ns = a.gu_ns;
+  const int rs4 = a.gu_rs / 4;
   const int64_t rb = H / 2, ngr = H / kGroup;
   const int stage_bytes = a.gu_rs * (H + H / 8);
   float *red = (float *)(smem + L.red);
   const int red_stride = a.gu_rs * T * a.gu_ncg * 2;
 
   if (warp == nwc) {
-    // ---------------- producer warp ----------------
+    // ---------------- producer warp: issue copies, finalise h ----------------
+    fence_proxy_async();   // the ring held the staged partials
     StageIter it(u0, u1, F4, rs4);
-    int sa[16], sr[16], sn[16];   // descriptors of stages in flight (ns <= 16)
-    int s = 0, fin = 0;
-    int ai, r0, n;
-    bool ok = true;
-    // L2 prefetch of the down rows that the same-index k_down CTA will read
-    auto prefetch_down = [&]() {
-      if (lane != 0 || c >= a.n_part) return;
-      const int UH = H / 4;
-      const int dh0 = 4 * part_lo(c, UH, a.n_part), dh1 = 4 * part_lo(c + 1, UH, a.n_part);
-      for (int q = 0; q < n_active && dh1 > dh0; ++q) {
-        const int e = s_act_expert[q];
-        prefetch_l2(a.packed + (int64_t)e * a.eb + (int64_t)F * H + (int64_t)dh0 * (F / 2),
-                    (uint32_t)((dh1 - dh0) * (F / 2)));
-        prefetch_l2(a.scales + (int64_t)e * a.es + (int64_t)2 * F * ngr + (int64_t)dh0 * (F / kGroup),
-                    (uint32_t)((dh1 - dh0) * (F / 16)));
-      }
-    };
-    auto finalize = [&](int st) {
-      const int slot = st % ns;
-      const int fa = sa[slot], f0 = sr[slot], fn = sn[slot];
-      const int j0 = s_act_off[fa], ntok = s_act_off[fa + 1] - j0;
-      const float *rd = red + slot * red_stride;
-      for (int i = lane; i < fn * ntok; i += 32) {
-        const int r = i / ntok, j = i - r * ntok;
-        float g = 0.0f, u = 0.0f;
-        for (int cg = 0; cg < a.gu_ncg; ++cg) {
-          g += rd[((r * T + j) * a.gu_ncg + cg) * 2];
-          u += rd[((r * T + j) * a.gu_ncg + cg) * 2 + 1];
+    int s = 0, fin = 0, ai, r0, n;
+    bool ok = true, prefetched = false;
+    for (;;) {
+      const bool more = ok && it.next(ai, r0, n);
+      // finalise the oldest stage when its slot is needed again, or at the end
+      while (ok && fin < s && (!more || s - fin >= ns)) {
+        const int slot = fin % ns;
+        if (!mbar_wait(done + slot, (fin / ns) & 1)) { ok = false; break; }
+        const int fa = s_desc[slot], f0 = s_desc[16 + slot], fn = s_desc[32 + slot];
+        const int j0 = s_act_off[fa], ntok = s_act_off[fa + 1] - j0;
+        const float *rd = red + slot * red_stride;
+        for (int i = lane; i < fn * ntok; i += 32) {
+          const int r = i / ntok, j = i - r * ntok;
+          float g = 0.0f, u = 0.0f;
+          for (int cg = 0; cg < a.gu_ncg; ++cg) {
+            g += rd[((r * T + j) * a.gu_ncg + cg) * 2];
+            u += rd[((r * T + j) * a.gu_ncg + cg) * 2 + 1];
+          }
+          const int slot_id = s_routes[j0 + j];
+          const float hv = silu(g) * u * s_slot_gate[slot_id];
+          for (int rr = 0; rr < a.n_rep; ++rr)
+            a.h[rr * a.h_stride + (int64_t)slot_id * F + f0 + r] = hv;
         }
-        const int slot_id = s_routes[j0 + j];
-        a.h[(int64_t)slot_id * F + f0 + r] = silu(g) * u * s_slot_gate[slot_id];
+        __syncwarp();
+        ++fin;
       }
-    };
-    while (ok && it.next(ai, r0, n)) {
+      if (!more) {
+        if (lane == 0) COLI_TRACE_POINT(0, 6);
+        break;
+      }
       const int slot = s % ns;
-      if (s >= ns) {
-        if (!mbar_wait(done + slot, ((s / ns) - 1) & 1)) { ok = false; break; }
-        finalize(fin++);
-      }
-      sa[slot] = ai; sr[slot] = r0; sn[slot] = n;
       if (lane == 0) {
+        s_desc[slot] = ai;
+        s_desc[16 + slot] = r0;
+        s_desc[32 + slot] = n;
         const int e = s_act_expert[ai];
         const uint8_t *pg = a.packed + (int64_t)e * a.eb + (int64_t)r0 * rb;
         const uint8_t *pu = pg + (int64_t)F * rb;
@@ -393,33 +513,52 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
         bulk_g2s(dst + 2 * a.gu_rs * rb, sg, sb, full + slot);
         bulk_g2s(dst + 2 * a.gu_rs * rb + a.gu_rs * ngr * 4, su, sb, full + slot);
       }
-      ++s;
-      if (s == ns) prefetch_down();
       __syncwarp();
-    }
-    if (s < ns) prefetch_down();
-    if (ok) {
-      for (; fin < s; ++fin) {
-        const int slot = fin % ns;
-        if (!mbar_wait(done + slot, (fin / ns) & 1)) { ok = false; break; }
-        finalize(fin);
+      ++s;
+      if (!prefetched && (s == ns || it.u >= it.u1)) {
+        prefetched = true;
+        if (lane == 0) COLI_TRACE_POINT(0, 4);
+        // L2 prefetch of the down rows the same-index k_down CTA will read
+        if (lane == 0 && c < a.n_part) {
+          const int UH = H / 4;
+          const int dh0 = 4 * part_lo(c, UH, a.n_part), dh1 = 4 * part_lo(c + 1, UH, a.n_part);
+          for (int q = 0; q < n_active && dh1 > dh0; ++q) {
+            const int e = s_act_expert[q];
+            prefetch_l2(a.packed + (int64_t)e * a.eb + (int64_t)F * H + (int64_t)dh0 * (F / 2),
+                        (uint32_t)((dh1 - dh0) * (F / 2)));
+            prefetch_l2(a.scales + (int64_t)e * a.es + (int64_t)2 * F * ngr +
+                            (int64_t)dh0 * (F / kGroup),
+                        (uint32_t)((dh1 - dh0) * (F / 16)));
+          }
+        }
       }
     }
     if (!ok) {
       if (lane == 0) set_flag(a.ctrl, COLI_FLAG_TIMEOUT);
-      *s_abort = 1;
+      *(volatile int *)s_abort = 1;
       // drain copies still in flight before the CTA may exit
-      for (int st = (s > ns ? s - ns : 0); st < s; ++st)
-        (void)mbar_wait(full + (st % ns), (st / ns) & 1);
+      for (int st = fin; st < s; ++st) (void)mbar_wait(full + (st % ns), (st / ns) & 1);
     }
   } else if (warp < nwc) {
     // ---------------- compute warps ----------------
     const int cg = warp % a.gu_ncg, rg = warp / a.gu_ncg, nrg = a.gu_nrg;
     const int col = cg * kChunkCols + 32 * lane;
     const bool act = col < H;
-    const XT *x = (const XT *)a.x;
+    const float *x = a.xrep + (size_t)(c % a.n_rep) * a.x_stride;
     Planes pl;
     int cached = -1;
+    if (u1 > u0) {
+      // quantise the first stage's token now, while the first weights are in flight
+      const int t = s_routes[s_act_off[u0 / F4]] / KS;
+      float v[32];
+      if (act) load32<float>(x + (int64_t)t * H + col, v);
+      else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+      }
+      quantize32(v, pl);
+      cached = t;
+    }
     StageIter it(u0, u1, F4, rs4);
     int s = 0, ai, r0, n;
     while (it.next(ai, r0, n)) {
@@ -429,6 +568,10 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
         break;
       }
       if (*(volatile int *)s_abort) break;
+      if (warp == 0 && lane == 0) {
+        if (s == 0) COLI_TRACE_POINT(0, 5);
+        COLI_TRACE_STAGE(0, s);
+      }
       const uint8_t *stg = smem + L.ring + (size_t)slot * stage_bytes;
       const uint8_t *wg = stg, *wu = stg + a.gu_rs * rb;
       const float *sgp = (const float *)(stg + 2 * a.gu_rs * rb);
@@ -440,7 +583,7 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
         const int t = s_routes[j0 + j] / KS;
         if (t != cached) {
           float v[32];
-          if (act) load32<XT>(x + (int64_t)t * H + col, v);
+          if (act) load32<float>(x + (int64_t)t * H + col, v);
           else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.0f;
@@ -493,17 +636,17 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
   const int UH = H / 4;
   const int dh0 = 4 * part_lo(c, UH, G), dh1 = 4 * part_lo(c + 1, UH, G);
   const int nr = dh1 - dh0;
+  const int ns = a.dn_ns;
   uint64_t *full = (uint64_t *)(smem + L.bar);
-  uint64_t *done = full + a.dn_ns;
-  uint64_t *hbar = done + a.dn_ns;
-  int *s_abort = (int *)(hbar + 1);
+  uint64_t *done = full + ns;
+  int *s_abort = (int *)(done + ns);
+  int *s_desc = (int *)(smem + L.desc);
   WT *s_wr = (WT *)(smem + L.wr);
   if (tid == 0) {
-    for (int i = 0; i < a.dn_ns; ++i) {
+    for (int i = 0; i < ns; ++i) {
       mbar_init(full + i, 1);
       mbar_init(done + i, nwc);
     }
-    mbar_init(hbar, 1);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -515,59 +658,64 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
       s_wr[i] = wr[(size_t)e * H + dh0 + r];
     }
   }
+  __syncthreads();
   grid_dependents_launch();
+  if (tid == 0) COLI_TRACE_POINT(1, 0);
   grid_dependency_wait();
+  if (tid == 0) COLI_TRACE_POINT(1, 1);
   int *s_act = (int *)(smem + L.act);
   int *s_act_expert = s_act + 1;
   int *s_act_off = s_act + 1 + (E + S);
   int *s_routes = (int *)(smem + L.routes);
   float *s_acc = (float *)(smem + L.acc);   // [T][nr]
+  uint32_t *s_planes = (uint32_t *)(smem + L.planes);
+  const int nbp = a.dn_nbp;
   for (int i = tid; i < 1 + 2 * (E + S) + 1; i += blockDim.x) s_act[i] = __ldcg(a.g_act + i);
   for (int i = tid; i < T * KS; i += blockDim.x) s_routes[i] = __ldcg(a.g_routes + i);
   for (int i = tid; i < T * nr; i += blockDim.x) s_acc[i] = 0.0f;
+  // the slots' h vectors, quantised once for the whole CTA
+  const float *h_rep = a.h + (size_t)(c % a.n_rep) * a.h_stride;
+  if (a.dn_planes) build_planes(h_rep, T * KS, F, s_planes, nbp);
   __syncthreads();
+  if (tid == 0) COLI_TRACE_POINT(1, 2);
   const int n_active = s_act[0];
-  const int ns = a.dn_ns, rs4 = a.dn_rs / 4;
+  const int rs4 = a.dn_rs / 4;
   const int64_t rb = F / 2, ngr = F / kGroup;
   const int stage_bytes = a.dn_rs * (F / 2 + F / 16);
   float *red = (float *)(smem + L.red);
   const int red_stride = a.dn_rs * T * a.dn_ncg;
-  const float *s_h = (const float *)(smem + L.h);
   const int64_t down_b = (int64_t)F * H, down_s = (int64_t)2 * F * (H / kGroup);
   const int seg4 = nr / 4;
+  const int n_units = seg4 > 0 ? n_active * seg4 : 0;
 
   if (warp == nwc) {
-    StageIter it(0, n_active * seg4, seg4 > 0 ? seg4 : 1, rs4);
-    if (seg4 == 0) it.u1 = 0;
-    int sa[16], sr[16], sn[16];
+    StageIter it(0, n_units, seg4 > 0 ? seg4 : 1, rs4);
     int s = 0, fin = 0, ai, r0, n;
     bool ok = true;
-    if (a.dn_h_smem && lane == 0) {
-      const uint32_t hb = (uint32_t)(T * KS * F * 4);
-      mbar_arrive_expect_tx(hbar, hb);
-      bulk_g2s((void *)s_h, a.h, hb, hbar);
-    }
-    auto finalize = [&](int st) {
-      const int slot = st % ns;
-      const int fa = sa[slot], f0 = sr[slot], fn = sn[slot];
-      const int j0 = s_act_off[fa], ntok = s_act_off[fa + 1] - j0;
-      const float *rd = red + slot * red_stride;
-      for (int i = lane; i < fn * ntok; i += 32) {
-        const int r = i / ntok, j = i - r * ntok;
-        float v = 0.0f;
-        for (int cg = 0; cg < a.dn_ncg; ++cg) v += rd[(r * T + j) * a.dn_ncg + cg];
-        const int t = s_routes[j0 + j] / KS;
-        s_acc[t * nr + f0 + r] += v;   // experts finalised in ascending order
+    for (;;) {
+      const bool more = ok && it.next(ai, r0, n);
+      while (ok && fin < s && (!more || s - fin >= ns)) {
+        const int slot = fin % ns;
+        if (!mbar_wait(done + slot, (fin / ns) & 1)) { ok = false; break; }
+        const int fa = s_desc[slot], f0 = s_desc[16 + slot], fn = s_desc[32 + slot];
+        const int j0 = s_act_off[fa], ntok = s_act_off[fa + 1] - j0;
+        const float *rd = red + slot * red_stride;
+        for (int i = lane; i < fn * ntok; i += 32) {
+          const int r = i / ntok, j = i - r * ntok;
+          float v = 0.0f;
+          for (int cg = 0; cg < a.dn_ncg; ++cg) v += rd[(r * T + j) * a.dn_ncg + cg];
+          const int t = s_routes[j0 + j] / KS;
+          s_acc[t * nr + f0 + r] += v;   // experts finalised in ascending order
+        }
+        __syncwarp();
+        ++fin;
       }
-    };
-    while (ok && it.next(ai, r0, n)) {
+      if (!more) break;
       const int slot = s % ns;
-      if (s >= ns) {
-        if (!mbar_wait(done + slot, ((s / ns) - 1) & 1)) { ok = false; break; }
-        finalize(fin++);
-      }
-      sa[slot] = ai; sr[slot] = r0; sn[slot] = n;
       if (lane == 0) {
+        s_desc[slot] = ai;
+        s_desc[16 + slot] = r0;
+        s_desc[32 + slot] = n;
         const int e = s_act_expert[ai];
         const uint8_t *pd = a.packed + (int64_t)e * a.eb + down_b + (int64_t)(dh0 + r0) * rb;
         const float *sd = a.scales + (int64_t)e * a.es + down_s + (int64_t)(dh0 + r0) * ngr;
@@ -580,38 +728,28 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
       __syncwarp();
       ++s;
     }
-    if (ok)
-      for (; fin < s; ++fin) {
-        const int slot = fin % ns;
-        if (!mbar_wait(done + slot, (fin / ns) & 1)) { ok = false; break; }
-        finalize(fin);
-      }
     if (!ok) {
       if (lane == 0) set_flag(a.ctrl, COLI_FLAG_TIMEOUT);
-      *s_abort = 1;
-      for (int st = (s > ns ? s - ns : 0); st < s; ++st)
-        (void)mbar_wait(full + (st % ns), (st / ns) & 1);
+      *(volatile int *)s_abort = 1;
+      for (int st = fin; st < s; ++st) (void)mbar_wait(full + (st % ns), (st / ns) & 1);
     }
-    if (a.dn_h_smem) (void)mbar_wait(hbar, 0);
   } else if (warp < nwc) {
     const int cg = warp % a.dn_ncg, rg = warp / a.dn_ncg, nrg = a.dn_nrg;
     const int col = cg * kChunkCols + 32 * lane;
     const bool act = col < F;
-    bool h_ready = !a.dn_h_smem;
-    StageIter it(0, n_active * seg4, seg4 > 0 ? seg4 : 1, rs4);
-    if (seg4 == 0) it.u1 = 0;
+    StageIter it(0, n_units, seg4 > 0 ? seg4 : 1, rs4);
     int s = 0, ai, r0, n;
     while (it.next(ai, r0, n)) {
       const int slot = s % ns;
-      if (!h_ready) {
-        if (!mbar_wait(hbar, 0)) { if (lane == 0) set_flag(a.ctrl, COLI_FLAG_TIMEOUT); break; }
-        h_ready = true;
-      }
       if (!mbar_wait(full + slot, (s / ns) & 1)) {
         if (lane == 0) set_flag(a.ctrl, COLI_FLAG_TIMEOUT);
         break;
       }
       if (*(volatile int *)s_abort) break;
+      if (warp == 0 && lane == 0) {
+        if (s == 0) COLI_TRACE_POINT(1, 3);
+        COLI_TRACE_STAGE(1, s);
+      }
       const uint8_t *stg = smem + L.ring + (size_t)slot * stage_bytes;
       const float *sdp = (const float *)(stg + a.dn_rs * rb);
       float *rd = red + slot * red_stride;
@@ -620,12 +758,13 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
       for (int j = 0; j < ntok; ++j) {
         const int slot_id = s_routes[j0 + j];
         Planes pl;
-        {
+        if (a.dn_planes) {
+          if (act) load_planes(s_planes, slot_id, col / 32, nbp, pl);
+          else { pl = Planes{}; }
+        } else {
           float v[32];
-          if (act) {
-            if (a.dn_h_smem) load32_smem(s_h + (int64_t)slot_id * F + col, v);
-            else load32<float>(a.h + (int64_t)slot_id * F + col, v);
-          } else {
+          if (act) load32<float>(h_rep + (int64_t)slot_id * F + col, v);
+          else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.0f;
           }
@@ -657,7 +796,9 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
       ++s;
     }
   }
+  if (tid == 0) COLI_TRACE_POINT(1, 4);
   __syncthreads();
+  if (tid == 0) COLI_TRACE_POINT(1, 5);
   // combine is complete: residual, outputs, next layer's partial logits
   float *s_xn = (float *)(smem + L.xn);   // [T][nr]
   for (int i = tid; i < T * nr; i += blockDim.x) {
@@ -668,6 +809,8 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
     const float xn = a.residual ? a.residual[o] + v : v;
     a.out[o] = xn;
     s_xn[i] = xn;
+    if (a.xrep)
+      for (int rr = 0; rr < a.n_rep; ++rr) a.xrep[rr * a.x_stride + o] = xn;
   }
   if (a.wr) {
     __syncthreads();
@@ -675,13 +818,26 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
       const int t = o / E, e = o - t * E;
       float sum = 0.0f;
       for (int r = 0; r < nr; ++r) sum = fmaf(to_f32(s_wr[e * nr + r]), s_xn[t * nr + r], sum);
-      a.partials[(size_t)c * T * E + o] = sum;
+      for (int rr = 0; rr < a.n_rep; ++rr)
+        a.partials[rr * a.part_stride + (size_t)c * T * E + o] = sum;
     }
   }
+#ifdef COLI_TRACE
+  __syncthreads();
+  if (tid == 0) COLI_TRACE_POINT(1, 6);
+#endif
 }
 
 // ---------------------------------------------------------------------------
 // host side
+
+#ifdef COLI_TRACE
+extern "C" int coli_trace_read(void *points, void *stages) {
+  if (cudaMemcpyFromSymbol(points, g_trace, sizeof(g_trace)) != cudaSuccess) return -1;
+  if (cudaMemcpyFromSymbol(stages, g_trace_stage, sizeof(g_trace_stage)) != cudaSuccess) return -1;
+  return 0;
+}
+#endif
 
 namespace {
 
@@ -738,11 +894,13 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
   g.logits = o; o = al16(o + (size_t)T * E * 4);
   g.idx = o; o = al16(o + (size_t)T * k * 4);
   g.gates = o; o = al16(o + (size_t)T * k * 4);
-  g.park = o; o = al16(o + (size_t)(kDec2MaxThreads / 32) * k * 4);
+  g.vals = o; o = al16(o + (size_t)T * k * 4);
+  g.rank = o; o = al16(o + (size_t)(T * E > T * k ? T * E : T * k) * 4);
   g.scratch = o; o = al16(o + (size_t)kDec2MaxThreads * 4);
   g.act = o; o = al16(o + (size_t)(2 + 2 * (E + S)) * 4);
   g.routes = o; o = al16(o + (size_t)T * KS * 4);
   g.slot_gate = o; o = al16(o + (size_t)T * KS * 4);
+  g.desc = o; o = al16(o + 48 * 4);
   const size_t fixed = o;
   const size_t row_bytes = (size_t)H + H / 8;   // gate + up nibbles and scales per row pair
   int rs = (int)(40960 / row_bytes) / 4 * 4;
@@ -760,9 +918,10 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
   o = al128(fixed);
   g.ring = o; o += (size_t)ns * rs * row_bytes;
   g.red = o; o = al16(o + (size_t)ns * rs * red_row);
-  g.bar = o; o += (size_t)ns * 16 + 16;
+  g.bar = o; o += (size_t)(2 * ns + 1) * 8 + 16;
   g.total = al16(o);
   a.gu = g;
+  a.gu_stage_partials = (size_t)n_part * T * E * 4 <= (size_t)ns * rs * row_bytes;
   // ---- down
   a.dn_ncg = (F + kChunkCols - 1) / kChunkCols;
   a.dn_nrg = 12 / a.dn_ncg;
@@ -771,6 +930,9 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
   if (a.dn_nrg < 1) return cudaErrorInvalidValue;
   const int UH = H / 4;
   const int max_nr = 4 * ((UH + n_part - 1) / n_part);
+  a.dn_nbp = F / 32;
+  const size_t planes_bytes = (size_t)T * KS * 18 * a.dn_nbp * 4;
+  a.dn_planes = planes_bytes <= 98304;
   DnSmem d{};
   o = 0;
   d.act = o; o = al16(o + (size_t)(2 + 2 * (E + S)) * 4);
@@ -778,31 +940,26 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
   d.acc = o; o = al16(o + (size_t)T * max_nr * 4);
   d.xn = o; o = al16(o + (size_t)T * max_nr * 4);
   d.wr = o; o = al16(o + (size_t)E * max_nr * 4);
+  d.desc = o; o = al16(o + 48 * 4);
+  d.planes = o; o = al16(o + (a.dn_planes ? planes_bytes : 0));
   const size_t fixed_d = o;
   const size_t drow = (size_t)F / 2 + F / 16;
   int rsd = max_nr;
   while ((size_t)rsd * drow > 65536 && rsd > 4) rsd -= 4;
   const size_t red_drow = (size_t)T * a.dn_ncg * 4;
-  const size_t hbytes = (size_t)T * KS * F * 4;
-  a.dn_h_smem = 0;
   int nsd = 0;
-  for (int try_h = 1; try_h >= 0; --try_h) {
-    const size_t hb = try_h ? al128(hbytes) : 0;
-    if (try_h && hbytes > 98304) continue;
-    for (nsd = 16; nsd >= 2; --nsd) {
-      const size_t need = al128(fixed_d) + hb + nsd * rsd * drow + nsd * rsd * red_drow + nsd * 16 + 96;
-      if (need <= budget) break;
-    }
-    if (nsd >= 2) { a.dn_h_smem = try_h; break; }
+  for (nsd = 16; nsd >= 2; --nsd) {
+    const size_t need = al128(fixed_d) + nsd * rsd * drow + nsd * rsd * red_drow + nsd * 16 + 96;
+    if (need <= budget) break;
   }
   if (nsd < 2) return cudaErrorInvalidValue;
   // no more stages than the CTA can use
-  const int stages_needed = ((E + S) < T * k + S ? (E + S) : T * k + S) * ((max_nr / 4 + rsd / 4 - 1) / (rsd / 4));
+  const int n_used = ((E < T * k) ? E : T * k) + S;
+  const int stages_needed = n_used * ((max_nr / 4 + rsd / 4 - 1) / (rsd / 4));
   if (nsd > stages_needed && stages_needed >= 2) nsd = stages_needed;
   a.dn_rs = rsd;
   a.dn_ns = nsd;
   o = al128(fixed_d);
-  d.h = o; o += a.dn_h_smem ? al128(hbytes) : 0;
   d.ring = o; o += (size_t)nsd * rsd * drow;
   d.red = o; o = al16(o + (size_t)nsd * rsd * red_drow);
   d.bar = o; o += (size_t)nsd * 16 + 32;
@@ -819,22 +976,22 @@ cudaError_t launch_route_partials(const Dec2Args &a, int x_bf16, int w_bf16, cud
   return launch(k_route<__nv_bfloat16, __nv_bfloat16>, a.n_part, 256, 0, s, pdl, a);
 }
 
-cudaError_t launch_topk(const Dec2Args &a, cudaStream_t s, bool pdl) {
-  const size_t smem = (size_t)(a.T * a.E + 2 * a.T * a.k + 8 * a.k + 256) * 4;
+cudaError_t launch_topk(const Dec2Args &a_in, cudaStream_t s, bool pdl) {
+  Dec2Args a = a_in;
+  const size_t rest = (size_t)(2 * a.T * a.E + 3 * a.T * a.k + 256) * 4;
+  const size_t stage = (size_t)a.n_part * a.T * a.E * 4;
+  a.gu_stage_partials = 128 + stage + rest <= (size_t)max_smem() - 2048;
+  const size_t smem = 128 + (a.gu_stage_partials ? stage : 0) + rest;
   cudaError_t e = allow_smem(k_topk, smem);
   if (e != cudaSuccess) return e;
   return launch(k_topk, 1, 256, smem, s, pdl, a);
 }
 
-cudaError_t launch_gateup(const Dec2Args &a, int x_bf16, int grid, cudaStream_t s, bool pdl) {
+cudaError_t launch_gateup(const Dec2Args &a, int grid, cudaStream_t s, bool pdl) {
   const int threads = (a.gu_ncg * a.gu_nrg + 1) * 32;
-  cudaError_t e;
-  if (x_bf16) {
-    if ((e = allow_smem(k_gateup<__nv_bfloat16>, a.gu.total)) != cudaSuccess) return e;
-    return launch(k_gateup<__nv_bfloat16>, grid, threads, a.gu.total, s, pdl, a);
-  }
-  if ((e = allow_smem(k_gateup<float>, a.gu.total)) != cudaSuccess) return e;
-  return launch(k_gateup<float>, grid, threads, a.gu.total, s, pdl, a);
+  cudaError_t e = allow_smem(k_gateup, a.gu.total);
+  if (e != cudaSuccess) return e;
+  return launch(k_gateup, grid, threads, a.gu.total, s, pdl, a);
 }
 
 cudaError_t launch_down(const Dec2Args &a, int wr_bf16, cudaStream_t s, bool pdl) {

@@ -18,80 +18,74 @@ __device__ __forceinline__ bool ranks_before(float a, int ia, float b, int ib) {
   return ia < ib;
 }
 
-// Top-k of one token's E logits (any memory space) by one warp.
-// Writes idx[0..k) (descending) and gates[0..k); returns true if a logit is NaN.
-// `park` is k floats of scratch used when k > 32.
-__device__ __noinline__ bool warp_topk(const float *lg, int E, int k, int *idx, float *gates,
-                                       float *park) {
-  const int lane = threadIdx.x & 31;
-  bool any_nan = false;
-  float sel_v = 0.0f;
-  int sel_i = 0;
-  // taken flags: bit i of the lane's mask is its entry e = lane + 32 i (E <= 1024)
-  uint32_t taken = 0;
-  for (int e = lane; e < E; e += 32)
-    if (lg[e] != lg[e]) any_nan = true;
-  for (int j = 0; j < k; ++j) {
-    float bv = 0.0f;
-    int bi = 0x7FFFFFFF;
-    for (int e = lane, i = 0; e < E; e += 32, ++i) {
-      if (taken & (1u << i)) continue;
-      const float v = lg[e];
-      if (bi == 0x7FFFFFFF || ranks_before(v, e, bv, bi)) { bv = v; bi = e; }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
-      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
-      if (oi != 0x7FFFFFFF && (bi == 0x7FFFFFFF || ranks_before(ov, oi, bv, bi))) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (j < 32 && lane == j) { sel_v = bv; sel_i = bi; }
-    if (j >= 32 && lane == 0) { idx[j] = bi; park[j] = bv; }
+// Block-parallel top-k of T tokens x E logits (shared memory), every thread of
+// the block taking part.  The rank of logit (t, e) is the number of logits of
+// token t that rank before it; the work is split into chunks whose counts are
+// added with shared-memory integer atomics, so the result does not depend on
+// scheduling.  s_rank: T*E ints of scratch.  Writes idx/gates [T][k]; returns
+// true (on every thread) if any logit is NaN.
+__device__ __forceinline__ bool block_topk(const float *lg, int T, int E, int k, int *idx,
+                                           float *gates, float *vals, int *s_rank, int *s_flag) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int TE = T * E;
+  int P = (nthr * 8) / TE;
+  if (P < 1) P = 1;
+  if (P > E / 8) P = E / 8 > 0 ? E / 8 : 1;
+  for (int i = tid; i < TE; i += nthr) s_rank[i] = 0;
+  if (tid == 0) *s_flag = 0;
+  __syncthreads();
+  const int chunk = (E + P - 1) / P;
+  for (int i = tid; i < TE * P; i += nthr) {
+    const int item = i / P, part = i - item * P;
+    const int t = item / E, e = item - t * E;
+    const float *lt = lg + t * E;
+    const float v = lt[e];
+    const int e0 = part * chunk, e1 = e0 + chunk < E ? e0 + chunk : E;
+    int r = 0;
+    for (int e2 = e0; e2 < e1; ++e2) r += ranks_before(lt[e2], e2, v, e);
+    if (r) atomicAdd(s_rank + item, r);
+    if (part == 0 && v != v) *s_flag = 1;
   }
-  any_nan = __any_sync(0xFFFFFFFFu, any_nan);
-  const float l0 = __shfl_sync(0xFFFFFFFFu, sel_v, 0);
-  const bool all_nan = (l0 != l0);
-  float num = 0.0f;
-  if (lane < k) num = (sel_v != sel_v) ? 0.0f : expf(sel_v - l0);
-  float extra = 0.0f;
-  if (lane == 0)
-    for (int j = 32; j < k; ++j) {
-      const float lj = park[j];
-      extra += (lj != lj) ? 0.0f : expf(lj - l0);
+  __syncthreads();
+  for (int i = tid; i < TE; i += nthr) {
+    const int r = s_rank[i];
+    if (r < k) {
+      const int t = i / E;
+      idx[t * k + r] = i - t * E;
+      vals[t * k + r] = lg[i];
     }
-  float den = num;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xFFFFFFFFu, den, off);
-  den += __shfl_sync(0xFFFFFFFFu, extra, 0);
-  if (lane < k) {
-    idx[lane] = sel_i;
-    gates[lane] = all_nan ? 1.0f / (float)k : num / den;
   }
-  if (lane == 0)
-    for (int j = 32; j < k; ++j) {
-      const float lj = park[j];
-      gates[j] = all_nan ? 1.0f / (float)k : ((lj != lj) ? 0.0f : expf(lj - l0) / den);
+  __syncthreads();
+  // gates = exp(l_j - l_0) / sum_j' exp(l_j' - l_0); NaN picks 0; all NaN -> 1/k
+  for (int i = tid; i < T * k; i += nthr) {
+    const int t = i / k;
+    const float *vt = vals + t * k;
+    const float l0 = vt[0];
+    float g;
+    if (l0 != l0) {
+      g = 1.0f / (float)k;
+    } else {
+      float den = 0.0f;
+      for (int j = 0; j < k; ++j) den += (vt[j] != vt[j]) ? 0.0f : expf(vt[j] - l0);
+      const float lj = vt[i - t * k];
+      g = (lj != lj) ? 0.0f : expf(lj - l0) / den;
     }
-  __syncwarp();
-  return any_nan;
+    gates[i] = g;
+  }
+  const bool nan = *(volatile int *)s_flag != 0;
+  __syncthreads();
+  return nan;
 }
 
-// Union lists (one warp): routed experts in ascending id, each with its slots
-// in token order, then the S shared experts with every token.  Slot of (t, j)
-// is t*(k+S) + j; shared expert s of token t is slot t*(k+S) + k + s.
-//   act_expert[na], act_off[na+1], routes[T*(k+S)], slot_gate[T*(k+S)]; returns na.
-__device__ __noinline__ int warp_union(const int *idx, const float *gates, int T, int k, int S,
-                                       int E, int *act_expert, int *act_off, int *routes,
-                                       float *slot_gate) {
-  const int lane = threadIdx.x & 31;
+// Block-parallel union lists (see warp_union for the layout).  s_sorted: T*k
+// ints of scratch.  Returns the number of used experts (routed + shared).
+__device__ __forceinline__ int block_union(const int *idx, const float *gates, int T, int k, int S,
+                                           int E, int *act, int *act_expert, int *act_off,
+                                           int *routes, float *slot_gate, int *s_sorted_e) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
   const int KS = k + S;
   const int n = T * k;
-  // rank of each route by (expert, route id): routes[rank] = slot
-  for (int r = lane; r < n; r += 32) {
+  for (int r = tid; r < n; r += nthr) {
     const int er = idx[r];
     int rank = 0;
     for (int q = 0; q < n; ++q) {
@@ -100,46 +94,32 @@ __device__ __noinline__ int warp_union(const int *idx, const float *gates, int T
     }
     const int t = r / k, j = r - t * k;
     routes[rank] = t * KS + j;
+    s_sorted_e[rank] = er;
     slot_gate[t * KS + j] = gates[r];
   }
-  for (int t = lane; t < T; t += 32)
-    for (int s = 0; s < S; ++s) {
-      slot_gate[t * KS + k + s] = 1.0f;
-      routes[n + s * T + t] = t * KS + k + s;
-    }
-  __syncwarp();
-  // expert boundaries in the sorted order
-  int na = 0;
-  for (int p0 = 0; p0 < n; p0 += 32) {
-    const int p = p0 + lane;
-    bool start = false;
-    int e = -1;
-    if (p < n) {
-      const int slot = routes[p];
-      e = idx[(slot / KS) * k + slot % KS];
-      if (p == 0) start = true;
-      else {
-        const int ps = routes[p - 1];
-        start = idx[(ps / KS) * k + ps % KS] != e;
-      }
-    }
-    const unsigned m = __ballot_sync(0xFFFFFFFFu, start);
-    if (start) {
-      const int pos = na + __popc(m & ((1u << lane) - 1));
-      act_expert[pos] = e;
-      act_off[pos] = p;
-    }
-    na += __popc(m);
+  for (int i = tid; i < T * S; i += nthr) {
+    const int s = i / T, t = i - s * T;
+    slot_gate[t * KS + k + s] = 1.0f;
+    routes[n + s * T + t] = t * KS + k + s;
   }
-  if (lane == 0) {
+  __syncthreads();
+  if (tid == 0) {
+    int na = 0;
+    for (int p = 0; p < n; ++p)
+      if (p == 0 || s_sorted_e[p] != s_sorted_e[p - 1]) {
+        act_expert[na] = s_sorted_e[p];
+        act_off[na] = p;
+        ++na;
+      }
     for (int s = 0; s < S; ++s) {
       act_expert[na + s] = E + s;
       act_off[na + s] = n + s * T;
     }
     act_off[na + S] = n + S * T;
+    act[0] = na + S;
   }
-  __syncwarp();
-  return na + S;
+  __syncthreads();
+  return act[0];
 }
 
 }  // namespace coli

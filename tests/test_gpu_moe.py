@@ -47,7 +47,7 @@ def check_layer(shape, T, x_dtype=torch.float32, seed=0, repeat=1):
 
 def test_tiny_config():
     err = check_layer(synth.TINY, 4)
-    assert err.max() < 1e-4      # f32 GEMV path: far inside the 2e-3 bound
+    assert err.max() < 5e-4      # 15-bit activations: far inside the 2e-3 bound
 
 
 SMALL = [
