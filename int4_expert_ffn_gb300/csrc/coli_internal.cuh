@@ -44,15 +44,15 @@ struct WsLayout {
 
 WsLayout ws_layout(int T, int H, int F, int E, int S, int k);
 
-constexpr int kDec2MaxThreads = 640;
+constexpr int kDec2MaxThreads = 512;
 
 // Shared-memory plan of k_gateup (byte offsets into dynamic smem).
 struct GuSmem {
-  size_t logits, idx, gates, vals, rank, scratch, act, routes, slot_gate, desc, ring, red, bar, total;
+  size_t logits, idx, gates, vals, rank, scratch, act, routes, slot_gate, red, xpl, stage, total;
 };
 // Shared-memory plan of k_down.
 struct DnSmem {
-  size_t act, routes, acc, xn, wr, desc, planes, ring, red, bar, total;
+  size_t act, routes, acc, xn, wr, planes, total;
 };
 
 // Arguments of the decode kernels (one layer, T <= kDecodeMaxT tokens).
@@ -82,8 +82,8 @@ struct Dec2Args {
   float *layer_out;         // or null
   int32_t *idx_out;         // k_topk user outputs (or null)
   float *gates_out;
-  int gu_ncg, gu_nrg, gu_rs, gu_ns, gu_stage_partials;
-  int dn_ncg, dn_nrg, dn_rs, dn_ns, dn_planes, dn_nbp;
+  int gu_ncg, gu_nrg, gu_stage_partials, gu_xpl;
+  int dn_ncg, dn_nrg, dn_slots;
   GuSmem gu;
   DnSmem dn;
 };

@@ -159,17 +159,34 @@ __device__ __forceinline__ float reduce8(float (&v)[8]) {
 // word w (0..15 planes, 16 = sq, 17 = sx bits) of 32-column block b of vector v
 // is at planes[(v * 18 + w) * nbp + b].  One warp handles 4 blocks at a time;
 // lane q of a block's 8 lanes holds its columns 4q..4q+3.
-__device__ void build_planes(const float *src, int n_vec, int F, uint32_t *planes, int nbp) {
+__device__ void build_planes_impl(const float *src, int n_vec, int F, const int *list,
+                                  uint32_t *planes, int nbp) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int groups_per_vec = (F + 127) / 128;
   const int n_groups = n_vec * groups_per_vec;
   const int q = lane & 7;
-  for (int g = warp; g < n_groups; g += nw) {
+  for (int g0 = warp; g0 < n_groups; g0 += 8 * nw) {
+    // issue up to eight independent loads before using any of them
+    float4 xs[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int g = g0 + u * nw;
+      xs[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (g < n_groups) {
+        const int v = g / groups_per_vec, gc = g - v * groups_per_vec;
+        const int col = gc * 128 + 4 * lane;
+        const int64_t row = list ? list[v] : v;
+        if (col < F) xs[u] = __ldcg((const float4 *)(src + row * F + col));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+    const int g = g0 + u * nw;
+    if (g >= n_groups) break;
     const int v = g / groups_per_vec, gc = g - v * groups_per_vec;
     const int col = gc * 128 + 4 * lane;
     const bool act = col < F;
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (act) x = __ldcg((const float4 *)(src + (int64_t)v * F + col));
+    const float4 x = xs[u];
     float m = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
     bool bad = (x.x != x.x) | (x.y != x.y) | (x.z != x.z) | (x.w != x.w);
 #pragma unroll
@@ -215,7 +232,21 @@ __device__ void build_planes(const float *src, int n_vec, int F, uint32_t *plane
         pv[(size_t)17 * nbp] = __float_as_uint(sx);
       }
     }
+    }
   }
+}
+
+// build_planes over a list of source rows: vector p is row list[p] of src.
+__device__ void build_planes_list(const float *src, int F, const int *list, int n, uint32_t *planes,
+                                  int nbp);
+
+__device__ void build_planes(const float *src, int n_vec, int F, uint32_t *planes, int nbp) {
+  build_planes_impl(src, n_vec, F, nullptr, planes, nbp);
+}
+
+__device__ void build_planes_list(const float *src, int F, const int *list, int n, uint32_t *planes,
+                                  int nbp) {
+  build_planes_impl(src, n, F, list, planes, nbp);
 }
 
 __device__ __forceinline__ void load_planes(const uint32_t *planes, int v, int b, int nbp,
@@ -242,24 +273,6 @@ __device__ __forceinline__ void set_flag(uint32_t *ctrl, uint32_t f) {
   atomicOr(ctrl + kCtrlFlags, f);
 }
 
-struct StageIter {
-  int u, u1, seg4, rs4;
-  __device__ StageIter(int u0_, int u1_, int seg4_, int rs4_)
-      : u(u0_), u1(u1_), seg4(seg4_), rs4(rs4_) {}
-  // next (segment index, first row in segment, rows) in units of 4 rows
-  __device__ bool next(int &a, int &r0, int &n) {
-    if (u >= u1) return false;
-    a = u / seg4;
-    const int ru = u - a * seg4;
-    int nu = rs4;
-    if (nu > u1 - u) nu = u1 - u;
-    if (nu > seg4 - ru) nu = seg4 - ru;
-    r0 = ru * 4;
-    n = nu * 4;
-    u += nu;
-    return true;
-  }
-};
 
 }  // namespace
 
@@ -299,21 +312,32 @@ __global__ void __launch_bounds__(256) k_route(Dec2Args a) {
 // Routing shared by k_gateup and k_topk: logits from the partials (fixed
 // order), top-k per token by warps, NaN flag.
 
+// Routing shared by k_gateup and k_topk: logits from this CTA's replica of the
+// router partials (fixed summation order), block-parallel top-k, NaN flag and,
+// if `publish`, the user-visible idx/gates and route counts.
 __device__ void route_block(const Dec2Args &a, float *s_logits, int *s_idx, float *s_gates,
                             float *s_vals, int *s_rank, float *s_scratch, float *s_stage,
-                            uint64_t *pbar, bool publish) {
+                            bool publish) {
   const int T = a.T, E = a.E, k = a.k;
   const int TE = T * E;
   const int nthr = blockDim.x;
   const float *src = a.partials + (size_t)(blockIdx.x % a.n_rep) * a.part_stride;
   if (s_stage) {
-    // one bulk copy of all partials into shared memory, then reduce there
-    if (threadIdx.x == 0) {
-      const uint32_t bytes = (uint32_t)((size_t)a.n_part * TE * 4);
-      mbar_arrive_expect_tx(pbar, bytes);
-      bulk_g2s(s_stage, src, bytes, pbar);
+    // all threads copy the partials into shared memory, every load in flight at once
+    const int n4 = (a.n_part * TE) / 4, tail = (a.n_part * TE) & 3;
+    const float4 *s4 = (const float4 *)src;
+    float4 *d4 = (float4 *)s_stage;
+    for (int i0 = threadIdx.x; i0 < n4; i0 += 8 * nthr) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (i0 + u * nthr < n4) v[u] = __ldcg(s4 + i0 + u * nthr);
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (i0 + u * nthr < n4) d4[i0 + u * nthr] = v[u];
     }
-    if (!mbar_wait(pbar, 0)) set_flag(a.ctrl, COLI_FLAG_TIMEOUT);
+    if (threadIdx.x < tail) s_stage[4 * n4 + threadIdx.x] = __ldcg(src + 4 * n4 + threadIdx.x);
+    __syncthreads();
     src = s_stage;
   }
   int nsplit = nthr / TE;
@@ -368,15 +392,9 @@ __device__ void route_block(const Dec2Args &a, float *s_logits, int *s_idx, floa
 __global__ void __launch_bounds__(256) k_topk(Dec2Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   grid_dependents_launch();
-  uint64_t *pbar = (uint64_t *)smem;
-  if (threadIdx.x == 0) {
-    mbar_init(pbar, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
   grid_dependency_wait();
   const int T = a.T, E = a.E, k = a.k;
-  float *s_stage = (float *)(smem + 128);
+  float *s_stage = (float *)smem;
   float *s_logits = s_stage + (a.gu_stage_partials ? (size_t)a.n_part * T * E : 0);
   int *s_rank = (int *)(s_logits + T * E);
   int *s_idx = s_rank + T * E;
@@ -384,7 +402,7 @@ __global__ void __launch_bounds__(256) k_topk(Dec2Args a) {
   float *s_vals = s_gates + T * k;
   float *s_scratch = s_vals + T * k;
   route_block(a, s_logits, s_idx, s_gates, s_vals, s_rank, s_scratch,
-              a.gu_stage_partials ? s_stage : nullptr, pbar, true);
+              a.gu_stage_partials ? s_stage : nullptr, true);
   __syncthreads();
   for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
     if (a.idx_out) a.idx_out[i] = s_idx[i];
@@ -393,35 +411,22 @@ __global__ void __launch_bounds__(256) k_topk(Dec2Args a) {
 }
 
 // ---------------------------------------------------------------------------
-// gate/up
+// gate/up: each compute warp owns one 1024-column chunk (cg) of every row
+// congruent to rg modulo nrg within the CTA's row range, issues the loads of
+// up to kGuBatch rows before computing any of them, and leaves per-row partial
+// sums in shared memory; after one barrier the block finalises
+// h = silu(g) * u * gate and writes it to every replica.
+
+constexpr int kGuBatch = 4;
 
 __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const GuSmem &L = a.gu;
   const int T = a.T, H = a.H, F = a.F, E = a.E, S = a.S, k = a.k, KS = k + S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nwc = a.gu_ncg * a.gu_nrg;   // compute warps; warp nwc is the producer
-  const int ns = a.gu_ns;
-  uint64_t *full = (uint64_t *)(smem + L.bar);
-  uint64_t *done = full + ns;
-  uint64_t *pbar = done + ns;
-  int *s_abort = (int *)(pbar + 1);
-  int *s_desc = (int *)(smem + L.desc);   // [3][16]: segment, first row, rows per slot
-  if (tid == 0) {
-    for (int i = 0; i < ns; ++i) {
-      mbar_init(full + i, 1);
-      mbar_init(done + i, nwc);
-    }
-    mbar_init(pbar, 1);
-    *s_abort = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
   grid_dependents_launch();
-  if (tid == 0) COLI_TRACE_POINT(0, 0);
   grid_dependency_wait();
-  if (tid == 0) COLI_TRACE_POINT(0, 1);
-
+  COLI_TRACE_POINT(0, 1);
   float *s_logits = (float *)(smem + L.logits);
   int *s_idx = (int *)(smem + L.idx);
   float *s_gates = (float *)(smem + L.gates);
@@ -433,11 +438,13 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
   int *s_act_off = s_act + 1 + (E + S);
   int *s_routes = (int *)(smem + L.routes);
   float *s_slot_gate = (float *)(smem + L.slot_gate);
+  uint32_t *s_xpl = (uint32_t *)(smem + L.xpl);
+  float *red = (float *)(smem + L.red);
   const bool cta0 = blockIdx.x == 0;
+  const int G = gridDim.x, c = blockIdx.x;
 
-  // partials are staged in the (not yet used) weight ring
   route_block(a, s_logits, s_idx, s_gates, s_vals, s_rank, s_scratch,
-              a.gu_stage_partials ? (float *)(smem + L.ring) : nullptr, pbar, cta0);
+              a.gu_stage_partials ? (float *)(smem + L.stage) : nullptr, cta0);
   if (tid == 0) COLI_TRACE_POINT(0, 2);
   const int n_active = block_union(s_idx, s_gates, T, k, S, E, s_act, s_act_expert, s_act_off,
                                    s_routes, s_slot_gate, s_rank);
@@ -449,181 +456,137 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
       a.g_slot_gate[i] = s_slot_gate[i];
     }
   }
-
-  // this CTA's rows in the flattened (used expert, row) space, units of 4 rows
-  const int G = gridDim.x, c = blockIdx.x;
-  const int F4 = F / 4;
-  const int U = n_active * F4;
-  const int u0 = part_lo(c, U, G), u1 = part_lo(c + 1, U, G);
-  const int rs4 = a.gu_rs / 4;
   const int64_t rb = H / 2, ngr = H / kGroup;
-  const int stage_bytes = a.gu_rs * (H + H / 8);
-  float *red = (float *)(smem + L.red);
-  const int red_stride = a.gu_rs * T * a.gu_ncg * 2;
+  // L2 prefetch of the down rows that the same-index k_down CTA will read
+  if (warp == 0 && c < a.n_part) {
+    const int UH = H / 4;
+    const int dh0 = 4 * part_lo(c, UH, a.n_part), dh1 = 4 * part_lo(c + 1, UH, a.n_part);
+    for (int q = lane; q < n_active && dh1 > dh0; q += 32) {
+      const int e = s_act_expert[q];
+      prefetch_l2(a.packed + (int64_t)e * a.eb + (int64_t)F * H + (int64_t)dh0 * (F / 2),
+                  (uint32_t)((dh1 - dh0) * (F / 2)));
+      prefetch_l2(a.scales + (int64_t)e * a.es + (int64_t)2 * F * ngr + (int64_t)dh0 * (F / kGroup),
+                  (uint32_t)((dh1 - dh0) * (F / 16)));
+    }
+  }
+  // this CTA's rows in the flattened (used expert, row) space, units of 4 rows
+  const int U = n_active * (F / 4);
+  const int row0 = 4 * part_lo(c, U, G), nrows = 4 * part_lo(c + 1, U, G) - row0;
+  const float *xr = a.xrep + (size_t)(c % a.n_rep) * a.x_stride;
+  const int nbx = H / 32;
+  if (a.gu_xpl) build_planes(xr, T, H, s_xpl, nbx);
+  __syncthreads();
+  if (tid == 0) COLI_TRACE_POINT(0, 4);
 
-  if (warp == nwc) {
-    // ---------------- producer warp: issue copies, finalise h ----------------
-    fence_proxy_async();   // the ring held the staged partials
-    StageIter it(u0, u1, F4, rs4);
-    int s = 0, fin = 0, ai, r0, n;
-    bool ok = true, prefetched = false;
-    for (;;) {
-      const bool more = ok && it.next(ai, r0, n);
-      // finalise the oldest stage when its slot is needed again, or at the end
-      while (ok && fin < s && (!more || s - fin >= ns)) {
-        const int slot = fin % ns;
-        if (!mbar_wait(done + slot, (fin / ns) & 1)) { ok = false; break; }
-        const int fa = s_desc[slot], f0 = s_desc[16 + slot], fn = s_desc[32 + slot];
-        const int j0 = s_act_off[fa], ntok = s_act_off[fa + 1] - j0;
-        const float *rd = red + slot * red_stride;
-        for (int i = lane; i < fn * ntok; i += 32) {
-          const int r = i / ntok, j = i - r * ntok;
-          float g = 0.0f, u = 0.0f;
-          for (int cg = 0; cg < a.gu_ncg; ++cg) {
-            g += rd[((r * T + j) * a.gu_ncg + cg) * 2];
-            u += rd[((r * T + j) * a.gu_ncg + cg) * 2 + 1];
-          }
-          const int slot_id = s_routes[j0 + j];
-          const float hv = silu(g) * u * s_slot_gate[slot_id];
-          for (int rr = 0; rr < a.n_rep; ++rr)
-            a.h[rr * a.h_stride + (int64_t)slot_id * F + f0 + r] = hv;
-        }
-        __syncwarp();
-        ++fin;
-      }
-      if (!more) {
-        if (lane == 0) COLI_TRACE_POINT(0, 6);
-        break;
-      }
-      const int slot = s % ns;
-      if (lane == 0) {
-        s_desc[slot] = ai;
-        s_desc[16 + slot] = r0;
-        s_desc[32 + slot] = n;
-        const int e = s_act_expert[ai];
-        const uint8_t *pg = a.packed + (int64_t)e * a.eb + (int64_t)r0 * rb;
-        const uint8_t *pu = pg + (int64_t)F * rb;
-        const float *sg = a.scales + (int64_t)e * a.es + (int64_t)r0 * ngr;
-        const float *su = sg + (int64_t)F * ngr;
-        uint8_t *dst = smem + L.ring + (size_t)slot * stage_bytes;
-        const uint32_t nb = (uint32_t)(n * rb), sb = (uint32_t)(n * ngr * 4);
-        mbar_arrive_expect_tx(full + slot, 2 * nb + 2 * sb);
-        bulk_g2s(dst, pg, nb, full + slot);
-        bulk_g2s(dst + a.gu_rs * rb, pu, nb, full + slot);
-        bulk_g2s(dst + 2 * a.gu_rs * rb, sg, sb, full + slot);
-        bulk_g2s(dst + 2 * a.gu_rs * rb + a.gu_rs * ngr * 4, su, sb, full + slot);
-      }
-      __syncwarp();
-      ++s;
-      if (!prefetched && (s == ns || it.u >= it.u1)) {
-        prefetched = true;
-        if (lane == 0) COLI_TRACE_POINT(0, 4);
-        // L2 prefetch of the down rows the same-index k_down CTA will read
-        if (lane == 0 && c < a.n_part) {
-          const int UH = H / 4;
-          const int dh0 = 4 * part_lo(c, UH, a.n_part), dh1 = 4 * part_lo(c + 1, UH, a.n_part);
-          for (int q = 0; q < n_active && dh1 > dh0; ++q) {
-            const int e = s_act_expert[q];
-            prefetch_l2(a.packed + (int64_t)e * a.eb + (int64_t)F * H + (int64_t)dh0 * (F / 2),
-                        (uint32_t)((dh1 - dh0) * (F / 2)));
-            prefetch_l2(a.scales + (int64_t)e * a.es + (int64_t)2 * F * ngr +
-                            (int64_t)dh0 * (F / kGroup),
-                        (uint32_t)((dh1 - dh0) * (F / 16)));
-          }
-        }
-      }
-    }
-    if (!ok) {
-      if (lane == 0) set_flag(a.ctrl, COLI_FLAG_TIMEOUT);
-      *(volatile int *)s_abort = 1;
-      // drain copies still in flight before the CTA may exit
-      for (int st = fin; st < s; ++st) (void)mbar_wait(full + (st % ns), (st / ns) & 1);
-    }
-  } else if (warp < nwc) {
-    // ---------------- compute warps ----------------
-    const int cg = warp % a.gu_ncg, rg = warp / a.gu_ncg, nrg = a.gu_nrg;
+  const int ncg = a.gu_ncg, nrg = a.gu_nrg;
+  if (warp < ncg * nrg) {
+    const int cg = warp % ncg, rg = warp / ncg;
     const int col = cg * kChunkCols + 32 * lane;
     const bool act = col < H;
-    const float *x = a.xrep + (size_t)(c % a.n_rep) * a.x_stride;
+    const int nq = nrows > rg ? (nrows - rg + nrg - 1) / nrg : 0;
     Planes pl;
-    int cached = -1;
-    if (u1 > u0) {
-      // quantise the first stage's token now, while the first weights are in flight
-      const int t = s_routes[s_act_off[u0 / F4]] / KS;
-      float v[32];
-      if (act) load32<float>(x + (int64_t)t * H + col, v);
-      else {
+    int pl_tok = -1;
+    for (int q0 = 0; q0 < nq; q0 += kGuBatch) {
+      uint4 wg[kGuBatch], wu[kGuBatch];
+      float sg[kGuBatch], su[kGuBatch];
+      int ra[kGuBatch];   // used-expert index of each row (-1: none)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-      }
-      quantize32(v, pl);
-      cached = t;
-    }
-    StageIter it(u0, u1, F4, rs4);
-    int s = 0, ai, r0, n;
-    while (it.next(ai, r0, n)) {
-      const int slot = s % ns;
-      if (!mbar_wait(full + slot, (s / ns) & 1)) {
-        if (lane == 0) set_flag(a.ctrl, COLI_FLAG_TIMEOUT);
-        break;
-      }
-      if (*(volatile int *)s_abort) break;
-      if (warp == 0 && lane == 0) {
-        if (s == 0) COLI_TRACE_POINT(0, 5);
-        COLI_TRACE_STAGE(0, s);
-      }
-      const uint8_t *stg = smem + L.ring + (size_t)slot * stage_bytes;
-      const uint8_t *wg = stg, *wu = stg + a.gu_rs * rb;
-      const float *sgp = (const float *)(stg + 2 * a.gu_rs * rb);
-      const float *sup = sgp + a.gu_rs * ngr;
-      float *rd = red + slot * red_stride;
-      const int j0 = s_act_off[ai], ntok = s_act_off[ai + 1] - j0;
-      const int nrows = n > rg ? (n - rg + nrg - 1) / nrg : 0;
-      for (int j = 0; j < ntok; ++j) {
-        const int t = s_routes[j0 + j] / KS;
-        if (t != cached) {
-          float v[32];
-          if (act) load32<float>(x + (int64_t)t * H + col, v);
-          else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+      for (int b = 0; b < kGuBatch; ++b) {
+        ra[b] = -1;
+        const int q = q0 + b;
+        if (q < nq) {
+          const int gr = row0 + rg + q * nrg;
+          const int ai = gr / F, f = gr - ai * F;
+          ra[b] = ai;
+          if (act) {
+            const int e = s_act_expert[ai];
+            const uint8_t *pg = a.packed + (int64_t)e * a.eb + (int64_t)f * rb + col / 2;
+            const float *pgs = a.scales + (int64_t)e * a.es + (int64_t)f * ngr + col / kGroup;
+            wg[b] = ldg_stream(pg);
+            wu[b] = ldg_stream(pg + (int64_t)F * rb);
+            sg[b] = __ldg(pgs);
+            su[b] = __ldg(pgs + (int64_t)F * ngr);
           }
-          quantize32(v, pl);
-          cached = t;
         }
-        for (int q0 = 0; q0 < nrows; q0 += 4) {
+      }
+      if (q0 == 0 && tid == 0) COLI_TRACE_POINT(0, 5);
+#pragma unroll
+      for (int b0 = 0; b0 < kGuBatch; b0 += 4) {
+        int maxtok = 0;
+#pragma unroll
+        for (int b = b0; b < b0 + 4; ++b)
+          if (ra[b] >= 0) {
+            const int nt = s_act_off[ra[b] + 1] - s_act_off[ra[b]];
+            maxtok = nt > maxtok ? nt : maxtok;
+          }
+        for (int j = 0; j < maxtok; ++j) {
           float v[8];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            v[2 * q] = 0.0f;
-            v[2 * q + 1] = 0.0f;
-            const int r = rg + (q0 + q) * nrg;
-            if (q0 + q < nrows && act) {
-              const uint4 g4 = *(const uint4 *)(wg + r * rb + col / 2);
-              const uint4 u4 = *(const uint4 *)(wu + r * rb + col / 2);
-              v[2 * q] = sgp[r * ngr + col / kGroup] * dot32(g4, pl);
-              v[2 * q + 1] = sup[r * ngr + col / kGroup] * dot32(u4, pl);
+          for (int b = b0; b < b0 + 4; ++b) {
+            v[2 * (b - b0)] = 0.0f;
+            v[2 * (b - b0) + 1] = 0.0f;
+            if (ra[b] >= 0) {
+              const int j0 = s_act_off[ra[b]], nt = s_act_off[ra[b] + 1] - j0;
+              if (j < nt && act) {
+                const int t = s_routes[j0 + j] / KS;
+                if (t != pl_tok) {
+                  if (a.gu_xpl) {
+                    load_planes(s_xpl, t, col / 32, nbx, pl);
+                  } else {
+                    float xv[32];
+                    load32<float>(xr + (int64_t)t * H + col, xv);
+                    quantize32(xv, pl);
+                  }
+                  pl_tok = t;
+                }
+                v[2 * (b - b0)] = sg[b] * dot32(wg[b], pl);
+                v[2 * (b - b0) + 1] = su[b] * dot32(wu[b], pl);
+              }
             }
           }
           const float tot = reduce8(v);
           if ((lane & 3) == 0) {
-            const int vi = lane >> 2, q = vi >> 1;
-            if (q0 + q < nrows) {
-              const int r = rg + (q0 + q) * nrg;
-              rd[((r * T + j) * a.gu_ncg + cg) * 2 + (vi & 1)] = tot;
+            const int vi = lane >> 2, b = b0 + (vi >> 1);
+            if (ra[b] >= 0) {
+              const int nt = s_act_off[ra[b] + 1] - s_act_off[ra[b]];
+              if (j < nt) {
+                const int i = rg + (q0 + b) * nrg;
+                red[((i * T + j) * ncg + cg) * 2 + (vi & 1)] = tot;
+              }
             }
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(done + slot);
-      ++s;
     }
   }
+  __syncthreads();
+  if (tid == 0) COLI_TRACE_POINT(0, 6);
+  // finalise h for every (row, token) of this CTA
+  for (int it = tid; it < nrows * T; it += blockDim.x) {
+    const int i = it / T, j = it - i * T;
+    const int gr = row0 + i;
+    const int ai = gr / F, f = gr - ai * F;
+    const int j0 = s_act_off[ai], nt = s_act_off[ai + 1] - j0;
+    if (j >= nt) continue;
+    float g = 0.0f, u = 0.0f;
+    for (int cg = 0; cg < ncg; ++cg) {
+      g += red[((i * T + j) * ncg + cg) * 2];
+      u += red[((i * T + j) * ncg + cg) * 2 + 1];
+    }
+    const int slot_id = s_routes[j0 + j];
+    const float hv = silu(g) * u * s_slot_gate[slot_id];
+    for (int rr = 0; rr < a.n_rep; ++rr) a.h[rr * a.h_stride + (int64_t)slot_id * F + f] = hv;
+  }
+  if (tid == 0) COLI_TRACE_POINT(0, 7);
 }
 
 // ---------------------------------------------------------------------------
-// down + combine + residual + next layer's router partials
+// down + combine + residual + next layer's router partials.  Each CTA owns a
+// block of output rows; a warp owns one 1024-column chunk (cg) of its rows and
+// walks the used experts in ascending order (8 rows' loads in flight), adding
+// each slot's contribution into per-token registers.
+
+constexpr int kDnBatch = 8;
 
 template <typename WT>
 __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
@@ -631,25 +594,11 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
   const DnSmem &L = a.dn;
   const int T = a.T, H = a.H, F = a.F, E = a.E, S = a.S, k = a.k, KS = k + S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nwc = a.dn_ncg * a.dn_nrg;
   const int G = gridDim.x, c = blockIdx.x;
   const int UH = H / 4;
   const int dh0 = 4 * part_lo(c, UH, G), dh1 = 4 * part_lo(c + 1, UH, G);
   const int nr = dh1 - dh0;
-  const int ns = a.dn_ns;
-  uint64_t *full = (uint64_t *)(smem + L.bar);
-  uint64_t *done = full + ns;
-  int *s_abort = (int *)(done + ns);
-  int *s_desc = (int *)(smem + L.desc);
   WT *s_wr = (WT *)(smem + L.wr);
-  if (tid == 0) {
-    for (int i = 0; i < ns; ++i) {
-      mbar_init(full + i, 1);
-      mbar_init(done + i, nwc);
-    }
-    *s_abort = 0;
-    fence_mbar_init();
-  }
   // the next layer's router rows [dh0, dh1) do not depend on the previous kernel
   if (a.wr) {
     const WT *wr = (const WT *)a.wr;
@@ -658,153 +607,99 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
       s_wr[i] = wr[(size_t)e * H + dh0 + r];
     }
   }
-  __syncthreads();
   grid_dependents_launch();
-  if (tid == 0) COLI_TRACE_POINT(1, 0);
   grid_dependency_wait();
   if (tid == 0) COLI_TRACE_POINT(1, 1);
   int *s_act = (int *)(smem + L.act);
   int *s_act_expert = s_act + 1;
   int *s_act_off = s_act + 1 + (E + S);
   int *s_routes = (int *)(smem + L.routes);
-  float *s_acc = (float *)(smem + L.acc);   // [T][nr]
+  float *red = (float *)(smem + L.acc);   // [nr][T][ncg]
   uint32_t *s_planes = (uint32_t *)(smem + L.planes);
-  const int nbp = a.dn_nbp;
+  const int ncg = a.dn_ncg, nrg = a.dn_nrg;
   for (int i = tid; i < 1 + 2 * (E + S) + 1; i += blockDim.x) s_act[i] = __ldcg(a.g_act + i);
   for (int i = tid; i < T * KS; i += blockDim.x) s_routes[i] = __ldcg(a.g_routes + i);
-  for (int i = tid; i < T * nr; i += blockDim.x) s_acc[i] = 0.0f;
-  // the slots' h vectors, quantised once for the whole CTA
-  const float *h_rep = a.h + (size_t)(c % a.n_rep) * a.h_stride;
-  if (a.dn_planes) build_planes(h_rep, T * KS, F, s_planes, nbp);
+  for (int i = tid; i < nr * T * ncg; i += blockDim.x) red[i] = 0.0f;
   __syncthreads();
-  if (tid == 0) COLI_TRACE_POINT(1, 2);
   const int n_active = s_act[0];
-  const int rs4 = a.dn_rs / 4;
+  const float *h_rep = a.h + (size_t)(c % a.n_rep) * a.h_stride;
   const int64_t rb = F / 2, ngr = F / kGroup;
-  const int stage_bytes = a.dn_rs * (F / 2 + F / 16);
-  float *red = (float *)(smem + L.red);
-  const int red_stride = a.dn_rs * T * a.dn_ncg;
   const int64_t down_b = (int64_t)F * H, down_s = (int64_t)2 * F * (H / kGroup);
-  const int seg4 = nr / 4;
-  const int n_units = seg4 > 0 ? n_active * seg4 : 0;
-
-  if (warp == nwc) {
-    StageIter it(0, n_units, seg4 > 0 ? seg4 : 1, rs4);
-    int s = 0, fin = 0, ai, r0, n;
-    bool ok = true;
-    for (;;) {
-      const bool more = ok && it.next(ai, r0, n);
-      while (ok && fin < s && (!more || s - fin >= ns)) {
-        const int slot = fin % ns;
-        if (!mbar_wait(done + slot, (fin / ns) & 1)) { ok = false; break; }
-        const int fa = s_desc[slot], f0 = s_desc[16 + slot], fn = s_desc[32 + slot];
-        const int j0 = s_act_off[fa], ntok = s_act_off[fa + 1] - j0;
-        const float *rd = red + slot * red_stride;
-        for (int i = lane; i < fn * ntok; i += 32) {
-          const int r = i / ntok, j = i - r * ntok;
-          float v = 0.0f;
-          for (int cg = 0; cg < a.dn_ncg; ++cg) v += rd[(r * T + j) * a.dn_ncg + cg];
-          const int t = s_routes[j0 + j] / KS;
-          s_acc[t * nr + f0 + r] += v;   // experts finalised in ascending order
-        }
-        __syncwarp();
-        ++fin;
-      }
-      if (!more) break;
-      const int slot = s % ns;
-      if (lane == 0) {
-        s_desc[slot] = ai;
-        s_desc[16 + slot] = r0;
-        s_desc[32 + slot] = n;
-        const int e = s_act_expert[ai];
-        const uint8_t *pd = a.packed + (int64_t)e * a.eb + down_b + (int64_t)(dh0 + r0) * rb;
-        const float *sd = a.scales + (int64_t)e * a.es + down_s + (int64_t)(dh0 + r0) * ngr;
-        uint8_t *dst = smem + L.ring + (size_t)slot * stage_bytes;
-        const uint32_t nb = (uint32_t)(n * rb), sb = (uint32_t)(n * ngr * 4);
-        mbar_arrive_expect_tx(full + slot, nb + sb);
-        bulk_g2s(dst, pd, nb, full + slot);
-        bulk_g2s(dst + a.dn_rs * rb, sd, sb, full + slot);
-      }
-      __syncwarp();
-      ++s;
-    }
-    if (!ok) {
-      if (lane == 0) set_flag(a.ctrl, COLI_FLAG_TIMEOUT);
-      *(volatile int *)s_abort = 1;
-      for (int st = fin; st < s; ++st) (void)mbar_wait(full + (st % ns), (st / ns) & 1);
-    }
-  } else if (warp < nwc) {
-    const int cg = warp % a.dn_ncg, rg = warp / a.dn_ncg, nrg = a.dn_nrg;
-    const int col = cg * kChunkCols + 32 * lane;
-    const bool act = col < F;
-    StageIter it(0, n_units, seg4 > 0 ? seg4 : 1, rs4);
-    int s = 0, ai, r0, n;
-    while (it.next(ai, r0, n)) {
-      const int slot = s % ns;
-      if (!mbar_wait(full + slot, (s / ns) & 1)) {
-        if (lane == 0) set_flag(a.ctrl, COLI_FLAG_TIMEOUT);
-        break;
-      }
-      if (*(volatile int *)s_abort) break;
-      if (warp == 0 && lane == 0) {
-        if (s == 0) COLI_TRACE_POINT(1, 3);
-        COLI_TRACE_STAGE(1, s);
-      }
-      const uint8_t *stg = smem + L.ring + (size_t)slot * stage_bytes;
-      const float *sdp = (const float *)(stg + a.dn_rs * rb);
-      float *rd = red + slot * red_stride;
-      const int j0 = s_act_off[ai], ntok = s_act_off[ai + 1] - j0;
-      const int nrows = n > rg ? (n - rg + nrg - 1) / nrg : 0;
-      for (int j = 0; j < ntok; ++j) {
-        const int slot_id = s_routes[j0 + j];
-        Planes pl;
-        if (a.dn_planes) {
-          if (act) load_planes(s_planes, slot_id, col / 32, nbp, pl);
-          else { pl = Planes{}; }
-        } else {
-          float v[32];
-          if (act) load32<float>(h_rep + (int64_t)slot_id * F + col, v);
-          else {
+  const int nbp = F / 32;
+  const int cap = a.dn_slots;     // slots whose planes fit in shared memory at once
+  const int cg = warp % ncg, rg = warp / ncg;
+  const int col = cg * kChunkCols + 32 * lane;
+  const bool act = col < F;
+  const bool worker = warp < ncg * nrg;
+  // experts in groups whose slots' planes fit; groups run in ascending order
+  for (int ga = 0; ga < n_active;) {
+    int gb = ga;
+    while (gb < n_active && s_act_off[gb + 1] - s_act_off[ga] <= cap) ++gb;
+    if (gb == ga) gb = ga + 1;   // cap >= T, so a single expert always fits
+    const int p0 = s_act_off[ga], np = s_act_off[gb] - p0;
+    build_planes_list(h_rep, F, s_routes + p0, np, s_planes, nbp);
+    __syncthreads();
+    if (ga == 0 && tid == 0) COLI_TRACE_POINT(1, 2);
+    if (worker) {
+      for (int r = rg; r < nr; r += nrg) {
+        float acc[kDecodeMaxT];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+        for (int t = 0; t < kDecodeMaxT; ++t) acc[t] = 0.0f;
+        for (int a0 = ga; a0 < gb; a0 += kDnBatch) {
+          uint4 w[kDnBatch];
+          float sc[kDnBatch];
+#pragma unroll
+          for (int b = 0; b < kDnBatch; ++b)
+            if (a0 + b < gb && act) {
+              const int e = s_act_expert[a0 + b];
+              w[b] = ldg_stream(a.packed + (int64_t)e * a.eb + down_b + (int64_t)(dh0 + r) * rb +
+                                col / 2);
+              sc[b] = __ldg(a.scales + (int64_t)e * a.es + down_s + (int64_t)(dh0 + r) * ngr +
+                            col / kGroup);
+            }
+#pragma unroll
+          for (int b = 0; b < kDnBatch; ++b) {
+            if (a0 + b >= gb) break;
+            if (!act) continue;
+            const int j0 = s_act_off[a0 + b], nt = s_act_off[a0 + b + 1] - j0;
+            for (int j = 0; j < nt; ++j) {
+              Planes pl;
+              load_planes(s_planes, j0 + j - p0, col / 32, nbp, pl);
+              const float v = sc[b] * dot32(w[b], pl);
+              const int t = s_routes[j0 + j] / KS;
+#pragma unroll
+              for (int tt = 0; tt < kDecodeMaxT; ++tt)
+                if (tt == t) acc[tt] += v;
+            }
           }
-          quantize32(v, pl);
         }
-        for (int q0 = 0; q0 < nrows; q0 += 8) {
+        // reduce over lanes, 8 tokens at a time; the owning lane accumulates
+        for (int t0 = 0; t0 < T; t0 += 8) {
           float v[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             v[q] = 0.0f;
-            const int r = rg + (q0 + q) * nrg;
-            if (q0 + q < nrows && act) {
-              const uint4 w4 = *(const uint4 *)(stg + r * rb + col / 2);
-              v[q] = sdp[r * ngr + col / kGroup] * dot32(w4, pl);
-            }
+#pragma unroll
+            for (int tt = 0; tt < kDecodeMaxT; ++tt)
+              if (tt == t0 + q) v[q] = acc[tt];
           }
           const float tot = reduce8(v);
-          if ((lane & 3) == 0) {
-            const int q = lane >> 2;
-            if (q0 + q < nrows) {
-              const int r = rg + (q0 + q) * nrg;
-              rd[(r * T + j) * a.dn_ncg + cg] = tot;
-            }
-          }
+          const int t = t0 + (lane >> 2);
+          if ((lane & 3) == 0 && t < T) red[(r * T + t) * ncg + cg] += tot;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(done + slot);
-      ++s;
     }
+    __syncthreads();
+    ga = gb;
   }
   if (tid == 0) COLI_TRACE_POINT(1, 4);
-  __syncthreads();
-  if (tid == 0) COLI_TRACE_POINT(1, 5);
   // combine is complete: residual, outputs, next layer's partial logits
   float *s_xn = (float *)(smem + L.xn);   // [T][nr]
   for (int i = tid; i < T * nr; i += blockDim.x) {
     const int t = i / nr, r = i - t * nr;
     const int64_t o = (int64_t)t * H + dh0 + r;
-    const float v = s_acc[i];
+    float v = 0.0f;
+    for (int q = 0; q < ncg; ++q) v += red[(r * T + t) * ncg + q];
     if (a.layer_out) a.layer_out[o] = v;
     const float xn = a.residual ? a.residual[o] + v : v;
     a.out[o] = xn;
@@ -822,19 +717,17 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
         a.partials[rr * a.part_stride + (size_t)c * T * E + o] = sum;
     }
   }
-#ifdef COLI_TRACE
-  __syncthreads();
   if (tid == 0) COLI_TRACE_POINT(1, 6);
-#endif
 }
 
 // ---------------------------------------------------------------------------
 // host side
 
 #ifdef COLI_TRACE
-extern "C" int coli_trace_read(void *points, void *stages) {
+extern "C" int coli_trace_read(void *points, void *stages, void *issues) {
   if (cudaMemcpyFromSymbol(points, g_trace, sizeof(g_trace)) != cudaSuccess) return -1;
   if (cudaMemcpyFromSymbol(stages, g_trace_stage, sizeof(g_trace_stage)) != cudaSuccess) return -1;
+  if (cudaMemcpyFromSymbol(issues, g_trace_issue, sizeof(g_trace_issue)) != cudaSuccess) return -1;
   return 0;
 }
 #endif
@@ -881,14 +774,16 @@ cudaError_t allow_smem(K kernel, size_t bytes) {
 // Geometry and shared-memory plans of both kernels for one layer shape.
 cudaError_t plan_decode(Dec2Args &a, int n_part) {
   const int T = a.T, H = a.H, F = a.F, E = a.E, S = a.S, k = a.k, KS = k + S;
-  const size_t budget = (size_t)max_smem() - 2048;
+  const size_t budget = (size_t)max_smem() - 4096;
+  const int G = num_sms();
   a.n_part = n_part;
   // ---- gate/up
   a.gu_ncg = (H + kChunkCols - 1) / kChunkCols;
-  a.gu_nrg = 12 / a.gu_ncg;
+  a.gu_nrg = 16 / a.gu_ncg;
   if (a.gu_nrg < 1) a.gu_nrg = 1;
-  if (a.gu_ncg * a.gu_nrg > kDec2MaxThreads / 32 - 1) a.gu_nrg = (kDec2MaxThreads / 32 - 1) / a.gu_ncg;
-  if (a.gu_nrg < 1) return cudaErrorInvalidValue;
+  if (a.gu_ncg * a.gu_nrg > kDec2MaxThreads / 32) return cudaErrorInvalidValue;
+  const int n_used = ((E < T * k) ? E : T * k) + S;
+  const int max_rows = 4 * ((n_used * (F / 4) + G - 1) / G);
   GuSmem g{};
   size_t o = 0;
   g.logits = o; o = al16(o + (size_t)T * E * 4);
@@ -900,70 +795,38 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
   g.act = o; o = al16(o + (size_t)(2 + 2 * (E + S)) * 4);
   g.routes = o; o = al16(o + (size_t)T * KS * 4);
   g.slot_gate = o; o = al16(o + (size_t)T * KS * 4);
-  g.desc = o; o = al16(o + 48 * 4);
-  const size_t fixed = o;
-  const size_t row_bytes = (size_t)H + H / 8;   // gate + up nibbles and scales per row pair
-  int rs = (int)(40960 / row_bytes) / 4 * 4;
-  if (rs < 4) rs = 4;
-  if (rs > 32) rs = 32;
-  const size_t red_row = (size_t)T * a.gu_ncg * 2 * 4;
-  int ns = 0;
-  for (ns = 16; ns >= 2; --ns) {
-    const size_t need = al128(fixed) + ns * rs * row_bytes + ns * rs * red_row + ns * 16 + 64;
-    if (need <= budget) break;
-  }
-  if (ns < 2) return cudaErrorInvalidValue;
-  a.gu_rs = rs;
-  a.gu_ns = ns;
-  o = al128(fixed);
-  g.ring = o; o += (size_t)ns * rs * row_bytes;
-  g.red = o; o = al16(o + (size_t)ns * rs * red_row);
-  g.bar = o; o += (size_t)(2 * ns + 1) * 8 + 16;
-  g.total = al16(o);
+  g.red = o; o = al16(o + (size_t)max_rows * T * a.gu_ncg * 2 * 4);
+  if (o > budget) return cudaErrorInvalidValue;
+  const size_t xpl_bytes = (size_t)T * 18 * (H / 32) * 4;
+  a.gu_xpl = o + al16(xpl_bytes) <= budget;
+  g.xpl = o; o = al16(o + (a.gu_xpl ? xpl_bytes : 0));
+  const size_t stage_bytes = (size_t)n_part * T * E * 4;
+  a.gu_stage_partials = o + al16(stage_bytes) <= budget;
+  g.stage = o; o = al16(o + (a.gu_stage_partials ? stage_bytes : 0));
+  g.total = o;
   a.gu = g;
-  a.gu_stage_partials = (size_t)n_part * T * E * 4 <= (size_t)ns * rs * row_bytes;
   // ---- down
   a.dn_ncg = (F + kChunkCols - 1) / kChunkCols;
-  a.dn_nrg = 12 / a.dn_ncg;
+  a.dn_nrg = 16 / a.dn_ncg;
   if (a.dn_nrg < 1) a.dn_nrg = 1;
-  if (a.dn_ncg * a.dn_nrg > kDec2MaxThreads / 32 - 1) a.dn_nrg = (kDec2MaxThreads / 32 - 1) / a.dn_ncg;
-  if (a.dn_nrg < 1) return cudaErrorInvalidValue;
+  if (a.dn_ncg * a.dn_nrg > kDec2MaxThreads / 32) return cudaErrorInvalidValue;
   const int UH = H / 4;
   const int max_nr = 4 * ((UH + n_part - 1) / n_part);
-  a.dn_nbp = F / 32;
-  const size_t planes_bytes = (size_t)T * KS * 18 * a.dn_nbp * 4;
-  a.dn_planes = planes_bytes <= 98304;
   DnSmem d{};
   o = 0;
   d.act = o; o = al16(o + (size_t)(2 + 2 * (E + S)) * 4);
   d.routes = o; o = al16(o + (size_t)T * KS * 4);
-  d.acc = o; o = al16(o + (size_t)T * max_nr * 4);
+  d.acc = o; o = al16(o + (size_t)max_nr * T * a.dn_ncg * 4);
   d.xn = o; o = al16(o + (size_t)T * max_nr * 4);
   d.wr = o; o = al16(o + (size_t)E * max_nr * 4);
-  d.desc = o; o = al16(o + 48 * 4);
-  d.planes = o; o = al16(o + (a.dn_planes ? planes_bytes : 0));
-  const size_t fixed_d = o;
-  const size_t drow = (size_t)F / 2 + F / 16;
-  int rsd = max_nr;
-  while ((size_t)rsd * drow > 65536 && rsd > 4) rsd -= 4;
-  const size_t red_drow = (size_t)T * a.dn_ncg * 4;
-  int nsd = 0;
-  for (nsd = 16; nsd >= 2; --nsd) {
-    const size_t need = al128(fixed_d) + nsd * rsd * drow + nsd * rsd * red_drow + nsd * 16 + 96;
-    if (need <= budget) break;
-  }
-  if (nsd < 2) return cudaErrorInvalidValue;
-  // no more stages than the CTA can use
-  const int n_used = ((E < T * k) ? E : T * k) + S;
-  const int stages_needed = n_used * ((max_nr / 4 + rsd / 4 - 1) / (rsd / 4));
-  if (nsd > stages_needed && stages_needed >= 2) nsd = stages_needed;
-  a.dn_rs = rsd;
-  a.dn_ns = nsd;
-  o = al128(fixed_d);
-  d.ring = o; o += (size_t)nsd * rsd * drow;
-  d.red = o; o = al16(o + (size_t)nsd * rsd * red_drow);
-  d.bar = o; o += (size_t)nsd * 16 + 32;
-  d.total = al16(o);
+  const size_t per_slot = (size_t)18 * (F / 32) * 4;
+  size_t room = budget > o ? budget - o : 0;
+  int slots = (int)(room / per_slot);
+  if (slots > T * KS) slots = T * KS;
+  if (slots < T) return cudaErrorInvalidValue;   // one expert's tokens must fit
+  a.dn_slots = slots;
+  d.planes = o; o = al16(o + (size_t)slots * per_slot);
+  d.total = o;
   a.dn = d;
   return cudaSuccess;
 }
@@ -980,22 +843,22 @@ cudaError_t launch_topk(const Dec2Args &a_in, cudaStream_t s, bool pdl) {
   Dec2Args a = a_in;
   const size_t rest = (size_t)(2 * a.T * a.E + 3 * a.T * a.k + 256) * 4;
   const size_t stage = (size_t)a.n_part * a.T * a.E * 4;
-  a.gu_stage_partials = 128 + stage + rest <= (size_t)max_smem() - 2048;
-  const size_t smem = 128 + (a.gu_stage_partials ? stage : 0) + rest;
+  a.gu_stage_partials = stage + rest <= (size_t)max_smem() - 2048;
+  const size_t smem = (a.gu_stage_partials ? stage : 0) + rest;
   cudaError_t e = allow_smem(k_topk, smem);
   if (e != cudaSuccess) return e;
   return launch(k_topk, 1, 256, smem, s, pdl, a);
 }
 
 cudaError_t launch_gateup(const Dec2Args &a, int grid, cudaStream_t s, bool pdl) {
-  const int threads = (a.gu_ncg * a.gu_nrg + 1) * 32;
+  const int threads = a.gu_ncg * a.gu_nrg * 32;
   cudaError_t e = allow_smem(k_gateup, a.gu.total);
   if (e != cudaSuccess) return e;
   return launch(k_gateup, grid, threads, a.gu.total, s, pdl, a);
 }
 
 cudaError_t launch_down(const Dec2Args &a, int wr_bf16, cudaStream_t s, bool pdl) {
-  const int threads = (a.dn_ncg * a.dn_nrg + 1) * 32;
+  const int threads = a.dn_ncg * a.dn_nrg * 32;
   cudaError_t e;
   if (wr_bf16) {
     if ((e = allow_smem(k_down<__nv_bfloat16>, a.dn.total)) != cudaSuccess) return e;
