@@ -18,11 +18,10 @@ WsLayout ws_layout(int T, int H, int F, int E, int S, int k) {
   L.n_part = num_sms() < H / 4 ? num_sms() : H / 4;
   // replica strides: whole 256-byte units plus one, so replicas start at
   // different offsets modulo any power of two
-  L.part_stride = (align256((size_t)L.n_part * T * E * 4) + 256) / 4;
   L.h_stride = (align256((size_t)T * KS * F * 4) + 256) / 4;
   L.x_stride = (align256((size_t)T * H * 4) + 256) / 4;
   L.ctrl = o;      o = align256(o + kCtrlWords * sizeof(uint32_t));
-  L.partials = o;  o = align256(o + kReplicas * L.part_stride * 4);
+  L.partials = o;  o = align256(o + (size_t)L.n_part * T * E * 4);
   L.idx = o;       o = align256(o + (size_t)T * k * sizeof(int32_t));
   L.gates = o;     o = align256(o + (size_t)T * k * sizeof(float));
   L.act = o;       o = align256(o + (size_t)(2 * (E + S) + 2) * sizeof(int32_t));
@@ -89,7 +88,6 @@ Dec2Args make_args(const coli_moe_desc *d, int k, int tn, uint8_t *ws, const WsL
   a.n_part = L.n_part;
   a.n_rep = kReplicas;
   a.partials = (float *)(ws + L.partials);
-  a.part_stride = L.part_stride;
   a.h_stride = L.h_stride;
   a.xrep = (float *)(ws + L.xrep);
   a.x_stride = L.x_stride;
@@ -167,12 +165,13 @@ int coli_router_topk(const coli_moe_desc *d, int top_k, const void *x, const voi
     Dec2Args a = make_args(d, k, tn, ws, L);
     a.x = (const char *)x + (size_t)t0 * H * xsize(d->x_dtype);
     a.wr = router_w;
-    a.counts = route_counts;
+    a.route_counts = route_counts;
     a.idx_out = idx + (size_t)t0 * k;
     a.gates_out = gates + (size_t)t0 * k;
+    a.build_union = 0;
+    a.xrep = nullptr;
     cudaError_t e = launch_route_partials(a, d->x_dtype == COLI_BF16,
                                           d->router_dtype == COLI_BF16, stream, true);
-    if (e == cudaSuccess) e = launch_topk(a, stream, true);
     if (e != cudaSuccess) return COLI_ECUDA;
   }
   return COLI_OK;
@@ -195,22 +194,25 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
   if (plan_decode(a, L.n_part) != cudaSuccess) return COLI_EUNSUPPORTED;
   const int wr_bf16 = d->router_dtype == COLI_BF16;
   cudaError_t e = cudaSuccess;
+  a.build_union = 1;
   for (int l = 0; l < n_layers && e == cudaSuccess; ++l) {
     const void *xin = (l == 0) ? x : (const void *)out;
-    const int x_bf16 = (l == 0) ? (x_dtype == COLI_BF16) : 0;
     a.x = xin;
     a.packed = packed + l * pk_stride;
     a.scales = scales + l * sc_stride;
-    a.counts = route_counts ? route_counts + (size_t)l * E : nullptr;
     if (l == 0) {
+      // router partials of layer 0; the last CTA routes it
       a.wr = router_w;
-      e = launch_route_partials(a, x_bf16, wr_bf16, stream, true);
+      a.route_counts = route_counts;
+      e = launch_route_partials(a, x_dtype == COLI_BF16, wr_bf16, stream, true);
       if (e != cudaSuccess) break;
     }
     e = launch_gateup(a, num_sms(), stream, true);
     if (e != cudaSuccess) break;
-    a.wr = (l + 1 < n_layers) ? (const void *)((const char *)router_w + (l + 1) * wr_stride)
-                              : nullptr;
+    // down also forms the next layer's router partials and routes it
+    const bool next = l + 1 < n_layers;
+    a.wr = next ? (const void *)((const char *)router_w + (l + 1) * wr_stride) : nullptr;
+    a.next_counts = (next && route_counts) ? route_counts + (size_t)(l + 1) * E : nullptr;
     a.residual = residual ? (const float *)xin : nullptr;
     a.out = out;
     a.layer_out = layer_out ? layer_out + (size_t)l * T_H : nullptr;

@@ -48,7 +48,7 @@ constexpr int kDec2MaxThreads = 512;
 
 // Shared-memory plan of k_gateup (byte offsets into dynamic smem).
 struct GuSmem {
-  size_t logits, idx, gates, vals, rank, scratch, act, routes, slot_gate, red, xpl, stage, total;
+  size_t act, routes, slot_gate, red, xpl, total;
 };
 // Shared-memory plan of k_down.
 struct DnSmem {
@@ -64,8 +64,7 @@ struct Dec2Args {
   const uint8_t *packed;    // this layer's expert records
   const float *scales;
   int64_t eb, es;           // packed bytes / scales per expert
-  float *partials;          // [n_rep][n_part][T][E]: replica r at partials + r * part_stride
-  size_t part_stride;
+  float *partials;          // [n_part][T][E] router partial logits
   int n_part;
   int n_rep;                // replicas of the buffers every CTA reads
   float *xrep;              // [n_rep][T][H] f32 layer input (or null)
@@ -77,12 +76,15 @@ struct Dec2Args {
   float *g_slot_gate;
   float *h;                 // [n_rep][T*(k+S)][F]
   uint32_t *ctrl;
-  uint32_t *counts;         // route counts [E] (or null)
+  uint32_t *route_counts;   // route counts [E] of the layer this kernel routes (or null)
+  uint32_t *next_counts;    // k_down: route counts of the next layer (or null)
   float *out;               // k_down output [T][H]
   float *layer_out;         // or null
   int32_t *idx_out;         // k_topk user outputs (or null)
   float *gates_out;
-  int gu_ncg, gu_nrg, gu_stage_partials, gu_xpl;
+  int build_union;          // k_topk also builds and publishes the union lists
+  int stage_partials;       // routing stages the partials in shared memory
+  int gu_ncg, gu_nrg, gu_xpl;
   int dn_ncg, dn_nrg, dn_slots;
   GuSmem gu;
   DnSmem dn;
@@ -91,7 +93,6 @@ struct Dec2Args {
 cudaError_t plan_decode(Dec2Args &a, int n_part);
 cudaError_t launch_route_partials(const Dec2Args &a, int x_bf16, int w_bf16, cudaStream_t s,
                                   bool pdl);
-cudaError_t launch_topk(const Dec2Args &a, cudaStream_t s, bool pdl);
 cudaError_t launch_gateup(const Dec2Args &a, int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_down(const Dec2Args &a, int wr_bf16, cudaStream_t s, bool pdl);
 

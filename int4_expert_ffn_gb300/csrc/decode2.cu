@@ -25,6 +25,9 @@
 // nibbles by dp4a; the exact integer sum sum_i (u_i - 8) xq_i is scaled by the
 // group scale and the activation scale.  Activation rounding is at most
 // max|x| / 32638 per element; all accumulation is exact or f32.
+#include <mutex>
+#include <unordered_map>
+
 #include "coli_internal.cuh"
 #include "ptx.cuh"
 #include "topk.cuh"
@@ -281,7 +284,7 @@ __device__ __forceinline__ void set_flag(uint32_t *ctrl, uint32_t f) {
 // router row against x:  partials[c][t][e] = sum_{h in [h0,h1)} Wr[e][h] x[t][h].
 
 template <typename XT, typename WT>
-__global__ void __launch_bounds__(256) k_route(Dec2Args a) {
+__global__ void __launch_bounds__(kDec2MaxThreads) k_route(Dec2Args a) {
   grid_dependents_launch();
   grid_dependency_wait();
   const int c = blockIdx.x, G = gridDim.x;
@@ -294,8 +297,7 @@ __global__ void __launch_bounds__(256) k_route(Dec2Args a) {
     float s = 0.0f;
     for (int h = h0; h < h1; ++h)
       s = fmaf(to_f32(wr[(size_t)e * a.H + h]), to_f32(x[(size_t)t * a.H + h]), s);
-    for (int r = 0; r < a.n_rep; ++r)
-      a.partials[r * a.part_stride + (size_t)c * a.T * a.E + o] = s;
+    a.partials[(size_t)c * a.T * a.E + o] = s;
   }
   // the layer input, widened to f32, in every replica (read by all gate/up CTAs)
   if (a.xrep) {
@@ -306,6 +308,8 @@ __global__ void __launch_bounds__(256) k_route(Dec2Args a) {
       for (int r = 0; r < a.n_rep; ++r) a.xrep[r * a.x_stride + (size_t)t * a.H + h] = v;
     }
   }
+  extern __shared__ __align__(128) uint8_t smem_route[];
+  route_if_last(a, smem_route);
 }
 
 // ---------------------------------------------------------------------------
@@ -321,7 +325,7 @@ __device__ void route_block(const Dec2Args &a, float *s_logits, int *s_idx, floa
   const int T = a.T, E = a.E, k = a.k;
   const int TE = T * E;
   const int nthr = blockDim.x;
-  const float *src = a.partials + (size_t)(blockIdx.x % a.n_rep) * a.part_stride;
+  const float *src = a.partials;
   if (s_stage) {
     // all threads copy the partials into shared memory, every load in flight at once
     const int n4 = (a.n_part * TE) / 4, tail = (a.n_part * TE) & 3;
@@ -384,30 +388,60 @@ __device__ void route_block(const Dec2Args &a, float *s_logits, int *s_idx, floa
     for (int i = threadIdx.x; i < T * k; i += nthr) {
       a.g_idx[i] = s_idx[i];
       a.g_gates[i] = s_gates[i];
-      if (a.counts) atomicAdd(a.counts + s_idx[i], 1u);
+      if (a.route_counts) atomicAdd(a.route_counts + s_idx[i], 1u);
     }
   }
 }
 
-__global__ void __launch_bounds__(256) k_topk(Dec2Args a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  grid_dependents_launch();
-  grid_dependency_wait();
-  const int T = a.T, E = a.E, k = a.k;
+// Routing of one layer from its router partials, run by the last CTA of the
+// kernel that produced them: logits (fixed summation order), top-k, gates,
+// route counts, and the union lists the expert kernels read.  `smem` holds
+// at least route_smem_bytes(a) bytes.
+__device__ void route_finish(const Dec2Args &a, uint8_t *smem) {
+  const int T = a.T, E = a.E, k = a.k, S = a.S, KS = k + S;
   float *s_stage = (float *)smem;
-  float *s_logits = s_stage + (a.gu_stage_partials ? (size_t)a.n_part * T * E : 0);
+  float *s_logits = s_stage + (a.stage_partials ? (size_t)a.n_part * T * E : 0);
   int *s_rank = (int *)(s_logits + T * E);
   int *s_idx = s_rank + T * E;
   float *s_gates = (float *)(s_idx + T * k);
   float *s_vals = s_gates + T * k;
   float *s_scratch = s_vals + T * k;
   route_block(a, s_logits, s_idx, s_gates, s_vals, s_rank, s_scratch,
-              a.gu_stage_partials ? s_stage : nullptr, true);
+              a.stage_partials ? s_stage : nullptr, true);
   __syncthreads();
   for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
     if (a.idx_out) a.idx_out[i] = s_idx[i];
     if (a.gates_out) a.gates_out[i] = s_gates[i];
   }
+  if (a.build_union) {
+    int *s_act = (int *)(s_scratch + kDec2MaxThreads);
+    int *s_routes = s_act + 2 + 2 * (E + S);
+    float *s_slot_gate = (float *)(s_routes + T * KS);
+    block_union(s_idx, s_gates, T, k, S, E, s_act, s_act + 1, s_act + 1 + (E + S), s_routes,
+                s_slot_gate, s_rank);
+    for (int i = threadIdx.x; i < 2 + 2 * (E + S); i += blockDim.x) a.g_act[i] = s_act[i];
+    for (int i = threadIdx.x; i < T * KS; i += blockDim.x) {
+      a.g_routes[i] = s_routes[i];
+      a.g_slot_gate[i] = s_slot_gate[i];
+    }
+  }
+}
+
+// Every CTA has written its partials: the last one to arrive (atomic ticket)
+// routes the layer and resets the ticket for the next use.
+__device__ void route_if_last(const Dec2Args &a, uint8_t *smem) {
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned t = atomicAdd(a.ctrl + kCtrlRouterTicket, 1u);
+    s_last = (t == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  route_finish(a, smem);
+  if (threadIdx.x == 0) a.ctrl[kCtrlRouterTicket] = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -427,12 +461,6 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
   grid_dependents_launch();
   grid_dependency_wait();
   COLI_TRACE_POINT(0, 1);
-  float *s_logits = (float *)(smem + L.logits);
-  int *s_idx = (int *)(smem + L.idx);
-  float *s_gates = (float *)(smem + L.gates);
-  float *s_vals = (float *)(smem + L.vals);
-  int *s_rank = (int *)(smem + L.rank);
-  float *s_scratch = (float *)(smem + L.scratch);
   int *s_act = (int *)(smem + L.act);          // [0] n_active, act_expert, act_off
   int *s_act_expert = s_act + 1;
   int *s_act_off = s_act + 1 + (E + S);
@@ -440,22 +468,17 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
   float *s_slot_gate = (float *)(smem + L.slot_gate);
   uint32_t *s_xpl = (uint32_t *)(smem + L.xpl);
   float *red = (float *)(smem + L.red);
-  const bool cta0 = blockIdx.x == 0;
   const int G = gridDim.x, c = blockIdx.x;
 
-  route_block(a, s_logits, s_idx, s_gates, s_vals, s_rank, s_scratch,
-              a.gu_stage_partials ? (float *)(smem + L.stage) : nullptr, cta0);
-  if (tid == 0) COLI_TRACE_POINT(0, 2);
-  const int n_active = block_union(s_idx, s_gates, T, k, S, E, s_act, s_act_expert, s_act_off,
-                                   s_routes, s_slot_gate, s_rank);
-  if (tid == 0) COLI_TRACE_POINT(0, 3);
-  if (cta0) {
-    for (int i = tid; i < 1 + 2 * (E + S) + 1; i += blockDim.x) a.g_act[i] = s_act[i];
-    for (int i = tid; i < T * KS; i += blockDim.x) {
-      a.g_routes[i] = s_routes[i];
-      a.g_slot_gate[i] = s_slot_gate[i];
-    }
+  // routing was done by the routing kernel: read its union lists
+  for (int i = tid; i < 2 + 2 * (E + S); i += blockDim.x) s_act[i] = __ldcg(a.g_act + i);
+  for (int i = tid; i < T * KS; i += blockDim.x) {
+    s_routes[i] = __ldcg(a.g_routes + i);
+    s_slot_gate[i] = __ldcg(a.g_slot_gate + i);
   }
+  __syncthreads();
+  const int n_active = s_act[0];
+  if (tid == 0) COLI_TRACE_POINT(0, 3);
   const int64_t rb = H / 2, ngr = H / kGroup;
   // L2 prefetch of the down rows that the same-index k_down CTA will read
   if (warp == 0 && c < a.n_part) {
@@ -713,9 +736,12 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
       const int t = o / E, e = o - t * E;
       float sum = 0.0f;
       for (int r = 0; r < nr; ++r) sum = fmaf(to_f32(s_wr[e * nr + r]), s_xn[t * nr + r], sum);
-      for (int rr = 0; rr < a.n_rep; ++rr)
-        a.partials[rr * a.part_stride + (size_t)c * T * E + o] = sum;
+      a.partials[(size_t)c * T * E + o] = sum;
     }
+    // the last CTA routes the next layer (its shared memory is free again)
+    Dec2Args r = a;
+    r.route_counts = a.next_counts;
+    route_if_last(r, smem);
   }
   if (tid == 0) COLI_TRACE_POINT(1, 6);
 }
@@ -764,9 +790,21 @@ int max_smem() {
   return v;
 }
 
+// Raise a kernel's dynamic shared-memory limit once per device (the limit is
+// only ever raised, so later smaller launches need no call).
 template <typename K>
 cudaError_t allow_smem(K kernel, size_t bytes) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  static std::mutex mu;
+  static std::unordered_map<const void *, size_t> done[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  size_t &cur = done[dev][(const void *)kernel];
+  if (bytes <= cur) return cudaSuccess;
+  cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) cur = bytes;
+  return e;
 }
 
 }  // namespace
@@ -786,12 +824,6 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
   const int max_rows = 4 * ((n_used * (F / 4) + G - 1) / G);
   GuSmem g{};
   size_t o = 0;
-  g.logits = o; o = al16(o + (size_t)T * E * 4);
-  g.idx = o; o = al16(o + (size_t)T * k * 4);
-  g.gates = o; o = al16(o + (size_t)T * k * 4);
-  g.vals = o; o = al16(o + (size_t)T * k * 4);
-  g.rank = o; o = al16(o + (size_t)(T * E > T * k ? T * E : T * k) * 4);
-  g.scratch = o; o = al16(o + (size_t)kDec2MaxThreads * 4);
   g.act = o; o = al16(o + (size_t)(2 + 2 * (E + S)) * 4);
   g.routes = o; o = al16(o + (size_t)T * KS * 4);
   g.slot_gate = o; o = al16(o + (size_t)T * KS * 4);
@@ -800,9 +832,6 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
   const size_t xpl_bytes = (size_t)T * 18 * (H / 32) * 4;
   a.gu_xpl = o + al16(xpl_bytes) <= budget;
   g.xpl = o; o = al16(o + (a.gu_xpl ? xpl_bytes : 0));
-  const size_t stage_bytes = (size_t)n_part * T * E * 4;
-  a.gu_stage_partials = o + al16(stage_bytes) <= budget;
-  g.stage = o; o = al16(o + (a.gu_stage_partials ? stage_bytes : 0));
   g.total = o;
   a.gu = g;
   // ---- down
@@ -831,23 +860,31 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
   return cudaSuccess;
 }
 
-cudaError_t launch_route_partials(const Dec2Args &a, int x_bf16, int w_bf16, cudaStream_t s,
-                                  bool pdl) {
-  if (!x_bf16 && !w_bf16) return launch(k_route<float, float>, a.n_part, 256, 0, s, pdl, a);
-  if (!x_bf16 && w_bf16) return launch(k_route<float, __nv_bfloat16>, a.n_part, 256, 0, s, pdl, a);
-  if (x_bf16 && !w_bf16) return launch(k_route<__nv_bfloat16, float>, a.n_part, 256, 0, s, pdl, a);
-  return launch(k_route<__nv_bfloat16, __nv_bfloat16>, a.n_part, 256, 0, s, pdl, a);
+// Shared memory the last CTA needs to route a layer (see route_finish).
+size_t route_smem_bytes(const Dec2Args &a, bool *stage) {
+  const size_t rest = (size_t)(2 * a.T * a.E + 3 * a.T * a.k + kDec2MaxThreads + 2 +
+                               2 * (a.E + a.S) + 2 * a.T * (a.k + a.S)) * 4;
+  const size_t st = (size_t)a.n_part * a.T * a.E * 4;
+  *stage = st + rest <= (size_t)max_smem() - 4096;
+  return (*stage ? st : 0) + rest;
 }
 
-cudaError_t launch_topk(const Dec2Args &a_in, cudaStream_t s, bool pdl) {
+cudaError_t launch_route_partials(const Dec2Args &a_in, int x_bf16, int w_bf16, cudaStream_t s,
+                                  bool pdl) {
   Dec2Args a = a_in;
-  const size_t rest = (size_t)(2 * a.T * a.E + 3 * a.T * a.k + 256) * 4;
-  const size_t stage = (size_t)a.n_part * a.T * a.E * 4;
-  a.gu_stage_partials = stage + rest <= (size_t)max_smem() - 2048;
-  const size_t smem = (a.gu_stage_partials ? stage : 0) + rest;
-  cudaError_t e = allow_smem(k_topk, smem);
-  if (e != cudaSuccess) return e;
-  return launch(k_topk, 1, 256, smem, s, pdl, a);
+  bool stage = false;
+  const size_t smem = route_smem_bytes(a, &stage);
+  a.stage_partials = stage;
+  const int threads = kDec2MaxThreads;
+  cudaError_t e;
+#define COLI_LAUNCH_ROUTE(XT, WT)                                             \
+  if ((e = allow_smem(k_route<XT, WT>, smem)) != cudaSuccess) return e;      \
+  return launch(k_route<XT, WT>, a.n_part, threads, smem, s, pdl, a);
+  if (!x_bf16 && !w_bf16) { COLI_LAUNCH_ROUTE(float, float) }
+  if (!x_bf16 && w_bf16) { COLI_LAUNCH_ROUTE(float, __nv_bfloat16) }
+  if (x_bf16 && !w_bf16) { COLI_LAUNCH_ROUTE(__nv_bfloat16, float) }
+  COLI_LAUNCH_ROUTE(__nv_bfloat16, __nv_bfloat16)
+#undef COLI_LAUNCH_ROUTE
 }
 
 cudaError_t launch_gateup(const Dec2Args &a, int grid, cudaStream_t s, bool pdl) {
@@ -857,15 +894,23 @@ cudaError_t launch_gateup(const Dec2Args &a, int grid, cudaStream_t s, bool pdl)
   return launch(k_gateup, grid, threads, a.gu.total, s, pdl, a);
 }
 
-cudaError_t launch_down(const Dec2Args &a, int wr_bf16, cudaStream_t s, bool pdl) {
+cudaError_t launch_down(const Dec2Args &a_in, int wr_bf16, cudaStream_t s, bool pdl) {
+  Dec2Args a = a_in;
   const int threads = a.dn_ncg * a.dn_nrg * 32;
+  size_t smem = a.dn.total;
+  if (a.wr) {
+    bool stage = false;
+    const size_t rs = route_smem_bytes(a, &stage);
+    a.stage_partials = stage;
+    if (rs > smem) smem = rs;
+  }
   cudaError_t e;
   if (wr_bf16) {
-    if ((e = allow_smem(k_down<__nv_bfloat16>, a.dn.total)) != cudaSuccess) return e;
-    return launch(k_down<__nv_bfloat16>, a.n_part, threads, a.dn.total, s, pdl, a);
+    if ((e = allow_smem(k_down<__nv_bfloat16>, smem)) != cudaSuccess) return e;
+    return launch(k_down<__nv_bfloat16>, a.n_part, threads, smem, s, pdl, a);
   }
-  if ((e = allow_smem(k_down<float>, a.dn.total)) != cudaSuccess) return e;
-  return launch(k_down<float>, a.n_part, threads, a.dn.total, s, pdl, a);
+  if ((e = allow_smem(k_down<float>, smem)) != cudaSuccess) return e;
+  return launch(k_down<float>, a.n_part, threads, smem, s, pdl, a);
 }
 
 }  // namespace coli
