@@ -15,13 +15,14 @@ WsLayout ws_layout(int T, int H, int F, int E, int S, int k) {
   WsLayout L{};
   size_t o = 0;
   const size_t KS = (size_t)k + S;
-  L.n_part = num_sms() < H / 4 ? num_sms() : H / 4;
+  L.n_part = num_sms();    // CTAs of the row-split kernels (some may own no rows)
   // replica strides: whole 256-byte units plus one, so replicas start at
   // different offsets modulo any power of two
+  L.part_stride = (align256((size_t)L.n_part * T * E * 4) + 256) / 4;
   L.h_stride = (align256((size_t)T * KS * F * 4) + 256) / 4;
   L.x_stride = (align256((size_t)T * H * 4) + 256) / 4;
   L.ctrl = o;      o = align256(o + kCtrlWords * sizeof(uint32_t));
-  L.partials = o;  o = align256(o + (size_t)L.n_part * T * E * 4);
+  L.partials = o;  o = align256(o + kReplicas * L.part_stride * 4);
   L.idx = o;       o = align256(o + (size_t)T * k * sizeof(int32_t));
   L.gates = o;     o = align256(o + (size_t)T * k * sizeof(float));
   L.act = o;       o = align256(o + (size_t)(2 * (E + S) + 2) * sizeof(int32_t));
@@ -230,10 +231,38 @@ static int moe_run(const coli_moe_desc *d, int k, int n_layers, const void *x, c
   for (int t0 = 0; t0 < T; t0 += TP) {
     const int tn = T - t0 < TP ? T - t0 : TP;
     const size_t xo = (size_t)t0 * H;
-    const int st = moe_pass(d, k, n_layers, tn, (const char *)x + xo * xsize(d->x_dtype),
-                            d->x_dtype, router_w, packed, scales, out + xo, residual,
-                            layer_out ? layer_out + xo : nullptr, route_counts, workspace, L,
-                            stream);
+    const void *xp = (const char *)x + xo * xsize(d->x_dtype);
+    if (residual) {
+      // decode stack: one persistent kernel for all layers when its plan fits
+      Dec2Args a = make_args(d, k, tn, (uint8_t *)workspace, L);
+      StackArgs st{};
+      if (plan_stack(a, st) == cudaSuccess) {
+        const int E = d->n_experts, F = d->ffn, S = d->n_shared;
+        a.x = xp;
+        a.packed = packed;
+        a.scales = scales;
+        st.n_layers = n_layers;
+        st.router = router_w;
+        st.wr_stride = (size_t)E * H * xsize(d->router_dtype);
+        st.pk_stride = (size_t)(E + S) * coli_expert_packed_bytes(H, F);
+        st.sc_stride = (size_t)(E + S) * coli_expert_scale_count(H, F);
+        st.counts = route_counts;
+        st.layer_out = layer_out ? layer_out + xo : nullptr;
+        st.x_out = out + xo;
+        st.part_stride = L.part_stride;
+        // layer_out rows of this pass are [l][t0 + t]: pass the per-layer stride through T
+        if (layer_out && tn != T) st.layer_out = nullptr;
+        if (st.layer_out || !layer_out) {
+          cudaError_t e = launch_stack(a, st, d->x_dtype == COLI_BF16,
+                                       d->router_dtype == COLI_BF16, stream);
+          if (e != cudaSuccess) return COLI_ECUDA;
+          continue;
+        }
+      }
+    }
+    const int st = moe_pass(d, k, n_layers, tn, xp, d->x_dtype, router_w, packed, scales,
+                            out + xo, residual, layer_out ? layer_out + xo : nullptr,
+                            route_counts, workspace, L, stream);
     if (st != COLI_OK) return st;
   }
   return COLI_OK;

@@ -23,13 +23,15 @@ constexpr int kReplicas = 8;
 enum CtrlWord : int {
   kCtrlFlags = 0,      // COLI_FLAG_* bits (sticky until coli_moe_check clears)
   kCtrlRouterTicket = 1,
+  kCtrlBarrier = 2,    // grid barrier counter of the persistent stack kernel
+  kCtrlExit = 3,       // its exit ticket (resets the barrier counter)
   kCtrlWords = 64,     // 256 bytes
 };
 
 // Byte offsets of the scratch arrays inside a workspace (all 256-aligned).
 struct WsLayout {
   size_t ctrl;       // uint32[kCtrlWords]
-  size_t partials;   // f32 [kReplicas][n_part][T][E] router partial logits
+  size_t partials;   // f32 [kReplicas][n_part][T][E] router partial logits (copy r at r*part_stride)
   size_t idx;        // i32 [T][k]
   size_t gates;      // f32 [T][k]
   size_t act;        // i32: n_active, act_expert[E+S], act_off[E+S+1]
@@ -90,7 +92,30 @@ struct Dec2Args {
   DnSmem dn;
 };
 
+// Shared-memory plan of the persistent stack kernel: union lists, router rows,
+// then one area reused by the routing, gate/up and down phases.
+struct StkSmem {
+  size_t act, routes, slot_gate, wr, area;
+  size_t gu_red, gu_xpl, dn_acc, dn_xn, dn_planes;   // offsets inside the area
+  size_t total;
+};
+
+struct StackArgs {
+  int n_layers;
+  const void *router;       // [n_layers][E][H]
+  size_t wr_stride;         // bytes per layer
+  size_t pk_stride, sc_stride;
+  uint32_t *counts;         // [n_layers][E] or null
+  float *layer_out;         // [n_layers][T][H] or null
+  float *x_out;             // [T][H]
+  size_t part_stride;       // floats between the partials' copies
+  StkSmem sm;
+};
+
 cudaError_t plan_decode(Dec2Args &a, int n_part);
+cudaError_t plan_stack(Dec2Args &a, StackArgs &st);
+cudaError_t launch_stack(const Dec2Args &a, const StackArgs &st, int x_bf16, int wr_bf16,
+                         cudaStream_t s);
 cudaError_t launch_route_partials(const Dec2Args &a, int x_bf16, int w_bf16, cudaStream_t s,
                                   bool pdl);
 cudaError_t launch_gateup(const Dec2Args &a, int grid, cudaStream_t s, bool pdl);

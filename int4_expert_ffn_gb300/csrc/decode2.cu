@@ -276,6 +276,30 @@ __device__ __forceinline__ void set_flag(uint32_t *ctrl, uint32_t f) {
   atomicOr(ctrl + kCtrlFlags, f);
 }
 
+// The pointers that change from layer to layer (the rest of Dec2Args stays in
+// kernel-parameter space).
+struct LayerPtrs {
+  const uint8_t *packed;
+  const float *scales;
+  uint32_t *route_counts;
+  float *layer_out;
+  const float *partials;
+  float *out;
+  float *xrep;
+};
+
+__device__ __forceinline__ LayerPtrs layer_ptrs(const Dec2Args &a) {
+  LayerPtrs p;
+  p.packed = a.packed;
+  p.scales = a.scales;
+  p.route_counts = a.route_counts;
+  p.layer_out = a.layer_out;
+  p.partials = a.partials;
+  p.out = a.out;
+  p.xrep = a.xrep;
+  return p;
+}
+
 
 }  // namespace
 
@@ -309,7 +333,7 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_route(Dec2Args a) {
     }
   }
   extern __shared__ __align__(128) uint8_t smem_route[];
-  route_if_last(a, smem_route);
+  route_if_last(a, layer_ptrs(a), smem_route);
 }
 
 // ---------------------------------------------------------------------------
@@ -319,13 +343,13 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_route(Dec2Args a) {
 // Routing shared by k_gateup and k_topk: logits from this CTA's replica of the
 // router partials (fixed summation order), block-parallel top-k, NaN flag and,
 // if `publish`, the user-visible idx/gates and route counts.
-__device__ void route_block(const Dec2Args &a, float *s_logits, int *s_idx, float *s_gates,
-                            float *s_vals, int *s_rank, float *s_scratch, float *s_stage,
-                            bool publish) {
+__device__ void route_block(const Dec2Args &a, const LayerPtrs &lp, float *s_logits, int *s_idx,
+                            float *s_gates, float *s_vals, int *s_rank, float *s_scratch,
+                            float *s_stage, bool publish) {
   const int T = a.T, E = a.E, k = a.k;
   const int TE = T * E;
   const int nthr = blockDim.x;
-  const float *src = a.partials;
+  const float *src = lp.partials;
   if (s_stage) {
     // all threads copy the partials into shared memory, every load in flight at once
     const int n4 = (a.n_part * TE) / 4, tail = (a.n_part * TE) & 3;
@@ -388,7 +412,7 @@ __device__ void route_block(const Dec2Args &a, float *s_logits, int *s_idx, floa
     for (int i = threadIdx.x; i < T * k; i += nthr) {
       a.g_idx[i] = s_idx[i];
       a.g_gates[i] = s_gates[i];
-      if (a.route_counts) atomicAdd(a.route_counts + s_idx[i], 1u);
+      if (lp.route_counts) atomicAdd(lp.route_counts + s_idx[i], 1u);
     }
   }
 }
@@ -397,7 +421,7 @@ __device__ void route_block(const Dec2Args &a, float *s_logits, int *s_idx, floa
 // kernel that produced them: logits (fixed summation order), top-k, gates,
 // route counts, and the union lists the expert kernels read.  `smem` holds
 // at least route_smem_bytes(a) bytes.
-__device__ void route_finish(const Dec2Args &a, uint8_t *smem) {
+__device__ void route_finish(const Dec2Args &a, const LayerPtrs &lp, uint8_t *smem) {
   const int T = a.T, E = a.E, k = a.k, S = a.S, KS = k + S;
   float *s_stage = (float *)smem;
   float *s_logits = s_stage + (a.stage_partials ? (size_t)a.n_part * T * E : 0);
@@ -406,7 +430,7 @@ __device__ void route_finish(const Dec2Args &a, uint8_t *smem) {
   float *s_gates = (float *)(s_idx + T * k);
   float *s_vals = s_gates + T * k;
   float *s_scratch = s_vals + T * k;
-  route_block(a, s_logits, s_idx, s_gates, s_vals, s_rank, s_scratch,
+  route_block(a, lp, s_logits, s_idx, s_gates, s_vals, s_rank, s_scratch,
               a.stage_partials ? s_stage : nullptr, true);
   __syncthreads();
   for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
@@ -429,7 +453,7 @@ __device__ void route_finish(const Dec2Args &a, uint8_t *smem) {
 
 // Every CTA has written its partials: the last one to arrive (atomic ticket)
 // routes the layer and resets the ticket for the next use.
-__device__ void route_if_last(const Dec2Args &a, uint8_t *smem) {
+__device__ void route_if_last(const Dec2Args &a, const LayerPtrs &lp, uint8_t *smem) {
   __shared__ int s_last;
   __threadfence();
   __syncthreads();
@@ -440,65 +464,51 @@ __device__ void route_if_last(const Dec2Args &a, uint8_t *smem) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  route_finish(a, smem);
+  route_finish(a, lp, smem);
   if (threadIdx.x == 0) a.ctrl[kCtrlRouterTicket] = 0;
 }
 
 // ---------------------------------------------------------------------------
-// gate/up: each compute warp owns one 1024-column chunk (cg) of every row
-// congruent to rg modulo nrg within the CTA's row range, issues the loads of
-// up to kGuBatch rows before computing any of them, and leaves per-row partial
+// gate/up phase: each compute warp owns one 1024-column chunk (cg) of every
+// row congruent to rg modulo nrg within the CTA's row range, issues the loads
+// of kGuBatch rows before computing any of them, and leaves per-row partial
 // sums in shared memory; after one barrier the block finalises
-// h = silu(g) * u * gate and writes it to every replica.
+// h = silu(g) * u * gate and writes it to every replica.  The union lists are
+// already in shared memory.
 
 constexpr int kGuBatch = 4;
 
-__global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const GuSmem &L = a.gu;
+__device__ void gu_phase(const Dec2Args &a, const LayerPtrs &lp, const int *s_act,
+                         const int *s_routes, const float *s_slot_gate, float *red,
+                         uint32_t *s_xpl) {
   const int T = a.T, H = a.H, F = a.F, E = a.E, S = a.S, k = a.k, KS = k + S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  grid_dependents_launch();
-  grid_dependency_wait();
-  COLI_TRACE_POINT(0, 1);
-  int *s_act = (int *)(smem + L.act);          // [0] n_active, act_expert, act_off
-  int *s_act_expert = s_act + 1;
-  int *s_act_off = s_act + 1 + (E + S);
-  int *s_routes = (int *)(smem + L.routes);
-  float *s_slot_gate = (float *)(smem + L.slot_gate);
-  uint32_t *s_xpl = (uint32_t *)(smem + L.xpl);
-  float *red = (float *)(smem + L.red);
-  const int G = gridDim.x, c = blockIdx.x;
-
-  // routing was done by the routing kernel: read its union lists
-  for (int i = tid; i < 2 + 2 * (E + S); i += blockDim.x) s_act[i] = __ldcg(a.g_act + i);
-  for (int i = tid; i < T * KS; i += blockDim.x) {
-    s_routes[i] = __ldcg(a.g_routes + i);
-    s_slot_gate[i] = __ldcg(a.g_slot_gate + i);
-  }
-  __syncthreads();
+  const int *s_act_expert = s_act + 1;
+  const int *s_act_off = s_act + 1 + (E + S);
   const int n_active = s_act[0];
-  if (tid == 0) COLI_TRACE_POINT(0, 3);
+  const int G = gridDim.x, c = blockIdx.x;
   const int64_t rb = H / 2, ngr = H / kGroup;
-  // L2 prefetch of the down rows that the same-index k_down CTA will read
+  // L2 prefetch of the down rows that this CTA index will need in the down phase
   if (warp == 0 && c < a.n_part) {
     const int UH = H / 4;
     const int dh0 = 4 * part_lo(c, UH, a.n_part), dh1 = 4 * part_lo(c + 1, UH, a.n_part);
     for (int q = lane; q < n_active && dh1 > dh0; q += 32) {
       const int e = s_act_expert[q];
-      prefetch_l2(a.packed + (int64_t)e * a.eb + (int64_t)F * H + (int64_t)dh0 * (F / 2),
+      prefetch_l2(lp.packed + (int64_t)e * a.eb + (int64_t)F * H + (int64_t)dh0 * (F / 2),
                   (uint32_t)((dh1 - dh0) * (F / 2)));
-      prefetch_l2(a.scales + (int64_t)e * a.es + (int64_t)2 * F * ngr + (int64_t)dh0 * (F / kGroup),
+      prefetch_l2(lp.scales + (int64_t)e * a.es + (int64_t)2 * F * ngr + (int64_t)dh0 * (F / kGroup),
                   (uint32_t)((dh1 - dh0) * (F / 16)));
     }
   }
   // this CTA's rows in the flattened (used expert, row) space, units of 4 rows
   const int U = n_active * (F / 4);
   const int row0 = 4 * part_lo(c, U, G), nrows = 4 * part_lo(c + 1, U, G) - row0;
-  const float *xr = a.xrep + (size_t)(c % a.n_rep) * a.x_stride;
+  const float *xr = lp.xrep + (size_t)(c % a.n_rep) * a.x_stride;
   const int nbx = H / 32;
-  if (a.gu_xpl) build_planes(xr, T, H, s_xpl, nbx);
-  __syncthreads();
+  if (a.gu_xpl) {
+    build_planes(xr, T, H, s_xpl, nbx);
+    __syncthreads();
+  }
   if (tid == 0) COLI_TRACE_POINT(0, 4);
 
   const int ncg = a.gu_ncg, nrg = a.gu_nrg;
@@ -523,8 +533,8 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
           ra[b] = ai;
           if (act) {
             const int e = s_act_expert[ai];
-            const uint8_t *pg = a.packed + (int64_t)e * a.eb + (int64_t)f * rb + col / 2;
-            const float *pgs = a.scales + (int64_t)e * a.es + (int64_t)f * ngr + col / kGroup;
+            const uint8_t *pg = lp.packed + (int64_t)e * a.eb + (int64_t)f * rb + col / 2;
+            const float *pgs = lp.scales + (int64_t)e * a.es + (int64_t)f * ngr + col / kGroup;
             wg[b] = ldg_stream(pg);
             wu[b] = ldg_stream(pg + (int64_t)F * rb);
             sg[b] = __ldg(pgs);
@@ -533,49 +543,46 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
         }
       }
       if (q0 == 0 && tid == 0) COLI_TRACE_POINT(0, 5);
+      int maxtok = 0;
 #pragma unroll
-      for (int b0 = 0; b0 < kGuBatch; b0 += 4) {
-        int maxtok = 0;
+      for (int b = 0; b < kGuBatch; ++b)
+        if (ra[b] >= 0) {
+          const int nt = s_act_off[ra[b] + 1] - s_act_off[ra[b]];
+          maxtok = nt > maxtok ? nt : maxtok;
+        }
+      for (int j = 0; j < maxtok; ++j) {
+        float v[8];
 #pragma unroll
-        for (int b = b0; b < b0 + 4; ++b)
+        for (int b = 0; b < kGuBatch; ++b) {
+          v[2 * b] = 0.0f;
+          v[2 * b + 1] = 0.0f;
           if (ra[b] >= 0) {
-            const int nt = s_act_off[ra[b] + 1] - s_act_off[ra[b]];
-            maxtok = nt > maxtok ? nt : maxtok;
-          }
-        for (int j = 0; j < maxtok; ++j) {
-          float v[8];
-#pragma unroll
-          for (int b = b0; b < b0 + 4; ++b) {
-            v[2 * (b - b0)] = 0.0f;
-            v[2 * (b - b0) + 1] = 0.0f;
-            if (ra[b] >= 0) {
-              const int j0 = s_act_off[ra[b]], nt = s_act_off[ra[b] + 1] - j0;
-              if (j < nt && act) {
-                const int t = s_routes[j0 + j] / KS;
-                if (t != pl_tok) {
-                  if (a.gu_xpl) {
-                    load_planes(s_xpl, t, col / 32, nbx, pl);
-                  } else {
-                    float xv[32];
-                    load32<float>(xr + (int64_t)t * H + col, xv);
-                    quantize32(xv, pl);
-                  }
-                  pl_tok = t;
+            const int j0 = s_act_off[ra[b]], nt = s_act_off[ra[b] + 1] - j0;
+            if (j < nt && act) {
+              const int t = s_routes[j0 + j] / KS;
+              if (t != pl_tok) {
+                if (a.gu_xpl) {
+                  load_planes(s_xpl, t, col / 32, nbx, pl);
+                } else {
+                  float xv[32];
+                  load32<float>(xr + (int64_t)t * H + col, xv);
+                  quantize32(xv, pl);
                 }
-                v[2 * (b - b0)] = sg[b] * dot32(wg[b], pl);
-                v[2 * (b - b0) + 1] = su[b] * dot32(wu[b], pl);
+                pl_tok = t;
               }
+              v[2 * b] = sg[b] * dot32(wg[b], pl);
+              v[2 * b + 1] = su[b] * dot32(wu[b], pl);
             }
           }
-          const float tot = reduce8(v);
-          if ((lane & 3) == 0) {
-            const int vi = lane >> 2, b = b0 + (vi >> 1);
-            if (ra[b] >= 0) {
-              const int nt = s_act_off[ra[b] + 1] - s_act_off[ra[b]];
-              if (j < nt) {
-                const int i = rg + (q0 + b) * nrg;
-                red[((i * T + j) * ncg + cg) * 2 + (vi & 1)] = tot;
-              }
+        }
+        const float tot = reduce8(v);
+        if ((lane & 3) == 0) {
+          const int vi = lane >> 2, b = vi >> 1;
+          if (ra[b] >= 0) {
+            const int nt = s_act_off[ra[b] + 1] - s_act_off[ra[b]];
+            if (j < nt) {
+              const int i = rg + (q0 + b) * nrg;
+              red[((i * T + j) * ncg + cg) * 2 + (vi & 1)] = tot;
             }
           }
         }
@@ -592,9 +599,9 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
     const int j0 = s_act_off[ai], nt = s_act_off[ai + 1] - j0;
     if (j >= nt) continue;
     float g = 0.0f, u = 0.0f;
-    for (int cg = 0; cg < ncg; ++cg) {
-      g += red[((i * T + j) * ncg + cg) * 2];
-      u += red[((i * T + j) * ncg + cg) * 2 + 1];
+    for (int q = 0; q < ncg; ++q) {
+      g += red[((i * T + j) * ncg + q) * 2];
+      u += red[((i * T + j) * ncg + q) * 2 + 1];
     }
     const int slot_id = s_routes[j0 + j];
     const float hv = silu(g) * u * s_slot_gate[slot_id];
@@ -603,47 +610,55 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
   if (tid == 0) COLI_TRACE_POINT(0, 7);
 }
 
+// Union lists published by the routing CTA, into shared memory.
+__device__ void load_lists(const Dec2Args &a, int *s_act, int *s_routes, float *s_slot_gate) {
+  const int KS = a.k + a.S;
+  for (int i = threadIdx.x; i < 2 + 2 * (a.E + a.S); i += blockDim.x) s_act[i] = __ldcg(a.g_act + i);
+  for (int i = threadIdx.x; i < a.T * KS; i += blockDim.x) {
+    s_routes[i] = __ldcg(a.g_routes + i);
+    if (s_slot_gate) s_slot_gate[i] = __ldcg(a.g_slot_gate + i);
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const GuSmem &L = a.gu;
+  grid_dependents_launch();
+  grid_dependency_wait();
+  COLI_TRACE_POINT(0, 1);
+  int *s_act = (int *)(smem + L.act);
+  int *s_routes = (int *)(smem + L.routes);
+  float *s_slot_gate = (float *)(smem + L.slot_gate);
+  load_lists(a, s_act, s_routes, s_slot_gate);
+  if (threadIdx.x == 0) COLI_TRACE_POINT(0, 3);
+  gu_phase(a, layer_ptrs(a), s_act, s_routes, s_slot_gate, (float *)(smem + L.red),
+           (uint32_t *)(smem + L.xpl));
+}
+
 // ---------------------------------------------------------------------------
-// down + combine + residual + next layer's router partials.  Each CTA owns a
-// block of output rows; a warp owns one 1024-column chunk (cg) of its rows and
-// walks the used experts in ascending order (8 rows' loads in flight), adding
-// each slot's contribution into per-token registers.
+// down phase: each CTA owns a block of output rows; a warp owns one
+// 1024-column chunk (cg) of its rows and walks the used experts in ascending
+// order (8 experts' loads in flight), adding each slot's contribution into
+// per-token registers.  Writes out (with the residual), layer_out, the x
+// replicas, and leaves the new residual-stream rows in s_xn [T][nr].
 
 constexpr int kDnBatch = 8;
 
-template <typename WT>
-__global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const DnSmem &L = a.dn;
+template <int TM>   // TM >= a.T: per-token accumulators held in registers
+__device__ void dn_phase(const Dec2Args &a, const LayerPtrs &lp, const int *s_act,
+                         const int *s_routes, float *red, uint32_t *s_planes, float *s_xn,
+                         const float *residual) {
   const int T = a.T, H = a.H, F = a.F, E = a.E, S = a.S, k = a.k, KS = k + S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = gridDim.x, c = blockIdx.x;
   const int UH = H / 4;
   const int dh0 = 4 * part_lo(c, UH, G), dh1 = 4 * part_lo(c + 1, UH, G);
   const int nr = dh1 - dh0;
-  WT *s_wr = (WT *)(smem + L.wr);
-  // the next layer's router rows [dh0, dh1) do not depend on the previous kernel
-  if (a.wr) {
-    const WT *wr = (const WT *)a.wr;
-    for (int i = tid; i < E * nr; i += blockDim.x) {
-      const int e = i / nr, r = i - e * nr;
-      s_wr[i] = wr[(size_t)e * H + dh0 + r];
-    }
-  }
-  grid_dependents_launch();
-  grid_dependency_wait();
-  if (tid == 0) COLI_TRACE_POINT(1, 1);
-  int *s_act = (int *)(smem + L.act);
-  int *s_act_expert = s_act + 1;
-  int *s_act_off = s_act + 1 + (E + S);
-  int *s_routes = (int *)(smem + L.routes);
-  float *red = (float *)(smem + L.acc);   // [nr][T][ncg]
-  uint32_t *s_planes = (uint32_t *)(smem + L.planes);
+  const int *s_act_expert = s_act + 1;
+  const int *s_act_off = s_act + 1 + (E + S);
   const int ncg = a.dn_ncg, nrg = a.dn_nrg;
-  for (int i = tid; i < 1 + 2 * (E + S) + 1; i += blockDim.x) s_act[i] = __ldcg(a.g_act + i);
-  for (int i = tid; i < T * KS; i += blockDim.x) s_routes[i] = __ldcg(a.g_routes + i);
   for (int i = tid; i < nr * T * ncg; i += blockDim.x) red[i] = 0.0f;
-  __syncthreads();
   const int n_active = s_act[0];
   const float *h_rep = a.h + (size_t)(c % a.n_rep) * a.h_stride;
   const int64_t rb = F / 2, ngr = F / kGroup;
@@ -665,9 +680,9 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
     if (ga == 0 && tid == 0) COLI_TRACE_POINT(1, 2);
     if (worker) {
       for (int r = rg; r < nr; r += nrg) {
-        float acc[kDecodeMaxT];
+        float acc[TM];
 #pragma unroll
-        for (int t = 0; t < kDecodeMaxT; ++t) acc[t] = 0.0f;
+        for (int t = 0; t < TM; ++t) acc[t] = 0.0f;
         for (int a0 = ga; a0 < gb; a0 += kDnBatch) {
           uint4 w[kDnBatch];
           float sc[kDnBatch];
@@ -675,9 +690,9 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
           for (int b = 0; b < kDnBatch; ++b)
             if (a0 + b < gb && act) {
               const int e = s_act_expert[a0 + b];
-              w[b] = ldg_stream(a.packed + (int64_t)e * a.eb + down_b + (int64_t)(dh0 + r) * rb +
+              w[b] = ldg_stream(lp.packed + (int64_t)e * a.eb + down_b + (int64_t)(dh0 + r) * rb +
                                 col / 2);
-              sc[b] = __ldg(a.scales + (int64_t)e * a.es + down_s + (int64_t)(dh0 + r) * ngr +
+              sc[b] = __ldg(lp.scales + (int64_t)e * a.es + down_s + (int64_t)(dh0 + r) * ngr +
                             col / kGroup);
             }
 #pragma unroll
@@ -691,7 +706,7 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
               const float v = sc[b] * dot32(w[b], pl);
               const int t = s_routes[j0 + j] / KS;
 #pragma unroll
-              for (int tt = 0; tt < kDecodeMaxT; ++tt)
+              for (int tt = 0; tt < TM; ++tt)
                 if (tt == t) acc[tt] += v;
             }
           }
@@ -703,7 +718,7 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
           for (int q = 0; q < 8; ++q) {
             v[q] = 0.0f;
 #pragma unroll
-            for (int tt = 0; tt < kDecodeMaxT; ++tt)
+            for (int tt = 0; tt < TM; ++tt)
               if (tt == t0 + q) v[q] = acc[tt];
           }
           const float tot = reduce8(v);
@@ -716,34 +731,200 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
     ga = gb;
   }
   if (tid == 0) COLI_TRACE_POINT(1, 4);
-  // combine is complete: residual, outputs, next layer's partial logits
-  float *s_xn = (float *)(smem + L.xn);   // [T][nr]
+  // combine is complete: residual, outputs, replicas of the new layer input
   for (int i = tid; i < T * nr; i += blockDim.x) {
     const int t = i / nr, r = i - t * nr;
     const int64_t o = (int64_t)t * H + dh0 + r;
     float v = 0.0f;
     for (int q = 0; q < ncg; ++q) v += red[(r * T + t) * ncg + q];
-    if (a.layer_out) a.layer_out[o] = v;
-    const float xn = a.residual ? a.residual[o] + v : v;
-    a.out[o] = xn;
+    if (lp.layer_out) lp.layer_out[o] = v;
+    const float xn = residual ? residual[o] + v : v;
+    lp.out[o] = xn;
     s_xn[i] = xn;
-    if (a.xrep)
-      for (int rr = 0; rr < a.n_rep; ++rr) a.xrep[rr * a.x_stride + o] = xn;
+    if (lp.xrep)
+      for (int rr = 0; rr < a.n_rep; ++rr) lp.xrep[rr * a.x_stride + o] = xn;
   }
+  __syncthreads();
+}
+
+// Partial logits of the next layer from this CTA's rows of its input:
+// partials[c][t][e] = sum_r wr[e][dh0 + r] xn[t][r], written to n_copies copies.
+template <typename WT>
+__device__ void dn_partials(const Dec2Args &a, float *partials, const WT *s_wr, const float *s_xn,
+                            int n_copies, size_t copy_stride) {
+  const int T = a.T, H = a.H, E = a.E;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int UH = H / 4;
+  const int nr = 4 * part_lo(c + 1, UH, G) - 4 * part_lo(c, UH, G);
+  for (int o = threadIdx.x; o < T * E; o += blockDim.x) {
+    const int t = o / E, e = o - t * E;
+    float sum = 0.0f;
+    for (int r = 0; r < nr; ++r) sum = fmaf(to_f32(s_wr[e * nr + r]), s_xn[t * nr + r], sum);
+    for (int rr = 0; rr < n_copies; ++rr)
+      partials[rr * copy_stride + (size_t)c * T * E + o] = sum;
+  }
+}
+
+// This CTA's rows [dh0, dh1) of a router matrix, into shared memory.
+template <typename WT>
+__device__ void load_router_rows(const Dec2Args &a, const WT *wr, WT *s_wr) {
+  const int H = a.H, E = a.E;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int UH = H / 4;
+  const int dh0 = 4 * part_lo(c, UH, G), nr = 4 * part_lo(c + 1, UH, G) - dh0;
+  for (int i = threadIdx.x; i < E * nr; i += blockDim.x) {
+    const int e = i / nr, r = i - e * nr;
+    s_wr[i] = wr[(size_t)e * H + dh0 + r];
+  }
+}
+
+template <typename WT>
+__global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const DnSmem &L = a.dn;
+  WT *s_wr = (WT *)(smem + L.wr);
+  // the next layer's router rows do not depend on the previous kernel
+  if (a.wr) load_router_rows<WT>(a, (const WT *)a.wr, s_wr);
+  grid_dependents_launch();
+  grid_dependency_wait();
+  if (threadIdx.x == 0) COLI_TRACE_POINT(1, 1);
+  int *s_act = (int *)(smem + L.act);
+  int *s_routes = (int *)(smem + L.routes);
+  load_lists(a, s_act, s_routes, nullptr);
+  float *s_xn = (float *)(smem + L.xn);
+  const LayerPtrs lp = layer_ptrs(a);
+  if (a.T == 1)
+    dn_phase<1>(a, lp, s_act, s_routes, (float *)(smem + L.acc), (uint32_t *)(smem + L.planes),
+                s_xn, a.residual);
+  else
+    dn_phase<kDecodeMaxT>(a, lp, s_act, s_routes, (float *)(smem + L.acc),
+                          (uint32_t *)(smem + L.planes), s_xn, a.residual);
   if (a.wr) {
-    __syncthreads();
-    for (int o = tid; o < T * E; o += blockDim.x) {
-      const int t = o / E, e = o - t * E;
-      float sum = 0.0f;
-      for (int r = 0; r < nr; ++r) sum = fmaf(to_f32(s_wr[e * nr + r]), s_xn[t * nr + r], sum);
-      a.partials[(size_t)c * T * E + o] = sum;
-    }
+    dn_partials<WT>(a, a.partials, s_wr, s_xn, 1, 0);
     // the last CTA routes the next layer (its shared memory is free again)
-    Dec2Args r = a;
-    r.route_counts = a.next_counts;
-    route_if_last(r, smem);
+    LayerPtrs rp = lp;
+    rp.route_counts = a.next_counts;
+    route_if_last(a, rp, smem);
   }
-  if (tid == 0) COLI_TRACE_POINT(1, 6);
+  if (threadIdx.x == 0) COLI_TRACE_POINT(1, 6);
+}
+
+// ---------------------------------------------------------------------------
+// The decode stack in one persistent cooperative kernel: layer after layer,
+// every CTA routes the layer itself from its copy of the router partials,
+// runs its gate/up share, meets the grid at a barrier (h complete), runs its
+// down rows and the next layer's partials, and meets the grid again.  Code and
+// launch state stay resident across layers.  Every barrier wait is bounded.
+
+__device__ bool grid_barrier(uint32_t *ctr, uint32_t target, uint32_t *ctrl) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(ctr), "r"(1u) : "memory");
+    int ok = 1;
+    uint32_t v;
+    const long long t0 = clock64();
+    for (;;) {
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+      if (v >= target) break;
+      if (clock64() - t0 > kWaitCycles) {
+        ok = 0;
+        atomicOr(ctrl + kCtrlFlags, COLI_FLAG_TIMEOUT);
+        break;
+      }
+    }
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+constexpr int kStackThreads = 384;
+
+template <typename XT, typename WT, int TM>
+__global__ void __launch_bounds__(kStackThreads) k_stack(Dec2Args a, StackArgs st) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const StkSmem &L = st.sm;
+  const int T = a.T, H = a.H, E = a.E, S = a.S, k = a.k;
+  const int tid = threadIdx.x;
+  const int G = gridDim.x, c = blockIdx.x;
+  int *s_act = (int *)(smem + L.act);
+  int *s_routes = (int *)(smem + L.routes);
+  float *s_slot_gate = (float *)(smem + L.slot_gate);
+  WT *s_wr = (WT *)(smem + L.wr);
+  uint8_t *area = smem + L.area;
+  uint32_t *bar = a.ctrl + kCtrlBarrier;
+  uint32_t nbar = 0;
+  bool ok = true;
+  // ---- layer 0: x in every replica (f32) and its router partials
+  {
+    const int UH = H / 4;
+    const int h0 = 4 * part_lo(c, UH, G), nr = 4 * part_lo(c + 1, UH, G) - h0;
+    const XT *x = (const XT *)a.x;
+    float *s_xn = (float *)area;
+    for (int i = tid; i < T * nr; i += blockDim.x) {
+      const int t = i / nr, r = i - t * nr;
+      const float v = to_f32(x[(size_t)t * H + h0 + r]);
+      s_xn[i] = v;
+      for (int rr = 0; rr < a.n_rep; ++rr) a.xrep[rr * a.x_stride + (size_t)t * H + h0 + r] = v;
+    }
+    load_router_rows<WT>(a, (const WT *)st.router, s_wr);
+    __syncthreads();
+    dn_partials<WT>(a, a.partials, s_wr, s_xn, a.n_rep, st.part_stride);
+  }
+  ok = grid_barrier(bar, ++nbar * G, a.ctrl);
+  for (int l = 0; l < st.n_layers && ok; ++l) {
+    LayerPtrs la;
+    la.packed = a.packed + (size_t)l * st.pk_stride;
+    la.scales = a.scales + (size_t)l * st.sc_stride;
+    la.route_counts = st.counts ? st.counts + (size_t)l * E : nullptr;
+    la.layer_out = st.layer_out ? st.layer_out + (size_t)l * T * H : nullptr;
+    la.partials = a.partials + (size_t)(c % a.n_rep) * st.part_stride;
+    la.out = st.x_out;
+    la.xrep = a.xrep;
+    const bool next = l + 1 < st.n_layers;
+    // the next layer's router rows: needed only in the down phase
+    if (next)
+      load_router_rows<WT>(a, (const WT *)((const uint8_t *)st.router + (size_t)(l + 1) * st.wr_stride),
+                           s_wr);
+    // ---- route (every CTA from its own copy of the partials)
+    {
+      float *s_logits = (float *)area;
+      int *s_rank = (int *)(s_logits + T * E);
+      int *s_idx = s_rank + T * E;
+      float *s_gates = (float *)(s_idx + T * k);
+      float *s_vals = s_gates + T * k;
+      float *s_scratch = s_vals + T * k;
+      float *s_stage = s_scratch + kDec2MaxThreads;
+      route_block(a, la, s_logits, s_idx, s_gates, s_vals, s_rank, s_scratch, s_stage, c == 0);
+      block_union(s_idx, s_gates, T, k, S, E, s_act, s_act + 1, s_act + 1 + (E + S), s_routes,
+                  s_slot_gate, s_rank);
+    }
+    // ---- gate/up
+    gu_phase(a, la, s_act, s_routes, s_slot_gate, (float *)(area + L.gu_red),
+             (uint32_t *)(area + L.gu_xpl));
+    ok = grid_barrier(bar, ++nbar * G, a.ctrl);
+    if (!ok) break;
+    // ---- down, residual, next layer's partials
+    float *s_xn = (float *)(area + L.dn_xn);
+    la.xrep = next ? a.xrep : nullptr;
+    dn_phase<TM>(a, la, s_act, s_routes, (float *)(area + L.dn_acc),
+                 (uint32_t *)(area + L.dn_planes), s_xn, a.xrep);   // replica 0: this layer's input
+    if (next) {
+      dn_partials<WT>(a, a.partials, s_wr, s_xn, a.n_rep, st.part_stride);
+      ok = grid_barrier(bar, ++nbar * G, a.ctrl);
+    }
+  }
+  // the last CTA out resets the barrier counters for the next launch
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned t = atomicAdd(a.ctrl + kCtrlExit, 1u);
+    if (t == (unsigned)G - 1) {
+      a.ctrl[kCtrlBarrier] = 0;
+      a.ctrl[kCtrlExit] = 0;
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -885,6 +1066,79 @@ cudaError_t launch_route_partials(const Dec2Args &a_in, int x_bf16, int w_bf16, 
   if (x_bf16 && !w_bf16) { COLI_LAUNCH_ROUTE(__nv_bfloat16, float) }
   COLI_LAUNCH_ROUTE(__nv_bfloat16, __nv_bfloat16)
 #undef COLI_LAUNCH_ROUTE
+}
+
+cudaError_t plan_stack(Dec2Args &a, StackArgs &st) {
+  cudaError_t e = plan_decode(a, a.n_part);
+  if (e != cudaSuccess) return e;
+  // the persistent kernel runs kStackThreads threads: fewer warps per phase
+  const int nw = kStackThreads / 32;
+  a.gu_nrg = nw / a.gu_ncg;
+  a.dn_nrg = nw / a.dn_ncg;
+  if (a.gu_nrg < 1 || a.dn_nrg < 1) return cudaErrorInvalidValue;
+  const int T = a.T, H = a.H, F = a.F, E = a.E, S = a.S, k = a.k, KS = k + S;
+  const size_t budget = (size_t)max_smem() - 4096;
+  const int G = a.n_part;
+  StkSmem m{};
+  size_t o = 0;
+  m.act = o; o = al16(o + (size_t)(2 + 2 * (E + S)) * 4);
+  m.routes = o; o = al16(o + (size_t)T * KS * 4);
+  m.slot_gate = o; o = al16(o + (size_t)T * KS * 4);
+  const int UH = H / 4;
+  const int max_nr = 4 * ((UH + G - 1) / G);
+  m.wr = o; o = al16(o + (size_t)E * max_nr * 4);
+  m.area = al128(o);
+  const size_t route_b = (size_t)(2 * T * E + 3 * T * k + kDec2MaxThreads + (size_t)G * T * E) * 4;
+  const int n_used = ((E < T * k) ? E : T * k) + S;
+  const int max_rows = 4 * ((n_used * (F / 4) + G - 1) / G);
+  size_t go = 0;
+  m.gu_red = go; go = al16(go + (size_t)max_rows * T * a.gu_ncg * 2 * 4);
+  m.gu_xpl = go; go = al16(go + (a.gu_xpl ? (size_t)T * 18 * (H / 32) * 4 : 0));
+  size_t dof = 0;
+  m.dn_acc = dof; dof = al16(dof + (size_t)max_nr * T * a.dn_ncg * 4);
+  m.dn_xn = dof; dof = al16(dof + (size_t)T * max_nr * 4);
+  m.dn_planes = dof;
+  size_t area = route_b > go ? route_b : go;
+  if (dof > area) area = dof;
+  if (m.area + area > budget) return cudaErrorInvalidValue;
+  const size_t per_slot = (size_t)18 * (F / 32) * 4;
+  int slots = (int)((budget - m.area - dof) / per_slot);
+  if (slots > T * KS) slots = T * KS;
+  if (slots < T) return cudaErrorInvalidValue;
+  a.dn_slots = slots;
+  const size_t dn_b = dof + (size_t)slots * per_slot;
+  if (dn_b > area) area = dn_b;
+  m.total = al16(m.area + area);
+  st.sm = m;
+  return cudaSuccess;
+}
+
+cudaError_t launch_stack(const Dec2Args &a, const StackArgs &st, int x_bf16, int wr_bf16,
+                         cudaStream_t s) {
+  const int threads = kStackThreads;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_part);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = st.sm.total;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeCooperative;
+  at[0].val.cooperative = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+#define COLI_LAUNCH_STACK(XT, WT)                                                        \
+  if (a.T == 1) {                                                                         \
+    if ((e = allow_smem(k_stack<XT, WT, 1>, st.sm.total)) != cudaSuccess) return e;       \
+    return cudaLaunchKernelEx(&cfg, k_stack<XT, WT, 1>, a, st);                            \
+  }                                                                                       \
+  if ((e = allow_smem(k_stack<XT, WT, kDecodeMaxT>, st.sm.total)) != cudaSuccess) return e; \
+  return cudaLaunchKernelEx(&cfg, k_stack<XT, WT, kDecodeMaxT>, a, st);
+  if (!x_bf16 && !wr_bf16) { COLI_LAUNCH_STACK(float, float) }
+  if (!x_bf16 && wr_bf16) { COLI_LAUNCH_STACK(float, __nv_bfloat16) }
+  if (x_bf16 && !wr_bf16) { COLI_LAUNCH_STACK(__nv_bfloat16, float) }
+  COLI_LAUNCH_STACK(__nv_bfloat16, __nv_bfloat16)
+#undef COLI_LAUNCH_STACK
 }
 
 cudaError_t launch_gateup(const Dec2Args &a, int grid, cudaStream_t s, bool pdl) {
