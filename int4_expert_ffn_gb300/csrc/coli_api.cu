@@ -69,6 +69,11 @@ int check_desc(const coli_moe_desc *d, int top_k) {
   return COLI_OK;
 }
 
+// The persistent one-launch decode stack (k_stack) is built and kept in step
+// with the kernel chain, but measured slower on GB300 (685 vs 537 us per
+// 16-layer OLMoE-like token): the chain is used.
+constexpr bool kUseStackKernel = false;
+
 // Tokens per internal pass of the GEMV path; larger calls run in passes.
 int pass_tokens(int T) { return T < kDecodeMaxT ? T : kDecodeMaxT; }
 
@@ -232,7 +237,7 @@ static int moe_run(const coli_moe_desc *d, int k, int n_layers, const void *x, c
     const int tn = T - t0 < TP ? T - t0 : TP;
     const size_t xo = (size_t)t0 * H;
     const void *xp = (const char *)x + xo * xsize(d->x_dtype);
-    if (residual) {
+    if (residual && kUseStackKernel) {
       // decode stack: one persistent kernel for all layers when its plan fits
       Dec2Args a = make_args(d, k, tn, (uint8_t *)workspace, L);
       StackArgs st{};

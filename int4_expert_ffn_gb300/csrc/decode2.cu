@@ -888,6 +888,7 @@ __global__ void __launch_bounds__(kStackThreads) k_stack(Dec2Args a, StackArgs s
     if (next)
       load_router_rows<WT>(a, (const WT *)((const uint8_t *)st.router + (size_t)(l + 1) * st.wr_stride),
                            s_wr);
+    if (l == 3 && tid == 0) COLI_TRACE_POINT(1, 8);
     // ---- route (every CTA from its own copy of the partials)
     {
       float *s_logits = (float *)area;
@@ -901,19 +902,25 @@ __global__ void __launch_bounds__(kStackThreads) k_stack(Dec2Args a, StackArgs s
       block_union(s_idx, s_gates, T, k, S, E, s_act, s_act + 1, s_act + 1 + (E + S), s_routes,
                   s_slot_gate, s_rank);
     }
+    if (l == 3 && tid == 0) COLI_TRACE_POINT(1, 9);
     // ---- gate/up
     gu_phase(a, la, s_act, s_routes, s_slot_gate, (float *)(area + L.gu_red),
              (uint32_t *)(area + L.gu_xpl));
+    if (l == 3 && tid == 0) COLI_TRACE_POINT(1, 10);
     ok = grid_barrier(bar, ++nbar * G, a.ctrl);
     if (!ok) break;
+    if (l == 3 && tid == 0) COLI_TRACE_POINT(1, 11);
     // ---- down, residual, next layer's partials
     float *s_xn = (float *)(area + L.dn_xn);
     la.xrep = next ? a.xrep : nullptr;
     dn_phase<TM>(a, la, s_act, s_routes, (float *)(area + L.dn_acc),
                  (uint32_t *)(area + L.dn_planes), s_xn, a.xrep);   // replica 0: this layer's input
+    if (l == 3 && tid == 0) COLI_TRACE_POINT(1, 12);
     if (next) {
       dn_partials<WT>(a, a.partials, s_wr, s_xn, a.n_rep, st.part_stride);
+      if (l == 3 && tid == 0) COLI_TRACE_POINT(1, 13);
       ok = grid_barrier(bar, ++nbar * G, a.ctrl);
+      if (l == 3 && tid == 0) COLI_TRACE_POINT(1, 14);
     }
   }
   // the last CTA out resets the barrier counters for the next launch
