@@ -30,10 +30,15 @@ import torch  # noqa: E402
 
 METRIC = "MoE decode tokens/s and int4 expert-weight GB/s vs GB300 HBM peak"
 
-# DRAM traffic per launch of the dominant kernel from an ncu capture of the
-# same kernel build (dram__bytes_read.sum + dram__bytes_write.sum); None until
-# a capture of the current kernel exists.  Source file named beside each value.
-NCU_TRAFFIC = {}
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
+# each kernel from an ncu capture of the current kernel build, keyed by
+# workload and kernel; absent until such a capture exists.  The profiles/
+# summary it comes from is named beside each value.
+NCU_TRAFFIC = {
+    # profiles/k_gateup_k_down_olmoe_2layer.md (batch 1: same launches per layer
+    # as the 16-layer stack)
+    "olmoe_decode": {"k_gateup": 28456960 + 256, "k_down": 10098944},
+}
 
 
 def read_peaks():
@@ -198,6 +203,28 @@ class DecodeWorkload:
         passes = (self.shape.tokens + 15) // 16
         return passes * (1 + 2 * self.shape.layers)
 
+    def kernel_bytes(self, kernel, steps):
+        """Algorithmic bytes of every launch of one kernel over the given steps.
+        gate/up: gate and up nibbles + scales of the layer's distinct routed
+        experts and its shared experts, x in, h out.  down: down nibbles +
+        scales of the same experts, h in, residual in, output out, and the
+        next layer's router weights (the routing that follows in its tail)."""
+        c, sh = self.coli, self.shape
+        T, H, F, E, S, k = sh.tokens, sh.hidden, sh.ffn, sh.experts, sh.shared, sh.top_k
+        uniq = (self.counts[steps] > 0).sum(dim=2).cpu().numpy()          # [K, L]
+        n_exp = uniq + S
+        h_bytes = T * (k + S) * F * 4
+        rb = sh.experts * sh.hidden * (2 if sh.router_dtype == "bf16" else 4)
+        if kernel == c.COLI_KERNEL_GATEUP:
+            per_exp = 2 * (F * H // 2 + 4 * F * H // 64)
+            return int((n_exp * per_exp).sum() + uniq.size * (T * H * 4 + h_bytes))
+        if kernel == c.COLI_KERNEL_DOWN:
+            per_exp = H * F // 2 + 4 * H * F // 64
+            next_router = rb * (sh.layers - 1) * len(steps)
+            return int((n_exp * per_exp).sum() + uniq.size * (h_bytes + 2 * T * H * 4)
+                       + next_router)
+        return int(len(steps) * (rb + T * H * 4))
+
     def algorithmic_bytes(self, steps):
         """Bytes the method must move for the given steps: packed nibbles and
         scales of every distinct expert each layer routed to, the shared
@@ -272,9 +299,57 @@ def run_decode(args, shape, dev, world, rank):
         "clocks": sampler.summary(t0, t1),
         "launches": steps * wl.kernels_per_step(),
     }
-    res["e2e"] = run_e2e(wl, args, dev, world, stream)
     del graphs
+    res["kernels"] = {name: kernel_timing(wl, args, stream, kid)
+                      for name, kid in (("k_gateup", wl.coli.COLI_KERNEL_GATEUP),
+                                        ("k_down", wl.coli.COLI_KERNEL_DOWN))}
+    res["e2e"] = run_e2e(wl, args, dev, world, stream)
     return wl, res
+
+
+def kernel_timing(wl, args, stream, kernel):
+    """Average launch duration of one kernel of the layer forward over the same
+    steps as the timed region: the steps' graphs are captured again with CUDA
+    event pairs around every launch of `kernel` (recorded on the launch
+    stream) and replayed once.  The bracketing events serialise that kernel
+    behind its predecessor, so this replay is kept apart from the timed step
+    region; its own step time is reported beside the result."""
+    c = wl.coli
+    sh = wl.shape
+    steps, warmup = args.steps, args.warmup
+    per_step = sh.layers if kernel != c.COLI_KERNEL_ROUTE else 1
+    n = steps * per_step
+    before = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    after = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in before + after:     # torch creates the CUDA event on first record
+        e.record(stream)
+    stream.synchronize()
+    c.coli_profile_events(kernel, before, after)
+    try:
+        graphs = capture_graphs(wl, range(warmup, warmup + steps), stream)
+    finally:
+        got = c.coli_profile_events(kernel, [], [])
+    assert got == n, "bracketed %d launches, expected %d" % (got, n)
+    save = wl.counts.clone()
+    wl.counts.zero_()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for g in graphs:
+            g.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    durations = np.array([b.elapsed_time(a) for b, a in zip(before, after)]) * 1e3   # us
+    counts_ok = torch.equal(wl.counts[warmup:warmup + steps], save[warmup:warmup + steps])
+    wl.counts.copy_(save)
+    del graphs
+    alg = wl.kernel_bytes(kernel, list(range(warmup, warmup + steps)))
+    return {"launches": n, "us_per_launch": float(durations.mean()),
+            "us_median": float(np.median(durations)), "total_ms": float(durations.sum() / 1e3),
+            "alg_bytes_per_launch": alg / n,
+            "bracketed_ms_per_step": ev0.elapsed_time(ev1) / steps,
+            "same_routes": bool(counts_ok)}
 
 
 def run_e2e(wl, args, dev, world, stream):
@@ -377,6 +452,8 @@ def main():
     ap.add_argument("--workload", default="olmoe_decode",
                     choices=["olmoe_decode", "glm_decode_b1", "glm_decode_b8"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="override the stack depth (small profiling cases only)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -390,6 +467,9 @@ def main():
 
     from int4_expert_ffn_gb300 import synth
     shape = synth.SHAPES[args.workload]
+    if args.layers is not None:
+        import dataclasses
+        shape = dataclasses.replace(shape, layers=args.layers)
     config = {"workload": "%s: %d MoE layers, hidden %d, %d experts of FFN width %d, top-%d, "
                           "%d shared, batch %d, int4-grouped g64 f32 scales, %s router"
                           % (shape.name, shape.layers, shape.hidden, shape.experts, shape.ffn,
@@ -425,19 +505,26 @@ def main():
     sec = res["ms"] / 1e3
     value = world * res["tokens_per_rank"] / sec
     gbs = res["alg_bytes"] / sec / 1e9
-    kernel = "decode step (router + gate/up + down per layer, CUDA graph)"
-    traffic = NCU_TRAFFIC.get(args.workload)
+    kern = res["kernels"]
+    dom = max(kern, key=lambda n: kern[n]["total_ms"])
+    kd = kern[dom]
+    k_gbs = kd["alg_bytes_per_launch"] / (kd["us_per_launch"] * 1e-6) / 1e9
+    traffic = NCU_TRAFFIC.get(args.workload, {}).get(dom)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"] / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; weights N(0,0.02) bf16 quantised on the GPU)",
         "config": config,
-        "gbs": gbs,
-        "roofline": {"bound": "hbm", "kernel": kernel, "achieved": gbs, "peak": hbm_peak,
-                     "unit": "GB/s", "frac": gbs / hbm_peak, "peak_kind": peak_kind,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": k_gbs, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": k_gbs / hbm_peak,
+                     "peak_kind": "%s (hbm_gbs, burst copy)" % peak_kind,
                      "traffic": traffic,
-                     "alg_bytes_per_step": res["alg_bytes"] / args.steps},
+                     "alg_bytes_per_launch": kd["alg_bytes_per_launch"],
+                     "us_per_launch": kd["us_per_launch"]},
+        "step_roofline": {"achieved": gbs, "unit": "GB/s", "frac": gbs / hbm_peak,
+                          "alg_bytes_per_step": res["alg_bytes"] / args.steps},
+        "kernels": kern,
         "clocks": res["clocks"],
         "e2e": res["e2e"],
         "gpu_launches": res["launches"],

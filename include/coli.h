@@ -182,6 +182,27 @@ int coli_moe_stack_forward(const coli_moe_desc *d, int top_k, int n_layers,
                            float *x_out, float *layer_out, uint32_t *route_counts,
                            void *workspace, size_t ws_bytes, cudaStream_t stream);
 
+/* Kernels of the layer forward that coli_profile_events can bracket. */
+#define COLI_KERNEL_ROUTE  0   /* router partials of a pass's first layer */
+#define COLI_KERNEL_GATEUP 1   /* gate/up expert GEMVs + SwiGLU */
+#define COLI_KERNEL_DOWN   2   /* down expert GEMVs + combine (+ next routing) */
+
+/*
+ * coli_profile_events -- diagnostic, not on the compute path: record the
+ * caller's CUDA events before[i] / after[i] on the launch stream around the
+ * next n launches of one kernel of the layer forward (COLI_KERNEL_*), so a
+ * caller can time that kernel inside a larger region.  Works while the stream
+ * is captured into a CUDA graph (the records become event-record nodes).  The
+ * records order the bracketed kernel after all earlier work of its stream, so
+ * they remove the overlap of its launch with the kernel before it.
+ * before/after are host arrays of n cudaEvent_t (the library copies them);
+ * n = 0 turns recording off.  Process-wide state: not for concurrent callers.
+ * Returns the number of launches bracketed under the previous setting (>= 0),
+ * or COLI_EINVAL.
+ */
+int coli_profile_events(int kernel, const cudaEvent_t *before, const cudaEvent_t *after,
+                        int n);
+
 /*
  * coli_moe_check -- read (and optionally clear) the device-side flag word of a
  * workspace.  Synchronises `stream`.  *flags receives COLI_FLAG_* bits.

@@ -19,6 +19,7 @@ COLI_OK, COLI_EINVAL, COLI_EALIGN, COLI_ECUDA, COLI_ETIMEOUT, COLI_ENOMEM, COLI_
     0, -1, -2, -3, -4, -5, -6)
 COLI_F32, COLI_BF16 = 0, 1
 COLI_FLAG_NAN_LOGITS, COLI_FLAG_TIMEOUT = 0x1, 0x2
+COLI_KERNEL_ROUTE, COLI_KERNEL_GATEUP, COLI_KERNEL_DOWN = 0, 1, 2
 GROUP = 64
 
 # every symbol include/coli.h declares
@@ -27,7 +28,7 @@ EXPORTS = (
     "coli_expert_packed_bytes", "coli_expert_scale_count", "coli_quant_i4g",
     "coli_router_workspace_size", "coli_moe_workspace_size", "coli_router_topk",
     "coli_moe_forward", "coli_moe_forward_noalloc", "coli_moe_stack_forward",
-    "coli_moe_check",
+    "coli_profile_events", "coli_moe_check",
 )
 
 
@@ -73,6 +74,8 @@ def _load():
     L.coli_moe_stack_forward.argtypes = [dp, C.c_int, C.c_int, vp, vp, vp, vp, vp, vp, vp,
                                          vp, sz, vp]
     L.coli_moe_stack_forward.restype = C.c_int
+    L.coli_profile_events.argtypes = [C.c_int, C.POINTER(vp), C.POINTER(vp), C.c_int]
+    L.coli_profile_events.restype = C.c_int
     L.coli_moe_check.argtypes = [vp, C.c_int, C.POINTER(C.c_uint32), vp]
     L.coli_moe_check.restype = C.c_int
     return L
@@ -230,6 +233,21 @@ def coli_moe_stack_forward(desc: MoEDesc, top_k, n_layers, x, router_w, packed_e
         _ptr(scales), _ptr(x_out), _ptr(layer_out), _ptr(route_counts), _ptr(workspace),
         workspace.numel(), _stream(stream)))
     return x_out
+
+
+def coli_profile_events(kernel, before, after):
+    """Bracket the next len(before) launches of `kernel` (COLI_KERNEL_*) with
+    the given torch.cuda.Event pairs (diagnostic, see coli.h); empty lists turn
+    recording off.  Returns the launches bracketed under the previous setting."""
+    n = len(before)
+    if len(after) != n:
+        raise ValueError("before/after lengths differ")
+    arr_b = (C.c_void_p * max(n, 1))(*[e.cuda_event for e in before])
+    arr_a = (C.c_void_p * max(n, 1))(*[e.cuda_event for e in after])
+    st = lib.coli_profile_events(kernel, arr_b, arr_a, n)
+    if st < 0:
+        raise ColiError("coli_profile_events", st)
+    return st
 
 
 def coli_moe_check(workspace, clear=True, stream=None):

@@ -4,6 +4,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <vector>
 
 #include "coli_internal.cuh"
 
@@ -78,6 +79,45 @@ constexpr bool kUseStackKernel = false;
 int pass_tokens(int T) { return T < kDecodeMaxT ? T : kDecodeMaxT; }
 
 int map_err(cudaError_t e) { return e == cudaSuccess ? COLI_OK : COLI_ECUDA; }
+
+// Diagnostic event recording around the gate/up kernel (coli_profile_events).
+struct ProfileState {
+  std::mutex mu;
+  int kernel = -1;
+  std::vector<cudaEvent_t> before, after;
+  size_t next = 0;
+};
+ProfileState &profile() {
+  static ProfileState p;
+  return p;
+}
+
+cudaError_t record_profile(int kernel, cudaStream_t s, bool is_after, size_t *slot) {
+  ProfileState &p = profile();
+  std::lock_guard<std::mutex> lock(p.mu);
+  if (!is_after) {
+    if (kernel != p.kernel || p.next >= p.before.size()) { *slot = (size_t)-1; return cudaSuccess; }
+    *slot = p.next++;
+  }
+  if (*slot == (size_t)-1) return cudaSuccess;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cs);
+  if (e != cudaSuccess) return e;
+  const unsigned flags = cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : 0;
+  cudaEvent_t ev = is_after ? p.after[*slot] : p.before[*slot];
+  return cudaEventRecordWithFlags(ev, s, flags);
+}
+
+// Launch one kernel of the layer forward, bracketed by the caller's profiling
+// events when coli_profile_events selected it.
+template <class Launch>
+cudaError_t profiled(int kernel, cudaStream_t s, Launch launch) {
+  size_t slot = 0;
+  cudaError_t e = record_profile(kernel, s, false, &slot);
+  if (e == cudaSuccess) e = launch();
+  if (e == cudaSuccess) e = record_profile(kernel, s, true, &slot);
+  return e;
+}
 
 size_t xsize(coli_dtype t) { return t == COLI_BF16 ? 2 : 4; }
 
@@ -210,10 +250,12 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
       // router partials of layer 0; the last CTA routes it
       a.wr = router_w;
       a.route_counts = route_counts;
-      e = launch_route_partials(a, x_dtype == COLI_BF16, wr_bf16, stream, true);
+      e = profiled(COLI_KERNEL_ROUTE, stream, [&] {
+        return launch_route_partials(a, x_dtype == COLI_BF16, wr_bf16, stream, true);
+      });
       if (e != cudaSuccess) break;
     }
-    e = launch_gateup(a, num_sms(), stream, true);
+    e = profiled(COLI_KERNEL_GATEUP, stream, [&] { return launch_gateup(a, num_sms(), stream, true); });
     if (e != cudaSuccess) break;
     // down also forms the next layer's router partials and routes it
     const bool next = l + 1 < n_layers;
@@ -222,7 +264,7 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
     a.residual = residual ? (const float *)xin : nullptr;
     a.out = out;
     a.layer_out = layer_out ? layer_out + (size_t)l * T_H : nullptr;
-    e = launch_down(a, wr_bf16, stream, true);
+    e = profiled(COLI_KERNEL_DOWN, stream, [&] { return launch_down(a, wr_bf16, stream, true); });
   }
   return e == cudaSuccess ? COLI_OK : COLI_ECUDA;
 }
@@ -309,6 +351,20 @@ int coli_moe_stack_forward(const coli_moe_desc *d, int top_k, int n_layers, cons
   if (d->x_dtype != COLI_F32) return COLI_EUNSUPPORTED;
   return moe_run(d, top_k, n_layers, x, router_w, packed_experts, scales, x_out, true, layer_out,
                  route_counts, workspace, stream);
+}
+
+int coli_profile_events(int kernel, const cudaEvent_t *before, const cudaEvent_t *after,
+                        int n) {
+  if (n < 0 || (n > 0 && (!before || !after))) return COLI_EINVAL;
+  if (kernel < COLI_KERNEL_ROUTE || kernel > COLI_KERNEL_DOWN) return COLI_EINVAL;
+  ProfileState &p = profile();
+  std::lock_guard<std::mutex> lock(p.mu);
+  const int done = (int)p.next;
+  p.kernel = n > 0 ? kernel : -1;
+  p.before.assign(before, before + n);
+  p.after.assign(after, after + n);
+  p.next = 0;
+  return done;
 }
 
 int coli_moe_check(void *workspace, int clear, uint32_t *flags, cudaStream_t stream) {

@@ -96,3 +96,27 @@ def test_entry_points_validate_before_launch(coli):
     assert lib.coli_moe_forward(C.byref(empty), 2, None, None, None, None, None, None, None,
                                 0, None) == coli.COLI_OK
     assert lib.coli_quant_i4g(None, coli.COLI_BF16, 0, 64, None, None, None) == coli.COLI_OK
+
+
+def header_defines():
+    src = open(os.path.join(ROOT, "include", "coli.h")).read()
+    return {m.group(1): int(m.group(2), 0)
+            for m in re.finditer(r"#define\s+(COLI_[A-Z0-9_]+)\s+(0x[0-9a-fA-F]+|\d+)u?", src)}
+
+
+def test_header_constants_match_binding(coli):
+    defs = header_defines()
+    assert {"COLI_FLAG_NAN_LOGITS", "COLI_FLAG_TIMEOUT", "COLI_KERNEL_ROUTE",
+            "COLI_KERNEL_GATEUP", "COLI_KERNEL_DOWN"} <= set(defs)
+    for name, value in defs.items():
+        assert getattr(coli, name) == value, name
+
+
+def test_profile_events_validation(coli):
+    lib = coli.lib
+    arr = (C.c_void_p * 1)()
+    assert lib.coli_profile_events(coli.COLI_KERNEL_GATEUP, arr, arr, -1) == coli.COLI_EINVAL
+    assert lib.coli_profile_events(7, arr, arr, 1) == coli.COLI_EINVAL
+    assert lib.coli_profile_events(coli.COLI_KERNEL_GATEUP, None, None, 1) == coli.COLI_EINVAL
+    # turning recording off is always valid and reports no bracketed launches
+    assert lib.coli_profile_events(coli.COLI_KERNEL_GATEUP, None, None, 0) == 0

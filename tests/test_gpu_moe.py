@@ -124,3 +124,47 @@ def test_stack_tiny_chain():
     for l in range(3):
         assert rel_err(layer_out[l].cpu().numpy(), outs[l]).max() <= REL_TOL
     assert np.array_equal(counts.cpu().numpy(), ocounts)
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_profile_events_bracket_each_kernel(graph):
+    """coli_profile_events brackets exactly the selected kernel's launches, in
+    eager mode and inside a captured graph, without changing the results."""
+    shape = dataclasses.replace(synth.TINY, layers=3, tokens=2)
+    layers = [Layer(shape, l, 0) for l in range(3)]
+    gp = [ly.gpu() for ly in layers]
+    packed = torch.cat([g[0] for g in gp])
+    scales = torch.cat([g[1] for g in gp])
+    wr = torch.cat([g[2] for g in gp])
+    x = synth.tokens(shape).cuda()
+    c = coli()
+    desc = desc_for(shape, 2)
+    ws = c.new_workspace(desc, shape.top_k)
+    ref = c.coli_moe_stack_forward(desc, shape.top_k, 3, x, wr, packed, scales, ws).clone()
+    stream = torch.cuda.Stream()
+    for kernel, n in ((c.COLI_KERNEL_ROUTE, 1), (c.COLI_KERNEL_GATEUP, 3), (c.COLI_KERNEL_DOWN, 3)):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n)]
+        for e in ev:
+            e.record(stream)
+        out = torch.empty_like(ref)
+        torch.cuda.synchronize()
+        c.coli_profile_events(kernel, ev[:n], ev[n:])
+        try:
+            if graph:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    c.coli_moe_stack_forward(desc, shape.top_k, 3, x, wr, packed, scales, ws,
+                                             x_out=out, stream=stream)
+            else:
+                with torch.cuda.stream(stream):
+                    c.coli_moe_stack_forward(desc, shape.top_k, 3, x, wr, packed, scales, ws,
+                                             x_out=out, stream=stream)
+        finally:
+            got = c.coli_profile_events(kernel, [], [])
+        assert got == n
+        if graph:
+            g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+        times = [b.elapsed_time(a) for b, a in zip(ev[:n], ev[n:])]
+        assert all(0.0 < t < 1000.0 for t in times), times
