@@ -180,9 +180,18 @@ class DecodeWorkload:
                     s0 += ns
             wrs.append(synth.router_weights(shape, l, seed, device=dev))
         self.router = torch.stack(wrs).contiguous()
-        self.x = torch.stack([synth.tokens(shape, seed, i, device=dev)
-                              for i in range(steps_total)]).contiguous()
-        self.out = torch.empty((steps_total, T, H), dtype=torch.float32, device=dev)
+        # chained: one input per step ([K, T, H]); else one per step and layer ([K, L, T, H])
+        if shape.chained:
+            self.x = torch.stack([synth.tokens(shape, seed, i, device=dev)
+                                  for i in range(steps_total)]).contiguous()
+            self.out = torch.empty((steps_total, T, H), dtype=torch.float32, device=dev)
+        else:
+            self.x = torch.stack([torch.stack([synth.tokens(shape, seed, i, device=dev, layer=l)
+                                               for l in range(L)])
+                                  for i in range(steps_total)]).contiguous()
+            self.out = torch.empty((steps_total, L, T, H), dtype=torch.float32, device=dev)
+        self.layer_bytes = n * self.eb
+        self.layer_scales = n * self.es
         self.counts = torch.zeros((steps_total, L, E), dtype=torch.int32, device=dev)
         self.desc = c.MoEDesc(H, F, E, S, T, c.COLI_F32,
                               c.COLI_BF16 if shape.router_dtype == "bf16" else c.COLI_F32)
@@ -190,18 +199,34 @@ class DecodeWorkload:
         torch.cuda.synchronize()
 
     def step(self, i, stream=None, x=None, out=None):
-        c = self.coli
-        c.coli_moe_stack_forward(self.desc, self.shape.top_k, self.shape.layers,
-                                 self.x[i] if x is None else x, self.router, self.packed,
-                                 self.scales, self.ws,
-                                 x_out=self.out[i] if out is None else out,
-                                 route_counts=self.counts[i], stream=stream)
+        """One decode step: the token(s) through every layer.  Chained stacks
+        are one stack call; otherwise one layer call per layer."""
+        c, sh = self.coli, self.shape
+        x = self.x[i] if x is None else x
+        out = self.out[i] if out is None else out
+        if sh.chained:
+            c.coli_moe_stack_forward(self.desc, sh.top_k, sh.layers, x, self.router,
+                                     self.packed, self.scales, self.ws, x_out=out,
+                                     route_counts=self.counts[i], stream=stream)
+            return
+        pb, sb = self.layer_bytes, self.layer_scales
+        for l in range(sh.layers):
+            c.coli_moe_forward(self.desc, sh.top_k, x[l], self.router[l],
+                               self.packed[l * pb:(l + 1) * pb], self.scales[l * sb:(l + 1) * sb],
+                               self.ws, out=out[l], route_counts=self.counts[i, l], stream=stream)
 
     def kernels_per_step(self):
-        # per 16-token pass: the first layer's router partials, then gate/up
-        # and down for every layer
-        passes = (self.shape.tokens + 15) // 16
-        return passes * (1 + 2 * self.shape.layers)
+        # per 16-token pass: chained, the first layer's router partials, then
+        # gate/up and down for every layer; else router, gate/up, down per layer
+        sh = self.shape
+        passes = (sh.tokens + 15) // 16
+        return passes * ((1 + 2 * sh.layers) if sh.chained else 3 * sh.layers)
+
+    def io_bytes_per_step(self):
+        """Host <-> device bytes of one step's input and output (f32)."""
+        sh = self.shape
+        n = sh.tokens * sh.hidden * 4
+        return (n, n) if sh.chained else (sh.layers * n, sh.layers * n)
 
     def kernel_bytes(self, kernel, steps):
         """Algorithmic bytes of every launch of one kernel over the given steps.
@@ -220,10 +245,11 @@ class DecodeWorkload:
             return int((n_exp * per_exp).sum() + uniq.size * (T * H * 4 + h_bytes))
         if kernel == c.COLI_KERNEL_DOWN:
             per_exp = H * F // 2 + 4 * H * F // 64
-            next_router = rb * (sh.layers - 1) * len(steps)
+            next_router = rb * (sh.layers - 1) * len(steps) if sh.chained else 0
             return int((n_exp * per_exp).sum() + uniq.size * (h_bytes + 2 * T * H * 4)
                        + next_router)
-        return int(len(steps) * (rb + T * H * 4))
+        n_route = len(steps) * (1 if sh.chained else sh.layers)
+        return int(n_route * (rb + T * H * 4))
 
     def algorithmic_bytes(self, steps):
         """Bytes the method must move for the given steps: packed nibbles and
@@ -359,9 +385,9 @@ def run_e2e(wl, args, dev, world, stream):
     steps, warmup = args.steps, args.warmup
     n = warmup + steps
     host_x = wl.x.cpu().pin_memory()
-    host_out = torch.empty((n, sh.tokens, sh.hidden), dtype=torch.float32).pin_memory()
-    dx = torch.empty((sh.tokens, sh.hidden), dtype=torch.float32, device=dev)
-    dout = torch.empty((sh.tokens, sh.hidden), dtype=torch.float32, device=dev)
+    host_out = torch.empty(tuple(wl.out.shape), dtype=torch.float32).pin_memory()
+    dx = torch.empty(tuple(wl.x.shape[1:]), dtype=torch.float32, device=dev)
+    dout = torch.empty(tuple(wl.out.shape[1:]), dtype=torch.float32, device=dev)
     graphs = []
     for i in range(n):
         g = torch.cuda.CUDAGraph()
@@ -386,9 +412,9 @@ def run_e2e(wl, args, dev, world, stream):
     barrier(world)
     ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     assert torch.equal(host_out[warmup:n], wl.out[warmup:n].cpu()), "e2e output mismatch"
-    bi = sh.tokens * sh.hidden * 4
+    bi, bo = wl.io_bytes_per_step()
     return {"value": world * steps * sh.tokens / (ms / 1e3), "unit": "tokens/s",
-            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bi}
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
 
 
 # ---------------------------------------------------------------------------
@@ -477,6 +503,9 @@ def main():
               "layers": shape.layers, "hidden": shape.hidden, "experts": shape.experts,
               "ffn": shape.ffn, "top_k": shape.top_k, "shared": shape.shared,
               "batch": shape.tokens, "parallelism": "replicas" if world > 1 else "single",
+              "inputs": ("layer 0 takes a fresh N(0,1) token each step; layer l>0 takes "
+                         "x_l + MoE_l(x_l)" if shape.chained else
+                         "every layer takes its own fresh N(0,1) input each step"),
               "l2": "inputs larger than L2: %.2f GB of experts resident, fresh routing each step"}
 
     if args.impl == "reference":

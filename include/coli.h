@@ -69,6 +69,10 @@ typedef struct {
 
 const char *coli_status_str(int status);
 
+/* Message of the last CUDA error that a call made on this host thread
+ * returned as COLI_ECUDA ("no error" before any).  Static storage; never NULL. */
+const char *coli_last_error(void);
+
 /* Size helpers of the packed format (bytes / element counts). */
 int64_t coli_packed_row_bytes(int64_t cols);            /* ceil(cols/2) */
 int64_t coli_scales_per_row(int64_t cols);              /* ceil(cols/64) */

@@ -24,7 +24,7 @@ GROUP = 64
 
 # every symbol include/coli.h declares
 EXPORTS = (
-    "coli_status_str", "coli_packed_row_bytes", "coli_scales_per_row",
+    "coli_status_str", "coli_last_error", "coli_packed_row_bytes", "coli_scales_per_row",
     "coli_expert_packed_bytes", "coli_expert_scale_count", "coli_quant_i4g",
     "coli_router_workspace_size", "coli_moe_workspace_size", "coli_router_topk",
     "coli_moe_forward", "coli_moe_forward_noalloc", "coli_moe_stack_forward",
@@ -35,7 +35,10 @@ EXPORTS = (
 class ColiError(RuntimeError):
     def __init__(self, fn, status):
         self.status = status
-        super().__init__("%s failed: %s (%d)" % (fn, _status_str(status), status))
+        msg = "%s failed: %s (%d)" % (fn, _status_str(status), status)
+        if status == COLI_ECUDA:
+            msg += ": " + coli_last_error()
+        super().__init__(msg)
 
 
 class coli_moe_desc(C.Structure):
@@ -54,6 +57,8 @@ def _load():
     dp = C.POINTER(coli_moe_desc)
     L.coli_status_str.argtypes = [C.c_int]
     L.coli_status_str.restype = C.c_char_p
+    L.coli_last_error.argtypes = []
+    L.coli_last_error.restype = C.c_char_p
     for f in ("coli_packed_row_bytes", "coli_scales_per_row"):
         getattr(L, f).argtypes = [i64]
         getattr(L, f).restype = i64
@@ -86,6 +91,11 @@ lib = _load()
 
 def _status_str(status):
     return lib.coli_status_str(status).decode()
+
+
+def coli_last_error():
+    """Message of the last CUDA error a call on this thread returned as COLI_ECUDA."""
+    return lib.coli_last_error().decode()
 
 
 def _check(fn, status):

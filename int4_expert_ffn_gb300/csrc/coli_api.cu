@@ -19,11 +19,10 @@ WsLayout ws_layout(int T, int H, int F, int E, int S, int k) {
   L.n_part = num_sms();    // CTAs of the row-split kernels (some may own no rows)
   // replica strides: whole 256-byte units plus one, so replicas start at
   // different offsets modulo any power of two
-  L.part_stride = (align256((size_t)L.n_part * T * E * 4) + 256) / 4;
   L.h_stride = (align256((size_t)T * KS * F * 4) + 256) / 4;
   L.x_stride = (align256((size_t)T * H * 4) + 256) / 4;
   L.ctrl = o;      o = align256(o + kCtrlWords * sizeof(uint32_t));
-  L.partials = o;  o = align256(o + kReplicas * L.part_stride * 4);
+  L.partials = o;  o = align256(o + (size_t)L.n_part * T * E * 4);
   L.idx = o;       o = align256(o + (size_t)T * k * sizeof(int32_t));
   L.gates = o;     o = align256(o + (size_t)T * k * sizeof(float));
   L.act = o;       o = align256(o + (size_t)(2 * (E + S) + 2) * sizeof(int32_t));
@@ -48,6 +47,17 @@ int num_sms() {
   return sms;
 }
 
+// Message of the last CUDA error that a call on this thread returned as COLI_ECUDA.
+static thread_local const char *t_last_error = "no error";
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return COLI_OK;
+  t_last_error = cudaGetErrorString(e);
+  return COLI_ECUDA;
+}
+
+const char *last_error() { return t_last_error; }
+
 }  // namespace coli
 
 using namespace coli;
@@ -70,15 +80,11 @@ int check_desc(const coli_moe_desc *d, int top_k) {
   return COLI_OK;
 }
 
-// The persistent one-launch decode stack (k_stack) is built and kept in step
-// with the kernel chain, but measured slower on GB300 (685 vs 537 us per
-// 16-layer OLMoE-like token): the chain is used.
-constexpr bool kUseStackKernel = false;
 
 // Tokens per internal pass of the GEMV path; larger calls run in passes.
 int pass_tokens(int T) { return T < kDecodeMaxT ? T : kDecodeMaxT; }
 
-int map_err(cudaError_t e) { return e == cudaSuccess ? COLI_OK : COLI_ECUDA; }
+int map_err(cudaError_t e) { return coli::cuda_status(e); }
 
 // Diagnostic event recording around the gate/up kernel (coli_profile_events).
 struct ProfileState {
@@ -151,6 +157,8 @@ Dec2Args make_args(const coli_moe_desc *d, int k, int tn, uint8_t *ws, const WsL
 
 extern "C" {
 
+const char *coli_last_error(void) { return coli::last_error(); }
+
 const char *coli_status_str(int status) {
   switch (status) {
     case COLI_OK: return "ok";
@@ -218,7 +226,7 @@ int coli_router_topk(const coli_moe_desc *d, int top_k, const void *x, const voi
     a.xrep = nullptr;
     cudaError_t e = launch_route_partials(a, d->x_dtype == COLI_BF16,
                                           d->router_dtype == COLI_BF16, stream, true);
-    if (e != cudaSuccess) return COLI_ECUDA;
+    if (e != cudaSuccess) return map_err(e);
   }
   return COLI_OK;
 }
@@ -244,6 +252,7 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
   for (int l = 0; l < n_layers && e == cudaSuccess; ++l) {
     const void *xin = (l == 0) ? x : (const void *)out;
     a.x = xin;
+    a.layer = l;
     a.packed = packed + l * pk_stride;
     a.scales = scales + l * sc_stride;
     if (l == 0) {
@@ -266,7 +275,7 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
     a.layer_out = layer_out ? layer_out + (size_t)l * T_H : nullptr;
     e = profiled(COLI_KERNEL_DOWN, stream, [&] { return launch_down(a, wr_bf16, stream, true); });
   }
-  return e == cudaSuccess ? COLI_OK : COLI_ECUDA;
+  return map_err(e);
 }
 
 static int moe_run(const coli_moe_desc *d, int k, int n_layers, const void *x, const void *router_w,
@@ -279,34 +288,6 @@ static int moe_run(const coli_moe_desc *d, int k, int n_layers, const void *x, c
     const int tn = T - t0 < TP ? T - t0 : TP;
     const size_t xo = (size_t)t0 * H;
     const void *xp = (const char *)x + xo * xsize(d->x_dtype);
-    if (residual && kUseStackKernel) {
-      // decode stack: one persistent kernel for all layers when its plan fits
-      Dec2Args a = make_args(d, k, tn, (uint8_t *)workspace, L);
-      StackArgs st{};
-      if (plan_stack(a, st) == cudaSuccess) {
-        const int E = d->n_experts, F = d->ffn, S = d->n_shared;
-        a.x = xp;
-        a.packed = packed;
-        a.scales = scales;
-        st.n_layers = n_layers;
-        st.router = router_w;
-        st.wr_stride = (size_t)E * H * xsize(d->router_dtype);
-        st.pk_stride = (size_t)(E + S) * coli_expert_packed_bytes(H, F);
-        st.sc_stride = (size_t)(E + S) * coli_expert_scale_count(H, F);
-        st.counts = route_counts;
-        st.layer_out = layer_out ? layer_out + xo : nullptr;
-        st.x_out = out + xo;
-        st.part_stride = L.part_stride;
-        // layer_out rows of this pass are [l][t0 + t]: pass the per-layer stride through T
-        if (layer_out && tn != T) st.layer_out = nullptr;
-        if (st.layer_out || !layer_out) {
-          cudaError_t e = launch_stack(a, st, d->x_dtype == COLI_BF16,
-                                       d->router_dtype == COLI_BF16, stream);
-          if (e != cudaSuccess) return COLI_ECUDA;
-          continue;
-        }
-      }
-    }
     const int st = moe_pass(d, k, n_layers, tn, xp, d->x_dtype, router_w, packed, scales,
                             out + xo, residual, layer_out ? layer_out + xo : nullptr,
                             route_counts, workspace, L, stream);
@@ -371,11 +352,10 @@ int coli_moe_check(void *workspace, int clear, uint32_t *flags, cudaStream_t str
   if (!workspace || !flags) return COLI_EINVAL;
   uint32_t v = 0;
   uint32_t *dev = (uint32_t *)workspace + kCtrlFlags;
-  if (cudaMemcpyAsync(&v, dev, sizeof(v), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
-    return COLI_ECUDA;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return COLI_ECUDA;
-  if (clear && v && cudaMemsetAsync(dev, 0, sizeof(uint32_t), stream) != cudaSuccess)
-    return COLI_ECUDA;
+  cudaError_t e = cudaMemcpyAsync(&v, dev, sizeof(v), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess && clear && v) e = cudaMemsetAsync(dev, 0, sizeof(uint32_t), stream);
+  if (e != cudaSuccess) return map_err(e);
   *flags = v;
   return (v & COLI_FLAG_TIMEOUT) ? COLI_ETIMEOUT : COLI_OK;
 }

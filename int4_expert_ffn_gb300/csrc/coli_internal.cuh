@@ -14,7 +14,7 @@ constexpr int kDecodeMaxT = 16;     // tokens per call served by the GEMV path
 constexpr int kMaxTopK = 64;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxShared = 8;
-// Buffers that every CTA of a kernel reads (layer input, h, router partials)
+// Buffers that every CTA of a kernel reads (layer input, h)
 // are written in this many copies, each read by 1/kReplicas of the CTAs, so
 // that no single L2 slice serves the whole grid.
 constexpr int kReplicas = 8;
@@ -23,15 +23,13 @@ constexpr int kReplicas = 8;
 enum CtrlWord : int {
   kCtrlFlags = 0,      // COLI_FLAG_* bits (sticky until coli_moe_check clears)
   kCtrlRouterTicket = 1,
-  kCtrlBarrier = 2,    // grid barrier counter of the persistent stack kernel
-  kCtrlExit = 3,       // its exit ticket (resets the barrier counter)
   kCtrlWords = 64,     // 256 bytes
 };
 
 // Byte offsets of the scratch arrays inside a workspace (all 256-aligned).
 struct WsLayout {
   size_t ctrl;       // uint32[kCtrlWords]
-  size_t partials;   // f32 [kReplicas][n_part][T][E] router partial logits (copy r at r*part_stride)
+  size_t partials;   // f32 [n_part][T][E] router partial logits
   size_t idx;        // i32 [T][k]
   size_t gates;      // f32 [T][k]
   size_t act;        // i32: n_active, act_expert[E+S], act_off[E+S+1]
@@ -41,7 +39,7 @@ struct WsLayout {
   size_t xrep;       // f32 [kReplicas][T][H]
   size_t total;
   int n_part;
-  size_t part_stride, h_stride, x_stride;   // replica strides (floats)
+  size_t h_stride, x_stride;   // replica strides (floats)
 };
 
 WsLayout ws_layout(int T, int H, int F, int E, int S, int k);
@@ -50,16 +48,17 @@ constexpr int kDec2MaxThreads = 512;
 
 // Shared-memory plan of k_gateup (byte offsets into dynamic smem).
 struct GuSmem {
-  size_t act, routes, slot_gate, red, xpl, total;
+  size_t act, routes, slot_gate, xpl, ring, red, total;
 };
 // Shared-memory plan of k_down.
 struct DnSmem {
-  size_t act, routes, acc, xn, wr, planes, total;
+  size_t act, routes, acc, xn, wr, ring, red, planes, total;
 };
 
 // Arguments of the decode kernels (one layer, T <= kDecodeMaxT tokens).
 struct Dec2Args {
   int T, H, F, E, S, k;
+  int layer;                // index of the layer in the stack (phase tracing only)
   const void *x;            // layer input [T][H], f32 or bf16
   const void *wr;           // k_route: this layer's router; k_down: next layer's (or null)
   const float *residual;    // k_down: added to the layer output (or null)
@@ -86,36 +85,23 @@ struct Dec2Args {
   float *gates_out;
   int build_union;          // k_topk also builds and publishes the union lists
   int stage_partials;       // routing stages the partials in shared memory
-  int gu_ncg, gu_nrg, gu_xpl;
-  int dn_ncg, dn_nrg, dn_slots;
+  int gu_ncg;               // 1024-column chunks of a gate/up row
+  int gu_nw;                // warps of k_gateup
+  int gu_slots;             // depth of each warp's cp.async pipeline (2..4)
+  int gu_rows;              // rows whose partial sums fit in shared memory at once
+  int gu_xpl;               // x planes held in shared memory
+  int dn_ncg;               // 1024-column chunks of a down row
+  int dn_nw;                // warps of k_down
+  int dn_slots_pipe;        // depth of each warp's cp.async pipeline
+  int dn_slots;             // token slots whose planes fit in shared memory at once
+  int dn_batch;             // experts whose partial sums fit in shared memory at once
   GuSmem gu;
   DnSmem dn;
 };
 
-// Shared-memory plan of the persistent stack kernel: union lists, router rows,
-// then one area reused by the routing, gate/up and down phases.
-struct StkSmem {
-  size_t act, routes, slot_gate, wr, area;
-  size_t gu_red, gu_xpl, dn_acc, dn_xn, dn_planes;   // offsets inside the area
-  size_t total;
-};
 
-struct StackArgs {
-  int n_layers;
-  const void *router;       // [n_layers][E][H]
-  size_t wr_stride;         // bytes per layer
-  size_t pk_stride, sc_stride;
-  uint32_t *counts;         // [n_layers][E] or null
-  float *layer_out;         // [n_layers][T][H] or null
-  float *x_out;             // [T][H]
-  size_t part_stride;       // floats between the partials' copies
-  StkSmem sm;
-};
-
+// Fill the kernels' launch plan (warps per phase, shared-memory layouts).
 cudaError_t plan_decode(Dec2Args &a, int n_part);
-cudaError_t plan_stack(Dec2Args &a, StackArgs &st);
-cudaError_t launch_stack(const Dec2Args &a, const StackArgs &st, int x_bf16, int wr_bf16,
-                         cudaStream_t s);
 cudaError_t launch_route_partials(const Dec2Args &a, int x_bf16, int w_bf16, cudaStream_t s,
                                   bool pdl);
 cudaError_t launch_gateup(const Dec2Args &a, int grid, cudaStream_t s, bool pdl);
@@ -126,6 +112,10 @@ cudaError_t launch_quant_i4g(const void *w, int w_dtype, int64_t rows, int64_t c
                              uint8_t *packed, float *scales, cudaStream_t s);
 
 int num_sms();
+// COLI_OK for cudaSuccess; else records the error's message for
+// coli_last_error() and returns COLI_ECUDA.
+int cuda_status(cudaError_t e);
+const char *last_error();
 
 // ---------------------------------------------------------------------------
 // device helpers

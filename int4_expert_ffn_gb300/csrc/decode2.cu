@@ -106,28 +106,6 @@ __device__ __forceinline__ void load32<float>(const float *p, float (&v)[32]) {
   }
 }
 
-template <>
-__device__ __forceinline__ void load32<__nv_bfloat16>(const __nv_bfloat16 *p, float (&v)[32]) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 q = __ldcg((const uint4 *)p + i);
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
-      v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-    }
-  }
-}
-
-__device__ __forceinline__ void load32_smem(const float *p, float (&v)[32]) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float4 q = ((const float4 *)p)[i];
-    v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
-  }
-}
-
 // Reduce 8 values across the warp in 9 shuffles; lane l ends with the total of
 // value (l >> 2).
 __device__ __forceinline__ float reduce8(float (&v)[8]) {
@@ -163,8 +141,8 @@ __device__ __forceinline__ float reduce8(float (&v)[8]) {
 // is at planes[(v * 18 + w) * nbp + b].  One warp handles 4 blocks at a time;
 // lane q of a block's 8 lanes holds its columns 4q..4q+3.
 __device__ void build_planes_impl(const float *src, int n_vec, int F, const int *list,
-                                  uint32_t *planes, int nbp) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+                                  uint32_t *planes, int nbp, int warp, int nw) {
+  const int lane = threadIdx.x & 31;
   const int groups_per_vec = (F + 127) / 128;
   const int n_groups = n_vec * groups_per_vec;
   const int q = lane & 7;
@@ -243,13 +221,9 @@ __device__ void build_planes_impl(const float *src, int n_vec, int F, const int 
 __device__ void build_planes_list(const float *src, int F, const int *list, int n, uint32_t *planes,
                                   int nbp);
 
-__device__ void build_planes(const float *src, int n_vec, int F, uint32_t *planes, int nbp) {
-  build_planes_impl(src, n_vec, F, nullptr, planes, nbp);
-}
-
 __device__ void build_planes_list(const float *src, int F, const int *list, int n, uint32_t *planes,
                                   int nbp) {
-  build_planes_impl(src, n, F, list, planes, nbp);
+  build_planes_impl(src, n, F, list, planes, nbp, threadIdx.x >> 5, blockDim.x >> 5);
 }
 
 __device__ __forceinline__ void load_planes(const uint32_t *planes, int v, int b, int nbp,
@@ -340,6 +314,12 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_route(Dec2Args a) {
 // Routing shared by k_gateup and k_topk: logits from the partials (fixed
 // order), top-k per token by warps, NaN flag.
 
+// Partial logits were written by other CTAs of this kernel: global reads go
+// through L2 (never a stale L1 line).
+__device__ __forceinline__ float ld_part(const float *src, size_t i, bool staged) {
+  return staged ? src[i] : __ldcg(src + i);
+}
+
 // Routing shared by k_gateup and k_topk: logits from this CTA's replica of the
 // router partials (fixed summation order), block-parallel top-k, NaN flag and,
 // if `publish`, the user-visible idx/gates and route counts.
@@ -368,6 +348,7 @@ __device__ void route_block(const Dec2Args &a, const LayerPtrs &lp, float *s_log
     __syncthreads();
     src = s_stage;
   }
+  const bool staged = s_stage != nullptr;
   int nsplit = nthr / TE;
   if (nsplit > 8) nsplit = 8;
   if (nsplit <= 1) {
@@ -375,12 +356,12 @@ __device__ void route_block(const Dec2Args &a, const LayerPtrs &lp, float *s_log
       float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
       int p = 0;
       for (; p + 4 <= a.n_part; p += 4) {
-        s0 += src[(size_t)p * TE + o];
-        s1 += src[(size_t)(p + 1) * TE + o];
-        s2 += src[(size_t)(p + 2) * TE + o];
-        s3 += src[(size_t)(p + 3) * TE + o];
+        s0 += ld_part(src, (size_t)p * TE + o, staged);
+        s1 += ld_part(src, (size_t)(p + 1) * TE + o, staged);
+        s2 += ld_part(src, (size_t)(p + 2) * TE + o, staged);
+        s3 += ld_part(src, (size_t)(p + 3) * TE + o, staged);
       }
-      for (; p < a.n_part; ++p) s0 += src[(size_t)p * TE + o];
+      for (; p < a.n_part; ++p) s0 += ld_part(src, (size_t)p * TE + o, staged);
       s_logits[o] = (s0 + s1) + (s2 + s3);
     }
   } else {
@@ -391,10 +372,10 @@ __device__ void route_block(const Dec2Args &a, const LayerPtrs &lp, float *s_log
       float s0 = 0.0f, s1 = 0.0f;
       int p = p0;
       for (; p + 2 <= p1; p += 2) {
-        s0 += src[(size_t)p * TE + o];
-        s1 += src[(size_t)(p + 1) * TE + o];
+        s0 += ld_part(src, (size_t)p * TE + o, staged);
+        s1 += ld_part(src, (size_t)(p + 1) * TE + o, staged);
       }
-      if (p < p1) s0 += src[(size_t)p * TE + o];
+      if (p < p1) s0 += ld_part(src, (size_t)p * TE + o, staged);
       s_scratch[part * TE + o] = s0 + s1;
     }
     __syncthreads();
@@ -464,150 +445,113 @@ __device__ void route_if_last(const Dec2Args &a, const LayerPtrs &lp, uint8_t *s
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  COLI_TRACE_POINT(a.layer, kTpRouteStart);
   route_finish(a, lp, smem);
   if (threadIdx.x == 0) a.ctrl[kCtrlRouterTicket] = 0;
 }
 
 // ---------------------------------------------------------------------------
-// gate/up phase: each compute warp owns one 1024-column chunk (cg) of every
-// row congruent to rg modulo nrg within the CTA's row range, issues the loads
-// of kGuBatch rows before computing any of them, and leaves per-row partial
-// sums in shared memory; after one barrier the block finalises
-// h = silu(g) * u * gate and writes it to every replica.  The union lists are
-// already in shared memory.
+// gate/up: the CTA owns a contiguous range of rows in the flattened (used
+// expert, f) space; a row is gate row f and up row f of that expert.  Work is
+// cut into tasks of (4-row group, 1024-column chunk).  Each warp runs its
+// tasks (a round robin over the warps) through a private multi-stage
+// cp.async pipeline, gu_slots - 1 tasks ahead: lane l copies the 16-byte
+// slice of each of the 8 rows that it consumes, and the warp copies the 8
+// rows' scales of the chunk, so tens of KB per SM stay in flight without
+// holding registers.  Partial sums per (row, token, chunk) go to shared
+// memory; rows are finalised in batches of gu_rows into h = silu(g) * u *
+// gate, written to every replica.
 
-constexpr int kGuBatch = 4;
+// slot: weights [8 rows][32 lanes][16 B] | scales [8 rows][32] f32
+constexpr int kGuSlotBytes = 8 * 32 * 16 + 8 * 32 * 4;
 
-__device__ void gu_phase(const Dec2Args &a, const LayerPtrs &lp, const int *s_act,
-                         const int *s_routes, const float *s_slot_gate, float *red,
-                         uint32_t *s_xpl) {
-  const int T = a.T, H = a.H, F = a.F, E = a.E, S = a.S, k = a.k, KS = k + S;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int *s_act_expert = s_act + 1;
-  const int *s_act_off = s_act + 1 + (E + S);
-  const int n_active = s_act[0];
-  const int G = gridDim.x, c = blockIdx.x;
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_dyn(int n) {
+  switch (n) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    default: cp_async_wait<3>(); break;
+  }
+}
+
+// Position of a warp's task in its row batch, stepped without divisions:
+// task l = warp + i * NW is (4-row group g = l / ncg, chunk cg = l % ncg);
+// the group's first row is expert ai, row f (f a multiple of 4).
+struct GuTask {
+  int g, cg, ai, f;
+  __device__ __forceinline__ void init(int l, int ncg, int gr_base, int F) {
+    g = l / ncg;
+    cg = l - g * ncg;
+    const int gr = gr_base + 4 * g;
+    ai = gr / F;
+    f = gr - ai * F;
+  }
+  __device__ __forceinline__ void next(int dg, int dcg, int ncg, int F) {
+    int d = dg;
+    cg += dcg;
+    if (cg >= ncg) { cg -= ncg; ++d; }
+    g += d;
+    f += 4 * d;
+    while (f >= F) { f -= F; ++ai; }
+  }
+};
+
+// Issue the copies of one task into `slot`.
+__device__ __forceinline__ void gu_copy(const Dec2Args &a, const LayerPtrs &lp,
+                                        const int *s_act_expert, uint8_t *slot, const GuTask &k,
+                                        bool vec_scales) {
+  const int H = a.H, F = a.F, lane = threadIdx.x & 31;
   const int64_t rb = H / 2, ngr = H / kGroup;
-  // L2 prefetch of the down rows that this CTA index will need in the down phase
-  if (warp == 0 && c < a.n_part) {
-    const int UH = H / 4;
-    const int dh0 = 4 * part_lo(c, UH, a.n_part), dh1 = 4 * part_lo(c + 1, UH, a.n_part);
-    for (int q = lane; q < n_active && dh1 > dh0; q += 32) {
-      const int e = s_act_expert[q];
-      prefetch_l2(lp.packed + (int64_t)e * a.eb + (int64_t)F * H + (int64_t)dh0 * (F / 2),
-                  (uint32_t)((dh1 - dh0) * (F / 2)));
-      prefetch_l2(lp.scales + (int64_t)e * a.es + (int64_t)2 * F * ngr + (int64_t)dh0 * (F / kGroup),
-                  (uint32_t)((dh1 - dh0) * (F / 16)));
+  const int e = s_act_expert[k.ai];
+  const int col = k.cg * kChunkCols + 32 * lane;
+  const uint8_t *pg = lp.packed + (int64_t)e * a.eb + (int64_t)k.f * rb;
+  const float *ps = lp.scales + (int64_t)e * a.es + (int64_t)k.f * ngr + k.cg * 16;
+  float *ss = (float *)(slot + 8 * 32 * 16);
+  if (col < H) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      cp_async16(slot + ((2 * b) * 32 + lane) * 16, pg + b * rb + col / 2);
+      cp_async16(slot + ((2 * b + 1) * 32 + lane) * 16, pg + (int64_t)F * rb + b * rb + col / 2);
     }
   }
-  // this CTA's rows in the flattened (used expert, row) space, units of 4 rows
-  const int U = n_active * (F / 4);
-  const int row0 = 4 * part_lo(c, U, G), nrows = 4 * part_lo(c + 1, U, G) - row0;
-  const float *xr = lp.xrep + (size_t)(c % a.n_rep) * a.x_stride;
-  const int nbx = H / 32;
-  if (a.gu_xpl) {
-    build_planes(xr, T, H, s_xpl, nbx);
-    __syncthreads();
+  if (vec_scales) {
+    // 16 groups of the chunk for 8 rows: lane l copies row l / 4, groups 4 (l % 4) .. + 3
+    const int q = lane >> 2, b = q >> 1, m = q & 1, gq = 4 * (lane & 3);
+    if (k.cg * 16 + gq < ngr)
+      cp_async16(ss + q * 16 + gq, ps + (m ? (int64_t)F * ngr : 0) + b * ngr + gq);
+  } else if (col < H) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      cp_async4(ss + (2 * b) * 32 + lane, ps + b * ngr + lane / 2);
+      cp_async4(ss + (2 * b + 1) * 32 + lane, ps + (int64_t)F * ngr + b * ngr + lane / 2);
+    }
   }
-  if (tid == 0) COLI_TRACE_POINT(0, 4);
+}
 
-  const int ncg = a.gu_ncg, nrg = a.gu_nrg;
-  if (warp < ncg * nrg) {
-    const int cg = warp % ncg, rg = warp / ncg;
-    const int col = cg * kChunkCols + 32 * lane;
-    const bool act = col < H;
-    const int nq = nrows > rg ? (nrows - rg + nrg - 1) / nrg : 0;
-    Planes pl;
-    int pl_tok = -1;
-    for (int q0 = 0; q0 < nq; q0 += kGuBatch) {
-      uint4 wg[kGuBatch], wu[kGuBatch];
-      float sg[kGuBatch], su[kGuBatch];
-      int ra[kGuBatch];   // used-expert index of each row (-1: none)
+__device__ __forceinline__ void gu_slot_values(const uint8_t *slot, bool act, bool vec_scales,
+                                               uint4 (&w)[8], float (&sc)[8]) {
+  const int lane = threadIdx.x & 31;
+  const float *ss = (const float *)(slot + 8 * 32 * 16);
 #pragma unroll
-      for (int b = 0; b < kGuBatch; ++b) {
-        ra[b] = -1;
-        const int q = q0 + b;
-        if (q < nq) {
-          const int gr = row0 + rg + q * nrg;
-          const int ai = gr / F, f = gr - ai * F;
-          ra[b] = ai;
-          if (act) {
-            const int e = s_act_expert[ai];
-            const uint8_t *pg = lp.packed + (int64_t)e * a.eb + (int64_t)f * rb + col / 2;
-            const float *pgs = lp.scales + (int64_t)e * a.es + (int64_t)f * ngr + col / kGroup;
-            wg[b] = ldg_stream(pg);
-            wu[b] = ldg_stream(pg + (int64_t)F * rb);
-            sg[b] = __ldg(pgs);
-            su[b] = __ldg(pgs + (int64_t)F * ngr);
-          }
-        }
-      }
-      if (q0 == 0 && tid == 0) COLI_TRACE_POINT(0, 5);
-      int maxtok = 0;
-#pragma unroll
-      for (int b = 0; b < kGuBatch; ++b)
-        if (ra[b] >= 0) {
-          const int nt = s_act_off[ra[b] + 1] - s_act_off[ra[b]];
-          maxtok = nt > maxtok ? nt : maxtok;
-        }
-      for (int j = 0; j < maxtok; ++j) {
-        float v[8];
-#pragma unroll
-        for (int b = 0; b < kGuBatch; ++b) {
-          v[2 * b] = 0.0f;
-          v[2 * b + 1] = 0.0f;
-          if (ra[b] >= 0) {
-            const int j0 = s_act_off[ra[b]], nt = s_act_off[ra[b] + 1] - j0;
-            if (j < nt && act) {
-              const int t = s_routes[j0 + j] / KS;
-              if (t != pl_tok) {
-                if (a.gu_xpl) {
-                  load_planes(s_xpl, t, col / 32, nbx, pl);
-                } else {
-                  float xv[32];
-                  load32<float>(xr + (int64_t)t * H + col, xv);
-                  quantize32(xv, pl);
-                }
-                pl_tok = t;
-              }
-              v[2 * b] = sg[b] * dot32(wg[b], pl);
-              v[2 * b + 1] = su[b] * dot32(wu[b], pl);
-            }
-          }
-        }
-        const float tot = reduce8(v);
-        if ((lane & 3) == 0) {
-          const int vi = lane >> 2, b = vi >> 1;
-          if (ra[b] >= 0) {
-            const int nt = s_act_off[ra[b] + 1] - s_act_off[ra[b]];
-            if (j < nt) {
-              const int i = rg + (q0 + b) * nrg;
-              red[((i * T + j) * ncg + cg) * 2 + (vi & 1)] = tot;
-            }
-          }
-        }
-      }
-    }
+  for (int q = 0; q < 8; ++q) {
+    w[q] = act ? *(const uint4 *)(slot + (q * 32 + lane) * 16) : make_uint4(0, 0, 0, 0);
+    sc[q] = act ? (vec_scales ? ss[q * 16 + (lane >> 1)] : ss[q * 32 + lane]) : 0.0f;
   }
-  __syncthreads();
-  if (tid == 0) COLI_TRACE_POINT(0, 6);
-  // finalise h for every (row, token) of this CTA
-  for (int it = tid; it < nrows * T; it += blockDim.x) {
-    const int i = it / T, j = it - i * T;
-    const int gr = row0 + i;
-    const int ai = gr / F, f = gr - ai * F;
-    const int j0 = s_act_off[ai], nt = s_act_off[ai + 1] - j0;
-    if (j >= nt) continue;
-    float g = 0.0f, u = 0.0f;
-    for (int q = 0; q < ncg; ++q) {
-      g += red[((i * T + j) * ncg + q) * 2];
-      u += red[((i * T + j) * ncg + q) * 2 + 1];
-    }
-    const int slot_id = s_routes[j0 + j];
-    const float hv = silu(g) * u * s_slot_gate[slot_id];
-    for (int rr = 0; rr < a.n_rep; ++rr) a.h[rr * a.h_stride + (int64_t)slot_id * F + f] = hv;
-  }
-  if (tid == 0) COLI_TRACE_POINT(0, 7);
 }
 
 // Union lists published by the routing CTA, into shared memory.
@@ -621,122 +565,313 @@ __device__ void load_lists(const Dec2Args &a, int *s_act, int *s_routes, float *
   __syncthreads();
 }
 
+// kOne: one token per call (every used expert serves token 0): the planes of
+// the warp's chunk stay in registers and the token loop disappears.
+template <bool kOne>
 __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const GuSmem &L = a.gu;
-  grid_dependents_launch();
-  grid_dependency_wait();
-  COLI_TRACE_POINT(0, 1);
+  COLI_TRACE_POINT(a.layer, kTpGuEntry);
   int *s_act = (int *)(smem + L.act);
   int *s_routes = (int *)(smem + L.routes);
   float *s_slot_gate = (float *)(smem + L.slot_gate);
-  load_lists(a, s_act, s_routes, s_slot_gate);
-  if (threadIdx.x == 0) COLI_TRACE_POINT(0, 3);
-  gu_phase(a, layer_ptrs(a), s_act, s_routes, s_slot_gate, (float *)(smem + L.red),
-           (uint32_t *)(smem + L.xpl));
+  uint32_t *s_xpl = (uint32_t *)(smem + L.xpl);
+  float *red = (float *)(smem + L.red);
+  grid_dependents_launch();
+  grid_dependency_wait();
+  COLI_TRACE_POINT(a.layer, kTpGuDepWait);
+  load_lists(a, s_act, s_routes, s_slot_gate);   // ends with __syncthreads
+  COLI_TRACE_POINT(a.layer, kTpGuLists);
+  const LayerPtrs lp = layer_ptrs(a);
+  const int T = a.T, H = a.H, F = a.F, KS = a.k + a.S;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, NW = blockDim.x >> 5;
+  const int n_active = s_act[0];
+  const int *s_act_expert = s_act + 1;
+  const int *s_act_off = s_act + 1 + (a.E + a.S);
+  const int G = gridDim.x, c = blockIdx.x;
+  const int U = n_active * (F / 4);
+  const int row0 = 4 * part_lo(c, U, G), nrows = 4 * part_lo(c + 1, U, G) - row0;
+  const float *xr = lp.xrep + (size_t)(c % a.n_rep) * a.x_stride;
+  const int ncg = a.gu_ncg, S = a.gu_slots, nbx = H / 32;
+  const int dg = NW / ncg, dcg = NW - dg * ncg;
+  const bool vec_scales = (H % 256) == 0;
+  uint8_t *ring = smem + L.ring + (size_t)warp * S * kGuSlotBytes;
+
+  for (int rb0 = 0; rb0 < nrows; rb0 += a.gu_rows) {
+    const int nrb = nrows - rb0 < a.gu_rows ? nrows - rb0 : a.gu_rows;
+    const int n_tasks = (nrb / 4) * ncg;
+    const int my_tasks = n_tasks > warp ? (n_tasks - warp + NW - 1) / NW : 0;
+    GuTask ci, cc;      // the next task to copy, the next task to compute
+    ci.init(warp, ncg, row0 + rb0, F);
+    cc = ci;
+    if (rb0 == 0) {
+      // L2 prefetch of the down rows that this CTA index reads in the down kernel
+      if (warp == 0 && c < a.n_part) {
+        const int64_t ngr = H / kGroup;
+        const int UH = H / 4;
+        const int dh0 = 4 * part_lo(c, UH, a.n_part), dh1 = 4 * part_lo(c + 1, UH, a.n_part);
+        for (int q = lane; q < n_active && dh1 > dh0; q += 32) {
+          const int e = s_act_expert[q];
+          prefetch_l2(lp.packed + (int64_t)e * a.eb + (int64_t)F * H + (int64_t)dh0 * (F / 2),
+                      (uint32_t)((dh1 - dh0) * (F / 2)));
+          prefetch_l2(lp.scales + (int64_t)e * a.es + (int64_t)2 * F * ngr +
+                          (int64_t)dh0 * (F / kGroup),
+                      (uint32_t)((dh1 - dh0) * (F / 16)));
+        }
+      }
+      if (a.gu_xpl) {
+        build_planes_impl(xr, T, H, nullptr, s_xpl, nbx, warp, NW);
+        __syncthreads();
+      }
+      COLI_TRACE_POINT(a.layer, kTpGuPlanes);
+    }
+    // prologue: the first S - 1 tasks of this warp in flight
+    for (int p = 0; p < S - 1; ++p) {
+      if (p < my_tasks) {
+        gu_copy(a, lp, s_act_expert, ring + (size_t)p * kGuSlotBytes, ci, vec_scales);
+        ci.next(dg, dcg, ncg, F);
+      }
+      cp_async_commit();
+    }
+    if (rb0 == 0) COLI_TRACE_POINT(a.layer, kTpGuFirstLoads);
+    Planes pl;
+    int pl_key = -1;            // (token, chunk) whose planes are in `pl`
+    for (int i = 0; i < my_tasks; ++i) {
+      if (i + S - 1 < my_tasks) {
+        gu_copy(a, lp, s_act_expert, ring + (size_t)((i + S - 1) % S) * kGuSlotBytes, ci,
+                vec_scales);
+        ci.next(dg, dcg, ncg, F);
+      }
+      cp_async_commit();
+      cp_async_wait_dyn(S - 1);      // this lane's copies of task i have landed
+      if (vec_scales) __syncwarp();  // scales were copied by other lanes
+      const uint8_t *slot = ring + (size_t)(i % S) * kGuSlotBytes;
+      const int col = cc.cg * kChunkCols + 32 * lane;
+      const bool act = col < H;
+      uint4 w[8];
+      float sc[8];
+      gu_slot_values(slot, act, vec_scales, w, sc);
+      const int j0 = s_act_off[cc.ai];
+      const int nt = kOne ? 1 : s_act_off[cc.ai + 1] - j0;
+      for (int j = 0; j < nt; ++j) {
+        const int t = kOne ? 0 : s_routes[j0 + j] / KS;
+        float v[8];
+        if (act) {
+          const int key = t * ncg + cc.cg;
+          if (key != pl_key) {
+            if (a.gu_xpl) {
+              load_planes(s_xpl, t, col / 32, nbx, pl);
+            } else {
+              float xv[32];
+              load32<float>(xr + (int64_t)t * H + col, xv);
+              quantize32(xv, pl);
+            }
+            pl_key = key;
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) v[q] = sc[q] * dot32(w[q], pl);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) v[q] = 0.0f;
+        }
+        const float tot = reduce8(v);    // lane 4 vi: value vi = 2 * row + (0 gate | 1 up)
+        if ((lane & 3) == 0) {
+          const int vi = lane >> 2;
+          red[(((4 * cc.g + (vi >> 1)) * T + j) * ncg + cc.cg) * 2 + (vi & 1)] = tot;
+        }
+      }
+      __syncwarp();                  // the slot is refilled by the next iteration's copy
+      cc.next(dg, dcg, ncg, F);
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+    if (rb0 == 0) COLI_TRACE_POINT(a.layer, kTpGuCompute);
+    // finalise h for every (row, token) of this batch
+    for (int it = tid; it < nrb * T; it += blockDim.x) {
+      const int i = it / T, j = it - i * T;
+      const int gr = row0 + rb0 + i;
+      const int ai = gr / F, f = gr - ai * F;
+      const int j0 = s_act_off[ai], nt = s_act_off[ai + 1] - j0;
+      if (j >= nt) continue;
+      float gs = 0.0f, us = 0.0f;
+      for (int q = 0; q < ncg; ++q) {
+        gs += red[((i * T + j) * ncg + q) * 2];
+        us += red[((i * T + j) * ncg + q) * 2 + 1];
+      }
+      const int slot_id = s_routes[j0 + j];
+      const float hv = silu(gs) * us * s_slot_gate[slot_id];
+      for (int rr = 0; rr < a.n_rep; ++rr) a.h[rr * a.h_stride + (int64_t)slot_id * F + f] = hv;
+    }
+    __syncthreads();
+  }
+  COLI_TRACE_POINT(a.layer, kTpGuEnd);
 }
 
 // ---------------------------------------------------------------------------
-// down phase: each CTA owns a block of output rows; a warp owns one
-// 1024-column chunk (cg) of its rows and walks the used experts in ascending
-// order (8 experts' loads in flight), adding each slot's contribution into
-// per-token registers.  Writes out (with the residual), layer_out, the x
-// replicas, and leaves the new residual-stream rows in s_xn [T][nr].
+// down: each CTA owns output rows [dh0, dh1) of every used expert's down
+// matrix.  Work is cut into tasks of (expert, 8-row group, 1024-column chunk)
+// that run, like the gate/up tasks, through each warp's cp.async pipeline
+// (the same slot layout: 8 rows x 16 bytes per lane, plus scales).  Experts
+// are taken in batches whose slots' activation planes fit in shared memory;
+// a task leaves the partial sum of each (row, token, chunk) in the batch's
+// reduction area, and after the batch every (row, token) adds its experts'
+// and chunks' partial sums, in a fixed order, to its accumulator.  The
+// combine then writes out (with the residual), layer_out, the x replicas,
+// and leaves the new residual-stream rows in s_xn [T][nr].
 
-constexpr int kDnBatch = 8;
+struct DnTask {
+  int a, gi, cg;     // expert (index into the used list), 8-row group, chunk
+  __device__ __forceinline__ void init(int l, int ncg, int gpe, int ga) {
+    const int u = l / ncg;
+    cg = l - u * ncg;
+    a = ga + u / gpe;
+    gi = u - (a - ga) * gpe;
+  }
+  __device__ __forceinline__ void next(int du, int dcg, int ncg, int gpe) {
+    int d = du;
+    cg += dcg;
+    if (cg >= ncg) { cg -= ncg; ++d; }
+    gi += d;
+    while (gi >= gpe) { gi -= gpe; ++a; }
+  }
+};
 
-template <int TM>   // TM >= a.T: per-token accumulators held in registers
+__device__ __forceinline__ void dn_copy(const Dec2Args &a, const LayerPtrs &lp,
+                                        const int *s_act_expert, uint8_t *slot, const DnTask &k,
+                                        int dh0, int nr, bool vec_scales) {
+  const int H = a.H, F = a.F, lane = threadIdx.x & 31;
+  const int64_t rb = F / 2, ngr = F / kGroup;
+  const int e = s_act_expert[k.a];
+  const int col = k.cg * kChunkCols + 32 * lane;
+  const int r0 = 8 * k.gi, nq = nr - r0 < 8 ? nr - r0 : 8;
+  const uint8_t *pw = lp.packed + (int64_t)e * a.eb + (int64_t)F * H + (int64_t)(dh0 + r0) * rb;
+  const float *ps = lp.scales + (int64_t)e * a.es + (int64_t)2 * F * (H / kGroup) +
+                    (int64_t)(dh0 + r0) * ngr + k.cg * 16;
+  float *ss = (float *)(slot + 8 * 32 * 16);
+  if (col < F) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (q < nq) cp_async16(slot + (q * 32 + lane) * 16, pw + q * rb + col / 2);
+  }
+  if (vec_scales) {
+    const int q = lane >> 2, gq = 4 * (lane & 3);
+    if (q < nq && k.cg * 16 + gq < ngr) cp_async16(ss + q * 16 + gq, ps + q * ngr + gq);
+  } else if (col < F) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (q < nq) cp_async4(ss + q * 32 + lane, ps + q * ngr + lane / 2);
+  }
+}
+
+template <bool kOne>
 __device__ void dn_phase(const Dec2Args &a, const LayerPtrs &lp, const int *s_act,
-                         const int *s_routes, float *red, uint32_t *s_planes, float *s_xn,
-                         const float *residual) {
-  const int T = a.T, H = a.H, F = a.F, E = a.E, S = a.S, k = a.k, KS = k + S;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+                         const int *s_routes, uint8_t *smem, float *s_xn, const float *residual) {
+  const DnSmem &L = a.dn;
+  const int T = a.T, H = a.H, F = a.F, E = a.E, S = a.S, KS = a.k + S;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, NW = blockDim.x >> 5;
   const int G = gridDim.x, c = blockIdx.x;
   const int UH = H / 4;
   const int dh0 = 4 * part_lo(c, UH, G), dh1 = 4 * part_lo(c + 1, UH, G);
   const int nr = dh1 - dh0;
   const int *s_act_expert = s_act + 1;
   const int *s_act_off = s_act + 1 + (E + S);
-  const int ncg = a.dn_ncg, nrg = a.dn_nrg;
-  for (int i = tid; i < nr * T * ncg; i += blockDim.x) red[i] = 0.0f;
   const int n_active = s_act[0];
   const float *h_rep = a.h + (size_t)(c % a.n_rep) * a.h_stride;
-  const int64_t rb = F / 2, ngr = F / kGroup;
-  const int64_t down_b = (int64_t)F * H, down_s = (int64_t)2 * F * (H / kGroup);
-  const int nbp = F / 32;
-  const int cap = a.dn_slots;     // slots whose planes fit in shared memory at once
-  const int cg = warp % ncg, rg = warp / ncg;
-  const int col = cg * kChunkCols + 32 * lane;
-  const bool act = col < F;
-  const bool worker = warp < ncg * nrg;
-  // experts in groups whose slots' planes fit; groups run in ascending order
+  const int ncg = a.dn_ncg, Sl = a.dn_slots_pipe, nbp = F / 32;
+  const int gpe = (nr + 7) / 8;                  // 8-row groups per expert
+  const int du = NW / ncg, dcg = NW - du * ncg;
+  const bool vec_scales = (F % 256) == 0;
+  float *acc = (float *)(smem + L.acc);          // [nr][T]
+  float *red = (float *)(smem + L.red);          // [batch expert][nr][T][ncg]
+  uint32_t *s_planes = (uint32_t *)(smem + L.planes);
+  uint8_t *ring = smem + L.ring + (size_t)warp * Sl * kGuSlotBytes;
+  for (int i = tid; i < nr * T; i += blockDim.x) acc[i] = 0.0f;
+  // experts in batches: their slots' planes and their partial sums must fit
   for (int ga = 0; ga < n_active;) {
     int gb = ga;
-    while (gb < n_active && s_act_off[gb + 1] - s_act_off[ga] <= cap) ++gb;
-    if (gb == ga) gb = ga + 1;   // cap >= T, so a single expert always fits
+    while (gb < n_active && gb - ga < a.dn_batch && s_act_off[gb + 1] - s_act_off[ga] <= a.dn_slots)
+      ++gb;
+    if (gb == ga) gb = ga + 1;   // the plan guarantees one expert's tokens fit
     const int p0 = s_act_off[ga], np = s_act_off[gb] - p0;
+    const int n_tasks = (gb - ga) * gpe * ncg;
+    const int my_tasks = n_tasks > warp ? (n_tasks - warp + NW - 1) / NW : 0;
+    DnTask ci, cc;
+    if (my_tasks) ci.init(warp, ncg, gpe, ga);
+    cc = ci;
+    for (int i = tid; i < (gb - ga) * nr * T * ncg; i += blockDim.x) red[i] = 0.0f;
     build_planes_list(h_rep, F, s_routes + p0, np, s_planes, nbp);
     __syncthreads();
-    if (ga == 0 && tid == 0) COLI_TRACE_POINT(1, 2);
-    if (worker) {
-      for (int r = rg; r < nr; r += nrg) {
-        float acc[TM];
-#pragma unroll
-        for (int t = 0; t < TM; ++t) acc[t] = 0.0f;
-        for (int a0 = ga; a0 < gb; a0 += kDnBatch) {
-          uint4 w[kDnBatch];
-          float sc[kDnBatch];
-#pragma unroll
-          for (int b = 0; b < kDnBatch; ++b)
-            if (a0 + b < gb && act) {
-              const int e = s_act_expert[a0 + b];
-              w[b] = ldg_stream(lp.packed + (int64_t)e * a.eb + down_b + (int64_t)(dh0 + r) * rb +
-                                col / 2);
-              sc[b] = __ldg(lp.scales + (int64_t)e * a.es + down_s + (int64_t)(dh0 + r) * ngr +
-                            col / kGroup);
-            }
-#pragma unroll
-          for (int b = 0; b < kDnBatch; ++b) {
-            if (a0 + b >= gb) break;
-            if (!act) continue;
-            const int j0 = s_act_off[a0 + b], nt = s_act_off[a0 + b + 1] - j0;
-            for (int j = 0; j < nt; ++j) {
-              Planes pl;
-              load_planes(s_planes, j0 + j - p0, col / 32, nbp, pl);
-              const float v = sc[b] * dot32(w[b], pl);
-              const int t = s_routes[j0 + j] / KS;
-#pragma unroll
-              for (int tt = 0; tt < TM; ++tt)
-                if (tt == t) acc[tt] += v;
-            }
+    if (ga == 0) COLI_TRACE_POINT(a.layer, kTpDnPlanes);
+    for (int p = 0; p < Sl - 1; ++p) {
+      if (p < my_tasks) {
+        dn_copy(a, lp, s_act_expert, ring + (size_t)p * kGuSlotBytes, ci, dh0, nr, vec_scales);
+        ci.next(du, dcg, ncg, gpe);
+      }
+      cp_async_commit();
+    }
+    Planes pl;
+    int pl_key = -1;
+    for (int i = 0; i < my_tasks; ++i) {
+      if (i + Sl - 1 < my_tasks) {
+        dn_copy(a, lp, s_act_expert, ring + (size_t)((i + Sl - 1) % Sl) * kGuSlotBytes, ci, dh0,
+                nr, vec_scales);
+        ci.next(du, dcg, ncg, gpe);
+      }
+      cp_async_commit();
+      cp_async_wait_dyn(Sl - 1);
+      if (vec_scales) __syncwarp();
+      const uint8_t *slot = ring + (size_t)(i % Sl) * kGuSlotBytes;
+      const int col = cc.cg * kChunkCols + 32 * lane;
+      const bool act = col < F;
+      const int r0 = 8 * cc.gi, nq = nr - r0 < 8 ? nr - r0 : 8;
+      uint4 w[8];
+      float sc[8];
+      gu_slot_values(slot, act, vec_scales, w, sc);
+      const int j0 = s_act_off[cc.a];
+      const int nt = kOne ? 1 : s_act_off[cc.a + 1] - j0;
+      for (int j = 0; j < nt; ++j) {
+        const int t = kOne ? 0 : s_routes[j0 + j] / KS;
+        float v[8];
+        if (act) {
+          const int key = (j0 + j) * 64 + cc.cg;
+          if (key != pl_key) {
+            load_planes(s_planes, j0 + j - p0, col / 32, nbp, pl);
+            pl_key = key;
           }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) v[q] = q < nq ? sc[q] * dot32(w[q], pl) : 0.0f;
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) v[q] = 0.0f;
         }
-        // reduce over lanes, 8 tokens at a time; the owning lane accumulates
-        for (int t0 = 0; t0 < T; t0 += 8) {
-          float v[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            v[q] = 0.0f;
-#pragma unroll
-            for (int tt = 0; tt < TM; ++tt)
-              if (tt == t0 + q) v[q] = acc[tt];
-          }
-          const float tot = reduce8(v);
-          const int t = t0 + (lane >> 2);
-          if ((lane & 3) == 0 && t < T) red[(r * T + t) * ncg + cg] += tot;
+        const float tot = reduce8(v);   // lane 4 q ends with row q
+        if ((lane & 3) == 0) {
+          const int q = lane >> 2;
+          if (q < nq)
+            red[((((cc.a - ga) * nr + r0 + q) * T + t) * ncg) + cc.cg] = tot;
         }
       }
+      __syncwarp();
+      cc.next(du, dcg, ncg, gpe);
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+    // add the batch's partial sums, experts and chunks in a fixed order
+    for (int i = tid; i < nr * T; i += blockDim.x) {
+      float s = 0.0f;
+      for (int x = 0; x < gb - ga; ++x)
+        for (int q = 0; q < ncg; ++q) s += red[((x * nr) * T + i) * ncg + q];
+      acc[i] += s;
     }
     __syncthreads();
     ga = gb;
   }
-  if (tid == 0) COLI_TRACE_POINT(1, 4);
+  COLI_TRACE_POINT(a.layer, kTpDnCompute);
   // combine is complete: residual, outputs, replicas of the new layer input
   for (int i = tid; i < T * nr; i += blockDim.x) {
     const int t = i / nr, r = i - t * nr;
     const int64_t o = (int64_t)t * H + dh0 + r;
-    float v = 0.0f;
-    for (int q = 0; q < ncg; ++q) v += red[(r * T + t) * ncg + q];
+    const float v = acc[r * T + t];
     if (lp.layer_out) lp.layer_out[o] = v;
     const float xn = residual ? residual[o] + v : v;
     lp.out[o] = xn;
@@ -778,171 +913,51 @@ __device__ void load_router_rows(const Dec2Args &a, const WT *wr, WT *s_wr) {
   }
 }
 
-template <typename WT>
+template <typename WT, bool kOne>
 __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const DnSmem &L = a.dn;
   WT *s_wr = (WT *)(smem + L.wr);
+  COLI_TRACE_POINT(a.layer, kTpDnEntry);
   // the next layer's router rows do not depend on the previous kernel
   if (a.wr) load_router_rows<WT>(a, (const WT *)a.wr, s_wr);
   grid_dependents_launch();
   grid_dependency_wait();
-  if (threadIdx.x == 0) COLI_TRACE_POINT(1, 1);
+  COLI_TRACE_POINT(a.layer, kTpDnDepWait);
   int *s_act = (int *)(smem + L.act);
   int *s_routes = (int *)(smem + L.routes);
   load_lists(a, s_act, s_routes, nullptr);
+  COLI_TRACE_POINT(a.layer, kTpDnLists);
   float *s_xn = (float *)(smem + L.xn);
   const LayerPtrs lp = layer_ptrs(a);
-  if (a.T == 1)
-    dn_phase<1>(a, lp, s_act, s_routes, (float *)(smem + L.acc), (uint32_t *)(smem + L.planes),
-                s_xn, a.residual);
-  else
-    dn_phase<kDecodeMaxT>(a, lp, s_act, s_routes, (float *)(smem + L.acc),
-                          (uint32_t *)(smem + L.planes), s_xn, a.residual);
+  dn_phase<kOne>(a, lp, s_act, s_routes, smem, s_xn, a.residual);
+  COLI_TRACE_POINT(a.layer, kTpDnCombine);
   if (a.wr) {
     dn_partials<WT>(a, a.partials, s_wr, s_xn, 1, 0);
+    COLI_TRACE_POINT(a.layer, kTpDnPartials);
     // the last CTA routes the next layer (its shared memory is free again)
     LayerPtrs rp = lp;
     rp.route_counts = a.next_counts;
     route_if_last(a, rp, smem);
   }
-  if (threadIdx.x == 0) COLI_TRACE_POINT(1, 6);
-}
-
-// ---------------------------------------------------------------------------
-// The decode stack in one persistent cooperative kernel: layer after layer,
-// every CTA routes the layer itself from its copy of the router partials,
-// runs its gate/up share, meets the grid at a barrier (h complete), runs its
-// down rows and the next layer's partials, and meets the grid again.  Code and
-// launch state stay resident across layers.  Every barrier wait is bounded.
-
-__device__ bool grid_barrier(uint32_t *ctr, uint32_t target, uint32_t *ctrl) {
-  __shared__ int s_ok;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(ctr), "r"(1u) : "memory");
-    int ok = 1;
-    uint32_t v;
-    const long long t0 = clock64();
-    for (;;) {
-      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
-      if (v >= target) break;
-      if (clock64() - t0 > kWaitCycles) {
-        ok = 0;
-        atomicOr(ctrl + kCtrlFlags, COLI_FLAG_TIMEOUT);
-        break;
-      }
-    }
-    s_ok = ok;
-  }
-  __syncthreads();
-  return s_ok != 0;
-}
-
-constexpr int kStackThreads = 384;
-
-template <typename XT, typename WT, int TM>
-__global__ void __launch_bounds__(kStackThreads) k_stack(Dec2Args a, StackArgs st) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const StkSmem &L = st.sm;
-  const int T = a.T, H = a.H, E = a.E, S = a.S, k = a.k;
-  const int tid = threadIdx.x;
-  const int G = gridDim.x, c = blockIdx.x;
-  int *s_act = (int *)(smem + L.act);
-  int *s_routes = (int *)(smem + L.routes);
-  float *s_slot_gate = (float *)(smem + L.slot_gate);
-  WT *s_wr = (WT *)(smem + L.wr);
-  uint8_t *area = smem + L.area;
-  uint32_t *bar = a.ctrl + kCtrlBarrier;
-  uint32_t nbar = 0;
-  bool ok = true;
-  // ---- layer 0: x in every replica (f32) and its router partials
-  {
-    const int UH = H / 4;
-    const int h0 = 4 * part_lo(c, UH, G), nr = 4 * part_lo(c + 1, UH, G) - h0;
-    const XT *x = (const XT *)a.x;
-    float *s_xn = (float *)area;
-    for (int i = tid; i < T * nr; i += blockDim.x) {
-      const int t = i / nr, r = i - t * nr;
-      const float v = to_f32(x[(size_t)t * H + h0 + r]);
-      s_xn[i] = v;
-      for (int rr = 0; rr < a.n_rep; ++rr) a.xrep[rr * a.x_stride + (size_t)t * H + h0 + r] = v;
-    }
-    load_router_rows<WT>(a, (const WT *)st.router, s_wr);
-    __syncthreads();
-    dn_partials<WT>(a, a.partials, s_wr, s_xn, a.n_rep, st.part_stride);
-  }
-  ok = grid_barrier(bar, ++nbar * G, a.ctrl);
-  for (int l = 0; l < st.n_layers && ok; ++l) {
-    LayerPtrs la;
-    la.packed = a.packed + (size_t)l * st.pk_stride;
-    la.scales = a.scales + (size_t)l * st.sc_stride;
-    la.route_counts = st.counts ? st.counts + (size_t)l * E : nullptr;
-    la.layer_out = st.layer_out ? st.layer_out + (size_t)l * T * H : nullptr;
-    la.partials = a.partials + (size_t)(c % a.n_rep) * st.part_stride;
-    la.out = st.x_out;
-    la.xrep = a.xrep;
-    const bool next = l + 1 < st.n_layers;
-    // the next layer's router rows: needed only in the down phase
-    if (next)
-      load_router_rows<WT>(a, (const WT *)((const uint8_t *)st.router + (size_t)(l + 1) * st.wr_stride),
-                           s_wr);
-    if (l == 3 && tid == 0) COLI_TRACE_POINT(1, 8);
-    // ---- route (every CTA from its own copy of the partials)
-    {
-      float *s_logits = (float *)area;
-      int *s_rank = (int *)(s_logits + T * E);
-      int *s_idx = s_rank + T * E;
-      float *s_gates = (float *)(s_idx + T * k);
-      float *s_vals = s_gates + T * k;
-      float *s_scratch = s_vals + T * k;
-      float *s_stage = s_scratch + kDec2MaxThreads;
-      route_block(a, la, s_logits, s_idx, s_gates, s_vals, s_rank, s_scratch, s_stage, c == 0);
-      block_union(s_idx, s_gates, T, k, S, E, s_act, s_act + 1, s_act + 1 + (E + S), s_routes,
-                  s_slot_gate, s_rank);
-    }
-    if (l == 3 && tid == 0) COLI_TRACE_POINT(1, 9);
-    // ---- gate/up
-    gu_phase(a, la, s_act, s_routes, s_slot_gate, (float *)(area + L.gu_red),
-             (uint32_t *)(area + L.gu_xpl));
-    if (l == 3 && tid == 0) COLI_TRACE_POINT(1, 10);
-    ok = grid_barrier(bar, ++nbar * G, a.ctrl);
-    if (!ok) break;
-    if (l == 3 && tid == 0) COLI_TRACE_POINT(1, 11);
-    // ---- down, residual, next layer's partials
-    float *s_xn = (float *)(area + L.dn_xn);
-    la.xrep = next ? a.xrep : nullptr;
-    dn_phase<TM>(a, la, s_act, s_routes, (float *)(area + L.dn_acc),
-                 (uint32_t *)(area + L.dn_planes), s_xn, a.xrep);   // replica 0: this layer's input
-    if (l == 3 && tid == 0) COLI_TRACE_POINT(1, 12);
-    if (next) {
-      dn_partials<WT>(a, a.partials, s_wr, s_xn, a.n_rep, st.part_stride);
-      if (l == 3 && tid == 0) COLI_TRACE_POINT(1, 13);
-      ok = grid_barrier(bar, ++nbar * G, a.ctrl);
-      if (l == 3 && tid == 0) COLI_TRACE_POINT(1, 14);
-    }
-  }
-  // the last CTA out resets the barrier counters for the next launch
-  __syncthreads();
-  if (tid == 0) {
-    const unsigned t = atomicAdd(a.ctrl + kCtrlExit, 1u);
-    if (t == (unsigned)G - 1) {
-      a.ctrl[kCtrlBarrier] = 0;
-      a.ctrl[kCtrlExit] = 0;
-    }
-  }
+  COLI_TRACE_POINT(a.layer, kTpEnd);
 }
 
 // ---------------------------------------------------------------------------
 // host side
 
 #ifdef COLI_TRACE
-extern "C" int coli_trace_read(void *points, void *stages, void *issues) {
-  if (cudaMemcpyFromSymbol(points, g_trace, sizeof(g_trace)) != cudaSuccess) return -1;
-  if (cudaMemcpyFromSymbol(stages, g_trace_stage, sizeof(g_trace_stage)) != cudaSuccess) return -1;
-  if (cudaMemcpyFromSymbol(issues, g_trace_issue, sizeof(g_trace_issue)) != cudaSuccess) return -1;
-  return 0;
+extern "C" int coli_trace_reset() {
+  static unsigned long long lo[kTraceLayers][kTracePoints];
+  for (auto &row : lo)
+    for (auto &v : row) v = ~0ull;
+  if (cudaMemcpyToSymbol(g_trace_lo, lo, sizeof(lo)) != cudaSuccess) return -1;
+  static unsigned long long hi[kTraceLayers][kTracePoints] = {};
+  return cudaMemcpyToSymbol(g_trace_hi, hi, sizeof(hi)) == cudaSuccess ? 0 : -1;
+}
+extern "C" int coli_trace_read(void *lo, void *hi) {
+  if (cudaMemcpyFromSymbol(lo, g_trace_lo, sizeof(g_trace_lo)) != cudaSuccess) return -1;
+  return cudaMemcpyFromSymbol(hi, g_trace_hi, sizeof(g_trace_hi)) == cudaSuccess ? 0 : -1;
 }
 #endif
 
@@ -1003,11 +1018,8 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
   const size_t budget = (size_t)max_smem() - 4096;
   const int G = num_sms();
   a.n_part = n_part;
-  // ---- gate/up
+  // ---- gate/up: gu_nw warps, each with a gu_slots-deep cp.async pipeline
   a.gu_ncg = (H + kChunkCols - 1) / kChunkCols;
-  a.gu_nrg = 16 / a.gu_ncg;
-  if (a.gu_nrg < 1) a.gu_nrg = 1;
-  if (a.gu_ncg * a.gu_nrg > kDec2MaxThreads / 32) return cudaErrorInvalidValue;
   const int n_used = ((E < T * k) ? E : T * k) + S;
   const int max_rows = 4 * ((n_used * (F / 4) + G - 1) / G);
   GuSmem g{};
@@ -1015,34 +1027,85 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
   g.act = o; o = al16(o + (size_t)(2 + 2 * (E + S)) * 4);
   g.routes = o; o = al16(o + (size_t)T * KS * 4);
   g.slot_gate = o; o = al16(o + (size_t)T * KS * 4);
-  g.red = o; o = al16(o + (size_t)max_rows * T * a.gu_ncg * 2 * 4);
-  if (o > budget) return cudaErrorInvalidValue;
-  const size_t xpl_bytes = (size_t)T * 18 * (H / 32) * 4;
-  a.gu_xpl = o + al16(xpl_bytes) <= budget;
-  g.xpl = o; o = al16(o + (a.gu_xpl ? xpl_bytes : 0));
-  g.total = o;
+  const size_t xpl_bytes = al16((size_t)T * 18 * (H / 32) * 4);
+  const size_t row_bytes = (size_t)T * a.gu_ncg * 2 * 4;
+  const int min_batch = max_rows < 64 ? max_rows : 64;
+  // warps x slots, by bytes in flight ahead of the compute: 12 x 3, then 16 x 2, ...
+  static const int kNw[] = {12, 16, 8, 8, 4};
+  static const int kSl[] = {3, 2, 3, 2, 2};
+  bool ok = false;
+  for (int xpl = 1; xpl >= 0 && !ok; --xpl)
+    for (int c = 0; c < 5 && !ok; ++c) {
+      const size_t ring = (size_t)kNw[c] * kSl[c] * kGuSlotBytes;
+      const size_t need = o + (xpl ? xpl_bytes : 0) + ring + 128 + (size_t)min_batch * row_bytes;
+      if (need <= budget) {
+        a.gu_xpl = xpl;
+        a.gu_nw = kNw[c];
+        a.gu_slots = kSl[c];
+        ok = true;
+      }
+    }
+  if (!ok) return cudaErrorInvalidValue;
+  g.xpl = o; o += a.gu_xpl ? xpl_bytes : 0;
+  g.ring = al128(o); o = g.ring + (size_t)a.gu_nw * a.gu_slots * kGuSlotBytes;
+  g.red = al16(o);
+  size_t fit = (budget - g.red) / row_bytes;
+  int rows = fit < (size_t)max_rows ? (int)fit : max_rows;
+  rows &= ~3;
+  if (rows < 4) return cudaErrorInvalidValue;
+  a.gu_rows = rows;
+  g.total = al16(g.red + (size_t)rows * row_bytes);
   a.gu = g;
-  // ---- down
+  // ---- down: dn_nw warps with dn_slots_pipe-deep cp.async pipelines; expert
+  // batches of at most dn_batch experts and dn_slots token slots
   a.dn_ncg = (F + kChunkCols - 1) / kChunkCols;
-  a.dn_nrg = 16 / a.dn_ncg;
-  if (a.dn_nrg < 1) a.dn_nrg = 1;
-  if (a.dn_ncg * a.dn_nrg > kDec2MaxThreads / 32) return cudaErrorInvalidValue;
   const int UH = H / 4;
   const int max_nr = 4 * ((UH + n_part - 1) / n_part);
   DnSmem d{};
   o = 0;
   d.act = o; o = al16(o + (size_t)(2 + 2 * (E + S)) * 4);
   d.routes = o; o = al16(o + (size_t)T * KS * 4);
-  d.acc = o; o = al16(o + (size_t)max_nr * T * a.dn_ncg * 4);
+  d.acc = o; o = al16(o + (size_t)max_nr * T * 4);
   d.xn = o; o = al16(o + (size_t)T * max_nr * 4);
   d.wr = o; o = al16(o + (size_t)E * max_nr * 4);
   const size_t per_slot = (size_t)18 * (F / 32) * 4;
-  size_t room = budget > o ? budget - o : 0;
-  int slots = (int)(room / per_slot);
-  if (slots > T * KS) slots = T * KS;
-  if (slots < T) return cudaErrorInvalidValue;   // one expert's tokens must fit
-  a.dn_slots = slots;
-  d.planes = o; o = al16(o + (size_t)slots * per_slot);
+  const size_t per_expert_red = (size_t)max_nr * T * a.dn_ncg * 4;
+  const int all_slots = T * KS;
+  // the largest tokens-per-expert count is T (routed) or T (shared)
+  static const int kDnNw[] = {12, 8, 16, 8, 12, 8, 4};
+  static const int kDnSl[] = {3, 4, 2, 3, 2, 2, 2};
+  bool dn_ok = false;
+  for (int pass = 0; pass < 2 && !dn_ok; ++pass)
+    for (int c = 0; c < 7 && !dn_ok; ++c) {
+      const size_t ring = (size_t)kDnNw[c] * kDnSl[c] * kGuSlotBytes;
+      const size_t base = al128(o) + ring + 128;
+      if (base >= budget) continue;
+      // pass 0: every slot's planes and every used expert's partials at once
+      const int n_exp = ((E < T * k) ? E : T * k) + S;
+      int slots = pass == 0 ? all_slots : T;
+      int batch = pass == 0 ? n_exp : 1;
+      size_t need = base + (size_t)slots * per_slot + (size_t)batch * per_expert_red;
+      if (pass == 1) {
+        // as many slots / experts as fit, in proportion
+        const size_t room = budget - base;
+        slots = (int)((room / 2) / per_slot);
+        batch = (int)((room / 2) / per_expert_red);
+        if (slots > all_slots) slots = all_slots;
+        if (batch > n_exp) batch = n_exp;
+        need = base + (size_t)slots * per_slot + (size_t)batch * per_expert_red;
+        if (slots < T || batch < 1) continue;
+      }
+      if (need > budget) continue;
+      a.dn_nw = kDnNw[c];
+      a.dn_slots_pipe = kDnSl[c];
+      a.dn_slots = slots;
+      a.dn_batch = batch;
+      dn_ok = true;
+    }
+  if (!dn_ok) return cudaErrorInvalidValue;
+  d.ring = al128(o); o = d.ring + (size_t)a.dn_nw * a.dn_slots_pipe * kGuSlotBytes;
+  d.red = al16(o); o = d.red + (size_t)a.dn_batch * per_expert_red;
+  d.planes = al16(o); o = al16(d.planes + (size_t)a.dn_slots * per_slot);
   d.total = o;
   a.dn = d;
   return cudaSuccess;
@@ -1075,89 +1138,20 @@ cudaError_t launch_route_partials(const Dec2Args &a_in, int x_bf16, int w_bf16, 
 #undef COLI_LAUNCH_ROUTE
 }
 
-cudaError_t plan_stack(Dec2Args &a, StackArgs &st) {
-  cudaError_t e = plan_decode(a, a.n_part);
-  if (e != cudaSuccess) return e;
-  // the persistent kernel runs kStackThreads threads: fewer warps per phase
-  const int nw = kStackThreads / 32;
-  a.gu_nrg = nw / a.gu_ncg;
-  a.dn_nrg = nw / a.dn_ncg;
-  if (a.gu_nrg < 1 || a.dn_nrg < 1) return cudaErrorInvalidValue;
-  const int T = a.T, H = a.H, F = a.F, E = a.E, S = a.S, k = a.k, KS = k + S;
-  const size_t budget = (size_t)max_smem() - 4096;
-  const int G = a.n_part;
-  StkSmem m{};
-  size_t o = 0;
-  m.act = o; o = al16(o + (size_t)(2 + 2 * (E + S)) * 4);
-  m.routes = o; o = al16(o + (size_t)T * KS * 4);
-  m.slot_gate = o; o = al16(o + (size_t)T * KS * 4);
-  const int UH = H / 4;
-  const int max_nr = 4 * ((UH + G - 1) / G);
-  m.wr = o; o = al16(o + (size_t)E * max_nr * 4);
-  m.area = al128(o);
-  const size_t route_b = (size_t)(2 * T * E + 3 * T * k + kDec2MaxThreads + (size_t)G * T * E) * 4;
-  const int n_used = ((E < T * k) ? E : T * k) + S;
-  const int max_rows = 4 * ((n_used * (F / 4) + G - 1) / G);
-  size_t go = 0;
-  m.gu_red = go; go = al16(go + (size_t)max_rows * T * a.gu_ncg * 2 * 4);
-  m.gu_xpl = go; go = al16(go + (a.gu_xpl ? (size_t)T * 18 * (H / 32) * 4 : 0));
-  size_t dof = 0;
-  m.dn_acc = dof; dof = al16(dof + (size_t)max_nr * T * a.dn_ncg * 4);
-  m.dn_xn = dof; dof = al16(dof + (size_t)T * max_nr * 4);
-  m.dn_planes = dof;
-  size_t area = route_b > go ? route_b : go;
-  if (dof > area) area = dof;
-  if (m.area + area > budget) return cudaErrorInvalidValue;
-  const size_t per_slot = (size_t)18 * (F / 32) * 4;
-  int slots = (int)((budget - m.area - dof) / per_slot);
-  if (slots > T * KS) slots = T * KS;
-  if (slots < T) return cudaErrorInvalidValue;
-  a.dn_slots = slots;
-  const size_t dn_b = dof + (size_t)slots * per_slot;
-  if (dn_b > area) area = dn_b;
-  m.total = al16(m.area + area);
-  st.sm = m;
-  return cudaSuccess;
-}
-
-cudaError_t launch_stack(const Dec2Args &a, const StackArgs &st, int x_bf16, int wr_bf16,
-                         cudaStream_t s) {
-  const int threads = kStackThreads;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.n_part);
-  cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = st.sm.total;
-  cfg.stream = s;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeCooperative;
-  at[0].val.cooperative = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  cudaError_t e;
-#define COLI_LAUNCH_STACK(XT, WT)                                                        \
-  if (a.T == 1) {                                                                         \
-    if ((e = allow_smem(k_stack<XT, WT, 1>, st.sm.total)) != cudaSuccess) return e;       \
-    return cudaLaunchKernelEx(&cfg, k_stack<XT, WT, 1>, a, st);                            \
-  }                                                                                       \
-  if ((e = allow_smem(k_stack<XT, WT, kDecodeMaxT>, st.sm.total)) != cudaSuccess) return e; \
-  return cudaLaunchKernelEx(&cfg, k_stack<XT, WT, kDecodeMaxT>, a, st);
-  if (!x_bf16 && !wr_bf16) { COLI_LAUNCH_STACK(float, float) }
-  if (!x_bf16 && wr_bf16) { COLI_LAUNCH_STACK(float, __nv_bfloat16) }
-  if (x_bf16 && !wr_bf16) { COLI_LAUNCH_STACK(__nv_bfloat16, float) }
-  COLI_LAUNCH_STACK(__nv_bfloat16, __nv_bfloat16)
-#undef COLI_LAUNCH_STACK
-}
-
 cudaError_t launch_gateup(const Dec2Args &a, int grid, cudaStream_t s, bool pdl) {
-  const int threads = a.gu_ncg * a.gu_nrg * 32;
-  cudaError_t e = allow_smem(k_gateup, a.gu.total);
-  if (e != cudaSuccess) return e;
-  return launch(k_gateup, grid, threads, a.gu.total, s, pdl, a);
+  const int threads = 32 * a.gu_nw;
+  cudaError_t e;
+  if (a.T == 1) {
+    if ((e = allow_smem(k_gateup<true>, a.gu.total)) != cudaSuccess) return e;
+    return launch(k_gateup<true>, grid, threads, a.gu.total, s, pdl, a);
+  }
+  if ((e = allow_smem(k_gateup<false>, a.gu.total)) != cudaSuccess) return e;
+  return launch(k_gateup<false>, grid, threads, a.gu.total, s, pdl, a);
 }
 
 cudaError_t launch_down(const Dec2Args &a_in, int wr_bf16, cudaStream_t s, bool pdl) {
   Dec2Args a = a_in;
-  const int threads = a.dn_ncg * a.dn_nrg * 32;
+  const int threads = a.dn_nw * 32;
   size_t smem = a.dn.total;
   if (a.wr) {
     bool stage = false;
@@ -1166,12 +1160,14 @@ cudaError_t launch_down(const Dec2Args &a_in, int wr_bf16, cudaStream_t s, bool 
     if (rs > smem) smem = rs;
   }
   cudaError_t e;
-  if (wr_bf16) {
-    if ((e = allow_smem(k_down<__nv_bfloat16>, smem)) != cudaSuccess) return e;
-    return launch(k_down<__nv_bfloat16>, a.n_part, threads, smem, s, pdl, a);
-  }
-  if ((e = allow_smem(k_down<float>, smem)) != cudaSuccess) return e;
-  return launch(k_down<float>, a.n_part, threads, smem, s, pdl, a);
+#define COLI_LAUNCH_DOWN(WT, ONE)                                                        \
+  if ((e = allow_smem(k_down<WT, ONE>, smem)) != cudaSuccess) return e;                  \
+  return launch(k_down<WT, ONE>, a.n_part, threads, smem, s, pdl, a);
+  if (wr_bf16 && a.T == 1) { COLI_LAUNCH_DOWN(__nv_bfloat16, true) }
+  if (wr_bf16) { COLI_LAUNCH_DOWN(__nv_bfloat16, false) }
+  if (a.T == 1) { COLI_LAUNCH_DOWN(float, true) }
+  COLI_LAUNCH_DOWN(float, false)
+#undef COLI_LAUNCH_DOWN
 }
 
 }  // namespace coli

@@ -24,12 +24,14 @@ void *g_scratch_ptr[kMaxDevices] = {};
 // with that device current, and cached.
 int scratch_address(void **out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return COLI_ECUDA;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return coli::cuda_status(e);
   if (dev < 0 || dev >= kMaxDevices) return COLI_EUNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
   if (!g_scratch_ptr[dev]) {
     void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_coli_scratch) != cudaSuccess || !p) return COLI_ECUDA;
+    e = cudaGetSymbolAddress(&p, g_coli_scratch);
+    if (e != cudaSuccess || !p) return coli::cuda_status(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
     g_scratch_ptr[dev] = p;
   }
   *out = g_scratch_ptr[dev];
@@ -51,8 +53,8 @@ extern "C" int coli_moe_forward_noalloc(const coli_moe_desc *d, int top_k, const
   if (st != COLI_OK) return st;
   // The control words (flags, completion ticket) must start at zero; the
   // array keeps whatever the previous call left.
-  if (cudaMemsetAsync(ws, 0, coli::kCtrlWords * sizeof(uint32_t), stream) != cudaSuccess)
-    return COLI_ECUDA;
+  const cudaError_t e = cudaMemsetAsync(ws, 0, coli::kCtrlWords * sizeof(uint32_t), stream);
+  if (e != cudaSuccess) return coli::cuda_status(e);
   return coli_moe_forward(d, top_k, x, router_w, packed_experts, scales, out, route_counts, ws,
                           kNoAllocScratchBytes, stream);
 }

@@ -33,12 +33,21 @@ class MoEShape:
     router_dtype: str  # "f32" | "bf16"
     x_dtype: str       # "f32" | "bf16"
     steps: int = 1     # sequential decode steps (fresh input each)
+    # decode stacks: layer l > 0 takes x_l + MoE_l(x_l) of the layer before
+    # (True), or its own fresh N(0, 1) draw for the step (False)
+    chained: bool = True
 
 
 TINY = MoEShape("tiny", 1, 256, 512, 8, 1, 2, 4, "f32", "f32")
 OLMOE_DECODE = MoEShape("olmoe_decode", 16, 2048, 1024, 64, 0, 8, 1, "bf16", "f32", steps=256)
-GLM_DECODE_B1 = MoEShape("glm_decode_b1", 8, 6144, 2048, 256, 1, 8, 1, "bf16", "f32")
-GLM_DECODE_B8 = MoEShape("glm_decode_b8", 8, 6144, 2048, 256, 1, 8, 8, "bf16", "f32")
+# Without the normalisation a real model applies before each MoE layer, a
+# residual chain of these wide SwiGLU layers grows without bound (the FFN is
+# quadratic in its input) and overflows f32 within eight layers, so each layer
+# of a step gets its own unit-variance input.
+GLM_DECODE_B1 = MoEShape("glm_decode_b1", 8, 6144, 2048, 256, 1, 8, 1, "bf16", "f32",
+                         chained=False)
+GLM_DECODE_B8 = MoEShape("glm_decode_b8", 8, 6144, 2048, 256, 1, 8, 8, "bf16", "f32",
+                         chained=False)
 GLM_PREFILL = MoEShape("glm_prefill", 1, 6144, 2048, 256, 1, 8, 4096, "bf16", "bf16")
 
 SHAPES = {s.name: s for s in (TINY, OLMOE_DECODE, GLM_DECODE_B1, GLM_DECODE_B8, GLM_PREFILL)}
@@ -84,10 +93,12 @@ def _tdt(name):
     return {"f32": torch.float32, "bf16": torch.bfloat16}[name]
 
 
-def tokens(shape: MoEShape, seed=0, step=0, device="cpu", attempt=0):
-    """Layer-0 input activations [T, H], N(0, 1), of the shape's x dtype."""
-    return normal((shape.tokens, shape.hidden), 1.0, _tdt(shape.x_dtype), seed,
-                  _T_X, step, attempt, device=device)
+def tokens(shape: MoEShape, seed=0, step=0, device="cpu", attempt=0, layer=0):
+    """Input activations [T, H], N(0, 1), of the shape's x dtype, for layer 0
+    (or, for stacks that are not chained, for the given layer) of a step."""
+    keys = (_T_X, step, attempt) if layer == 0 else (_T_X, step, attempt, layer)
+    return normal((shape.tokens, shape.hidden), 1.0, _tdt(shape.x_dtype), seed, *keys,
+                  device=device)
 
 
 def router_weights(shape: MoEShape, layer, seed=0, device="cpu", row_std=None):

@@ -120,3 +120,7 @@ def test_profile_events_validation(coli):
     assert lib.coli_profile_events(coli.COLI_KERNEL_GATEUP, None, None, 1) == coli.COLI_EINVAL
     # turning recording off is always valid and reports no bracketed launches
     assert lib.coli_profile_events(coli.COLI_KERNEL_GATEUP, None, None, 0) == 0
+
+
+def test_last_error_before_any_failure(coli):
+    assert coli.coli_last_error() == "no error"
