@@ -264,6 +264,136 @@ class DecodeWorkload:
         return int(unique * per_expert + len(steps) * per_step_fixed), int(unique)
 
 
+class PrefillWorkload:
+    """One batched (prefill) layer resident in HBM: experts, a skewed router and
+    a fresh batch of tokens per step."""
+
+    def __init__(self, shape, steps_total, dev, seed=0):
+        import int4_expert_ffn_gb300 as pkg
+        from int4_expert_ffn_gb300 import synth
+        self.coli = c = pkg.binding
+        self.shape = shape
+        H, F, E, S, T = shape.hidden, shape.ffn, shape.experts, shape.shared, shape.tokens
+        self.eb = c.coli_expert_packed_bytes(H, F)
+        self.es = c.coli_expert_scale_count(H, F)
+        n = E + S
+        self.packed = torch.empty(n * self.eb, dtype=torch.uint8, device=dev)
+        self.scales = torch.empty(n * self.es, dtype=torch.float32, device=dev)
+        p0 = s0 = 0
+        for e in range(n):
+            for m in range(3):
+                w = synth.expert_matrix(shape, 0, e, m, seed, device=dev)
+                rows, cols = w.shape
+                nb, ns = rows * cols // 2, rows * cols // 64
+                c.coli_quant_i4g(w, self.packed[p0:p0 + nb].view(rows, -1),
+                                 self.scales[s0:s0 + ns].view(rows, -1))
+                p0 += nb
+                s0 += ns
+        self.router = synth.router_weights(shape, 0, seed, device=dev,
+                                           row_std=synth.skewed_router_std(E, H))
+        self.x = torch.stack([synth.tokens(shape, seed, i, device=dev)
+                              for i in range(steps_total)]).contiguous()
+        self.out = torch.empty((T, H), dtype=torch.float32, device=dev)
+        self.counts = torch.zeros((steps_total, E), dtype=torch.int32, device=dev)
+        self.desc = c.MoEDesc(H, F, E, S, T, c.COLI_BF16 if shape.x_dtype == "bf16" else c.COLI_F32,
+                              c.COLI_BF16 if shape.router_dtype == "bf16" else c.COLI_F32)
+        self.ws = c.new_workspace(self.desc, shape.top_k)
+        torch.cuda.synchronize()
+
+    def step(self, i, stream=None, x=None, out=None):
+        self.coli.coli_moe_forward(self.desc, self.shape.top_k, self.x[i] if x is None else x,
+                                   self.router, self.packed, self.scales, self.ws,
+                                   out=self.out if out is None else out,
+                                   route_counts=self.counts[i], stream=stream)
+
+    def gemm_flops(self):
+        """Algorithmic FLOPs of one call's expert GEMMs: (gate/up, down)."""
+        sh = self.shape
+        routes = sh.tokens * (sh.top_k + sh.shared)
+        return 2 * routes * 2 * sh.hidden * sh.ffn, 2 * routes * sh.hidden * sh.ffn
+
+    def flops_per_step(self):
+        sh = self.shape
+        gu, dn = self.gemm_flops()
+        return gu + dn + 2 * sh.tokens * sh.experts * sh.hidden
+
+
+def run_prefill(args, shape, dev, world):
+    steps, warmup = args.steps, args.warmup
+    wl = PrefillWorkload(shape, warmup + steps, dev)
+    c = wl.coli
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            wl.step(i, stream=stream)
+    stream.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[0]))
+    sampler.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(warmup, warmup + steps):
+            wl.step(i, stream=stream)
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    time.sleep(0.15)
+    sampler.stop()
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+    # the two grouped GEMMs, each bracketed by events in a separate pass
+    kern = {}
+    gu_f, dn_f = wl.gemm_flops()
+    for name, kid, fl in (("k_pgemm_gateup", c.COLI_KERNEL_PREFILL_GATEUP, gu_f),
+                          ("k_pgemm_down", c.COLI_KERNEL_PREFILL_DOWN, dn_f)):
+        before = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        after = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        for e in before + after:
+            e.record(stream)
+        stream.synchronize()
+        c.coli_profile_events(kid, before, after)
+        try:
+            with torch.cuda.stream(stream):
+                for i in range(warmup, warmup + steps):
+                    wl.step(i, stream=stream)
+        finally:
+            got = c.coli_profile_events(kid, [], [])
+        torch.cuda.synchronize()
+        assert got == steps
+        us = float(np.mean([b.elapsed_time(a) for b, a in zip(before, after)])) * 1e3
+        kern[name] = {"launches": steps, "us_per_launch": us, "flops_per_launch": fl,
+                      "tflops": fl / (us * 1e-6) / 1e12}
+    # end to end: bf16 tokens from pinned host memory in, f32 output back
+    host_x = wl.x.cpu().pin_memory()
+    host_out = torch.empty((steps, shape.tokens, shape.hidden), dtype=torch.float32).pin_memory()
+    dx = torch.empty_like(wl.x[0])
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(steps):
+            dx.copy_(host_x[warmup + i], non_blocking=True)
+            wl.step(warmup + i, stream=stream, x=dx)
+            host_out[i].copy_(wl.out, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e = {"value": world * steps * shape.tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": shape.tokens * shape.hidden * 2,
+           "d2h_bytes_per_step": shape.tokens * shape.hidden * 4}
+    hot = wl.counts[warmup:].sum(0).cpu().numpy()
+    top32 = float(np.sort(hot)[::-1][:32].sum() / max(1, hot.sum()))
+    res = {"tokens_per_rank": steps * shape.tokens, "ms": ms, "clocks": sampler.summary(t0, t1),
+           "kernels": kern, "e2e": e2e, "launches": steps * 9, "top32_share": top32,
+           "flops_per_step": wl.flops_per_step()}
+    return wl, res
+
+
 def capture_graphs(wl, idxs, stream):
     graphs = []
     for i in idxs:
@@ -476,10 +606,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="coli", choices=["coli", "reference"])
     ap.add_argument("--workload", default="olmoe_decode",
-                    choices=["olmoe_decode", "glm_decode_b1", "glm_decode_b8"])
+                    choices=["olmoe_decode", "glm_decode_b1", "glm_decode_b8", "glm_prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the stack depth (small profiling cases only)")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the batch size (small profiling cases only)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -493,9 +625,10 @@ def main():
 
     from int4_expert_ffn_gb300 import synth
     shape = synth.SHAPES[args.workload]
-    if args.layers is not None:
+    if args.layers is not None or args.tokens is not None:
         import dataclasses
-        shape = dataclasses.replace(shape, layers=args.layers)
+        shape = dataclasses.replace(shape, layers=args.layers or shape.layers,
+                                    tokens=args.tokens or shape.tokens)
     config = {"workload": "%s: %d MoE layers, hidden %d, %d experts of FFN width %d, top-%d, "
                           "%d shared, batch %d, int4-grouped g64 f32 scales, %s router"
                           % (shape.name, shape.layers, shape.hidden, shape.experts, shape.ffn,
@@ -503,7 +636,8 @@ def main():
               "layers": shape.layers, "hidden": shape.hidden, "experts": shape.experts,
               "ffn": shape.ffn, "top_k": shape.top_k, "shared": shape.shared,
               "batch": shape.tokens, "parallelism": "replicas" if world > 1 else "single",
-              "inputs": ("layer 0 takes a fresh N(0,1) token each step; layer l>0 takes "
+              "inputs": ("a fresh batch of N(0,1) tokens each step" if shape.layers == 1 else
+                         "layer 0 takes a fresh N(0,1) token each step; layer l>0 takes "
                          "x_l + MoE_l(x_l)" if shape.chained else
                          "every layer takes its own fresh N(0,1) input each step"),
               "l2": "inputs larger than L2: %.2f GB of experts resident, fresh routing each step"}
@@ -527,6 +661,9 @@ def main():
     if rank == 0:
         b.build()
     barrier(world)
+    if shape.name == "glm_prefill":
+        emit_prefill(args, shape, dev, world, rank, config)
+        return
     wl, res = run_decode(args, shape, dev, world, rank)
     resident = wl.packed.numel() + 4 * wl.scales.numel()
     config["l2"] = config["l2"] % (resident / 1e9)
@@ -560,6 +697,42 @@ def main():
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_baseline(shape, dev)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def emit_prefill(args, shape, dev, world, rank, config):
+    """Bench line of the batched (prefill) layer: tokens/s, with the dominant
+    grouped GEMM's tensor throughput as the roofline."""
+    wl, res = run_prefill(args, shape, dev, world)
+    _, tf_peak, peak_kind = read_peaks()
+    sec = res["ms"] / 1e3
+    kern = res["kernels"]
+    dom = max(kern, key=lambda n: kern[n]["us_per_launch"])
+    kd = kern[dom]
+    config = dict(config, l2="inputs larger than L2: %.2f GB of experts resident"
+                  % ((wl.packed.numel() + 4 * wl.scales.numel()) / 1e9),
+                  routing="skewed router: the 32 most-used experts took %.1f%% of routes"
+                  % (100 * res["top32_share"]))
+    line = {
+        "metric": "MoE prefill tokens/s (batched grouped int4 GEMMs on tcgen05)",
+        "value": world * res["tokens_per_rank"] / sec, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"] / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp16 operands, f32 accumulate",
+        "data": "synthetic (seeded; weights N(0,0.02) bf16 quantised on the GPU; bf16 tokens)",
+        "config": config,
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": kd["tflops"], "peak": tf_peak,
+                     "unit": "TFLOP/s", "frac": kd["tflops"] / tf_peak,
+                     "peak_kind": "%s bf16 burst (fp16 has the same nominal dense rate)" % peak_kind,
+                     "traffic": None, "flops_per_launch": kd["flops_per_launch"],
+                     "us_per_launch": kd["us_per_launch"]},
+        "step_tflops": res["flops_per_step"] * args.steps / sec / 1e12,
+        "kernels": kern, "clocks": res["clocks"], "e2e": res["e2e"],
+        "gpu_launches": res["launches"],
+    }
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -190,6 +190,8 @@ int coli_moe_stack_forward(const coli_moe_desc *d, int top_k, int n_layers,
 #define COLI_KERNEL_ROUTE  0   /* router partials of a pass's first layer */
 #define COLI_KERNEL_GATEUP 1   /* gate/up expert GEMVs + SwiGLU */
 #define COLI_KERNEL_DOWN   2   /* down expert GEMVs + combine (+ next routing) */
+#define COLI_KERNEL_PREFILL_GATEUP 3  /* batched path: gate/up grouped GEMM + SwiGLU */
+#define COLI_KERNEL_PREFILL_DOWN   4  /* batched path: down grouped GEMM */
 
 /*
  * coli_profile_events -- diagnostic, not on the compute path: record the

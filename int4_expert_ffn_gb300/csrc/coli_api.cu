@@ -84,6 +84,12 @@ int check_desc(const coli_moe_desc *d, int top_k) {
 // Tokens per internal pass of the GEMV path; larger calls run in passes.
 int pass_tokens(int T) { return T < kDecodeMaxT ? T : kDecodeMaxT; }
 
+// Calls with many tokens take the batched path (grouped tensor-core GEMMs)
+// when its tile shapes divide the layer.
+bool use_prefill(const coli_moe_desc *d) {
+  return d->n_tokens >= kPrefillMinT && prefill_supported(d->hidden, d->ffn);
+}
+
 int map_err(cudaError_t e) { return coli::cuda_status(e); }
 
 // Diagnostic event recording around the gate/up kernel (coli_profile_events).
@@ -98,7 +104,9 @@ ProfileState &profile() {
   return p;
 }
 
-cudaError_t record_profile(int kernel, cudaStream_t s, bool is_after, size_t *slot) {
+}  // namespace
+
+cudaError_t coli::record_profile(int kernel, cudaStream_t s, bool is_after, size_t *slot) {
   ProfileState &p = profile();
   std::lock_guard<std::mutex> lock(p.mu);
   if (!is_after) {
@@ -114,14 +122,16 @@ cudaError_t record_profile(int kernel, cudaStream_t s, bool is_after, size_t *sl
   return cudaEventRecordWithFlags(ev, s, flags);
 }
 
+namespace {
+
 // Launch one kernel of the layer forward, bracketed by the caller's profiling
 // events when coli_profile_events selected it.
 template <class Launch>
 cudaError_t profiled(int kernel, cudaStream_t s, Launch launch) {
   size_t slot = 0;
-  cudaError_t e = record_profile(kernel, s, false, &slot);
+  cudaError_t e = coli::record_profile(kernel, s, false, &slot);
   if (e == cudaSuccess) e = launch();
-  if (e == cudaSuccess) e = record_profile(kernel, s, true, &slot);
+  if (e == cudaSuccess) e = coli::record_profile(kernel, s, true, &slot);
   return e;
 }
 
@@ -196,6 +206,8 @@ size_t coli_router_workspace_size(const coli_moe_desc *d, int top_k) {
 
 size_t coli_moe_workspace_size(const coli_moe_desc *d, int top_k) {
   if (check_desc(d, top_k) != COLI_OK) return 0;
+  if (use_prefill(d))
+    return prefill_layout(d->n_tokens, d->hidden, d->ffn, d->n_experts, d->n_shared, top_k).total;
   const int T = pass_tokens(d->n_tokens);
   return ws_layout(T > 0 ? T : 1, d->hidden, d->ffn, d->n_experts, d->n_shared, top_k).total;
 }
@@ -278,9 +290,57 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
   return map_err(e);
 }
 
+// The batched path: every layer in one pass over all T tokens.
+static int prefill_run(const coli_moe_desc *d, int k, int n_layers, const void *x,
+                       const void *router_w, const uint8_t *packed, const float *scales,
+                       float *out, bool residual, float *layer_out, uint32_t *route_counts,
+                       void *workspace, cudaStream_t stream) {
+  const int T = d->n_tokens, H = d->hidden, F = d->ffn, E = d->n_experts, S = d->n_shared;
+  const PrefillLayout L = prefill_layout(T, H, F, E, S, k);
+  uint8_t *ws = (uint8_t *)workspace;
+  const size_t wr_stride = (size_t)E * H * xsize(d->router_dtype);
+  const size_t pk_stride = (size_t)(E + S) * coli_expert_packed_bytes(H, F);
+  const size_t sc_stride = (size_t)(E + S) * coli_expert_scale_count(H, F);
+  for (int l = 0; l < n_layers; ++l) {
+    PrefillArgs a{};
+    a.T = T; a.H = H; a.F = F; a.E = E; a.S = S; a.k = k;
+    a.x = l == 0 ? x : (const void *)out;
+    a.wr = (const char *)router_w + l * wr_stride;
+    a.packed = packed + l * pk_stride;
+    a.scales = scales + l * sc_stride;
+    a.eb = coli_expert_packed_bytes(H, F);
+    a.es = coli_expert_scale_count(H, F);
+    a.residual = residual ? (l == 0 ? (const float *)x : out) : nullptr;
+    a.out = out;
+    a.layer_out = layer_out ? layer_out + (size_t)l * T * H : nullptr;
+    a.route_counts = route_counts ? route_counts + (size_t)l * E : nullptr;
+    a.ctrl = (uint32_t *)ws;
+    a.x16 = (__half *)(ws + L.x16);
+    a.logits = (float *)(ws + L.logits);
+    a.idx = (int32_t *)(ws + L.idx);
+    a.gates = (float *)(ws + L.gates);
+    a.hist = (int32_t *)(ws + L.hist);
+    a.offsets = (int32_t *)(ws + L.offsets);
+    a.item_begin = (int32_t *)(ws + L.item_begin);
+    a.n_groups = E + S;
+    a.route_tok = (int32_t *)(ws + L.route_tok);
+    a.route_gate = (float *)(ws + L.route_gate);
+    a.inv = (int32_t *)(ws + L.inv);
+    a.h16 = (__half *)(ws + L.h16);
+    a.y = (float *)(ws + L.y);
+    const int xdt = l == 0 ? d->x_dtype : COLI_F32;
+    const cudaError_t e = launch_prefill(a, xdt, d->router_dtype, stream);
+    if (e != cudaSuccess) return map_err(e);
+  }
+  return COLI_OK;
+}
+
 static int moe_run(const coli_moe_desc *d, int k, int n_layers, const void *x, const void *router_w,
                    const uint8_t *packed, const float *scales, float *out, bool residual,
                    float *layer_out, uint32_t *route_counts, void *workspace, cudaStream_t stream) {
+  if (use_prefill(d))
+    return prefill_run(d, k, n_layers, x, router_w, packed, scales, out, residual, layer_out,
+                       route_counts, workspace, stream);
   const int T = d->n_tokens, H = d->hidden;
   const int TP = pass_tokens(T);
   const WsLayout L = ws_layout(TP, H, d->ffn, d->n_experts, d->n_shared, k);
@@ -337,7 +397,7 @@ int coli_moe_stack_forward(const coli_moe_desc *d, int top_k, int n_layers, cons
 int coli_profile_events(int kernel, const cudaEvent_t *before, const cudaEvent_t *after,
                         int n) {
   if (n < 0 || (n > 0 && (!before || !after))) return COLI_EINVAL;
-  if (kernel < COLI_KERNEL_ROUTE || kernel > COLI_KERNEL_DOWN) return COLI_EINVAL;
+  if (kernel < COLI_KERNEL_ROUTE || kernel > COLI_KERNEL_PREFILL_DOWN) return COLI_EINVAL;
   ProfileState &p = profile();
   std::lock_guard<std::mutex> lock(p.mu);
   const int done = (int)p.next;

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cuda_fp16.h>
+
 #include "coli.h"
 
 namespace coli {
@@ -23,6 +25,7 @@ constexpr int kReplicas = 8;
 enum CtrlWord : int {
   kCtrlFlags = 0,      // COLI_FLAG_* bits (sticky until coli_moe_check clears)
   kCtrlRouterTicket = 1,
+  kCtrlPrefillMTiles = 2,  // m-tiles of the current batched call (written by the grouping)
   kCtrlWords = 64,     // 256 bytes
 };
 
@@ -100,6 +103,43 @@ struct Dec2Args {
 };
 
 
+// Batched (prefill) path: arguments of its kernels for one layer.
+constexpr int kPrefillMinT = 64;      // calls with at least this many tokens take it
+constexpr int kGroupTokens = 256;     // tokens per block of the counting sort
+struct PrefillArgs {
+  int T, H, F, E, S, k;
+  const void *x;            // [T][H] x_dtype
+  const void *wr;           // [E][H] router dtype
+  const uint8_t *packed;    // expert records of this layer
+  const float *scales;
+  int64_t eb, es;
+  const float *residual;    // added to out (or null)
+  float *out;               // [T][H]
+  float *layer_out;         // [T][H] MoE output without the residual (or null)
+  uint32_t *route_counts;   // [E] (or null)
+  uint32_t *ctrl;
+  __half *x16;              // [T][H]
+  float *logits;            // [T][E]
+  int32_t *idx;             // [T][k]
+  float *gates;             // [T][k]
+  int32_t *hist;            // [blocks][E]
+  int32_t *offsets;         // [E+S+1] first route position of each expert
+  int32_t *item_begin;      // [E+S+1] m-tile prefix
+  int n_groups;             // E + S
+  int32_t *route_tok;       // [T(k+S)] token of each route position
+  float *route_gate;        // [T(k+S)] its gate (1 for shared experts)
+  int32_t *inv;             // [T k] route position of (t, j)
+  __half *h16;              // [T(k+S)][F]
+  float *y;                 // [T(k+S)][H]
+};
+struct PrefillLayout {
+  size_t x16, logits, idx, gates, hist, offsets, item_begin, route_tok, route_gate, inv, h16, y,
+      total;
+};
+PrefillLayout prefill_layout(int T, int H, int F, int E, int S, int k);
+bool prefill_supported(int H, int F);
+cudaError_t launch_prefill(const PrefillArgs &p, int x_dtype, int wr_dtype, cudaStream_t s);
+
 // Fill the kernels' launch plan (warps per phase, shared-memory layouts).
 cudaError_t plan_decode(Dec2Args &a, int n_part);
 cudaError_t launch_route_partials(const Dec2Args &a, int x_bf16, int w_bf16, cudaStream_t s,
@@ -112,6 +152,9 @@ cudaError_t launch_quant_i4g(const void *w, int w_dtype, int64_t rows, int64_t c
                              uint8_t *packed, float *scales, cudaStream_t s);
 
 int num_sms();
+// Records the caller's profiling event before (is_after false: claims a slot)
+// or after a launch of `kernel` if coli_profile_events selected it.
+cudaError_t record_profile(int kernel, cudaStream_t s, bool is_after, size_t *slot);
 // COLI_OK for cudaSuccess; else records the error's message for
 // coli_last_error() and returns COLI_ECUDA.
 int cuda_status(cudaError_t e);

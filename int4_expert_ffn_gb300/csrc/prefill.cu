@@ -1,0 +1,710 @@
+// Batched (prefill) path of the routed-MoE layer: many tokens per call.
+//
+// Pages: "Colibrì 深度解析" §四 / §十一 (route, group the batch's tokens by
+// expert so that each expert's weights are read once, expert FFNs, combine);
+// "从源码开始colibri纯C引擎的编译、权重转换与.bin直映射实战" §权重转换 (the
+// int4-grouped format the expert GEMMs dequantise).
+//
+//   k_x16       activations -> fp16 operand copy
+//   k_logits    router logits, tiled f32 SIMT GEMM (any x / router dtype)
+//   k_ptopk     top-k, gates, NaN flag and route counts (block-parallel top-k)
+//   k_gcount / k_gscan / k_gscatter
+//               counting sort of the routes by expert (stable in (token, slot)
+//               order), expert m-tiles and the GEMM work list
+//   k_pgemm<MODE>
+//               token-sorted grouped GEMM on tcgen05 tensor cores: 128-row
+//               m-tiles of one expert's routes x 256-column n-tiles, K in
+//               steps of 64 (one scale group).  Four producer warps stage the
+//               activation rows with cp.async and dequantise the int4 weight
+//               tile to fp16 into 128-byte-swizzled shared memory; one thread
+//               issues tcgen05.mma (kind::f16, f32 accumulator in TMEM); the
+//               same four warps drain TMEM in the epilogue:
+//                 gate/up: h = silu(g) * u * gate  -> fp16 [route][F]
+//                 down:    y                        -> f32  [route][H]
+//   k_pcombine  out[t] = sum_j y[route(t, j)] + sum_s y[shared s, t] (+ residual)
+#include <cuda_fp16.h>
+
+#include "coli_internal.cuh"
+#include "ptx.cuh"
+#include "topk.cuh"
+
+namespace coli {
+
+namespace {
+
+constexpr int kBM = 128;          // m-tile rows (routes)
+constexpr int kBK = 64;           // K per k-tile: one scale group
+constexpr int kBN = 256;          // n-tile columns (gate/up: 128 gate + 128 up)
+constexpr int kNA = 5;            // A ring (fp16 activation tiles)
+constexpr int kNB = 3;            // B ring (dequantised fp16 weight tiles)
+constexpr int kNR = 4;            // raw ring (int4 rows + scales as copied)
+constexpr int kDist = 3;          // copies run this many k-tiles ahead of the dequantisation
+constexpr int kProducerWarps = 8; // one B row per producer thread
+constexpr int kProducerThreads = 32 * kProducerWarps;
+constexpr int kMmaWarp = kProducerWarps;
+constexpr int kEpilogueWarps = 4;
+constexpr int kEpilogueThreads = 32 * kEpilogueWarps;
+constexpr int kGemmThreads = 32 * (kProducerWarps + 1 + kEpilogueWarps);
+constexpr int kATileBytes = kBM * kBK * 2;     // 16 KB
+constexpr int kBTileBytes = kBN * kBK * 2;     // 32 KB
+constexpr int kRawBytes = kBN * (kBK / 2) + kBN * 4;   // 8 KB nibbles + 1 KB scales
+constexpr int kTableBytes = 2 * (kMaxExperts + kMaxShared + 1) * 4;   // item_begin, offsets
+constexpr int kGemmSmem = kNA * kATileBytes + kNB * kBTileBytes + kNR * kRawBytes + kTableBytes + 2048;
+static_assert(kNR > kDist, "a raw slot is refilled only after its dequantisation");
+static_assert(kProducerThreads == kBN, "one B row per producer thread");
+
+enum GemmMode : int { kModeGateUp = 0, kModeDown = 1 };
+
+__device__ __forceinline__ void set_flag_p(uint32_t *ctrl, uint32_t f) {
+  atomicOr(ctrl + kCtrlFlags, f);
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 / TMEM helpers (inline PTX)
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, M = 128, N from idesc, K = 16.
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// The mbarrier completes one arrival when all earlier tcgen05 ops of this thread finish.
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+// 32 lanes x 32 consecutive 32-bit columns: thread i gets lane (taddr.lane + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile stored as rows of 128
+// bytes (64 fp16) with the 128-byte swizzle: 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) /* LBO 16 B (unused) */ |
+         ((uint64_t)(1024 >> 4) << 32) /* SBO */ | ((uint64_t)1 << 46) /* descriptor version */ |
+         ((uint64_t)2 << 61) /* 128-byte swizzle */;
+}
+// Instruction descriptor, kind::f16: f32 accumulator, fp16 A and B, both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16(int n, int m) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
+}
+// Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled tile.
+__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
+  return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ void cp16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp4(uint32_t dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void st_shared_zero16(uint32_t dst) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0) : "memory");
+}
+__device__ __forceinline__ void st_shared16(uint32_t dst, uint32_t a, uint32_t b, uint32_t c,
+                                            uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// 8 packed bytes (16 int4 values, even column low nibble) -> 8 fp16x2 words of
+// (u - 8) * s.  For byte j the pair (2j, 2j+1) is built exactly as fp16
+// 1024 + u_even and 1024 + 16 u_odd, mapped to (u - 8) by one fused
+// multiply-add (x1, x1/16), then scaled.
+__device__ __forceinline__ void dequant8(uint32_t w0, uint32_t w1, __half2 s2, uint32_t (&o)[8]) {
+  const __half2 mul = __halves2half2(__float2half_rn(1.0f), __float2half_rn(1.0f / 16.0f));
+  const __half2 add = __halves2half2(__float2half_rn(-1032.0f), __float2half_rn(-72.0f));
+  const uint32_t ws[2] = {w0, w1};
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t t = __byte_perm(ws[i], 0, 0x4040u | (j * 0x0101u));
+      const uint32_t m = (t & 0x00F0000Fu) | 0x64006400u;
+      __half2 h = *reinterpret_cast<const __half2 *>(&m);
+      h = __hfma2(h, mul, add);
+      h = __hmul2(h, s2);
+      o[4 * i + j] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+// A GEMM work item: expert e, n-tile ni, and the rows [p0, p0 + rows) of its
+// m-tile in route order.  Items are ordered (expert, n-tile, m-tile);
+// begin[] (shared memory) holds the experts' m-tile prefix, off[] their
+// first route position.
+struct Item {
+  int e, ni, p0, rows;
+};
+__device__ __forceinline__ Item decode_item(const int *begin, const int *off, int n_groups, int w,
+                                            int n_ntiles) {
+  int lo = 0, hi = n_groups;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (begin[mid] * n_ntiles <= w) lo = mid; else hi = mid;
+  }
+  Item it;
+  it.e = lo;
+  const int nm = begin[lo + 1] - begin[lo];
+  const int local = w - begin[lo] * n_ntiles;
+  it.ni = local / nm;
+  const int mi = local - it.ni * nm;
+  it.p0 = off[lo] + mi * kBM;
+  const int left = off[lo + 1] - it.p0;
+  it.rows = left < kBM ? left : kBM;
+  return it;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Activations to fp16 (exact for bf16 inputs inside the fp16 range).
+
+template <typename XT>
+__global__ void k_x16(const XT *x, __half *x16, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    x16[i] = __float2half_rn(to_f32(x[i]));
+}
+
+// ---------------------------------------------------------------------------
+// Router logits [T][E] = x [T][H] . Wr [E][H]^T, f32 accumulation.  64 x 64
+// tiles, K in steps of 32 through shared memory; 256 threads x (4 x 4).
+
+template <typename XT, typename WT>
+__global__ void __launch_bounds__(256) k_logits(const XT *x, const WT *wr, float *logits, int T,
+                                                int H, int E) {
+  __shared__ float sx[32][65];
+  __shared__ float sw[32][65];
+  const int t0 = blockIdx.y * 64, e0 = blockIdx.x * 64;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < H; k0 += 32) {
+    for (int i = threadIdx.x; i < 64 * 32; i += 256) {
+      const int r = i >> 5, kk = i & 31;
+      sx[kk][r] = (t0 + r < T) ? to_f32(x[(size_t)(t0 + r) * H + k0 + kk]) : 0.0f;
+      sw[kk][r] = (e0 + r < E) ? to_f32(wr[(size_t)(e0 + r) * H + k0 + kk]) : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < 32; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        a[i] = sx[kk][ty * 4 + i];
+        b[i] = sw[kk][tx * 4 + i];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int t = t0 + ty * 4 + i, e = e0 + tx * 4 + j;
+      if (t < T && e < E) logits[(size_t)t * E + e] = acc[i][j];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Top-k of kPTopkTokens tokens per block (the decode path's block top-k).
+
+constexpr int kPTopkTokens = 8;
+
+__global__ void __launch_bounds__(256) k_ptopk(PrefillArgs p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int T = p.T, E = p.E, k = p.k;
+  const int t0 = blockIdx.x * kPTopkTokens;
+  const int TB = (T - t0 < kPTopkTokens) ? T - t0 : kPTopkTokens;
+  float *lg = (float *)smem;
+  int *s_rank = (int *)(lg + kPTopkTokens * E);
+  int *s_idx = s_rank + kPTopkTokens * E;
+  float *s_gates = (float *)(s_idx + kPTopkTokens * k);
+  float *s_vals = s_gates + kPTopkTokens * k;
+  int *s_flag = (int *)(s_vals + kPTopkTokens * k);
+  for (int i = threadIdx.x; i < TB * E; i += blockDim.x) lg[i] = p.logits[(size_t)t0 * E + i];
+  __syncthreads();
+  const bool nan = block_topk(lg, TB, E, k, s_idx, s_gates, s_vals, s_rank, s_flag);
+  if (threadIdx.x == 0 && nan) set_flag_p(p.ctrl, COLI_FLAG_NAN_LOGITS);
+  for (int i = threadIdx.x; i < TB * k; i += blockDim.x) {
+    p.idx[(size_t)t0 * k + i] = s_idx[i];
+    p.gates[(size_t)t0 * k + i] = s_gates[i];
+    if (p.route_counts) atomicAdd(p.route_counts + s_idx[i], 1u);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Counting sort of the T*k routes by expert.  Block b owns tokens
+// [b * kGroupTokens, ...): k_gcount histograms them, k_gscan turns the
+// histograms into per-(block, expert) start positions and lays out the expert
+// m-tiles and GEMM work items, k_gscatter places every route in (token, slot)
+// order within its block.  Shared expert s serves all T tokens at positions
+// T*k + s*T + t.
+
+__global__ void __launch_bounds__(256) k_gcount(PrefillArgs p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  int *hist = (int *)smem;
+  const int E = p.E, k = p.k;
+  for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int t0 = blockIdx.x * kGroupTokens;
+  const int t1 = (t0 + kGroupTokens < p.T) ? t0 + kGroupTokens : p.T;
+  for (int i = t0 * k + threadIdx.x; i < t1 * k; i += blockDim.x) atomicAdd(hist + p.idx[i], 1);
+  __syncthreads();
+  for (int i = threadIdx.x; i < E; i += blockDim.x) p.hist[(size_t)blockIdx.x * E + i] = hist[i];
+}
+
+// One block: expert offsets (routed experts, then the shared ones), the
+// per-(block, expert) start positions (in place of the histograms), m-tile
+// counts and the work-item prefix of the GEMMs.
+__global__ void __launch_bounds__(1024) k_gscan(PrefillArgs p, int n_blocks) {
+  __shared__ int s_cnt[kMaxExperts + kMaxShared + 1];
+  __shared__ int s_items[kMaxExperts + kMaxShared + 1];
+  const int E = p.E, S = p.S, T = p.T, G = E + S;
+  for (int e = threadIdx.x; e < G; e += blockDim.x) {
+    int n = T;
+    if (e < E) {
+      n = 0;
+      for (int b = 0; b < n_blocks; ++b) {
+        const int c = p.hist[(size_t)b * E + e];
+        p.hist[(size_t)b * E + e] = n;       // start of block b within expert e
+        n += c;
+      }
+    }
+    s_cnt[e] = n;
+    s_items[e] = (n + kBM - 1) / kBM;        // m-tiles of expert e
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int off = 0, it = 0;
+    for (int e = 0; e < G; ++e) {
+      p.offsets[e] = off;
+      p.item_begin[e] = it;
+      off += s_cnt[e];
+      it += s_items[e];
+    }
+    p.offsets[G] = off;
+    p.item_begin[G] = it;           // m-tiles in total; the GEMMs scale by their n-tiles
+    p.ctrl[kCtrlPrefillMTiles] = (uint32_t)it;
+  }
+}
+
+__global__ void __launch_bounds__(256) k_gscatter(PrefillArgs p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  int *base = (int *)smem;                  // [E] next position of each expert in this block
+  const int E = p.E, k = p.k, T = p.T;
+  const int t0 = blockIdx.x * kGroupTokens;
+  const int t1 = (t0 + kGroupTokens < T) ? t0 + kGroupTokens : T;
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    base[e] = p.offsets[e] + p.hist[(size_t)blockIdx.x * E + e];
+  __syncthreads();
+  // one thread per expert walks the block's routes in (token, slot) order
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int pos = base[e];
+    for (int i = t0 * k; i < t1 * k; ++i)
+      if (p.idx[i] == e) {
+        p.route_tok[pos] = i / k;
+        p.route_gate[pos] = p.gates[i];
+        p.inv[i] = pos;
+        ++pos;
+      }
+  }
+  // shared experts: every token, in order
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.S * T; i += gridDim.x * blockDim.x) {
+    const int pos = T * k + i;
+    p.route_tok[pos] = i % T;
+    p.route_gate[pos] = 1.0f;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The grouped GEMM.
+
+template <int MODE>
+__global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t *a_ring = smem;                                  // kNA x 16 KB (fp16, swizzled)
+  uint8_t *b_ring = a_ring + kNA * kATileBytes;            // kNB x 32 KB (fp16, swizzled)
+  uint8_t *r_ring = b_ring + kNB * kBTileBytes;            // kNR x raw int4 rows + scales
+  uint64_t *full = (uint64_t *)(r_ring + kNR * kRawBytes);
+  uint64_t *a_empty = full + kNB;
+  uint64_t *b_empty = a_empty + kNA;
+  uint64_t *tm_full = b_empty + kNB;                       // [2]
+  uint64_t *tm_empty = tm_full + 2;                        // [2]
+  uint32_t *s_taddr = (uint32_t *)(tm_empty + 2);
+  int *s_abort = (int *)(s_taddr + 1);
+  int *s_begin = s_abort + 4;                              // [n_groups + 1]
+  int *s_off = s_begin + (kMaxExperts + kMaxShared + 1);   // [n_groups + 1]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int H = p.H, F = p.F;
+  const int K = MODE == kModeGateUp ? H : F;
+  const int nk = K / kBK;
+  const int n_ntiles = MODE == kModeGateUp ? F / (kBN / 2) : H / kBN;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kNB; ++s) {
+      mbar_init(&full[s], kProducerThreads);
+      mbar_init(&b_empty[s], 1);
+    }
+    for (int s = 0; s < kNA; ++s) mbar_init(&a_empty[s], 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tm_full[b], 1);
+      mbar_init(&tm_empty[b], kEpilogueThreads);
+    }
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(s_taddr, 2 * kBN);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  grid_dependents_launch();
+  grid_dependency_wait();
+  for (int i = threadIdx.x; i <= p.n_groups; i += blockDim.x) {
+    s_begin[i] = __ldcg(p.item_begin + i);
+    s_off[i] = __ldcg(p.offsets + i);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *s_taddr;
+  const int n_items = s_begin[p.n_groups] * n_ntiles;
+  const int my_items = n_items > (int)blockIdx.x ? (n_items - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  const int n_ticks = my_items * nk;         // this CTA's k-tiles over all its items
+
+  if (warp < kProducerWarps) {
+    // ---- producers: tick t issues the copies of k-tile t (A rows, raw B row)
+    // and dequantises k-tile t - kDist into the B ring
+    const int th = threadIdx.x;                      // B row th; A row th % 128
+    const int ar = th & (kBM - 1), ac0 = 4 * (th >> 7);
+    Item it{};
+    const __half *a_src = nullptr;
+    bool a_ok = false;
+    const uint8_t *b_src = nullptr;
+    const float *b_sc = nullptr;
+    bool ok = true;
+    int item = 0, kt = 0;                  // k-tile t = item * nk + kt
+    for (int t = 0; t < n_ticks + kDist && ok; ++t) {
+      if (t < n_ticks) {
+        if (kt == 0) {
+          it = decode_item(s_begin, s_off, p.n_groups, blockIdx.x + item * gridDim.x, n_ntiles);
+          a_ok = ar < it.rows;
+          if (a_ok)
+            a_src = MODE == kModeGateUp ? p.x16 + (int64_t)p.route_tok[it.p0 + ar] * H
+                                        : p.h16 + (int64_t)(it.p0 + ar) * F;
+          const uint8_t *pk = p.packed + (int64_t)it.e * p.eb;
+          const float *sc = p.scales + (int64_t)it.e * p.es;
+          if (MODE == kModeGateUp) {
+            const int f = it.ni * (kBN / 2) + (th & 127);
+            const int64_t mat = th < 128 ? 0 : 1;      // gate rows, then up rows
+            b_src = pk + mat * (int64_t)F * (H / 2) + (int64_t)f * (H / 2);
+            b_sc = sc + mat * (int64_t)F * (H / kGroup) + (int64_t)f * (H / kGroup);
+          } else {
+            const int hr = it.ni * kBN + th;
+            b_src = pk + (int64_t)F * H + (int64_t)hr * (F / 2);
+            b_sc = sc + (int64_t)2 * F * (H / kGroup) + (int64_t)hr * (F / kGroup);
+          }
+        }
+        const int sa = t % kNA;
+        if (!mbar_wait(&a_empty[sa], ((t / kNA) & 1) ^ 1)) { ok = false; break; }
+        const uint32_t a_dst = smem_u32(a_ring + sa * kATileBytes);
+        const int k0 = kt * kBK;
+        if (a_ok) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) cp16(a_dst + sw128_off(ar, ac0 + c), a_src + k0 + 8 * (ac0 + c));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) st_shared_zero16(a_dst + sw128_off(ar, ac0 + c));
+        }
+        // raw row th: first 16 bytes at [th], second at [kBN + th] (conflict-free)
+        uint8_t *raw = r_ring + (t % kNR) * kRawBytes;
+        cp16(smem_u32(raw + th * 16), b_src + k0 / 2);
+        cp16(smem_u32(raw + (kBN + th) * 16), b_src + k0 / 2 + 16);
+        cp4(smem_u32(raw + kBN * 32 + th * 4), b_sc + kt);
+        if (++kt == nk) { kt = 0; ++item; }
+      }
+      cp_commit();
+      const int c = t - kDist;
+      if (c < 0) continue;
+      cp_wait<kDist>();            // groups of ticks <= c have landed (this thread's copies)
+      const int sb = c % kNB;
+      if (!mbar_wait(&b_empty[sb], ((c / kNB) & 1) ^ 1)) { ok = false; break; }
+      const uint8_t *raw = r_ring + (c % kNR) * kRawBytes;
+      const uint4 w0 = *(const uint4 *)(raw + th * 16);
+      const uint4 w1 = *(const uint4 *)(raw + (kBN + th) * 16);
+      const __half2 s2 = __float2half2_rn(*(const float *)(raw + kBN * 32 + th * 4));
+      const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+      const uint32_t b_dst = smem_u32(b_ring + sb * kBTileBytes);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t o[8];
+        dequant8(wd[2 * q], wd[2 * q + 1], s2, o);
+        st_shared16(b_dst + sw128_off(th, 2 * q), o[0], o[1], o[2], o[3]);
+        st_shared16(b_dst + sw128_off(th, 2 * q + 1), o[4], o[5], o[6], o[7]);
+      }
+      fence_proxy_async();         // A (landed copies) and B of k-tile c -> tensor core reads
+      mbar_arrive(&full[sb]);
+    }
+    cp_wait<0>();
+    if (!ok) {
+      set_flag_p(p.ctrl, COLI_FLAG_TIMEOUT);
+      *(volatile int *)s_abort = 1;
+    }
+  } else if (warp == kMmaWarp) {
+    // ---- MMA issuer (one lane)
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(kBN, kBM);
+      for (int c = 0; c < n_ticks; ++c) {
+        const int item = c / nk, kt = c % nk, buf = item & 1;
+        const uint32_t acc = tbase + (uint32_t)(buf * kBN);
+        if (kt == 0 && !mbar_wait(&tm_empty[buf], ((item >> 1) & 1) ^ 1)) break;
+        const int sb = c % kNB, sa = c % kNA;
+        if (!mbar_wait(&full[sb], (c / kNB) & 1)) break;
+        if (*(volatile int *)s_abort) break;
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(a_ring + sa * kATileBytes);
+        const uint32_t b0 = smem_u32(b_ring + sb * kBTileBytes);
+#pragma unroll
+        for (int k16 = 0; k16 < kBK / 16; ++k16)
+          tc_mma(acc, sw128_desc(a0 + 32 * k16), sw128_desc(b0 + 32 * k16), idesc,
+                 (kt | k16) != 0);
+        tc_commit(&a_empty[sa]);
+        tc_commit(&b_empty[sb]);
+        if (kt == nk - 1) tc_commit(&tm_full[buf]);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue warps: TMEM lane quarter (warp % 4) holds rows 32 (warp % 4) + lane
+    const int q = warp & 3;
+    const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    for (int i = 0; i < my_items; ++i) {
+      const int buf = i & 1;
+      if (!mbar_wait(&tm_full[buf], (i >> 1) & 1)) {
+        set_flag_p(p.ctrl, COLI_FLAG_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      const Item it = decode_item(s_begin, s_off, p.n_groups, blockIdx.x + i * gridDim.x, n_ntiles);
+      const int r = 32 * q + lane;
+      const bool r_ok = r < it.rows;
+      const uint32_t trow = tbase + lane_off + (uint32_t)(buf * kBN);
+      if (MODE == kModeGateUp) {
+        const float gate = r_ok ? p.route_gate[it.p0 + r] : 0.0f;
+        __half *dst = p.h16 + (int64_t)(it.p0 + r) * F + it.ni * (kBN / 2);
+        for (int cc = 0; cc < kBN / 2; cc += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32(trow + cc, g);
+          tmem_ld32(trow + kBN / 2 + cc, u);
+          tmem_ld_wait();
+          uint32_t o[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float h0 = silu_f(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]) * gate;
+            const float h1 =
+                silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]) * gate;
+            const __half2 hh = __floats2half2_rn(h0, h1);
+            o[j] = *reinterpret_cast<const uint32_t *>(&hh);
+          }
+          if (r_ok) {
+            uint4 *d4 = (uint4 *)(dst + cc);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              d4[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+          }
+        }
+      } else {
+        float *dst = p.y + (int64_t)(it.p0 + r) * H + it.ni * kBN;
+        for (int cc = 0; cc < kBN; cc += 32) {
+          uint32_t v[32];
+          tmem_ld32(trow + cc, v);
+          tmem_ld_wait();
+          if (r_ok) {
+            float4 *d4 = (float4 *)(dst + cc);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              d4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                  __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tm_empty[buf]);
+    }
+  }
+  // every MMA has been waited for by the epilogue (or abandoned on a timeout)
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tbase, 2 * kBN);
+}
+
+// ---------------------------------------------------------------------------
+// Combine: out[t] = sum_j y[inv(t, j)] + sum_s y[T k + s T + t] (+ residual),
+// fixed order; layer_out receives the MoE output without the residual.
+
+__global__ void k_pcombine(PrefillArgs p) {
+  const int T = p.T, H = p.H, k = p.k, S = p.S;
+  const int H4 = H / 4;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (int64_t)T * H4;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / H4), c = (int)(i - (int64_t)t * H4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+      const float4 v = ((const float4 *)(p.y + (int64_t)p.inv[t * k + j] * H))[c];
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    for (int s = 0; s < S; ++s) {
+      const float4 v = ((const float4 *)(p.y + (int64_t)(T * k + s * T + t) * H))[c];
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    if (p.layer_out) ((float4 *)(p.layer_out + (int64_t)t * H))[c] = acc;
+    if (p.residual) {
+      const float4 r = ((const float4 *)(p.residual + (int64_t)t * H))[c];
+      acc.x += r.x; acc.y += r.y; acc.z += r.z; acc.w += r.w;
+    }
+    ((float4 *)(p.out + (int64_t)t * H))[c] = acc;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+
+namespace {
+template <typename K>
+cudaError_t set_smem(K kernel, size_t bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+}  // namespace
+
+PrefillLayout prefill_layout(int T, int H, int F, int E, int S, int k) {
+  auto a256 = [](size_t v) { return (v + 255) & ~(size_t)255; };
+  PrefillLayout L{};
+  const size_t P = (size_t)T * (k + S);
+  const size_t nb = ((size_t)T + kGroupTokens - 1) / kGroupTokens;
+  size_t o = a256(kCtrlWords * 4);
+  L.x16 = o;        o = a256(o + (size_t)T * H * 2);
+  L.logits = o;     o = a256(o + (size_t)T * E * 4);
+  L.idx = o;        o = a256(o + (size_t)T * k * 4);
+  L.gates = o;      o = a256(o + (size_t)T * k * 4);
+  L.hist = o;       o = a256(o + nb * E * 4);
+  L.offsets = o;    o = a256(o + (size_t)(E + S + 1) * 4);
+  L.item_begin = o; o = a256(o + (size_t)(E + S + 1) * 4);
+  L.route_tok = o;  o = a256(o + P * 4);
+  L.route_gate = o; o = a256(o + P * 4);
+  L.inv = o;        o = a256(o + (size_t)T * k * 4);
+  L.h16 = o;        o = a256(o + P * F * 2);
+  L.y = o;          o = a256(o + P * H * 4);
+  L.total = o;
+  return L;
+}
+
+bool prefill_supported(int H, int F) {
+  // K of both GEMMs in whole stages, n-tiles whole
+  return H % kBN == 0 && F % (kBN / 2) == 0 && H % kBK == 0 && F % kBK == 0;
+}
+
+size_t prefill_gemm_smem() { return kGemmSmem; }
+
+cudaError_t launch_prefill(const PrefillArgs &p, int x_dtype, int wr_dtype, cudaStream_t s) {
+  cudaError_t e;
+  const int T = p.T, H = p.H, E = p.E, k = p.k;
+  const int nsm = num_sms();
+  // activations -> fp16
+  const int64_t nx = (int64_t)T * H;
+  const int gx = (int)((nx + 255) / 256 < 4 * nsm ? (nx + 255) / 256 : 4 * nsm);
+  if (x_dtype == COLI_BF16) k_x16<__nv_bfloat16><<<gx, 256, 0, s>>>((const __nv_bfloat16 *)p.x, p.x16, nx);
+  else k_x16<float><<<gx, 256, 0, s>>>((const float *)p.x, p.x16, nx);
+  // router logits
+  const dim3 gl((E + 63) / 64, (T + 63) / 64);
+#define COLI_LOGITS(XT, WT) \
+  k_logits<XT, WT><<<gl, 256, 0, s>>>((const XT *)p.x, (const WT *)p.wr, p.logits, T, H, E)
+  if (x_dtype == COLI_BF16 && wr_dtype == COLI_BF16) COLI_LOGITS(__nv_bfloat16, __nv_bfloat16);
+  else if (x_dtype == COLI_BF16) COLI_LOGITS(__nv_bfloat16, float);
+  else if (wr_dtype == COLI_BF16) COLI_LOGITS(float, __nv_bfloat16);
+  else COLI_LOGITS(float, float);
+#undef COLI_LOGITS
+  // top-k
+  const size_t tk_smem = (size_t)kPTopkTokens * E * 8 + (size_t)kPTopkTokens * k * 12 + 16;
+  if ((e = set_smem(k_ptopk, tk_smem)) != cudaSuccess) return e;
+  k_ptopk<<<(T + kPTopkTokens - 1) / kPTopkTokens, 256, tk_smem, s>>>(p);
+  // grouping
+  const int nb = (T + kGroupTokens - 1) / kGroupTokens;
+  k_gcount<<<nb, 256, (size_t)E * 4, s>>>(p);
+  k_gscan<<<1, 1024, 0, s>>>(p, nb);
+  k_gscatter<<<nb, 256, (size_t)E * 4, s>>>(p);
+  // GEMMs
+  if ((e = set_smem(k_pgemm<kModeGateUp>, kGemmSmem)) != cudaSuccess) return e;
+  if ((e = set_smem(k_pgemm<kModeDown>, kGemmSmem)) != cudaSuccess) return e;
+  size_t slot = 0;
+  if ((e = record_profile(COLI_KERNEL_PREFILL_GATEUP, s, false, &slot)) != cudaSuccess) return e;
+  k_pgemm<kModeGateUp><<<nsm, kGemmThreads, kGemmSmem, s>>>(p);
+  if ((e = record_profile(COLI_KERNEL_PREFILL_GATEUP, s, true, &slot)) != cudaSuccess) return e;
+  if ((e = record_profile(COLI_KERNEL_PREFILL_DOWN, s, false, &slot)) != cudaSuccess) return e;
+  k_pgemm<kModeDown><<<nsm, kGemmThreads, kGemmSmem, s>>>(p);
+  if ((e = record_profile(COLI_KERNEL_PREFILL_DOWN, s, true, &slot)) != cudaSuccess) return e;
+  // combine
+  const int64_t nc = (int64_t)T * (H / 4);
+  const int gc = (int)((nc + 255) / 256 < 8 * nsm ? (nc + 255) / 256 : 8 * nsm);
+  k_pcombine<<<gc, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace coli

@@ -101,6 +101,19 @@ def tokens(shape: MoEShape, seed=0, step=0, device="cpu", attempt=0, layer=0):
                   device=device)
 
 
+# Exponent of the skewed router: with top-8 over 256 experts and N(0, 1)
+# tokens, the 32 most-used experts take about half of all routes.
+PREFILL_SKEW = 0.28
+
+
+def skewed_router_std(E, H, gamma=PREFILL_SKEW):
+    """Per-expert router row std that falls as a power of the expert's rank,
+    (e + 1) ** -gamma, normalised to mean 1 / sqrt(H): the larger a row's
+    scale, the more often its expert is among a token's top-k."""
+    w = (np.arange(E, dtype=np.float64) + 1.0) ** (-gamma)
+    return (w / w.mean() / np.sqrt(H)).astype(np.float32)
+
+
 def router_weights(shape: MoEShape, layer, seed=0, device="cpu", row_std=None):
     """Router matrix [E, H], N(0, 1/H) of the shape's router dtype.
 

@@ -190,3 +190,52 @@ def test_glm_stack_two_deep(T):
     from the overflow a longer unnormalised chain of these layers reaches)."""
     shape = dataclasses.replace(synth.GLM_DECODE_B1, layers=2, tokens=T, chained=True)
     check_stack(shape, n_steps=1)
+
+
+def test_glm_prefill_sampled():
+    """The batched path at the prefill workload: one GLM-like layer, 4096 bf16
+    tokens, a router skewed so that 32 experts take about half of the routes.
+    Every token's route count is checked against the oracle's routing of all
+    4096 tokens (near-ties, where f32 and f64 logits may order differently,
+    are allowed to move their two routes); 16 sampled tie-free tokens' outputs
+    are checked against the oracle's layer on those tokens."""
+    c = coli()
+    shape = synth.GLM_PREFILL
+    T, H, F, E, S, k = shape.tokens, shape.hidden, shape.ffn, shape.experts, shape.shared, shape.top_k
+    eb, es = layer_geometry(H, F)
+    packed = torch.empty((E + S) * eb, dtype=torch.uint8, device="cuda")
+    scales = torch.empty((E + S) * es, dtype=torch.float32, device="cuda")
+    p0 = s0 = 0
+    for e in range(E + S):
+        mats = [synth.expert_matrix(shape, 0, e, m, SEED, device="cuda") for m in range(3)]
+        p0, s0 = quant_gpu_into(mats, packed, scales, p0, s0)
+    wr = synth.router_weights(shape, 0, SEED, device="cuda",
+                              row_std=synth.skewed_router_std(E, H))
+    x = synth.tokens(shape, SEED, 0)                     # host bf16 [T, H]
+    desc = c.MoEDesc(H, F, E, S, T, c.COLI_BF16, c.COLI_BF16)
+    ws = c.new_workspace(desc, k)
+    counts = torch.zeros(E, dtype=torch.int32, device="cuda")
+    out = c.coli_moe_forward(desc, k, x.cuda(), wr, packed, scales, ws, route_counts=counts)
+    out2 = c.coli_moe_forward(desc, k, x.cuda(), wr, packed, scales, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2), "not deterministic"
+    ol = OracleLayer(shape, 0, wr)
+    x64 = x.double().numpy()
+    lg = orc.router_logits(x64, ol.wr)
+    ocounts = np.zeros(E, np.int64)
+    gaps = np.zeros(T)
+    for t in range(T):
+        idx, _, _ = orc.topk(lg[t], k)
+        ocounts[idx] += 1
+        srt = np.sort(lg[t].astype(np.float32))[::-1]
+        gaps[t] = np.min(srt[:k] - srt[1:k + 1])
+    near = int((gaps < 1e-5).sum())
+    diff = np.abs(counts.cpu().numpy().astype(np.int64) - ocounts).sum()
+    assert diff <= 2 * near, "route counts differ by %d with %d near-ties" % (diff, near)
+    assert np.sort(ocounts)[::-1][:32].sum() > 0.4 * T * k, "router not skewed"
+    sample = [t for t in np.random.default_rng(1).permutation(T) if gaps[t] > 1e-4][:16]
+    need = np.unique(np.argsort(-lg[sample], axis=1)[:, :k + 1])
+    ol.need(need)
+    ref, _, _, _ = orc.moe_forward(x64[sample], ol.wr, ol.packed, ol.scales, H, F, E, S, k)
+    err = rel_err(out.cpu().numpy()[sample], ref)
+    assert err.max() <= REL_TOL, "max rel err %.3g" % err.max()
