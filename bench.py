@@ -34,11 +34,7 @@ METRIC = "MoE decode tokens/s and int4 expert-weight GB/s vs GB300 HBM peak"
 # each kernel from an ncu capture of the current kernel build, keyed by
 # workload and kernel; absent until such a capture exists.  The profiles/
 # summary it comes from is named beside each value.
-NCU_TRAFFIC = {
-    # profiles/k_gateup_k_down_olmoe_2layer.md (batch 1: same launches per layer
-    # as the 16-layer stack)
-    "olmoe_decode": {"k_gateup": 28456960 + 256, "k_down": 10098944},
-}
+NCU_TRAFFIC = {}
 
 
 def read_peaks():
@@ -580,7 +576,7 @@ def oracle_baseline(shape, dev, budget_s=15.0, seed=0):
 
     materialise(range(E, E + S))
     n_tok, spent = 0, 0.0
-    while spent < budget_s and n_tok < 64:
+    while spent < budget_s and n_tok < 512:
         x = synth.tokens(shape, seed, 10_000 + n_tok, device=dev).double().cpu().numpy()
         lg = orc.router_logits(x, wr)
         materialise(sorted({int(e) for row in lg for e in np.argsort(-row)[:k + 2]}))
@@ -606,7 +602,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="coli", choices=["coli", "reference"])
     ap.add_argument("--workload", default="olmoe_decode",
-                    choices=["olmoe_decode", "glm_decode_b1", "glm_decode_b8", "glm_prefill"])
+                    choices=["olmoe_decode", "glm_decode_b1", "glm_decode_b8", "glm_prefill",
+                             "quant"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the stack depth (small profiling cases only)")
@@ -624,6 +621,12 @@ def main():
     torch.cuda.set_device(dev)
 
     from int4_expert_ffn_gb300 import synth
+    if args.workload == "quant":
+        from int4_expert_ffn_gb300 import build as b
+        if rank == 0:
+            b.build()
+        emit_quant(args, dev, world, rank)
+        return
     shape = synth.SHAPES[args.workload]
     if args.layers is not None or args.tokens is not None:
         import dataclasses
@@ -697,6 +700,72 @@ def main():
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_baseline(shape, dev)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def emit_quant(args, dev, world, rank):
+    """Quantiser workload: 256 experts x {gate, up [2048, 6144], down [6144, 2048]}
+    bf16 N(0, 0.02) with 1% outliers x20, one call per matrix kind (all experts'
+    rows stacked).  Bytes moved: bf16 in, nibbles and f32 scales out."""
+    import int4_expert_ffn_gb300 as pkg
+    from int4_expert_ffn_gb300 import synth
+    c = pkg.binding
+    E, F, H = 256, 2048, 6144
+    kinds = [(F, H), (F, H), (H, F)]
+    mats = []
+    for m, (rows, cols) in enumerate(kinds):
+        w = torch.empty((E * rows, cols), dtype=torch.bfloat16, device=dev)
+        for e in range(E):
+            w[e * rows:(e + 1) * rows] = synth.matrix(rows, cols, 0.02, 0, 5, e, m, device=dev,
+                                                      outliers=0.01)
+        packed = torch.empty((E * rows, cols // 2), dtype=torch.uint8, device=dev)
+        scales = torch.empty((E * rows, cols // 64), dtype=torch.float32, device=dev)
+        mats.append((w, packed, scales))
+    elems = sum(w.numel() for w, _, _ in mats)
+    nbytes = sum(w.numel() * 2 + p.numel() + 4 * s.numel() for w, p, s in mats)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        for w, p, s in mats:
+            c.coli_quant_i4g(w, p, s, stream=stream)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[0]))
+    sampler.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    sampler.stop()
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev) / args.steps
+    hbm_peak, _, peak_kind = read_peaks()
+    gbs = nbytes / (ms / 1e3) / 1e9
+    line = {
+        "metric": "int4-grouped quantiser throughput (elements/s; bytes moved vs HBM peak)",
+        "value": world * elems / (ms / 1e3), "unit": "elements/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 -> u8 + f32",
+        "data": "synthetic (seeded bf16 N(0,0.02), 1% outliers x20)",
+        "config": {"workload": "quantiser: 256 experts x {gate, up [2048,6144], down [6144,2048]}",
+                   "elements": elems, "bytes_per_step": nbytes,
+                   "l2": "inputs larger than L2 (%.1f GB)" % (nbytes / 1e9)},
+        "roofline": {"bound": "hbm", "kernel": "k_quant_vec", "achieved": gbs, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": gbs / hbm_peak, "peak_kind": peak_kind,
+                     "traffic": None},
+        "clocks": sampler.summary(t0, t1), "gpu_launches": 3 * args.steps,
+    }
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
