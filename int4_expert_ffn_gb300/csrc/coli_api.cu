@@ -21,7 +21,9 @@ WsLayout ws_layout(int T, int H, int F, int E, int S, int k) {
   // different offsets modulo any power of two
   L.h_stride = (align256((size_t)T * KS * F * 4) + 256) / 4;
   L.x_stride = (align256((size_t)T * H * 4) + 256) / 4;
-  L.ctrl = o;      o = align256(o + kCtrlWords * sizeof(uint32_t));
+  L.ctrl = o;
+  L.fx = kFxOffset;
+  o = kWsFixedBytes;
   L.partials = o;  o = align256(o + (size_t)L.n_part * T * E * 4);
   L.idx = o;       o = align256(o + (size_t)T * k * sizeof(int32_t));
   L.gates = o;     o = align256(o + (size_t)T * k * sizeof(float));
@@ -160,6 +162,9 @@ Dec2Args make_args(const coli_moe_desc *d, int k, int tn, uint8_t *ws, const WsL
   a.g_slot_gate = (float *)(ws + L.slot_gate);
   a.h = (float *)(ws + L.h);
   a.ctrl = (uint32_t *)(ws + L.ctrl);
+  a.fx = tn * a.E <= kFxMaxTE;
+  a.fx_acc = (long long *)(ws + L.fx);
+  a.fx_flag = (uint32_t *)(ws + L.fx + (size_t)tn * a.E * 8);
   return a;
 }
 
@@ -267,10 +272,12 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
     a.layer = l;
     a.packed = packed + l * pk_stride;
     a.scales = scales + l * sc_stride;
+    // counts of layer l: added by whichever kernel routes it (the gate/up CTAs
+    // with fixed-point logits, else the last CTA of the partials' kernel)
+    a.route_counts = route_counts ? route_counts + (size_t)l * E : nullptr;
     if (l == 0) {
-      // router partials of layer 0; the last CTA routes it
+      // router partials of layer 0
       a.wr = router_w;
-      a.route_counts = route_counts;
       e = profiled(COLI_KERNEL_ROUTE, stream, [&] {
         return launch_route_partials(a, x_dtype == COLI_BF16, wr_bf16, stream, true);
       });
@@ -278,7 +285,8 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
     }
     e = profiled(COLI_KERNEL_GATEUP, stream, [&] { return launch_gateup(a, num_sms(), stream, true); });
     if (e != cudaSuccess) break;
-    // down also forms the next layer's router partials and routes it
+    // down also forms the next layer's router partials (and, without fixed-point
+    // logits, routes it in its last CTA)
     const bool next = l + 1 < n_layers;
     a.wr = next ? (const void *)((const char *)router_w + (l + 1) * wr_stride) : nullptr;
     a.next_counts = (next && route_counts) ? route_counts + (size_t)(l + 1) * E : nullptr;

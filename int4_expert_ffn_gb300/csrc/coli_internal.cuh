@@ -16,6 +16,17 @@ constexpr int kDecodeMaxT = 16;     // tokens per call served by the GEMV path
 constexpr int kMaxTopK = 64;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxShared = 8;
+// Router logits accumulated as fixed-point integers (deterministic in any
+// order) by the CTAs that form their partials; the last CTA to finish reads
+// them, routes the layer and clears them.
+constexpr int kFxMaxTE = 2048;          // tokens x experts routed this way (else a ticket)
+// The fixed-point buffers sit at one offset for every shape, right after the
+// control words, and every call leaves them zero; no other array of any
+// layout overlaps them, so a workspace zero-filled once stays valid across
+// calls of different shapes.
+constexpr size_t kFxOffset = 256;
+constexpr size_t kFxRegionBytes = (size_t)kFxMaxTE * 8 + (size_t)kFxMaxTE * 4;
+constexpr size_t kWsFixedBytes = kFxOffset + ((kFxRegionBytes + 255) & ~(size_t)255);
 // Buffers that every CTA of a kernel reads (layer input, h)
 // are written in this many copies, each read by 1/kReplicas of the CTAs, so
 // that no single L2 slice serves the whole grid.
@@ -28,11 +39,13 @@ enum CtrlWord : int {
   kCtrlPrefillMTiles = 2,  // m-tiles of the current batched call (written by the grouping)
   kCtrlWords = 64,     // 256 bytes
 };
+static_assert(kCtrlWords * 4 <= kFxOffset, "control words precede the fixed-point region");
 
 // Byte offsets of the scratch arrays inside a workspace (all 256-aligned).
 struct WsLayout {
   size_t ctrl;       // uint32[kCtrlWords]
   size_t partials;   // f32 [n_part][T][E] router partial logits
+  size_t fx;         // i64 [T][E] fixed-point logits, then u32 [T][E] flags
   size_t idx;        // i32 [T][k]
   size_t gates;      // f32 [T][k]
   size_t act;        // i32: n_active, act_expert[E+S], act_off[E+S+1]
@@ -62,6 +75,9 @@ struct DnSmem {
 struct Dec2Args {
   int T, H, F, E, S, k;
   int layer;                // index of the layer in the stack (phase tracing only)
+  int fx;                   // router partials as fixed-point sums (T*E <= kFxMaxTE)
+  long long *fx_acc;        // [T][E]
+  uint32_t *fx_flag;        // [T][E] non-finite or out-of-range partial seen
   const void *x;            // layer input [T][H], f32 or bf16
   const void *wr;           // k_route: this layer's router; k_down: next layer's (or null)
   const float *residual;    // k_down: added to the layer output (or null)

@@ -275,6 +275,19 @@ __device__ __forceinline__ LayerPtrs layer_ptrs(const Dec2Args &a) {
 }
 
 
+// Fixed-point router logits (2^-32 units): a partial p of logit (t, e) is
+// added with an integer atomic, so the total does not depend on the order in
+// which CTAs arrive.  A non-finite partial, or one of magnitude 1e7 or more,
+// marks the logit as NaN instead.
+__device__ __forceinline__ void fx_add(const Dec2Args &a, int o, float p) {
+  if (!(fabsf(p) < 1.0e7f)) {
+    atomicOr(a.fx_flag + o, 1u);
+    return;
+  }
+  atomicAdd((unsigned long long *)(a.fx_acc + o),
+            (unsigned long long)__float2ll_rn(p * 4294967296.0f));
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -295,7 +308,8 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_route(Dec2Args a) {
     float s = 0.0f;
     for (int h = h0; h < h1; ++h)
       s = fmaf(to_f32(wr[(size_t)e * a.H + h]), to_f32(x[(size_t)t * a.H + h]), s);
-    a.partials[(size_t)c * a.T * a.E + o] = s;
+    if (a.fx) fx_add(a, o, s);
+    else a.partials[(size_t)c * a.T * a.E + o] = s;
   }
   // the layer input, widened to f32, in every replica (read by all gate/up CTAs)
   if (a.xrep) {
@@ -330,7 +344,18 @@ __device__ void route_block(const Dec2Args &a, const LayerPtrs &lp, float *s_log
   const int TE = T * E;
   const int nthr = blockDim.x;
   const float *src = lp.partials;
-  if (s_stage) {
+  if (a.fx) {
+    // fixed-point sums: read once and cleared for the next use
+    for (int i = threadIdx.x; i < TE; i += nthr) {
+      const long long v = __ldcg(a.fx_acc + i);
+      const uint32_t f = __ldcg(a.fx_flag + i);
+      s_logits[i] = f ? __int_as_float(0x7FC00000) : (float)((double)v * 0x1p-32);
+      a.fx_acc[i] = 0;
+      a.fx_flag[i] = 0u;
+    }
+    __syncthreads();
+    COLI_TRACE_POINT(a.layer, kTpRtLogits);
+  } else if (s_stage) {
     // all threads copy the partials into shared memory, every load in flight at once
     const int n4 = (a.n_part * TE) / 4, tail = (a.n_part * TE) & 3;
     const float4 *s4 = (const float4 *)src;
@@ -349,9 +374,11 @@ __device__ void route_block(const Dec2Args &a, const LayerPtrs &lp, float *s_log
     src = s_stage;
   }
   const bool staged = s_stage != nullptr;
-  int nsplit = nthr / TE;
+  int nsplit = a.fx ? 0 : nthr / TE;
   if (nsplit > 8) nsplit = 8;
-  if (nsplit <= 1) {
+  if (a.fx) {
+    // logits already in shared memory
+  } else if (nsplit <= 1) {
     for (int o = threadIdx.x; o < TE; o += nthr) {
       float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
       int p = 0;
@@ -386,8 +413,8 @@ __device__ void route_block(const Dec2Args &a, const LayerPtrs &lp, float *s_log
     }
   }
   __syncthreads();
-  const bool nan = block_topk(s_logits, T, E, k, s_idx, s_gates, s_vals, s_rank,
-                              (int *)s_scratch);
+  const bool nan = select_topk(s_logits, T, E, k, s_idx, s_gates, s_vals, s_rank, (int *)s_scratch);
+  COLI_TRACE_POINT(a.layer, kTpRtTopk);
   if (publish) {
     if (threadIdx.x == 0 && nan) set_flag(a.ctrl, COLI_FLAG_NAN_LOGITS);
     for (int i = threadIdx.x; i < T * k; i += nthr) {
@@ -398,19 +425,44 @@ __device__ void route_block(const Dec2Args &a, const LayerPtrs &lp, float *s_log
   }
 }
 
+// Shared-memory layout of the routing CTA (byte offsets).
+struct RouteSmem {
+  size_t logits, topk, idx, gates, vals, scratch, act, routes, slot_gate, total;
+};
+__host__ __device__ inline RouteSmem route_smem(int T, int E, int k, int S, int n_part, bool stage) {
+  auto a16 = [](size_t v) { return (v + 15) & ~(size_t)15; };
+  RouteSmem R{};
+  size_t o = stage ? (size_t)n_part * T * E * 4 : 0;
+  R.logits = a16(o); o = R.logits + (size_t)T * E * 4;
+  R.topk = a16(o);
+  size_t tk = topk_scratch_bytes(T, E, k);
+  if (tk < (size_t)T * k * 4) tk = (size_t)T * k * 4;       // the union's sort scratch
+  o = R.topk + tk;
+  R.idx = a16(o); o = R.idx + (size_t)T * k * 4;
+  R.gates = o; o += (size_t)T * k * 4;
+  R.vals = o; o += (size_t)T * k * 4;
+  R.scratch = a16(o); o = R.scratch + (size_t)kDec2MaxThreads * 4;
+  R.act = o; o += (size_t)(2 + 2 * (E + S)) * 4;
+  R.routes = o; o += (size_t)T * (k + S) * 4;
+  R.slot_gate = o; o += (size_t)T * (k + S) * 4;
+  R.total = a16(o);
+  return R;
+}
+
 // Routing of one layer from its router partials, run by the last CTA of the
 // kernel that produced them: logits (fixed summation order), top-k, gates,
 // route counts, and the union lists the expert kernels read.  `smem` holds
 // at least route_smem_bytes(a) bytes.
 __device__ void route_finish(const Dec2Args &a, const LayerPtrs &lp, uint8_t *smem) {
   const int T = a.T, E = a.E, k = a.k, S = a.S, KS = k + S;
+  const RouteSmem R = route_smem(T, E, k, S, a.n_part, a.stage_partials);
   float *s_stage = (float *)smem;
-  float *s_logits = s_stage + (a.stage_partials ? (size_t)a.n_part * T * E : 0);
-  int *s_rank = (int *)(s_logits + T * E);
-  int *s_idx = s_rank + T * E;
-  float *s_gates = (float *)(s_idx + T * k);
-  float *s_vals = s_gates + T * k;
-  float *s_scratch = s_vals + T * k;
+  float *s_logits = (float *)(smem + R.logits);
+  int *s_rank = (int *)(smem + R.topk);
+  int *s_idx = (int *)(smem + R.idx);
+  float *s_gates = (float *)(smem + R.gates);
+  float *s_vals = (float *)(smem + R.vals);
+  float *s_scratch = (float *)(smem + R.scratch);
   route_block(a, lp, s_logits, s_idx, s_gates, s_vals, s_rank, s_scratch,
               a.stage_partials ? s_stage : nullptr, true);
   __syncthreads();
@@ -418,10 +470,11 @@ __device__ void route_finish(const Dec2Args &a, const LayerPtrs &lp, uint8_t *sm
     if (a.idx_out) a.idx_out[i] = s_idx[i];
     if (a.gates_out) a.gates_out[i] = s_gates[i];
   }
+  COLI_TRACE_POINT(a.layer, kTpRtPublish);
   if (a.build_union) {
-    int *s_act = (int *)(s_scratch + kDec2MaxThreads);
-    int *s_routes = s_act + 2 + 2 * (E + S);
-    float *s_slot_gate = (float *)(s_routes + T * KS);
+    int *s_act = (int *)(smem + R.act);
+    int *s_routes = (int *)(smem + R.routes);
+    float *s_slot_gate = (float *)(smem + R.slot_gate);
     block_union(s_idx, s_gates, T, k, S, E, s_act, s_act + 1, s_act + 1 + (E + S), s_routes,
                 s_slot_gate, s_rank);
     for (int i = threadIdx.x; i < 2 + 2 * (E + S); i += blockDim.x) a.g_act[i] = s_act[i];
@@ -429,6 +482,7 @@ __device__ void route_finish(const Dec2Args &a, const LayerPtrs &lp, uint8_t *sm
       a.g_routes[i] = s_routes[i];
       a.g_slot_gate[i] = s_slot_gate[i];
     }
+    COLI_TRACE_POINT(a.layer, kTpRtUnion);
   }
 }
 
@@ -900,6 +954,22 @@ __device__ void dn_partials(const Dec2Args &a, float *partials, const WT *s_wr, 
   }
 }
 
+// The same partial logits, added to the next layer's fixed-point buffer.
+template <typename WT>
+__device__ void dn_partials_fx(const Dec2Args &a, const WT *s_wr, const float *s_xn) {
+  const int T = a.T, H = a.H, E = a.E;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int UH = H / 4;
+  const int nr = 4 * part_lo(c + 1, UH, G) - 4 * part_lo(c, UH, G);
+  if (nr <= 0) return;
+  for (int o = threadIdx.x; o < T * E; o += blockDim.x) {
+    const int t = o / E, e = o - t * E;
+    float sum = 0.0f;
+    for (int r = 0; r < nr; ++r) sum = fmaf(to_f32(s_wr[e * nr + r]), s_xn[t * nr + r], sum);
+    fx_add(a, o, sum);
+  }
+}
+
 // This CTA's rows [dh0, dh1) of a router matrix, into shared memory.
 template <typename WT>
 __device__ void load_router_rows(const Dec2Args &a, const WT *wr, WT *s_wr) {
@@ -907,9 +977,22 @@ __device__ void load_router_rows(const Dec2Args &a, const WT *wr, WT *s_wr) {
   const int G = gridDim.x, c = blockIdx.x;
   const int UH = H / 4;
   const int dh0 = 4 * part_lo(c, UH, G), nr = 4 * part_lo(c + 1, UH, G) - dh0;
-  for (int i = threadIdx.x; i < E * nr; i += blockDim.x) {
-    const int e = i / nr, r = i - e * nr;
-    s_wr[i] = wr[(size_t)e * H + dh0 + r];
+  // eight loads in flight per thread before any store
+  for (int i0 = threadIdx.x; i0 < E * nr; i0 += 8 * blockDim.x) {
+    WT v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < E * nr) {
+        const int e = i / nr, r = i - e * nr;
+        v[u] = __ldg(wr + (size_t)e * H + dh0 + r);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < E * nr) s_wr[i] = v[u];
+    }
   }
 }
 
@@ -933,7 +1016,8 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
   dn_phase<kOne>(a, lp, s_act, s_routes, smem, s_xn, a.residual);
   COLI_TRACE_POINT(a.layer, kTpDnCombine);
   if (a.wr) {
-    dn_partials<WT>(a, a.partials, s_wr, s_xn, 1, 0);
+    if (a.fx) dn_partials_fx<WT>(a, s_wr, s_xn);
+    else dn_partials<WT>(a, a.partials, s_wr, s_xn, 1, 0);
     COLI_TRACE_POINT(a.layer, kTpDnPartials);
     // the last CTA routes the next layer (its shared memory is free again)
     LayerPtrs rp = lp;
@@ -1113,11 +1197,10 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
 
 // Shared memory the last CTA needs to route a layer (see route_finish).
 size_t route_smem_bytes(const Dec2Args &a, bool *stage) {
-  const size_t rest = (size_t)(2 * a.T * a.E + 3 * a.T * a.k + kDec2MaxThreads + 2 +
-                               2 * (a.E + a.S) + 2 * a.T * (a.k + a.S)) * 4;
-  const size_t st = (size_t)a.n_part * a.T * a.E * 4;
-  *stage = st + rest <= (size_t)max_smem() - 4096;
-  return (*stage ? st : 0) + rest;
+  const RouteSmem plain = route_smem(a.T, a.E, a.k, a.S, a.n_part, false);
+  const RouteSmem staged = route_smem(a.T, a.E, a.k, a.S, a.n_part, true);
+  *stage = !a.fx && staged.total <= (size_t)max_smem() - 4096;
+  return *stage ? staged.total : plain.total;
 }
 
 cudaError_t launch_route_partials(const Dec2Args &a_in, int x_bf16, int w_bf16, cudaStream_t s,

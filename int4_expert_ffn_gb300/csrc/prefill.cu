@@ -269,15 +269,15 @@ __global__ void __launch_bounds__(256) k_ptopk(PrefillArgs p) {
   const int T = p.T, E = p.E, k = p.k;
   const int t0 = blockIdx.x * kPTopkTokens;
   const int TB = (T - t0 < kPTopkTokens) ? T - t0 : kPTopkTokens;
-  float *lg = (float *)smem;
-  int *s_rank = (int *)(lg + kPTopkTokens * E);
-  int *s_idx = s_rank + kPTopkTokens * E;
+  float *lg = (float *)smem;                                      // [kPTopkTokens][E]
+  uint8_t *s_tk = smem + ((kPTopkTokens * E * 4 + 15) & ~15);    // top-k scratch
+  int *s_idx = (int *)(s_tk + ((topk_scratch_bytes(kPTopkTokens, E, k) + 15) & ~(size_t)15));
   float *s_gates = (float *)(s_idx + kPTopkTokens * k);
   float *s_vals = s_gates + kPTopkTokens * k;
   int *s_flag = (int *)(s_vals + kPTopkTokens * k);
   for (int i = threadIdx.x; i < TB * E; i += blockDim.x) lg[i] = p.logits[(size_t)t0 * E + i];
   __syncthreads();
-  const bool nan = block_topk(lg, TB, E, k, s_idx, s_gates, s_vals, s_rank, s_flag);
+  const bool nan = select_topk(lg, TB, E, k, s_idx, s_gates, s_vals, s_tk, s_flag);
   if (threadIdx.x == 0 && nan) set_flag_p(p.ctrl, COLI_FLAG_NAN_LOGITS);
   for (int i = threadIdx.x; i < TB * k; i += blockDim.x) {
     p.idx[(size_t)t0 * k + i] = s_idx[i];
@@ -639,7 +639,7 @@ PrefillLayout prefill_layout(int T, int H, int F, int E, int S, int k) {
   PrefillLayout L{};
   const size_t P = (size_t)T * (k + S);
   const size_t nb = ((size_t)T + kGroupTokens - 1) / kGroupTokens;
-  size_t o = a256(kCtrlWords * 4);
+  size_t o = kWsFixedBytes;         // control words and the decode path's fixed region first
   L.x16 = o;        o = a256(o + (size_t)T * H * 2);
   L.logits = o;     o = a256(o + (size_t)T * E * 4);
   L.idx = o;        o = a256(o + (size_t)T * k * 4);
@@ -682,7 +682,9 @@ cudaError_t launch_prefill(const PrefillArgs &p, int x_dtype, int wr_dtype, cuda
   else COLI_LOGITS(float, float);
 #undef COLI_LOGITS
   // top-k
-  const size_t tk_smem = (size_t)kPTopkTokens * E * 8 + (size_t)kPTopkTokens * k * 12 + 16;
+  const size_t tk_smem = (((size_t)kPTopkTokens * E * 4 + 15) & ~(size_t)15) +
+                         ((topk_scratch_bytes(kPTopkTokens, E, k) + 15) & ~(size_t)15) +
+                         (size_t)kPTopkTokens * k * 12 + 16;
   if ((e = set_smem(k_ptopk, tk_smem)) != cudaSuccess) return e;
   k_ptopk<<<(T + kPTopkTokens - 1) / kPTopkTokens, 256, tk_smem, s>>>(p);
   // grouping

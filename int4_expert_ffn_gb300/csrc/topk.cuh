@@ -18,46 +18,10 @@ __device__ __forceinline__ bool ranks_before(float a, int ia, float b, int ib) {
   return ia < ib;
 }
 
-// Block-parallel top-k of T tokens x E logits (shared memory), every thread of
-// the block taking part.  The rank of logit (t, e) is the number of logits of
-// token t that rank before it; the work is split into chunks whose counts are
-// added with shared-memory integer atomics, so the result does not depend on
-// scheduling.  s_rank: T*E ints of scratch.  Writes idx/gates [T][k]; returns
-// true (on every thread) if any logit is NaN.
-__device__ __forceinline__ bool block_topk(const float *lg, int T, int E, int k, int *idx,
-                                           float *gates, float *vals, int *s_rank, int *s_flag) {
-  const int tid = threadIdx.x, nthr = blockDim.x;
-  const int TE = T * E;
-  int P = (nthr * 8) / TE;
-  if (P < 1) P = 1;
-  if (P > E / 8) P = E / 8 > 0 ? E / 8 : 1;
-  for (int i = tid; i < TE; i += nthr) s_rank[i] = 0;
-  if (tid == 0) *s_flag = 0;
-  __syncthreads();
-  const int chunk = (E + P - 1) / P;
-  for (int i = tid; i < TE * P; i += nthr) {
-    const int item = i / P, part = i - item * P;
-    const int t = item / E, e = item - t * E;
-    const float *lt = lg + t * E;
-    const float v = lt[e];
-    const int e0 = part * chunk, e1 = e0 + chunk < E ? e0 + chunk : E;
-    int r = 0;
-    for (int e2 = e0; e2 < e1; ++e2) r += ranks_before(lt[e2], e2, v, e);
-    if (r) atomicAdd(s_rank + item, r);
-    if (part == 0 && v != v) *s_flag = 1;
-  }
-  __syncthreads();
-  for (int i = tid; i < TE; i += nthr) {
-    const int r = s_rank[i];
-    if (r < k) {
-      const int t = i / E;
-      idx[t * k + r] = i - t * E;
-      vals[t * k + r] = lg[i];
-    }
-  }
-  __syncthreads();
-  // gates = exp(l_j - l_0) / sum_j' exp(l_j' - l_0); NaN picks 0; all NaN -> 1/k
-  for (int i = tid; i < T * k; i += nthr) {
+// Renormalised gates of T tokens from their picked logits (rank order):
+// exp(l_j - l_0) / sum_j' exp(l_j' - l_0); a NaN pick gets 0; all NaN -> 1/k.
+__device__ __forceinline__ void block_gates(const float *vals, int T, int k, float *gates) {
+  for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
     const int t = i / k;
     const float *vt = vals + t * k;
     const float l0 = vt[0];
@@ -72,9 +36,198 @@ __device__ __forceinline__ bool block_topk(const float *lg, int T, int E, int k,
     }
     gates[i] = g;
   }
+}
+
+// Order key of a logit: the float order mapped onto unsigned integers, NaN
+// lowest and -0 folded into +0.  ranks_before(a, ia, b, ib) is exactly
+// key(a) > key(b) || (key(a) == key(b) && ia < ib).
+__device__ __forceinline__ uint32_t topk_key(float v) {
+  v = v + 0.0f;
+  const uint32_t b = __float_as_uint(v);
+  return (v != v) ? 0u : ((b & 0x80000000u) ? ~b : (b | 0x80000000u));
+}
+
+__device__ __forceinline__ int rank_step(uint32_t o, int j, uint32_t key, int e) {
+  return (o > key) | ((o == key) & (j < e));
+}
+
+// Top-k of T tokens x E logits (shared memory): one thread per logit counts
+// the logits of its token that rank before it (its rank) and, if the rank is
+// below k, writes itself to that slot; no atomics, results independent of
+// scheduling.  s_key: T*E 32-bit words of scratch (16-byte aligned).  Returns
+// true (on every thread) if any logit is NaN.
+__device__ __forceinline__ bool rank_topk(const float *lg, int T, int E, int k, int *idx,
+                                          float *gates, float *vals, uint32_t *s_key,
+                                          int *s_flag) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int TE = T * E;
+  if (tid == 0) *s_flag = 0;
+  __syncthreads();
+  for (int i = tid; i < TE; i += nthr) {
+    const float v = lg[i];
+    s_key[i] = topk_key(v);
+    if (v != v) *s_flag = 1;
+  }
+  __syncthreads();
+  const bool vec = (E & 3) == 0 && ((uintptr_t)s_key & 15) == 0;
+  for (int i = tid; i < TE; i += nthr) {
+    const int t = i / E, e = i - t * E;
+    const uint32_t key = s_key[i];
+    const uint32_t *row = s_key + (size_t)t * E;
+    int r = 0, j = 0;
+    if (vec) {
+      const uint4 *row4 = (const uint4 *)row;
+      for (; j + 16 <= E; j += 16) {
+        uint4 q[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) q[u] = row4[j / 4 + u];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int jj = j + 4 * u;
+          r += rank_step(q[u].x, jj, key, e) + rank_step(q[u].y, jj + 1, key, e) +
+               rank_step(q[u].z, jj + 2, key, e) + rank_step(q[u].w, jj + 3, key, e);
+        }
+      }
+    }
+    for (; j < E; ++j) r += rank_step(row[j], j, key, e);
+    if (r < k) {
+      idx[t * k + r] = e;
+      vals[t * k + r] = lg[i];
+    }
+  }
+  __syncthreads();
+  block_gates(vals, T, k, gates);
   const bool nan = *(volatile int *)s_flag != 0;
   __syncthreads();
   return nan;
+}
+
+// Top-k of one token's E logits by one warp: k rounds of a warp arg-max under
+// ranks_before (a total order), each lane scanning its elements e = lane + 32 i
+// (E <= 1024) and skipping the ones already taken.  Lane 0 writes idx / vals in
+// rank order.  Returns true on every lane if any logit is NaN.
+__device__ __forceinline__ bool warp_topk_row(const float *lg, int E, int k, int *idx,
+                                              float *vals) {
+  const int lane = threadIdx.x & 31;
+  uint32_t taken = 0;
+  bool nan = false;
+  for (int e = lane; e < E; e += 32) nan |= lg[e] != lg[e];
+  for (int j = 0; j < k; ++j) {
+    float bv = 0.0f;
+    int bi = -1;
+    for (int i = 0, e = lane; e < E; ++i, e += 32) {
+      if ((taken >> i) & 1u) continue;
+      const float v = lg[e];
+      if (bi < 0 || ranks_before(v, e, bv, bi)) {
+        bv = v;
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
+      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
+      if (oi >= 0 && (bi < 0 || ranks_before(ov, oi, bv, bi))) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == 0) {
+      idx[j] = bi;
+      vals[j] = bv;
+    }
+  }
+  return __any_sync(0xFFFFFFFFu, nan) != 0;
+}
+
+// Top-k of T tokens by the block's warps (one token per warp at a time), then
+// the gates.  Same results as block_topk.  s_flag: one int of scratch.
+__device__ __forceinline__ bool warp_topk(const float *lg, int T, int E, int k, int *idx,
+                                          float *gates, float *vals, int *s_flag) {
+  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (threadIdx.x == 0) *s_flag = 0;
+  __syncthreads();
+  for (int t = warp; t < T; t += nw)
+    if (warp_topk_row(lg + (size_t)t * E, E, k, idx + t * k, vals + t * k) &&
+        (threadIdx.x & 31) == 0)
+      *s_flag = 1;
+  __syncthreads();
+  block_gates(vals, T, k, gates);
+  const bool nan = *(volatile int *)s_flag != 0;
+  __syncthreads();
+  return nan;
+}
+
+// Top-k by a tournament (k <= 32): each warp sorts a 32-logit chunk of one
+// token with a shuffle bitonic network on 64-bit keys (order key, then the
+// complement of the expert id, so keys are distinct and larger ranks first;
+// padding is 0, below every logit) and keeps its k best; one thread per
+// candidate then counts the token's larger candidates.  s_cand: T *
+// ceil(E/32) * k 64-bit words.  Returns true (on every thread) if any logit
+// is NaN.
+__device__ __forceinline__ bool tournament_topk(const float *lg, int T, int E, int k, int *idx,
+                                                float *gates, float *vals,
+                                                unsigned long long *s_cand, int *s_flag) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  const int nch = (E + 31) >> 5, C = nch * k;
+  if (tid == 0) *s_flag = 0;
+  __syncthreads();
+  for (int task = warp; task < T * nch; task += nw) {
+    const int t = task / nch, ch = task - t * nch, e = 32 * ch + lane;
+    unsigned long long key = 0ull;
+    if (e < E) {
+      const float v = lg[(size_t)t * E + e];
+      if (v != v) *s_flag = 1;
+      key = ((unsigned long long)topk_key(v) << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)e);
+    }
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, key, stride);
+        const bool desc = (lane & size) == 0, first = (lane & stride) == 0;
+        const unsigned long long mx = key > o ? key : o, mn = key > o ? o : key;
+        key = (first == desc) ? mx : mn;
+      }
+    if (lane < k) s_cand[(size_t)t * C + ch * k + lane] = key;
+  }
+  __syncthreads();
+  for (int i = tid; i < T * C; i += blockDim.x) {
+    const int t = i / C;
+    const unsigned long long c = s_cand[i];
+    if (c == 0ull) continue;
+    const unsigned long long *row = s_cand + (size_t)t * C;
+    int r = 0;
+    for (int j = 0; j < C; ++j) r += row[j] > c;
+    if (r < k) {
+      const int e = (int)(0xFFFFFFFFu - (uint32_t)c);
+      idx[t * k + r] = e;
+      vals[t * k + r] = lg[(size_t)t * E + e];
+    }
+  }
+  __syncthreads();
+  block_gates(vals, T, k, gates);
+  const bool nan = *(volatile int *)s_flag != 0;
+  __syncthreads();
+  return nan;
+}
+
+// Scratch bytes select_topk needs (16-byte aligned start).
+__host__ __device__ constexpr size_t topk_scratch_bytes(int T, int E, int k) {
+  return ((size_t)T * E * 4 > (size_t)T * ((E + 31) / 32) * k * 8 ? (size_t)T * E * 4
+                                                                   : (size_t)T * ((E + 31) / 32) * k * 8);
+}
+
+// The block's top-k by the faster method for the size: the tournament for
+// k <= 32, else rank counting for up to 1024 logits, else a warp per token.
+__device__ __forceinline__ bool select_topk(const float *lg, int T, int E, int k, int *idx,
+                                            float *gates, float *vals, void *scratch,
+                                            int *s_flag) {
+  if (k <= 32)
+    return tournament_topk(lg, T, E, k, idx, gates, vals, (unsigned long long *)scratch, s_flag);
+  if (T * E <= 1024) return rank_topk(lg, T, E, k, idx, gates, vals, (uint32_t *)scratch, s_flag);
+  return warp_topk(lg, T, E, k, idx, gates, vals, s_flag);
 }
 
 // Block-parallel union lists (see warp_union for the layout).  s_sorted: T*k
@@ -103,20 +256,28 @@ __device__ __forceinline__ int block_union(const int *idx, const float *gates, i
     routes[n + s * T + t] = t * KS + k + s;
   }
   __syncthreads();
-  if (tid == 0) {
+  if (tid < 32) {
+    // group starts in sorted order, 32 positions per step (warp ballot)
     int na = 0;
-    for (int p = 0; p < n; ++p)
-      if (p == 0 || s_sorted_e[p] != s_sorted_e[p - 1]) {
-        act_expert[na] = s_sorted_e[p];
-        act_off[na] = p;
-        ++na;
+    for (int p0 = 0; p0 < n; p0 += 32) {
+      const int p = p0 + tid;
+      const bool first = p < n && (p == 0 || s_sorted_e[p] != s_sorted_e[p - 1]);
+      const uint32_t m = __ballot_sync(0xFFFFFFFFu, first);
+      if (first) {
+        const int gi = na + __popc(m & ((1u << tid) - 1u));
+        act_expert[gi] = s_sorted_e[p];
+        act_off[gi] = p;
       }
-    for (int s = 0; s < S; ++s) {
+      na += __popc(m);
+    }
+    for (int s = tid; s < S; s += 32) {
       act_expert[na + s] = E + s;
       act_off[na + s] = n + s * T;
     }
-    act_off[na + S] = n + S * T;
-    act[0] = na + S;
+    if (tid == 0) {
+      act_off[na + S] = n + S * T;
+      act[0] = na + S;
+    }
   }
   __syncthreads();
   return act[0];

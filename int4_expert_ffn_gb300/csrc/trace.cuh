@@ -9,7 +9,7 @@
 
 namespace coli {
 
-constexpr int kTraceLayers = 64, kTracePoints = 16;
+constexpr int kTraceLayers = 64, kTracePoints = 24;
 
 #ifdef COLI_TRACE
 // Defined here; only the decode translation unit includes this header.
@@ -32,6 +32,7 @@ enum TracePoint : int {
   kTpGuEntry = 0, kTpGuDepWait, kTpGuLists, kTpGuPlanes, kTpGuFirstLoads, kTpGuCompute, kTpGuEnd,
   kTpDnEntry, kTpDnDepWait, kTpDnLists, kTpDnPlanes, kTpDnCompute, kTpDnCombine,
   kTpDnPartials, kTpRouteStart, kTpEnd,
+  kTpRtLogits, kTpRtTopk, kTpRtPublish, kTpRtUnion,
 };
 
 }  // namespace coli
