@@ -34,7 +34,13 @@ METRIC = "MoE decode tokens/s and int4 expert-weight GB/s vs GB300 HBM peak"
 # each kernel from an ncu capture of the current kernel build, keyed by
 # workload and kernel; absent until such a capture exists.  The profiles/
 # summary it comes from is named beside each value.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/k_gateup_k_down_olmoe_2layer.md (batch 1: the same launch per layer
+    # as the 16-layer stack; cold-cache capture)
+    "olmoe_decode": {"k_gateup": 28446976, "k_down": 10076672},
+    # profiles/k_gateup_k_down_glm_layer.md
+    "glm_decode_b1": {"k_gateup": 154663424 + 3702272, "k_down": 64362240 + 419840},
+}
 
 
 def read_peaks():
