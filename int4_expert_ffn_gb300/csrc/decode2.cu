@@ -619,6 +619,24 @@ __device__ void load_lists(const Dec2Args &a, int *s_act, int *s_routes, float *
   __syncthreads();
 }
 
+// L2 prefetch of the down rows [dh0, dh1) of every used expert (the rows that
+// CTA c owns in the down kernel), one bulk prefetch per expert and lane.
+__device__ __forceinline__ void prefetch_down_rows(const Dec2Args &a, const LayerPtrs &lp,
+                                                   const int *s_act_expert, int n_active, int c) {
+  if (c >= a.n_part) return;
+  const int H = a.H, F = a.F, lane = threadIdx.x & 31;
+  const int64_t ngr = H / kGroup;
+  const int UH = H / 4;
+  const int dh0 = 4 * part_lo(c, UH, a.n_part), dh1 = 4 * part_lo(c + 1, UH, a.n_part);
+  for (int q = lane; q < n_active && dh1 > dh0; q += 32) {
+    const int e = s_act_expert[q];
+    prefetch_l2(lp.packed + (int64_t)e * a.eb + (int64_t)F * H + (int64_t)dh0 * (F / 2),
+                (uint32_t)((dh1 - dh0) * (F / 2)));
+    prefetch_l2(lp.scales + (int64_t)e * a.es + (int64_t)2 * F * ngr + (int64_t)dh0 * (F / kGroup),
+                (uint32_t)((dh1 - dh0) * (F / 16)));
+  }
+}
+
 // kOne: one token per call (every used expert serves token 0): the planes of
 // the warp's chunk stay in registers and the token loop disappears.
 template <bool kOne>
@@ -659,20 +677,6 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
     ci.init(warp, ncg, row0 + rb0, F);
     cc = ci;
     if (rb0 == 0) {
-      // L2 prefetch of the down rows that this CTA index reads in the down kernel
-      if (warp == 0 && c < a.n_part) {
-        const int64_t ngr = H / kGroup;
-        const int UH = H / 4;
-        const int dh0 = 4 * part_lo(c, UH, a.n_part), dh1 = 4 * part_lo(c + 1, UH, a.n_part);
-        for (int q = lane; q < n_active && dh1 > dh0; q += 32) {
-          const int e = s_act_expert[q];
-          prefetch_l2(lp.packed + (int64_t)e * a.eb + (int64_t)F * H + (int64_t)dh0 * (F / 2),
-                      (uint32_t)((dh1 - dh0) * (F / 2)));
-          prefetch_l2(lp.scales + (int64_t)e * a.es + (int64_t)2 * F * ngr +
-                          (int64_t)dh0 * (F / kGroup),
-                      (uint32_t)((dh1 - dh0) * (F / 16)));
-        }
-      }
       if (a.gu_xpl) {
         build_planes_impl(xr, T, H, nullptr, s_xpl, nbx, warp, NW);
         __syncthreads();
@@ -695,6 +699,12 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
         gu_copy(a, lp, s_act_expert, ring + (size_t)((i + S - 1) % S) * kGuSlotBytes, ci,
                 vec_scales);
         ci.next(dg, dcg, ncg, F);
+      }
+      if (i == (my_tasks > S - 1 ? my_tasks - (S - 1) : 0) && warp == 0 &&
+          rb0 + a.gu_rows >= nrows) {
+        // every gate/up copy of this warp is issued: L2 prefetch of the down rows
+        // that this CTA index reads in the down kernel, behind this kernel's own stream
+        prefetch_down_rows(a, lp, s_act_expert, n_active, c);
       }
       cp_async_commit();
       cp_async_wait_dyn(S - 1);      // this lane's copies of task i have landed
