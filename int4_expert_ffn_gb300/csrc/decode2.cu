@@ -676,8 +676,11 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
     GuTask ci, cc;      // the next task to copy, the next task to compute
     ci.init(warp, ncg, row0 + rb0, F);
     cc = ci;
+    // one token: every warp quantises its own 1024-column slice of x when it
+    // first needs it (kept in registers), so no warp waits for a block-wide build
+    const bool xpl = a.gu_xpl && !kOne;
     if (rb0 == 0) {
-      if (a.gu_xpl) {
+      if (xpl) {
         build_planes_impl(xr, T, H, nullptr, s_xpl, nbx, warp, NW);
         __syncthreads();
       }
@@ -723,7 +726,7 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
         if (act) {
           const int key = t * ncg + cc.cg;
           if (key != pl_key) {
-            if (a.gu_xpl) {
+            if (xpl) {
               load_planes(s_xpl, t, col / 32, nbx, pl);
             } else {
               float xv[32];
