@@ -162,6 +162,7 @@ Dec2Args make_args(const coli_moe_desc *d, int k, int tn, uint8_t *ws, const WsL
   a.g_slot_gate = (float *)(ws + L.slot_gate);
   a.h = (float *)(ws + L.h);
   a.ctrl = (uint32_t *)(ws + L.ctrl);
+  a.wr_bf16 = d->router_dtype == COLI_BF16;
   a.fx = tn * a.E <= kFxMaxTE;
   a.fx_acc = (long long *)(ws + L.fx);
   a.fx_flag = (uint32_t *)(ws + L.fx + (size_t)tn * a.E * 8);

@@ -107,11 +107,14 @@ struct Dec2Args {
   int gu_ncg;               // 1024-column chunks of a gate/up row
   int gu_nw;                // warps of k_gateup
   int gu_slots;             // depth of each warp's cp.async pipeline (2..4)
+  int gu_slot_bytes;        // bytes of one pipeline slot (weights + scales)
   int gu_rows;              // rows whose partial sums fit in shared memory at once
   int gu_xpl;               // x planes held in shared memory
   int dn_ncg;               // 1024-column chunks of a down row
   int dn_nw;                // warps of k_down
   int dn_slots_pipe;        // depth of each warp's cp.async pipeline
+  int dn_slot_bytes;
+  int wr_bf16;              // the router (and its rows in k_down's shared memory) is bf16
   int dn_slots;             // token slots whose planes fit in shared memory at once
   int dn_batch;             // experts whose partial sums fit in shared memory at once
   GuSmem gu;

@@ -516,8 +516,12 @@ __device__ void route_if_last(const Dec2Args &a, const LayerPtrs &lp, uint8_t *s
 // memory; rows are finalised in batches of gu_rows into h = silu(g) * u *
 // gate, written to every replica.
 
-// slot: weights [8 rows][32 lanes][16 B] | scales [8 rows][32] f32
-constexpr int kGuSlotBytes = 8 * 32 * 16 + 8 * 32 * 4;
+// slot: weights [8 rows][32 lanes][16 B] | scales: [8 rows][16 groups] f32 when
+// the row's scales are 16-byte aligned (K % 256 == 0), else [8 rows][32 lanes]
+constexpr int kGuSlotWeights = 8 * 32 * 16;
+__host__ __device__ constexpr int slot_bytes(int K) {
+  return kGuSlotWeights + (K % 256 == 0 ? 8 * 16 * 4 : 8 * 32 * 4);
+}
 
 __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
@@ -539,7 +543,9 @@ __device__ __forceinline__ void cp_async_wait_dyn(int n) {
     case 0: cp_async_wait<0>(); break;
     case 1: cp_async_wait<1>(); break;
     case 2: cp_async_wait<2>(); break;
-    default: cp_async_wait<3>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    default: cp_async_wait<5>(); break;
   }
 }
 
@@ -575,7 +581,7 @@ __device__ __forceinline__ void gu_copy(const Dec2Args &a, const LayerPtrs &lp,
   const int col = k.cg * kChunkCols + 32 * lane;
   const uint8_t *pg = lp.packed + (int64_t)e * a.eb + (int64_t)k.f * rb;
   const float *ps = lp.scales + (int64_t)e * a.es + (int64_t)k.f * ngr + k.cg * 16;
-  float *ss = (float *)(slot + 8 * 32 * 16);
+  float *ss = (float *)(slot + kGuSlotWeights);
   if (col < H) {
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
@@ -600,7 +606,7 @@ __device__ __forceinline__ void gu_copy(const Dec2Args &a, const LayerPtrs &lp,
 __device__ __forceinline__ void gu_slot_values(const uint8_t *slot, bool act, bool vec_scales,
                                                uint4 (&w)[8], float (&sc)[8]) {
   const int lane = threadIdx.x & 31;
-  const float *ss = (const float *)(slot + 8 * 32 * 16);
+  const float *ss = (const float *)(slot + kGuSlotWeights);
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     w[q] = act ? *(const uint4 *)(slot + (q * 32 + lane) * 16) : make_uint4(0, 0, 0, 0);
@@ -667,7 +673,8 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
   const int ncg = a.gu_ncg, S = a.gu_slots, nbx = H / 32;
   const int dg = NW / ncg, dcg = NW - dg * ncg;
   const bool vec_scales = (H % 256) == 0;
-  uint8_t *ring = smem + L.ring + (size_t)warp * S * kGuSlotBytes;
+  const int SB = a.gu_slot_bytes;
+  uint8_t *ring = smem + L.ring + (size_t)warp * S * SB;
 
   for (int rb0 = 0; rb0 < nrows; rb0 += a.gu_rows) {
     const int nrb = nrows - rb0 < a.gu_rows ? nrows - rb0 : a.gu_rows;
@@ -689,7 +696,7 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
     // prologue: the first S - 1 tasks of this warp in flight
     for (int p = 0; p < S - 1; ++p) {
       if (p < my_tasks) {
-        gu_copy(a, lp, s_act_expert, ring + (size_t)p * kGuSlotBytes, ci, vec_scales);
+        gu_copy(a, lp, s_act_expert, ring + (size_t)p * SB, ci, vec_scales);
         ci.next(dg, dcg, ncg, F);
       }
       cp_async_commit();
@@ -699,7 +706,7 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
     int pl_key = -1;            // (token, chunk) whose planes are in `pl`
     for (int i = 0; i < my_tasks; ++i) {
       if (i + S - 1 < my_tasks) {
-        gu_copy(a, lp, s_act_expert, ring + (size_t)((i + S - 1) % S) * kGuSlotBytes, ci,
+        gu_copy(a, lp, s_act_expert, ring + (size_t)((i + S - 1) % S) * SB, ci,
                 vec_scales);
         ci.next(dg, dcg, ncg, F);
       }
@@ -712,7 +719,7 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
       cp_async_commit();
       cp_async_wait_dyn(S - 1);      // this lane's copies of task i have landed
       if (vec_scales) __syncwarp();  // scales were copied by other lanes
-      const uint8_t *slot = ring + (size_t)(i % S) * kGuSlotBytes;
+      const uint8_t *slot = ring + (size_t)(i % S) * SB;
       const int col = cc.cg * kChunkCols + 32 * lane;
       const bool act = col < H;
       uint4 w[8];
@@ -814,7 +821,7 @@ __device__ __forceinline__ void dn_copy(const Dec2Args &a, const LayerPtrs &lp,
   const uint8_t *pw = lp.packed + (int64_t)e * a.eb + (int64_t)F * H + (int64_t)(dh0 + r0) * rb;
   const float *ps = lp.scales + (int64_t)e * a.es + (int64_t)2 * F * (H / kGroup) +
                     (int64_t)(dh0 + r0) * ngr + k.cg * 16;
-  float *ss = (float *)(slot + 8 * 32 * 16);
+  float *ss = (float *)(slot + kGuSlotWeights);
   if (col < F) {
 #pragma unroll
     for (int q = 0; q < 8; ++q)
@@ -851,7 +858,8 @@ __device__ void dn_phase(const Dec2Args &a, const LayerPtrs &lp, const int *s_ac
   float *acc = (float *)(smem + L.acc);          // [nr][T]
   float *red = (float *)(smem + L.red);          // [batch expert][nr][T][ncg]
   uint32_t *s_planes = (uint32_t *)(smem + L.planes);
-  uint8_t *ring = smem + L.ring + (size_t)warp * Sl * kGuSlotBytes;
+  const int SB = a.dn_slot_bytes;
+  uint8_t *ring = smem + L.ring + (size_t)warp * Sl * SB;
   for (int i = tid; i < nr * T; i += blockDim.x) acc[i] = 0.0f;
   // experts in batches: their slots' planes and their partial sums must fit
   for (int ga = 0; ga < n_active;) {
@@ -871,7 +879,7 @@ __device__ void dn_phase(const Dec2Args &a, const LayerPtrs &lp, const int *s_ac
     if (ga == 0) COLI_TRACE_POINT(a.layer, kTpDnPlanes);
     for (int p = 0; p < Sl - 1; ++p) {
       if (p < my_tasks) {
-        dn_copy(a, lp, s_act_expert, ring + (size_t)p * kGuSlotBytes, ci, dh0, nr, vec_scales);
+        dn_copy(a, lp, s_act_expert, ring + (size_t)p * SB, ci, dh0, nr, vec_scales);
         ci.next(du, dcg, ncg, gpe);
       }
       cp_async_commit();
@@ -880,14 +888,14 @@ __device__ void dn_phase(const Dec2Args &a, const LayerPtrs &lp, const int *s_ac
     int pl_key = -1;
     for (int i = 0; i < my_tasks; ++i) {
       if (i + Sl - 1 < my_tasks) {
-        dn_copy(a, lp, s_act_expert, ring + (size_t)((i + Sl - 1) % Sl) * kGuSlotBytes, ci, dh0,
+        dn_copy(a, lp, s_act_expert, ring + (size_t)((i + Sl - 1) % Sl) * SB, ci, dh0,
                 nr, vec_scales);
         ci.next(du, dcg, ncg, gpe);
       }
       cp_async_commit();
       cp_async_wait_dyn(Sl - 1);
       if (vec_scales) __syncwarp();
-      const uint8_t *slot = ring + (size_t)(i % Sl) * kGuSlotBytes;
+      const uint8_t *slot = ring + (size_t)(i % Sl) * SB;
       const int col = cc.cg * kChunkCols + 32 * lane;
       const bool act = col < F;
       const int r0 = 8 * cc.gi, nq = nr - r0 < 8 ? nr - r0 : 8;
@@ -1127,13 +1135,18 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
   const size_t xpl_bytes = al16((size_t)T * 18 * (H / 32) * 4);
   const size_t row_bytes = (size_t)T * a.gu_ncg * 2 * 4;
   const int min_batch = max_rows < 64 ? max_rows : 64;
-  // warps x slots, by bytes in flight ahead of the compute: 12 x 3, then 16 x 2, ...
+  // warps x slots, by bytes in flight ahead of the compute: 12 x 3, 16 x 2, ...
+  // A one-token call quantises x per warp for the chunk it works on, so warp
+  // counts that keep every warp on one chunk (NW % gu_ncg == 0) come first.
   static const int kNw[] = {12, 16, 8, 8, 4};
   static const int kSl[] = {3, 2, 3, 2, 2};
+  a.gu_slot_bytes = slot_bytes(H);
   bool ok = false;
-  for (int xpl = 1; xpl >= 0 && !ok; --xpl)
+  for (int pass = 0; pass < 4 && !ok; ++pass) {
+    const int xpl = T > 1 && pass < 2, strict = T == 1 && (pass & 1) == 0;
     for (int c = 0; c < 5 && !ok; ++c) {
-      const size_t ring = (size_t)kNw[c] * kSl[c] * kGuSlotBytes;
+      if (strict && kNw[c] % a.gu_ncg != 0) continue;
+      const size_t ring = (size_t)kNw[c] * kSl[c] * a.gu_slot_bytes;
       const size_t need = o + (xpl ? xpl_bytes : 0) + ring + 128 + (size_t)min_batch * row_bytes;
       if (need <= budget) {
         a.gu_xpl = xpl;
@@ -1142,9 +1155,10 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
         ok = true;
       }
     }
+  }
   if (!ok) return cudaErrorInvalidValue;
   g.xpl = o; o += a.gu_xpl ? xpl_bytes : 0;
-  g.ring = al128(o); o = g.ring + (size_t)a.gu_nw * a.gu_slots * kGuSlotBytes;
+  g.ring = al128(o); o = g.ring + (size_t)a.gu_nw * a.gu_slots * a.gu_slot_bytes;
   g.red = al16(o);
   size_t fit = (budget - g.red) / row_bytes;
   int rows = fit < (size_t)max_rows ? (int)fit : max_rows;
@@ -1164,17 +1178,20 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
   d.routes = o; o = al16(o + (size_t)T * KS * 4);
   d.acc = o; o = al16(o + (size_t)max_nr * T * 4);
   d.xn = o; o = al16(o + (size_t)T * max_nr * 4);
-  d.wr = o; o = al16(o + (size_t)E * max_nr * 4);
+  d.wr = o; o = al16(o + (size_t)E * max_nr * (a.wr_bf16 ? 2 : 4));
   const size_t per_slot = (size_t)18 * (F / 32) * 4;
   const size_t per_expert_red = (size_t)max_nr * T * a.dn_ncg * 4;
   const int all_slots = T * KS;
+  a.dn_slot_bytes = slot_bytes(F);
   // the largest tokens-per-expert count is T (routed) or T (shared)
-  static const int kDnNw[] = {12, 8, 16, 8, 12, 8, 4};
-  static const int kDnSl[] = {3, 4, 2, 3, 2, 2, 2};
+  // more warps before deeper pipelines: each warp works its tasks in order, so
+  // the down phase's latency follows the tasks per warp
+  static const int kDnNw[] = {16, 12, 8, 12, 8, 8, 4};
+  static const int kDnSl[] = {2, 3, 4, 2, 3, 2, 2};
   bool dn_ok = false;
   for (int pass = 0; pass < 2 && !dn_ok; ++pass)
     for (int c = 0; c < 7 && !dn_ok; ++c) {
-      const size_t ring = (size_t)kDnNw[c] * kDnSl[c] * kGuSlotBytes;
+      const size_t ring = (size_t)kDnNw[c] * kDnSl[c] * a.dn_slot_bytes;
       const size_t base = al128(o) + ring + 128;
       if (base >= budget) continue;
       // pass 0: every slot's planes and every used expert's partials at once
@@ -1200,7 +1217,7 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
       dn_ok = true;
     }
   if (!dn_ok) return cudaErrorInvalidValue;
-  d.ring = al128(o); o = d.ring + (size_t)a.dn_nw * a.dn_slots_pipe * kGuSlotBytes;
+  d.ring = al128(o); o = d.ring + (size_t)a.dn_nw * a.dn_slots_pipe * a.dn_slot_bytes;
   d.red = al16(o); o = d.red + (size_t)a.dn_batch * per_expert_red;
   d.planes = al16(o); o = al16(d.planes + (size_t)a.dn_slots * per_slot);
   d.total = o;
