@@ -64,7 +64,7 @@ constexpr int kDec2MaxThreads = 512;
 
 // Shared-memory plan of k_gateup (byte offsets into dynamic smem).
 struct GuSmem {
-  size_t act, routes, slot_gate, xpl, ring, red, total;
+  size_t act, routes, slot_gate, tok, xpl, ring, red, total;
 };
 // Shared-memory plan of k_down.
 struct DnSmem {

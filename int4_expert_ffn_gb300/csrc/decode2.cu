@@ -643,9 +643,9 @@ __device__ __forceinline__ void prefetch_down_rows(const Dec2Args &a, const Laye
   }
 }
 
-// kOne: one token per call (every used expert serves token 0): the planes of
-// the warp's chunk stay in registers and the token loop disappears.
-template <bool kOne>
+// One token per call: every used expert serves token 0, each warp quantises
+// the 1024-column slice of x that its chunk needs once (kept in registers),
+// and there is no token loop.
 __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const GuSmem &L = a.gu;
@@ -653,7 +653,6 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
   int *s_act = (int *)(smem + L.act);
   int *s_routes = (int *)(smem + L.routes);
   float *s_slot_gate = (float *)(smem + L.slot_gate);
-  uint32_t *s_xpl = (uint32_t *)(smem + L.xpl);
   float *red = (float *)(smem + L.red);
   grid_dependents_launch();
   grid_dependency_wait();
@@ -661,7 +660,7 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
   load_lists(a, s_act, s_routes, s_slot_gate);   // ends with __syncthreads
   COLI_TRACE_POINT(a.layer, kTpGuLists);
   const LayerPtrs lp = layer_ptrs(a);
-  const int T = a.T, H = a.H, F = a.F, KS = a.k + a.S;
+  const int H = a.H, F = a.F;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, NW = blockDim.x >> 5;
   const int n_active = s_act[0];
   const int *s_act_expert = s_act + 1;
@@ -670,7 +669,7 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
   const int U = n_active * (F / 4);
   const int row0 = 4 * part_lo(c, U, G), nrows = 4 * part_lo(c + 1, U, G) - row0;
   const float *xr = lp.xrep + (size_t)(c % a.n_rep) * a.x_stride;
-  const int ncg = a.gu_ncg, S = a.gu_slots, nbx = H / 32;
+  const int ncg = a.gu_ncg, S = a.gu_slots;
   const int dg = NW / ncg, dcg = NW - dg * ncg;
   const bool vec_scales = (H % 256) == 0;
   const int SB = a.gu_slot_bytes;
@@ -683,16 +682,7 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
     GuTask ci, cc;      // the next task to copy, the next task to compute
     ci.init(warp, ncg, row0 + rb0, F);
     cc = ci;
-    // one token: every warp quantises its own 1024-column slice of x when it
-    // first needs it (kept in registers), so no warp waits for a block-wide build
-    const bool xpl = a.gu_xpl && !kOne;
-    if (rb0 == 0) {
-      if (xpl) {
-        build_planes_impl(xr, T, H, nullptr, s_xpl, nbx, warp, NW);
-        __syncthreads();
-      }
-      COLI_TRACE_POINT(a.layer, kTpGuPlanes);
-    }
+    if (rb0 == 0) COLI_TRACE_POINT(a.layer, kTpGuPlanes);
     // prologue: the first S - 1 tasks of this warp in flight
     for (int p = 0; p < S - 1; ++p) {
       if (p < my_tasks) {
@@ -703,11 +693,10 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
     }
     if (rb0 == 0) COLI_TRACE_POINT(a.layer, kTpGuFirstLoads);
     Planes pl;
-    int pl_key = -1;            // (token, chunk) whose planes are in `pl`
+    int pl_cg = -1;             // chunk whose planes are in `pl`
     for (int i = 0; i < my_tasks; ++i) {
       if (i + S - 1 < my_tasks) {
-        gu_copy(a, lp, s_act_expert, ring + (size_t)((i + S - 1) % S) * SB, ci,
-                vec_scales);
+        gu_copy(a, lp, s_act_expert, ring + (size_t)((i + S - 1) % S) * SB, ci, vec_scales);
         ci.next(dg, dcg, ncg, F);
       }
       if (i == (my_tasks > S - 1 ? my_tasks - (S - 1) : 0) && warp == 0 &&
@@ -725,34 +714,24 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
       uint4 w[8];
       float sc[8];
       gu_slot_values(slot, act, vec_scales, w, sc);
-      const int j0 = s_act_off[cc.ai];
-      const int nt = kOne ? 1 : s_act_off[cc.ai + 1] - j0;
-      for (int j = 0; j < nt; ++j) {
-        const int t = kOne ? 0 : s_routes[j0 + j] / KS;
-        float v[8];
-        if (act) {
-          const int key = t * ncg + cc.cg;
-          if (key != pl_key) {
-            if (xpl) {
-              load_planes(s_xpl, t, col / 32, nbx, pl);
-            } else {
-              float xv[32];
-              load32<float>(xr + (int64_t)t * H + col, xv);
-              quantize32(xv, pl);
-            }
-            pl_key = key;
-          }
-#pragma unroll
-          for (int q = 0; q < 8; ++q) v[q] = sc[q] * dot32(w[q], pl);
-        } else {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) v[q] = 0.0f;
+      float v[8];
+      if (act) {
+        if (cc.cg != pl_cg) {
+          float xv[32];
+          load32<float>(xr + col, xv);
+          quantize32(xv, pl);
+          pl_cg = cc.cg;
         }
-        const float tot = reduce8(v);    // lane 4 vi: value vi = 2 * row + (0 gate | 1 up)
-        if ((lane & 3) == 0) {
-          const int vi = lane >> 2;
-          red[(((4 * cc.g + (vi >> 1)) * T + j) * ncg + cc.cg) * 2 + (vi & 1)] = tot;
-        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = sc[q] * dot32(w[q], pl);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = 0.0f;
+      }
+      const float tot = reduce8(v);    // lane 4 vi: value vi = 2 * row + (0 gate | 1 up)
+      if ((lane & 3) == 0) {
+        const int vi = lane >> 2;
+        red[((4 * cc.g + (vi >> 1)) * ncg + cc.cg) * 2 + (vi & 1)] = tot;
       }
       __syncwarp();                  // the slot is refilled by the next iteration's copy
       cc.next(dg, dcg, ncg, F);
@@ -760,24 +739,190 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
     cp_async_wait<0>();
     __syncthreads();
     if (rb0 == 0) COLI_TRACE_POINT(a.layer, kTpGuCompute);
-    // finalise h for every (row, token) of this batch
-    for (int it = tid; it < nrb * T; it += blockDim.x) {
-      const int i = it / T, j = it - i * T;
+    // finalise h for every row of this batch
+    for (int i = tid; i < nrb; i += blockDim.x) {
       const int gr = row0 + rb0 + i;
       const int ai = gr / F, f = gr - ai * F;
-      const int j0 = s_act_off[ai], nt = s_act_off[ai + 1] - j0;
-      if (j >= nt) continue;
       float gs = 0.0f, us = 0.0f;
       for (int q = 0; q < ncg; ++q) {
-        gs += red[((i * T + j) * ncg + q) * 2];
-        us += red[((i * T + j) * ncg + q) * 2 + 1];
+        gs += red[(i * ncg + q) * 2];
+        us += red[(i * ncg + q) * 2 + 1];
       }
-      const int slot_id = s_routes[j0 + j];
+      const int slot_id = s_routes[s_act_off[ai]];
       const float hv = silu(gs) * us * s_slot_gate[slot_id];
       for (int rr = 0; rr < a.n_rep; ++rr) a.h[rr * a.h_stride + (int64_t)slot_id * F + f] = hv;
     }
     __syncthreads();
   }
+  COLI_TRACE_POINT(a.layer, kTpGuEnd);
+}
+
+// Several tokens per call.  A used expert serving nt tokens costs more per
+// row than one serving a single token (the shared expert serves all of them),
+// so the (used expert, 4-row group) space is split over the CTAs by cost,
+// 1 + 2 nt units per group, not by rows.  A warp owns whole groups: it runs
+// their chunks in order through its pipeline, adds each chunk's partial sums
+// per (token, row) in its own shared-memory accumulator, and after the last
+// chunk writes h = silu(g) * u * gate for the group's rows.  The CTA quantises
+// only the tokens its experts serve (into shared memory when they fit, else
+// per task in registers).
+__device__ __forceinline__ int group_at_cost(const int *s_act_off, int n_active, int gpe,
+                                             long long b) {
+  long long before = 0;
+  for (int ai = 0; ai < n_active; ++ai) {
+    const long long w = 1 + 2LL * (s_act_off[ai + 1] - s_act_off[ai]);
+    const long long span = w * gpe;
+    if (b < before + span) return ai * gpe + (int)((b - before + w - 1) / w);
+    before += span;
+  }
+  return n_active * gpe;
+}
+
+struct MTask {
+  int u, cg, ai, f;   // 4-row group (flattened), chunk, used expert, first row
+  __device__ __forceinline__ void set(int u_, int gpe) {
+    u = u_;
+    cg = 0;
+    ai = u / gpe;
+    f = 4 * (u - ai * gpe);
+  }
+  __device__ __forceinline__ void next(int NW, int ncg, int gpe) {
+    if (++cg == ncg) set(u + NW, gpe);
+  }
+  __device__ __forceinline__ GuTask gu() const { return GuTask{0, cg, ai, f}; }
+};
+
+__global__ void __launch_bounds__(kDec2MaxThreads) k_gateup_multi(Dec2Args a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const GuSmem &L = a.gu;
+  COLI_TRACE_POINT(a.layer, kTpGuEntry);
+  int *s_act = (int *)(smem + L.act);
+  int *s_routes = (int *)(smem + L.routes);
+  float *s_slot_gate = (float *)(smem + L.slot_gate);
+  int *s_tok = (int *)(smem + L.tok);            // [T] needed tokens, then [T] token -> plane
+  uint32_t *s_xpl = (uint32_t *)(smem + L.xpl);
+  grid_dependents_launch();
+  grid_dependency_wait();
+  COLI_TRACE_POINT(a.layer, kTpGuDepWait);
+  load_lists(a, s_act, s_routes, s_slot_gate);   // ends with __syncthreads
+  COLI_TRACE_POINT(a.layer, kTpGuLists);
+  const LayerPtrs lp = layer_ptrs(a);
+  const int T = a.T, H = a.H, F = a.F, KS = a.k + a.S;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, NW = blockDim.x >> 5;
+  const int n_active = s_act[0];
+  const int *s_act_expert = s_act + 1;
+  const int *s_act_off = s_act + 1 + (a.E + a.S);
+  const int G = gridDim.x, c = blockIdx.x;
+  const int gpe = F / 4;
+  long long total = 0;
+  for (int ai = 0; ai < n_active; ++ai)
+    total += (1 + 2LL * (s_act_off[ai + 1] - s_act_off[ai])) * gpe;
+  const int u0 = group_at_cost(s_act_off, n_active, gpe, total * c / G);
+  const int u1 = group_at_cost(s_act_off, n_active, gpe, total * (c + 1) / G);
+  const float *xr = lp.xrep + (size_t)(c % a.n_rep) * a.x_stride;
+  const int ncg = a.gu_ncg, S = a.gu_slots, nbx = H / 32;
+  const bool vec_scales = (H % 256) == 0;
+  const bool xpl = a.gu_xpl != 0;
+  const int SB = a.gu_slot_bytes;
+  uint8_t *ring = smem + L.ring + (size_t)warp * S * SB;
+  float *acc = (float *)(smem + L.red) + (size_t)warp * T * 8;   // [T][8] of this warp
+
+  // the tokens that the experts of groups [u0, u1) serve, in token order
+  if (u1 > u0 && xpl) {
+    if (warp == 0) {
+      const int r0 = s_act_off[u0 / gpe], r1 = s_act_off[(u1 - 1) / gpe + 1];
+      uint32_t need = 0;
+      for (int r = r0 + lane; r < r1; r += 32) need |= 1u << (s_routes[r] / KS);
+      need = __reduce_or_sync(0xFFFFFFFFu, need);
+      if (lane < T) {
+        const bool mine = (need >> lane) & 1u;
+        const int pos = __popc(need & ((1u << lane) - 1u));
+        if (mine) s_tok[pos] = lane;
+        s_tok[T + lane] = mine ? pos : -1;
+      }
+      if (lane == 0) s_tok[2 * T] = __popc(need);
+    }
+    __syncthreads();
+    build_planes_impl(xr, s_tok[2 * T], H, s_tok, s_xpl, nbx, warp, NW);
+    __syncthreads();
+  }
+  COLI_TRACE_POINT(a.layer, kTpGuPlanes);
+
+  const int n_groups = u1 - u0;
+  const int my_groups = n_groups > warp ? (n_groups - warp + NW - 1) / NW : 0;
+  const int my_tasks = my_groups * ncg;
+  MTask ci, cc;
+  ci.set(u0 + warp, gpe);
+  cc = ci;
+  for (int p = 0; p < S - 1; ++p) {
+    if (p < my_tasks) {
+      gu_copy(a, lp, s_act_expert, ring + (size_t)p * SB, ci.gu(), vec_scales);
+      ci.next(NW, ncg, gpe);
+    }
+    cp_async_commit();
+  }
+  COLI_TRACE_POINT(a.layer, kTpGuFirstLoads);
+  Planes pl;
+  int pl_key = -1;            // (token, chunk) whose planes are in `pl`
+  for (int i = 0; i < my_tasks; ++i) {
+    if (i + S - 1 < my_tasks) {
+      gu_copy(a, lp, s_act_expert, ring + (size_t)((i + S - 1) % S) * SB, ci.gu(), vec_scales);
+      ci.next(NW, ncg, gpe);
+    }
+    if (i == (my_tasks > S - 1 ? my_tasks - (S - 1) : 0) && warp == 0)
+      prefetch_down_rows(a, lp, s_act_expert, n_active, c);
+    cp_async_commit();
+    cp_async_wait_dyn(S - 1);
+    if (vec_scales) __syncwarp();
+    const uint8_t *slot = ring + (size_t)(i % S) * SB;
+    const int col = cc.cg * kChunkCols + 32 * lane;
+    const bool act = col < H;
+    uint4 w[8];
+    float sc[8];
+    gu_slot_values(slot, act, vec_scales, w, sc);
+    const int j0 = s_act_off[cc.ai], nt = s_act_off[cc.ai + 1] - j0;
+    for (int j = 0; j < nt; ++j) {
+      const int t = s_routes[j0 + j] / KS;
+      float v[8];
+      if (act) {
+        const int key = t * ncg + cc.cg;
+        if (key != pl_key) {
+          if (xpl) {
+            load_planes(s_xpl, s_tok[T + t], col / 32, nbx, pl);
+          } else {
+            float xv[32];
+            load32<float>(xr + (int64_t)t * H + col, xv);
+            quantize32(xv, pl);
+          }
+          pl_key = key;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = sc[q] * dot32(w[q], pl);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = 0.0f;
+      }
+      const float tot = reduce8(v);    // lane 4 vi: value vi = 2 * row + (0 gate | 1 up)
+      if ((lane & 3) == 0) {
+        float *p = acc + j * 8 + (lane >> 2);
+        *p = (cc.cg == 0 ? 0.0f : *p) + tot;   // chunks added in order
+      }
+    }
+    if (cc.cg == ncg - 1) {
+      __syncwarp();
+      for (int it = lane; it < 4 * nt; it += 32) {
+        const int j = it >> 2, r = it & 3;
+        const float gs = acc[j * 8 + 2 * r], us = acc[j * 8 + 2 * r + 1];
+        const int slot_id = s_routes[j0 + j];
+        const float hv = silu(gs) * us * s_slot_gate[slot_id];
+        for (int rr = 0; rr < a.n_rep; ++rr)
+          a.h[rr * a.h_stride + (int64_t)slot_id * F + cc.f + r] = hv;
+      }
+    }
+    __syncwarp();                  // the slot (and the accumulator) are reused next
+    cc.next(NW, ncg, gpe);
+  }
+  cp_async_wait<0>();
   COLI_TRACE_POINT(a.layer, kTpGuEnd);
 }
 
@@ -1125,47 +1270,68 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
   a.n_part = n_part;
   // ---- gate/up: gu_nw warps, each with a gu_slots-deep cp.async pipeline
   a.gu_ncg = (H + kChunkCols - 1) / kChunkCols;
-  const int n_used = ((E < T * k) ? E : T * k) + S;
-  const int max_rows = 4 * ((n_used * (F / 4) + G - 1) / G);
+  a.gu_slot_bytes = slot_bytes(H);
   GuSmem g{};
   size_t o = 0;
   g.act = o; o = al16(o + (size_t)(2 + 2 * (E + S)) * 4);
   g.routes = o; o = al16(o + (size_t)T * KS * 4);
   g.slot_gate = o; o = al16(o + (size_t)T * KS * 4);
-  const size_t xpl_bytes = al16((size_t)T * 18 * (H / 32) * 4);
-  const size_t row_bytes = (size_t)T * a.gu_ncg * 2 * 4;
-  const int min_batch = max_rows < 64 ? max_rows : 64;
   // warps x slots, by bytes in flight ahead of the compute: 12 x 3, 16 x 2, ...
-  // A one-token call quantises x per warp for the chunk it works on, so warp
-  // counts that keep every warp on one chunk (NW % gu_ncg == 0) come first.
-  static const int kNw[] = {12, 16, 8, 8, 4};
-  static const int kSl[] = {3, 2, 3, 2, 2};
-  a.gu_slot_bytes = slot_bytes(H);
+  static const int kNw[] = {12, 16, 8, 12, 8, 4};
+  static const int kSl[] = {3, 2, 3, 2, 2, 2};
   bool ok = false;
-  for (int pass = 0; pass < 4 && !ok; ++pass) {
-    const int xpl = T > 1 && pass < 2, strict = T == 1 && (pass & 1) == 0;
-    for (int c = 0; c < 5 && !ok; ++c) {
-      if (strict && kNw[c] % a.gu_ncg != 0) continue;
-      const size_t ring = (size_t)kNw[c] * kSl[c] * a.gu_slot_bytes;
-      const size_t need = o + (xpl ? xpl_bytes : 0) + ring + 128 + (size_t)min_batch * row_bytes;
-      if (need <= budget) {
-        a.gu_xpl = xpl;
-        a.gu_nw = kNw[c];
-        a.gu_slots = kSl[c];
-        ok = true;
+  if (T == 1) {
+    // one token: partial sums per (row, chunk) in shared memory, rows in
+    // batches of gu_rows.  x is quantised per warp for the chunk it works on,
+    // so warp counts that keep every warp on one chunk (NW % gu_ncg == 0) come first.
+    const int n_used = (E < k ? E : k) + S;
+    const int max_rows = 4 * ((n_used * (F / 4) + G - 1) / G);
+    const size_t row_bytes = (size_t)a.gu_ncg * 2 * 4;
+    const int min_batch = max_rows < 64 ? max_rows : 64;
+    for (int pass = 0; pass < 2 && !ok; ++pass)
+      for (int c = 0; c < 6 && !ok; ++c) {
+        if (pass == 0 && kNw[c] % a.gu_ncg != 0) continue;
+        const size_t ring = (size_t)kNw[c] * kSl[c] * a.gu_slot_bytes;
+        if (al128(o) + ring + 128 + (size_t)min_batch * row_bytes <= budget) {
+          a.gu_nw = kNw[c];
+          a.gu_slots = kSl[c];
+          ok = true;
+        }
       }
-    }
+    if (!ok) return cudaErrorInvalidValue;
+    a.gu_xpl = 0;
+    g.xpl = g.tok = o;
+    g.ring = al128(o); o = g.ring + (size_t)a.gu_nw * a.gu_slots * a.gu_slot_bytes;
+    g.red = al16(o);
+    const size_t fit = (budget - g.red) / row_bytes;
+    int rows = fit < (size_t)max_rows ? (int)fit : max_rows;
+    rows &= ~3;
+    if (rows < 4) return cudaErrorInvalidValue;
+    a.gu_rows = rows;
+    g.total = al16(g.red + (size_t)rows * row_bytes);
+  } else {
+    // several tokens: the needed tokens' planes (when they fit), one [T][8]
+    // accumulator per warp, the ring
+    g.tok = o; o = al16(o + (size_t)(2 * T + 1) * 4);
+    const size_t xpl_bytes = al16((size_t)T * 18 * (H / 32) * 4);
+    for (int xpl = 1; xpl >= 0 && !ok; --xpl)
+      for (int c = 0; c < 6 && !ok; ++c) {
+        const size_t acc = (size_t)kNw[c] * T * 8 * 4;
+        const size_t ring = (size_t)kNw[c] * kSl[c] * a.gu_slot_bytes;
+        if (al128(o + (xpl ? xpl_bytes : 0) + acc) + ring <= budget) {
+          a.gu_xpl = xpl;
+          a.gu_nw = kNw[c];
+          a.gu_slots = kSl[c];
+          ok = true;
+        }
+      }
+    if (!ok) return cudaErrorInvalidValue;
+    a.gu_rows = 0;
+    g.xpl = o; o += a.gu_xpl ? xpl_bytes : 0;
+    g.red = al16(o); o = g.red + (size_t)a.gu_nw * T * 8 * 4;
+    g.ring = al128(o); o = g.ring + (size_t)a.gu_nw * a.gu_slots * a.gu_slot_bytes;
+    g.total = al16(o);
   }
-  if (!ok) return cudaErrorInvalidValue;
-  g.xpl = o; o += a.gu_xpl ? xpl_bytes : 0;
-  g.ring = al128(o); o = g.ring + (size_t)a.gu_nw * a.gu_slots * a.gu_slot_bytes;
-  g.red = al16(o);
-  size_t fit = (budget - g.red) / row_bytes;
-  int rows = fit < (size_t)max_rows ? (int)fit : max_rows;
-  rows &= ~3;
-  if (rows < 4) return cudaErrorInvalidValue;
-  a.gu_rows = rows;
-  g.total = al16(g.red + (size_t)rows * row_bytes);
   a.gu = g;
   // ---- down: dn_nw warps with dn_slots_pipe-deep cp.async pipelines; expert
   // batches of at most dn_batch experts and dn_slots token slots
@@ -1255,11 +1421,11 @@ cudaError_t launch_gateup(const Dec2Args &a, int grid, cudaStream_t s, bool pdl)
   const int threads = 32 * a.gu_nw;
   cudaError_t e;
   if (a.T == 1) {
-    if ((e = allow_smem(k_gateup<true>, a.gu.total)) != cudaSuccess) return e;
-    return launch(k_gateup<true>, grid, threads, a.gu.total, s, pdl, a);
+    if ((e = allow_smem(k_gateup, a.gu.total)) != cudaSuccess) return e;
+    return launch(k_gateup, grid, threads, a.gu.total, s, pdl, a);
   }
-  if ((e = allow_smem(k_gateup<false>, a.gu.total)) != cudaSuccess) return e;
-  return launch(k_gateup<false>, grid, threads, a.gu.total, s, pdl, a);
+  if ((e = allow_smem(k_gateup_multi, a.gu.total)) != cudaSuccess) return e;
+  return launch(k_gateup_multi, grid, threads, a.gu.total, s, pdl, a);
 }
 
 cudaError_t launch_down(const Dec2Args &a_in, int wr_bf16, cudaStream_t s, bool pdl) {
