@@ -32,6 +32,7 @@ WsLayout ws_layout(int T, int H, int F, int E, int S, int k) {
   L.slot_gate = o; o = align256(o + (size_t)T * KS * sizeof(float));
   L.h = o;         o = align256(o + kReplicas * L.h_stride * 4);
   L.xrep = o;      o = align256(o + kReplicas * L.x_stride * 4);
+  L.y = o;         o = align256(o + (T > 1 ? (size_t)T * KS * H * 4 : 0));
   L.total = o;
   return L;
 }
@@ -161,6 +162,7 @@ Dec2Args make_args(const coli_moe_desc *d, int k, int tn, uint8_t *ws, const WsL
   a.g_routes = (int32_t *)(ws + L.routes);
   a.g_slot_gate = (float *)(ws + L.slot_gate);
   a.h = (float *)(ws + L.h);
+  a.y = (float *)(ws + L.y);
   a.ctrl = (uint32_t *)(ws + L.ctrl);
   a.wr_bf16 = d->router_dtype == COLI_BF16;
   a.fx = tn * a.E <= kFxMaxTE;
@@ -294,7 +296,14 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
     a.residual = residual ? (const float *)xin : nullptr;
     a.out = out;
     a.layer_out = layer_out ? layer_out + (size_t)l * T_H : nullptr;
-    e = profiled(COLI_KERNEL_DOWN, stream, [&] { return launch_down(a, wr_bf16, stream, true); });
+    // several tokens: the expert GEMVs (k_down_multi), then the combine (k_down)
+    e = profiled(COLI_KERNEL_DOWN, stream, [&] {
+      if (a.T > 1) {
+        const cudaError_t em = launch_down_multi(a, stream, true);
+        if (em != cudaSuccess) return em;
+      }
+      return launch_down(a, wr_bf16, stream, true);
+    });
   }
   return map_err(e);
 }

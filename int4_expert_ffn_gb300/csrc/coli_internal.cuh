@@ -53,6 +53,7 @@ struct WsLayout {
   size_t slot_gate;  // f32 [T*(k+S)]
   size_t h;          // f32 [kReplicas][T*(k+S)][F]
   size_t xrep;       // f32 [kReplicas][T][H]
+  size_t y;          // f32 [T*(k+S)][H] (T > 1 only)
   size_t total;
   int n_part;
   size_t h_stride, x_stride;   // replica strides (floats)
@@ -69,6 +70,10 @@ struct GuSmem {
 // Shared-memory plan of k_down.
 struct DnSmem {
   size_t act, routes, acc, xn, wr, ring, red, planes, total;
+};
+// Shared-memory plan of k_down_multi.
+struct DmSmem {
+  size_t act, routes, planes, acc, ring, total;
 };
 
 // Arguments of the decode kernels (one layer, T <= kDecodeMaxT tokens).
@@ -117,8 +122,13 @@ struct Dec2Args {
   int wr_bf16;              // the router (and its rows in k_down's shared memory) is bf16
   int dn_slots;             // token slots whose planes fit in shared memory at once
   int dn_batch;             // experts whose partial sums fit in shared memory at once
+  int dm_nw;                // warps of k_down_multi
+  int dm_slots_pipe;        // depth of each warp's cp.async pipeline
+  int dm_cap;               // h rows whose planes fit in k_down_multi's shared memory
+  float *y;                 // [T*(k+S)][H] per-slot down outputs (several tokens)
   GuSmem gu;
   DnSmem dn;
+  DmSmem dm;
 };
 
 
@@ -165,6 +175,7 @@ cudaError_t launch_route_partials(const Dec2Args &a, int x_bf16, int w_bf16, cud
                                   bool pdl);
 cudaError_t launch_gateup(const Dec2Args &a, int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_down(const Dec2Args &a, int wr_bf16, cudaStream_t s, bool pdl);
+cudaError_t launch_down_multi(const Dec2Args &a, cudaStream_t s, bool pdl);
 
 // Quantiser (quant.cu).
 cudaError_t launch_quant_i4g(const void *w, int w_dtype, int64_t rows, int64_t cols,

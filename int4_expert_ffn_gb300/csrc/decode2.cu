@@ -625,11 +625,15 @@ __device__ void load_lists(const Dec2Args &a, int *s_act, int *s_routes, float *
   __syncthreads();
 }
 
+constexpr int64_t kPrefetchMaxBytes = int64_t(96) << 20;
+
 // L2 prefetch of the down rows [dh0, dh1) of every used expert (the rows that
 // CTA c owns in the down kernel), one bulk prefetch per expert and lane.
 __device__ __forceinline__ void prefetch_down_rows(const Dec2Args &a, const LayerPtrs &lp,
                                                    const int *s_act_expert, int n_active, int c) {
   if (c >= a.n_part) return;
+  if ((int64_t)n_active * ((int64_t)a.H * a.F / 2 + (int64_t)a.H * a.F / 16) > kPrefetchMaxBytes)
+    return;   // would not stay in L2 until the down kernel reads it
   const int H = a.H, F = a.F, lane = threadIdx.x & 31;
   const int64_t ngr = H / kGroup;
   const int UH = H / 4;
@@ -1005,9 +1009,20 @@ __device__ void dn_phase(const Dec2Args &a, const LayerPtrs &lp, const int *s_ac
   uint32_t *s_planes = (uint32_t *)(smem + L.planes);
   const int SB = a.dn_slot_bytes;
   uint8_t *ring = smem + L.ring + (size_t)warp * Sl * SB;
-  for (int i = tid; i < nr * T; i += blockDim.x) acc[i] = 0.0f;
+  if (!kOne) {
+    // several tokens: k_down_multi left each slot's down output in y; a
+    // token's rows add its slots in slot order (routed by rank, then shared)
+    for (int i = tid; i < nr * T; i += blockDim.x) {
+      const int t = i / nr, r = i - t * nr;
+      float sum = 0.0f;
+      for (int p = 0; p < KS; ++p) sum += __ldcg(a.y + (size_t)(t * KS + p) * H + dh0 + r);
+      acc[r * T + t] = sum;
+    }
+    __syncthreads();
+  }
+  for (int i = tid; i < nr * T && kOne; i += blockDim.x) acc[i] = 0.0f;
   // experts in batches: their slots' planes and their partial sums must fit
-  for (int ga = 0; ga < n_active;) {
+  for (int ga = 0; ga < (kOne ? n_active : 0);) {
     int gb = ga;
     while (gb < n_active && gb - ga < a.dn_batch && s_act_off[gb + 1] - s_act_off[ga] <= a.dn_slots)
       ++gb;
@@ -1193,6 +1208,120 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
   COLI_TRACE_POINT(a.layer, kTpEnd);
 }
 
+// Down GEMVs of a several-token call, split like k_gateup_multi: the (used
+// expert, 8-row group) space goes to the CTAs by cost (1 + 2 nt units per
+// group); a warp owns whole groups, runs their chunks in order, and after the
+// last one writes y[slot][row] = sum_f down[row][f] h[slot][f] for each token
+// slot of the expert.  The CTA's slots' h rows are quantised once into shared
+// memory when they fit (else per task in registers).  k_down then adds each
+// token's slots.
+__global__ void __launch_bounds__(kDec2MaxThreads) k_down_multi(Dec2Args a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const DmSmem &L = a.dm;
+  int *s_act = (int *)(smem + L.act);
+  int *s_routes = (int *)(smem + L.routes);
+  uint32_t *s_planes = (uint32_t *)(smem + L.planes);
+  grid_dependents_launch();
+  grid_dependency_wait();
+  load_lists(a, s_act, s_routes, nullptr);   // ends with __syncthreads
+  const LayerPtrs lp = layer_ptrs(a);
+  const int H = a.H, F = a.F, T = a.T;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, NW = blockDim.x >> 5;
+  const int n_active = s_act[0];
+  const int *s_act_expert = s_act + 1;
+  const int *s_act_off = s_act + 1 + (a.E + a.S);
+  const int G = gridDim.x, c = blockIdx.x;
+  const int gpe = H / 8;
+  long long total = 0;
+  for (int ai = 0; ai < n_active; ++ai)
+    total += (1 + 2LL * (s_act_off[ai + 1] - s_act_off[ai])) * gpe;
+  const int u0 = group_at_cost(s_act_off, n_active, gpe, total * c / G);
+  const int u1 = group_at_cost(s_act_off, n_active, gpe, total * (c + 1) / G);
+  const float *h_rep = a.h + (size_t)(c % a.n_rep) * a.h_stride;
+  const int ncg = a.dn_ncg, Sl = a.dm_slots_pipe, nbp = F / 32;
+  const bool vec_scales = (F % 256) == 0;
+  const int SB = a.dn_slot_bytes;
+  uint8_t *ring = smem + L.ring + (size_t)warp * Sl * SB;
+  float *acc = (float *)(smem + L.acc) + (size_t)warp * T * 8;   // [T][8] of this warp
+  // h rows (slots) of the experts of groups [u0, u1): routes [r0, r1)
+  const int r0 = u1 > u0 ? s_act_off[u0 / gpe] : 0;
+  const int r1 = u1 > u0 ? s_act_off[(u1 - 1) / gpe + 1] : 0;
+  const bool xpl = r1 - r0 <= a.dm_cap;
+  if (u1 > u0 && xpl) {
+    build_planes_list(h_rep, F, s_routes + r0, r1 - r0, s_planes, nbp);
+    __syncthreads();
+  }
+  const int n_groups = u1 - u0;
+  const int my_groups = n_groups > warp ? (n_groups - warp + NW - 1) / NW : 0;
+  const int my_tasks = my_groups * ncg;
+  // task: group u (expert u / gpe, rows 8 (u % gpe) ..), chunk cg
+  int ci_u = u0 + warp, ci_cg = 0, cc_u = ci_u, cc_cg = 0;
+  auto task = [&](int u, int cg) { return DnTask{u / gpe, u - (u / gpe) * gpe, cg}; };
+  for (int p = 0; p < Sl - 1; ++p) {
+    if (p < my_tasks) {
+      dn_copy(a, lp, s_act_expert, ring + (size_t)p * SB, task(ci_u, ci_cg), 0, H, vec_scales);
+      if (++ci_cg == ncg) { ci_cg = 0; ci_u += NW; }
+    }
+    cp_async_commit();
+  }
+  Planes pl;
+  int pl_key = -1;
+  for (int i = 0; i < my_tasks; ++i) {
+    if (i + Sl - 1 < my_tasks) {
+      dn_copy(a, lp, s_act_expert, ring + (size_t)((i + Sl - 1) % Sl) * SB, task(ci_u, ci_cg),
+              0, H, vec_scales);
+      if (++ci_cg == ncg) { ci_cg = 0; ci_u += NW; }
+    }
+    cp_async_commit();
+    cp_async_wait_dyn(Sl - 1);
+    if (vec_scales) __syncwarp();
+    const uint8_t *slot = ring + (size_t)(i % Sl) * SB;
+    const int col = cc_cg * kChunkCols + 32 * lane;
+    const bool act = col < F;
+    uint4 w[8];
+    float sc[8];
+    gu_slot_values(slot, act, vec_scales, w, sc);
+    const int ai = cc_u / gpe, row0 = 8 * (cc_u - ai * gpe);
+    const int j0 = s_act_off[ai], nt = s_act_off[ai + 1] - j0;
+    for (int j = 0; j < nt; ++j) {
+      float v[8];
+      if (act) {
+        const int key = (j0 + j) * 64 + cc_cg;
+        if (key != pl_key) {
+          if (xpl) {
+            load_planes(s_planes, j0 + j - r0, col / 32, nbp, pl);
+          } else {
+            float xv[32];
+            load32<float>(h_rep + (int64_t)s_routes[j0 + j] * F + col, xv);
+            quantize32(xv, pl);
+          }
+          pl_key = key;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = sc[q] * dot32(w[q], pl);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = 0.0f;
+      }
+      const float tot = reduce8(v);   // lane 4 q ends with row q
+      if ((lane & 3) == 0) {
+        float *p = acc + j * 8 + (lane >> 2);
+        *p = (cc_cg == 0 ? 0.0f : *p) + tot;   // chunks added in order
+      }
+    }
+    if (cc_cg == ncg - 1) {
+      __syncwarp();
+      for (int it = lane; it < 8 * nt; it += 32) {
+        const int j = it >> 3, q = it & 7;
+        a.y[(size_t)s_routes[j0 + j] * H + row0 + q] = acc[j * 8 + q];
+      }
+    }
+    __syncwarp();
+    if (++cc_cg == ncg) { cc_cg = 0; cc_u += NW; }
+  }
+  cp_async_wait<0>();
+}
+
 // ---------------------------------------------------------------------------
 // host side
 
@@ -1261,6 +1390,8 @@ cudaError_t allow_smem(K kernel, size_t bytes) {
 }
 
 }  // namespace
+
+static cudaError_t plan_down_multi(Dec2Args &a);
 
 // Geometry and shared-memory plans of both kernels for one layer shape.
 cudaError_t plan_decode(Dec2Args &a, int n_part) {
@@ -1336,6 +1467,8 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
   // ---- down: dn_nw warps with dn_slots_pipe-deep cp.async pipelines; expert
   // batches of at most dn_batch experts and dn_slots token slots
   a.dn_ncg = (F + kChunkCols - 1) / kChunkCols;
+  a.dn_slot_bytes = slot_bytes(F);
+  if (T > 1) return plan_down_multi(a);
   const int UH = H / 4;
   const int max_nr = 4 * ((UH + n_part - 1) / n_part);
   DnSmem d{};
@@ -1348,7 +1481,6 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
   const size_t per_slot = (size_t)18 * (F / 32) * 4;
   const size_t per_expert_red = (size_t)max_nr * T * a.dn_ncg * 4;
   const int all_slots = T * KS;
-  a.dn_slot_bytes = slot_bytes(F);
   // the largest tokens-per-expert count is T (routed) or T (shared)
   // more warps before deeper pipelines: each warp works its tasks in order, so
   // the down phase's latency follows the tasks per warp
@@ -1391,6 +1523,58 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
   return cudaSuccess;
 }
 
+// Several tokens: k_down_multi runs the expert GEMVs and k_down only adds the
+// slots (no ring, planes or partial sums of its own).
+static cudaError_t plan_down_multi(Dec2Args &a) {
+  const int T = a.T, H = a.H, F = a.F, E = a.E, S = a.S, KS = a.k + S;
+  const size_t budget = (size_t)max_smem() - 4096;
+  const int G = a.n_part;
+  const int max_nr = 4 * ((H / 4 + G - 1) / G);
+  DnSmem d{};
+  size_t o = 0;
+  d.act = o; o = al16(o + (size_t)(2 + 2 * (E + S)) * 4);
+  d.routes = o; o = al16(o + (size_t)T * KS * 4);
+  d.acc = o; o = al16(o + (size_t)max_nr * T * 4);
+  d.xn = o; o = al16(o + (size_t)T * max_nr * 4);
+  d.wr = o; o = al16(o + (size_t)E * max_nr * (a.wr_bf16 ? 2 : 4));
+  d.ring = d.red = d.planes = o;
+  d.total = o;
+  a.dn = d;
+  a.dn_nw = 16;
+  a.dn_slots_pipe = 2;
+  a.dn_slots = a.dn_batch = 0;
+  // k_down_multi: warps x slots, then as many h rows' planes as fit (at least
+  // one expert's tokens plus one more, else planes per task)
+  DmSmem m{};
+  o = 0;
+  m.act = o; o = al16(o + (size_t)(2 + 2 * (E + S)) * 4);
+  m.routes = o; o = al16(o + (size_t)T * KS * 4);
+  const size_t per_slot = (size_t)18 * (F / 32) * 4;
+  static const int kNw[] = {16, 12, 8, 12, 8, 8, 4};
+  static const int kSl[] = {2, 3, 4, 2, 3, 2, 2};
+  int pick = -1, cap = 0;
+  for (int pass = 0; pass < 2 && pick < 0; ++pass)
+    for (int c = 0; c < 7 && pick < 0; ++c) {
+      const size_t fixed = al128(o + (size_t)kNw[c] * T * 8 * 4) +
+                           (size_t)kNw[c] * kSl[c] * a.dn_slot_bytes;
+      if (fixed + 128 > budget) continue;
+      const size_t n = (budget - fixed - 128) / per_slot;   // 128: alignment slack
+      if (pass == 0 && n < (size_t)(T + 1)) continue;
+      pick = c;
+      cap = n > (size_t)(T * KS) ? T * KS : (int)n;
+    }
+  if (pick < 0) return cudaErrorInvalidValue;
+  a.dm_nw = kNw[pick];
+  a.dm_slots_pipe = kSl[pick];
+  a.dm_cap = cap;
+  m.planes = o; o = al16(o + (size_t)cap * per_slot);
+  m.acc = o; o = o + (size_t)a.dm_nw * T * 8 * 4;
+  m.ring = al128(o); o = m.ring + (size_t)a.dm_nw * a.dm_slots_pipe * a.dn_slot_bytes;
+  m.total = al16(o);
+  a.dm = m;
+  return cudaSuccess;
+}
+
 // Shared memory the last CTA needs to route a layer (see route_finish).
 size_t route_smem_bytes(const Dec2Args &a, bool *stage) {
   const RouteSmem plain = route_smem(a.T, a.E, a.k, a.S, a.n_part, false);
@@ -1426,6 +1610,12 @@ cudaError_t launch_gateup(const Dec2Args &a, int grid, cudaStream_t s, bool pdl)
   }
   if ((e = allow_smem(k_gateup_multi, a.gu.total)) != cudaSuccess) return e;
   return launch(k_gateup_multi, grid, threads, a.gu.total, s, pdl, a);
+}
+
+cudaError_t launch_down_multi(const Dec2Args &a, cudaStream_t s, bool pdl) {
+  cudaError_t e;
+  if ((e = allow_smem(k_down_multi, a.dm.total)) != cudaSuccess) return e;
+  return launch(k_down_multi, num_sms(), 32 * a.dm_nw, a.dm.total, s, pdl, a);
 }
 
 cudaError_t launch_down(const Dec2Args &a_in, int wr_bf16, cudaStream_t s, bool pdl) {
