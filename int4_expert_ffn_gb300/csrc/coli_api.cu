@@ -171,6 +171,14 @@ Dec2Args make_args(const coli_moe_desc *d, int k, int tn, uint8_t *ws, const WsL
   return a;
 }
 
+// Fixed-point buffer b (0 or 1) of a workspace.
+void fx_buffer(const Dec2Args &a, uint8_t *ws, const WsLayout &L, int b, long long **acc,
+               uint32_t **flag) {
+  uint8_t *base = ws + L.fx + (size_t)b * kFxBufBytes;
+  *acc = (long long *)base;
+  *flag = (uint32_t *)(base + (size_t)a.T * a.E * 8);
+}
+
 }  // namespace
 
 extern "C" {
@@ -269,6 +277,9 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
   const int wr_bf16 = d->router_dtype == COLI_BF16;
   cudaError_t e = cudaSuccess;
   a.build_union = 1;
+  // with fixed-point logits every gate/up CTA routes its own layer
+  a.route_gu = a.fx && a.gu_route_fits;
+  uint8_t *ws = (uint8_t *)workspace;
   for (int l = 0; l < n_layers && e == cudaSuccess; ++l) {
     const void *xin = (l == 0) ? x : (const void *)out;
     a.x = xin;
@@ -278,6 +289,18 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
     // counts of layer l: added by whichever kernel routes it (the gate/up CTAs
     // with fixed-point logits, else the last CTA of the partials' kernel)
     a.route_counts = route_counts ? route_counts + (size_t)l * E : nullptr;
+    if (a.route_gu) {
+      // layer l's logits in buffer l % 2 (read by its gate/up, cleared by its
+      // down kernel); the down kernel adds layer l + 1's into the other
+      long long *rd_acc;
+      uint32_t *rd_flag;
+      fx_buffer(a, ws, L, l & 1, &rd_acc, &rd_flag);
+      a.fx_rd_acc = rd_acc;
+      a.fx_rd_flag = rd_flag;
+      a.fx_clr_acc = rd_acc;
+      a.fx_clr_flag = rd_flag;
+      fx_buffer(a, ws, L, l == 0 ? 0 : (l + 1) & 1, &a.fx_acc, &a.fx_flag);
+    }
     if (l == 0) {
       // router partials of layer 0
       a.wr = router_w;
@@ -285,6 +308,7 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
         return launch_route_partials(a, x_dtype == COLI_BF16, wr_bf16, stream, true);
       });
       if (e != cudaSuccess) break;
+      if (a.route_gu) fx_buffer(a, ws, L, 1, &a.fx_acc, &a.fx_flag);
     }
     e = profiled(COLI_KERNEL_GATEUP, stream, [&] { return launch_gateup(a, num_sms(), stream, true); });
     if (e != cudaSuccess) break;

@@ -17,15 +17,18 @@ constexpr int kMaxTopK = 64;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxShared = 8;
 // Router logits accumulated as fixed-point integers (deterministic in any
-// order) by the CTAs that form their partials; the last CTA to finish reads
-// them, routes the layer and clears them.
+// order) by the CTAs that form their partials.  In the layer forward every
+// CTA of the next gate/up kernel routes from them (two buffers, by layer
+// parity; the down kernel of a layer clears the buffer its gate/up read);
+// the router-only call routes in the last CTA of the partials' kernel.
 constexpr int kFxMaxTE = 2048;          // tokens x experts routed this way (else a ticket)
 // The fixed-point buffers sit at one offset for every shape, right after the
 // control words, and every call leaves them zero; no other array of any
 // layout overlaps them, so a workspace zero-filled once stays valid across
 // calls of different shapes.
 constexpr size_t kFxOffset = 256;
-constexpr size_t kFxRegionBytes = (size_t)kFxMaxTE * 8 + (size_t)kFxMaxTE * 4;
+constexpr size_t kFxBufBytes = (size_t)kFxMaxTE * 8 + (size_t)kFxMaxTE * 4;
+constexpr size_t kFxRegionBytes = 2 * kFxBufBytes;
 constexpr size_t kWsFixedBytes = kFxOffset + ((kFxRegionBytes + 255) & ~(size_t)255);
 // Buffers that every CTA of a kernel reads (layer input, h)
 // are written in this many copies, each read by 1/kReplicas of the CTAs, so
@@ -81,8 +84,14 @@ struct Dec2Args {
   int T, H, F, E, S, k;
   int layer;                // index of the layer in the stack (phase tracing only)
   int fx;                   // router partials as fixed-point sums (T*E <= kFxMaxTE)
-  long long *fx_acc;        // [T][E]
+  long long *fx_acc;        // [T][E] partials are added here
   uint32_t *fx_flag;        // [T][E] non-finite or out-of-range partial seen
+  int route_gu;             // every gate/up CTA routes its layer from fx_rd_*
+  int gu_route_fits;        // the routing scratch fits in k_gateup's pipeline ring
+  const long long *fx_rd_acc;   // k_gateup: this layer's fixed-point logits
+  const uint32_t *fx_rd_flag;
+  long long *fx_clr_acc;    // k_down: buffer its gate/up read, cleared here
+  uint32_t *fx_clr_flag;
   const void *x;            // layer input [T][H], f32 or bf16
   const void *wr;           // k_route: this layer's router; k_down: next layer's (or null)
   const float *residual;    // k_down: added to the layer output (or null)

@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_route(Dec2Args a) {
     }
   }
   extern __shared__ __align__(128) uint8_t smem_route[];
-  route_if_last(a, layer_ptrs(a), smem_route);
+  if (!a.route_gu) route_if_last(a, layer_ptrs(a), smem_route);
 }
 
 // ---------------------------------------------------------------------------
@@ -625,6 +625,84 @@ __device__ void load_lists(const Dec2Args &a, int *s_act, int *s_routes, float *
   __syncthreads();
 }
 
+// Shared-memory scratch of gu_route (byte offsets from its base).
+struct GuRouteSmem {
+  size_t logits, topk, idx, gates, vals, flag, total;
+};
+__host__ __device__ inline GuRouteSmem gu_route_smem(int T, int E, int k) {
+  auto a16 = [](size_t v) { return (v + 15) & ~(size_t)15; };
+  GuRouteSmem R{};
+  size_t o = 0;
+  R.logits = o; o = a16(o + (size_t)T * E * 4);
+  R.topk = o;
+  size_t tk = topk_scratch_bytes(T, E, k);
+  if (tk < (size_t)T * k * 4) tk = (size_t)T * k * 4;   // the union's sort scratch
+  o = a16(R.topk + tk);
+  R.idx = o; o += (size_t)T * k * 4;
+  R.gates = o; o += (size_t)T * k * 4;
+  R.vals = o; o += (size_t)T * k * 4;
+  R.flag = a16(o); o = R.flag + 16;
+  R.total = o;
+  return R;
+}
+
+// The union lists of this layer in the gate/up CTA's shared memory: routed
+// here from the fixed-point logits (every CTA alike, same integers, same
+// result; CTA 0 also publishes the lists for the down kernel, the counts and
+// the NaN flag), else loaded from the routing CTA's.  `scratch` is free
+// shared memory (the pipeline ring, not yet in use).  Ends with __syncthreads.
+__device__ void gu_lists(const Dec2Args &a, const LayerPtrs &lp, uint8_t *scratch, int *s_act,
+                         int *s_routes, float *s_slot_gate) {
+  if (!a.route_gu) {
+    load_lists(a, s_act, s_routes, s_slot_gate);
+    return;
+  }
+  const int T = a.T, E = a.E, k = a.k, S = a.S, KS = k + S, TE = T * E;
+  const GuRouteSmem R = gu_route_smem(T, E, k);
+  float *s_logits = (float *)(scratch + R.logits);
+  int *s_idx = (int *)(scratch + R.idx);
+  float *s_gates = (float *)(scratch + R.gates);
+  for (int i = threadIdx.x; i < TE; i += blockDim.x) {
+    const long long v = __ldcg(a.fx_rd_acc + i);
+    const uint32_t f = __ldcg(a.fx_rd_flag + i);
+    s_logits[i] = f ? __int_as_float(0x7FC00000) : (float)((double)v * 0x1p-32);
+  }
+  __syncthreads();
+  COLI_TRACE_POINT(a.layer, kTpRtLogits);
+  const bool nan = select_topk(s_logits, T, E, k, s_idx, s_gates, (float *)(scratch + R.vals),
+                               scratch + R.topk, (int *)(scratch + R.flag));
+  COLI_TRACE_POINT(a.layer, kTpRtTopk);
+  block_union(s_idx, s_gates, T, k, S, E, s_act, s_act + 1, s_act + 1 + (E + S), s_routes,
+              s_slot_gate, (int *)(scratch + R.topk));
+  if (blockIdx.x == 0) {
+    if (threadIdx.x == 0 && nan) set_flag(a.ctrl, COLI_FLAG_NAN_LOGITS);
+    for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
+      a.g_idx[i] = s_idx[i];
+      a.g_gates[i] = s_gates[i];
+      if (lp.route_counts) atomicAdd(lp.route_counts + s_idx[i], 1u);
+    }
+    for (int i = threadIdx.x; i < 2 + 2 * (E + S); i += blockDim.x) a.g_act[i] = s_act[i];
+    for (int i = threadIdx.x; i < T * KS; i += blockDim.x) {
+      a.g_routes[i] = s_routes[i];
+      a.g_slot_gate[i] = s_slot_gate[i];
+    }
+  }
+  __syncthreads();
+}
+
+// The down kernel of a layer clears the fixed-point buffer that the layer's
+// gate/up CTAs routed from (they have all finished): CTA c its share.
+__device__ __forceinline__ void clear_fx(const Dec2Args &a) {
+  if (!a.route_gu) return;
+  const int TE = a.T * a.E, G = gridDim.x, c = blockIdx.x;
+  const int i0 = part_lo(c, TE, G), i1 = part_lo(c + 1, TE, G);
+  for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
+    a.fx_clr_acc[i] = 0;
+    a.fx_clr_flag[i] = 0u;
+  }
+}
+
+
 constexpr int64_t kPrefetchMaxBytes = int64_t(96) << 20;
 
 // L2 prefetch of the down rows [dh0, dh1) of every used expert (the rows that
@@ -661,9 +739,9 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
   grid_dependents_launch();
   grid_dependency_wait();
   COLI_TRACE_POINT(a.layer, kTpGuDepWait);
-  load_lists(a, s_act, s_routes, s_slot_gate);   // ends with __syncthreads
-  COLI_TRACE_POINT(a.layer, kTpGuLists);
   const LayerPtrs lp = layer_ptrs(a);
+  gu_lists(a, lp, smem + L.ring, s_act, s_routes, s_slot_gate);   // ends with __syncthreads
+  COLI_TRACE_POINT(a.layer, kTpGuLists);
   const int H = a.H, F = a.F;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, NW = blockDim.x >> 5;
   const int n_active = s_act[0];
@@ -808,9 +886,9 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup_multi(Dec2Args a) {
   grid_dependents_launch();
   grid_dependency_wait();
   COLI_TRACE_POINT(a.layer, kTpGuDepWait);
-  load_lists(a, s_act, s_routes, s_slot_gate);   // ends with __syncthreads
-  COLI_TRACE_POINT(a.layer, kTpGuLists);
   const LayerPtrs lp = layer_ptrs(a);
+  gu_lists(a, lp, smem + L.ring, s_act, s_routes, s_slot_gate);   // ends with __syncthreads
+  COLI_TRACE_POINT(a.layer, kTpGuLists);
   const int T = a.T, H = a.H, F = a.F, KS = a.k + a.S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, NW = blockDim.x >> 5;
   const int n_active = s_act[0];
@@ -1034,7 +1112,9 @@ __device__ void dn_phase(const Dec2Args &a, const LayerPtrs &lp, const int *s_ac
     if (my_tasks) ci.init(warp, ncg, gpe, ga);
     cc = ci;
     for (int i = tid; i < (gb - ga) * nr * T * ncg; i += blockDim.x) red[i] = 0.0f;
+    if (ga == 0) COLI_TRACE_POINT(a.layer, kTpDnPlaneStart);
     build_planes_list(h_rep, F, s_routes + p0, np, s_planes, nbp);
+    if (ga == 0) COLI_TRACE_POINT(a.layer, kTpDnPlaneBuilt);
     __syncthreads();
     if (ga == 0) COLI_TRACE_POINT(a.layer, kTpDnPlanes);
     for (int p = 0; p < Sl - 1; ++p) {
@@ -1188,6 +1268,7 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
   grid_dependents_launch();
   grid_dependency_wait();
   COLI_TRACE_POINT(a.layer, kTpDnDepWait);
+  clear_fx(a);
   int *s_act = (int *)(smem + L.act);
   int *s_routes = (int *)(smem + L.routes);
   load_lists(a, s_act, s_routes, nullptr);
@@ -1200,10 +1281,13 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
     if (a.fx) dn_partials_fx<WT>(a, s_wr, s_xn);
     else dn_partials<WT>(a, a.partials, s_wr, s_xn, 1, 0);
     COLI_TRACE_POINT(a.layer, kTpDnPartials);
-    // the last CTA routes the next layer (its shared memory is free again)
-    LayerPtrs rp = lp;
-    rp.route_counts = a.next_counts;
-    route_if_last(a, rp, smem);
+    // without fixed-point logits the last CTA routes the next layer (its
+    // shared memory is free again); with them the next gate/up does
+    if (!a.route_gu) {
+      LayerPtrs rp = lp;
+      rp.route_counts = a.next_counts;
+      route_if_last(a, rp, smem);
+    }
   }
   COLI_TRACE_POINT(a.layer, kTpEnd);
 }
@@ -1327,16 +1411,32 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down_multi(Dec2Args a) {
 
 #ifdef COLI_TRACE
 extern "C" int coli_trace_reset() {
-  static unsigned long long lo[kTraceLayers][kTracePoints];
-  for (auto &row : lo)
-    for (auto &v : row) v = ~0ull;
-  if (cudaMemcpyToSymbol(g_trace_lo, lo, sizeof(lo)) != cudaSuccess) return -1;
-  static unsigned long long hi[kTraceLayers][kTracePoints] = {};
-  return cudaMemcpyToSymbol(g_trace_hi, hi, sizeof(hi)) == cudaSuccess ? 0 : -1;
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_trace) != cudaSuccess) return -1;
+  return cudaMemset(p, 0, sizeof(g_trace)) == cudaSuccess ? 0 : -1;
 }
+// [layer][point][cta] timestamps (0: not reached).
+extern "C" int coli_trace_read_raw(void *buf) {
+  return cudaMemcpyFromSymbol(buf, g_trace, sizeof(g_trace)) == cudaSuccess ? 0 : -1;
+}
+// Earliest / latest timestamp per [layer][point] over the CTAs that reached it.
 extern "C" int coli_trace_read(void *lo, void *hi) {
-  if (cudaMemcpyFromSymbol(lo, g_trace_lo, sizeof(g_trace_lo)) != cudaSuccess) return -1;
-  return cudaMemcpyFromSymbol(hi, g_trace_hi, sizeof(g_trace_hi)) == cudaSuccess ? 0 : -1;
+  static unsigned long long raw[kTraceLayers][kTracePoints][kTraceCtas];
+  if (coli_trace_read_raw(raw) != 0) return -1;
+  auto *L = (unsigned long long *)lo, *Hh = (unsigned long long *)hi;
+  for (int l = 0; l < kTraceLayers; ++l)
+    for (int p = 0; p < kTracePoints; ++p) {
+      unsigned long long mn = ~0ull, mx = 0;
+      for (int c = 0; c < kTraceCtas; ++c) {
+        const unsigned long long t = raw[l][p][c];
+        if (!t) continue;
+        mn = t < mn ? t : mn;
+        mx = t > mx ? t : mx;
+      }
+      L[l * kTracePoints + p] = mn;
+      Hh[l * kTracePoints + p] = mx;
+    }
+  return 0;
 }
 #endif
 
@@ -1464,6 +1564,8 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
     g.total = al16(o);
   }
   a.gu = g;
+  a.gu_route_fits = gu_route_smem(T, E, k).total <=
+                    (size_t)a.gu_nw * a.gu_slots * a.gu_slot_bytes;
   // ---- down: dn_nw warps with dn_slots_pipe-deep cp.async pipelines; expert
   // batches of at most dn_batch experts and dn_slots token slots
   a.dn_ncg = (F + kChunkCols - 1) / kChunkCols;
