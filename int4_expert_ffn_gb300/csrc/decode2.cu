@@ -1022,19 +1022,6 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup_multi(Dec2Args a) {
 
 struct DnTask {
   int a, gi, cg;     // expert (index into the used list), 8-row group, chunk
-  __device__ __forceinline__ void init(int l, int ncg, int gpe, int ga) {
-    const int u = l / ncg;
-    cg = l - u * ncg;
-    a = ga + u / gpe;
-    gi = u - (a - ga) * gpe;
-  }
-  __device__ __forceinline__ void next(int du, int dcg, int ncg, int gpe) {
-    int d = du;
-    cg += dcg;
-    if (cg >= ncg) { cg -= ncg; ++d; }
-    gi += d;
-    while (gi >= gpe) { gi -= gpe; ++a; }
-  }
 };
 
 __device__ __forceinline__ void dn_copy(const Dec2Args &a, const LayerPtrs &lp,
@@ -1064,6 +1051,24 @@ __device__ __forceinline__ void dn_copy(const Dec2Args &a, const LayerPtrs &lp,
   }
 }
 
+// A warp's run of one-token down tasks in (expert, chunk, 8-row group) order.
+struct DnSeq {
+  int a, cg, gi;
+  __device__ __forceinline__ void init(int l, int ncg, int gpe) {
+    gi = l % gpe;
+    const int u = l / gpe;
+    cg = u % ncg;
+    a = u / ncg;
+  }
+  __device__ __forceinline__ void next(int ncg, int gpe) {
+    if (++gi == gpe) {
+      gi = 0;
+      if (++cg == ncg) { cg = 0; ++a; }
+    }
+  }
+  __device__ __forceinline__ DnTask task() const { return DnTask{a, gi, cg}; }
+};
+
 template <bool kOne>
 __device__ void dn_phase(const Dec2Args &a, const LayerPtrs &lp, const int *s_act,
                          const int *s_routes, uint8_t *smem, float *s_xn, const float *residual) {
@@ -1074,19 +1079,7 @@ __device__ void dn_phase(const Dec2Args &a, const LayerPtrs &lp, const int *s_ac
   const int UH = H / 4;
   const int dh0 = 4 * part_lo(c, UH, G), dh1 = 4 * part_lo(c + 1, UH, G);
   const int nr = dh1 - dh0;
-  const int *s_act_expert = s_act + 1;
-  const int *s_act_off = s_act + 1 + (E + S);
-  const int n_active = s_act[0];
-  const float *h_rep = a.h + (size_t)(c % a.n_rep) * a.h_stride;
-  const int ncg = a.dn_ncg, Sl = a.dn_slots_pipe, nbp = F / 32;
-  const int gpe = (nr + 7) / 8;                  // 8-row groups per expert
-  const int du = NW / ncg, dcg = NW - du * ncg;
-  const bool vec_scales = (F % 256) == 0;
   float *acc = (float *)(smem + L.acc);          // [nr][T]
-  float *red = (float *)(smem + L.red);          // [batch expert][nr][T][ncg]
-  uint32_t *s_planes = (uint32_t *)(smem + L.planes);
-  const int SB = a.dn_slot_bytes;
-  uint8_t *ring = smem + L.ring + (size_t)warp * Sl * SB;
   if (!kOne) {
     // several tokens: k_down_multi left each slot's down output in y; a
     // token's rows add its slots in slot order (routed by rank, then shared)
@@ -1097,30 +1090,33 @@ __device__ void dn_phase(const Dec2Args &a, const LayerPtrs &lp, const int *s_ac
       acc[r * T + t] = sum;
     }
     __syncthreads();
-  }
-  for (int i = tid; i < nr * T && kOne; i += blockDim.x) acc[i] = 0.0f;
-  // experts in batches: their slots' planes and their partial sums must fit
-  for (int ga = 0; ga < (kOne ? n_active : 0);) {
-    int gb = ga;
-    while (gb < n_active && gb - ga < a.dn_batch && s_act_off[gb + 1] - s_act_off[ga] <= a.dn_slots)
-      ++gb;
-    if (gb == ga) gb = ga + 1;   // the plan guarantees one expert's tokens fit
-    const int p0 = s_act_off[ga], np = s_act_off[gb] - p0;
-    const int n_tasks = (gb - ga) * gpe * ncg;
-    const int my_tasks = n_tasks > warp ? (n_tasks - warp + NW - 1) / NW : 0;
-    DnTask ci, cc;
-    if (my_tasks) ci.init(warp, ncg, gpe, ga);
+  } else {
+    // one token: every used expert's (8-row group, chunk) tasks at once; a
+    // warp quantises the h slice of a task's expert in registers when the
+    // (expert, chunk) changes, so no block-wide plane build precedes the work
+    const int *s_act_expert = s_act + 1;
+    const int *s_act_off = s_act + 1 + (E + S);
+    const int n_active = s_act[0];
+    const float *h_rep = a.h + (size_t)(c % a.n_rep) * a.h_stride;
+    const int ncg = a.dn_ncg, Sl = a.dn_slots_pipe;
+    const int gpe = (nr + 7) / 8;                  // 8-row groups per expert
+    const bool vec_scales = (F % 256) == 0;
+    float *red = (float *)(smem + L.red);          // [expert][nr][ncg]
+    const int SB = a.dn_slot_bytes;
+    uint8_t *ring = smem + L.ring + (size_t)warp * Sl * SB;
+    // warp w takes tasks [l0, l1) in (expert, chunk, group) order, so its
+    // consecutive tasks share the expert's h slice
+    const int n_tasks = n_active * gpe * ncg;
+    const int l0 = part_lo(warp, n_tasks, NW);
+    const int my_tasks = part_lo(warp + 1, n_tasks, NW) - l0;
+    DnSeq ci, cc;
+    ci.init(l0, ncg, gpe);
     cc = ci;
-    for (int i = tid; i < (gb - ga) * nr * T * ncg; i += blockDim.x) red[i] = 0.0f;
-    if (ga == 0) COLI_TRACE_POINT(a.layer, kTpDnPlaneStart);
-    build_planes_list(h_rep, F, s_routes + p0, np, s_planes, nbp);
-    if (ga == 0) COLI_TRACE_POINT(a.layer, kTpDnPlaneBuilt);
-    __syncthreads();
-    if (ga == 0) COLI_TRACE_POINT(a.layer, kTpDnPlanes);
+    COLI_TRACE_POINT(a.layer, kTpDnPlanes);
     for (int p = 0; p < Sl - 1; ++p) {
       if (p < my_tasks) {
-        dn_copy(a, lp, s_act_expert, ring + (size_t)p * SB, ci, dh0, nr, vec_scales);
-        ci.next(du, dcg, ncg, gpe);
+        dn_copy(a, lp, s_act_expert, ring + (size_t)p * SB, ci.task(), dh0, nr, vec_scales);
+        ci.next(ncg, gpe);
       }
       cp_async_commit();
     }
@@ -1128,58 +1124,54 @@ __device__ void dn_phase(const Dec2Args &a, const LayerPtrs &lp, const int *s_ac
     int pl_key = -1;
     for (int i = 0; i < my_tasks; ++i) {
       if (i + Sl - 1 < my_tasks) {
-        dn_copy(a, lp, s_act_expert, ring + (size_t)((i + Sl - 1) % Sl) * SB, ci, dh0,
+        dn_copy(a, lp, s_act_expert, ring + (size_t)((i + Sl - 1) % Sl) * SB, ci.task(), dh0,
                 nr, vec_scales);
-        ci.next(du, dcg, ncg, gpe);
+        ci.next(ncg, gpe);
       }
       cp_async_commit();
+      const int col = cc.cg * kChunkCols + 32 * lane;
+      const bool act = col < F;
+      const int key = cc.a * 64 + cc.cg;
+      if (act && key != pl_key) {
+        // the h loads go out before this task's weights are waited for
+        float xv[32];
+        load32<float>(h_rep + (int64_t)s_routes[s_act_off[cc.a]] * F + col, xv);
+        quantize32(xv, pl);
+        pl_key = key;
+      }
       cp_async_wait_dyn(Sl - 1);
       if (vec_scales) __syncwarp();
       const uint8_t *slot = ring + (size_t)(i % Sl) * SB;
-      const int col = cc.cg * kChunkCols + 32 * lane;
-      const bool act = col < F;
       const int r0 = 8 * cc.gi, nq = nr - r0 < 8 ? nr - r0 : 8;
       uint4 w[8];
       float sc[8];
       gu_slot_values(slot, act, vec_scales, w, sc);
-      const int j0 = s_act_off[cc.a];
-      const int nt = kOne ? 1 : s_act_off[cc.a + 1] - j0;
-      for (int j = 0; j < nt; ++j) {
-        const int t = kOne ? 0 : s_routes[j0 + j] / KS;
-        float v[8];
-        if (act) {
-          const int key = (j0 + j) * 64 + cc.cg;
-          if (key != pl_key) {
-            load_planes(s_planes, j0 + j - p0, col / 32, nbp, pl);
-            pl_key = key;
-          }
+      float v[8];
+      if (act) {
 #pragma unroll
-          for (int q = 0; q < 8; ++q) v[q] = q < nq ? sc[q] * dot32(w[q], pl) : 0.0f;
-        } else {
+        for (int q = 0; q < 8; ++q) v[q] = q < nq ? sc[q] * dot32(w[q], pl) : 0.0f;
+      } else {
 #pragma unroll
-          for (int q = 0; q < 8; ++q) v[q] = 0.0f;
-        }
-        const float tot = reduce8(v);   // lane 4 q ends with row q
-        if ((lane & 3) == 0) {
-          const int q = lane >> 2;
-          if (q < nq)
-            red[((((cc.a - ga) * nr + r0 + q) * T + t) * ncg) + cc.cg] = tot;
-        }
+        for (int q = 0; q < 8; ++q) v[q] = 0.0f;
+      }
+      const float tot = reduce8(v);   // lane 4 q ends with row q
+      if ((lane & 3) == 0) {
+        const int q = lane >> 2;
+        if (q < nq) red[(cc.a * nr + r0 + q) * ncg + cc.cg] = tot;
       }
       __syncwarp();
-      cc.next(du, dcg, ncg, gpe);
+      cc.next(ncg, gpe);
     }
     cp_async_wait<0>();
     __syncthreads();
-    // add the batch's partial sums, experts and chunks in a fixed order
-    for (int i = tid; i < nr * T; i += blockDim.x) {
-      float s = 0.0f;
-      for (int x = 0; x < gb - ga; ++x)
-        for (int q = 0; q < ncg; ++q) s += red[((x * nr) * T + i) * ncg + q];
-      acc[i] += s;
+    // every row adds its experts' and chunks' partial sums in a fixed order
+    for (int r = tid; r < nr; r += blockDim.x) {
+      float sum = 0.0f;
+      for (int x = 0; x < n_active; ++x)
+        for (int q = 0; q < ncg; ++q) sum += red[(x * nr + r) * ncg + q];
+      acc[r] = sum;
     }
     __syncthreads();
-    ga = gb;
   }
   COLI_TRACE_POINT(a.layer, kTpDnCompute);
   // combine is complete: residual, outputs, replicas of the new layer input
@@ -1580,47 +1572,27 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
   d.acc = o; o = al16(o + (size_t)max_nr * T * 4);
   d.xn = o; o = al16(o + (size_t)T * max_nr * 4);
   d.wr = o; o = al16(o + (size_t)E * max_nr * (a.wr_bf16 ? 2 : 4));
-  const size_t per_slot = (size_t)18 * (F / 32) * 4;
-  const size_t per_expert_red = (size_t)max_nr * T * a.dn_ncg * 4;
-  const int all_slots = T * KS;
-  // the largest tokens-per-expert count is T (routed) or T (shared)
+  // one token: every used expert's partial sums [expert][row][chunk] at once
+  const int n_exp = (E < k ? E : k) + S;
+  const size_t red_bytes = (size_t)n_exp * max_nr * a.dn_ncg * 4;
   // more warps before deeper pipelines: each warp works its tasks in order, so
   // the down phase's latency follows the tasks per warp
   static const int kDnNw[] = {16, 12, 8, 12, 8, 8, 4};
   static const int kDnSl[] = {2, 3, 4, 2, 3, 2, 2};
   bool dn_ok = false;
-  for (int pass = 0; pass < 2 && !dn_ok; ++pass)
-    for (int c = 0; c < 7 && !dn_ok; ++c) {
-      const size_t ring = (size_t)kDnNw[c] * kDnSl[c] * a.dn_slot_bytes;
-      const size_t base = al128(o) + ring + 128;
-      if (base >= budget) continue;
-      // pass 0: every slot's planes and every used expert's partials at once
-      const int n_exp = ((E < T * k) ? E : T * k) + S;
-      int slots = pass == 0 ? all_slots : T;
-      int batch = pass == 0 ? n_exp : 1;
-      size_t need = base + (size_t)slots * per_slot + (size_t)batch * per_expert_red;
-      if (pass == 1) {
-        // as many slots / experts as fit, in proportion
-        const size_t room = budget - base;
-        slots = (int)((room / 2) / per_slot);
-        batch = (int)((room / 2) / per_expert_red);
-        if (slots > all_slots) slots = all_slots;
-        if (batch > n_exp) batch = n_exp;
-        need = base + (size_t)slots * per_slot + (size_t)batch * per_expert_red;
-        if (slots < T || batch < 1) continue;
-      }
-      if (need > budget) continue;
-      a.dn_nw = kDnNw[c];
-      a.dn_slots_pipe = kDnSl[c];
-      a.dn_slots = slots;
-      a.dn_batch = batch;
-      dn_ok = true;
-    }
+  for (int c = 0; c < 7 && !dn_ok; ++c) {
+    const size_t ring = (size_t)kDnNw[c] * kDnSl[c] * a.dn_slot_bytes;
+    if (al128(o) + ring + 16 + red_bytes > budget) continue;
+    a.dn_nw = kDnNw[c];
+    a.dn_slots_pipe = kDnSl[c];
+    dn_ok = true;
+  }
   if (!dn_ok) return cudaErrorInvalidValue;
+  a.dn_slots = a.dn_batch = 0;
   d.ring = al128(o); o = d.ring + (size_t)a.dn_nw * a.dn_slots_pipe * a.dn_slot_bytes;
-  d.red = al16(o); o = d.red + (size_t)a.dn_batch * per_expert_red;
-  d.planes = al16(o); o = al16(d.planes + (size_t)a.dn_slots * per_slot);
-  d.total = o;
+  d.red = al16(o); o = d.red + red_bytes;
+  d.planes = o;
+  d.total = al16(o);
   a.dn = d;
   return cudaSuccess;
 }
