@@ -728,6 +728,9 @@ __device__ __forceinline__ void prefetch_down_rows(const Dec2Args &a, const Laye
 // One token per call: every used expert serves token 0, each warp quantises
 // the 1024-column slice of x that its chunk needs once (kept in registers),
 // and there is no token loop.
+// kFast: H a multiple of 1024 (every lane of every chunk active, 16-byte
+// aligned scale rows), checks folded away.
+template <bool kFast>
 __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const GuSmem &L = a.gu;
@@ -753,7 +756,7 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
   const float *xr = lp.xrep + (size_t)(c % a.n_rep) * a.x_stride;
   const int ncg = a.gu_ncg, S = a.gu_slots;
   const int dg = NW / ncg, dcg = NW - dg * ncg;
-  const bool vec_scales = (H % 256) == 0;
+  const bool vec_scales = kFast || (H % 256) == 0;
   const int SB = a.gu_slot_bytes;
   uint8_t *ring = smem + L.ring + (size_t)warp * S * SB;
 
@@ -776,11 +779,13 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
     if (rb0 == 0) COLI_TRACE_POINT(a.layer, kTpGuFirstLoads);
     Planes pl;
     int pl_cg = -1;             // chunk whose planes are in `pl`
+    int ld = S - 1, cs = 0;     // ring slots of the next copy / the next compute
     for (int i = 0; i < my_tasks; ++i) {
       if (i + S - 1 < my_tasks) {
-        gu_copy(a, lp, s_act_expert, ring + (size_t)((i + S - 1) % S) * SB, ci, vec_scales);
+        gu_copy(a, lp, s_act_expert, ring + (size_t)ld * SB, ci, vec_scales);
         ci.next(dg, dcg, ncg, F);
       }
+      if (++ld == S) ld = 0;
       if (i == (my_tasks > S - 1 ? my_tasks - (S - 1) : 0) && warp == 0 &&
           rb0 + a.gu_rows >= nrows) {
         // every gate/up copy of this warp is issued: L2 prefetch of the down rows
@@ -790,9 +795,10 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
       cp_async_commit();
       cp_async_wait_dyn(S - 1);      // this lane's copies of task i have landed
       if (vec_scales) __syncwarp();  // scales were copied by other lanes
-      const uint8_t *slot = ring + (size_t)(i % S) * SB;
+      const uint8_t *slot = ring + (size_t)cs * SB;
+      if (++cs == S) cs = 0;
       const int col = cc.cg * kChunkCols + 32 * lane;
-      const bool act = col < H;
+      const bool act = kFast || col < H;
       uint4 w[8];
       float sc[8];
       gu_slot_values(slot, act, vec_scales, w, sc);
@@ -874,6 +880,7 @@ struct MTask {
   __device__ __forceinline__ GuTask gu() const { return GuTask{0, cg, ai, f}; }
 };
 
+template <bool kFast>
 __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup_multi(Dec2Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const GuSmem &L = a.gu;
@@ -903,7 +910,7 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup_multi(Dec2Args a) {
   const int u1 = group_at_cost(s_act_off, n_active, gpe, total * (c + 1) / G);
   const float *xr = lp.xrep + (size_t)(c % a.n_rep) * a.x_stride;
   const int ncg = a.gu_ncg, S = a.gu_slots, nbx = H / 32;
-  const bool vec_scales = (H % 256) == 0;
+  const bool vec_scales = kFast || (H % 256) == 0;
   const bool xpl = a.gu_xpl != 0;
   const int SB = a.gu_slot_bytes;
   uint8_t *ring = smem + L.ring + (size_t)warp * S * SB;
@@ -946,19 +953,22 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup_multi(Dec2Args a) {
   COLI_TRACE_POINT(a.layer, kTpGuFirstLoads);
   Planes pl;
   int pl_key = -1;            // (token, chunk) whose planes are in `pl`
+  int ld = S - 1, cs = 0;     // ring slots of the next copy / the next compute
   for (int i = 0; i < my_tasks; ++i) {
     if (i + S - 1 < my_tasks) {
-      gu_copy(a, lp, s_act_expert, ring + (size_t)((i + S - 1) % S) * SB, ci.gu(), vec_scales);
+      gu_copy(a, lp, s_act_expert, ring + (size_t)ld * SB, ci.gu(), vec_scales);
       ci.next(NW, ncg, gpe);
     }
+    if (++ld == S) ld = 0;
     if (i == (my_tasks > S - 1 ? my_tasks - (S - 1) : 0) && warp == 0)
       prefetch_down_rows(a, lp, s_act_expert, n_active, c);
     cp_async_commit();
     cp_async_wait_dyn(S - 1);
     if (vec_scales) __syncwarp();
-    const uint8_t *slot = ring + (size_t)(i % S) * SB;
+    const uint8_t *slot = ring + (size_t)cs * SB;
+    if (++cs == S) cs = 0;
     const int col = cc.cg * kChunkCols + 32 * lane;
-    const bool act = col < H;
+    const bool act = kFast || col < H;
     uint4 w[8];
     float sc[8];
     gu_slot_values(slot, act, vec_scales, w, sc);
@@ -1069,7 +1079,7 @@ struct DnSeq {
   __device__ __forceinline__ DnTask task() const { return DnTask{a, gi, cg}; }
 };
 
-template <bool kOne>
+template <bool kOne, bool kFast>
 __device__ void dn_phase(const Dec2Args &a, const LayerPtrs &lp, const int *s_act,
                          const int *s_routes, uint8_t *smem, float *s_xn, const float *residual) {
   const DnSmem &L = a.dn;
@@ -1100,7 +1110,7 @@ __device__ void dn_phase(const Dec2Args &a, const LayerPtrs &lp, const int *s_ac
     const float *h_rep = a.h + (size_t)(c % a.n_rep) * a.h_stride;
     const int ncg = a.dn_ncg, Sl = a.dn_slots_pipe;
     const int gpe = (nr + 7) / 8;                  // 8-row groups per expert
-    const bool vec_scales = (F % 256) == 0;
+    const bool vec_scales = kFast || (F % 256) == 0;
     float *red = (float *)(smem + L.red);          // [expert][nr][ncg]
     const int SB = a.dn_slot_bytes;
     uint8_t *ring = smem + L.ring + (size_t)warp * Sl * SB;
@@ -1122,15 +1132,16 @@ __device__ void dn_phase(const Dec2Args &a, const LayerPtrs &lp, const int *s_ac
     }
     Planes pl;
     int pl_key = -1;
+    int ld = Sl - 1, cs = 0;    // ring slots of the next copy / the next compute
     for (int i = 0; i < my_tasks; ++i) {
       if (i + Sl - 1 < my_tasks) {
-        dn_copy(a, lp, s_act_expert, ring + (size_t)((i + Sl - 1) % Sl) * SB, ci.task(), dh0,
-                nr, vec_scales);
+        dn_copy(a, lp, s_act_expert, ring + (size_t)ld * SB, ci.task(), dh0, nr, vec_scales);
         ci.next(ncg, gpe);
       }
+      if (++ld == Sl) ld = 0;
       cp_async_commit();
       const int col = cc.cg * kChunkCols + 32 * lane;
-      const bool act = col < F;
+      const bool act = kFast || col < F;
       const int key = cc.a * 64 + cc.cg;
       if (act && key != pl_key) {
         // the h loads go out before this task's weights are waited for
@@ -1141,7 +1152,8 @@ __device__ void dn_phase(const Dec2Args &a, const LayerPtrs &lp, const int *s_ac
       }
       cp_async_wait_dyn(Sl - 1);
       if (vec_scales) __syncwarp();
-      const uint8_t *slot = ring + (size_t)(i % Sl) * SB;
+      const uint8_t *slot = ring + (size_t)cs * SB;
+      if (++cs == Sl) cs = 0;
       const int r0 = 8 * cc.gi, nq = nr - r0 < 8 ? nr - r0 : 8;
       uint4 w[8];
       float sc[8];
@@ -1249,7 +1261,7 @@ __device__ void load_router_rows(const Dec2Args &a, const WT *wr, WT *s_wr) {
   }
 }
 
-template <typename WT, bool kOne>
+template <typename WT, bool kOne, bool kFast>
 __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const DnSmem &L = a.dn;
@@ -1267,7 +1279,7 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
   COLI_TRACE_POINT(a.layer, kTpDnLists);
   float *s_xn = (float *)(smem + L.xn);
   const LayerPtrs lp = layer_ptrs(a);
-  dn_phase<kOne>(a, lp, s_act, s_routes, smem, s_xn, a.residual);
+  dn_phase<kOne, kFast>(a, lp, s_act, s_routes, smem, s_xn, a.residual);
   COLI_TRACE_POINT(a.layer, kTpDnCombine);
   if (a.wr) {
     if (a.fx) dn_partials_fx<WT>(a, s_wr, s_xn);
@@ -1291,6 +1303,7 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
 // slot of the expert.  The CTA's slots' h rows are quantised once into shared
 // memory when they fit (else per task in registers).  k_down then adds each
 // token's slots.
+template <bool kFast>
 __global__ void __launch_bounds__(kDec2MaxThreads) k_down_multi(Dec2Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const DmSmem &L = a.dm;
@@ -1315,7 +1328,7 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down_multi(Dec2Args a) {
   const int u1 = group_at_cost(s_act_off, n_active, gpe, total * (c + 1) / G);
   const float *h_rep = a.h + (size_t)(c % a.n_rep) * a.h_stride;
   const int ncg = a.dn_ncg, Sl = a.dm_slots_pipe, nbp = F / 32;
-  const bool vec_scales = (F % 256) == 0;
+  const bool vec_scales = kFast || (F % 256) == 0;
   const int SB = a.dn_slot_bytes;
   uint8_t *ring = smem + L.ring + (size_t)warp * Sl * SB;
   float *acc = (float *)(smem + L.acc) + (size_t)warp * T * 8;   // [T][8] of this warp
@@ -1342,18 +1355,20 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down_multi(Dec2Args a) {
   }
   Planes pl;
   int pl_key = -1;
+  int ld = Sl - 1, cs = 0;    // ring slots of the next copy / the next compute
   for (int i = 0; i < my_tasks; ++i) {
     if (i + Sl - 1 < my_tasks) {
-      dn_copy(a, lp, s_act_expert, ring + (size_t)((i + Sl - 1) % Sl) * SB, task(ci_u, ci_cg),
-              0, H, vec_scales);
+      dn_copy(a, lp, s_act_expert, ring + (size_t)ld * SB, task(ci_u, ci_cg), 0, H, vec_scales);
       if (++ci_cg == ncg) { ci_cg = 0; ci_u += NW; }
     }
+    if (++ld == Sl) ld = 0;
     cp_async_commit();
     cp_async_wait_dyn(Sl - 1);
     if (vec_scales) __syncwarp();
-    const uint8_t *slot = ring + (size_t)(i % Sl) * SB;
+    const uint8_t *slot = ring + (size_t)cs * SB;
+    if (++cs == Sl) cs = 0;
     const int col = cc_cg * kChunkCols + 32 * lane;
-    const bool act = col < F;
+    const bool act = kFast || col < F;
     uint4 w[8];
     float sc[8];
     gu_slot_values(slot, act, vec_scales, w, sc);
@@ -1678,18 +1693,25 @@ cudaError_t launch_route_partials(const Dec2Args &a_in, int x_bf16, int w_bf16, 
 cudaError_t launch_gateup(const Dec2Args &a, int grid, cudaStream_t s, bool pdl) {
   const int threads = 32 * a.gu_nw;
   cudaError_t e;
-  if (a.T == 1) {
-    if ((e = allow_smem(k_gateup, a.gu.total)) != cudaSuccess) return e;
-    return launch(k_gateup, grid, threads, a.gu.total, s, pdl, a);
-  }
-  if ((e = allow_smem(k_gateup_multi, a.gu.total)) != cudaSuccess) return e;
-  return launch(k_gateup_multi, grid, threads, a.gu.total, s, pdl, a);
+  const bool fast = a.H % kChunkCols == 0;
+#define COLI_LAUNCH_GU(K)                                                                \
+  if ((e = allow_smem(K, a.gu.total)) != cudaSuccess) return e;                         \
+  return launch(K, grid, threads, a.gu.total, s, pdl, a);
+  if (a.T == 1 && fast) { COLI_LAUNCH_GU(k_gateup<true>) }
+  if (a.T == 1) { COLI_LAUNCH_GU(k_gateup<false>) }
+  if (fast) { COLI_LAUNCH_GU(k_gateup_multi<true>) }
+  COLI_LAUNCH_GU(k_gateup_multi<false>)
+#undef COLI_LAUNCH_GU
 }
 
 cudaError_t launch_down_multi(const Dec2Args &a, cudaStream_t s, bool pdl) {
   cudaError_t e;
-  if ((e = allow_smem(k_down_multi, a.dm.total)) != cudaSuccess) return e;
-  return launch(k_down_multi, num_sms(), 32 * a.dm_nw, a.dm.total, s, pdl, a);
+  if (a.F % kChunkCols == 0) {
+    if ((e = allow_smem(k_down_multi<true>, a.dm.total)) != cudaSuccess) return e;
+    return launch(k_down_multi<true>, num_sms(), 32 * a.dm_nw, a.dm.total, s, pdl, a);
+  }
+  if ((e = allow_smem(k_down_multi<false>, a.dm.total)) != cudaSuccess) return e;
+  return launch(k_down_multi<false>, num_sms(), 32 * a.dm_nw, a.dm.total, s, pdl, a);
 }
 
 cudaError_t launch_down(const Dec2Args &a_in, int wr_bf16, cudaStream_t s, bool pdl) {
@@ -1703,13 +1725,17 @@ cudaError_t launch_down(const Dec2Args &a_in, int wr_bf16, cudaStream_t s, bool 
     if (rs > smem) smem = rs;
   }
   cudaError_t e;
-#define COLI_LAUNCH_DOWN(WT, ONE)                                                        \
-  if ((e = allow_smem(k_down<WT, ONE>, smem)) != cudaSuccess) return e;                  \
-  return launch(k_down<WT, ONE>, a.n_part, threads, smem, s, pdl, a);
-  if (wr_bf16 && a.T == 1) { COLI_LAUNCH_DOWN(__nv_bfloat16, true) }
-  if (wr_bf16) { COLI_LAUNCH_DOWN(__nv_bfloat16, false) }
-  if (a.T == 1) { COLI_LAUNCH_DOWN(float, true) }
-  COLI_LAUNCH_DOWN(float, false)
+#define COLI_LAUNCH_DOWN(WT, ONE, FAST)                                                  \
+  if ((e = allow_smem(k_down<WT, ONE, FAST>, smem)) != cudaSuccess) return e;            \
+  return launch(k_down<WT, ONE, FAST>, a.n_part, threads, smem, s, pdl, a);
+  // the several-token k_down only adds slots: no chunked loop to specialise
+  const bool fast = a.F % kChunkCols == 0;
+  if (wr_bf16 && a.T == 1 && fast) { COLI_LAUNCH_DOWN(__nv_bfloat16, true, true) }
+  if (wr_bf16 && a.T == 1) { COLI_LAUNCH_DOWN(__nv_bfloat16, true, false) }
+  if (wr_bf16) { COLI_LAUNCH_DOWN(__nv_bfloat16, false, false) }
+  if (a.T == 1 && fast) { COLI_LAUNCH_DOWN(float, true, true) }
+  if (a.T == 1) { COLI_LAUNCH_DOWN(float, true, false) }
+  COLI_LAUNCH_DOWN(float, false, false)
 #undef COLI_LAUNCH_DOWN
 }
 
