@@ -76,7 +76,7 @@ struct DnSmem {
 };
 // Shared-memory plan of k_down_multi.
 struct DmSmem {
-  size_t act, routes, planes, acc, ring, total;
+  size_t act, routes, u, planes, acc, ring, total;
 };
 
 // Arguments of the decode kernels (one layer, T <= kDecodeMaxT tokens).

@@ -136,84 +136,36 @@ __device__ __forceinline__ float reduce8(float (&v)[8]) {
 }
 
 // Quantise n_vec f32 vectors of length F (global, row-major [n_vec][F]) into
-// activation planes in shared memory, transposed for conflict-free reads:
+// activation planes in shared memory, transposed for conflict-free access:
 // word w (0..15 planes, 16 = sq, 17 = sx bits) of 32-column block b of vector v
-// is at planes[(v * 18 + w) * nbp + b].  One warp handles 4 blocks at a time;
-// lane q of a block's 8 lanes holds its columns 4q..4q+3.
+// is at planes[(v * 18 + w) * nbp + b].  Each lane quantises whole blocks in
+// registers (the same arithmetic as the per-warp paths); CTAs start at
+// different blocks so the grid's reads of the same vectors spread over L2.
 __device__ void build_planes_impl(const float *src, int n_vec, int F, const int *list,
                                   uint32_t *planes, int nbp, int warp, int nw) {
-  const int lane = threadIdx.x & 31;
-  const int groups_per_vec = (F + 127) / 128;
-  const int n_groups = n_vec * groups_per_vec;
-  const int q = lane & 7;
-  for (int g0 = warp; g0 < n_groups; g0 += 8 * nw) {
-    // issue up to eight independent loads before using any of them
-    float4 xs[8];
+  const int nb = F / 32;   // F is a multiple of 64
+  const int n_blocks = n_vec * nb;
+  if (n_blocks == 0) return;
+  const int rot = (int)(((long long)blockIdx.x * 37) % n_blocks);
+  for (int i = warp * 32 + (threadIdx.x & 31); i < n_blocks; i += nw * 32) {
+    int g = i + rot;
+    if (g >= n_blocks) g -= n_blocks;
+    const int v = g / nb, b = g - v * nb;
+    const int64_t row = list ? list[v] : v;
+    float xv[32];
+    load32<float>(src + row * F + 32 * b, xv);
+    Planes p;
+    quantize32(xv, p);
+    uint32_t *pv = planes + (size_t)v * 18 * nbp + b;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int g = g0 + u * nw;
-      xs[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (g < n_groups) {
-        const int v = g / groups_per_vec, gc = g - v * groups_per_vec;
-        const int col = gc * 128 + 4 * lane;
-        const int64_t row = list ? list[v] : v;
-        if (col < F) xs[u] = __ldcg((const float4 *)(src + row * F + col));
-      }
+    for (int j = 0; j < 4; ++j) {
+      pv[(size_t)j * nbp] = p.eh[j];
+      pv[(size_t)(4 + j) * nbp] = p.el[j];
+      pv[(size_t)(8 + j) * nbp] = p.oh[j];
+      pv[(size_t)(12 + j) * nbp] = p.ol[j];
     }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-    const int g = g0 + u * nw;
-    if (g >= n_groups) break;
-    const int v = g / groups_per_vec, gc = g - v * groups_per_vec;
-    const int col = gc * 128 + 4 * lane;
-    const bool act = col < F;
-    const float4 x = xs[u];
-    float m = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
-    bool bad = (x.x != x.x) | (x.y != x.y) | (x.z != x.z) | (x.w != x.w);
-#pragma unroll
-    for (int off = 1; off < 8; off <<= 1) {
-      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-      bad |= __shfl_xor_sync(0xFFFFFFFFu, (int)bad, off) != 0;
-    }
-    const float inv = m > 0.0f ? (float)kQ / m : 0.0f;
-    const float sx = bad ? __int_as_float(0x7FC00000) : m / (float)kQ;
-    int qv[4];
-    const float xv[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      qv[i] = (int)fminf(fmaxf(rintf(xv[i] * inv), -(float)kQ), (float)kQ);
-    int hv[4], lv[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      hv[i] = (qv[i] + 64) >> 7;
-      lv[i] = qv[i] - (hv[i] << 7);
-    }
-    // 16-bit halves of the plane words: even columns are elements 0, 2; odd 1, 3
-    const uint32_t eh = (uint32_t)(hv[0] & 0xFF) | ((uint32_t)(hv[2] & 0xFF) << 8);
-    const uint32_t el = (uint32_t)(lv[0] & 0xFF) | ((uint32_t)(lv[2] & 0xFF) << 8);
-    const uint32_t oh = (uint32_t)(hv[1] & 0xFF) | ((uint32_t)(hv[3] & 0xFF) << 8);
-    const uint32_t ol = (uint32_t)(lv[1] & 0xFF) | ((uint32_t)(lv[3] & 0xFF) << 8);
-    const uint32_t eh2 = __shfl_down_sync(0xFFFFFFFFu, eh, 1);
-    const uint32_t el2 = __shfl_down_sync(0xFFFFFFFFu, el, 1);
-    const uint32_t oh2 = __shfl_down_sync(0xFFFFFFFFu, oh, 1);
-    const uint32_t ol2 = __shfl_down_sync(0xFFFFFFFFu, ol, 1);
-    int sq = qv[0] + qv[1] + qv[2] + qv[3];
-#pragma unroll
-    for (int off = 1; off < 8; off <<= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, off);
-    const int b = (gc * 128 + 32 * (lane >> 3)) / 32;   // block index within the vector
-    if (act && (q & 1) == 0) {
-      const int i = q >> 1;
-      uint32_t *pv = planes + (size_t)v * 18 * nbp + b;
-      pv[(size_t)i * nbp] = eh | (eh2 << 16);
-      pv[(size_t)(4 + i) * nbp] = el | (el2 << 16);
-      pv[(size_t)(8 + i) * nbp] = oh | (oh2 << 16);
-      pv[(size_t)(12 + i) * nbp] = ol | (ol2 << 16);
-      if (q == 0) {
-        pv[(size_t)16 * nbp] = (uint32_t)sq;
-        pv[(size_t)17 * nbp] = __float_as_uint(sx);
-      }
-    }
-    }
+    pv[(size_t)16 * nbp] = (uint32_t)p.sq;
+    pv[(size_t)17 * nbp] = __float_as_uint(p.sx);
   }
 }
 
@@ -279,6 +231,12 @@ __device__ __forceinline__ LayerPtrs layer_ptrs(const Dec2Args &a) {
 // added with an integer atomic, so the total does not depend on the order in
 // which CTAs arrive.  A non-finite partial, or one of magnitude 1e7 or more,
 // marks the logit as NaN instead.
+// A fixed-point sum as a float: one rounding of the integer, then the exact
+// power-of-two scale.
+__device__ __forceinline__ float fx_to_float(long long v) {
+  return __ll2float_rn(v) * 0x1p-32f;
+}
+
 __device__ __forceinline__ void fx_add(const Dec2Args &a, int o, float p) {
   if (!(fabsf(p) < 1.0e7f)) {
     atomicOr(a.fx_flag + o, 1u);
@@ -349,7 +307,7 @@ __device__ void route_block(const Dec2Args &a, const LayerPtrs &lp, float *s_log
     for (int i = threadIdx.x; i < TE; i += nthr) {
       const long long v = __ldcg(a.fx_acc + i);
       const uint32_t f = __ldcg(a.fx_flag + i);
-      s_logits[i] = f ? __int_as_float(0x7FC00000) : (float)((double)v * 0x1p-32);
+      s_logits[i] = f ? __int_as_float(0x7FC00000) : fx_to_float(v);
       a.fx_acc[i] = 0;
       a.fx_flag[i] = 0u;
     }
@@ -665,7 +623,7 @@ __device__ void gu_lists(const Dec2Args &a, const LayerPtrs &lp, uint8_t *scratc
   for (int i = threadIdx.x; i < TE; i += blockDim.x) {
     const long long v = __ldcg(a.fx_rd_acc + i);
     const uint32_t f = __ldcg(a.fx_rd_flag + i);
-    s_logits[i] = f ? __int_as_float(0x7FC00000) : (float)((double)v * 0x1p-32);
+    s_logits[i] = f ? __int_as_float(0x7FC00000) : fx_to_float(v);
   }
   __syncthreads();
   COLI_TRACE_POINT(a.layer, kTpRtLogits);
@@ -854,16 +812,56 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
 // chunk writes h = silu(g) * u * gate for the group's rows.  The CTA quantises
 // only the tokens its experts serve (into shared memory when they fit, else
 // per task in registers).
-__device__ __forceinline__ int group_at_cost(const int *s_act_off, int n_active, int gpe,
-                                             long long b) {
-  long long before = 0;
-  for (int ai = 0; ai < n_active; ++ai) {
-    const long long w = 1 + 2LL * (s_act_off[ai + 1] - s_act_off[ai]);
-    const long long span = w * gpe;
-    if (b < before + span) return ai * gpe + (int)((b - before + w - 1) / w);
-    before += span;
+// The (used expert, group) space split by cost: a group of an expert that
+// serves nt tokens costs 1 + 2 nt units; CTA c of G gets the groups [u0, u1)
+// whose cost prefix starts in [c C / G, (c + 1) C / G), C the total.  Warp 0
+// scans the experts 32 at a time and leaves the bounds in s_u (2 ints); all
+// threads read them after the barrier.
+__device__ void cost_split(const int *s_act_off, int n_active, int gpe, int c, int G, int *s_u,
+                           int *u0, int *u1) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    long long total = 0;
+    for (int a0 = 0; a0 < n_active; a0 += 32) {
+      const int ai = a0 + lane;
+      const long long span =
+          ai < n_active ? (1 + 2LL * (s_act_off[ai + 1] - s_act_off[ai])) * gpe : 0;
+      total += span;   // per-lane partial, reduced below
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) total += __shfl_xor_sync(0xFFFFFFFFu, total, off);
+    // first group whose cost prefix reaches b, for the two bounds
+    for (int k = 0; k < 2; ++k) {
+      const long long b = total * (c + k) / G;
+      long long before = 0;
+      int u = n_active * gpe;
+      for (int a0 = 0; a0 < n_active; a0 += 32) {
+        const int ai = a0 + lane;
+        const long long w = ai < n_active ? 1 + 2LL * (s_act_off[ai + 1] - s_act_off[ai]) : 0;
+        long long incl = w * gpe;   // inclusive scan of the spans over the lanes
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const long long o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+          if (lane >= off) incl += o;
+        }
+        const long long excl = before + incl - w * gpe;
+        const bool hit = ai < n_active && b < before + incl;
+        const uint32_t m = __ballot_sync(0xFFFFFFFFu, hit);
+        if (m) {
+          const int src = __ffs(m) - 1;
+          const long long e_b = __shfl_sync(0xFFFFFFFFu, excl, src);
+          const long long w_b = __shfl_sync(0xFFFFFFFFu, w, src);
+          u = (a0 + src) * gpe + (int)((b - e_b + w_b - 1) / w_b);
+          break;
+        }
+        before += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      }
+      if (lane == 0) s_u[k] = u;
+    }
   }
-  return n_active * gpe;
+  __syncthreads();
+  *u0 = s_u[0];
+  *u1 = s_u[1];
 }
 
 struct MTask {
@@ -880,7 +878,7 @@ struct MTask {
   __device__ __forceinline__ GuTask gu() const { return GuTask{0, cg, ai, f}; }
 };
 
-template <bool kFast>
+template <bool kFast, bool kXpl>
 __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup_multi(Dec2Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const GuSmem &L = a.gu;
@@ -889,12 +887,12 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup_multi(Dec2Args a) {
   int *s_routes = (int *)(smem + L.routes);
   float *s_slot_gate = (float *)(smem + L.slot_gate);
   int *s_tok = (int *)(smem + L.tok);            // [T] needed tokens, then [T] token -> plane
-  uint32_t *s_xpl = (uint32_t *)(smem + L.xpl);
+  uint32_t *s_xpl = (uint32_t *)(smem + L.xpl);  // the needed tokens' planes, then the ring
   grid_dependents_launch();
   grid_dependency_wait();
   COLI_TRACE_POINT(a.layer, kTpGuDepWait);
   const LayerPtrs lp = layer_ptrs(a);
-  gu_lists(a, lp, smem + L.ring, s_act, s_routes, s_slot_gate);   // ends with __syncthreads
+  gu_lists(a, lp, smem + L.xpl, s_act, s_routes, s_slot_gate);   // ends with __syncthreads
   COLI_TRACE_POINT(a.layer, kTpGuLists);
   const int T = a.T, H = a.H, F = a.F, KS = a.k + a.S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, NW = blockDim.x >> 5;
@@ -903,18 +901,16 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup_multi(Dec2Args a) {
   const int *s_act_off = s_act + 1 + (a.E + a.S);
   const int G = gridDim.x, c = blockIdx.x;
   const int gpe = F / 4;
-  long long total = 0;
-  for (int ai = 0; ai < n_active; ++ai)
-    total += (1 + 2LL * (s_act_off[ai + 1] - s_act_off[ai])) * gpe;
-  const int u0 = group_at_cost(s_act_off, n_active, gpe, total * c / G);
-  const int u1 = group_at_cost(s_act_off, n_active, gpe, total * (c + 1) / G);
+  int u0, u1;
+  cost_split(s_act_off, n_active, gpe, c, G, (int *)(smem + L.tok) + 2 * T + 1, &u0, &u1);
+  COLI_TRACE_POINT(a.layer, kTpGuSplit);
   const float *xr = lp.xrep + (size_t)(c % a.n_rep) * a.x_stride;
-  const int ncg = a.gu_ncg, S = a.gu_slots, nbx = H / 32;
+  const int ncg = a.gu_ncg, nbx = H / 32;
   const bool vec_scales = kFast || (H % 256) == 0;
-  const bool xpl = a.gu_xpl != 0;
+  const bool xpl = kXpl;   // a.gu_xpl
   const int SB = a.gu_slot_bytes;
-  uint8_t *ring = smem + L.ring + (size_t)warp * S * SB;
   float *acc = (float *)(smem + L.red) + (size_t)warp * T * 8;   // [T][8] of this warp
+  int n_need = 0;
 
   // the tokens that the experts of groups [u0, u1) serve, in token order
   if (u1 > u0 && xpl) {
@@ -932,10 +928,17 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup_multi(Dec2Args a) {
       if (lane == 0) s_tok[2 * T] = __popc(need);
     }
     __syncthreads();
-    build_planes_impl(xr, s_tok[2 * T], H, s_tok, s_xpl, nbx, warp, NW);
+    COLI_TRACE_POINT(a.layer, kTpGuNeed);
+    n_need = s_tok[2 * T];
+    build_planes_impl(xr, n_need, H, s_tok, s_xpl, nbx, warp, NW);
     __syncthreads();
   }
   COLI_TRACE_POINT(a.layer, kTpGuPlanes);
+  // the ring after this CTA's planes, as deep as the rest of shared memory allows
+  const size_t ring_off = (L.xpl + (size_t)n_need * 18 * nbx * 4 + 127) & ~(size_t)127;
+  int S = (int)((L.total - ring_off) / ((size_t)NW * SB));
+  S = S < a.gu_slots ? S : a.gu_slots;
+  uint8_t *ring = smem + ring_off + (size_t)warp * S * SB;
 
   const int n_groups = u1 - u0;
   const int my_groups = n_groups > warp ? (n_groups - warp + NW - 1) / NW : 0;
@@ -1296,50 +1299,21 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
   COLI_TRACE_POINT(a.layer, kTpEnd);
 }
 
-// Down GEMVs of a several-token call, split like k_gateup_multi: the (used
-// expert, 8-row group) space goes to the CTAs by cost (1 + 2 nt units per
-// group); a warp owns whole groups, runs their chunks in order, and after the
-// last one writes y[slot][row] = sum_f down[row][f] h[slot][f] for each token
-// slot of the expert.  The CTA's slots' h rows are quantised once into shared
-// memory when they fit (else per task in registers).  k_down then adds each
-// token's slots.
-template <bool kFast>
-__global__ void __launch_bounds__(kDec2MaxThreads) k_down_multi(Dec2Args a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const DmSmem &L = a.dm;
-  int *s_act = (int *)(smem + L.act);
-  int *s_routes = (int *)(smem + L.routes);
-  uint32_t *s_planes = (uint32_t *)(smem + L.planes);
-  grid_dependents_launch();
-  grid_dependency_wait();
-  load_lists(a, s_act, s_routes, nullptr);   // ends with __syncthreads
-  const LayerPtrs lp = layer_ptrs(a);
-  const int H = a.H, F = a.F, T = a.T;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, NW = blockDim.x >> 5;
-  const int n_active = s_act[0];
-  const int *s_act_expert = s_act + 1;
-  const int *s_act_off = s_act + 1 + (a.E + a.S);
-  const int G = gridDim.x, c = blockIdx.x;
+// The task loop of k_down_multi, compiled apart for planes in shared memory
+// (kXpl) and for planes quantised per task, so that the common case does not
+// carry the fallback's registers.
+template <bool kFast, bool kXpl>
+__device__ __forceinline__ void dm_loop(const Dec2Args &a, const LayerPtrs &lp,
+                                        const int *s_act_expert, const int *s_act_off,
+                                        const int *s_routes, const uint32_t *s_planes,
+                                        const float *h_rep, int u0, int u1, int r0,
+                                        uint8_t *ring, float *acc) {
+  const int H = a.H, F = a.F;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, NW = blockDim.x >> 5;
   const int gpe = H / 8;
-  long long total = 0;
-  for (int ai = 0; ai < n_active; ++ai)
-    total += (1 + 2LL * (s_act_off[ai + 1] - s_act_off[ai])) * gpe;
-  const int u0 = group_at_cost(s_act_off, n_active, gpe, total * c / G);
-  const int u1 = group_at_cost(s_act_off, n_active, gpe, total * (c + 1) / G);
-  const float *h_rep = a.h + (size_t)(c % a.n_rep) * a.h_stride;
   const int ncg = a.dn_ncg, Sl = a.dm_slots_pipe, nbp = F / 32;
   const bool vec_scales = kFast || (F % 256) == 0;
   const int SB = a.dn_slot_bytes;
-  uint8_t *ring = smem + L.ring + (size_t)warp * Sl * SB;
-  float *acc = (float *)(smem + L.acc) + (size_t)warp * T * 8;   // [T][8] of this warp
-  // h rows (slots) of the experts of groups [u0, u1): routes [r0, r1)
-  const int r0 = u1 > u0 ? s_act_off[u0 / gpe] : 0;
-  const int r1 = u1 > u0 ? s_act_off[(u1 - 1) / gpe + 1] : 0;
-  const bool xpl = r1 - r0 <= a.dm_cap;
-  if (u1 > u0 && xpl) {
-    build_planes_list(h_rep, F, s_routes + r0, r1 - r0, s_planes, nbp);
-    __syncthreads();
-  }
   const int n_groups = u1 - u0;
   const int my_groups = n_groups > warp ? (n_groups - warp + NW - 1) / NW : 0;
   const int my_tasks = my_groups * ncg;
@@ -1379,7 +1353,7 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down_multi(Dec2Args a) {
       if (act) {
         const int key = (j0 + j) * 64 + cc_cg;
         if (key != pl_key) {
-          if (xpl) {
+          if (kXpl) {
             load_planes(s_planes, j0 + j - r0, col / 32, nbp, pl);
           } else {
             float xv[32];
@@ -1409,6 +1383,56 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_down_multi(Dec2Args a) {
     }
     __syncwarp();
     if (++cc_cg == ncg) { cc_cg = 0; cc_u += NW; }
+  }
+  cp_async_wait<0>();
+}
+
+// Down GEMVs of a several-token call, split like k_gateup_multi: the (used
+// expert, 8-row group) space goes to the CTAs by cost (1 + 2 nt units per
+// group); a warp owns whole groups, runs their chunks in order, and after the
+// last one writes y[slot][row] = sum_f down[row][f] h[slot][f] for each token
+// slot of the expert.  The CTA's slots' h rows are quantised once into shared
+// memory when they fit (else per task in registers).  k_down then adds each
+// token's slots.
+template <bool kFast>
+__global__ void __launch_bounds__(kDec2MaxThreads) k_down_multi(Dec2Args a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const DmSmem &L = a.dm;
+  int *s_act = (int *)(smem + L.act);
+  int *s_routes = (int *)(smem + L.routes);
+  uint32_t *s_planes = (uint32_t *)(smem + L.planes);
+  grid_dependents_launch();
+  grid_dependency_wait();
+  load_lists(a, s_act, s_routes, nullptr);   // ends with __syncthreads
+  const LayerPtrs lp = layer_ptrs(a);
+  const int H = a.H, F = a.F, T = a.T;
+  const int warp = threadIdx.x >> 5;
+  const int n_active = s_act[0];
+  const int *s_act_expert = s_act + 1;
+  const int *s_act_off = s_act + 1 + (a.E + a.S);
+  const int G = gridDim.x, c = blockIdx.x;
+  const int gpe = H / 8;
+  int u0, u1;
+  cost_split(s_act_off, n_active, gpe, c, G, (int *)(smem + L.u), &u0, &u1);
+  const float *h_rep = a.h + (size_t)(c % a.n_rep) * a.h_stride;
+  const int Sl = a.dm_slots_pipe, nbp = F / 32;
+  const int SB = a.dn_slot_bytes;
+  uint8_t *ring = smem + L.ring + (size_t)warp * Sl * SB;
+  float *acc = (float *)(smem + L.acc) + (size_t)warp * T * 8;   // [T][8] of this warp
+  // h rows (slots) of the experts of groups [u0, u1): routes [r0, r1)
+  const int r0 = u1 > u0 ? s_act_off[u0 / gpe] : 0;
+  const int r1 = u1 > u0 ? s_act_off[(u1 - 1) / gpe + 1] : 0;
+  const bool xpl = r1 - r0 <= a.dm_cap;
+  if (u1 > u0 && xpl) {
+    build_planes_list(h_rep, F, s_routes + r0, r1 - r0, s_planes, nbp);
+    __syncthreads();
+  }
+  if (xpl) {
+    dm_loop<kFast, true>(a, lp, s_act_expert, s_act_off, s_routes, s_planes, h_rep, u0, u1, r0,
+                         ring, acc);
+  } else {
+    dm_loop<kFast, false>(a, lp, s_act_expert, s_act_off, s_routes, s_planes, h_rep, u0, u1, r0,
+                          ring, acc);
   }
   cp_async_wait<0>();
 }
@@ -1548,31 +1572,35 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
     a.gu_rows = rows;
     g.total = al16(g.red + (size_t)rows * row_bytes);
   } else {
-    // several tokens: the needed tokens' planes (when they fit), one [T][8]
-    // accumulator per warp, the ring
-    g.tok = o; o = al16(o + (size_t)(2 * T + 1) * 4);
-    const size_t xpl_bytes = al16((size_t)T * 18 * (H / 32) * 4);
+    // several tokens: one [T][8] accumulator per warp, then the planes of the
+    // tokens the CTA serves and the ring.  Each CTA sizes its ring from what
+    // its planes leave (up to gu_slots deep); the plan makes sure a CTA that
+    // serves all T tokens still gets two slots.  Without room for that, no
+    // planes (x quantised per task).
+    g.tok = o; o = al16(o + (size_t)(2 * T + 3) * 4);
+    const size_t xpl_bytes = (size_t)T * 18 * (H / 32) * 4;
+    static const int kNwM[] = {8, 12, 16, 4};
     for (int xpl = 1; xpl >= 0 && !ok; --xpl)
-      for (int c = 0; c < 6 && !ok; ++c) {
-        const size_t acc = (size_t)kNw[c] * T * 8 * 4;
-        const size_t ring = (size_t)kNw[c] * kSl[c] * a.gu_slot_bytes;
-        if (al128(o + (xpl ? xpl_bytes : 0) + acc) + ring <= budget) {
+      for (int c = 0; c < 4 && !ok; ++c) {
+        const size_t acc = (size_t)kNwM[c] * T * 8 * 4;
+        const size_t ring2 = (size_t)kNwM[c] * 2 * a.gu_slot_bytes;
+        if (al128(al16(o + acc) + (xpl ? xpl_bytes : 0)) + ring2 <= budget) {
           a.gu_xpl = xpl;
-          a.gu_nw = kNw[c];
-          a.gu_slots = kSl[c];
+          a.gu_nw = kNwM[c];
+          a.gu_slots = 4;
           ok = true;
         }
       }
     if (!ok) return cudaErrorInvalidValue;
     a.gu_rows = 0;
-    g.xpl = o; o += a.gu_xpl ? xpl_bytes : 0;
-    g.red = al16(o); o = g.red + (size_t)a.gu_nw * T * 8 * 4;
-    g.ring = al128(o); o = g.ring + (size_t)a.gu_nw * a.gu_slots * a.gu_slot_bytes;
-    g.total = al16(o);
+    g.red = o; o = al16(g.red + (size_t)a.gu_nw * T * 8 * 4);
+    g.xpl = g.ring = o;
+    g.total = budget;
   }
   a.gu = g;
+  // routing scratch: the T = 1 kernel's ring, the several-token kernel's plane area
   a.gu_route_fits = gu_route_smem(T, E, k).total <=
-                    (size_t)a.gu_nw * a.gu_slots * a.gu_slot_bytes;
+                    (T == 1 ? (size_t)a.gu_nw * a.gu_slots * a.gu_slot_bytes : g.total - g.xpl);
   // ---- down: dn_nw warps with dn_slots_pipe-deep cp.async pipelines; expert
   // batches of at most dn_batch experts and dn_slots token slots
   a.dn_ncg = (F + kChunkCols - 1) / kChunkCols;
@@ -1638,6 +1666,7 @@ static cudaError_t plan_down_multi(Dec2Args &a) {
   o = 0;
   m.act = o; o = al16(o + (size_t)(2 + 2 * (E + S)) * 4);
   m.routes = o; o = al16(o + (size_t)T * KS * 4);
+  m.u = o; o += 16;
   const size_t per_slot = (size_t)18 * (F / 32) * 4;
   static const int kNw[] = {16, 12, 8, 12, 8, 8, 4};
   static const int kSl[] = {2, 3, 4, 2, 3, 2, 2};
@@ -1699,8 +1728,10 @@ cudaError_t launch_gateup(const Dec2Args &a, int grid, cudaStream_t s, bool pdl)
   return launch(K, grid, threads, a.gu.total, s, pdl, a);
   if (a.T == 1 && fast) { COLI_LAUNCH_GU(k_gateup<true>) }
   if (a.T == 1) { COLI_LAUNCH_GU(k_gateup<false>) }
-  if (fast) { COLI_LAUNCH_GU(k_gateup_multi<true>) }
-  COLI_LAUNCH_GU(k_gateup_multi<false>)
+  if (fast && a.gu_xpl) { COLI_LAUNCH_GU((k_gateup_multi<true, true>)) }
+  if (fast) { COLI_LAUNCH_GU((k_gateup_multi<true, false>)) }
+  if (a.gu_xpl) { COLI_LAUNCH_GU((k_gateup_multi<false, true>)) }
+  COLI_LAUNCH_GU((k_gateup_multi<false, false>))
 #undef COLI_LAUNCH_GU
 }
 

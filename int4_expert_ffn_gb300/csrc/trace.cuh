@@ -32,6 +32,7 @@ enum TracePoint : int {
   kTpDnEntry, kTpDnDepWait, kTpDnLists, kTpDnPlanes, kTpDnCompute, kTpDnCombine,
   kTpDnPartials, kTpRouteStart, kTpEnd,
   kTpRtLogits, kTpRtTopk, kTpRtPublish, kTpRtUnion, kTpDnPlaneStart, kTpDnPlaneBuilt,
+  kTpGuSplit, kTpGuNeed,
 };
 
 }  // namespace coli
