@@ -252,33 +252,78 @@ __device__ __forceinline__ void fx_add(const Dec2Args &a, int o, float p) {
 // Router partial logits: CTA c of G sums its rows [h0, h1) of every expert's
 // router row against x:  partials[c][t][e] = sum_{h in [h0,h1)} Wr[e][h] x[t][h].
 
+// Four consecutive router weights as floats (the row slice start and every
+// offset used here are multiples of four elements).
+__device__ __forceinline__ void load4w(const float *p, float (&v)[4]) {
+  const float4 q = __ldg((const float4 *)p);
+  v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+}
+__device__ __forceinline__ void load4w(const __nv_bfloat16 *p, float (&v)[4]) {
+  const uint2 q = __ldg((const uint2 *)p);
+  v[0] = __uint_as_float(q.x << 16); v[1] = __uint_as_float(q.x & 0xFFFF0000u);
+  v[2] = __uint_as_float(q.y << 16); v[3] = __uint_as_float(q.y & 0xFFFF0000u);
+}
+
 template <typename XT, typename WT>
 __global__ void __launch_bounds__(kDec2MaxThreads) k_route(Dec2Args a) {
+  extern __shared__ __align__(128) uint8_t smem_route[];
   grid_dependents_launch();
   grid_dependency_wait();
-  const int c = blockIdx.x, G = gridDim.x;
-  const int U = a.H / 4;
-  const int h0 = 4 * part_lo(c, U, G), h1 = 4 * part_lo(c + 1, U, G);
+  const int c = blockIdx.x, G = gridDim.x, T = a.T, E = a.E, H = a.H;
+  const int U = H / 4;
+  const int h0 = 4 * part_lo(c, U, G), h1 = 4 * part_lo(c + 1, U, G), nr = h1 - h0;
   const XT *x = (const XT *)a.x;
   const WT *wr = (const WT *)a.wr;
-  for (int o = threadIdx.x; o < a.T * a.E; o += blockDim.x) {
-    const int t = o / a.E, e = o - t * a.E;
-    float s = 0.0f;
-    for (int h = h0; h < h1; ++h)
-      s = fmaf(to_f32(wr[(size_t)e * a.H + h]), to_f32(x[(size_t)t * a.H + h]), s);
-    if (a.fx) fx_add(a, o, s);
-    else a.partials[(size_t)c * a.T * a.E + o] = s;
+  // this CTA's columns of the layer input, widened to f32: into shared memory
+  // and into every replica (read by all gate/up CTAs)
+  float *s_x = (float *)smem_route;   // [T][nr]
+  for (int i = threadIdx.x; i < T * nr; i += blockDim.x) {
+    const int t = i / nr, h = h0 + (i - t * nr);
+    const float v = to_f32(x[(size_t)t * H + h]);
+    s_x[i] = v;
+    if (a.xrep)
+      for (int r = 0; r < a.n_rep; ++r) a.xrep[r * a.x_stride + (size_t)t * H + h] = v;
   }
-  // the layer input, widened to f32, in every replica (read by all gate/up CTAs)
-  if (a.xrep) {
-    const int nr = h1 - h0;
-    for (int i = threadIdx.x; i < a.T * nr; i += blockDim.x) {
-      const int t = i / nr, h = h0 + (i - t * nr);
-      const float v = to_f32(x[(size_t)t * a.H + h]);
-      for (int r = 0; r < a.n_rep; ++r) a.xrep[r * a.x_stride + (size_t)t * a.H + h] = v;
+  __syncthreads();
+  // one thread per expert: its row slice in 16-element pieces (four vector
+  // loads in flight), against up to four tokens at a time
+  constexpr int kTok = 4;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const WT *w = wr + (size_t)e * H + h0;
+    for (int t0 = 0; t0 < T; t0 += kTok) {
+      float acc[kTok] = {0.0f, 0.0f, 0.0f, 0.0f};
+      for (int r0 = 0; r0 < nr; r0 += 16) {
+        float wv[4][4];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          if (r0 + 4 * v < nr) {
+            load4w(w + r0 + 4 * v, wv[v]);
+          } else {
+            wv[v][0] = wv[v][1] = wv[v][2] = wv[v][3] = 0.0f;
+          }
+        }
+#pragma unroll
+        for (int tt = 0; tt < kTok; ++tt) {
+          if (t0 + tt < T) {
+            const float *xs = s_x + (t0 + tt) * nr + r0;
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              if (r0 + 4 * v < nr)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[tt] = fmaf(wv[v][j], xs[4 * v + j], acc[tt]);
+          }
+        }
+      }
+#pragma unroll
+      for (int tt = 0; tt < kTok; ++tt) {
+        if (t0 + tt >= T) break;
+        const int o = (t0 + tt) * E + e;
+        if (a.fx) fx_add(a, o, acc[tt]);
+        else a.partials[(size_t)c * T * E + o] = acc[tt];
+      }
     }
   }
-  extern __shared__ __align__(128) uint8_t smem_route[];
+  __syncthreads();   // s_x is dead; the routing below may reuse the memory
   if (!a.route_gu) route_if_last(a, layer_ptrs(a), smem_route);
 }
 
@@ -1705,8 +1750,10 @@ cudaError_t launch_route_partials(const Dec2Args &a_in, int x_bf16, int w_bf16, 
                                   bool pdl) {
   Dec2Args a = a_in;
   bool stage = false;
-  const size_t smem = route_smem_bytes(a, &stage);
+  size_t smem = route_smem_bytes(a, &stage);
   a.stage_partials = stage;
+  const size_t x_bytes = (size_t)a.T * 4 * ((a.H / 4 + a.n_part - 1) / a.n_part) * 4;
+  if (smem < x_bytes) smem = x_bytes;
   const int threads = kDec2MaxThreads;
   cudaError_t e;
 #define COLI_LAUNCH_ROUTE(XT, WT)                                             \
