@@ -273,6 +273,7 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
   const size_t sc_stride = (size_t)(E + S) * coli_expert_scale_count(H, F);
   const size_t T_H = (size_t)d->n_tokens * H;
   Dec2Args a = make_args(d, k, tn, (uint8_t *)workspace, L);
+  a.chain = n_layers > 1;
   if (plan_decode(a, L.n_part) != cudaSuccess) return COLI_EUNSUPPORTED;
   const int wr_bf16 = d->router_dtype == COLI_BF16;
   cudaError_t e = cudaSuccess;

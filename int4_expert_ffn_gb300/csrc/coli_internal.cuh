@@ -129,6 +129,7 @@ struct Dec2Args {
   int dn_slots_pipe;        // depth of each warp's cp.async pipeline
   int dn_slot_bytes;
   int wr_bf16;              // the router (and its rows in k_down's shared memory) is bf16
+  int chain;                // a next layer follows (k_down forms its router partials)
   int dn_slots;             // token slots whose planes fit in shared memory at once
   int dn_batch;             // experts whose partial sums fit in shared memory at once
   int dm_nw;                // warps of k_down_multi

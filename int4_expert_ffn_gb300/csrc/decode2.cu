@@ -6,18 +6,20 @@
 // expert's three matrices adjacent; batch union reads each used expert once),
 // §十一 (route -> union -> compute), "colibrì 路由遥测全解析" (route counts, gates).
 //
-// Per layer two kernels, chained with programmatic dependent launch:
-//   k_gateup: every CTA reduces the router partial logits (fixed order), runs
-//     the top-k and builds the union lists itself; CTA 0 publishes them and
-//     the route counts.  The CTA then streams its share of the used experts'
-//     gate/up rows through a bulk-copy (TMA) ring in shared memory, forms
-//     h = silu(g) * u * gate, and prefetches into L2 the down rows that the
-//     same-index CTA of k_down will read.
-//   k_down: each CTA owns a block of output rows; it streams those rows of
-//     every used expert's down matrix, sums the experts in ascending id order,
-//     adds the residual, and forms the next layer's router partial logits
-//     from its rows (the router GEMV split by rows).
-// k_route forms the partial logits of the first layer.
+// Per layer, kernels chained with programmatic dependent launch inside one
+// CUDA graph per step:
+//   k_route (first layer of a pass): the router partial logits of each CTA's
+//     slice of the hidden dimension, added as fixed-point integers.
+//   k_gateup (one token) / k_gateup_multi (several): every CTA routes the
+//     layer itself from the fixed-point logits (top-k, union lists; CTA 0
+//     publishes them and the route counts), then streams its share of the
+//     used experts' gate/up rows through per-warp cp.async rings in shared
+//     memory and writes h = silu(g) * u * gate.
+//   k_down (one token): each CTA owns a block of output rows of every used
+//     expert's down matrix, sums the experts in a fixed order, adds the
+//     residual, and adds its rows' share of the next layer's router logits.
+//   k_down_multi + k_down (several tokens): the down GEMVs split by expert
+//     and cost into per-slot outputs, then k_down adds each token's slots.
 //
 // Arithmetic: each lane owns 32 consecutive columns.  Its 32 activations are
 // quantised to 15-bit fixed point (scale = max|x| / 16319), split into signed
@@ -706,28 +708,6 @@ __device__ __forceinline__ void clear_fx(const Dec2Args &a) {
 }
 
 
-constexpr int64_t kPrefetchMaxBytes = int64_t(96) << 20;
-
-// L2 prefetch of the down rows [dh0, dh1) of every used expert (the rows that
-// CTA c owns in the down kernel), one bulk prefetch per expert and lane.
-__device__ __forceinline__ void prefetch_down_rows(const Dec2Args &a, const LayerPtrs &lp,
-                                                   const int *s_act_expert, int n_active, int c) {
-  if (c >= a.n_part) return;
-  if ((int64_t)n_active * ((int64_t)a.H * a.F / 2 + (int64_t)a.H * a.F / 16) > kPrefetchMaxBytes)
-    return;   // would not stay in L2 until the down kernel reads it
-  const int H = a.H, F = a.F, lane = threadIdx.x & 31;
-  const int64_t ngr = H / kGroup;
-  const int UH = H / 4;
-  const int dh0 = 4 * part_lo(c, UH, a.n_part), dh1 = 4 * part_lo(c + 1, UH, a.n_part);
-  for (int q = lane; q < n_active && dh1 > dh0; q += 32) {
-    const int e = s_act_expert[q];
-    prefetch_l2(lp.packed + (int64_t)e * a.eb + (int64_t)F * H + (int64_t)dh0 * (F / 2),
-                (uint32_t)((dh1 - dh0) * (F / 2)));
-    prefetch_l2(lp.scales + (int64_t)e * a.es + (int64_t)2 * F * ngr + (int64_t)dh0 * (F / kGroup),
-                (uint32_t)((dh1 - dh0) * (F / 16)));
-  }
-}
-
 // One token per call: every used expert serves token 0, each warp quantises
 // the 1024-column slice of x that its chunk needs once (kept in registers),
 // and there is no token loop.
@@ -789,12 +769,6 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
         ci.next(dg, dcg, ncg, F);
       }
       if (++ld == S) ld = 0;
-      if (i == (my_tasks > S - 1 ? my_tasks - (S - 1) : 0) && warp == 0 &&
-          rb0 + a.gu_rows >= nrows) {
-        // every gate/up copy of this warp is issued: L2 prefetch of the down rows
-        // that this CTA index reads in the down kernel, behind this kernel's own stream
-        prefetch_down_rows(a, lp, s_act_expert, n_active, c);
-      }
       cp_async_commit();
       cp_async_wait_dyn(S - 1);      // this lane's copies of task i have landed
       if (vec_scales) __syncwarp();  // scales were copied by other lanes
@@ -1008,8 +982,6 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup_multi(Dec2Args a) {
       ci.next(NW, ncg, gpe);
     }
     if (++ld == S) ld = 0;
-    if (i == (my_tasks > S - 1 ? my_tasks - (S - 1) : 0) && warp == 0)
-      prefetch_down_rows(a, lp, s_act_expert, n_active, c);
     cp_async_commit();
     cp_async_wait_dyn(S - 1);
     if (vec_scales) __syncwarp();
@@ -1659,7 +1631,7 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
   d.routes = o; o = al16(o + (size_t)T * KS * 4);
   d.acc = o; o = al16(o + (size_t)max_nr * T * 4);
   d.xn = o; o = al16(o + (size_t)T * max_nr * 4);
-  d.wr = o; o = al16(o + (size_t)E * max_nr * (a.wr_bf16 ? 2 : 4));
+  d.wr = o; o = al16(o + (a.chain ? (size_t)E * max_nr * (a.wr_bf16 ? 2 : 4) : 0));
   // one token: every used expert's partial sums [expert][row][chunk] at once
   const int n_exp = (E < k ? E : k) + S;
   const size_t red_bytes = (size_t)n_exp * max_nr * a.dn_ncg * 4;
@@ -1698,7 +1670,7 @@ static cudaError_t plan_down_multi(Dec2Args &a) {
   d.routes = o; o = al16(o + (size_t)T * KS * 4);
   d.acc = o; o = al16(o + (size_t)max_nr * T * 4);
   d.xn = o; o = al16(o + (size_t)T * max_nr * 4);
-  d.wr = o; o = al16(o + (size_t)E * max_nr * (a.wr_bf16 ? 2 : 4));
+  d.wr = o; o = al16(o + (a.chain ? (size_t)E * max_nr * (a.wr_bf16 ? 2 : 4) : 0));
   d.ring = d.red = d.planes = o;
   d.total = o;
   a.dn = d;
