@@ -11,6 +11,10 @@ Parity status of each function (what pins it, see ``tests/test_oracle_pins.py``)
   ``matvec_i4g``       pinned: on-grid weights round-trip exactly; numpy matmul.
 * ``router_logits`` /
   ``topk``             pinned: brute-force sort, closed-form gates, NaN rule.
+* ``topk_sigmoid``     pinned: a hand example with exact sigmoid scores (1/2, 3/4,
+                       1/4, 9/10) and closed-form gates, the bias-only-selects
+                       rule, invariance to a common bias shift, zero bias picks
+                       as softmax, NaN rule.
 * ``expert``           pinned: torch float64 SwiGLU on on-grid weights.
 * ``moe_forward``      pinned: dense masked MoE, k=1, k=E equal-logit mean,
                        route-count histogram.

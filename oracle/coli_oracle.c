@@ -23,6 +23,10 @@
  *   - a NaN weight is ignored by the max and stored as q = 0;
  *   - odd column count: the high nibble of the last byte is 0;
  *   - routing = softmax over E, top-k (ties to the lower id), renormalise;
+ *   - the GLM router ("per-layer n_group=1 sigmoid + noaux_tc", [P1] §十一):
+ *     scores s = 1 / (1 + e^-l); experts ranked by s + b with b a per-expert
+ *     bias used only for the choice (one group: plain top-k over all
+ *     experts); gates = the picked s over their sum, no further scale;
  *   - NaN logits rank below every number; if all are NaN the slots take
  *     experts 0..k-1 with gates 1/k ([P4] §测试与 CI, rt_router_pick);
  *   - activation SwiGLU, silu(z) = z / (1 + e^-z); the shared expert is added
@@ -182,6 +186,52 @@ int orc_topk(const double *logits, int64_t E, int k, int32_t *idx, double *gates
     return any_nan;
 }
 
+/* Top-k of the GLM router for one token ([P1] §十一: "per-layer n_group=1
+ * sigmoid + noaux_tc"): s_e = 1 / (1 + exp(-l_e)); the k experts with the
+ * largest s_e + bias_e (bias may be NULL = 0) in the orc_topk order, the keys
+ * ranked in f32 like the logits above; gates[j] = s_{idx[j]} / sum_j' s_{idx[j']}.
+ * NaN rules as orc_topk: a NaN key ranks last, a picked NaN score gets gate 0,
+ * an all-NaN token takes experts 0..k-1 with gates 1/k.  Returns 1 if any
+ * logit of the token is NaN. */
+int orc_topk_sigmoid(const double *logits, const double *bias, int64_t E, int k,
+                     int32_t *idx, double *gates)
+{
+    int64_t *ord = (int64_t *)malloc((size_t)E * sizeof(int64_t));
+    float *key = (float *)malloc((size_t)E * sizeof(float));
+    double *sc = (double *)malloc((size_t)E * sizeof(double));
+    int any_nan = 0;
+    for (int64_t e = 0; e < E; ++e) {
+        ord[e] = e;
+        sc[e] = 1.0 / (1.0 + exp(-logits[e]));
+        key[e] = (float)(sc[e] + (bias ? bias[e] : 0.0));
+        if (logits[e] != logits[e]) any_nan = 1;
+    }
+    for (int64_t i = 1; i < E; ++i) {
+        int64_t v = ord[i], j = i - 1;
+        while (j >= 0 && orc_ranks_before(key[v], v, key[ord[j]], ord[j])) {
+            ord[j + 1] = ord[j];
+            --j;
+        }
+        ord[j + 1] = v;
+    }
+    for (int j = 0; j < k; ++j) idx[j] = (int32_t)ord[j];
+    if (sc[ord[0]] != sc[ord[0]]) {    /* every logit NaN */
+        for (int j = 0; j < k; ++j) gates[j] = 1.0 / (double)k;
+    } else {
+        double den = 0.0;
+        for (int j = 0; j < k; ++j) {
+            const double s = sc[ord[j]];
+            gates[j] = (s != s) ? 0.0 : s;
+            den += gates[j];
+        }
+        for (int j = 0; j < k; ++j) gates[j] /= den;
+    }
+    free(ord);
+    free(key);
+    free(sc);
+    return any_nan;
+}
+
 /* ---------------------------------------------------------------------- */
 /* Expert record: gate[F][H] | up[F][H] | down[H][F], each matrix in the
  * packed format, stored adjacently ([P1] §四: the three matrices of an expert
@@ -228,10 +278,27 @@ void orc_expert(const uint8_t *pe, const float *se, int64_t H, int64_t F,
  *   idx     [T][k], gates [T][k]
  *   counts  [E]                 += 1 per (token, slot); may be NULL
  * Returns the number of tokens that saw a NaN logit. */
+int orc_moe_forward_router(const double *x, int64_t T, int64_t H, int64_t F, int64_t E,
+                           int64_t n_shared, const double *wr, int router_fn,
+                           const double *bias, const uint8_t *packed, const float *scales,
+                           int k, double *out, int32_t *idx, double *gates, uint32_t *counts);
+
 int orc_moe_forward(const double *x, int64_t T, int64_t H, int64_t F, int64_t E,
                     int64_t n_shared, const double *wr, const uint8_t *packed,
                     const float *scales, int k, double *out, int32_t *idx,
                     double *gates, uint32_t *counts)
+{
+    return orc_moe_forward_router(x, T, H, F, E, n_shared, wr, 0, NULL, packed, scales, k,
+                                  out, idx, gates, counts);
+}
+
+/* The same layer with the routing function chosen: router_fn 0 = softmax
+ * (orc_topk), 1 = sigmoid scores with a selection bias (orc_topk_sigmoid,
+ * bias [E] or NULL). */
+int orc_moe_forward_router(const double *x, int64_t T, int64_t H, int64_t F, int64_t E,
+                           int64_t n_shared, const double *wr, int router_fn,
+                           const double *bias, const uint8_t *packed, const float *scales,
+                           int k, double *out, int32_t *idx, double *gates, uint32_t *counts)
 {
     const int64_t eb = orc_expert_packed_bytes(H, F);
     const int64_t es = orc_expert_scales(H, F);
@@ -240,7 +307,9 @@ int orc_moe_forward(const double *x, int64_t T, int64_t H, int64_t F, int64_t E,
     int nan_tokens = 0;
     orc_router_logits(x, wr, T, H, E, logits);
     for (int64_t t = 0; t < T; ++t) {
-        nan_tokens += orc_topk(logits + t * E, E, k, idx + t * k, gates + t * k);
+        nan_tokens += router_fn == 1
+            ? orc_topk_sigmoid(logits + t * E, bias, E, k, idx + t * k, gates + t * k)
+            : orc_topk(logits + t * E, E, k, idx + t * k, gates + t * k);
         if (counts)
             for (int j = 0; j < k; ++j) counts[idx[t * k + j]] += 1u;
         double *o = out + t * H;

@@ -12,7 +12,7 @@ from .build import build_oracle
 __all__ = [
     "GROUP", "packed_row_bytes", "scales_per_row", "expert_packed_bytes",
     "expert_scales", "quant_i4g", "dequant_i4g", "matvec_i4g", "router_logits",
-    "topk", "expert", "moe_forward", "moe_stack_forward", "lib",
+    "topk", "topk_sigmoid", "expert", "moe_forward", "moe_stack_forward", "lib",
 ]
 
 GROUP = 64
@@ -48,6 +48,11 @@ def lib():
         L.orc_moe_forward.argtypes = [f64p, i64, i64, i64, i64, i64, f64p, u8p, f32p,
                                       C.c_int, f64p, i32p, f64p, u32p]
         L.orc_moe_forward.restype = C.c_int
+        L.orc_topk_sigmoid.argtypes = [f64p, f64p, i64, C.c_int, i32p, f64p]
+        L.orc_topk_sigmoid.restype = C.c_int
+        L.orc_moe_forward_router.argtypes = [f64p, i64, i64, i64, i64, i64, f64p, C.c_int, f64p,
+                                             u8p, f32p, C.c_int, f64p, i32p, f64p, u32p]
+        L.orc_moe_forward_router.restype = C.c_int
         _lib = L
     return _lib
 
@@ -126,6 +131,19 @@ def topk(logits, k):
     return idx, gates, bool(nan)
 
 
+def topk_sigmoid(logits, k, bias=None):
+    """GLM router for one token: logits [E], bias [E] or None ->
+    (idx int32 [k], gates float64 [k], any_nan)."""
+    logits = _c(logits, np.float64)
+    idx = np.zeros(k, np.int32)
+    gates = np.zeros(k, np.float64)
+    b64 = None if bias is None else _c(bias, np.float64)   # kept alive for the call
+    bp = None if b64 is None else _p(b64, C.c_double)
+    nan = lib().orc_topk_sigmoid(_p(logits, C.c_double), bp, logits.shape[0], k,
+                                 _p(idx, C.c_int32), _p(gates, C.c_double))
+    return idx, gates, bool(nan)
+
+
 def expert(packed_e, scales_e, H, F, x):
     packed_e, scales_e, x = _c(packed_e, np.uint8), _c(scales_e, np.float32), _c(x, np.float64)
     y = np.zeros(H, np.float64)
@@ -134,12 +152,14 @@ def expert(packed_e, scales_e, H, F, x):
     return y
 
 
-def moe_forward(x, wr, packed, scales, H, F, E, n_shared, k, counts=None):
+def moe_forward(x, wr, packed, scales, H, F, E, n_shared, k, counts=None, router="softmax",
+                bias=None):
     """One routed-MoE layer.
 
     x [T, H]; wr [E, H]; packed / scales: flat arrays holding experts 0..E+S-1
     in the library layout.  Returns (out [T,H] f64, idx [T,k] i32, gates [T,k]
     f64, nan_tokens).  ``counts`` (uint32 [E]) is accumulated in place.
+    ``router``: "softmax" or "sigmoid" (scores with the selection ``bias`` [E]).
     """
     x, wr = _c(x, np.float64), _c(wr, np.float64)
     packed, scales = _c(packed.reshape(-1), np.uint8), _c(scales.reshape(-1), np.float32)
@@ -151,24 +171,31 @@ def moe_forward(x, wr, packed, scales, H, F, E, n_shared, k, counts=None):
     if counts is not None:
         assert counts.dtype == np.uint32 and counts.flags.c_contiguous
         cp = _p(counts, C.c_uint32)
-    nan = lib().orc_moe_forward(_p(x, C.c_double), T, H, F, E, n_shared,
-                                _p(wr, C.c_double), _p(packed, C.c_uint8),
-                                _p(scales, C.c_float), k, _p(out, C.c_double),
-                                _p(idx, C.c_int32), _p(gates, C.c_double), cp)
+    fn = {"softmax": 0, "sigmoid": 1}[router]
+    b64 = None if bias is None else _c(bias, np.float64)   # kept alive for the call
+    bp = None if b64 is None else _p(b64, C.c_double)
+    nan = lib().orc_moe_forward_router(_p(x, C.c_double), T, H, F, E, n_shared,
+                                       _p(wr, C.c_double), fn, bp, _p(packed, C.c_uint8),
+                                       _p(scales, C.c_float), k, _p(out, C.c_double),
+                                       _p(idx, C.c_int32), _p(gates, C.c_double), cp)
     return out, idx, gates, int(nan)
 
 
-def moe_stack_forward(x0, layers, H, F, E, n_shared, k, counts=None):
+def moe_stack_forward(x0, layers, H, F, E, n_shared, k, counts=None, router="softmax",
+                      biases=None):
     """Decode stack: x_{l+1} = x_l + MoE_l(x_l) (residual chain, no attention or norm).
 
-    ``layers`` is a list of (wr, packed, scales) per layer.  Returns
-    (x_L, per-layer outputs, per-layer idx).  ``counts`` is uint32 [L, E].
+    ``layers`` is a list of (wr, packed, scales) per layer; ``biases`` the
+    per-layer selection bias of the sigmoid router.  Returns (x_L, per-layer
+    outputs, per-layer idx).  ``counts`` is uint32 [L, E].
     """
     x = np.asarray(x0, np.float64)
     outs, idxs = [], []
     for l, (wr, packed, scales) in enumerate(layers):
         c = None if counts is None else counts[l]
-        out, idx, _, _ = moe_forward(x, wr, packed, scales, H, F, E, n_shared, k, c)
+        b = None if biases is None else biases[l]
+        out, idx, _, _ = moe_forward(x, wr, packed, scales, H, F, E, n_shared, k, c,
+                                     router=router, bias=b)
         outs.append(out)
         idxs.append(idx)
         x = x + out

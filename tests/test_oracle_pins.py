@@ -276,3 +276,85 @@ def test_stack_residual_chain():
     o1, _, _, _ = orc.moe_forward(x0 + o0, *layers[1], H, F, E, 1, k)
     np.testing.assert_array_equal(xL, x0 + o0 + o1)
     assert counts.sum() == 2 * k
+
+
+# ---------------------------------------------------------------------------
+# the GLM router: sigmoid scores, selection-only bias, normalised gates
+
+def test_topk_sigmoid_hand_example():
+    # logits 0, ln 3, -ln 3, ln 9 have sigmoid scores 1/2, 3/4, 1/4, 9/10 exactly
+    lg = np.array([0.0, np.log(3.0), -np.log(3.0), np.log(9.0)])
+    # no bias: the two largest scores, 9/10 and 3/4; gates 0.9/1.65 = 6/11, 5/11
+    idx, gates, nan = orc.topk_sigmoid(lg, 2)
+    assert not nan and idx.tolist() == [3, 1]
+    np.testing.assert_allclose(gates, [6 / 11, 5 / 11], rtol=1e-14)
+    # a bias of 0.8 on expert 2 lifts its key to 1.05 (first) and pushes expert
+    # 1 out; the gates still use the scores alone: 1/4 and 9/10 over 23/20
+    idx, gates, nan = orc.topk_sigmoid(lg, 2, np.array([0.0, 0.0, 0.8, 0.0]))
+    assert idx.tolist() == [2, 3]
+    np.testing.assert_allclose(gates, [5 / 23, 18 / 23], rtol=1e-14)
+
+
+def test_topk_sigmoid_zero_bias_picks_like_softmax():
+    # the sigmoid is increasing: without bias the picks equal the softmax ones
+    rng = np.random.default_rng(21)
+    for E, k in ((8, 2), (64, 8), (256, 8)):
+        for _ in range(5):
+            lg = rng.standard_normal(E) * 2
+            i_soft, _, _ = orc.topk(lg, k)
+            i_sig, g_sig, _ = orc.topk_sigmoid(lg, k)
+            assert i_sig.tolist() == i_soft.tolist()
+            assert abs(g_sig.sum() - 1) < 1e-12 and np.all(g_sig > 0)
+
+
+def test_topk_sigmoid_common_bias_shift_changes_nothing():
+    rng = np.random.default_rng(22)
+    lg = rng.standard_normal(32)
+    b = rng.standard_normal(32) * 0.1
+    i0, g0, _ = orc.topk_sigmoid(lg, 4, b)
+    i1, g1, _ = orc.topk_sigmoid(lg, 4, b + 0.25)
+    assert i0.tolist() == i1.tolist()
+    np.testing.assert_allclose(g0, g1, rtol=1e-14)
+
+
+def test_topk_sigmoid_brute_force():
+    rng = np.random.default_rng(23)
+    for E, k in ((8, 3), (48, 6)):
+        for _ in range(10):
+            lg = rng.standard_normal(E) * 2
+            b = rng.standard_normal(E) * 0.2
+            s = 1 / (1 + np.exp(-lg))
+            order = sorted(range(E), key=lambda e: (-np.float32(s[e] + b[e]), e))[:k]
+            idx, gates, _ = orc.topk_sigmoid(lg, k, b)
+            assert idx.tolist() == order
+            np.testing.assert_allclose(gates, s[order] / s[order].sum(), rtol=1e-12)
+
+
+def test_topk_sigmoid_nan_rules():
+    idx, gates, nan = orc.topk_sigmoid(np.full(5, np.nan), 2, np.zeros(5))
+    assert nan and idx.tolist() == [0, 1]
+    np.testing.assert_allclose(gates, 0.5)
+    lg = np.array([np.nan, 0.0, 1.0])
+    idx, gates, nan = orc.topk_sigmoid(lg, 3)
+    assert nan and idx.tolist() == [2, 1, 0] and gates[2] == 0
+    np.testing.assert_allclose(gates[:2].sum(), 1.0)
+
+
+def test_moe_sigmoid_router_dense_masked():
+    H, F, E, S, k, T = 64, 64, 6, 1, 2, 4
+    packed, scales, mats = _layer(H, F, E, S, seed=77)
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((T, H))
+    wr = rng.standard_normal((E, H)) / 8
+    b = rng.standard_normal(E) * 0.3
+    out, idx, gates, nan = orc.moe_forward(x, wr, packed, scales, H, F, E, S, k,
+                                           router="sigmoid", bias=b)
+    assert nan == 0
+    logits = x @ wr.T
+    for t in range(T):
+        s = 1 / (1 + np.exp(-logits[t]))
+        order = sorted(range(E), key=lambda e: (-np.float32(s[e] + b[e]), e))[:k]
+        assert idx[t].tolist() == order
+        ref = sum(s[e] / s[order].sum() * _torch_expert(mats[e], x[t]) for e in order)
+        ref = ref + _torch_expert(mats[E], x[t])
+        np.testing.assert_allclose(out[t], ref, rtol=1e-10, atol=1e-10)
