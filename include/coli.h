@@ -56,6 +56,22 @@ typedef enum { COLI_F32 = 0, COLI_BF16 = 1 } coli_dtype;
 #define COLI_FLAG_NAN_LOGITS 0x1u   /* a token had a NaN router logit */
 #define COLI_FLAG_TIMEOUT    0x2u   /* a bounded wait gave up */
 
+/*
+ * Routing function ([P1] §十一 "route"; GLM layers: "per-layer n_group=1
+ * sigmoid + noaux_tc").
+ *   COLI_ROUTER_SOFTMAX       rank the logits; gates = softmax over all E
+ *                             renormalised over the k picked.
+ *   COLI_ROUTER_SIGMOID_BIAS  scores s_e = 1 / (1 + e^-l_e); rank s_e + b_e,
+ *                             b = router_bias, a per-expert bias that only
+ *                             selects (noaux_tc with one group: plain top-k
+ *                             over all experts); gates = the picked s
+ *                             normalised to sum 1 (no further scaling).
+ * Both: equal keys -> lower expert id; NaN ranks below every number; a
+ * picked NaN gets gate 0; an all-NaN token takes experts 0..k-1 with gates
+ * 1/k and sets COLI_FLAG_NAN_LOGITS.
+ */
+typedef enum { COLI_ROUTER_SOFTMAX = 0, COLI_ROUTER_SIGMOID_BIAS = 1 } coli_router_fn;
+
 /* Shape of one MoE layer call. */
 typedef struct {
     int32_t hidden;        /* H: multiple of 64, 64 .. 16384 */
@@ -65,6 +81,10 @@ typedef struct {
     int32_t n_tokens;      /* T tokens in this call, >= 0 (0 is a no-op) */
     coli_dtype x_dtype;    /* activations x: COLI_F32 or COLI_BF16 */
     coli_dtype router_dtype; /* router weights: COLI_F32 or COLI_BF16 */
+    int32_t router_fn;     /* coli_router_fn; 0 (softmax) when zero-initialised */
+    const float *router_bias; /* COLI_ROUTER_SIGMOID_BIAS: device f32 [E] per layer
+                                 ([n_layers][E] for the stack), 4-byte aligned,
+                                 read-only; NULL = zero bias.  Ignored otherwise. */
 } coli_moe_desc;
 
 const char *coli_status_str(int status);
@@ -119,6 +139,9 @@ size_t coli_moe_workspace_size(const coli_moe_desc *d, int top_k);
  *                   token is NaN, idx = 0..k-1 and gates = 1/k
  *                   ([P4] §测试与 CI, the rt_router_pick fallback), and
  *                   COLI_FLAG_NAN_LOGITS is set in the workspace
+ *                   (with d->router_fn = COLI_ROUTER_SIGMOID_BIAS: ranked by
+ *                   sigmoid(l) + router_bias, gates the picked sigmoid(l)
+ *                   normalised, as described at coli_router_fn)
  *   route_counts[e] += number of (t, j) with idx[t][j] == e  (may be NULL;
  *                   never zeroed by the library: counts accumulate)
  *   x [T][H] (d->x_dtype), router_w [E][H] (d->router_dtype),
@@ -176,7 +199,7 @@ int coli_moe_forward_noalloc(const coli_moe_desc *d, int top_k, const void *x,
  *   x_0 = x;  x_{l+1} = x_l + MoE_l(x_l);  x_out = x_{n_layers}
  * Layer l uses router_w + l*E*H elements, packed_experts + l*(E+S)*
  * coli_expert_packed_bytes(H,F), scales + l*(E+S)*coli_expert_scale_count(H,F),
- * route_counts + l*E.  x is d->x_dtype; x_out f32 [T][H]; layer_out (may be
+ * route_counts + l*E, and (sigmoid router) router_bias + l*E.  x is d->x_dtype; x_out f32 [T][H]; layer_out (may be
  * NULL) receives MoE_l(x_l) as f32 [n_layers][T][H].  Same workspace size as
  * coli_moe_forward.
  */

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libcoli.so")
 COLI_OK, COLI_EINVAL, COLI_EALIGN, COLI_ECUDA, COLI_ETIMEOUT, COLI_ENOMEM, COLI_EUNSUPPORTED = (
     0, -1, -2, -3, -4, -5, -6)
 COLI_F32, COLI_BF16 = 0, 1
+COLI_ROUTER_SOFTMAX, COLI_ROUTER_SIGMOID_BIAS = 0, 1
 COLI_FLAG_NAN_LOGITS, COLI_FLAG_TIMEOUT = 0x1, 0x2
 COLI_KERNEL_ROUTE, COLI_KERNEL_GATEUP, COLI_KERNEL_DOWN = 0, 1, 2
 COLI_KERNEL_PREFILL_GATEUP, COLI_KERNEL_PREFILL_DOWN = 3, 4
@@ -45,7 +46,8 @@ class ColiError(RuntimeError):
 class coli_moe_desc(C.Structure):
     _fields_ = [("hidden", C.c_int32), ("ffn", C.c_int32), ("n_experts", C.c_int32),
                 ("n_shared", C.c_int32), ("n_tokens", C.c_int32), ("x_dtype", C.c_int),
-                ("router_dtype", C.c_int)]
+                ("router_dtype", C.c_int), ("router_fn", C.c_int32),
+                ("router_bias", C.c_void_p)]
 
 
 def _load():
@@ -137,10 +139,17 @@ class MoEDesc:
     n_tokens: int
     x_dtype: int = COLI_F32
     router_dtype: int = COLI_BF16
+    router_fn: int = COLI_ROUTER_SOFTMAX
+    router_bias: object = None    # f32 CUDA tensor [E] (or [n_layers, E]), or None
 
     def c(self):
+        b = self.router_bias
+        if b is not None:
+            if not (b.is_cuda and b.is_contiguous() and b.dtype == torch.float32):
+                raise ValueError("router_bias must be a contiguous float32 CUDA tensor")
         return coli_moe_desc(self.hidden, self.ffn, self.n_experts, self.n_shared,
-                             self.n_tokens, self.x_dtype, self.router_dtype)
+                             self.n_tokens, self.x_dtype, self.router_dtype, self.router_fn,
+                             None if b is None else b.data_ptr())
 
 
 def coli_packed_row_bytes(cols):

@@ -80,6 +80,10 @@ int check_desc(const coli_moe_desc *d, int top_k) {
   if ((d->x_dtype != COLI_F32 && d->x_dtype != COLI_BF16) ||
       (d->router_dtype != COLI_F32 && d->router_dtype != COLI_BF16))
     return COLI_EINVAL;
+  if (d->router_fn != COLI_ROUTER_SOFTMAX && d->router_fn != COLI_ROUTER_SIGMOID_BIAS)
+    return COLI_EINVAL;
+  if (d->router_fn == COLI_ROUTER_SIGMOID_BIAS && ((uintptr_t)d->router_bias & 3u))
+    return COLI_EALIGN;
   return COLI_OK;
 }
 
@@ -165,6 +169,8 @@ Dec2Args make_args(const coli_moe_desc *d, int k, int tn, uint8_t *ws, const WsL
   a.y = (float *)(ws + L.y);
   a.ctrl = (uint32_t *)(ws + L.ctrl);
   a.wr_bf16 = d->router_dtype == COLI_BF16;
+  a.router_fn = d->router_fn;
+  a.router_bias = d->router_fn == COLI_ROUTER_SIGMOID_BIAS ? d->router_bias : nullptr;
   a.fx = tn * a.E <= kFxMaxTE;
   a.fx_acc = (long long *)(ws + L.fx);
   a.fx_flag = (uint32_t *)(ws + L.fx + (size_t)tn * a.E * 8);
@@ -280,6 +286,7 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
   a.build_union = 1;
   // with fixed-point logits every gate/up CTA routes its own layer
   a.route_gu = a.fx && a.gu_route_fits;
+  const float *bias0 = d->router_fn == COLI_ROUTER_SIGMOID_BIAS ? d->router_bias : nullptr;
   uint8_t *ws = (uint8_t *)workspace;
   for (int l = 0; l < n_layers && e == cudaSuccess; ++l) {
     const void *xin = (l == 0) ? x : (const void *)out;
@@ -302,6 +309,9 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
       a.fx_clr_flag = rd_flag;
       fx_buffer(a, ws, L, l == 0 ? 0 : (l + 1) & 1, &a.fx_acc, &a.fx_flag);
     }
+    // the bias of the layer each launch routes: layer l for k_route (l = 0)
+    // and k_gateup, layer l + 1 for the last CTA of k_down (without fixed point)
+    a.router_bias = bias0 ? bias0 + (size_t)l * E : nullptr;
     if (l == 0) {
       // router partials of layer 0
       a.wr = router_w;
@@ -319,6 +329,7 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
     a.wr = next ? (const void *)((const char *)router_w + (l + 1) * wr_stride) : nullptr;
     a.next_counts = (next && route_counts) ? route_counts + (size_t)(l + 1) * E : nullptr;
     a.residual = residual ? (const float *)xin : nullptr;
+    if (bias0 && !a.route_gu) a.router_bias = bias0 + (size_t)(l + 1) * E;
     a.out = out;
     a.layer_out = layer_out ? layer_out + (size_t)l * T_H : nullptr;
     // several tokens: the expert GEMVs (k_down_multi), then the combine (k_down)
@@ -347,6 +358,9 @@ static int prefill_run(const coli_moe_desc *d, int k, int n_layers, const void *
   for (int l = 0; l < n_layers; ++l) {
     PrefillArgs a{};
     a.T = T; a.H = H; a.F = F; a.E = E; a.S = S; a.k = k;
+    a.router_fn = d->router_fn;
+    a.router_bias = (d->router_fn == COLI_ROUTER_SIGMOID_BIAS && d->router_bias)
+                        ? d->router_bias + (size_t)l * E : nullptr;
     a.x = l == 0 ? x : (const void *)out;
     a.wr = (const char *)router_w + l * wr_stride;
     a.packed = packed + l * pk_stride;

@@ -86,6 +86,8 @@ struct Dec2Args {
   int fx;                   // router partials as fixed-point sums (T*E <= kFxMaxTE)
   long long *fx_acc;        // [T][E] partials are added here
   uint32_t *fx_flag;        // [T][E] non-finite or out-of-range partial seen
+  int router_fn;            // coli_router_fn of the layer being routed
+  const float *router_bias; // its selection bias [E] (sigmoid router) or null
   int route_gu;             // every gate/up CTA routes its layer from fx_rd_*
   int gu_route_fits;        // the routing scratch fits in k_gateup's pipeline ring
   const long long *fx_rd_acc;   // k_gateup: this layer's fixed-point logits
@@ -147,6 +149,8 @@ constexpr int kPrefillMinT = 64;      // calls with at least this many tokens ta
 constexpr int kGroupTokens = 256;     // tokens per block of the counting sort
 struct PrefillArgs {
   int T, H, F, E, S, k;
+  int router_fn;            // coli_router_fn
+  const float *router_bias; // [E] (sigmoid router) or null
   const void *x;            // [T][H] x_dtype
   const void *wr;           // [E][H] router dtype
   const uint8_t *packed;    // expert records of this layer

@@ -342,9 +342,9 @@ __device__ __forceinline__ float ld_part(const float *src, size_t i, bool staged
 // Routing shared by k_gateup and k_topk: logits from this CTA's replica of the
 // router partials (fixed summation order), block-parallel top-k, NaN flag and,
 // if `publish`, the user-visible idx/gates and route counts.
-__device__ void route_block(const Dec2Args &a, const LayerPtrs &lp, float *s_logits, int *s_idx,
-                            float *s_gates, float *s_vals, int *s_rank, float *s_scratch,
-                            float *s_stage, bool publish) {
+__device__ void route_block(const Dec2Args &a, const LayerPtrs &lp, float *s_logits, float *s_sel,
+                            int *s_idx, float *s_gates, float *s_vals, int *s_rank,
+                            float *s_scratch, float *s_stage, bool publish) {
   const int T = a.T, E = a.E, k = a.k;
   const int TE = T * E;
   const int nthr = blockDim.x;
@@ -418,7 +418,11 @@ __device__ void route_block(const Dec2Args &a, const LayerPtrs &lp, float *s_log
     }
   }
   __syncthreads();
-  const bool nan = select_topk(s_logits, T, E, k, s_idx, s_gates, s_vals, s_rank, (int *)s_scratch);
+  const bool sig = a.router_fn == COLI_ROUTER_SIGMOID_BIAS;
+  if (sig) sigmoid_keys(s_logits, s_sel, a.router_bias, T, E);
+  const bool nan = select_topk(sig ? s_sel : s_logits, T, E, k, s_idx, s_gates, s_vals, s_rank,
+                               (int *)s_scratch);
+  if (sig) sigmoid_gates(s_logits, s_idx, T, E, k, s_gates);
   COLI_TRACE_POINT(a.layer, kTpRtTopk);
   if (publish) {
     if (threadIdx.x == 0 && nan) set_flag(a.ctrl, COLI_FLAG_NAN_LOGITS);
@@ -432,13 +436,14 @@ __device__ void route_block(const Dec2Args &a, const LayerPtrs &lp, float *s_log
 
 // Shared-memory layout of the routing CTA (byte offsets).
 struct RouteSmem {
-  size_t logits, topk, idx, gates, vals, scratch, act, routes, slot_gate, total;
+  size_t logits, sel, topk, idx, gates, vals, scratch, act, routes, slot_gate, total;
 };
 __host__ __device__ inline RouteSmem route_smem(int T, int E, int k, int S, int n_part, bool stage) {
   auto a16 = [](size_t v) { return (v + 15) & ~(size_t)15; };
   RouteSmem R{};
   size_t o = stage ? (size_t)n_part * T * E * 4 : 0;
   R.logits = a16(o); o = R.logits + (size_t)T * E * 4;
+  R.sel = a16(o); o = R.sel + (size_t)T * E * 4;
   R.topk = a16(o);
   size_t tk = topk_scratch_bytes(T, E, k);
   if (tk < (size_t)T * k * 4) tk = (size_t)T * k * 4;       // the union's sort scratch
@@ -468,7 +473,7 @@ __device__ void route_finish(const Dec2Args &a, const LayerPtrs &lp, uint8_t *sm
   float *s_gates = (float *)(smem + R.gates);
   float *s_vals = (float *)(smem + R.vals);
   float *s_scratch = (float *)(smem + R.scratch);
-  route_block(a, lp, s_logits, s_idx, s_gates, s_vals, s_rank, s_scratch,
+  route_block(a, lp, s_logits, (float *)(smem + R.sel), s_idx, s_gates, s_vals, s_rank, s_scratch,
               a.stage_partials ? s_stage : nullptr, true);
   __syncthreads();
   for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
@@ -632,13 +637,14 @@ __device__ void load_lists(const Dec2Args &a, int *s_act, int *s_routes, float *
 
 // Shared-memory scratch of gu_route (byte offsets from its base).
 struct GuRouteSmem {
-  size_t logits, topk, idx, gates, vals, flag, total;
+  size_t logits, sel, topk, idx, gates, vals, flag, total;
 };
 __host__ __device__ inline GuRouteSmem gu_route_smem(int T, int E, int k) {
   auto a16 = [](size_t v) { return (v + 15) & ~(size_t)15; };
   GuRouteSmem R{};
   size_t o = 0;
   R.logits = o; o = a16(o + (size_t)T * E * 4);
+  R.sel = o; o = a16(o + (size_t)T * E * 4);
   R.topk = o;
   size_t tk = topk_scratch_bytes(T, E, k);
   if (tk < (size_t)T * k * 4) tk = (size_t)T * k * 4;   // the union's sort scratch
@@ -674,8 +680,15 @@ __device__ void gu_lists(const Dec2Args &a, const LayerPtrs &lp, uint8_t *scratc
   }
   __syncthreads();
   COLI_TRACE_POINT(a.layer, kTpRtLogits);
-  const bool nan = select_topk(s_logits, T, E, k, s_idx, s_gates, (float *)(scratch + R.vals),
+  const bool sig = a.router_fn == COLI_ROUTER_SIGMOID_BIAS;
+  float *s_keys = s_logits;
+  if (sig) {
+    s_keys = (float *)(scratch + R.sel);
+    sigmoid_keys(s_logits, s_keys, a.router_bias, T, E);
+  }
+  const bool nan = select_topk(s_keys, T, E, k, s_idx, s_gates, (float *)(scratch + R.vals),
                                scratch + R.topk, (int *)(scratch + R.flag));
+  if (sig) sigmoid_gates(s_logits, s_idx, T, E, k, s_gates);
   COLI_TRACE_POINT(a.layer, kTpRtTopk);
   block_union(s_idx, s_gates, T, k, S, E, s_act, s_act + 1, s_act + 1 + (E + S), s_routes,
               s_slot_gate, (int *)(scratch + R.topk));

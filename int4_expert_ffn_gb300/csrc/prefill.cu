@@ -269,15 +269,20 @@ __global__ void __launch_bounds__(256) k_ptopk(PrefillArgs p) {
   const int T = p.T, E = p.E, k = p.k;
   const int t0 = blockIdx.x * kPTopkTokens;
   const int TB = (T - t0 < kPTopkTokens) ? T - t0 : kPTopkTokens;
+  const size_t lg_bytes = ((size_t)kPTopkTokens * E * 4 + 15) & ~(size_t)15;
   float *lg = (float *)smem;                                      // [kPTopkTokens][E]
-  uint8_t *s_tk = smem + ((kPTopkTokens * E * 4 + 15) & ~15);    // top-k scratch
+  float *sel = (float *)(smem + lg_bytes);                        // [kPTopkTokens][E]
+  uint8_t *s_tk = smem + 2 * lg_bytes;                            // top-k scratch
   int *s_idx = (int *)(s_tk + ((topk_scratch_bytes(kPTopkTokens, E, k) + 15) & ~(size_t)15));
   float *s_gates = (float *)(s_idx + kPTopkTokens * k);
   float *s_vals = s_gates + kPTopkTokens * k;
   int *s_flag = (int *)(s_vals + kPTopkTokens * k);
   for (int i = threadIdx.x; i < TB * E; i += blockDim.x) lg[i] = p.logits[(size_t)t0 * E + i];
   __syncthreads();
-  const bool nan = select_topk(lg, TB, E, k, s_idx, s_gates, s_vals, s_tk, s_flag);
+  const bool sig = p.router_fn == COLI_ROUTER_SIGMOID_BIAS;
+  if (sig) sigmoid_keys(lg, sel, p.router_bias, TB, E);
+  const bool nan = select_topk(sig ? sel : lg, TB, E, k, s_idx, s_gates, s_vals, s_tk, s_flag);
+  if (sig) sigmoid_gates(lg, s_idx, TB, E, k, s_gates);
   if (threadIdx.x == 0 && nan) set_flag_p(p.ctrl, COLI_FLAG_NAN_LOGITS);
   for (int i = threadIdx.x; i < TB * k; i += blockDim.x) {
     p.idx[(size_t)t0 * k + i] = s_idx[i];
@@ -682,7 +687,7 @@ cudaError_t launch_prefill(const PrefillArgs &p, int x_dtype, int wr_dtype, cuda
   else COLI_LOGITS(float, float);
 #undef COLI_LOGITS
   // top-k
-  const size_t tk_smem = (((size_t)kPTopkTokens * E * 4 + 15) & ~(size_t)15) +
+  const size_t tk_smem = 2 * (((size_t)kPTopkTokens * E * 4 + 15) & ~(size_t)15) +
                          ((topk_scratch_bytes(kPTopkTokens, E, k) + 15) & ~(size_t)15) +
                          (size_t)kPTopkTokens * k * 12 + 16;
   if ((e = set_smem(k_ptopk, tk_smem)) != cudaSuccess) return e;

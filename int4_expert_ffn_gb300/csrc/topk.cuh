@@ -230,6 +230,49 @@ __device__ __forceinline__ bool select_topk(const float *lg, int T, int E, int k
   return warp_topk(lg, T, E, k, idx, gates, vals, s_flag);
 }
 
+// Routing by sigmoid scores with a selection-only bias (the GLM layers'
+// n_group = 1 sigmoid + noaux_tc router; with one group the group-limited
+// step keeps every expert): s = 1 / (1 + e^-l); experts are ranked by
+// s + bias[e] under the select_topk rules; gates = the picked s over their
+// sum (a picked NaN gets 0; an all-NaN token gets 1/k).  Used around one
+// select_topk call, so the top-k code is not duplicated:
+//   sigmoid_keys   lg [T][E] logits -> s (in place), sel [T][E] = s + bias
+//   select_topk    on sel
+//   sigmoid_gates  gates of the picked experts from s
+// bias: E floats in global memory, or null (zero).
+__device__ __forceinline__ void sigmoid_keys(float *lg, float *sel, const float *bias, int T,
+                                             int E) {
+  for (int i = threadIdx.x; i < T * E; i += blockDim.x) {
+    const float sc = 1.0f / (1.0f + expf(-lg[i]));
+    lg[i] = sc;
+    sel[i] = sc + (bias ? __ldg(bias + i % E) : 0.0f);
+  }
+  __syncthreads();
+}
+
+static __device__ __noinline__ void sigmoid_gates(const float *s, const int *idx, int T, int E, int k,
+                                           float *gates) {
+  for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
+    const int t = i / k;
+    const int *it = idx + t * k;
+    const float s0 = s[(size_t)t * E + it[0]];
+    float g;
+    if (s0 != s0) {
+      g = 1.0f / (float)k;
+    } else {
+      float den = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        const float sj = s[(size_t)t * E + it[j]];
+        den += (sj != sj) ? 0.0f : sj;
+      }
+      const float si = s[(size_t)t * E + idx[i]];
+      g = (si != si) ? 0.0f : si / den;
+    }
+    gates[i] = g;
+  }
+  __syncthreads();
+}
+
 // Block-parallel union lists (see warp_union for the layout).  s_sorted: T*k
 // ints of scratch.  Returns the number of used experts (routed + shared).
 __device__ __forceinline__ int block_union(const int *idx, const float *gates, int T, int k, int S,

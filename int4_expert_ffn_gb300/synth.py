@@ -55,7 +55,7 @@ SHAPES = {s.name: s for s in (TINY, OLMOE_DECODE, GLM_DECODE_B1, GLM_DECODE_B8, 
 EXPERT_STD = 0.02  # expert weights N(0, 0.02)
 
 # sub-key tags
-_T_X, _T_ROUTER, _T_EXPERT, _T_OUTLIER = 1, 2, 3, 4
+_T_X, _T_ROUTER, _T_EXPERT, _T_OUTLIER, _T_BIAS = 1, 2, 3, 4, 5
 MAT_GATE, MAT_UP, MAT_DOWN = 0, 1, 2
 
 
@@ -126,6 +126,12 @@ def router_weights(shape: MoEShape, layer, seed=0, device="cpu", row_std=None):
     if row_std is not None:
         std = torch.as_tensor(np.asarray(row_std, np.float32).reshape(E, 1), device=base.device)
     return (base * std).to(_tdt(shape.router_dtype))
+
+
+def router_bias(shape: MoEShape, layer, seed=0, device="cpu", std=0.1):
+    """Selection bias [E] of the sigmoid router, N(0, std^2) f32 (the pages give
+    no values; trained biases of this kind are small next to the scores' 0..1)."""
+    return normal((shape.experts,), std, torch.float32, seed, _T_BIAS, layer, device=device)
 
 
 def expert_matrix(shape: MoEShape, layer, expert, mat, seed=0, device="cpu",

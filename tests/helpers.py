@@ -80,15 +80,23 @@ def min_topk_gap(logits, k):
     return float(np.min(lg[:, :kk - 1] - lg[:, 1:kk]))
 
 
-def tokens_without_ties(shape, wr64, seed=0, step=0, T=None, dtype=None):
-    """Layer input drawn with the next attempt index until no near-tie."""
+def selection_keys(logits, bias):
+    """Ranking keys of the sigmoid router: sigmoid(logit) + bias (f64)."""
+    return 1.0 / (1.0 + np.exp(-logits)) + np.asarray(bias, np.float64)[None, :]
+
+
+def tokens_without_ties(shape, wr64, seed=0, step=0, T=None, dtype=None, bias=None):
+    """Layer input drawn with the next attempt index until no near-tie (of the
+    logits, or with ``bias`` of the sigmoid router's keys)."""
     for attempt in range(50):
         x = synth.tokens(shape, seed, step, attempt=attempt)
         if T is not None:
             x = x[:T]
         if dtype is not None:
             x = x.to(dtype)
-        if min_topk_gap(orc.router_logits(x.double().numpy(), wr64), shape.top_k) > TIE_GAP:
+        lg = orc.router_logits(x.double().numpy(), wr64)
+        keys = lg if bias is None else selection_keys(lg, bias)
+        if min_topk_gap(keys, shape.top_k) > TIE_GAP:
             return x
     raise RuntimeError("could not draw tie-free tokens")
 
