@@ -156,7 +156,7 @@ def max_over_ranks(v, world, dev):
 class DecodeWorkload:
     """A decode stack resident in HBM: weights, routers, per-step inputs."""
 
-    def __init__(self, shape, steps_total, dev, seed=0):
+    def __init__(self, shape, steps_total, dev, seed=0, router="softmax"):
         import int4_expert_ffn_gb300 as pkg
         from int4_expert_ffn_gb300 import synth
         self.coli = pkg.binding
@@ -198,8 +198,19 @@ class DecodeWorkload:
         self.layer_bytes = n * self.eb
         self.layer_scales = n * self.es
         self.counts = torch.zeros((steps_total, L, E), dtype=torch.int32, device=dev)
-        self.desc = c.MoEDesc(H, F, E, S, T, c.COLI_F32,
-                              c.COLI_BF16 if shape.router_dtype == "bf16" else c.COLI_F32)
+        rdt = c.COLI_BF16 if shape.router_dtype == "bf16" else c.COLI_F32
+        if router == "sigmoid":
+            # the GLM router: per-layer selection biases; one descriptor per layer
+            # call (unchained) or one for the stack ([L, E] biases)
+            self.bias = torch.stack([synth.router_bias(shape, l, seed, device=dev)
+                                     for l in range(L)]).contiguous()
+            fn = c.COLI_ROUTER_SIGMOID_BIAS
+            self.desc = c.MoEDesc(H, F, E, S, T, c.COLI_F32, rdt, fn, self.bias)
+            self.layer_desc = [c.MoEDesc(H, F, E, S, T, c.COLI_F32, rdt, fn, self.bias[l])
+                               for l in range(L)]
+        else:
+            self.desc = c.MoEDesc(H, F, E, S, T, c.COLI_F32, rdt)
+            self.layer_desc = [self.desc] * L
         self.ws = c.new_workspace(self.desc, shape.top_k)
         torch.cuda.synchronize()
 
@@ -216,7 +227,7 @@ class DecodeWorkload:
             return
         pb, sb = self.layer_bytes, self.layer_scales
         for l in range(sh.layers):
-            c.coli_moe_forward(self.desc, sh.top_k, x[l], self.router[l],
+            c.coli_moe_forward(self.layer_desc[l], sh.top_k, x[l], self.router[l],
                                self.packed[l * pb:(l + 1) * pb], self.scales[l * sb:(l + 1) * sb],
                                self.ws, out=out[l], route_counts=self.counts[i, l], stream=stream)
 
@@ -411,7 +422,7 @@ def capture_graphs(wl, idxs, stream):
 
 def run_decode(args, shape, dev, world, rank):
     steps, warmup = args.steps, args.warmup
-    wl = DecodeWorkload(shape, warmup + steps, dev)
+    wl = DecodeWorkload(shape, warmup + steps, dev, router=getattr(args, "router", "softmax"))
     stream = torch.cuda.Stream(device=dev)
     # eager warm-up (first launches, module load), then graphs of each step
     with torch.cuda.stream(stream):
@@ -618,6 +629,9 @@ def main():
                     help="override the stack depth (small profiling cases only)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the batch size (small profiling cases only)")
+    ap.add_argument("--router", default="softmax", choices=["softmax", "sigmoid"],
+                    help="decode workloads: softmax routing, or the GLM router (sigmoid "
+                         "scores with a per-layer selection bias)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -642,9 +656,11 @@ def main():
         shape = dataclasses.replace(shape, layers=args.layers or shape.layers,
                                     tokens=args.tokens or shape.tokens)
     config = {"workload": "%s: %d MoE layers, hidden %d, %d experts of FFN width %d, top-%d, "
-                          "%d shared, batch %d, int4-grouped g64 f32 scales, %s router"
+                          "%d shared, batch %d, int4-grouped g64 f32 scales, %s router%s"
                           % (shape.name, shape.layers, shape.hidden, shape.experts, shape.ffn,
-                             shape.top_k, shape.shared, shape.tokens, shape.router_dtype),
+                             shape.top_k, shape.shared, shape.tokens, shape.router_dtype,
+                             ", sigmoid scores + selection bias" if args.router == "sigmoid"
+                             else ""),
               "layers": shape.layers, "hidden": shape.hidden, "experts": shape.experts,
               "ffn": shape.ffn, "top_k": shape.top_k, "shared": shape.shared,
               "batch": shape.tokens, "parallelism": "replicas" if world > 1 else "single",

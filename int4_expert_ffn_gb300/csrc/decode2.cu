@@ -637,7 +637,7 @@ __device__ void load_lists(const Dec2Args &a, int *s_act, int *s_routes, float *
 
 // Shared-memory scratch of gu_route (byte offsets from its base).
 struct GuRouteSmem {
-  size_t logits, sel, topk, idx, gates, vals, flag, total;
+  size_t logits, sel, bias, topk, idx, gates, vals, flag, total;
 };
 __host__ __device__ inline GuRouteSmem gu_route_smem(int T, int E, int k) {
   auto a16 = [](size_t v) { return (v + 15) & ~(size_t)15; };
@@ -645,6 +645,7 @@ __host__ __device__ inline GuRouteSmem gu_route_smem(int T, int E, int k) {
   size_t o = 0;
   R.logits = o; o = a16(o + (size_t)T * E * 4);
   R.sel = o; o = a16(o + (size_t)T * E * 4);
+  R.bias = o; o = a16(o + (size_t)E * 4);
   R.topk = o;
   size_t tk = topk_scratch_bytes(T, E, k);
   if (tk < (size_t)T * k * 4) tk = (size_t)T * k * 4;   // the union's sort scratch
@@ -684,7 +685,8 @@ __device__ void gu_lists(const Dec2Args &a, const LayerPtrs &lp, uint8_t *scratc
   float *s_keys = s_logits;
   if (sig) {
     s_keys = (float *)(scratch + R.sel);
-    sigmoid_keys(s_logits, s_keys, a.router_bias, T, E);
+    sigmoid_keys(s_logits, s_keys, a.router_bias ? (const float *)(scratch + R.bias) : nullptr,
+                 T, E);
   }
   const bool nan = select_topk(s_keys, T, E, k, s_idx, s_gates, (float *)(scratch + R.vals),
                                scratch + R.topk, (int *)(scratch + R.flag));
@@ -706,6 +708,14 @@ __device__ void gu_lists(const Dec2Args &a, const LayerPtrs &lp, uint8_t *scratc
     }
   }
   __syncthreads();
+}
+
+// The sigmoid router's bias does not depend on the previous kernel: the
+// gate/up CTAs copy it into gu_lists' scratch before their dependency wait.
+__device__ __forceinline__ void gu_bias_prefetch(const Dec2Args &a, uint8_t *scratch) {
+  if (!a.route_gu || a.router_fn != COLI_ROUTER_SIGMOID_BIAS || !a.router_bias) return;
+  float *s_bias = (float *)(scratch + gu_route_smem(a.T, a.E, a.k).bias);
+  for (int i = threadIdx.x; i < a.E; i += blockDim.x) s_bias[i] = __ldg(a.router_bias + i);
 }
 
 // The down kernel of a layer clears the fixed-point buffer that the layer's
@@ -735,6 +745,7 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
   int *s_routes = (int *)(smem + L.routes);
   float *s_slot_gate = (float *)(smem + L.slot_gate);
   float *red = (float *)(smem + L.red);
+  gu_bias_prefetch(a, smem + L.ring);
   grid_dependents_launch();
   grid_dependency_wait();
   COLI_TRACE_POINT(a.layer, kTpGuDepWait);
@@ -920,6 +931,7 @@ __global__ void __launch_bounds__(kDec2MaxThreads) k_gateup_multi(Dec2Args a) {
   float *s_slot_gate = (float *)(smem + L.slot_gate);
   int *s_tok = (int *)(smem + L.tok);            // [T] needed tokens, then [T] token -> plane
   uint32_t *s_xpl = (uint32_t *)(smem + L.xpl);  // the needed tokens' planes, then the ring
+  gu_bias_prefetch(a, smem + L.xpl);
   grid_dependents_launch();
   grid_dependency_wait();
   COLI_TRACE_POINT(a.layer, kTpGuDepWait);

@@ -239,13 +239,13 @@ __device__ __forceinline__ bool select_topk(const float *lg, int T, int E, int k
 //   sigmoid_keys   lg [T][E] logits -> s (in place), sel [T][E] = s + bias
 //   select_topk    on sel
 //   sigmoid_gates  gates of the picked experts from s
-// bias: E floats in global memory, or null (zero).
+// bias: E floats (global or shared memory), or null (zero).
 __device__ __forceinline__ void sigmoid_keys(float *lg, float *sel, const float *bias, int T,
                                              int E) {
   for (int i = threadIdx.x; i < T * E; i += blockDim.x) {
     const float sc = 1.0f / (1.0f + expf(-lg[i]));
     lg[i] = sc;
-    sel[i] = sc + (bias ? __ldg(bias + i % E) : 0.0f);
+    sel[i] = sc + (bias ? bias[i % E] : 0.0f);
   }
   __syncthreads();
 }

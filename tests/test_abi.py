@@ -64,6 +64,22 @@ def test_workspace_size_rejects_bad_desc(coli, bad):
     assert coli.coli_moe_workspace_size(_desc(coli, **bad), 2) == 0
 
 
+def test_router_fn_validated(coli):
+    # unknown routing function -> rejected before any launch or allocation size
+    assert coli.coli_moe_workspace_size(_desc(coli, router_fn=2), 2) == 0
+    assert coli.coli_moe_workspace_size(_desc(coli, router_fn=-1), 2) == 0
+    # the sigmoid router with no bias (zero bias) is a valid descriptor
+    assert coli.coli_moe_workspace_size(_desc(coli, router_fn=coli.COLI_ROUTER_SIGMOID_BIAS), 2) > 0
+
+
+def test_desc_layout_matches_header(coli):
+    # the ctypes mirror of coli_moe_desc: 8 int32-sized fields, then the bias pointer
+    D = coli.coli_moe_desc
+    assert D.router_fn.offset == 28 and D.router_bias.offset == 32 and C.sizeof(D) == 40
+    text = open(os.path.join(ROOT, "include", "coli.h")).read()
+    assert "COLI_ROUTER_SIGMOID_BIAS = 1" in text and "const float *router_bias;" in text
+
+
 def test_workspace_size_bad_topk(coli):
     d = _desc(coli)
     assert coli.coli_moe_workspace_size(d, 0) == 0
