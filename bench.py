@@ -629,6 +629,9 @@ def main():
                     help="override the stack depth (small profiling cases only)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the batch size (small profiling cases only)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="quant workload: experts converted per step (default 256; smaller for "
+                         "profiling captures)")
     ap.add_argument("--router", default="softmax", choices=["softmax", "sigmoid"],
                     help="decode workloads: softmax routing, or the GLM router (sigmoid "
                          "scores with a per-layer selection bias)")
@@ -738,7 +741,7 @@ def emit_quant(args, dev, world, rank):
     import int4_expert_ffn_gb300 as pkg
     from int4_expert_ffn_gb300 import synth
     c = pkg.binding
-    E, F, H = 256, 2048, 6144
+    E, F, H = args.experts or 256, 2048, 6144
     kinds = [(F, H), (F, H), (H, F)]
     mats = []
     for m, (rows, cols) in enumerate(kinds):
@@ -783,7 +786,7 @@ def emit_quant(args, dev, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 -> u8 + f32",
         "data": "synthetic (seeded bf16 N(0,0.02), 1% outliers x20)",
-        "config": {"workload": "quantiser: 256 experts x {gate, up [2048,6144], down [6144,2048]}",
+        "config": {"workload": "quantiser: %d experts x {gate, up [2048,6144], down [6144,2048]}" % E,
                    "elements": elems, "bytes_per_step": nbytes,
                    "l2": "inputs larger than L2 (%.1f GB)" % (nbytes / 1e9)},
         "roofline": {"bound": "hbm", "kernel": "k_quant_vec", "achieved": gbs, "peak": hbm_peak,

@@ -29,20 +29,33 @@ __device__ __forceinline__ int quant_one(float w, float s, float r) {
   return (int)v;
 }
 
-// The same result with fewer instructions, for the vectorised path.  Adding
-// 1.5 * 2^23 to a (|a| < 2^22) leaves round-half-even(a) in the low mantissa
-// bits, so the sum's bit pattern minus the constant's is rint(a), and
-// subtracting the constant back gives rint(a) as a float for the distance
-// check.  |a| < 7.5 keeps rint(a) in [-7, 7] (no clamp); anything else, and
-// any quotient within 4e-6 of a half-integer, takes quant_one's exact path.
+// The same result with fewer instructions, for the vectorised path: eight
+// elements of one group (scale s, r = rcp(s)) into one packed word.  Adding
+// 1.5 * 2^23 to a = w * r (|a| < 2^22) leaves round-half-even(a) in the low
+// mantissa bits, so the sum's bit pattern minus the constant's is rint(a);
+// subtracting the constant back gives rint(a) as a float, and |a - rint(a)|
+// is the distance to it.  For finite weights |a| <= 7 (1 + 2^-20), so
+// rint(a) is in [-7, 7] and needs no clamp.  If any of the eight quotients
+// lies within 4e-6 of a half-integer, or is not finite (the distance is then
+// NaN), the word is recomputed element by element with quant_one.
 constexpr float kRoundShift = 12582912.0f;   // 1.5 * 2^23
-__device__ __forceinline__ uint32_t quant_nibble(float w, float s, float r) {
-  const float a = w * r;
-  const float t = a + kRoundShift;
-  const float e = fabsf(a - (t - kRoundShift));   // distance to rint(a), in [0, 0.5]
-  uint32_t u = (uint32_t)(__float_as_int(t) - __float_as_int(kRoundShift) + 8);
-  if (!(e < 0.5f - 4e-6f && fabsf(a) < 7.5f)) u = (uint32_t)(quant_one(w, s, r) + 8);
-  return u;
+__device__ __forceinline__ uint32_t quant_word(const float (&v)[8], float s, float r) {
+  uint32_t word = 0;
+  bool exact = true;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float a = v[i] * r;
+    const float t = a + kRoundShift;
+    const float e = fabsf(a - (t - kRoundShift));
+    word |= (uint32_t)(__float_as_int(t) - __float_as_int(kRoundShift) + 8) << (4 * i);
+    exact = exact && (e < 0.5f - 4e-6f);
+  }
+  if (!exact) {
+    word = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) word |= (uint32_t)(quant_one(v[i], s, r) + 8) << (4 * i);
+  }
+  return word;
 }
 
 template <typename T>
@@ -106,10 +119,7 @@ __global__ void __launch_bounds__(256) k_quant_vec(const T *__restrict__ w, int6
       const float s = __fdiv_rn(m, 7.0f);
       uint32_t word = 0x88888888u;
       if (s != 0.0f) {
-        const float r = __frcp_rn(s);
-        word = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) word |= quant_nibble(v[u][i], s, r) << (4 * i);
+        word = quant_word(v[u], s, __frcp_rn(s));
       }
       packed[g * 8 + sub] = word;
       if (sub == 0) scales[g] = s;
