@@ -5,10 +5,11 @@
 //
 // HBM-bound: reads 2 B (bf16) per element and writes 0.5 B + 4 B per 64.
 // Bit-exactness with the f32 definition: the quotient w / s is formed as
-// w * rcp(s); it lies within 1.5e-6 of the correctly rounded f32 quotient, so
-// whenever it is farther than 4e-6 from a half-integer both round to the same
-// integer.  The rare element near a half-integer (or any non-finite value) takes
-// the exact IEEE division.
+// w * r with r the approximate reciprocal of s (rcp.approx, at most 1 ulp off);
+// for |w / s| <= 7 it lies within 1.7e-6 of the correctly rounded f32 quotient,
+// so whenever it is farther than 4e-6 from a half-integer both round to the
+// same integer.  The rare element near a half-integer (or any non-finite value,
+// or a subnormal s that the approximation flushes) takes the exact IEEE division.
 #include "coli_internal.cuh"
 
 namespace coli {
@@ -39,6 +40,14 @@ __device__ __forceinline__ int quant_one(float w, float s, float r) {
 // lies within 4e-6 of a half-integer, or is not finite (the distance is then
 // NaN), the word is recomputed element by element with quant_one.
 constexpr float kRoundShift = 12582912.0f;   // 1.5 * 2^23
+
+// Approximate reciprocal (PTX rcp.approx: at most 1 ulp of error; subnormal
+// input and output flushed to zero).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
 __device__ __forceinline__ uint32_t quant_word(const float (&v)[8], float s, float r) {
   uint32_t word = 0;
   bool exact = true;
@@ -91,7 +100,7 @@ struct Load8<float> {
 // flattened matrix is elements [64g, 64g+64), bytes [32g, 32g+32), scale g.
 // A team of 8 lanes owns one group; each lane holds 8 consecutive elements.
 template <typename T, int U>
-__global__ void __launch_bounds__(256) k_quant_vec(const T *__restrict__ w, int64_t n_groups,
+__global__ void __launch_bounds__(256, 4) k_quant_vec(const T *__restrict__ w, int64_t n_groups,
                                                    uint32_t *__restrict__ packed,
                                                    float *__restrict__ scales) {
   const int lane = threadIdx.x & 31;
@@ -119,7 +128,7 @@ __global__ void __launch_bounds__(256) k_quant_vec(const T *__restrict__ w, int6
       const float s = __fdiv_rn(m, 7.0f);
       uint32_t word = 0x88888888u;
       if (s != 0.0f) {
-        word = quant_word(v[u], s, __frcp_rn(s));
+        word = quant_word(v[u], s, rcp_approx(s));
       }
       packed[g * 8 + sub] = word;
       if (sub == 0) scales[g] = s;
@@ -170,7 +179,7 @@ cudaError_t launch_quant_i4g(const void *w, int w_dtype, int64_t rows, int64_t c
     const int64_t n_groups = rows * (cols / kGroup);
     const int64_t teams_needed = n_groups;
     int64_t blocks = (teams_needed * 8 + 255) / 256;
-    const int64_t cap = (int64_t)sms * 8;  // 8 blocks of 256 per SM resident
+    const int64_t cap = (int64_t)sms * 4;  // 4 blocks of 256 per SM resident (64 registers)
     if (blocks > cap) blocks = cap;
     if (w_dtype == COLI_BF16)
       k_quant_vec<__nv_bfloat16, 4><<<(unsigned)blocks, 256, 0, s>>>(
