@@ -921,8 +921,11 @@ struct MTask {
   __device__ __forceinline__ GuTask gu() const { return GuTask{0, cg, ai, f}; }
 };
 
+// At most 8 warps: the task loop then keeps its state in registers (no spills).
+constexpr int kGuMultiMaxThreads = 256;
+
 template <bool kFast, bool kXpl>
-__global__ void __launch_bounds__(kDec2MaxThreads) k_gateup_multi(Dec2Args a) {
+__global__ void __launch_bounds__(kGuMultiMaxThreads) k_gateup_multi(Dec2Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const GuSmem &L = a.gu;
   COLI_TRACE_POINT(a.layer, kTpGuEntry);
@@ -1622,9 +1625,9 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
     // planes (x quantised per task).
     g.tok = o; o = al16(o + (size_t)(2 * T + 3) * 4);
     const size_t xpl_bytes = (size_t)T * 18 * (H / 32) * 4;
-    static const int kNwM[] = {8, 12, 16, 4};
+    static const int kNwM[] = {kGuMultiMaxThreads / 32, 4};
     for (int xpl = 1; xpl >= 0 && !ok; --xpl)
-      for (int c = 0; c < 4 && !ok; ++c) {
+      for (int c = 0; c < 2 && !ok; ++c) {
         const size_t acc = (size_t)kNwM[c] * T * 8 * 4;
         const size_t ring2 = (size_t)kNwM[c] * 2 * a.gu_slot_bytes;
         if (al128(al16(o + acc) + (xpl ? xpl_bytes : 0)) + ring2 <= budget) {
