@@ -736,8 +736,11 @@ __device__ __forceinline__ void clear_fx(const Dec2Args &a) {
 // and there is no token loop.
 // kFast: H a multiple of 1024 (every lane of every chunk active, 16-byte
 // aligned scale rows), checks folded away.
+// At most 12 warps (the plan's choices), so the compiler may use up to 168 registers.
+constexpr int kGuOneMaxThreads = 384;
+
 template <bool kFast>
-__global__ void __launch_bounds__(kDec2MaxThreads) k_gateup(Dec2Args a) {
+__global__ void __launch_bounds__(kGuOneMaxThreads) k_gateup(Dec2Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const GuSmem &L = a.gu;
   COLI_TRACE_POINT(a.layer, kTpGuEntry);
@@ -1585,8 +1588,8 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
   g.slot_gate = o; o = al16(o + (size_t)T * KS * 4);
   // warps x slots (measured: 12 x 2 and 12 x 3 within 1-2 %; the smaller
   // ring leaves more of the SM's unified memory to L1), then 16 x 2, ...
-  static const int kNw[] = {12, 12, 16, 8, 8, 4};
-  static const int kSl[] = {2, 3, 2, 3, 2, 2};
+  static const int kNw[] = {12, 12, 8, 8, 4, 4};
+  static const int kSl[] = {2, 3, 3, 2, 3, 2};
   bool ok = false;
   if (T == 1) {
     // one token: partial sums per (row, chunk) in shared memory, rows in
