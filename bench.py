@@ -37,12 +37,12 @@ METRIC = "MoE decode tokens/s and int4 expert-weight GB/s vs GB300 HBM peak"
 NCU_TRAFFIC = {
     # profiles/k_gateup_k_down_olmoe_2layer.md (batch 1: the same launch per layer
     # as the 16-layer stack; cold-cache capture)
-    "olmoe_decode": {"k_gateup": 28454656 + 512, "k_down": 10036736},
+    "olmoe_decode": {"k_gateup": 19016192, "k_down": 10036736},
     # profiles/k_gateup_k_down_glm_layer.md
-    "glm_decode_b1": {"k_gateup": 157314816 + 3594240, "k_down": 64371456 + 350464},
+    "glm_decode_b1": {"k_gateup": 127681280 + 3630336, "k_down": 64375808 + 343296},
     # profiles/k_gateup_multi_k_down_multi_glm_b8_layer.md (k_gateup is the several-token
     # kernel k_gateup_multi; its experts per launch vary with the routing)
-    "glm_decode_b8": {"k_gateup": 880410368 + 8356352},
+    "glm_decode_b8": {"k_gateup": 879500288 + 7344384},
 }
 
 
