@@ -789,9 +789,13 @@ def emit_quant(args, dev, world, rank):
         "config": {"workload": "quantiser: %d experts x {gate, up [2048,6144], down [6144,2048]}" % E,
                    "elements": elems, "bytes_per_step": nbytes,
                    "l2": "inputs larger than L2 (%.1f GB)" % (nbytes / 1e9)},
+        # traffic per launch: profiles/k_quant_vec_quantiser_16experts.md captured one
+        # launch over 16 experts' matrices (402.7 MB read + 55.8 MB written); a launch
+        # here covers E experts' matrices of the same shape, so scaled by E / 16
         "roofline": {"bound": "hbm", "kernel": "k_quant_vec", "achieved": gbs, "peak": hbm_peak,
                      "unit": "GB/s", "frac": gbs / hbm_peak, "peak_kind": peak_kind,
-                     "traffic": None},
+                     "traffic": (402740480 + 55846144) * E / 16,
+                     "traffic_note": "from a 16-expert capture, scaled by experts"},
         "clocks": sampler.summary(t0, t1), "gpu_launches": 3 * args.steps,
     }
     if rank == 0:
