@@ -47,7 +47,9 @@ typedef enum {
     COLI_ECUDA = -3,         /* a CUDA launch or query failed */
     COLI_ETIMEOUT = -4,      /* a bounded device-side wait gave up */
     COLI_ENOMEM = -5,        /* the caller's workspace is too small */
-    COLI_EUNSUPPORTED = -6   /* valid, but outside what this build handles */
+    COLI_EUNSUPPORTED = -6,  /* valid, but outside what this build handles */
+    COLI_EIO = -7,           /* a file could not be opened, written or renamed */
+    COLI_EREFUSED = -8       /* a usage history belongs to another model or format */
 } coli_status;
 
 typedef enum { COLI_F32 = 0, COLI_BF16 = 1 } coli_dtype;
@@ -238,6 +240,54 @@ int coli_profile_events(int kernel, const cudaEvent_t *before, const cudaEvent_t
  * Returns COLI_ETIMEOUT if COLI_FLAG_TIMEOUT is set, else COLI_OK.
  */
 int coli_moe_check(void *workspace, int clear, uint32_t *flags, cudaStream_t stream);
+
+/*
+ * Route-count history file (".coli_usage", [P4] §历史文件): the per-(layer,
+ * expert) route counts of coli_moe_forward / coli_moe_stack_forward kept
+ * across runs.  Host-side; every pointer here is a host pointer.
+ *
+ * Format: text, one record of exactly three decimal fields per line,
+ *   -1 n_layers n_experts          geometry
+ *   -2 1 engine_id                 format version, then the writer's identity
+ *   layer expert count             one per nonzero count, layer-major order
+ * engine_id is the 32-bit FNV-1a hash of the engine's name (the third field,
+ * so a reader that takes the second field as a signed int never sees it).
+ * Records whose first field is negative are headers: a reader that only
+ * knows "layer expert count" skips them.  A history with no nonzero count is
+ * written as an empty (0-byte) file, without headers.
+ */
+
+/* 32-bit FNV-1a hash of a NUL-terminated name (the engine_id field). */
+uint32_t coli_usage_engine_id(const char *engine);
+
+/*
+ * coli_usage_save -- write counts [n_layers][n_experts] (uint32, host) to
+ * `path`: through "<path>.tmp" and rename(), so a reader never sees a partial
+ * file.  decay in (0, 1) first scales every count c > 0 to
+ * max(1, round(c * decay)) (older routes weigh less; an expert routed once
+ * stays); any other decay (1.0 included) leaves the counts as they are.
+ * Errors: COLI_EINVAL (null arguments, non-positive sizes, or a path so long
+ * that the temporary name would be truncated: refused before any file is
+ * touched), COLI_EIO.
+ */
+int coli_usage_save(const char *path, const uint32_t *counts, int32_t n_layers, int32_t n_experts,
+                    const char *engine, float decay);
+
+/*
+ * coli_usage_load -- add the records of `path` into counts [n_layers][n_experts]
+ * (uint32, host; not cleared) and set *n_records (may be NULL) to the number of
+ * records added.  An empty file adds nothing.  Records outside the geometry are
+ * discarded and not counted; header kinds other than -1 and -2 are skipped;
+ * files without headers (the older layout) are taken as they are.
+ * Refused with COLI_EREFUSED, adding nothing:
+ *   - a -1 record whose geometry differs, a -2 record of a later format
+ *     version, or a dense binary history (first four bytes "IKU1") -- always;
+ *   - a -2 record written by another engine -- unless `trusted` is nonzero
+ *     (the caller named this file on purpose).
+ * Errors: COLI_EINVAL, COLI_EIO (the file cannot be opened).
+ */
+int coli_usage_load(const char *path, uint32_t *counts, int32_t n_layers, int32_t n_experts,
+                    const char *engine, int trusted, int64_t *n_records);
 
 #ifdef __cplusplus
 }

@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_PKG, "libcoli.so")
 
 COLI_OK, COLI_EINVAL, COLI_EALIGN, COLI_ECUDA, COLI_ETIMEOUT, COLI_ENOMEM, COLI_EUNSUPPORTED = (
     0, -1, -2, -3, -4, -5, -6)
+COLI_EIO, COLI_EREFUSED = -7, -8
 COLI_F32, COLI_BF16 = 0, 1
 COLI_ROUTER_SOFTMAX, COLI_ROUTER_SIGMOID_BIAS = 0, 1
 COLI_FLAG_NAN_LOGITS, COLI_FLAG_TIMEOUT = 0x1, 0x2
@@ -30,7 +31,8 @@ EXPORTS = (
     "coli_expert_packed_bytes", "coli_expert_scale_count", "coli_quant_i4g",
     "coli_router_workspace_size", "coli_moe_workspace_size", "coli_router_topk",
     "coli_moe_forward", "coli_moe_forward_noalloc", "coli_moe_stack_forward",
-    "coli_profile_events", "coli_moe_check",
+    "coli_profile_events", "coli_moe_check", "coli_usage_engine_id", "coli_usage_save",
+    "coli_usage_load",
 )
 
 
@@ -86,6 +88,13 @@ def _load():
     L.coli_profile_events.restype = C.c_int
     L.coli_moe_check.argtypes = [vp, C.c_int, C.POINTER(C.c_uint32), vp]
     L.coli_moe_check.restype = C.c_int
+    L.coli_usage_engine_id.argtypes = [C.c_char_p]
+    L.coli_usage_engine_id.restype = C.c_uint32
+    L.coli_usage_save.argtypes = [C.c_char_p, vp, C.c_int32, C.c_int32, C.c_char_p, C.c_float]
+    L.coli_usage_save.restype = C.c_int
+    L.coli_usage_load.argtypes = [C.c_char_p, vp, C.c_int32, C.c_int32, C.c_char_p, C.c_int,
+                                  C.POINTER(C.c_int64)]
+    L.coli_usage_load.restype = C.c_int
     return L
 
 
@@ -277,3 +286,36 @@ def coli_moe_check(workspace, clear=True, stream=None):
     if st not in (COLI_OK, COLI_ETIMEOUT):
         raise ColiError("coli_moe_check", st)
     return flags.value
+
+
+def coli_usage_engine_id(engine):
+    """32-bit FNV-1a hash of an engine name (the usage history's identity field)."""
+    return int(lib.coli_usage_engine_id(engine.encode()))
+
+
+def _host_counts(counts):
+    import numpy as np
+    a = counts.detach().cpu().numpy() if isinstance(counts, torch.Tensor) else counts
+    return np.ascontiguousarray(a, dtype=np.uint32)
+
+
+def coli_usage_save(path, counts, engine, decay=1.0):
+    """Write route counts [n_layers, n_experts] (torch or numpy, any device) as a
+    usage history file; see coli.h."""
+    a = _host_counts(counts)
+    L, E = a.shape
+    _check("coli_usage_save", lib.coli_usage_save(os.fsencode(path), a.ctypes.data, L, E,
+                                                  engine.encode(), decay))
+
+
+def coli_usage_load(path, n_layers, n_experts, engine, trusted=False, counts=None):
+    """Read a usage history into counts (uint32 numpy [n_layers, n_experts], added to
+    ``counts`` if given).  Returns (counts, records added); raises ColiError if refused."""
+    import numpy as np
+    a = np.zeros((n_layers, n_experts), np.uint32) if counts is None else counts
+    assert a.dtype == np.uint32 and a.flags.c_contiguous and a.shape == (n_layers, n_experts)
+    n = C.c_int64(0)
+    _check("coli_usage_load", lib.coli_usage_load(os.fsencode(path), a.ctypes.data, n_layers,
+                                                  n_experts, engine.encode(), int(trusted),
+                                                  C.byref(n)))
+    return a, n.value

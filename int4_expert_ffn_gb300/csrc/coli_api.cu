@@ -200,6 +200,8 @@ const char *coli_status_str(int status) {
     case COLI_ETIMEOUT: return "device-side wait timed out";
     case COLI_ENOMEM: return "workspace too small";
     case COLI_EUNSUPPORTED: return "unsupported configuration";
+    case COLI_EIO: return "file I/O failed";
+    case COLI_EREFUSED: return "usage history of another model or format";
     default: return "unknown status";
   }
 }
