@@ -156,3 +156,29 @@ def test_bad_arguments_and_missing_file(coli, tmp_path):
     assert lib.coli_usage_load(os.fsencode(str(tmp_path / "none")), out.ctypes.data, 2, 4, b"e",
                                0, None) == coli.COLI_EIO
     assert coli._status_str(coli.COLI_EREFUSED).startswith("usage history")
+
+
+@pytest.mark.gpu
+def test_route_counts_of_a_stack_roundtrip(coli, tmp_path):
+    """The per-(layer, expert) counts of a GPU stack call, kept in a history file."""
+    import dataclasses
+    import torch
+    from int4_expert_ffn_gb300 import synth
+    from helpers import Layer
+    shape = dataclasses.replace(synth.TINY, layers=2, tokens=3)
+    layers = [Layer(shape, l, 0) for l in range(2)]
+    gp = [ly.gpu() for ly in layers]
+    c = coli
+    desc = c.MoEDesc(shape.hidden, shape.ffn, shape.experts, shape.shared, 3, c.COLI_F32,
+                     c.COLI_F32)
+    ws = c.new_workspace(desc, shape.top_k)
+    counts = torch.zeros((2, shape.experts), dtype=torch.int32, device="cuda")
+    c.coli_moe_stack_forward(desc, shape.top_k, 2, synth.tokens(shape).cuda(),
+                             torch.cat([g[2] for g in gp]), torch.cat([g[0] for g in gp]),
+                             torch.cat([g[1] for g in gp]), ws, route_counts=counts)
+    host = counts.cpu().numpy().astype(np.uint32)
+    assert host.sum() == 2 * 3 * shape.top_k
+    p = tmp_path / ".coli_usage"
+    c.coli_usage_save(str(p), counts, "int4_expert_ffn_gb300")
+    back, n = c.coli_usage_load(str(p), 2, shape.experts, "int4_expert_ffn_gb300")
+    assert np.array_equal(back, host) and n == int((host > 0).sum())
