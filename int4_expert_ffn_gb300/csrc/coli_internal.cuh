@@ -72,7 +72,7 @@ struct GuSmem {
 };
 // Shared-memory plan of k_down.
 struct DnSmem {
-  size_t act, routes, acc, xn, wr, ring, red, planes, total;
+  size_t act, routes, acc, xn, wr, ring, red, total;
 };
 // Shared-memory plan of k_down_multi.
 struct DmSmem {
@@ -132,8 +132,6 @@ struct Dec2Args {
   int dn_slot_bytes;
   int wr_bf16;              // the router (and its rows in k_down's shared memory) is bf16
   int chain;                // a next layer follows (k_down forms its router partials)
-  int dn_slots;             // token slots whose planes fit in shared memory at once
-  int dn_batch;             // experts whose partial sums fit in shared memory at once
   int dm_nw;                // warps of k_down_multi
   int dm_slots_pipe;        // depth of each warp's cp.async pipeline
   int dm_cap;               // h rows whose planes fit in k_down_multi's shared memory

@@ -1650,8 +1650,7 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
   // routing scratch: the T = 1 kernel's ring, the several-token kernel's plane area
   a.gu_route_fits = gu_route_smem(T, E, k).total <=
                     (T == 1 ? (size_t)a.gu_nw * a.gu_slots * a.gu_slot_bytes : g.total - g.xpl);
-  // ---- down: dn_nw warps with dn_slots_pipe-deep cp.async pipelines; expert
-  // batches of at most dn_batch experts and dn_slots token slots
+  // ---- down: dn_nw warps with dn_slots_pipe-deep cp.async pipelines
   a.dn_ncg = (F + kChunkCols - 1) / kChunkCols;
   a.dn_slot_bytes = slot_bytes(F);
   if (T > 1) return plan_down_multi(a);
@@ -1680,10 +1679,8 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
     dn_ok = true;
   }
   if (!dn_ok) return cudaErrorInvalidValue;
-  a.dn_slots = a.dn_batch = 0;
   d.ring = al128(o); o = d.ring + (size_t)a.dn_nw * a.dn_slots_pipe * a.dn_slot_bytes;
   d.red = al16(o); o = d.red + red_bytes;
-  d.planes = o;
   d.total = al16(o);
   a.dn = d;
   return cudaSuccess;
@@ -1703,12 +1700,11 @@ static cudaError_t plan_down_multi(Dec2Args &a) {
   d.acc = o; o = al16(o + (size_t)max_nr * T * 4);
   d.xn = o; o = al16(o + (size_t)T * max_nr * 4);
   d.wr = o; o = al16(o + (a.chain ? (size_t)E * max_nr * (a.wr_bf16 ? 2 : 4) : 0));
-  d.ring = d.red = d.planes = o;
+  d.ring = d.red = o;
   d.total = o;
   a.dn = d;
   a.dn_nw = 16;
   a.dn_slots_pipe = 2;
-  a.dn_slots = a.dn_batch = 0;
   // k_down_multi: warps x slots, then as many h rows' planes as fit (at least
   // one expert's tokens plus one more, else planes per task)
   DmSmem m{};
