@@ -515,16 +515,18 @@ __device__ void route_if_last(const Dec2Args &a, const LayerPtrs &lp, uint8_t *s
 }
 
 // ---------------------------------------------------------------------------
-// gate/up: the CTA owns a contiguous range of rows in the flattened (used
-// expert, f) space; a row is gate row f and up row f of that expert.  Work is
+// gate/up (one token; several tokens: k_gateup_multi below): the CTA owns a
+// contiguous range of rows in the flattened (used expert, f) space, after
+// routing the layer itself (gu_lists); a row is gate row f and up row f of
+// that expert.  Work is
 // cut into tasks of (4-row group, 1024-column chunk).  Each warp runs its
 // tasks (a round robin over the warps) through a private multi-stage
 // cp.async pipeline, gu_slots - 1 tasks ahead: lane l copies the 16-byte
 // slice of each of the 8 rows that it consumes, and the warp copies the 8
 // rows' scales of the chunk, so tens of KB per SM stay in flight without
-// holding registers.  Partial sums per (row, token, chunk) go to shared
-// memory; rows are finalised in batches of gu_rows into h = silu(g) * u *
-// gate, written to every replica.
+// holding registers.  Partial sums per (row, chunk) go to shared memory;
+// rows are finalised in batches of gu_rows into h = silu(g) * u * gate,
+// written to every replica.
 
 // slot: weights [8 rows][32 lanes][16 B] | scales: [8 rows][16 groups] f32 when
 // the row's scales are 16-byte aligned (K % 256 == 0), else [8 rows][32 lanes]
@@ -1070,16 +1072,17 @@ __global__ void __launch_bounds__(kGuMultiMaxThreads) k_gateup_multi(Dec2Args a)
 }
 
 // ---------------------------------------------------------------------------
-// down: each CTA owns output rows [dh0, dh1) of every used expert's down
-// matrix.  Work is cut into tasks of (expert, 8-row group, 1024-column chunk)
-// that run, like the gate/up tasks, through each warp's cp.async pipeline
-// (the same slot layout: 8 rows x 16 bytes per lane, plus scales).  Experts
-// are taken in batches whose slots' activation planes fit in shared memory;
-// a task leaves the partial sum of each (row, token, chunk) in the batch's
-// reduction area, and after the batch every (row, token) adds its experts'
-// and chunks' partial sums, in a fixed order, to its accumulator.  The
-// combine then writes out (with the residual), layer_out, the x replicas,
-// and leaves the new residual-stream rows in s_xn [T][nr].
+// down: each CTA owns output rows [dh0, dh1) (one token: of every used
+// expert's down matrix).  Work is cut into tasks of (expert, 8-row group,
+// 1024-column chunk) that run, like the gate/up tasks, through each warp's
+// cp.async pipeline (the same slot layout: 8 rows x 16 bytes per lane, plus
+// scales); each warp takes a contiguous run of tasks and quantises the h slice
+// of its task's expert in registers.  A task leaves the partial sum of each
+// (row, chunk) in shared memory, and every row then adds its experts' and
+// chunks' partial sums in a fixed order.  With several tokens k_down_multi
+// has already produced the per-slot outputs y and this kernel only adds each
+// token's slots.  The combine then writes out (with the residual), layer_out,
+// the x replicas, and leaves the new residual-stream rows in s_xn [T][nr].
 
 struct DnTask {
   int a, gi, cg;     // expert (index into the used list), 8-row group, chunk
