@@ -58,6 +58,12 @@ SMALL = [
     (1088, 1088, 9, 1, 2, 5),    # not a multiple of 1024: ragged chunk
     (256, 512, 8, 1, 2, 37),     # three 16-token passes, ragged tail
     (2048, 1024, 64, 0, 8, 8),
+    (16384, 64, 4, 1, 2, 1),     # the largest hidden size: 16 chunks per gate/up row
+    (64, 16384, 3, 0, 1, 2),     # the largest FFN width: 16 chunks per down row
+    (256, 256, 1, 0, 1, 3),      # a single routed expert
+    (128, 128, 4, 8, 2, 2),      # the most shared experts
+    (64, 64, 64, 0, 64, 1),      # k = 64 (the largest top-k): the rank top-k in the routing
+    (192, 128, 40, 1, 33, 4),    # k = 33 > 32, several tokens
 ]
 
 
