@@ -14,11 +14,11 @@
 //   k_pgemm<MODE>
 //               token-sorted grouped GEMM on tcgen05 tensor cores: 128-row
 //               m-tiles of one expert's routes x 256-column n-tiles, K in
-//               steps of 64 (one scale group).  Four producer warps stage the
+//               steps of 64 (one scale group).  Eight producer warps stage the
 //               activation rows with cp.async and dequantise the int4 weight
 //               tile to fp16 into 128-byte-swizzled shared memory; one thread
-//               issues tcgen05.mma (kind::f16, f32 accumulator in TMEM); the
-//               same four warps drain TMEM in the epilogue:
+//               issues tcgen05.mma (kind::f16, f32 accumulator in TMEM); four
+//               epilogue warps drain TMEM:
 //                 gate/up: h = silu(g) * u * gate  -> fp16 [route][F]
 //                 down:    y                        -> f32  [route][H]
 //   k_pcombine  out[t] = sum_j y[route(t, j)] + sum_s y[shared s, t] (+ residual)
@@ -47,11 +47,19 @@ constexpr int kEpilogueThreads = 32 * kEpilogueWarps;
 constexpr int kGemmThreads = 32 * (kProducerWarps + 1 + kEpilogueWarps);
 constexpr int kATileBytes = kBM * kBK * 2;     // 16 KB
 constexpr int kBTileBytes = kBN * kBK * 2;     // 32 KB
-constexpr int kRawBytes = kBN * (kBK / 2) + kBN * 4;   // 8 KB nibbles + 1 KB scales
+// Raw slot: the k-tile's 32 bytes of nibbles of every weight row as 16-byte
+// halves, [2][kProducerThreads] in copy order, then one scale per half.
+constexpr int kRawHalves = 2 * kProducerThreads;
+constexpr int kRawNibbleBytes = kRawHalves * 16;        // 8 KB
+constexpr int kRawBytes = kRawNibbleBytes + kRawHalves * 4;   // + 2 KB scales
+constexpr int kARowPasses = kBM * 8 / kProducerThreads;        // 128-byte rows: 8 threads each
 constexpr int kTableBytes = 2 * (kMaxExperts + kMaxShared + 1) * 4;   // item_begin, offsets
 constexpr int kGemmSmem = kNA * kATileBytes + kNB * kBTileBytes + kNR * kRawBytes + kTableBytes + 2048;
 static_assert(kNR > kDist, "a raw slot is refilled only after its dequantisation");
-static_assert(kProducerThreads == kBN, "one B row per producer thread");
+static_assert(kProducerThreads == kBN, "a thread pair per B row, two rows per pair");
+static_assert(kRawHalves == 2 * kBN && kARowPasses * kProducerThreads == 8 * kBM,
+              "copy shares of the producers");
+static_assert(kGemmSmem <= 232448, "shared memory of one block");
 
 enum GemmMode : int { kModeGateUp = 0, kModeDown = 1 };
 
@@ -435,54 +443,67 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
   const int n_ticks = my_items * nk;         // this CTA's k-tiles over all its items
 
   if (warp < kProducerWarps) {
-    // ---- producers: tick t issues the copies of k-tile t (A rows, raw B row)
-    // and dequantises k-tile t - kDist into the B ring
-    const int th = threadIdx.x;                      // B row th; A row th % 128
-    const int ar = th & (kBM - 1), ac0 = 4 * (th >> 7);
+    // ---- producers: tick t issues the copies of k-tile t (A rows, raw B
+    // rows) and dequantises k-tile t - kDist into the B ring.  Copies are laid
+    // out so that each warp instruction reads whole lines: for A, 8 threads
+    // per 128-byte activation row (rows th/8 + 32 j); for B, a thread pair per
+    // 32-byte weight sector (rows th/2 and th/2 + 128, half th % 2).  A thread
+    // dequantises only the halves it copied itself, so its own cp.async wait
+    // is the only one it needs.  A rows past the item's last route are left
+    // as they are: they reach only accumulator rows that are never stored.
+    const int th = threadIdx.x;
+    const int a_chunk = th & 7, a_row0 = th >> 3;
+    const int b_half = th & 1, b_row0 = th >> 1;
     Item it{};
-    const __half *a_src = nullptr;
-    bool a_ok = false;
-    const uint8_t *b_src = nullptr;
-    const float *b_sc = nullptr;
+    const __half *a_src[kARowPasses];
+    bool a_ok[kARowPasses];
+    const uint8_t *b_src[2];
+    const float *b_sc[2];
     bool ok = true;
     int item = 0, kt = 0;                  // k-tile t = item * nk + kt
     for (int t = 0; t < n_ticks + kDist && ok; ++t) {
       if (t < n_ticks) {
         if (kt == 0) {
           it = decode_item(s_begin, s_off, p.n_groups, blockIdx.x + item * gridDim.x, n_ntiles);
-          a_ok = ar < it.rows;
-          if (a_ok)
-            a_src = MODE == kModeGateUp ? p.x16 + (int64_t)p.route_tok[it.p0 + ar] * H
-                                        : p.h16 + (int64_t)(it.p0 + ar) * F;
+#pragma unroll
+          for (int j = 0; j < kARowPasses; ++j) {
+            const int r = a_row0 + 32 * j;
+            a_ok[j] = r < it.rows;
+            a_src[j] = nullptr;
+            if (a_ok[j])
+              a_src[j] = MODE == kModeGateUp ? p.x16 + (int64_t)p.route_tok[it.p0 + r] * H
+                                             : p.h16 + (int64_t)(it.p0 + r) * F;
+          }
           const uint8_t *pk = p.packed + (int64_t)it.e * p.eb;
           const float *sc = p.scales + (int64_t)it.e * p.es;
-          if (MODE == kModeGateUp) {
-            const int f = it.ni * (kBN / 2) + (th & 127);
-            const int64_t mat = th < 128 ? 0 : 1;      // gate rows, then up rows
-            b_src = pk + mat * (int64_t)F * (H / 2) + (int64_t)f * (H / 2);
-            b_sc = sc + mat * (int64_t)F * (H / kGroup) + (int64_t)f * (H / kGroup);
-          } else {
-            const int hr = it.ni * kBN + th;
-            b_src = pk + (int64_t)F * H + (int64_t)hr * (F / 2);
-            b_sc = sc + (int64_t)2 * F * (H / kGroup) + (int64_t)hr * (F / kGroup);
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            if (MODE == kModeGateUp) {
+              // B rows 0..127 are gate rows, 128..255 the up rows of the same f
+              const int f = it.ni * (kBN / 2) + b_row0;
+              const int64_t mat = j;
+              b_src[j] = pk + mat * (int64_t)F * (H / 2) + (int64_t)f * (H / 2);
+              b_sc[j] = sc + mat * (int64_t)F * (H / kGroup) + (int64_t)f * (H / kGroup);
+            } else {
+              const int hr = it.ni * kBN + b_row0 + 128 * j;
+              b_src[j] = pk + (int64_t)F * H + (int64_t)hr * (F / 2);
+              b_sc[j] = sc + (int64_t)2 * F * (H / kGroup) + (int64_t)hr * (F / kGroup);
+            }
           }
         }
         const int sa = t % kNA;
         if (!mbar_wait(&a_empty[sa], ((t / kNA) & 1) ^ 1)) { ok = false; break; }
         const uint32_t a_dst = smem_u32(a_ring + sa * kATileBytes);
         const int k0 = kt * kBK;
-        if (a_ok) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) cp16(a_dst + sw128_off(ar, ac0 + c), a_src + k0 + 8 * (ac0 + c));
-        } else {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) st_shared_zero16(a_dst + sw128_off(ar, ac0 + c));
-        }
-        // raw row th: first 16 bytes at [th], second at [kBN + th] (conflict-free)
+        for (int j = 0; j < kARowPasses; ++j)
+          if (a_ok[j]) cp16(a_dst + sw128_off(a_row0 + 32 * j, a_chunk), a_src[j] + k0 + 8 * a_chunk);
         uint8_t *raw = r_ring + (t % kNR) * kRawBytes;
-        cp16(smem_u32(raw + th * 16), b_src + k0 / 2);
-        cp16(smem_u32(raw + (kBN + th) * 16), b_src + k0 / 2 + 16);
-        cp4(smem_u32(raw + kBN * 32 + th * 4), b_sc + kt);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          cp16(smem_u32(raw + (j * kProducerThreads + th) * 16), b_src[j] + k0 / 2 + 16 * b_half);
+          cp4(smem_u32(raw + kRawNibbleBytes + (j * kProducerThreads + th) * 4), b_sc[j] + kt);
+        }
         if (++kt == nk) { kt = 0; ++item; }
       }
       cp_commit();
@@ -492,17 +513,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
       const int sb = c % kNB;
       if (!mbar_wait(&b_empty[sb], ((c / kNB) & 1) ^ 1)) { ok = false; break; }
       const uint8_t *raw = r_ring + (c % kNR) * kRawBytes;
-      const uint4 w0 = *(const uint4 *)(raw + th * 16);
-      const uint4 w1 = *(const uint4 *)(raw + (kBN + th) * 16);
-      const __half2 s2 = __float2half2_rn(*(const float *)(raw + kBN * 32 + th * 4));
-      const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
       const uint32_t b_dst = smem_u32(b_ring + sb * kBTileBytes);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t o[8];
-        dequant8(wd[2 * q], wd[2 * q + 1], s2, o);
-        st_shared16(b_dst + sw128_off(th, 2 * q), o[0], o[1], o[2], o[3]);
-        st_shared16(b_dst + sw128_off(th, 2 * q + 1), o[4], o[5], o[6], o[7]);
+      for (int j = 0; j < 2; ++j) {
+        const int slot = j * kProducerThreads + th;
+        const uint4 w = *(const uint4 *)(raw + slot * 16);
+        const __half2 s2 = __float2half2_rn(*(const float *)(raw + kRawNibbleBytes + slot * 4));
+        const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+        const int row = b_row0 + 128 * j;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          // columns 32 b_half + 16 q .. + 15: 16-byte chunks 4 b_half + 2 q, + 1
+          uint32_t o[8];
+          dequant8(wd[2 * q], wd[2 * q + 1], s2, o);
+          st_shared16(b_dst + sw128_off(row, 4 * b_half + 2 * q), o[0], o[1], o[2], o[3]);
+          st_shared16(b_dst + sw128_off(row, 4 * b_half + 2 * q + 1), o[4], o[5], o[6], o[7]);
+        }
       }
       fence_proxy_async();         // A (landed copies) and B of k-tile c -> tensor core reads
       mbar_arrive(&full[sb]);
