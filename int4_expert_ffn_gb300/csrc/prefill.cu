@@ -153,9 +153,6 @@ template <int N>
 __device__ __forceinline__ void cp_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-__device__ __forceinline__ void st_shared_zero16(uint32_t dst) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0) : "memory");
-}
 __device__ __forceinline__ void st_shared16(uint32_t dst, uint32_t a, uint32_t b, uint32_t c,
                                             uint32_t d) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(a), "r"(b), "r"(c),
@@ -215,42 +212,86 @@ __device__ __forceinline__ Item decode_item(const int *begin, const int *off, in
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// Activations to fp16 (exact for bf16 inputs inside the fp16 range).
+// Activations to fp16 (exact for bf16 inputs inside the fp16 range), 8
+// elements (one 16-byte store) per thread and step; n is a multiple of 8.
+
+__device__ __forceinline__ void load8(const __nv_bfloat16 *src, float (&v)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4 *>(src);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    v[2 * j] = __uint_as_float(w[j] << 16);
+    v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  }
+}
+__device__ __forceinline__ void load8(const float *src, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4 *>(src);
+  const float4 b = *reinterpret_cast<const float4 *>(src + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
 
 template <typename XT>
 __global__ void k_x16(const XT *x, __half *x16, int64_t n) {
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (int64_t)gridDim.x * blockDim.x)
-    x16[i] = __float2half_rn(to_f32(x[i]));
+  for (int64_t i = 8 * ((int64_t)blockIdx.x * blockDim.x + threadIdx.x); i < n;
+       i += 8 * (int64_t)gridDim.x * blockDim.x) {
+    float v[8];
+    load8(x + i, v);
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __half2 h = __floats2half2_rn(v[2 * j], v[2 * j + 1]);
+      o[j] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    *reinterpret_cast<uint4 *>(x16 + i) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
 }
 
 // ---------------------------------------------------------------------------
 // Router logits [T][E] = x [T][H] . Wr [E][H]^T, f32 accumulation.  64 x 64
-// tiles, K in steps of 32 through shared memory; 256 threads x (4 x 4).
+// tiles, K in steps of 32 through shared memory (stored k-major, so each
+// thread reads its 4 x 4 operands as two float4); 256 threads x (4 x 4), each
+// output a sequential fmaf chain over k.  Thread (r, q) fetches 8 consecutive
+// k of row r for the next step into registers while the current one computes.
 
 template <typename XT, typename WT>
 __global__ void __launch_bounds__(256) k_logits(const XT *x, const WT *wr, float *logits, int T,
                                                 int H, int E) {
-  __shared__ float sx[32][65];
-  __shared__ float sw[32][65];
+  __shared__ __align__(16) float sx[32][68];
+  __shared__ __align__(16) float sw[32][68];
   const int t0 = blockIdx.y * 64, e0 = blockIdx.x * 64;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int lr = threadIdx.x & 63, lq = threadIdx.x >> 6;     // fetch: row lr, k 8 lq .. + 7
+  const bool x_ok = t0 + lr < T, w_ok = e0 + lr < E;
+  const XT *xs = x + (size_t)(x_ok ? t0 + lr : 0) * H + 8 * lq;
+  const WT *ws = wr + (size_t)(w_ok ? e0 + lr : 0) * H + 8 * lq;
+  float rx[8], rw[8];
+  auto fetch = [&](int k0) {
+    if (x_ok) load8(xs + k0, rx);
+    else
+#pragma unroll
+      for (int j = 0; j < 8; ++j) rx[j] = 0.0f;
+    if (w_ok) load8(ws + k0, rw);
+    else
+#pragma unroll
+      for (int j = 0; j < 8; ++j) rw[j] = 0.0f;
+  };
   float acc[4][4] = {};
+  fetch(0);
   for (int k0 = 0; k0 < H; k0 += 32) {
-    for (int i = threadIdx.x; i < 64 * 32; i += 256) {
-      const int r = i >> 5, kk = i & 31;
-      sx[kk][r] = (t0 + r < T) ? to_f32(x[(size_t)(t0 + r) * H + k0 + kk]) : 0.0f;
-      sw[kk][r] = (e0 + r < E) ? to_f32(wr[(size_t)(e0 + r) * H + k0 + kk]) : 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      sx[8 * lq + j][lr] = rx[j];
+      sw[8 * lq + j][lr] = rw[j];
     }
     __syncthreads();
+    if (k0 + 32 < H) fetch(k0 + 32);
 #pragma unroll 8
     for (int kk = 0; kk < 32; ++kk) {
-      float a[4], b[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        a[i] = sx[kk][ty * 4 + i];
-        b[i] = sw[kk][tx * 4 + i];
-      }
+      const float4 a4 = *reinterpret_cast<const float4 *>(&sx[kk][ty * 4]);
+      const float4 b4 = *reinterpret_cast<const float4 *>(&sw[kk][tx * 4]);
+      const float a[4] = {a4.x, a4.y, a4.z, a4.w};
+      const float b[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -357,21 +398,25 @@ __global__ void __launch_bounds__(1024) k_gscan(PrefillArgs p, int n_blocks) {
 
 __global__ void __launch_bounds__(256) k_gscatter(PrefillArgs p) {
   extern __shared__ __align__(16) uint8_t smem[];
-  int *base = (int *)smem;                  // [E] next position of each expert in this block
   const int E = p.E, k = p.k, T = p.T;
+  int *base = (int *)smem;                  // [E] next position of each expert in this block
+  int *s_idx = base + E;                    // [kGroupTokens * k] the block's expert choices
   const int t0 = blockIdx.x * kGroupTokens;
   const int t1 = (t0 + kGroupTokens < T) ? t0 + kGroupTokens : T;
+  const int n = (t1 - t0) * k;
   for (int e = threadIdx.x; e < E; e += blockDim.x)
     base[e] = p.offsets[e] + p.hist[(size_t)blockIdx.x * E + e];
+  for (int i = threadIdx.x; i < n; i += blockDim.x) s_idx[i] = p.idx[(size_t)t0 * k + i];
   __syncthreads();
   // one thread per expert walks the block's routes in (token, slot) order
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int pos = base[e];
-    for (int i = t0 * k; i < t1 * k; ++i)
-      if (p.idx[i] == e) {
-        p.route_tok[pos] = i / k;
-        p.route_gate[pos] = p.gates[i];
-        p.inv[i] = pos;
+    for (int i = 0; i < n; ++i)
+      if (s_idx[i] == e) {
+        const int g = t0 * k + i;
+        p.route_tok[pos] = g / k;
+        p.route_gate[pos] = p.gates[g];
+        p.inv[g] = pos;
         ++pos;
       }
   }
@@ -700,7 +745,7 @@ cudaError_t launch_prefill(const PrefillArgs &p, int x_dtype, int wr_dtype, cuda
   const int nsm = num_sms();
   // activations -> fp16
   const int64_t nx = (int64_t)T * H;
-  const int gx = (int)((nx + 255) / 256 < 4 * nsm ? (nx + 255) / 256 : 4 * nsm);
+  const int gx = (int)((nx / 8 + 255) / 256 < 4 * nsm ? (nx / 8 + 255) / 256 : 4 * nsm);
   if (x_dtype == COLI_BF16) k_x16<__nv_bfloat16><<<gx, 256, 0, s>>>((const __nv_bfloat16 *)p.x, p.x16, nx);
   else k_x16<float><<<gx, 256, 0, s>>>((const float *)p.x, p.x16, nx);
   // router logits
@@ -722,7 +767,9 @@ cudaError_t launch_prefill(const PrefillArgs &p, int x_dtype, int wr_dtype, cuda
   const int nb = (T + kGroupTokens - 1) / kGroupTokens;
   k_gcount<<<nb, 256, (size_t)E * 4, s>>>(p);
   k_gscan<<<1, 1024, 0, s>>>(p, nb);
-  k_gscatter<<<nb, 256, (size_t)E * 4, s>>>(p);
+  const size_t gs_smem = (size_t)(E + kGroupTokens * k) * 4;
+  if ((e = set_smem(k_gscatter, gs_smem)) != cudaSuccess) return e;
+  k_gscatter<<<nb, 256, gs_smem, s>>>(p);
   // GEMMs
   if ((e = set_smem(k_pgemm<kModeGateUp>, kGemmSmem)) != cudaSuccess) return e;
   if ((e = set_smem(k_pgemm<kModeDown>, kGemmSmem)) != cudaSuccess) return e;
