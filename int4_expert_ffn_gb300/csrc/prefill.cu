@@ -400,25 +400,39 @@ __global__ void __launch_bounds__(256) k_gscatter(PrefillArgs p) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int E = p.E, k = p.k, T = p.T;
   int *base = (int *)smem;                  // [E] next position of each expert in this block
-  int *s_idx = base + E;                    // [kGroupTokens * k] the block's expert choices
   const int t0 = blockIdx.x * kGroupTokens;
   const int t1 = (t0 + kGroupTokens < T) ? t0 + kGroupTokens : T;
   const int n = (t1 - t0) * k;
   for (int e = threadIdx.x; e < E; e += blockDim.x)
     base[e] = p.offsets[e] + p.hist[(size_t)blockIdx.x * E + e];
-  for (int i = threadIdx.x; i < n; i += blockDim.x) s_idx[i] = p.idx[(size_t)t0 * k + i];
   __syncthreads();
-  // one thread per expert walks the block's routes in (token, slot) order
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int pos = base[e];
-    for (int i = 0; i < n; ++i)
-      if (s_idx[i] == e) {
-        const int g = t0 * k + i;
-        p.route_tok[pos] = g / k;
-        p.route_gate[pos] = p.gates[g];
-        p.inv[g] = pos;
-        ++pos;
+  // The block's routes in (token, slot) order, blockDim.x at a time: a route's
+  // place is its expert's next position plus the number of earlier routes of
+  // the same expert, counted inside the warp by a match and across warps by
+  // letting the warps take their experts' positions one after another.
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, n_warps = blockDim.x >> 5;
+  const unsigned lower = (1u << lane) - 1u;
+  for (int c0 = 0; c0 < n; c0 += blockDim.x) {
+    const int i = c0 + threadIdx.x;
+    const int g = t0 * k + i;
+    const int e = i < n ? p.idx[g] : -1;
+    const unsigned same = __match_any_sync(~0u, e);
+    const int leader = __ffs(same) - 1;
+    int first = 0;
+    for (int w = 0; w < n_warps; ++w) {
+      if (warp == w && lane == leader && e >= 0) {
+        first = base[e];
+        base[e] = first + __popc(same);
       }
+      __syncthreads();
+    }
+    first = __shfl_sync(~0u, first, leader);
+    if (e >= 0) {
+      const int pos = first + __popc(same & lower);
+      p.route_tok[pos] = g / k;
+      p.route_gate[pos] = p.gates[g];
+      p.inv[g] = pos;
+    }
   }
   // shared experts: every token, in order
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.S * T; i += gridDim.x * blockDim.x) {
@@ -767,9 +781,7 @@ cudaError_t launch_prefill(const PrefillArgs &p, int x_dtype, int wr_dtype, cuda
   const int nb = (T + kGroupTokens - 1) / kGroupTokens;
   k_gcount<<<nb, 256, (size_t)E * 4, s>>>(p);
   k_gscan<<<1, 1024, 0, s>>>(p, nb);
-  const size_t gs_smem = (size_t)(E + kGroupTokens * k) * 4;
-  if ((e = set_smem(k_gscatter, gs_smem)) != cudaSuccess) return e;
-  k_gscatter<<<nb, 256, gs_smem, s>>>(p);
+  k_gscatter<<<nb, 256, (size_t)E * 4, s>>>(p);
   // GEMMs
   if ((e = set_smem(k_pgemm<kModeGateUp>, kGemmSmem)) != cudaSuccess) return e;
   if ((e = set_smem(k_pgemm<kModeDown>, kGemmSmem)) != cudaSuccess) return e;
