@@ -39,7 +39,7 @@ constexpr int kNA = 5;            // A ring (fp16 activation tiles)
 constexpr int kNB = 3;            // B ring (dequantised fp16 weight tiles)
 constexpr int kNR = 4;            // raw ring (int4 rows + scales as copied)
 constexpr int kDist = 3;          // copies run this many k-tiles ahead of the dequantisation
-constexpr int kProducerWarps = 8; // one B row per producer thread
+constexpr int kProducerWarps = 8; // two weight-row halves and four activation pieces per thread
 constexpr int kProducerThreads = 32 * kProducerWarps;
 constexpr int kMmaWarp = kProducerWarps;
 constexpr int kEpilogueWarps = 4;
@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *a_ring = smem;                                  // kNA x 16 KB (fp16, swizzled)
   uint8_t *b_ring = a_ring + kNA * kATileBytes;            // kNB x 32 KB (fp16, swizzled)
-  uint8_t *r_ring = b_ring + kNB * kBTileBytes;            // kNR x raw int4 rows + scales
+  uint8_t *r_ring = b_ring + kNB * kBTileBytes;            // kNR x raw nibble halves + scales
   uint64_t *full = (uint64_t *)(r_ring + kNR * kRawBytes);
   uint64_t *a_empty = full + kNB;
   uint64_t *b_empty = a_empty + kNA;
