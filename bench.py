@@ -1,13 +1,15 @@
 """Benchmark of the routed-MoE decode forward over int4-grouped experts on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl coli|reference]
-                    [--workload olmoe_decode|glm_decode_b1|glm_decode_b8|quant]
+                    [--workload glm_decode_b1|glm_decode_b8|olmoe_decode|glm_prefill|quant]
 
-Default workload: the OLMoE-like decode stack -- 16 MoE layers, hidden 2048, 64
-experts of FFN width 1024, top-8, no shared expert, int4-grouped g64 experts
-quantised from N(0, 0.02) bf16, bf16 router, batch 1 token of fresh N(0,1)
-input per step.  One step = one token through all 16 layers (router, top-k,
-route counts, batch union, gate/up + SwiGLU, down, combine, residual).
+Default workload: GLM-like decode layers at batch 1 -- 8 MoE layers, hidden
+6144, 256 routed experts of FFN width 2048 plus 1 shared expert, top-8,
+int4-grouped g64 experts quantised from N(0, 0.02) bf16 (43.7 GB resident),
+bf16 router.  One step = one token through all 8 layers (router, top-k, route
+counts, batch union, gate/up + SwiGLU, down, combine, shared expert); each
+layer takes its own fresh N(0,1) input.  The timed region is the median of
+--repeats windows of K steps.
 
 Prints one JSON line (rank 0).  With torchrun (N > 1) every rank runs an
 independent replica on its own GPU (the decode path has no exchange step);
@@ -32,16 +34,13 @@ METRIC = "MoE decode tokens/s and int4 expert-weight GB/s vs GB300 HBM peak"
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
 # each kernel from an ncu capture of the current kernel build, keyed by
-# workload and kernel; absent until such a capture exists.  The profiles/
-# summary it comes from is named beside each value.
+# workload and kernel; absent (null in the line) until such a capture exists
+# or once the kernel has changed since.  Batch 1: the per-layer launch is the
+# same in a 1- or 2-layer capture as in the full stack.
 NCU_TRAFFIC = {
-    # profiles/k_gateup_k_down_olmoe_2layer.md (batch 1: the same launch per layer
-    # as the 16-layer stack; cold-cache capture)
     "olmoe_decode": {"k_gateup": 19016192, "k_down": 10036736},
-    # profiles/k_gateup_k_down_glm_layer.md
-    "glm_decode_b1": {"k_gateup": 127681280 + 3630336, "k_down": 64375808 + 343296},
-    # profiles/k_gateup_multi_k_down_multi_glm_b8_layer.md (k_gateup is the several-token
-    # kernel k_gateup_multi; its experts per launch vary with the routing)
+    # the several-token kernel k_gateup_multi; its experts per launch vary with
+    # the routing
     "glm_decode_b8": {"k_gateup": 879500288 + 7344384},
 }
 
@@ -440,32 +439,37 @@ def run_decode(args, shape, dev, world, rank):
             for i in range(warmup):
                 graphs[i].replay()
             stream.synchronize()
-    wl.counts.zero_()
     sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
                            else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[0]))
     sampler.start()
     time.sleep(0.3)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
+    windows = []
     t0 = time.time()
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for i in range(warmup, warmup + steps):
-            graphs[i].replay()
-        ev1.record(stream)
-    torch.cuda.synchronize()
+    for _ in range(args.repeats):
+        # each window: exactly K steps, barrier and synchronize on both sides
+        wl.counts.zero_()
+        barrier(world)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for i in range(warmup, warmup + steps):
+                graphs[i].replay()
+            ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        windows.append(ev0.elapsed_time(ev1))
     t1 = time.time()
-    barrier(world)
     time.sleep(0.15)
     sampler.stop()
-    ms = ev0.elapsed_time(ev1)
+    ms = statistics.median(windows)
     ms_max = max_over_ranks(ms, world, dev)
     tokens = steps * shape.tokens
     alg_bytes, n_unique = wl.algorithmic_bytes(list(range(warmup, warmup + steps)))
     res = {
         "tokens_per_rank": tokens,
         "ms": ms_max,
+        "windows_ms": [round(w, 4) for w in windows],
         "alg_bytes": alg_bytes,
         "unique_experts": n_unique,
         "clocks": sampler.summary(t0, t1),
@@ -567,12 +571,43 @@ def run_e2e(wl, args, dev, world, stream):
 # CPU baseline: the oracle on a bounded sample of the same workload
 
 
-def oracle_baseline(shape, dev, budget_s=15.0, seed=0):
-    """Time the oracle on layer 0 of the stack for as many fresh tokens as fit
-    in ~budget_s of CPU work; scale to tokens/s of the full stack."""
+def cpu_model():
+    """Name of the host CPU: lscpu's model name, else /proc/cpuinfo's (x86
+    "model name", Arm "CPU implementer" / "CPU part")."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    info = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    info.setdefault(k.strip().lower(), v.strip())
+    except OSError:
+        return "unknown"
+    if "model name" in info:
+        return info["model name"]
+    if "cpu part" in info:
+        return "arm implementer %s part %s" % (info.get("cpu implementer", "?"), info["cpu part"])
+    return "unknown"
+
+
+def oracle_baseline(shape, dev, budget_s=24.0, seed=0):
+    """Time the oracle (as it stands) on fresh tokens through layer 0 of the
+    workload and scale to tokens/s of the whole step (every layer has the
+    same shape and cost).  Two legs on the host cores: the single-threaded
+    build, one token at a time, and the OpenMP build over nproc threads, one
+    token per thread (each leg about budget_s / 2 of oracle time, at least one
+    batch).  Expert quantisation by the oracle is set-up, not timed."""
     import oracle as orc
     from int4_expert_ffn_gb300 import synth
     H, F, E, S, k = shape.hidden, shape.ffn, shape.experts, shape.shared, shape.top_k
+    nproc = os.cpu_count() or 1
     wr = synth.router_weights(shape, 0, seed, device=dev).double().cpu().numpy()
     eb = orc.expert_packed_bytes(H, F)
     es = orc.expert_scales(H, F)
@@ -581,35 +616,55 @@ def oracle_baseline(shape, dev, budget_s=15.0, seed=0):
     done = set()
 
     def materialise(experts):
-        for e in experts:
-            if e in done:
-                continue
-            ps, ss = [], []
-            for m in range(3):
-                w = synth.expert_matrix(shape, 0, e, m, seed, device=dev).float().cpu().numpy()
-                p, s = orc.quant_i4g(w)
-                ps.append(p.reshape(-1))
-                ss.append(s.reshape(-1))
-            packed[e * eb:(e + 1) * eb] = np.concatenate(ps)
-            scales[e * es:(e + 1) * es] = np.concatenate(ss)
-            done.add(e)
+        prev = orc.set_threads(nproc)
+        try:
+            for e in experts:
+                if e in done:
+                    continue
+                ps, ss = [], []
+                for m in range(3):
+                    w = synth.expert_matrix(shape, 0, e, m, seed, device=dev).float().cpu().numpy()
+                    p, s = orc.quant_i4g(w)
+                    ps.append(p.reshape(-1))
+                    ss.append(s.reshape(-1))
+                packed[e * eb:(e + 1) * eb] = np.concatenate(ps)
+                scales[e * es:(e + 1) * es] = np.concatenate(ss)
+                done.add(e)
+        finally:
+            orc.set_threads(prev)
 
     materialise(range(E, E + S))
-    n_tok, spent = 0, 0.0
-    while spent < budget_s and n_tok < 512:
-        x = synth.tokens(shape, seed, 10_000 + n_tok, device=dev).double().cpu().numpy()
-        lg = orc.router_logits(x, wr)
-        materialise(sorted({int(e) for row in lg for e in np.argsort(-row)[:k + 2]}))
-        t = time.perf_counter()
-        orc.moe_forward(x, wr, packed, scales, H, F, E, S, k)
-        spent += time.perf_counter() - t
-        n_tok += shape.tokens
-    per_token_layer = spent / n_tok
-    value = 1.0 / (per_token_layer * shape.layers)
-    return {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": "%d fresh tokens through layer 0 of the %d-layer stack (%.1f s of "
-                      "single-thread oracle time), scaled x%d layers"
-                      % (n_tok, shape.layers, spent, shape.layers)}
+    per_step_calls = shape.layers * shape.tokens   # token-layers per step
+    legs = {}
+    next_tok = 10_000
+    for name, threads, batch in (("single", 1, 1), ("nproc", nproc, nproc)):
+        n_tok, spent = 0, 0.0
+        while spent < budget_s / 2 and n_tok < 4 * batch + 64:
+            x = torch.cat([synth.tokens(shape, seed, next_tok + i, device=dev)[:1]
+                           for i in range(batch)]).double().cpu().numpy()
+            next_tok += batch
+            lg = orc.router_logits(x, wr)
+            materialise(sorted({int(e) for row in lg for e in np.argsort(-row)[:k + 2]}))
+            prev = orc.set_threads(threads)
+            try:
+                t = time.perf_counter()
+                orc.moe_forward(x, wr, packed, scales, H, F, E, S, k)
+                spent += time.perf_counter() - t
+            finally:
+                orc.set_threads(prev)
+            n_tok += batch
+        per_token_layer = spent / n_tok
+        legs[name] = {
+            "value": shape.tokens / (per_token_layer * per_step_calls), "cores": threads,
+            "sample": "%d fresh tokens through layer 0 (%.1f s of oracle time, %s), scaled to "
+                      "the %d layer calls of a step" % (
+                          n_tok, spent, "single-threaded build" if threads == 1 else
+                          "OpenMP build, %d threads, one token per thread" % threads,
+                          per_step_calls)}
+    best = legs["nproc"]
+    return {"value": best["value"], "unit": "tokens/s", "cores": best["cores"], "kind": "oracle",
+            "sample": best["sample"], "cpu_model": cpu_model(), "nproc": nproc,
+            "single_thread": legs["single"]}
 
 
 # ---------------------------------------------------------------------------
@@ -621,10 +676,13 @@ def main():
     ap.add_argument("--steps", type=int, default=256)
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="coli", choices=["coli", "reference"])
-    ap.add_argument("--workload", default="olmoe_decode",
+    ap.add_argument("--workload", default="glm_decode_b1",
                     choices=["olmoe_decode", "glm_decode_b1", "glm_decode_b8", "glm_prefill",
                              "quant"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--repeats", type=int, default=20,
+                    help="decode workloads: timed windows of K steps (the line reports the "
+                         "median window)")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the stack depth (small profiling cases only)")
     ap.add_argument("--tokens", type=int, default=None,
@@ -671,7 +729,9 @@ def main():
                          "layer 0 takes a fresh N(0,1) token each step; layer l>0 takes "
                          "x_l + MoE_l(x_l)" if shape.chained else
                          "every layer takes its own fresh N(0,1) input each step"),
-              "l2": "inputs larger than L2: %.2f GB of experts resident, fresh routing each step"}
+              "l2": "inputs larger than L2: %.2f GB of experts resident, fresh routing each step",
+              "timing": "median of %d windows of %d steps (CUDA events on the launch stream)"
+                        % (args.repeats, args.steps)}
 
     if args.impl == "reference":
         if rank == 0:
@@ -679,7 +739,9 @@ def main():
             line = {"metric": METRIC, "value": base["value"], "unit": "tokens/s",
                     "impl": "reference", "n_gpus": args.gpus, "steps": args.steps,
                     "warmup": args.warmup, "higher_is_better": True, "dtype": "f64",
-                    "data": "synthetic", "config": dict(config, l2="n/a (CPU)"),
+                    "data": "synthetic", "config": dict(config, l2="n/a (CPU)",
+                                                        timing="oracle wall time on the host "
+                                                               "cores (perf_counter)"),
                     "cpu_baseline": base,
                     "e2e": {"value": base["value"], "unit": "tokens/s",
                             "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -710,7 +772,9 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"] / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": ("int4 weights x 15-bit fixed-point activations (dp4a, exact int32 dot), "
+                  "f32 scale and accumulate"),
         "data": "synthetic (seeded; weights N(0,0.02) bf16 quantised on the GPU)",
         "config": config,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": k_gbs, "peak": hbm_peak,
@@ -789,9 +853,9 @@ def emit_quant(args, dev, world, rank):
         "config": {"workload": "quantiser: %d experts x {gate, up [2048,6144], down [6144,2048]}" % E,
                    "elements": elems, "bytes_per_step": nbytes,
                    "l2": "inputs larger than L2 (%.1f GB)" % (nbytes / 1e9)},
-        # traffic per launch: profiles/k_quant_vec_quantiser_16experts.md captured one
-        # launch over 16 experts' matrices (402.7 MB read + 55.8 MB written); a launch
-        # here covers E experts' matrices of the same shape, so scaled by E / 16
+        # traffic per launch: an ncu capture of one launch over 16 experts' matrices
+        # read 402.7 MB and wrote 55.8 MB; a launch here covers E experts'
+        # matrices of the same shape, so scaled by E / 16
         "roofline": {"bound": "hbm", "kernel": "k_quant_vec", "achieved": gbs, "peak": hbm_peak,
                      "unit": "GB/s", "frac": gbs / hbm_peak, "peak_kind": peak_kind,
                      "traffic": (402740480 + 55846144) * E / 16,

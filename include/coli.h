@@ -183,10 +183,17 @@ int coli_moe_forward(const coli_moe_desc *d, int top_k, const void *x,
  *   launch nothing.  The array's device address is looked up on the first
  *   call on each device (with that device current), so make that first call
  *   before any stream capture.
+ *   The cached address belongs to the device's current context: after
+ *   cudaDeviceReset (or anything else that destroys and re-creates the
+ *   primary context) this entry point must not be called again in the
+ *   process.
  *   All calls share the one array: calls that overlap on the GPU (different
  *   streams, or several host threads) race and give wrong results; order them.
- *   Each call clears the array's control words first, so the NaN-logit flag
- *   of coli_moe_check is not available through this entry point.
+ *   Each call first clears the array's control words and fixed-point router
+ *   buffers (a call that failed part-way may have left them non-zero), so the
+ *   NaN-logit flag of coli_moe_check is not available through this entry point.
+ *   Batched calls (n_tokens >= 64 with hidden % 256 == 0) run here too when
+ *   their workspace fits in the 4 MiB.
  *   Allocates nothing (no cudaMalloc, no allocating library routine); the
  *   caller still provides x, the weights, out and route_counts.
  */

@@ -3,6 +3,7 @@
 #include <limits.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -16,7 +17,11 @@ WsLayout ws_layout(int T, int H, int F, int E, int S, int k) {
   WsLayout L{};
   size_t o = 0;
   const size_t KS = (size_t)k + S;
-  L.n_part = num_sms();    // CTAs of the row-split kernels (some may own no rows)
+  // the row-split kernels run one CTA per SM; their f32 router partials (only
+  // when the logits do not fit the fixed-point buffers) are sized for the
+  // largest SM count the library accepts, so the layout does not depend on
+  // the device
+  L.n_part = kMaxParts;
   // replica strides: whole 256-byte units plus one, so replicas start at
   // different offsets modulo any power of two
   L.h_stride = (align256((size_t)T * KS * F * 4) + 256) / 4;
@@ -24,7 +29,8 @@ WsLayout ws_layout(int T, int H, int F, int E, int S, int k) {
   L.ctrl = o;
   L.fx = kFxOffset;
   o = kWsFixedBytes;
-  L.partials = o;  o = align256(o + (size_t)L.n_part * T * E * 4);
+  L.partials = o;
+  if ((size_t)T * E > (size_t)kFxMaxTE) o = align256(o + (size_t)kMaxParts * T * E * 4);
   L.idx = o;       o = align256(o + (size_t)T * k * sizeof(int32_t));
   L.gates = o;     o = align256(o + (size_t)T * k * sizeof(float));
   L.act = o;       o = align256(o + (size_t)(2 * (E + S) + 2) * sizeof(int32_t));
@@ -37,17 +43,19 @@ WsLayout ws_layout(int T, int H, int F, int E, int S, int k) {
   return L;
 }
 
+// SM count of the current device, queried once per device.  0 when there is
+// no usable device (the callers turn that into an error; there is no default).
 int num_sms() {
-  static int sms = 0;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        sms <= 0)
-      sms = 148;
-  });
-  return sms;
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cache[kMaxDev];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+    return 0;
+  cache[dev].store(v, std::memory_order_relaxed);
+  return v;
 }
 
 // Message of the last CUDA error that a call on this thread returned as COLI_ECUDA.
@@ -144,7 +152,19 @@ cudaError_t profiled(int kernel, cudaStream_t s, Launch launch) {
 
 size_t xsize(coli_dtype t) { return t == COLI_BF16 ? 2 : 4; }
 
-Dec2Args make_args(const coli_moe_desc *d, int k, int tn, uint8_t *ws, const WsLayout &L) {
+// CTAs of the row-split kernels on the current device (one per SM), or a
+// status: COLI_ECUDA without a usable device, COLI_EUNSUPPORTED above the SM
+// count the workspace layout provides for.
+int device_parts(int *parts) {
+  const int G = num_sms();
+  if (G <= 0) return coli::cuda_status(cudaErrorNoDevice);
+  if (G > kMaxParts) return COLI_EUNSUPPORTED;
+  *parts = G;
+  return COLI_OK;
+}
+
+Dec2Args make_args(const coli_moe_desc *d, int k, int tn, uint8_t *ws, const WsLayout &L,
+                   int parts) {
   Dec2Args a{};
   a.T = tn;
   a.H = d->hidden;
@@ -154,7 +174,7 @@ Dec2Args make_args(const coli_moe_desc *d, int k, int tn, uint8_t *ws, const WsL
   a.k = k;
   a.eb = coli_expert_packed_bytes(a.H, a.F);
   a.es = coli_expert_scale_count(a.H, a.F);
-  a.n_part = L.n_part;
+  a.n_part = parts;
   a.n_rep = kReplicas;
   a.partials = (float *)(ws + L.partials);
   a.h_stride = L.h_stride;
@@ -246,13 +266,15 @@ int coli_router_topk(const coli_moe_desc *d, int top_k, const void *x, const voi
   if (!x || !router_w || !idx || !gates || !workspace) return COLI_EINVAL;
   if (!aligned16(x) || !aligned16(router_w) || ((uintptr_t)workspace & 255u)) return COLI_EALIGN;
   if (ws_bytes < coli_router_workspace_size(d, top_k)) return COLI_ENOMEM;
+  int parts = 0;
+  if ((st = device_parts(&parts)) != COLI_OK) return st;
   const int H = d->hidden, E = d->n_experts, k = top_k;
   const int TP = pass_tokens(T);
   const WsLayout L = ws_layout(TP, H, d->ffn, E, d->n_shared, k);
   uint8_t *ws = (uint8_t *)workspace;
   for (int t0 = 0; t0 < T; t0 += TP) {
     const int tn = T - t0 < TP ? T - t0 : TP;
-    Dec2Args a = make_args(d, k, tn, ws, L);
+    Dec2Args a = make_args(d, k, tn, ws, L, parts);
     a.x = (const char *)x + (size_t)t0 * H * xsize(d->x_dtype);
     a.wr = router_w;
     a.route_counts = route_counts;
@@ -280,9 +302,12 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
   const size_t pk_stride = (size_t)(E + S) * coli_expert_packed_bytes(H, F);
   const size_t sc_stride = (size_t)(E + S) * coli_expert_scale_count(H, F);
   const size_t T_H = (size_t)d->n_tokens * H;
-  Dec2Args a = make_args(d, k, tn, (uint8_t *)workspace, L);
+  int parts = 0;
+  const int st = device_parts(&parts);
+  if (st != COLI_OK) return st;
+  Dec2Args a = make_args(d, k, tn, (uint8_t *)workspace, L, parts);
   a.chain = n_layers > 1;
-  if (plan_decode(a, L.n_part) != cudaSuccess) return COLI_EUNSUPPORTED;
+  if (plan_decode(a, parts) != cudaSuccess) return COLI_EUNSUPPORTED;
   const int wr_bf16 = d->router_dtype == COLI_BF16;
   cudaError_t e = cudaSuccess;
   a.build_union = 1;
@@ -323,7 +348,7 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
       if (e != cudaSuccess) break;
       if (a.route_gu) fx_buffer(a, ws, L, 1, &a.fx_acc, &a.fx_flag);
     }
-    e = profiled(COLI_KERNEL_GATEUP, stream, [&] { return launch_gateup(a, num_sms(), stream, true); });
+    e = profiled(COLI_KERNEL_GATEUP, stream, [&] { return launch_gateup(a, parts, stream, true); });
     if (e != cudaSuccess) break;
     // down also forms the next layer's router partials (and, without fixed-point
     // logits, routes it in its last CTA)

@@ -16,6 +16,8 @@ constexpr int kDecodeMaxT = 16;     // tokens per call served by the GEMV path
 constexpr int kMaxTopK = 64;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxShared = 8;
+// Largest SM count the workspace layout provides for (GB300: 152).
+constexpr int kMaxParts = 256;
 // Router logits accumulated as fixed-point integers (deterministic in any
 // order) by the CTAs that form their partials.  In the layer forward every
 // CTA of the next gate/up kernel routes from them (two buffers, by layer
@@ -58,7 +60,7 @@ struct WsLayout {
   size_t xrep;       // f32 [kReplicas][T][H]
   size_t y;          // f32 [T*(k+S)][H] (T > 1 only)
   size_t total;
-  int n_part;
+  int n_part;                  // kMaxParts: partials rows the layout holds
   size_t h_stride, x_stride;   // replica strides (floats)
 };
 

@@ -1579,7 +1579,7 @@ static cudaError_t plan_down_multi(Dec2Args &a);
 cudaError_t plan_decode(Dec2Args &a, int n_part) {
   const int T = a.T, H = a.H, F = a.F, E = a.E, S = a.S, k = a.k, KS = k + S;
   const size_t budget = (size_t)max_smem() - 4096;
-  const int G = num_sms();
+  const int G = n_part;
   a.n_part = n_part;
   // ---- gate/up: gu_nw warps, each with a gu_slots-deep cp.async pipeline
   a.gu_ncg = (H + kChunkCols - 1) / kChunkCols;
@@ -1789,10 +1789,10 @@ cudaError_t launch_down_multi(const Dec2Args &a, cudaStream_t s, bool pdl) {
   cudaError_t e;
   if (a.F % kChunkCols == 0) {
     if ((e = allow_smem(k_down_multi<true>, a.dm.total)) != cudaSuccess) return e;
-    return launch(k_down_multi<true>, num_sms(), 32 * a.dm_nw, a.dm.total, s, pdl, a);
+    return launch(k_down_multi<true>, a.n_part, 32 * a.dm_nw, a.dm.total, s, pdl, a);
   }
   if ((e = allow_smem(k_down_multi<false>, a.dm.total)) != cudaSuccess) return e;
-  return launch(k_down_multi<false>, num_sms(), 32 * a.dm_nw, a.dm.total, s, pdl, a);
+  return launch(k_down_multi<false>, a.n_part, 32 * a.dm_nw, a.dm.total, s, pdl, a);
 }
 
 cudaError_t launch_down(const Dec2Args &a_in, int wr_bf16, cudaStream_t s, bool pdl) {

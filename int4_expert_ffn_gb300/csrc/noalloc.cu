@@ -13,6 +13,7 @@ namespace {
 // until the process exits.
 constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
 constexpr int kMaxDevices = 64;
+static_assert(coli::kWsFixedBytes <= kNoAllocScratchBytes, "fixed region fits the scratch");
 
 static __device__ __align__(256) uint8_t g_coli_scratch[kNoAllocScratchBytes];
 
@@ -21,7 +22,8 @@ void *g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device.  In host code the
 // array's name is only a stand-in, so the address is looked up once per device
-// with that device current, and cached.
+// with that device current, and cached (a device reset invalidates it: see
+// coli.h).
 int scratch_address(void **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -51,9 +53,11 @@ extern "C" int coli_moe_forward_noalloc(const coli_moe_desc *d, int top_k, const
   void *ws = nullptr;
   int st = scratch_address(&ws);
   if (st != COLI_OK) return st;
-  // The control words (flags, completion ticket) must start at zero; the
-  // array keeps whatever the previous call left.
-  const cudaError_t e = cudaMemsetAsync(ws, 0, coli::kCtrlWords * sizeof(uint32_t), stream);
+  // The array keeps whatever the previous call left.  The control words (flags,
+  // completion ticket) and the fixed-point router buffers must start at zero; a
+  // successful call leaves them zero, but one that failed part-way may not, and
+  // no caller can reach this array to clear it, so every call clears them.
+  const cudaError_t e = cudaMemsetAsync(ws, 0, coli::kWsFixedBytes, stream);
   if (e != cudaSuccess) return coli::cuda_status(e);
   return coli_moe_forward(d, top_k, x, router_w, packed_experts, scales, out, route_counts, ws,
                           kNoAllocScratchBytes, stream);

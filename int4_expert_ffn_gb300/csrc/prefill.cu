@@ -757,6 +757,7 @@ cudaError_t launch_prefill(const PrefillArgs &p, int x_dtype, int wr_dtype, cuda
   cudaError_t e;
   const int T = p.T, H = p.H, E = p.E, k = p.k;
   const int nsm = num_sms();
+  if (nsm <= 0) return cudaErrorNoDevice;
   // activations -> fp16
   const int64_t nx = (int64_t)T * H;
   const int gx = (int)((nx / 8 + 255) / 256 < 4 * nsm ? (nx / 8 + 255) / 256 : 4 * nsm);

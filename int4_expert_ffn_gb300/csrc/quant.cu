@@ -173,6 +173,7 @@ cudaError_t launch_quant_i4g(const void *w, int w_dtype, int64_t rows, int64_t c
                              uint8_t *packed, float *scales, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
   const int sms = num_sms();
+  if (sms <= 0) return cudaErrorNoDevice;
   const bool aligned = ((uintptr_t)w % 16 == 0) && ((uintptr_t)packed % 4 == 0) &&
                        ((uintptr_t)scales % 4 == 0);
   if (cols % kGroup == 0 && aligned) {

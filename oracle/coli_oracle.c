@@ -32,7 +32,9 @@
  *   - activation SwiGLU, silu(z) = z / (1 + e^-z); the shared expert is added
  *     with weight 1 and is not counted.
  *
- * Build: cc -std=c11 -O2 -ffp-contract=off -fPIC -shared (no fast-math).
+ * Build: cc -std=c11 -O2 -ffp-contract=off -fPIC -shared (no fast-math); a
+ * second build adds -fopenmp, which only spreads independent rows / tokens
+ * over threads (every sum keeps its order, so both builds give the same bits).
  */
 #include <math.h>
 #include <stdint.h>
@@ -56,6 +58,9 @@ void orc_quant_i4g(const float *w, int64_t rows, int64_t cols,
 {
     const int64_t rb = orc_packed_row_bytes(cols);
     const int64_t ng = orc_scales_per_row(cols);
+    /* rows are independent; the OpenMP build of this file (the benchmark's
+     * multi-core leg, large test cases) splits them over threads */
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; ++r) {
         const float *wr = w + r * cols;
         uint8_t *pr = packed + r * rb;
@@ -128,6 +133,7 @@ void orc_matvec_i4g(const uint8_t *packed, const float *scales,
 void orc_router_logits(const double *x, const double *wr, int64_t T, int64_t H,
                        int64_t E, double *logits)
 {
+#pragma omp parallel for schedule(static)
     for (int64_t t = 0; t < T; ++t)
         for (int64_t e = 0; e < E; ++e) {
             double acc = 0.0;
@@ -303,7 +309,6 @@ int orc_moe_forward_router(const double *x, int64_t T, int64_t H, int64_t F, int
     const int64_t eb = orc_expert_packed_bytes(H, F);
     const int64_t es = orc_expert_scales(H, F);
     double *logits = (double *)malloc((size_t)(T * E) * sizeof(double));
-    double *y = (double *)malloc((size_t)H * sizeof(double));
     int nan_tokens = 0;
     orc_router_logits(x, wr, T, H, E, logits);
     for (int64_t t = 0; t < T; ++t) {
@@ -312,6 +317,12 @@ int orc_moe_forward_router(const double *x, int64_t T, int64_t H, int64_t F, int
             : orc_topk(logits + t * E, E, k, idx + t * k, gates + t * k);
         if (counts)
             for (int j = 0; j < k; ++j) counts[idx[t * k + j]] += 1u;
+    }
+    /* tokens are independent once routed (the OpenMP build runs them on
+     * several threads; each token's sum keeps the same order) */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < T; ++t) {
+        double *y = (double *)malloc((size_t)H * sizeof(double));
         double *o = out + t * H;
         for (int64_t h = 0; h < H; ++h) o[h] = 0.0;
         for (int j = 0; j < k; ++j) {
@@ -324,8 +335,8 @@ int orc_moe_forward_router(const double *x, int64_t T, int64_t H, int64_t F, int
             orc_expert(packed + e * eb, scales + e * es, H, F, x + t * H, y);
             for (int64_t h = 0; h < H; ++h) o[h] += y[h];
         }
+        free(y);
     }
     free(logits);
-    free(y);
     return nan_tokens;
 }

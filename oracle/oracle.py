@@ -7,22 +7,43 @@ import ctypes as C
 
 import numpy as np
 
-from .build import build_oracle
+from .build import build_oracle, build_oracle_omp
 
 __all__ = [
     "GROUP", "packed_row_bytes", "scales_per_row", "expert_packed_bytes",
     "expert_scales", "quant_i4g", "dequant_i4g", "matvec_i4g", "router_logits",
     "topk", "topk_sigmoid", "expert", "moe_forward", "moe_stack_forward", "lib",
+    "set_threads", "threads",
 ]
 
 GROUP = 64
-_lib = None
+_libs = {}
+_threads = 1
+
+
+def set_threads(n):
+    """Run the following oracle calls on n threads (the OpenMP build of the same
+    source; every sum keeps its order, so results do not depend on n).  n = 1
+    selects the single-threaded build.  Returns the previous setting."""
+    global _threads
+    prev, _threads = _threads, max(1, int(n))
+    if _threads > 1:
+        L = lib()
+        L.omp_set_num_threads(_threads)
+    return prev
+
+
+def threads():
+    return _threads
 
 
 def lib():
-    global _lib
-    if _lib is None:
-        L = C.CDLL(build_oracle())
+    key = "omp" if _threads > 1 else "serial"
+    if key not in _libs:
+        L = C.CDLL(build_oracle_omp() if key == "omp" else build_oracle())
+        if key == "omp":
+            L.omp_set_num_threads.argtypes = [C.c_int]
+            L.omp_set_num_threads.restype = None
         i64, f32p, f64p = C.c_int64, C.POINTER(C.c_float), C.POINTER(C.c_double)
         u8p, i32p, u32p = C.POINTER(C.c_uint8), C.POINTER(C.c_int32), C.POINTER(C.c_uint32)
         L.orc_packed_row_bytes.argtypes = [i64]
@@ -53,8 +74,8 @@ def lib():
         L.orc_moe_forward_router.argtypes = [f64p, i64, i64, i64, i64, i64, f64p, C.c_int, f64p,
                                              u8p, f32p, C.c_int, f64p, i32p, f64p, u32p]
         L.orc_moe_forward_router.restype = C.c_int
-        _lib = L
-    return _lib
+        _libs[key] = L
+    return _libs[key]
 
 
 def _p(a, ctype):

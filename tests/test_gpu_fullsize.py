@@ -18,6 +18,7 @@ rounding of the GPU path cannot flip a selection.  Each GPU call runs three
 times and must give bit-identical results.
 """
 import dataclasses
+import os
 
 import numpy as np
 import pytest
@@ -192,13 +193,34 @@ def test_glm_stack_two_deep(T):
     check_stack(shape, n_steps=1)
 
 
-def test_glm_prefill_sampled():
+def prefill_tokens_without_ties(shape, wr64, seed=SEED, step=0, gap=1e-4, max_attempts=40):
+    """The prefill batch with every near-tie token redrawn on its own: token t is
+    row t of the attempt-a_t draw, a_t the first attempt whose top-(k+1) f32
+    logits of that token have adjacent gaps above ``gap``."""
+    k = shape.top_k
+    x = synth.tokens(shape, seed, step)                  # attempt 0, host bf16 [T, H]
+    lg = orc.router_logits(x.double().numpy(), wr64)
+    todo = np.array([t for t in range(x.shape[0]) if min_topk_gap(lg[t:t + 1], k) <= gap])
+    for attempt in range(1, max_attempts):
+        if todo.size == 0:
+            return x, lg
+        xa = synth.tokens(shape, seed, step, attempt=attempt)[todo]
+        la = orc.router_logits(xa.double().numpy(), wr64)
+        ok = np.array([min_topk_gap(la[i:i + 1], k) > gap for i in range(len(todo))])
+        x[todo[ok]] = xa[ok]
+        lg[todo[ok]] = la[ok]
+        todo = todo[~ok]
+    raise RuntimeError("%d tokens kept a near-tie" % todo.size)
+
+
+def test_glm_prefill_tie_free():
     """The batched path at the prefill workload: one GLM-like layer, 4096 bf16
-    tokens, a router skewed so that 32 experts take about half of the routes.
-    Every token's route count is checked against the oracle's routing of all
-    4096 tokens (near-ties, where f32 and f64 logits may order differently,
-    are allowed to move their two routes); 16 sampled tie-free tokens' outputs
-    are checked against the oracle's layer on those tokens."""
+    tokens, a router skewed so that 32 experts take about half of the routes,
+    every token redrawn until its top-(k+1) logits are tie-free (gap > 1e-4).
+    Route counts must equal the oracle's bit for bit.  Outputs are compared with
+    the oracle on at least 512 tokens that include, for every expert with
+    routes, the token of its first route (its first 128-route m-tile) and the
+    token of its last route (its last, partial m-tile)."""
     c = coli()
     shape = synth.GLM_PREFILL
     T, H, F, E, S, k = shape.tokens, shape.hidden, shape.ffn, shape.experts, shape.shared, shape.top_k
@@ -211,31 +233,41 @@ def test_glm_prefill_sampled():
         p0, s0 = quant_gpu_into(mats, packed, scales, p0, s0)
     wr = synth.router_weights(shape, 0, SEED, device="cuda",
                               row_std=synth.skewed_router_std(E, H))
-    x = synth.tokens(shape, SEED, 0)                     # host bf16 [T, H]
-    desc = c.MoEDesc(H, F, E, S, T, c.COLI_BF16, c.COLI_BF16)
-    ws = c.new_workspace(desc, k)
-    counts = torch.zeros(E, dtype=torch.int32, device="cuda")
-    out = c.coli_moe_forward(desc, k, x.cuda(), wr, packed, scales, ws, route_counts=counts)
-    out2 = c.coli_moe_forward(desc, k, x.cuda(), wr, packed, scales, ws)
-    torch.cuda.synchronize()
-    assert torch.equal(out, out2), "not deterministic"
-    ol = OracleLayer(shape, 0, wr)
-    x64 = x.double().numpy()
-    lg = orc.router_logits(x64, ol.wr)
-    ocounts = np.zeros(E, np.int64)
-    gaps = np.zeros(T)
-    for t in range(T):
-        idx, _, _ = orc.topk(lg[t], k)
-        ocounts[idx] += 1
-        srt = np.sort(lg[t].astype(np.float32))[::-1]
-        gaps[t] = np.min(srt[:k] - srt[1:k + 1])
-    near = int((gaps < 1e-5).sum())
-    diff = np.abs(counts.cpu().numpy().astype(np.int64) - ocounts).sum()
-    assert diff <= 2 * near, "route counts differ by %d with %d near-ties" % (diff, near)
-    assert np.sort(ocounts)[::-1][:32].sum() > 0.4 * T * k, "router not skewed"
-    sample = [t for t in np.random.default_rng(1).permutation(T) if gaps[t] > 1e-4][:16]
-    need = np.unique(np.argsort(-lg[sample], axis=1)[:, :k + 1])
-    ol.need(need)
-    ref, _, _, _ = orc.moe_forward(x64[sample], ol.wr, ol.packed, ol.scales, H, F, E, S, k)
-    err = rel_err(out.cpu().numpy()[sample], ref)
-    assert err.max() <= REL_TOL, "max rel err %.3g" % err.max()
+    prev = orc.set_threads(os.cpu_count() or 1)
+    try:
+        ol = OracleLayer(shape, 0, wr)
+        x, lg = prefill_tokens_without_ties(shape, ol.wr)
+        desc = c.MoEDesc(H, F, E, S, T, c.COLI_BF16, c.COLI_BF16)
+        ws = c.new_workspace(desc, k)
+        counts = torch.zeros(E, dtype=torch.int32, device="cuda")
+        out = c.coli_moe_forward(desc, k, x.cuda(), wr, packed, scales, ws, route_counts=counts)
+        out2 = c.coli_moe_forward(desc, k, x.cuda(), wr, packed, scales, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out, out2), "not deterministic"
+        # routing of all 4096 tokens: the oracle's top-k, counted
+        idx = np.stack([orc.topk(lg[t], k)[0] for t in range(T)])
+        ocounts = np.bincount(idx.reshape(-1), minlength=E)
+        assert np.array_equal(counts.cpu().numpy().astype(np.int64), ocounts), "route counts differ"
+        assert np.sort(ocounts)[::-1][:32].sum() > 0.4 * T * k, "router not skewed"
+        # tokens to compare: first and last route of every routed expert, then
+        # random tokens up to 512
+        sample = set()
+        for e in range(E):
+            toks = np.nonzero((idx == e).any(axis=1))[0]
+            if toks.size:
+                sample.update((int(toks[0]), int(toks[-1])))
+        sample.update((0, T - 1))                        # the shared expert's first and last tile
+        for t in np.random.default_rng(1).permutation(T):
+            if len(sample) >= 512:
+                break
+            sample.add(int(t))
+        sample = np.array(sorted(sample))
+        ol.need(np.unique(idx[sample]))
+        ref, ridx, _, _ = orc.moe_forward(x.double().numpy()[sample], ol.wr, ol.packed, ol.scales,
+                                          H, F, E, S, k)
+        assert np.array_equal(ridx, idx[sample])
+        err = rel_err(out.cpu().numpy()[sample], ref)
+        assert err.max() <= REL_TOL, "max rel err %.3g (token %d)" % (err.max(),
+                                                                  sample[int(np.argmax(err))])
+    finally:
+        orc.set_threads(prev)

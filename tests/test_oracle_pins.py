@@ -358,3 +358,37 @@ def test_moe_sigmoid_router_dense_masked():
         ref = sum(s[e] / s[order].sum() * _torch_expert(mats[e], x[t]) for e in order)
         ref = ref + _torch_expert(mats[E], x[t])
         np.testing.assert_allclose(out[t], ref, rtol=1e-10, atol=1e-10)
+
+
+# ---------------------------------------------------------------------------
+# the OpenMP build of the oracle (the benchmark's multi-core leg, large test
+# cases) must give the single-threaded build's bits
+
+
+def test_openmp_build_gives_the_same_bits():
+    rng = np.random.default_rng(11)
+    H, F, E, S, k, T = 128, 192, 6, 1, 2, 9
+    w = (rng.standard_normal((37, 320)) * 0.02).astype(np.float32)
+    mats = [(rng.standard_normal(s) * 0.02).astype(np.float32)
+            for _ in range(E + S) for s in ((F, H), (F, H), (H, F))]
+    x = rng.standard_normal((T, H))
+    wr = rng.standard_normal((E, H)) / np.sqrt(H)
+
+    def run():
+        p, s = orc.quant_i4g(w)
+        qs = [orc.quant_i4g(m) for m in mats]
+        packed = np.concatenate([q[0].reshape(-1) for q in qs])
+        scales = np.concatenate([q[1].reshape(-1) for q in qs])
+        counts = np.zeros(E, np.uint32)
+        out, idx, gates, _ = orc.moe_forward(x, wr, packed, scales, H, F, E, S, k, counts)
+        return p, s, out, idx, gates, counts
+
+    prev = orc.set_threads(1)
+    try:
+        serial = run()
+        orc.set_threads(4)
+        par = run()
+    finally:
+        orc.set_threads(prev)
+    for a, b in zip(serial, par):
+        assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
