@@ -230,12 +230,25 @@ class DecodeWorkload:
                                self.packed[l * pb:(l + 1) * pb], self.scales[l * sb:(l + 1) * sb],
                                self.ws, out=out[l], route_counts=self.counts[i, l], stream=stream)
 
+    def fused(self):
+        """One token at whole 1024-column chunks with the used experts at most
+        512 KB per SM: one fused kernel per layer (the library's rule)."""
+        sh = self.shape
+        sms = torch.cuda.get_device_properties(self.dev).multi_processor_count
+        per_sm = (sh.top_k + sh.shared) * (self.eb + 4 * self.es) / sms
+        return (sh.tokens == 1 and sh.hidden % 1024 == 0 and sh.ffn % 1024 == 0
+                and per_sm <= 512 * 1024)
+
     def kernels_per_step(self):
         # per 16-token pass: chained, the first layer's router partials, then
-        # gate/up and down for every layer; else router, gate/up, down per layer
+        # the layer kernel(s) of every layer; else the router partials and the
+        # layer kernel(s) per layer
         sh = self.shape
         passes = (sh.tokens + 15) // 16
-        return passes * ((1 + 2 * sh.layers) if sh.chained else 3 * sh.layers)
+        # fused: one kernel; else gate/up and down (several tokens: gate/up,
+        # the per-expert down GEMVs and the combine)
+        per_layer = 1 if self.fused() else (2 if sh.tokens == 1 else 3)
+        return passes * ((1 + per_layer * sh.layers) if sh.chained else (1 + per_layer) * sh.layers)
 
     def io_bytes_per_step(self):
         """Host <-> device bytes of one step's input and output (f32)."""
@@ -248,7 +261,9 @@ class DecodeWorkload:
         gate/up: gate and up nibbles + scales of the layer's distinct routed
         experts and its shared experts, x in, h out.  down: down nibbles +
         scales of the same experts, h in, residual in, output out, and the
-        next layer's router weights (the routing that follows in its tail)."""
+        next layer's router weights (the routing that follows in its tail).
+        The one-token layer kernel: every used expert's whole record, x in,
+        output out, and the next layer's router weights."""
         c, sh = self.coli, self.shape
         T, H, F, E, S, k = sh.tokens, sh.hidden, sh.ffn, sh.experts, sh.shared, sh.top_k
         uniq = (self.counts[steps] > 0).sum(dim=2).cpu().numpy()          # [K, L]
@@ -263,6 +278,10 @@ class DecodeWorkload:
             next_router = rb * (sh.layers - 1) * len(steps) if sh.chained else 0
             return int((n_exp * per_exp).sum() + uniq.size * (h_bytes + 2 * T * H * 4)
                        + next_router)
+        if kernel == c.COLI_KERNEL_LAYER:
+            per_exp = self.eb + 4 * self.es
+            next_router = rb * (sh.layers - 1) * len(steps) if sh.chained else 0
+            return int((n_exp * per_exp).sum() + uniq.size * 2 * T * H * 4 + next_router)
         n_route = len(steps) * (1 if sh.chained else sh.layers)
         return int(n_route * (rb + T * H * 4))
 
@@ -476,9 +495,10 @@ def run_decode(args, shape, dev, world, rank):
         "launches": steps * wl.kernels_per_step(),
     }
     del graphs
-    res["kernels"] = {name: kernel_timing(wl, args, stream, kid)
-                      for name, kid in (("k_gateup", wl.coli.COLI_KERNEL_GATEUP),
-                                        ("k_down", wl.coli.COLI_KERNEL_DOWN))}
+    c = wl.coli
+    kset = ((("k_layer1", c.COLI_KERNEL_LAYER),) if wl.fused() else
+            (("k_gateup", c.COLI_KERNEL_GATEUP), ("k_down", c.COLI_KERNEL_DOWN)))
+    res["kernels"] = {name: kernel_timing(wl, args, stream, kid) for name, kid in kset}
     res["e2e"] = run_e2e(wl, args, dev, world, stream)
     return wl, res
 

@@ -224,6 +224,9 @@ int coli_moe_stack_forward(const coli_moe_desc *d, int top_k, int n_layers,
 #define COLI_KERNEL_DOWN   2   /* down expert GEMVs + combine (+ next routing) */
 #define COLI_KERNEL_PREFILL_GATEUP 3  /* batched path: gate/up grouped GEMM + SwiGLU */
 #define COLI_KERNEL_PREFILL_DOWN   4  /* batched path: down grouped GEMM */
+#define COLI_KERNEL_LAYER  5   /* one-token layer kernel (routing, gate/up, down,
+                                  combine in one launch; taken at one token when
+                                  hidden and ffn are multiples of 1024) */
 
 /*
  * coli_profile_events -- diagnostic, not on the compute path: record the

@@ -23,6 +23,7 @@ COLI_ROUTER_SOFTMAX, COLI_ROUTER_SIGMOID_BIAS = 0, 1
 COLI_FLAG_NAN_LOGITS, COLI_FLAG_TIMEOUT = 0x1, 0x2
 COLI_KERNEL_ROUTE, COLI_KERNEL_GATEUP, COLI_KERNEL_DOWN = 0, 1, 2
 COLI_KERNEL_PREFILL_GATEUP, COLI_KERNEL_PREFILL_DOWN = 3, 4
+COLI_KERNEL_LAYER = 5
 GROUP = 64
 
 # every symbol include/coli.h declares

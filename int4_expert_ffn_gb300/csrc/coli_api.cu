@@ -307,12 +307,16 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
   if (st != COLI_OK) return st;
   Dec2Args a = make_args(d, k, tn, (uint8_t *)workspace, L, parts);
   a.chain = n_layers > 1;
-  if (plan_decode(a, parts) != cudaSuccess) return COLI_EUNSUPPORTED;
+  // one token at shapes of whole 1024-column chunks: one fused kernel per
+  // layer (decode1.cu); otherwise the gate/up and down GEMV kernels
+  const bool fused = plan_layer1(a);
+  if (!fused && plan_decode(a, parts) != cudaSuccess) return COLI_EUNSUPPORTED;
   const int wr_bf16 = d->router_dtype == COLI_BF16;
   cudaError_t e = cudaSuccess;
   a.build_union = 1;
-  // with fixed-point logits every gate/up CTA routes its own layer
-  a.route_gu = a.fx && a.gu_route_fits;
+  // with fixed-point logits every gate/up CTA (every fused-kernel CTA) routes
+  // its own layer
+  a.route_gu = fused || (a.fx && a.gu_route_fits);
   const float *bias0 = d->router_fn == COLI_ROUTER_SIGMOID_BIAS ? d->router_bias : nullptr;
   uint8_t *ws = (uint8_t *)workspace;
   for (int l = 0; l < n_layers && e == cudaSuccess; ++l) {
@@ -347,6 +351,16 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
       });
       if (e != cudaSuccess) break;
       if (a.route_gu) fx_buffer(a, ws, L, 1, &a.fx_acc, &a.fx_flag);
+    }
+    if (fused) {
+      // routing, gate/up, down, combine and the next layer's router partials
+      const bool next = l + 1 < n_layers;
+      a.wr = next ? (const void *)((const char *)router_w + (l + 1) * wr_stride) : nullptr;
+      a.residual = residual ? (const float *)xin : nullptr;
+      a.out = out;
+      a.layer_out = layer_out ? layer_out + (size_t)l * T_H : nullptr;
+      e = profiled(COLI_KERNEL_LAYER, stream, [&] { return launch_layer1(a, stream, true); });
+      continue;
     }
     e = profiled(COLI_KERNEL_GATEUP, stream, [&] { return launch_gateup(a, parts, stream, true); });
     if (e != cudaSuccess) break;
@@ -481,7 +495,7 @@ int coli_moe_stack_forward(const coli_moe_desc *d, int top_k, int n_layers, cons
 int coli_profile_events(int kernel, const cudaEvent_t *before, const cudaEvent_t *after,
                         int n) {
   if (n < 0 || (n > 0 && (!before || !after))) return COLI_EINVAL;
-  if (kernel < COLI_KERNEL_ROUTE || kernel > COLI_KERNEL_PREFILL_DOWN) return COLI_EINVAL;
+  if (kernel < COLI_KERNEL_ROUTE || kernel > COLI_KERNEL_LAYER) return COLI_EINVAL;
   ProfileState &p = profile();
   std::lock_guard<std::mutex> lock(p.mu);
   const int done = (int)p.next;

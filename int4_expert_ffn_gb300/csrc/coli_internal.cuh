@@ -42,6 +42,10 @@ enum CtrlWord : int {
   kCtrlFlags = 0,      // COLI_FLAG_* bits (sticky until coli_moe_check clears)
   kCtrlRouterTicket = 1,
   kCtrlPrefillMTiles = 2,  // m-tiles of the current batched call (written by the grouping)
+  kCtrlBarArrive = 3,  // grid barrier of the one-token layer kernel: arrivals of this use
+  kCtrlBarGen = 4,     //   and its generation (left as they are between calls)
+  kCtrlWaitLimit = 5,  // 0: default bounded waits; else the grid barrier's spin limit in
+                       //   clock cycles (a test hook that makes the wait run out)
   kCtrlWords = 64,     // 256 bytes
 };
 static_assert(kCtrlWords * 4 <= kFxOffset, "control words precede the fixed-point region");
@@ -79,6 +83,10 @@ struct DnSmem {
 // Shared-memory plan of k_down_multi.
 struct DmSmem {
   size_t act, routes, u, planes, acc, ring, total;
+};
+// Shared-memory plan of the one-token layer kernel k_layer1 (decode1.cu).
+struct L1Smem {
+  size_t bar, lst, red, xn, wr, hacc, u, ring, total;
 };
 
 // Arguments of the decode kernels (one layer, T <= kDecodeMaxT tokens).
@@ -141,6 +149,13 @@ struct Dec2Args {
   GuSmem gu;
   DnSmem dn;
   DmSmem dm;
+  // one-token layer kernel (decode1.cu): l1_nc warps of l1_spw bulk-copy slots
+  // each (l1_ns in all) of l1_slot bytes; gate/up stages of
+  // l1_rg gate + l1_rg up rows, down stages of l1_dr rows; x (f32) and its
+  // planes at bytes l1_xs_off / l1_xpl_off of the kernel's U region; at most
+  // l1_nblk h blocks per CTA
+  int l1_ns, l1_nc, l1_spw, l1_rg, l1_slot, l1_dr, l1_xs_off, l1_xpl_off, l1_nblk;
+  L1Smem l1;
 };
 
 
@@ -190,6 +205,10 @@ cudaError_t launch_route_partials(const Dec2Args &a, int x_bf16, int w_bf16, cud
 cudaError_t launch_gateup(const Dec2Args &a, int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_down(const Dec2Args &a, int wr_bf16, cudaStream_t s, bool pdl);
 cudaError_t launch_down_multi(const Dec2Args &a, cudaStream_t s, bool pdl);
+// One-token layers (decode1.cu): plan_layer1 returns true when the fused
+// kernel handles this shape (and fills its plan); launch_layer1 runs one layer.
+bool plan_layer1(Dec2Args &a);
+cudaError_t launch_layer1(const Dec2Args &a, cudaStream_t s, bool pdl);
 
 // Quantiser (quant.cu).
 cudaError_t launch_quant_i4g(const void *w, int w_dtype, int64_t rows, int64_t cols,

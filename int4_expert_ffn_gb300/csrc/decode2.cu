@@ -31,224 +31,13 @@
 #include <unordered_map>
 
 #include "coli_internal.cuh"
+#include "decode_common.cuh"
 #include "ptx.cuh"
 #include "topk.cuh"
 #include "trace.cuh"
 
 namespace coli {
 
-namespace {
-
-constexpr int kQ = 16319;
-constexpr int kChunkCols = 1024;  // columns per warp pass (32 lanes x 32)
-
-struct Planes {
-  uint32_t eh[4], el[4], oh[4], ol[4];
-  int sq;
-  float sx;
-};
-
-__device__ __forceinline__ void quantize32(const float (&v)[32], Planes &p) {
-  float m = 0.0f;
-  bool bad = false;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    m = fmaxf(m, fabsf(v[i]));
-    bad |= (v[i] != v[i]);
-  }
-  const float inv = m > 0.0f ? (float)kQ / m : 0.0f;
-  p.sx = bad ? __int_as_float(0x7FC00000) : m / (float)kQ;
-  int sq = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t eh = 0, el = 0, oh = 0, ol = 0;
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const int qe = (int)fminf(fmaxf(rintf(v[8 * i + 2 * b] * inv), -(float)kQ), (float)kQ);
-      const int qo = (int)fminf(fmaxf(rintf(v[8 * i + 2 * b + 1] * inv), -(float)kQ), (float)kQ);
-      const int he = (qe + 64) >> 7, ho = (qo + 64) >> 7;
-      const int le = qe - (he << 7), lo = qo - (ho << 7);
-      eh |= (uint32_t)(he & 0xFF) << (8 * b);
-      el |= (uint32_t)(le & 0xFF) << (8 * b);
-      oh |= (uint32_t)(ho & 0xFF) << (8 * b);
-      ol |= (uint32_t)(lo & 0xFF) << (8 * b);
-      sq += qe + qo;
-    }
-    p.eh[i] = eh; p.el[i] = el; p.oh[i] = oh; p.ol[i] = ol;
-  }
-  p.sq = sq;
-}
-
-// sum over the 32 columns of (u - 8) * x, for 16 packed bytes w.
-__device__ __forceinline__ float dot32(const uint4 w, const Planes &p) {
-  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-  int aeh = 0, ael = 0, aoh = 0, aol = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t lo = ws[i] & 0x0F0F0F0Fu;   // even columns: u
-    const uint32_t hi = ws[i] & 0xF0F0F0F0u;   // odd columns: 16 u
-    aeh = dp4a_us(lo, p.eh[i], aeh);
-    ael = dp4a_us(lo, p.el[i], ael);
-    aoh = dp4a_us(hi, p.oh[i], aoh);
-    aol = dp4a_us(hi, p.ol[i], aol);
-  }
-  const int q = ((aeh + (aoh >> 4)) << 7) + ael + (aol >> 4) - 8 * p.sq;
-  return (float)q * p.sx;
-}
-
-template <typename XT>
-__device__ __forceinline__ void load32(const XT *p, float (&v)[32]);
-
-template <>
-__device__ __forceinline__ void load32<float>(const float *p, float (&v)[32]) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float4 q = __ldcg((const float4 *)p + i);
-    v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
-  }
-}
-
-// Reduce 8 values across the warp in 9 shuffles; lane l ends with the total of
-// value (l >> 2).
-__device__ __forceinline__ float reduce8(float (&v)[8]) {
-  const int lane = threadIdx.x & 31;
-  float a[4];
-  const bool b4 = lane & 16;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float keep = b4 ? v[i + 4] : v[i];
-    const float give = b4 ? v[i] : v[i + 4];
-    a[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, give, 16);
-  }
-  float c[2];
-  const bool b3 = lane & 8;
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const float keep = b3 ? a[i + 2] : a[i];
-    const float give = b3 ? a[i] : a[i + 2];
-    c[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, give, 8);
-  }
-  const bool b2 = lane & 4;
-  const float keep = b2 ? c[1] : c[0];
-  const float give = b2 ? c[0] : c[1];
-  float d = keep + __shfl_xor_sync(0xFFFFFFFFu, give, 4);
-  d += __shfl_xor_sync(0xFFFFFFFFu, d, 2);
-  d += __shfl_xor_sync(0xFFFFFFFFu, d, 1);
-  return d;
-}
-
-// Quantise n_vec f32 vectors of length F (global, row-major [n_vec][F]) into
-// activation planes in shared memory, transposed for conflict-free access:
-// word w (0..15 planes, 16 = sq, 17 = sx bits) of 32-column block b of vector v
-// is at planes[(v * 18 + w) * nbp + b].  Each lane quantises whole blocks in
-// registers (the same arithmetic as the per-warp paths); CTAs start at
-// different blocks so the grid's reads of the same vectors spread over L2.
-__device__ void build_planes_impl(const float *src, int n_vec, int F, const int *list,
-                                  uint32_t *planes, int nbp, int warp, int nw) {
-  const int nb = F / 32;   // F is a multiple of 64
-  const int n_blocks = n_vec * nb;
-  if (n_blocks == 0) return;
-  const int rot = (int)(((long long)blockIdx.x * 37) % n_blocks);
-  for (int i = warp * 32 + (threadIdx.x & 31); i < n_blocks; i += nw * 32) {
-    int g = i + rot;
-    if (g >= n_blocks) g -= n_blocks;
-    const int v = g / nb, b = g - v * nb;
-    const int64_t row = list ? list[v] : v;
-    float xv[32];
-    load32<float>(src + row * F + 32 * b, xv);
-    Planes p;
-    quantize32(xv, p);
-    uint32_t *pv = planes + (size_t)v * 18 * nbp + b;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      pv[(size_t)j * nbp] = p.eh[j];
-      pv[(size_t)(4 + j) * nbp] = p.el[j];
-      pv[(size_t)(8 + j) * nbp] = p.oh[j];
-      pv[(size_t)(12 + j) * nbp] = p.ol[j];
-    }
-    pv[(size_t)16 * nbp] = (uint32_t)p.sq;
-    pv[(size_t)17 * nbp] = __float_as_uint(p.sx);
-  }
-}
-
-// build_planes over a list of source rows: vector p is row list[p] of src.
-__device__ void build_planes_list(const float *src, int F, const int *list, int n, uint32_t *planes,
-                                  int nbp);
-
-__device__ void build_planes_list(const float *src, int F, const int *list, int n, uint32_t *planes,
-                                  int nbp) {
-  build_planes_impl(src, n, F, list, planes, nbp, threadIdx.x >> 5, blockDim.x >> 5);
-}
-
-__device__ __forceinline__ void load_planes(const uint32_t *planes, int v, int b, int nbp,
-                                            Planes &p) {
-  const uint32_t *pv = planes + (size_t)v * 18 * nbp + b;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    p.eh[i] = pv[(size_t)i * nbp];
-    p.el[i] = pv[(size_t)(4 + i) * nbp];
-    p.oh[i] = pv[(size_t)(8 + i) * nbp];
-    p.ol[i] = pv[(size_t)(12 + i) * nbp];
-  }
-  p.sq = (int)pv[(size_t)16 * nbp];
-  p.sx = __uint_as_float(pv[(size_t)17 * nbp]);
-}
-
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
-
-__device__ __forceinline__ int part_lo(int c, int n, int parts) {
-  return (int)(((long long)c * n) / parts);
-}
-
-__device__ __forceinline__ void set_flag(uint32_t *ctrl, uint32_t f) {
-  atomicOr(ctrl + kCtrlFlags, f);
-}
-
-// The pointers that change from layer to layer (the rest of Dec2Args stays in
-// kernel-parameter space).
-struct LayerPtrs {
-  const uint8_t *packed;
-  const float *scales;
-  uint32_t *route_counts;
-  float *layer_out;
-  const float *partials;
-  float *out;
-  float *xrep;
-};
-
-__device__ __forceinline__ LayerPtrs layer_ptrs(const Dec2Args &a) {
-  LayerPtrs p;
-  p.packed = a.packed;
-  p.scales = a.scales;
-  p.route_counts = a.route_counts;
-  p.layer_out = a.layer_out;
-  p.partials = a.partials;
-  p.out = a.out;
-  p.xrep = a.xrep;
-  return p;
-}
-
-
-// Fixed-point router logits (2^-32 units): a partial p of logit (t, e) is
-// added with an integer atomic, so the total does not depend on the order in
-// which CTAs arrive.  A non-finite partial, or one of magnitude 1e7 or more,
-// marks the logit as NaN instead.
-// A fixed-point sum as a float: one rounding of the integer, then the exact
-// power-of-two scale.
-__device__ __forceinline__ float fx_to_float(long long v) {
-  return __ll2float_rn(v) * 0x1p-32f;
-}
-
-__device__ __forceinline__ void fx_add(const Dec2Args &a, int o, float p) {
-  if (!(fabsf(p) < 1.0e7f)) {
-    atomicOr(a.fx_flag + o, 1u);
-    return;
-  }
-  atomicAdd((unsigned long long *)(a.fx_acc + o),
-            (unsigned long long)__float2ll_rn(p * 4294967296.0f));
-}
-
-}  // namespace
 
 // ---------------------------------------------------------------------------
 // Router partial logits: CTA c of G sums its rows [h0, h1) of every expert's
@@ -637,28 +426,6 @@ __device__ void load_lists(const Dec2Args &a, int *s_act, int *s_routes, float *
   __syncthreads();
 }
 
-// Shared-memory scratch of gu_route (byte offsets from its base).
-struct GuRouteSmem {
-  size_t logits, sel, bias, topk, idx, gates, vals, flag, total;
-};
-__host__ __device__ inline GuRouteSmem gu_route_smem(int T, int E, int k) {
-  auto a16 = [](size_t v) { return (v + 15) & ~(size_t)15; };
-  GuRouteSmem R{};
-  size_t o = 0;
-  R.logits = o; o = a16(o + (size_t)T * E * 4);
-  R.sel = o; o = a16(o + (size_t)T * E * 4);
-  R.bias = o; o = a16(o + (size_t)E * 4);
-  R.topk = o;
-  size_t tk = topk_scratch_bytes(T, E, k);
-  if (tk < (size_t)T * k * 4) tk = (size_t)T * k * 4;   // the union's sort scratch
-  o = a16(R.topk + tk);
-  R.idx = o; o += (size_t)T * k * 4;
-  R.gates = o; o += (size_t)T * k * 4;
-  R.vals = o; o += (size_t)T * k * 4;
-  R.flag = a16(o); o = R.flag + 16;
-  R.total = o;
-  return R;
-}
 
 // The union lists of this layer in the gate/up CTA's shared memory: routed
 // here from the fixed-point logits (every CTA alike, same integers, same
@@ -1255,65 +1022,6 @@ __device__ void dn_phase(const Dec2Args &a, const LayerPtrs &lp, const int *s_ac
   __syncthreads();
 }
 
-// Partial logits of the next layer from this CTA's rows of its input:
-// partials[c][t][e] = sum_r wr[e][dh0 + r] xn[t][r], written to n_copies copies.
-template <typename WT>
-__device__ void dn_partials(const Dec2Args &a, float *partials, const WT *s_wr, const float *s_xn,
-                            int n_copies, size_t copy_stride) {
-  const int T = a.T, H = a.H, E = a.E;
-  const int G = gridDim.x, c = blockIdx.x;
-  const int UH = H / 4;
-  const int nr = 4 * part_lo(c + 1, UH, G) - 4 * part_lo(c, UH, G);
-  for (int o = threadIdx.x; o < T * E; o += blockDim.x) {
-    const int t = o / E, e = o - t * E;
-    float sum = 0.0f;
-    for (int r = 0; r < nr; ++r) sum = fmaf(to_f32(s_wr[e * nr + r]), s_xn[t * nr + r], sum);
-    for (int rr = 0; rr < n_copies; ++rr)
-      partials[rr * copy_stride + (size_t)c * T * E + o] = sum;
-  }
-}
-
-// The same partial logits, added to the next layer's fixed-point buffer.
-template <typename WT>
-__device__ void dn_partials_fx(const Dec2Args &a, const WT *s_wr, const float *s_xn) {
-  const int T = a.T, H = a.H, E = a.E;
-  const int G = gridDim.x, c = blockIdx.x;
-  const int UH = H / 4;
-  const int nr = 4 * part_lo(c + 1, UH, G) - 4 * part_lo(c, UH, G);
-  if (nr <= 0) return;
-  for (int o = threadIdx.x; o < T * E; o += blockDim.x) {
-    const int t = o / E, e = o - t * E;
-    float sum = 0.0f;
-    for (int r = 0; r < nr; ++r) sum = fmaf(to_f32(s_wr[e * nr + r]), s_xn[t * nr + r], sum);
-    fx_add(a, o, sum);
-  }
-}
-
-// This CTA's rows [dh0, dh1) of a router matrix, into shared memory.
-template <typename WT>
-__device__ void load_router_rows(const Dec2Args &a, const WT *wr, WT *s_wr) {
-  const int H = a.H, E = a.E;
-  const int G = gridDim.x, c = blockIdx.x;
-  const int UH = H / 4;
-  const int dh0 = 4 * part_lo(c, UH, G), nr = 4 * part_lo(c + 1, UH, G) - dh0;
-  // eight loads in flight per thread before any store
-  for (int i0 = threadIdx.x; i0 < E * nr; i0 += 8 * blockDim.x) {
-    WT v[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i = i0 + u * blockDim.x;
-      if (i < E * nr) {
-        const int e = i / nr, r = i - e * nr;
-        v[u] = __ldg(wr + (size_t)e * H + dh0 + r);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i = i0 + u * blockDim.x;
-      if (i < E * nr) s_wr[i] = v[u];
-    }
-  }
-}
 
 template <typename WT, bool kOne, bool kFast>
 __global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
@@ -1522,56 +1230,6 @@ extern "C" int coli_trace_read(void *lo, void *hi) {
 }
 #endif
 
-namespace {
-
-template <typename K>
-cudaError_t launch(K kernel, int grid, int block, size_t smem, cudaStream_t s, bool pdl,
-                   const Dec2Args &args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(block);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kernel, args);
-}
-
-size_t al16(size_t v) { return (v + 15) & ~(size_t)15; }
-size_t al128(size_t v) { return (v + 127) & ~(size_t)127; }
-
-int max_smem() {
-  static int v = 0;
-  if (!v) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-      v = 227 * 1024;
-  }
-  return v;
-}
-
-// Raise a kernel's dynamic shared-memory limit once per device (the limit is
-// only ever raised, so later smaller launches need no call).
-template <typename K>
-cudaError_t allow_smem(K kernel, size_t bytes) {
-  static std::mutex mu;
-  static std::unordered_map<const void *, size_t> done[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  size_t &cur = done[dev][(const void *)kernel];
-  if (bytes <= cur) return cudaSuccess;
-  cudaError_t e =
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e == cudaSuccess) cur = bytes;
-  return e;
-}
-
-}  // namespace
 
 static cudaError_t plan_down_multi(Dec2Args &a);
 
