@@ -203,6 +203,87 @@ int coli_moe_forward_noalloc(const coli_moe_desc *d, int top_k, const void *x,
                              cudaStream_t stream);
 
 /*
+ * Tiered expert store ([P1] §四 "三层存储层级": each expert is read from the
+ * tier that holds it -- VRAM, RAM, NVMe -- and placement changes speed, never
+ * the result; §十一 place / overlap / learn; §三 LFRU admission).  On GB300
+ * the two tiers are an HBM pool of expert slots and the full store in pinned
+ * host memory, which the GPU reads directly over NVLink-C2C: a layer streams
+ * its resident experts from HBM and its missing ones from host memory in the
+ * same kernels, and a policy step then uploads experts that have earned a
+ * slot.  Every array is device memory unless said otherwise.
+ *   slot_of      int32 [E + S]   slot of each expert, or -1 (not resident)
+ *   slot_owner   int32 [n_slots] expert in each slot, or -1 (free)
+ *   pool_packed  uint8 [n_slots][coli_expert_packed_bytes(H, F)] resident records
+ *   pool_scales  f32   [n_slots][coli_expert_scale_count(H, F)]
+ *   heat         uint32 [E]  route counts with exponential decay (LFRU frequency)
+ *   last         uint32 [E]  tick of each expert's last route (LFRU recency)
+ *   clock        uint32 [1]  policy ticks so far
+ *   uploads      uint32 [1 + 2 * max_uploads]  written by coli_tier_update:
+ *                the number of uploads of its tick, then (expert, slot) pairs
+ * Zero heat, last and clock before the first use; slot_of and slot_owner must
+ * describe the same placement (coli_tier_place fills the slots they name).
+ * Shared experts (E .. E+S-1) may be placed in slots; the policy never evicts
+ * them and never admits them.
+ */
+typedef struct {
+    int32_t n_slots;
+    int32_t max_uploads;
+    int32_t *slot_of;
+    int32_t *slot_owner;
+    uint8_t *pool_packed;
+    float *pool_scales;
+    uint32_t *heat;
+    uint32_t *last;
+    uint32_t *clock;
+    uint32_t *uploads;
+} coli_tier;
+
+/*
+ * coli_moe_forward_tiered -- coli_moe_forward with each expert read from its
+ * slot of the HBM pool when resident, else from host_packed / host_scales:
+ * the full store (every expert, the expert record layout above) in pinned,
+ * device-accessible host memory (cudaHostAlloc / cudaHostRegister; host
+ * pointers).  Results are bit-identical to coli_moe_forward on the same
+ * experts.  COLI_EINVAL if the store is not pinned host memory.
+ */
+int coli_moe_forward_tiered(const coli_moe_desc *d, int top_k, const void *x,
+                            const void *router_w, const uint8_t *host_packed,
+                            const float *host_scales, const coli_tier *tier, float *out,
+                            uint32_t *route_counts, void *workspace, size_t ws_bytes,
+                            cudaStream_t stream);
+
+/*
+ * coli_tier_place -- copy every expert named in slot_owner from the host
+ * store into its slot (initial placement).  Asynchronous on `stream`.
+ */
+int coli_tier_place(const coli_moe_desc *d, const uint8_t *host_packed, const float *host_scales,
+                    const coli_tier *tier, cudaStream_t stream);
+
+/*
+ * coli_tier_update -- one LFRU policy tick after a layer call, then the
+ * uploads it decides, copied from the host store into the pool ([P1] §三).
+ * call_counts [E] (device uint32): route counts of that call alone.
+ *   clock += 1
+ *   heat[e] = heat[e] - (heat[e] >> 3) + call_counts[e]   (saturating)
+ *   last[e] = clock for every e with call_counts[e] > 0
+ *   score(e) = heat[e] * 256 + recent(e), recent = 255 - (clock - last[e]) if
+ *              that is positive, else 0: frequency first, recency only breaks
+ *              close calls (a route is worth more than any recency)
+ *   candidates: routed experts used in the call and not resident, by
+ *   decreasing score (equal scores: lower id first).  For each, the target
+ *   slot is the lowest free slot (cold heat 0) or else the resident routed
+ *   expert of lowest score (equal: lowest slot), and the candidate moves in
+ *   if heat[c] > cold + cold / 4 + 4 (in 64 bits: a saturated counter never
+ *   wraps the threshold).  At most max_uploads moves per tick; their (expert,
+ *   slot) pairs go to uploads.  Experts admitted this tick are not evicted in
+ *   the same tick.
+ * Asynchronous on `stream`; the policy runs on the GPU (no host sync).
+ */
+int coli_tier_update(const coli_moe_desc *d, const uint32_t *call_counts,
+                     const uint8_t *host_packed, const float *host_scales, const coli_tier *tier,
+                     cudaStream_t stream);
+
+/*
  * coli_moe_stack_forward -- n_layers MoE layers chained through a residual
  * stream (decode stack without attention or norms):
  *   x_0 = x;  x_{l+1} = x_l + MoE_l(x_l);  x_out = x_{n_layers}

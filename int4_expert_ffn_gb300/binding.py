@@ -33,7 +33,7 @@ EXPORTS = (
     "coli_router_workspace_size", "coli_moe_workspace_size", "coli_router_topk",
     "coli_moe_forward", "coli_moe_forward_noalloc", "coli_moe_stack_forward",
     "coli_profile_events", "coli_moe_check", "coli_usage_engine_id", "coli_usage_save",
-    "coli_usage_load",
+    "coli_usage_load", "coli_moe_forward_tiered", "coli_tier_place", "coli_tier_update",
 )
 
 
@@ -51,6 +51,13 @@ class coli_moe_desc(C.Structure):
                 ("n_shared", C.c_int32), ("n_tokens", C.c_int32), ("x_dtype", C.c_int),
                 ("router_dtype", C.c_int), ("router_fn", C.c_int32),
                 ("router_bias", C.c_void_p)]
+
+
+class coli_tier(C.Structure):
+    _fields_ = [("n_slots", C.c_int32), ("max_uploads", C.c_int32), ("slot_of", C.c_void_p),
+                ("slot_owner", C.c_void_p), ("pool_packed", C.c_void_p),
+                ("pool_scales", C.c_void_p), ("heat", C.c_void_p), ("last", C.c_void_p),
+                ("clock", C.c_void_p), ("uploads", C.c_void_p)]
 
 
 def _load():
@@ -96,6 +103,13 @@ def _load():
     L.coli_usage_load.argtypes = [C.c_char_p, vp, C.c_int32, C.c_int32, C.c_char_p, C.c_int,
                                   C.POINTER(C.c_int64)]
     L.coli_usage_load.restype = C.c_int
+    tp = C.POINTER(coli_tier)
+    L.coli_moe_forward_tiered.argtypes = [dp, C.c_int, vp, vp, vp, vp, tp, vp, vp, vp, sz, vp]
+    L.coli_moe_forward_tiered.restype = C.c_int
+    L.coli_tier_place.argtypes = [dp, vp, vp, tp, vp]
+    L.coli_tier_place.restype = C.c_int
+    L.coli_tier_update.argtypes = [dp, vp, vp, vp, tp, vp]
+    L.coli_tier_update.restype = C.c_int
     return L
 
 
@@ -287,6 +301,79 @@ def coli_moe_check(workspace, clear=True, stream=None):
     if st not in (COLI_OK, COLI_ETIMEOUT):
         raise ColiError("coli_moe_check", st)
     return flags.value
+
+
+class Tier:
+    """Device state of a tiered expert store (coli_tier in coli.h): a pool of
+    n_slots expert records in HBM and the LFRU policy state.  ``owners`` is the
+    initial expert of each slot (-1 free); the pool itself is filled by
+    coli_tier_place from the host store."""
+
+    def __init__(self, desc: MoEDesc, owners, max_uploads=8, device="cuda"):
+        E, S = desc.n_experts, desc.n_shared
+        n = len(owners)
+        eb = coli_expert_packed_bytes(desc.hidden, desc.ffn)
+        es = coli_expert_scale_count(desc.hidden, desc.ffn)
+        slot_of = [-1] * (E + S)
+        for sl, e in enumerate(owners):
+            if e >= 0:
+                slot_of[e] = sl
+        self.n_slots, self.max_uploads = n, max_uploads
+        self.slot_of = torch.tensor(slot_of, dtype=torch.int32, device=device)
+        self.slot_owner = torch.tensor(list(owners) or [0], dtype=torch.int32, device=device)[:n]
+        self.pool_packed = torch.empty(max(n, 1) * eb, dtype=torch.uint8, device=device)
+        self.pool_scales = torch.empty(max(n, 1) * es, dtype=torch.float32, device=device)
+        self.heat = torch.zeros(E, dtype=torch.int32, device=device)
+        self.last = torch.zeros(E, dtype=torch.int32, device=device)
+        self.clock = torch.zeros(1, dtype=torch.int32, device=device)
+        self.uploads = torch.zeros(1 + 2 * max(max_uploads, 1), dtype=torch.int32, device=device)
+
+    def c(self):
+        return coli_tier(self.n_slots, self.max_uploads, self.slot_of.data_ptr(),
+                         self.slot_owner.data_ptr(), self.pool_packed.data_ptr(),
+                         self.pool_scales.data_ptr(), self.heat.data_ptr(), self.last.data_ptr(),
+                         self.clock.data_ptr(), self.uploads.data_ptr())
+
+
+def _pinned(*ts):
+    for t in ts:
+        if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+            raise ValueError("the host store must be contiguous pinned host tensors")
+
+
+def coli_moe_forward_tiered(desc: MoEDesc, top_k, x, router_w, host_packed, host_scales,
+                            tier: Tier, workspace, out=None, route_counts=None, stream=None):
+    """coli_moe_forward over a tiered store: experts from their HBM slots when
+    resident, else from the pinned host store."""
+    _cuda(x, router_w, workspace, out, route_counts)
+    _pinned(host_packed, host_scales)
+    if out is None:
+        out = torch.empty((desc.n_tokens, desc.hidden), dtype=torch.float32, device=x.device)
+    d, t = desc.c(), tier.c()
+    _check("coli_moe_forward_tiered", lib.coli_moe_forward_tiered(
+        C.byref(d), top_k, _ptr(x), _ptr(router_w), _ptr(host_packed), _ptr(host_scales),
+        C.byref(t), _ptr(out), _ptr(route_counts), _ptr(workspace), workspace.numel(),
+        _stream(stream)))
+    return out
+
+
+def coli_tier_place(desc: MoEDesc, host_packed, host_scales, tier: Tier, stream=None):
+    _pinned(host_packed, host_scales)
+    d, t = desc.c(), tier.c()
+    _check("coli_tier_place", lib.coli_tier_place(C.byref(d), _ptr(host_packed),
+                                                   _ptr(host_scales), C.byref(t),
+                                                   _stream(stream)))
+
+
+def coli_tier_update(desc: MoEDesc, call_counts, host_packed, host_scales, tier: Tier,
+                     stream=None):
+    """One LFRU policy tick from a call's route counts, then its uploads."""
+    _cuda(call_counts)
+    _pinned(host_packed, host_scales)
+    d, t = desc.c(), tier.c()
+    _check("coli_tier_update", lib.coli_tier_update(C.byref(d), _ptr(call_counts),
+                                                     _ptr(host_packed), _ptr(host_scales),
+                                                     C.byref(t), _stream(stream)))
 
 
 def coli_usage_engine_id(engine):

@@ -164,8 +164,9 @@ int device_parts(int *parts) {
 }
 
 Dec2Args make_args(const coli_moe_desc *d, int k, int tn, uint8_t *ws, const WsLayout &L,
-                   int parts) {
+                   int parts, const TierMap *tier = nullptr) {
   Dec2Args a{};
+  if (tier) a.tier = *tier;
   a.T = tn;
   a.H = d->hidden;
   a.F = d->ffn;
@@ -296,7 +297,7 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
                     coli_dtype x_dtype, const void *router_w, const uint8_t *packed,
                     const float *scales, float *out, bool residual, float *layer_out,
                     uint32_t *route_counts, void *workspace, const WsLayout &L,
-                    cudaStream_t stream) {
+                    cudaStream_t stream, const TierMap *tier) {
   const int H = d->hidden, F = d->ffn, E = d->n_experts, S = d->n_shared;
   const size_t wr_stride = (size_t)E * H * xsize(d->router_dtype);
   const size_t pk_stride = (size_t)(E + S) * coli_expert_packed_bytes(H, F);
@@ -305,7 +306,7 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
   int parts = 0;
   const int st = device_parts(&parts);
   if (st != COLI_OK) return st;
-  Dec2Args a = make_args(d, k, tn, (uint8_t *)workspace, L, parts);
+  Dec2Args a = make_args(d, k, tn, (uint8_t *)workspace, L, parts, tier);
   a.chain = n_layers > 1;
   // one token at shapes of whole 1024-column chunks: one fused kernel per
   // layer (decode1.cu); otherwise the gate/up and down GEMV kernels
@@ -389,7 +390,7 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
 static int prefill_run(const coli_moe_desc *d, int k, int n_layers, const void *x,
                        const void *router_w, const uint8_t *packed, const float *scales,
                        float *out, bool residual, float *layer_out, uint32_t *route_counts,
-                       void *workspace, cudaStream_t stream) {
+                       void *workspace, cudaStream_t stream, const TierMap *tier) {
   const int T = d->n_tokens, H = d->hidden, F = d->ffn, E = d->n_experts, S = d->n_shared;
   const PrefillLayout L = prefill_layout(T, H, F, E, S, k);
   uint8_t *ws = (uint8_t *)workspace;
@@ -398,6 +399,7 @@ static int prefill_run(const coli_moe_desc *d, int k, int n_layers, const void *
   const size_t sc_stride = (size_t)(E + S) * coli_expert_scale_count(H, F);
   for (int l = 0; l < n_layers; ++l) {
     PrefillArgs a{};
+    if (tier) a.tier = *tier;
     a.T = T; a.H = H; a.F = F; a.E = E; a.S = S; a.k = k;
     a.router_fn = d->router_fn;
     a.router_bias = (d->router_fn == COLI_ROUTER_SIGMOID_BIAS && d->router_bias)
@@ -435,10 +437,11 @@ static int prefill_run(const coli_moe_desc *d, int k, int n_layers, const void *
 
 static int moe_run(const coli_moe_desc *d, int k, int n_layers, const void *x, const void *router_w,
                    const uint8_t *packed, const float *scales, float *out, bool residual,
-                   float *layer_out, uint32_t *route_counts, void *workspace, cudaStream_t stream) {
+                   float *layer_out, uint32_t *route_counts, void *workspace, cudaStream_t stream,
+                   const TierMap *tier = nullptr) {
   if (use_prefill(d))
     return prefill_run(d, k, n_layers, x, router_w, packed, scales, out, residual, layer_out,
-                       route_counts, workspace, stream);
+                       route_counts, workspace, stream, tier);
   const int T = d->n_tokens, H = d->hidden;
   const int TP = pass_tokens(T);
   const WsLayout L = ws_layout(TP, H, d->ffn, d->n_experts, d->n_shared, k);
@@ -448,11 +451,32 @@ static int moe_run(const coli_moe_desc *d, int k, int n_layers, const void *x, c
     const void *xp = (const char *)x + xo * xsize(d->x_dtype);
     const int st = moe_pass(d, k, n_layers, tn, xp, d->x_dtype, router_w, packed, scales,
                             out + xo, residual, layer_out ? layer_out + xo : nullptr,
-                            route_counts, workspace, L, stream);
+                            route_counts, workspace, L, stream, tier);
     if (st != COLI_OK) return st;
   }
   return COLI_OK;
 }
+
+}  // extern "C"
+
+// The layer forward over a tiered expert store (tier.cu validates the map).
+int coli::moe_forward_tiered(const coli_moe_desc *d, int top_k, const void *x,
+                             const void *router_w, const uint8_t *packed, const float *scales,
+                             const TierMap &tier, float *out, uint32_t *route_counts,
+                             void *workspace, size_t ws_bytes, cudaStream_t stream) {
+  int st = check_desc(d, top_k);
+  if (st) return st;
+  if (d->n_tokens == 0) return COLI_OK;
+  if (!x || !router_w || !packed || !scales || !out || !workspace) return COLI_EINVAL;
+  if (!aligned16(x) || !aligned16(router_w) || !aligned16(packed) || !aligned16(scales) ||
+      !aligned16(out) || ((uintptr_t)workspace & 255u))
+    return COLI_EALIGN;
+  if (ws_bytes < coli_moe_workspace_size(d, top_k)) return COLI_ENOMEM;
+  return moe_run(d, top_k, 1, x, router_w, packed, scales, out, false, nullptr, route_counts,
+                 workspace, stream, &tier);
+}
+
+extern "C" {
 
 int coli_moe_forward(const coli_moe_desc *d, int top_k, const void *x, const void *router_w,
                      const uint8_t *packed_experts, const float *scales, float *out,

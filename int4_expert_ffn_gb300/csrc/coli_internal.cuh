@@ -89,8 +89,34 @@ struct L1Smem {
   size_t bar, lst, red, xn, wr, hacc, u, ring, total;
 };
 
+// Tiered expert store of one layer (coli_moe_forward_tiered): experts whose
+// slot_of entry is >= 0 live in that slot of the HBM pool; the others are read
+// from the layer's own store (pinned host memory, device-accessible).  All
+// null: every expert in the layer's store.
+struct TierMap {
+  const int32_t *slot_of;       // [E + S]
+  const uint8_t *pool_packed;   // [n_slots] expert records
+  const float *pool_scales;
+};
+
+// Expert e's record: its HBM slot when the tier map holds it, else its place
+// in the layer's store.
+__device__ __forceinline__ void expert_record(const TierMap &t, const uint8_t *packed,
+                                              const float *scales, int64_t eb, int64_t es, int e,
+                                              const uint8_t **pk, const float **sc) {
+  const int slot = t.slot_of ? __ldg(t.slot_of + e) : -1;
+  if (slot >= 0) {
+    *pk = t.pool_packed + (int64_t)slot * eb;
+    *sc = t.pool_scales + (int64_t)slot * es;
+  } else {
+    *pk = packed + (int64_t)e * eb;
+    *sc = scales + (int64_t)e * es;
+  }
+}
+
 // Arguments of the decode kernels (one layer, T <= kDecodeMaxT tokens).
 struct Dec2Args {
+  TierMap tier;
   int T, H, F, E, S, k;
   int layer;                // index of the layer in the stack (phase tracing only)
   int fx;                   // router partials as fixed-point sums (T*E <= kFxMaxTE)
@@ -163,6 +189,7 @@ struct Dec2Args {
 constexpr int kPrefillMinT = 64;      // calls with at least this many tokens take it
 constexpr int kGroupTokens = 256;     // tokens per block of the counting sort
 struct PrefillArgs {
+  TierMap tier;
   int T, H, F, E, S, k;
   int router_fn;            // coli_router_fn
   const float *router_bias; // [E] (sigmoid router) or null
@@ -215,6 +242,12 @@ cudaError_t launch_quant_i4g(const void *w, int w_dtype, int64_t rows, int64_t c
                              uint8_t *packed, float *scales, cudaStream_t s);
 
 int num_sms();
+// The layer forward over a tiered expert store (coli_api.cu); `packed` and
+// `scales` are device-accessible addresses of the full store.
+int moe_forward_tiered(const coli_moe_desc *d, int top_k, const void *x, const void *router_w,
+                       const uint8_t *packed, const float *scales, const TierMap &tier,
+                       float *out, uint32_t *route_counts, void *workspace, size_t ws_bytes,
+                       cudaStream_t stream);
 // Records the caller's profiling event before (is_after false: claims a slot)
 // or after a launch of `kernel` if coli_profile_events selected it.
 cudaError_t record_profile(int kernel, cudaStream_t s, bool is_after, size_t *slot);

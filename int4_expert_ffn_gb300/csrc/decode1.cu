@@ -514,7 +514,9 @@ extern "C" int coli_trace1_read_raw(void *buf) {
 // Plan of the fused one-token layer kernel; false when the shape is outside
 // what it handles (the GEMV kernel pair takes it).
 bool plan_layer1(Dec2Args &a) {
-  if (a.T != 1 || !a.fx || a.n_rep != 8) return false;
+  // its bulk copies read HBM only: a tiered store (experts partly in host
+  // memory) takes the GEMV kernels
+  if (a.T != 1 || !a.fx || a.n_rep != 8 || a.tier.slot_of) return false;
   if (a.H % kChunkCols || a.F % kChunkCols) return false;
   // Taken where a layer's used experts are a small share per SM (the
   // latency-bound regime: one launch instead of two, no kernel boundary

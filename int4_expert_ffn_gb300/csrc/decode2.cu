@@ -380,8 +380,11 @@ __device__ __forceinline__ void gu_copy(const Dec2Args &a, const LayerPtrs &lp,
   const int64_t rb = H / 2, ngr = H / kGroup;
   const int e = s_act_expert[k.ai];
   const int col = k.cg * kChunkCols + 32 * lane;
-  const uint8_t *pg = lp.packed + (int64_t)e * a.eb + (int64_t)k.f * rb;
-  const float *ps = lp.scales + (int64_t)e * a.es + (int64_t)k.f * ngr + k.cg * 16;
+  const uint8_t *pe;
+  const float *se;
+  expert_record(a.tier, lp.packed, lp.scales, a.eb, a.es, e, &pe, &se);
+  const uint8_t *pg = pe + (int64_t)k.f * rb;
+  const float *ps = se + (int64_t)k.f * ngr + k.cg * 16;
   float *ss = (float *)(slot + kGuSlotWeights);
   if (col < H) {
 #pragma unroll
@@ -863,9 +866,11 @@ __device__ __forceinline__ void dn_copy(const Dec2Args &a, const LayerPtrs &lp,
   const int e = s_act_expert[k.a];
   const int col = k.cg * kChunkCols + 32 * lane;
   const int r0 = 8 * k.gi, nq = nr - r0 < 8 ? nr - r0 : 8;
-  const uint8_t *pw = lp.packed + (int64_t)e * a.eb + (int64_t)F * H + (int64_t)(dh0 + r0) * rb;
-  const float *ps = lp.scales + (int64_t)e * a.es + (int64_t)2 * F * (H / kGroup) +
-                    (int64_t)(dh0 + r0) * ngr + k.cg * 16;
+  const uint8_t *pe;
+  const float *se;
+  expert_record(a.tier, lp.packed, lp.scales, a.eb, a.es, e, &pe, &se);
+  const uint8_t *pw = pe + (int64_t)F * H + (int64_t)(dh0 + r0) * rb;
+  const float *ps = se + (int64_t)2 * F * (H / kGroup) + (int64_t)(dh0 + r0) * ngr + k.cg * 16;
   float *ss = (float *)(slot + kGuSlotWeights);
   if (col < F) {
 #pragma unroll

@@ -533,8 +533,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
               a_src[j] = MODE == kModeGateUp ? p.x16 + (int64_t)p.route_tok[it.p0 + r] * H
                                              : p.h16 + (int64_t)(it.p0 + r) * F;
           }
-          const uint8_t *pk = p.packed + (int64_t)it.e * p.eb;
-          const float *sc = p.scales + (int64_t)it.e * p.es;
+          const uint8_t *pk;
+          const float *sc;
+          expert_record(p.tier, p.packed, p.scales, p.eb, p.es, it.e, &pk, &sc);
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             if (MODE == kModeGateUp) {
