@@ -16,6 +16,7 @@ independent replica on its own GPU (the decode path has no exchange step);
 `value` sums the ranks' tokens over the slowest rank's time.
 """
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -698,7 +699,7 @@ def main():
     ap.add_argument("--impl", default="coli", choices=["coli", "reference"])
     ap.add_argument("--workload", default="glm_decode_b1",
                     choices=["olmoe_decode", "glm_decode_b1", "glm_decode_b8", "glm_prefill",
-                             "quant"])
+                             "quant", "glm_tiered"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--repeats", type=int, default=20,
                     help="decode workloads: timed windows of K steps (the line reports the "
@@ -725,6 +726,12 @@ def main():
     torch.cuda.set_device(dev)
 
     from int4_expert_ffn_gb300 import synth
+    if args.workload == "glm_tiered":
+        from int4_expert_ffn_gb300 import build as b
+        if rank == 0:
+            b.build()
+        emit_tiered(args, dev, world, rank)
+        return
     if args.workload == "quant":
         from int4_expert_ffn_gb300 import build as b
         if rank == 0:
@@ -881,6 +888,148 @@ def emit_quant(args, dev, world, rank):
                      "traffic": (402740480 + 55846144) * E / 16,
                      "traffic_note": "from a 16-expert capture, scaled by experts"},
         "clocks": sampler.summary(t0, t1), "gpu_launches": 3 * args.steps,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def emit_tiered(args, dev, world, rank):
+    """Tiered store workload: one GLM-like layer (hidden 6144, 256 routed
+    experts of width 2048, top-8, 1 shared) whose full store (5.46 GB) sits in
+    pinned host memory, with an HBM pool of 128 slots holding the shared expert
+    and 127 routed experts at the start; batch 1 decode through the layer
+    with the skewed router (32 experts take about half of the routes), one LFRU
+    tick (and its uploads) after every call.  A step = one token's forward plus
+    its policy tick; missing experts are read over the host link by the expert
+    GEMVs themselves."""
+    import int4_expert_ffn_gb300 as pkg
+    from int4_expert_ffn_gb300 import synth
+    c = pkg.binding
+    shape = dataclasses.replace(synth.GLM_DECODE_B1, name="glm_tiered", layers=1)
+    H, F, E, S, k = shape.hidden, shape.ffn, shape.experts, shape.shared, shape.top_k
+    eb, es = c.coli_expert_packed_bytes(H, F), c.coli_expert_scale_count(H, F)
+    rec = eb + 4 * es
+    steps, warmup = args.steps, args.warmup
+    packed = torch.empty((E + S) * eb, dtype=torch.uint8, device=dev)
+    scales = torch.empty((E + S) * es, dtype=torch.float32, device=dev)
+    p0 = s0 = 0
+    for e in range(E + S):
+        for m in range(3):
+            w = synth.expert_matrix(shape, 0, e, m, 0, device=dev)
+            rows, cols = w.shape
+            nb, ns = rows * cols // 2, rows * cols // 64
+            c.coli_quant_i4g(w, packed[p0:p0 + nb].view(rows, -1), scales[s0:s0 + ns].view(rows, -1))
+            p0 += nb
+            s0 += ns
+    host_p = packed.cpu().pin_memory()
+    host_s = scales.cpu().pin_memory()
+    del packed, scales
+    torch.cuda.empty_cache()
+    wr = synth.router_weights(shape, 0, 0, device=dev, row_std=synth.skewed_router_std(E, H))
+    xs = torch.stack([synth.tokens(shape, 0, i, device=dev) for i in range(warmup + steps)])
+    desc = c.MoEDesc(H, F, E, S, 1, c.COLI_F32, c.COLI_BF16)
+    n_slots = 128
+    owners = [E] + list(range(1, 2 * (n_slots - 1), 2))     # the shared expert, odd-numbered routed
+    ws = c.new_workspace(desc, k)
+    stream = torch.cuda.Stream(device=dev)
+    counts = torch.zeros((warmup + steps, E), dtype=torch.int32, device=dev)
+    out = torch.empty((warmup + steps, 1, H), dtype=torch.float32, device=dev)
+
+    def run(tier, i0, i1):
+        for i in range(i0, i1):
+            c.coli_moe_forward_tiered(desc, k, xs[i], wr, host_p, host_s, tier, ws, out=out[i],
+                                      route_counts=counts[i], stream=stream)
+            c.coli_tier_update(desc, counts[i], host_p, host_s, tier, stream=stream)
+
+    # host-link reference: a pinned host -> HBM copy of 2 GB by the copy engine
+    hbuf = torch.empty(2 << 30, dtype=torch.uint8).pin_memory()
+    dbuf = torch.empty(2 << 30, dtype=torch.uint8, device=dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = 1e9
+    for _ in range(3):
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            dbuf.copy_(hbuf, non_blocking=True)
+            ev1.record(stream)
+        torch.cuda.synchronize()
+        best = min(best, ev0.elapsed_time(ev1))
+    link_gbs = (2 << 30) / (best / 1e3) / 1e9
+    del hbuf, dbuf
+    # timed: warm-up steps, then K steps, from a fresh placement
+    tier = c.Tier(desc, owners, max_uploads=8, device=dev)
+    c.coli_tier_place(desc, host_p, host_s, tier, stream=stream)
+    with torch.cuda.stream(stream):
+        run(tier, 0, warmup)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[0]))
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        run(tier, warmup, warmup + steps)
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    time.sleep(0.15)
+    sampler.stop()
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+    # the same sequence again from the same placement, one step at a time, to
+    # count what the timed steps read from host memory and uploaded (the
+    # policy is deterministic: same inputs, same placements)
+    tier2 = c.Tier(desc, owners, max_uploads=8, device=dev)
+    c.coli_tier_place(desc, host_p, host_s, tier2, stream=stream)
+    cnt2 = torch.zeros_like(counts)
+    host_bytes = up_bytes = resident_used = used = 0
+    for i in range(warmup + steps):
+        slot_of = tier2.slot_of[:E].clone()
+        with torch.cuda.stream(stream):
+            c.coli_moe_forward_tiered(desc, k, xs[i], wr, host_p, host_s, tier2, ws,
+                                      route_counts=cnt2[i], stream=stream)
+            c.coli_tier_update(desc, cnt2[i], host_p, host_s, tier2, stream=stream)
+        torch.cuda.synchronize()
+        if i < warmup:
+            continue
+        u = (cnt2[i] > 0)
+        miss = int((u & (slot_of < 0)).sum())
+        used += int(u.sum())
+        resident_used += int(u.sum()) - miss
+        host_bytes += miss * rec
+        up_bytes += int(tier2.uploads[0]) * rec
+    assert torch.equal(cnt2[warmup:], counts[warmup:]), "the replay routed differently"
+    sec = ms / 1e3
+    hbm_peak, _, peak_kind = read_peaks()
+    line = {
+        "metric": "MoE decode tokens/s over a tiered expert store (HBM pool + pinned host memory)",
+        "value": world * steps / sec, "unit": "tokens/s", "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": ("int4 weights x 15-bit fixed-point activations (dp4a, exact int32 dot), "
+                  "f32 scale and accumulate"),
+        "data": "synthetic (seeded; weights N(0,0.02) bf16 quantised on the GPU)",
+        "config": {"workload": "glm_tiered: 1 MoE layer, hidden 6144, 256 experts of FFN width "
+                               "2048, top-8, 1 shared, batch 1; store of 257 experts (%.2f GB) "
+                               "in pinned host memory, HBM pool of %d slots (the shared expert "
+                               "and 127 routed at the start); skewed router; one LFRU tick and "
+                               "its uploads after every call" % ((E + S) * rec / 1e9, n_slots),
+                   "l2": "inputs larger than L2"},
+        "host_link": {"read_gbs": host_bytes / sec / 1e9, "upload_gbs": up_bytes / sec / 1e9,
+                      "peak_gbs": link_gbs,
+                      "peak_kind": "measured: pinned host -> HBM copy of 2 GB by the copy engine",
+                      "frac": (host_bytes + up_bytes) / sec / 1e9 / link_gbs,
+                      "host_bytes_per_step": host_bytes / steps,
+                      "upload_bytes_per_step": up_bytes / steps,
+                      "resident_hit_rate": resident_used / max(1, used)},
+        "roofline": {"bound": "hbm", "kernel": "whole step", "achieved": None, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": None, "peak_kind": peak_kind, "traffic": None,
+                     "note": "the host link bounds this workload; see host_link"},
+        "clocks": sampler.summary(t0, t1), "gpu_launches": steps * 5,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
