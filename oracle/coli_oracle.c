@@ -340,3 +340,206 @@ int orc_moe_forward_router(const double *x, int64_t T, int64_t H, int64_t F, int
     free(logits);
     return nan_tokens;
 }
+
+/* ---------------------------------------------------------------------- */
+/* Other container formats of the engine's registry ([P2] §权重转换 lists
+ * "7 MXFP4" and "8 fp8-e4m3-b128"; [P1] §十 "从 int4 到 MXFP4").  The pages
+ * name them only; their definitions are the public ones:
+ *
+ * MXFP4 (OCP Microscaling Formats v1.0): blocks of 32 consecutive elements
+ * of a row share one E8M0 scale X = 2^(e - 127) (a biased exponent byte);
+ * each element is FP4 E2M1 (1 sign, 2 exponent, 1 mantissa bit, bias 1):
+ * magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6.  Conversion of a block: shared
+ * exponent = floor(log2(max|v|)) - 2 (2 = the largest E2M1 exponent), then
+ * each v / X rounded to nearest E2M1, ties to the even mantissa, saturating
+ * at 6.  Storage, as the int4 container: codes packed two per byte, even
+ * column in the low nibble; scales one byte per 32 columns.
+ * Readings (design notes): an all-zero block stores e = 0 and codes 0; a NaN
+ * element is ignored by the max and stored as +0; the shared exponent is
+ * clamped to [-127, 127]; the sign of a value that rounds to zero is kept. */
+
+#define ORC_MX_BLOCK 32
+
+int64_t orc_mx_row_bytes(int64_t cols) { return (cols + 1) / 2; }
+int64_t orc_mx_scales_per_row(int64_t cols) { return (cols + ORC_MX_BLOCK - 1) / ORC_MX_BLOCK; }
+
+/* E2M1 magnitude of a 3-bit code (exponent bits 2..1, mantissa bit 0). */
+double orc_e2m1_magnitude(int m)
+{
+    const int ex = (m >> 1) & 3, man = m & 1;
+    if (ex == 0) return man ? 0.5 : 0.0;                 /* subnormal: m * 2^(1-1) / 2 */
+    return (1.0 + 0.5 * man) * ldexp(1.0, ex - 1);       /* (1 + m/2) 2^(e - bias) */
+}
+
+double orc_e2m1_value(int code)
+{
+    const double v = orc_e2m1_magnitude(code & 7);
+    return (code & 8) ? -v : v;
+}
+
+/* Nearest E2M1 magnitude code of a >= 0 (f32), ties to the even mantissa,
+ * saturating at 6: every magnitude is compared, plainly. */
+static int orc_e2m1_round(float a)
+{
+    int best = 0;
+    for (int m = 1; m < 8; ++m) {
+        const double d_best = fabs((double)a - orc_e2m1_magnitude(best));
+        const double d = fabs((double)a - orc_e2m1_magnitude(m));
+        if (d < d_best || (d == d_best && (m & 1) == 0 && (best & 1) == 1)) best = m;
+    }
+    return best;
+}
+
+void orc_quant_mxfp4(const float *w, int64_t rows, int64_t cols, uint8_t *packed, uint8_t *scales)
+{
+    const int64_t rb = orc_mx_row_bytes(cols);
+    const int64_t nb = orc_mx_scales_per_row(cols);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *wr = w + r * cols;
+        uint8_t *pr = packed + r * rb;
+        memset(pr, 0, (size_t)rb);
+        for (int64_t b = 0; b < nb; ++b) {
+            const int64_t c0 = b * ORC_MX_BLOCK;
+            const int64_t c1 = (c0 + ORC_MX_BLOCK < cols) ? c0 + ORC_MX_BLOCK : cols;
+            float m = 0.0f;
+            for (int64_t c = c0; c < c1; ++c) {
+                const float a = fabsf(wr[c]);
+                if (a > m) m = a;                       /* NaN never compares greater */
+            }
+            int se = -127;
+            if (m > 0.0f) {
+                int ex;
+                frexpf(m, &ex);                         /* m = f 2^ex, f in [0.5, 1) */
+                se = (ex - 1) - 2;                      /* floor(log2 m) - emax(E2M1) */
+                if (se < -127) se = -127;
+                if (se > 127) se = 127;
+            }
+            scales[r * nb + b] = (uint8_t)(se + 127);
+            for (int64_t c = c0; c < c1; ++c) {
+                int code = 0;
+                if (m > 0.0f && wr[c] == wr[c]) {
+                    const float q = ldexpf(wr[c], -se);  /* v / X, exact */
+                    code = orc_e2m1_round(fabsf(q)) | (signbit(q) ? 8 : 0);
+                }
+                if ((c & 1) == 0) pr[c >> 1] |= (uint8_t)code;
+                else pr[c >> 1] |= (uint8_t)(code << 4);
+            }
+        }
+    }
+}
+
+/* Dequantised element: X * value(code). */
+static double orc_mx_elem(const uint8_t *packed, const uint8_t *scales, int64_t rb, int64_t nb,
+                          int64_t r, int64_t c)
+{
+    const uint8_t byte = packed[r * rb + (c >> 1)];
+    const int code = (c & 1) ? (byte >> 4) : (byte & 0x0F);
+    const int e = scales[r * nb + c / ORC_MX_BLOCK];
+    return ldexp(orc_e2m1_value(code), e - 127);
+}
+
+void orc_dequant_mxfp4(const uint8_t *packed, const uint8_t *scales, int64_t rows, int64_t cols,
+                       double *w)
+{
+    const int64_t rb = orc_mx_row_bytes(cols), nb = orc_mx_scales_per_row(cols);
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) w[r * cols + c] = orc_mx_elem(packed, scales, rb, nb, r, c);
+}
+
+/* ---------------------------------------------------------------------- */
+/* The layer over a chosen container: fmt 4 = int4-grouped (the functions
+ * above), 7 = MXFP4.  Expert record: gate | up | down, each in the format;
+ * `scales` points to f32 scales (fmt 4) or E8M0 bytes (fmt 7), expert after
+ * expert in the same order. */
+
+int64_t orc_fmt_row_bytes(int fmt, int64_t cols)
+{
+    return fmt == 7 ? orc_mx_row_bytes(cols) : orc_packed_row_bytes(cols);
+}
+/* Bytes of one row's scales. */
+int64_t orc_fmt_scale_bytes(int fmt, int64_t cols)
+{
+    return fmt == 7 ? orc_mx_scales_per_row(cols) : 4 * orc_scales_per_row(cols);
+}
+int64_t orc_fmt_expert_bytes(int fmt, int64_t H, int64_t F)
+{
+    return 2 * F * orc_fmt_row_bytes(fmt, H) + H * orc_fmt_row_bytes(fmt, F);
+}
+int64_t orc_fmt_expert_scale_bytes(int fmt, int64_t H, int64_t F)
+{
+    return 2 * F * orc_fmt_scale_bytes(fmt, H) + H * orc_fmt_scale_bytes(fmt, F);
+}
+
+static void orc_matvec_fmt(int fmt, const uint8_t *packed, const uint8_t *scales, int64_t rows,
+                           int64_t cols, const double *x, double *y)
+{
+    if (fmt != 7) {
+        orc_matvec_i4g(packed, (const float *)scales, rows, cols, x, y);
+        return;
+    }
+    const int64_t rb = orc_mx_row_bytes(cols), nb = orc_mx_scales_per_row(cols);
+    for (int64_t r = 0; r < rows; ++r) {
+        double acc = 0.0;
+        for (int64_t c = 0; c < cols; ++c) acc += orc_mx_elem(packed, scales, rb, nb, r, c) * x[c];
+        y[r] = acc;
+    }
+}
+
+/* y = Wd (silu(Wg x) * (Wu x)) over the chosen container. */
+void orc_expert_fmt(int fmt, const uint8_t *pe, const uint8_t *se, int64_t H, int64_t F,
+                    const double *x, double *y)
+{
+    const uint8_t *pg = pe, *pu = pg + F * orc_fmt_row_bytes(fmt, H);
+    const uint8_t *pd = pu + F * orc_fmt_row_bytes(fmt, H);
+    const uint8_t *sg = se, *su = sg + F * orc_fmt_scale_bytes(fmt, H);
+    const uint8_t *sd = su + F * orc_fmt_scale_bytes(fmt, H);
+    double *g = (double *)malloc((size_t)F * sizeof(double));
+    double *u = (double *)malloc((size_t)F * sizeof(double));
+    orc_matvec_fmt(fmt, pg, sg, F, H, x, g);
+    orc_matvec_fmt(fmt, pu, su, F, H, x, u);
+    for (int64_t f = 0; f < F; ++f) g[f] = orc_silu(g[f]) * u[f];
+    orc_matvec_fmt(fmt, pd, sd, H, F, g, y);
+    free(g);
+    free(u);
+}
+
+/* orc_moe_forward_router over the chosen container (same routing, order and
+ * accumulation; only the weights' decoding differs). */
+int orc_moe_forward_fmt(int fmt, const double *x, int64_t T, int64_t H, int64_t F, int64_t E,
+                        int64_t n_shared, const double *wr, int router_fn, const double *bias,
+                        const uint8_t *packed, const uint8_t *scales, int k, double *out,
+                        int32_t *idx, double *gates, uint32_t *counts)
+{
+    const int64_t eb = orc_fmt_expert_bytes(fmt, H, F);
+    const int64_t es = orc_fmt_expert_scale_bytes(fmt, H, F);
+    double *logits = (double *)malloc((size_t)(T * E) * sizeof(double));
+    int nan_tokens = 0;
+    orc_router_logits(x, wr, T, H, E, logits);
+    for (int64_t t = 0; t < T; ++t) {
+        nan_tokens += router_fn == 1
+            ? orc_topk_sigmoid(logits + t * E, bias, E, k, idx + t * k, gates + t * k)
+            : orc_topk(logits + t * E, E, k, idx + t * k, gates + t * k);
+        if (counts)
+            for (int j = 0; j < k; ++j) counts[idx[t * k + j]] += 1u;
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < T; ++t) {
+        double *y = (double *)malloc((size_t)H * sizeof(double));
+        double *o = out + t * H;
+        for (int64_t h = 0; h < H; ++h) o[h] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            const int64_t e = idx[t * k + j];
+            orc_expert_fmt(fmt, packed + e * eb, scales + e * es, H, F, x + t * H, y);
+            for (int64_t h = 0; h < H; ++h) o[h] += gates[t * k + j] * y[h];
+        }
+        for (int64_t s = 0; s < n_shared; ++s) {
+            const int64_t e = E + s;
+            orc_expert_fmt(fmt, packed + e * eb, scales + e * es, H, F, x + t * H, y);
+            for (int64_t h = 0; h < H; ++h) o[h] += y[h];
+        }
+        free(y);
+    }
+    free(logits);
+    return nan_tokens;
+}

@@ -13,8 +13,11 @@ __all__ = [
     "GROUP", "packed_row_bytes", "scales_per_row", "expert_packed_bytes",
     "expert_scales", "quant_i4g", "dequant_i4g", "matvec_i4g", "router_logits",
     "topk", "topk_sigmoid", "expert", "moe_forward", "moe_stack_forward", "lib",
-    "set_threads", "threads",
+    "set_threads", "threads", "quant_mxfp4", "dequant_mxfp4", "e2m1_value", "fmt_expert_bytes",
+    "fmt_expert_scale_bytes", "moe_forward_fmt", "FMT_I4G", "FMT_MXFP4",
 ]
+
+FMT_I4G, FMT_MXFP4 = 4, 7
 
 GROUP = 64
 _libs = {}
@@ -74,6 +77,19 @@ def lib():
         L.orc_moe_forward_router.argtypes = [f64p, i64, i64, i64, i64, i64, f64p, C.c_int, f64p,
                                              u8p, f32p, C.c_int, f64p, i32p, f64p, u32p]
         L.orc_moe_forward_router.restype = C.c_int
+        u8 = C.POINTER(C.c_uint8)
+        L.orc_quant_mxfp4.argtypes = [f32p, i64, i64, u8, u8]
+        L.orc_quant_mxfp4.restype = None
+        L.orc_dequant_mxfp4.argtypes = [u8, u8, i64, i64, f64p]
+        L.orc_dequant_mxfp4.restype = None
+        L.orc_e2m1_value.argtypes = [C.c_int]
+        L.orc_e2m1_value.restype = C.c_double
+        for f in ("orc_fmt_expert_bytes", "orc_fmt_expert_scale_bytes"):
+            getattr(L, f).argtypes = [C.c_int, i64, i64]
+            getattr(L, f).restype = i64
+        L.orc_moe_forward_fmt.argtypes = [C.c_int, f64p, i64, i64, i64, i64, i64, f64p, C.c_int,
+                                          f64p, u8, u8, C.c_int, f64p, i32p, f64p, u32p]
+        L.orc_moe_forward_fmt.restype = C.c_int
         _libs[key] = L
     return _libs[key]
 
@@ -221,3 +237,65 @@ def moe_stack_forward(x0, layers, H, F, E, n_shared, k, counts=None, router="sof
         idxs.append(idx)
         x = x + out
     return x, outs, idxs
+
+
+# ---------------------------------------------------------------------------
+# other container formats (MXFP4)
+
+
+def quant_mxfp4(w):
+    """w: [rows, cols] float32 -> (packed u8 [rows, ceil(cols/2)], E8M0 scales u8
+    [rows, ceil(cols/32)])."""
+    w = _c(w, np.float32)
+    rows, cols = w.shape
+    packed = np.zeros((rows, (cols + 1) // 2), np.uint8)
+    scales = np.zeros((rows, (cols + 31) // 32), np.uint8)
+    lib().orc_quant_mxfp4(_p(w, C.c_float), rows, cols, _p(packed, C.c_uint8),
+                          _p(scales, C.c_uint8))
+    return packed, scales
+
+
+def dequant_mxfp4(packed, scales, cols):
+    packed, scales = _c(packed, np.uint8), _c(scales, np.uint8)
+    rows = packed.shape[0]
+    w = np.zeros((rows, cols), np.float64)
+    lib().orc_dequant_mxfp4(_p(packed, C.c_uint8), _p(scales, C.c_uint8), rows, cols,
+                            _p(w, C.c_double))
+    return w
+
+
+def e2m1_value(code):
+    return float(lib().orc_e2m1_value(int(code)))
+
+
+def fmt_expert_bytes(fmt, H, F):
+    return int(lib().orc_fmt_expert_bytes(fmt, H, F))
+
+
+def fmt_expert_scale_bytes(fmt, H, F):
+    return int(lib().orc_fmt_expert_scale_bytes(fmt, H, F))
+
+
+def moe_forward_fmt(fmt, x, wr, packed, scales, H, F, E, n_shared, k, counts=None,
+                    router="softmax", bias=None):
+    """moe_forward over the container `fmt` (FMT_I4G: scales f32; FMT_MXFP4:
+    scales are E8M0 bytes), experts 0..E+S-1 in the record layout."""
+    x, wr = _c(x, np.float64), _c(wr, np.float64)
+    packed = _c(packed.reshape(-1), np.uint8)
+    scales = _c(np.asarray(scales).reshape(-1).view(np.uint8), np.uint8)
+    T = x.shape[0]
+    out = np.zeros((T, H), np.float64)
+    idx = np.zeros((T, k), np.int32)
+    gates = np.zeros((T, k), np.float64)
+    cp = None
+    if counts is not None:
+        assert counts.dtype == np.uint32 and counts.flags.c_contiguous
+        cp = _p(counts, C.c_uint32)
+    fn = {"softmax": 0, "sigmoid": 1}[router]
+    b64 = None if bias is None else _c(bias, np.float64)
+    bp = None if b64 is None else _p(b64, C.c_double)
+    nan = lib().orc_moe_forward_fmt(fmt, _p(x, C.c_double), T, H, F, E, n_shared,
+                                    _p(wr, C.c_double), fn, bp, _p(packed, C.c_uint8),
+                                    _p(scales, C.c_uint8), k, _p(out, C.c_double),
+                                    _p(idx, C.c_int32), _p(gates, C.c_double), cp)
+    return out, idx, gates, int(nan)
