@@ -87,7 +87,26 @@ typedef struct {
     const float *router_bias; /* COLI_ROUTER_SIGMOID_BIAS: device f32 [E] per layer
                                  ([n_layers][E] for the stack), 4-byte aligned,
                                  read-only; NULL = zero bias.  Ignored otherwise. */
+    int32_t weight_fmt;    /* coli_weight_fmt of the expert records; 0 = int4-grouped */
 } coli_moe_desc;
+
+/*
+ * Expert weight containers (the engine's format registry, [P2] §权重转换:
+ * "4 int4-grouped", "7 MXFP4"; [P1] §十 "从 int4 到 MXFP4").
+ *   COLI_FMT_I4G    int4-grouped, the format above: nibbles + f32 scale per 64
+ *   COLI_FMT_MXFP4  OCP Microscaling MXFP4: blocks of 32 columns share one
+ *                   E8M0 scale byte e (X = 2^(e - 127)); each element is an
+ *                   FP4 E2M1 code (sign bit 3; magnitudes 0, .5, 1, 1.5, 2, 3,
+ *                   4, 6), packed two per byte, even column in the low nibble:
+ *                     packed uint8 [O][ceil(I/2)], scales uint8 [O][ceil(I/32)]
+ *                   and W[o][i] = X[o][i/32] * e2m1(code).  The expert record
+ *                   and its scales keep the gate | up | down order; `scales`
+ *                   arguments then point to these bytes.  MXFP4 layers run on
+ *                   the tensor-core grouped GEMM at every token count, and
+ *                   need hidden % 256 == 0 and ffn % 128 == 0; the decoded
+ *                   weights must lie in the fp16 range (as the activations).
+ */
+typedef enum { COLI_FMT_I4G = 4, COLI_FMT_MXFP4 = 7 } coli_weight_fmt;
 
 const char *coli_status_str(int status);
 
@@ -100,6 +119,12 @@ int64_t coli_packed_row_bytes(int64_t cols);            /* ceil(cols/2) */
 int64_t coli_scales_per_row(int64_t cols);              /* ceil(cols/64) */
 int64_t coli_expert_packed_bytes(int64_t H, int64_t F); /* 2 F ceil(H/2) + H ceil(F/2) */
 int64_t coli_expert_scale_count(int64_t H, int64_t F);  /* 2 F ceil(H/64) + H ceil(F/64) */
+/* The same for a chosen container: bytes of a packed row, of a row's scales,
+ * of an expert record and of its scales (0 for an unknown format). */
+int64_t coli_fmt_row_bytes(int32_t fmt, int64_t cols);
+int64_t coli_fmt_scale_bytes(int32_t fmt, int64_t cols);
+int64_t coli_fmt_expert_bytes(int32_t fmt, int64_t H, int64_t F);
+int64_t coli_fmt_expert_scale_bytes(int32_t fmt, int64_t H, int64_t F);
 
 /*
  * coli_quant_i4g -- quantise W[rows][cols] into the int4-grouped format
@@ -118,6 +143,20 @@ int64_t coli_expert_scale_count(int64_t H, int64_t F);  /* 2 F ceil(H/64) + H ce
  */
 int coli_quant_i4g(const void *w, coli_dtype w_dtype, int64_t rows, int64_t cols,
                    uint8_t *packed, float *scales, cudaStream_t stream);
+
+/*
+ * coli_quant_mxfp4 -- quantise W[rows][cols] into MXFP4 (COLI_FMT_MXFP4, OCP
+ * Microscaling v1.0).  Per row and block of 32 columns: shared exponent
+ * se = floor(log2 max|w|) - 2, clamped to [-127, 127]; scale byte se + 127;
+ * code of each w = the E2M1 value nearest to w / 2^se, ties to the even
+ * mantissa, saturating at 6, with w's sign.  An all-zero block stores scale
+ * byte 0 and codes 0; a NaN weight is ignored by the max and stored as +0.
+ *   w       [rows][cols] row-major, dtype w_dtype (COLI_BF16 or COLI_F32)
+ *   packed  [rows][ceil(cols/2)] written;  scales [rows][ceil(cols/32)] written
+ * rows >= 0, cols >= 1, any alignment.  Bit-identical to the definition.
+ */
+int coli_quant_mxfp4(const void *w, coli_dtype w_dtype, int64_t rows, int64_t cols,
+                     uint8_t *packed, uint8_t *scales, cudaStream_t stream);
 
 /*
  * Workspace: every routed call needs caller-owned device scratch of at least
@@ -164,11 +203,12 @@ int coli_router_topk(const coli_moe_desc *d, int top_k, const void *x,
  * once (batch union).  The per-token sum runs in a fixed order, so results
  * are deterministic.
  *   x [T][H] (d->x_dtype), router_w [E][H], packed_experts / scales in the
- *   expert record layout above, out f32 [T][H].
+ *   expert record layout above (f32 scales, or the E8M0 bytes of an MXFP4
+ *   layer: d->weight_fmt), out f32 [T][H].
  */
 int coli_moe_forward(const coli_moe_desc *d, int top_k, const void *x,
                      const void *router_w, const uint8_t *packed_experts,
-                     const float *scales, float *out, uint32_t *route_counts,
+                     const void *scales, float *out, uint32_t *route_counts,
                      void *workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
@@ -199,7 +239,7 @@ int coli_moe_forward(const coli_moe_desc *d, int top_k, const void *x,
  */
 int coli_moe_forward_noalloc(const coli_moe_desc *d, int top_k, const void *x,
                              const void *router_w, const uint8_t *packed_experts,
-                             const float *scales, float *out, uint32_t *route_counts,
+                             const void *scales, float *out, uint32_t *route_counts,
                              cudaStream_t stream);
 
 /*
@@ -223,7 +263,8 @@ int coli_moe_forward_noalloc(const coli_moe_desc *d, int top_k, const void *x,
  * Zero heat, last and clock before the first use; slot_of and slot_owner must
  * describe the same placement (coli_tier_place fills the slots they name).
  * Shared experts (E .. E+S-1) may be placed in slots; the policy never evicts
- * them and never admits them.
+ * them and never admits them.  Int4-grouped layers only (COLI_EUNSUPPORTED
+ * for another d->weight_fmt).
  */
 typedef struct {
     int32_t n_slots;
@@ -295,7 +336,7 @@ int coli_tier_update(const coli_moe_desc *d, const uint32_t *call_counts,
  */
 int coli_moe_stack_forward(const coli_moe_desc *d, int top_k, int n_layers,
                            const void *x, const void *router_w,
-                           const uint8_t *packed_experts, const float *scales,
+                           const uint8_t *packed_experts, const void *scales,
                            float *x_out, float *layer_out, uint32_t *route_counts,
                            void *workspace, size_t ws_bytes, cudaStream_t stream);
 

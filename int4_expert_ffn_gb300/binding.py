@@ -24,6 +24,7 @@ COLI_FLAG_NAN_LOGITS, COLI_FLAG_TIMEOUT = 0x1, 0x2
 COLI_KERNEL_ROUTE, COLI_KERNEL_GATEUP, COLI_KERNEL_DOWN = 0, 1, 2
 COLI_KERNEL_PREFILL_GATEUP, COLI_KERNEL_PREFILL_DOWN = 3, 4
 COLI_KERNEL_LAYER = 5
+COLI_FMT_I4G, COLI_FMT_MXFP4 = 4, 7
 GROUP = 64
 
 # every symbol include/coli.h declares
@@ -34,6 +35,8 @@ EXPORTS = (
     "coli_moe_forward", "coli_moe_forward_noalloc", "coli_moe_stack_forward",
     "coli_profile_events", "coli_moe_check", "coli_usage_engine_id", "coli_usage_save",
     "coli_usage_load", "coli_moe_forward_tiered", "coli_tier_place", "coli_tier_update",
+    "coli_quant_mxfp4", "coli_fmt_row_bytes", "coli_fmt_scale_bytes", "coli_fmt_expert_bytes",
+    "coli_fmt_expert_scale_bytes",
 )
 
 
@@ -50,7 +53,7 @@ class coli_moe_desc(C.Structure):
     _fields_ = [("hidden", C.c_int32), ("ffn", C.c_int32), ("n_experts", C.c_int32),
                 ("n_shared", C.c_int32), ("n_tokens", C.c_int32), ("x_dtype", C.c_int),
                 ("router_dtype", C.c_int), ("router_fn", C.c_int32),
-                ("router_bias", C.c_void_p)]
+                ("router_bias", C.c_void_p), ("weight_fmt", C.c_int32)]
 
 
 class coli_tier(C.Structure):
@@ -80,6 +83,14 @@ def _load():
         getattr(L, f).restype = i64
     L.coli_quant_i4g.argtypes = [vp, C.c_int, i64, i64, vp, vp, vp]
     L.coli_quant_i4g.restype = C.c_int
+    L.coli_quant_mxfp4.argtypes = [vp, C.c_int, i64, i64, vp, vp, vp]
+    L.coli_quant_mxfp4.restype = C.c_int
+    for f in ("coli_fmt_row_bytes", "coli_fmt_scale_bytes"):
+        getattr(L, f).argtypes = [C.c_int32, i64]
+        getattr(L, f).restype = i64
+    for f in ("coli_fmt_expert_bytes", "coli_fmt_expert_scale_bytes"):
+        getattr(L, f).argtypes = [C.c_int32, i64, i64]
+        getattr(L, f).restype = i64
     for f in ("coli_router_workspace_size", "coli_moe_workspace_size"):
         getattr(L, f).argtypes = [dp, C.c_int]
         getattr(L, f).restype = sz
@@ -165,6 +176,7 @@ class MoEDesc:
     router_dtype: int = COLI_BF16
     router_fn: int = COLI_ROUTER_SOFTMAX
     router_bias: object = None    # f32 CUDA tensor [E] (or [n_layers, E]), or None
+    weight_fmt: int = 0           # COLI_FMT_I4G (0 also) or COLI_FMT_MXFP4
 
     def c(self):
         b = self.router_bias
@@ -173,7 +185,7 @@ class MoEDesc:
                 raise ValueError("router_bias must be a contiguous float32 CUDA tensor")
         return coli_moe_desc(self.hidden, self.ffn, self.n_experts, self.n_shared,
                              self.n_tokens, self.x_dtype, self.router_dtype, self.router_fn,
-                             None if b is None else b.data_ptr())
+                             None if b is None else b.data_ptr(), self.weight_fmt)
 
 
 def coli_packed_row_bytes(cols):
@@ -204,6 +216,29 @@ def coli_quant_i4g(w, packed=None, scales=None, stream=None):
     _check("coli_quant_i4g", lib.coli_quant_i4g(_ptr(w), _dt(w), rows, cols, _ptr(packed),
                                                  _ptr(scales), _stream(stream)))
     return packed, scales
+
+
+def coli_quant_mxfp4(w, packed=None, scales=None, stream=None):
+    """Quantise w [rows, cols] (bf16 or f32, CUDA) to MXFP4 -> (packed u8
+    [rows, ceil(cols/2)], E8M0 scales u8 [rows, ceil(cols/32)])."""
+    _cuda(w)
+    rows, cols = w.shape
+    if packed is None:
+        packed = torch.empty((rows, (cols + 1) // 2), dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty((rows, (cols + 31) // 32), dtype=torch.uint8, device=w.device)
+    _cuda(packed, scales)
+    _check("coli_quant_mxfp4", lib.coli_quant_mxfp4(_ptr(w), _dt(w), rows, cols, _ptr(packed),
+                                                     _ptr(scales), _stream(stream)))
+    return packed, scales
+
+
+def coli_fmt_expert_bytes(fmt, H, F):
+    return lib.coli_fmt_expert_bytes(fmt, H, F)
+
+
+def coli_fmt_expert_scale_bytes(fmt, H, F):
+    return lib.coli_fmt_expert_scale_bytes(fmt, H, F)
 
 
 def coli_moe_workspace_size(desc: MoEDesc, top_k):

@@ -92,8 +92,12 @@ int check_desc(const coli_moe_desc *d, int top_k) {
     return COLI_EINVAL;
   if (d->router_fn == COLI_ROUTER_SIGMOID_BIAS && ((uintptr_t)d->router_bias & 3u))
     return COLI_EALIGN;
+  if (d->weight_fmt != 0 && d->weight_fmt != COLI_FMT_I4G && d->weight_fmt != COLI_FMT_MXFP4)
+    return COLI_EINVAL;
   return COLI_OK;
 }
+
+int weight_fmt(const coli_moe_desc *d) { return d->weight_fmt == 0 ? COLI_FMT_I4G : d->weight_fmt; }
 
 
 // Tokens per internal pass of the GEMV path; larger calls run in passes.
@@ -101,8 +105,15 @@ int pass_tokens(int T) { return T < kDecodeMaxT ? T : kDecodeMaxT; }
 
 // Calls with many tokens take the batched path (grouped tensor-core GEMMs)
 // when its tile shapes divide the layer.
+// MXFP4 layers take it at every token count.
 bool use_prefill(const coli_moe_desc *d) {
+  if (weight_fmt(d) == COLI_FMT_MXFP4) return true;
   return d->n_tokens >= kPrefillMinT && prefill_supported(d->hidden, d->ffn);
+}
+
+// A format the layer's shape cannot run in.
+int fmt_unsupported(const coli_moe_desc *d) {
+  return weight_fmt(d) == COLI_FMT_MXFP4 && !prefill_supported(d->hidden, d->ffn);
 }
 
 int map_err(cudaError_t e) { return coli::cuda_status(e); }
@@ -236,6 +247,24 @@ int64_t coli_expert_scale_count(int64_t H, int64_t F) {
   return 2 * F * coli_scales_per_row(H) + H * coli_scales_per_row(F);
 }
 
+int64_t coli_fmt_row_bytes(int32_t fmt, int64_t cols) {
+  if (cols < 0) return 0;
+  if (fmt == 0 || fmt == COLI_FMT_I4G || fmt == COLI_FMT_MXFP4) return (cols + 1) / 2;
+  return 0;
+}
+int64_t coli_fmt_scale_bytes(int32_t fmt, int64_t cols) {
+  if (cols < 0) return 0;
+  if (fmt == 0 || fmt == COLI_FMT_I4G) return 4 * coli_scales_per_row(cols);
+  if (fmt == COLI_FMT_MXFP4) return (cols + kMxBlock - 1) / kMxBlock;
+  return 0;
+}
+int64_t coli_fmt_expert_bytes(int32_t fmt, int64_t H, int64_t F) {
+  return 2 * F * coli_fmt_row_bytes(fmt, H) + H * coli_fmt_row_bytes(fmt, F);
+}
+int64_t coli_fmt_expert_scale_bytes(int32_t fmt, int64_t H, int64_t F) {
+  return 2 * F * coli_fmt_scale_bytes(fmt, H) + H * coli_fmt_scale_bytes(fmt, F);
+}
+
 int coli_quant_i4g(const void *w, coli_dtype w_dtype, int64_t rows, int64_t cols,
                    uint8_t *packed, float *scales, cudaStream_t stream) {
   if (rows < 0 || cols < 1) return COLI_EINVAL;
@@ -249,8 +278,17 @@ size_t coli_router_workspace_size(const coli_moe_desc *d, int top_k) {
   return coli_moe_workspace_size(d, top_k);
 }
 
+int coli_quant_mxfp4(const void *w, coli_dtype w_dtype, int64_t rows, int64_t cols,
+                     uint8_t *packed, uint8_t *scales, cudaStream_t stream) {
+  if (rows < 0 || cols < 1) return COLI_EINVAL;
+  if (w_dtype != COLI_F32 && w_dtype != COLI_BF16) return COLI_EINVAL;
+  if (rows > 0 && (!w || !packed || !scales)) return COLI_EINVAL;
+  if (rows > 0 && cols > INT64_MAX / rows) return COLI_EINVAL;
+  return map_err(launch_quant_mxfp4(w, w_dtype, rows, cols, packed, scales, stream));
+}
+
 size_t coli_moe_workspace_size(const coli_moe_desc *d, int top_k) {
-  if (check_desc(d, top_k) != COLI_OK) return 0;
+  if (check_desc(d, top_k) != COLI_OK || fmt_unsupported(d)) return 0;
   if (use_prefill(d))
     return prefill_layout(d->n_tokens, d->hidden, d->ffn, d->n_experts, d->n_shared, top_k).total;
   const int T = pass_tokens(d->n_tokens);
@@ -394,9 +432,10 @@ static int prefill_run(const coli_moe_desc *d, int k, int n_layers, const void *
   const int T = d->n_tokens, H = d->hidden, F = d->ffn, E = d->n_experts, S = d->n_shared;
   const PrefillLayout L = prefill_layout(T, H, F, E, S, k);
   uint8_t *ws = (uint8_t *)workspace;
+  const int fmt = weight_fmt(d);
   const size_t wr_stride = (size_t)E * H * xsize(d->router_dtype);
-  const size_t pk_stride = (size_t)(E + S) * coli_expert_packed_bytes(H, F);
-  const size_t sc_stride = (size_t)(E + S) * coli_expert_scale_count(H, F);
+  const size_t pk_stride = (size_t)(E + S) * coli_fmt_expert_bytes(fmt, H, F);
+  const size_t sc_bytes = (size_t)(E + S) * coli_fmt_expert_scale_bytes(fmt, H, F);
   for (int l = 0; l < n_layers; ++l) {
     PrefillArgs a{};
     if (tier) a.tier = *tier;
@@ -406,10 +445,12 @@ static int prefill_run(const coli_moe_desc *d, int k, int n_layers, const void *
                         ? d->router_bias + (size_t)l * E : nullptr;
     a.x = l == 0 ? x : (const void *)out;
     a.wr = (const char *)router_w + l * wr_stride;
+    a.fmt = fmt;
     a.packed = packed + l * pk_stride;
-    a.scales = scales + l * sc_stride;
-    a.eb = coli_expert_packed_bytes(H, F);
-    a.es = coli_expert_scale_count(H, F);
+    a.scales = (const float *)((const uint8_t *)scales + l * sc_bytes);
+    a.eb = coli_fmt_expert_bytes(fmt, H, F);
+    a.es = fmt == COLI_FMT_MXFP4 ? coli_fmt_expert_scale_bytes(fmt, H, F)
+                                 : coli_expert_scale_count(H, F);
     a.residual = residual ? (l == 0 ? (const float *)x : out) : nullptr;
     a.out = out;
     a.layer_out = layer_out ? layer_out + (size_t)l * T * H : nullptr;
@@ -466,6 +507,7 @@ int coli::moe_forward_tiered(const coli_moe_desc *d, int top_k, const void *x,
                              void *workspace, size_t ws_bytes, cudaStream_t stream) {
   int st = check_desc(d, top_k);
   if (st) return st;
+  if (weight_fmt(d) != COLI_FMT_I4G) return COLI_EUNSUPPORTED;
   if (d->n_tokens == 0) return COLI_OK;
   if (!x || !router_w || !packed || !scales || !out || !workspace) return COLI_EINVAL;
   if (!aligned16(x) || !aligned16(router_w) || !aligned16(packed) || !aligned16(scales) ||
@@ -479,11 +521,13 @@ int coli::moe_forward_tiered(const coli_moe_desc *d, int top_k, const void *x,
 extern "C" {
 
 int coli_moe_forward(const coli_moe_desc *d, int top_k, const void *x, const void *router_w,
-                     const uint8_t *packed_experts, const float *scales, float *out,
+                     const uint8_t *packed_experts, const void *scales_v, float *out,
                      uint32_t *route_counts, void *workspace, size_t ws_bytes,
                      cudaStream_t stream) {
+  const float *scales = (const float *)scales_v;   // E8M0 bytes for an MXFP4 layer
   int st = check_desc(d, top_k);
   if (st) return st;
+  if (fmt_unsupported(d)) return COLI_EUNSUPPORTED;
   if (d->n_tokens == 0) return COLI_OK;
   if (!x || !router_w || !packed_experts || !scales || !out || !workspace) return COLI_EINVAL;
   if (!aligned16(x) || !aligned16(router_w) || !aligned16(packed_experts) ||
@@ -496,11 +540,13 @@ int coli_moe_forward(const coli_moe_desc *d, int top_k, const void *x, const voi
 
 int coli_moe_stack_forward(const coli_moe_desc *d, int top_k, int n_layers, const void *x,
                            const void *router_w, const uint8_t *packed_experts,
-                           const float *scales, float *x_out, float *layer_out,
+                           const void *scales_v, float *x_out, float *layer_out,
                            uint32_t *route_counts, void *workspace, size_t ws_bytes,
                            cudaStream_t stream) {
+  const float *scales = (const float *)scales_v;   // E8M0 bytes for an MXFP4 layer
   int st = check_desc(d, top_k);
   if (st) return st;
+  if (fmt_unsupported(d)) return COLI_EUNSUPPORTED;
   if (n_layers < 1) return COLI_EINVAL;
   if (d->n_tokens == 0) return COLI_OK;
   if (!x || !router_w || !packed_experts || !scales || !x_out || !workspace)

@@ -46,8 +46,8 @@ namespace {
 
 // Phase trace of k_layer1, compiled in only with -DCOLI_TRACE (a diagnostic
 // build): one %globaltimer stamp per (point, CTA), read by coli_trace1_read_raw.
-constexpr int kT1Points = 12, kT1Ctas = 160;
 #ifdef COLI_TRACE
+constexpr int kT1Points = 12, kT1Ctas = 160;
 static __device__ unsigned long long g_trace1[kT1Points][kT1Ctas];
 __device__ __forceinline__ void t1_point(int pt) {
   if (blockIdx.x >= kT1Ctas) return;

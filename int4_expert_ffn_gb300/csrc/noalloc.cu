@@ -44,7 +44,7 @@ int scratch_address(void **out) {
 
 extern "C" int coli_moe_forward_noalloc(const coli_moe_desc *d, int top_k, const void *x,
                                         const void *router_w, const uint8_t *packed_experts,
-                                        const float *scales, float *out,
+                                        const void *scales, float *out,
                                         uint32_t *route_counts, cudaStream_t stream) {
   const size_t need = coli_moe_workspace_size(d, top_k);
   if (need == 0) return COLI_EINVAL;

@@ -11,12 +11,13 @@
 //   k_gcount / k_gscan / k_gscatter
 //               counting sort of the routes by expert (stable in (token, slot)
 //               order), expert m-tiles and the GEMM work list
-//   k_pgemm<MODE>
+//   k_pgemm<MODE, FMT>
 //               token-sorted grouped GEMM on tcgen05 tensor cores: 128-row
 //               m-tiles of one expert's routes x 256-column n-tiles, K in
 //               steps of 64 (one scale group).  Eight producer warps stage the
-//               activation rows with cp.async and dequantise the int4 weight
-//               tile to fp16 into 128-byte-swizzled shared memory; one thread
+//               activation rows with cp.async and dequantise the weight tile
+//               (int4-grouped, or MXFP4 E2M1 codes with E8M0 scales) to fp16
+//               into 128-byte-swizzled shared memory; one thread
 //               issues tcgen05.mma (kind::f16, f32 accumulator in TMEM); four
 //               epilogue warps drain TMEM:
 //                 gate/up: h = silu(g) * u * gate  -> fp16 [route][F]
@@ -179,6 +180,42 @@ __device__ __forceinline__ void dequant8(uint32_t w0, uint32_t w1, __half2 s2, u
       h = __hmul2(h, s2);
       o[4 * i + j] = *reinterpret_cast<const uint32_t *>(&h);
     }
+}
+
+// 8 packed bytes of MXFP4 (16 E2M1 codes, even column low nibble) -> 8 fp16x2
+// words of e2m1(code) * X.  The eight E2M1 magnitudes are exact fp16 numbers
+// whose low bytes are zero: a byte permute of the 3-bit magnitude codes picks
+// their high bytes from a table, the code's sign bit goes to the fp16 sign,
+// and the power-of-two scale X (as fp16) multiplies exactly while the product
+// stays in the fp16 range.
+__device__ __forceinline__ void dequant8_mx(uint32_t w0, uint32_t w1, __half2 s2, uint32_t (&o)[8]) {
+  constexpr uint32_t kMagLo = 0x3E3C3800u;   // fp16 high bytes of 0, 0.5, 1, 1.5
+  constexpr uint32_t kMagHi = 0x46444240u;   //                    2, 3, 4, 6
+  const uint32_t ws[2] = {w0, w1};
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint32_t w = ws[i];
+    const uint32_t m = w & 0x77777777u;
+    const uint32_t r0 = __byte_perm(kMagLo, kMagHi, m);         // columns 0..3 of the word
+    const uint32_t r1 = __byte_perm(kMagLo, kMagHi, m >> 16);   // columns 4..7
+    uint32_t h[4];
+    h[0] = __byte_perm(r0, 0, 0x1404) | ((w << 12) & 0x8000u) | ((w << 24) & 0x80000000u);
+    h[1] = __byte_perm(r0, 0, 0x3424) | ((w << 4) & 0x8000u) | ((w << 16) & 0x80000000u);
+    h[2] = __byte_perm(r1, 0, 0x1404) | ((w >> 4) & 0x8000u) | ((w << 8) & 0x80000000u);
+    h[3] = __byte_perm(r1, 0, 0x3424) | ((w >> 12) & 0x8000u) | (w & 0x80000000u);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      __half2 v = *reinterpret_cast<const __half2 *>(&h[j]);
+      v = __hmul2(v, s2);
+      o[4 * i + j] = *reinterpret_cast<const uint32_t *>(&v);
+    }
+  }
+}
+
+// The E8M0 scale byte e as an fp16 pair: 2^(e - 127) (255: NaN).
+__device__ __forceinline__ __half2 e8m0_half2(uint32_t e) {
+  const float x = e == 255u ? __int_as_float(0x7FC00000) : ldexpf(1.0f, (int)e - 127);
+  return __float2half2_rn(x);
 }
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
@@ -445,7 +482,10 @@ __global__ void __launch_bounds__(256) k_gscatter(PrefillArgs p) {
 // ---------------------------------------------------------------------------
 // The grouped GEMM.
 
-template <int MODE>
+// FMT: COLI_FMT_I4G (one f32 scale per row and k-tile) or COLI_FMT_MXFP4 (one
+// E8M0 byte per row and 32 columns: a thread's 16-byte half of the k-tile has
+// exactly one; the copy brings the aligned 4-byte word that holds it).
+template <int MODE, int FMT>
 __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -517,7 +557,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
     const __half *a_src[kARowPasses];
     bool a_ok[kARowPasses];
     const uint8_t *b_src[2];
-    const float *b_sc[2];
+    const uint8_t *b_sc[2];          // the row's scales (bytes)
     bool ok = true;
     int item = 0, kt = 0;                  // k-tile t = item * nk + kt
     for (int t = 0; t < n_ticks + kDist && ok; ++t) {
@@ -534,8 +574,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
                                              : p.h16 + (int64_t)(it.p0 + r) * F;
           }
           const uint8_t *pk;
-          const float *sc;
-          expert_record(p.tier, p.packed, p.scales, p.eb, p.es, it.e, &pk, &sc);
+          const uint8_t *sc;
+          if (FMT == COLI_FMT_MXFP4) {
+            pk = p.packed + (int64_t)it.e * p.eb;
+            sc = (const uint8_t *)p.scales + (int64_t)it.e * p.es;
+          } else {
+            const float *scf;
+            expert_record(p.tier, p.packed, p.scales, p.eb, p.es, it.e, &pk, &scf);
+            sc = (const uint8_t *)scf;
+          }
+          // bytes of one row's scales (K columns), the gate/up/down matrices' rows
+          const int64_t sh = FMT == COLI_FMT_MXFP4 ? H / kMxBlock : 4 * (H / kGroup);
+          const int64_t sf = FMT == COLI_FMT_MXFP4 ? F / kMxBlock : 4 * (F / kGroup);
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             if (MODE == kModeGateUp) {
@@ -543,11 +593,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
               const int f = it.ni * (kBN / 2) + b_row0;
               const int64_t mat = j;
               b_src[j] = pk + mat * (int64_t)F * (H / 2) + (int64_t)f * (H / 2);
-              b_sc[j] = sc + mat * (int64_t)F * (H / kGroup) + (int64_t)f * (H / kGroup);
+              b_sc[j] = sc + mat * (int64_t)F * sh + (int64_t)f * sh;
             } else {
               const int hr = it.ni * kBN + b_row0 + 128 * j;
               b_src[j] = pk + (int64_t)F * H + (int64_t)hr * (F / 2);
-              b_sc[j] = sc + (int64_t)2 * F * (H / kGroup) + (int64_t)hr * (F / kGroup);
+              b_sc[j] = sc + (int64_t)2 * F * sh + (int64_t)hr * sf;
             }
           }
         }
@@ -562,7 +612,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           cp16(smem_u32(raw + (j * kProducerThreads + th) * 16), b_src[j] + k0 / 2 + 16 * b_half);
-          cp4(smem_u32(raw + kRawNibbleBytes + (j * kProducerThreads + th) * 4), b_sc[j] + kt);
+          // int4: the k-tile's f32 scale; MXFP4: the word holding its two E8M0 bytes
+          cp4(smem_u32(raw + kRawNibbleBytes + (j * kProducerThreads + th) * 4),
+              b_sc[j] + (FMT == COLI_FMT_MXFP4 ? (kt >> 1) * 4 : kt * 4));
         }
         if (++kt == nk) { kt = 0; ++item; }
       }
@@ -574,18 +626,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
       if (!mbar_wait(&b_empty[sb], ((c / kNB) & 1) ^ 1)) { ok = false; break; }
       const uint8_t *raw = r_ring + (c % kNR) * kRawBytes;
       const uint32_t b_dst = smem_u32(b_ring + sb * kBTileBytes);
+      const int kt_c = c % nk;
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int slot = j * kProducerThreads + th;
         const uint4 w = *(const uint4 *)(raw + slot * 16);
-        const __half2 s2 = __float2half2_rn(*(const float *)(raw + kRawNibbleBytes + slot * 4));
+        const uint32_t sw = *(const uint32_t *)(raw + kRawNibbleBytes + slot * 4);
+        const __half2 s2 = FMT == COLI_FMT_MXFP4
+                               ? e8m0_half2((sw >> (8 * (2 * (kt_c & 1) + b_half))) & 0xFFu)
+                               : __float2half2_rn(__uint_as_float(sw));
         const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
         const int row = b_row0 + 128 * j;
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           // columns 32 b_half + 16 q .. + 15: 16-byte chunks 4 b_half + 2 q, + 1
           uint32_t o[8];
-          dequant8(wd[2 * q], wd[2 * q + 1], s2, o);
+          if (FMT == COLI_FMT_MXFP4) dequant8_mx(wd[2 * q], wd[2 * q + 1], s2, o);
+          else dequant8(wd[2 * q], wd[2 * q + 1], s2, o);
           st_shared16(b_dst + sw128_off(row, 4 * b_half + 2 * q), o[0], o[1], o[2], o[3]);
           st_shared16(b_dst + sw128_off(row, 4 * b_half + 2 * q + 1), o[4], o[5], o[6], o[7]);
         }
@@ -785,14 +842,18 @@ cudaError_t launch_prefill(const PrefillArgs &p, int x_dtype, int wr_dtype, cuda
   k_gscan<<<1, 1024, 0, s>>>(p, nb);
   k_gscatter<<<nb, 256, (size_t)E * 4, s>>>(p);
   // GEMMs
-  if ((e = set_smem(k_pgemm<kModeGateUp>, kGemmSmem)) != cudaSuccess) return e;
-  if ((e = set_smem(k_pgemm<kModeDown>, kGemmSmem)) != cudaSuccess) return e;
+  auto gemm_gu = p.fmt == COLI_FMT_MXFP4 ? k_pgemm<kModeGateUp, COLI_FMT_MXFP4>
+                                         : k_pgemm<kModeGateUp, COLI_FMT_I4G>;
+  auto gemm_dn = p.fmt == COLI_FMT_MXFP4 ? k_pgemm<kModeDown, COLI_FMT_MXFP4>
+                                         : k_pgemm<kModeDown, COLI_FMT_I4G>;
+  if ((e = set_smem(gemm_gu, kGemmSmem)) != cudaSuccess) return e;
+  if ((e = set_smem(gemm_dn, kGemmSmem)) != cudaSuccess) return e;
   size_t slot = 0;
   if ((e = record_profile(COLI_KERNEL_PREFILL_GATEUP, s, false, &slot)) != cudaSuccess) return e;
-  k_pgemm<kModeGateUp><<<nsm, kGemmThreads, kGemmSmem, s>>>(p);
+  gemm_gu<<<nsm, kGemmThreads, kGemmSmem, s>>>(p);
   if ((e = record_profile(COLI_KERNEL_PREFILL_GATEUP, s, true, &slot)) != cudaSuccess) return e;
   if ((e = record_profile(COLI_KERNEL_PREFILL_DOWN, s, false, &slot)) != cudaSuccess) return e;
-  k_pgemm<kModeDown><<<nsm, kGemmThreads, kGemmSmem, s>>>(p);
+  gemm_dn<<<nsm, kGemmThreads, kGemmSmem, s>>>(p);
   if ((e = record_profile(COLI_KERNEL_PREFILL_DOWN, s, true, &slot)) != cudaSuccess) return e;
   // combine
   const int64_t nc = (int64_t)T * (H / 4);

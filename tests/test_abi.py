@@ -73,11 +73,14 @@ def test_router_fn_validated(coli):
 
 
 def test_desc_layout_matches_header(coli):
-    # the ctypes mirror of coli_moe_desc: 8 int32-sized fields, then the bias pointer
+    # the ctypes mirror of coli_moe_desc: 8 int32-sized fields, the bias pointer,
+    # then the weight format
     D = coli.coli_moe_desc
-    assert D.router_fn.offset == 28 and D.router_bias.offset == 32 and C.sizeof(D) == 40
+    assert D.router_fn.offset == 28 and D.router_bias.offset == 32
+    assert D.weight_fmt.offset == 40 and C.sizeof(D) == 48
     text = open(os.path.join(ROOT, "include", "coli.h")).read()
     assert "COLI_ROUTER_SIGMOID_BIAS = 1" in text and "const float *router_bias;" in text
+    assert "int32_t weight_fmt;" in text and "COLI_FMT_MXFP4 = 7" in text
 
 
 def test_workspace_size_bad_topk(coli):
@@ -140,3 +143,22 @@ def test_profile_events_validation(coli):
 
 def test_last_error_before_any_failure(coli):
     assert coli.coli_last_error() == "no error"
+
+
+def test_weight_format_rules(coli):
+    # MXFP4 runs on the grouped GEMM: hidden % 256 == 0, ffn % 128 == 0
+    d = coli.MoEDesc(320, 128, 8, 1, 4, coli.COLI_F32, coli.COLI_BF16,
+                     weight_fmt=coli.COLI_FMT_MXFP4)
+    assert coli.coli_moe_workspace_size(d, 2) == 0
+    d = coli.MoEDesc(256, 128, 8, 1, 4, coli.COLI_F32, coli.COLI_BF16,
+                     weight_fmt=coli.COLI_FMT_MXFP4)
+    assert coli.coli_moe_workspace_size(d, 2) > 0
+    d = coli.MoEDesc(256, 128, 8, 1, 4, coli.COLI_F32, coli.COLI_BF16, weight_fmt=5)
+    assert coli.coli_moe_workspace_size(d, 2) == 0
+    # sizes: MXFP4 rows are the int4 rows; one scale byte per 32 columns
+    assert coli.lib.coli_fmt_row_bytes(coli.COLI_FMT_MXFP4, 333) == 167
+    assert coli.lib.coli_fmt_scale_bytes(coli.COLI_FMT_MXFP4, 333) == 11
+    assert coli.lib.coli_fmt_scale_bytes(coli.COLI_FMT_I4G, 333) == 4 * 6
+    assert coli.coli_fmt_expert_bytes(coli.COLI_FMT_MXFP4, 256, 128) == coli.coli_expert_packed_bytes(256, 128)
+    assert coli.coli_fmt_expert_scale_bytes(coli.COLI_FMT_MXFP4, 256, 128) == 3 * 256 * 128 // 32
+    assert coli.lib.coli_fmt_row_bytes(9, 64) == 0

@@ -1,0 +1,161 @@
+"""MXFP4 container (COLI_FMT_MXFP4) on the GPU against the oracle: the
+quantiser bit for bit (hand vectors, random weights with outliers, ragged
+columns, NaN and zero blocks, bf16 and f32), and MXFP4 layers -- which run on
+the tensor-core grouped GEMM at every token count -- within the tolerance of
+the other tests, route counts exact, including the sigmoid router, shared
+experts and a chained stack."""
+import dataclasses
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from conftest import parse_golden
+from int4_expert_ffn_gb300 import synth
+from helpers import REL_TOL, coli, rel_err, tokens_without_ties
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = parse_golden(os.path.join(os.path.dirname(__file__), "golden", "mxfp4_hand.txt"))
+
+
+def gpu_quant(w):
+    p, s = coli().coli_quant_mxfp4(w.cuda())
+    torch.cuda.synchronize()
+    return p.cpu().numpy(), s.cpu().numpy()
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("case", GOLDEN, ids=[c["name"] for c in GOLDEN])
+def test_quant_hand_vectors(case, dtype):
+    w = torch.tensor(case["w"], dtype=torch.float32).to(dtype)
+    if dtype == torch.bfloat16 and not torch.equal(w.float(), torch.tensor(case["w"])):
+        pytest.skip("values not exact in bf16")
+    p, s = gpu_quant(w)
+    assert p.tolist() == case["bytes"]
+    assert s.tolist() == case["scales"]
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 32), (64, 64), (100, 6144), (37, 2048), (33, 200),
+                                       (7, 333), (5, 1), (3, 65)])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_quant_random_with_outliers(rows, cols, dtype):
+    w = synth.matrix(rows, cols, 0.02, 11, rows, cols, dtype=dtype, outliers=0.01)
+    w[0, : min(cols, 32)] = 0             # an all-zero block
+    if rows > 2 and cols > 40:
+        w[1, 5] = float("nan")
+        w[2, 3] = -0.0
+    p, s = gpu_quant(w)
+    op, os_ = orc.quant_mxfp4(w.float().cpu().numpy())
+    assert np.array_equal(s, os_)
+    bad = np.argwhere(p != op)
+    assert bad.size == 0, "%d bytes differ, first %s" % (len(bad), bad[:3].tolist())
+
+
+class MxLayer:
+    """One MoE layer in MXFP4: quantised on the GPU and, independently, by the oracle."""
+
+    def __init__(self, shape, layer=0, seed=0):
+        c = coli()
+        H, F, E, S = shape.hidden, shape.ffn, shape.experts, shape.shared
+        self.shape = shape
+        mats = [synth.expert_matrix(shape, layer, e, m, seed) for e in range(E + S)
+                for m in range(3)]
+        eb = c.coli_fmt_expert_bytes(c.COLI_FMT_MXFP4, H, F)
+        es = c.coli_fmt_expert_scale_bytes(c.COLI_FMT_MXFP4, H, F)
+        self.packed = torch.empty((E + S) * eb, dtype=torch.uint8, device="cuda")
+        self.scales = torch.empty((E + S) * es, dtype=torch.uint8, device="cuda")
+        p0 = s0 = 0
+        ops, oss = [], []
+        for m in mats:
+            rows, cols = m.shape
+            nb, ns = rows * cols // 2, rows * cols // 32
+            c.coli_quant_mxfp4(m.cuda(), self.packed[p0:p0 + nb].view(rows, -1),
+                               self.scales[s0:s0 + ns].view(rows, -1))
+            p0, s0 = p0 + nb, s0 + ns
+            a, b = orc.quant_mxfp4(m.float().numpy())
+            ops.append(a.reshape(-1))
+            oss.append(b.reshape(-1))
+        self.o_packed, self.o_scales = np.concatenate(ops), np.concatenate(oss)
+        self.wr = synth.router_weights(shape, layer, seed)
+        torch.cuda.synchronize()
+        assert np.array_equal(self.packed.cpu().numpy(), self.o_packed)
+        assert np.array_equal(self.scales.cpu().numpy(), self.o_scales)
+
+
+def desc_mx(shape, T, bias=None, x_dtype=None):
+    c = coli()
+    args = [shape.hidden, shape.ffn, shape.experts, shape.shared, T,
+            c.COLI_F32 if (x_dtype or torch.float32) == torch.float32 else c.COLI_BF16,
+            c.COLI_F32 if shape.router_dtype == "f32" else c.COLI_BF16]
+    if bias is not None:
+        args += [c.COLI_ROUTER_SIGMOID_BIAS, bias]
+    else:
+        args += [c.COLI_ROUTER_SOFTMAX, None]
+    return c.MoEDesc(*args, weight_fmt=c.COLI_FMT_MXFP4)
+
+
+SHAPES = [
+    # (hidden, ffn, experts, shared, top_k, tokens)
+    (256, 128, 8, 1, 2, 1),
+    (256, 128, 8, 1, 2, 3),
+    (512, 256, 16, 2, 4, 17),
+    (256, 256, 8, 0, 3, 64),
+    (512, 128, 12, 1, 2, 200),
+    (6144, 2048, 6, 1, 2, 5),      # the GLM-like widths
+]
+
+
+@pytest.mark.parametrize("H,F,E,S,k,T", SHAPES)
+def test_mxfp4_layer(H, F, E, S, k, T):
+    c = coli()
+    shape = synth.MoEShape("mx", 1, H, F, E, S, k, T, "bf16", "f32")
+    prev = orc.set_threads(os.cpu_count() or 1)
+    try:
+        ly = MxLayer(shape, 0, seed=9)
+        x = tokens_without_ties(shape, ly.wr.double().numpy(), seed=9)
+        d = desc_mx(shape, T)
+        ws = c.new_workspace(d, k)
+        counts = torch.zeros(E, dtype=torch.int32, device="cuda")
+        out = c.coli_moe_forward(d, k, x.cuda(), ly.wr.cuda(), ly.packed, ly.scales, ws,
+                                 route_counts=counts)
+        out2 = c.coli_moe_forward(d, k, x.cuda(), ly.wr.cuda(), ly.packed, ly.scales, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out, out2), "not deterministic"
+        ocounts = np.zeros(E, np.uint32)
+        ref, _, _, _ = orc.moe_forward_fmt(orc.FMT_MXFP4, x.double().numpy(),
+                                           ly.wr.double().numpy(), ly.o_packed, ly.o_scales,
+                                           H, F, E, S, k, ocounts)
+    finally:
+        orc.set_threads(prev)
+    err = rel_err(out.cpu().numpy(), ref)
+    assert err.max() <= REL_TOL, "max rel err %.3g" % err.max()
+    assert np.array_equal(counts.cpu().numpy().astype(np.uint32), ocounts)
+
+
+def test_mxfp4_sigmoid_router_and_stack():
+    c = coli()
+    shape = synth.MoEShape("mxs", 2, 512, 256, 16, 1, 4, 6, "bf16", "f32")
+    layers = [MxLayer(shape, l, seed=10) for l in range(2)]
+    biases = [synth.router_bias(shape, l, 10) for l in range(2)]
+    x = tokens_without_ties(shape, layers[0].wr.double().numpy(), seed=10,
+                            bias=biases[0].double().numpy())
+    d = desc_mx(shape, 6, bias=torch.cat(biases).cuda())
+    ws = c.new_workspace(d, 4)
+    counts = torch.zeros((2, 16), dtype=torch.int32, device="cuda")
+    xo = c.coli_moe_stack_forward(d, 4, 2, x.cuda(), torch.cat([ly.wr for ly in layers]).cuda(),
+                                  torch.cat([ly.packed for ly in layers]),
+                                  torch.cat([ly.scales for ly in layers]), ws,
+                                  route_counts=counts)
+    torch.cuda.synchronize()
+    xr = x.double().numpy()
+    ocounts = np.zeros((2, 16), np.uint32)
+    for l, ly in enumerate(layers):
+        o, _, _, _ = orc.moe_forward_fmt(orc.FMT_MXFP4, xr, ly.wr.double().numpy(), ly.o_packed,
+                                         ly.o_scales, 512, 256, 16, 1, 4, ocounts[l],
+                                         router="sigmoid", bias=biases[l].double().numpy())
+        xr = xr + o
+    assert rel_err(xo.cpu().numpy(), xr).max() <= REL_TOL
+    assert np.array_equal(counts.cpu().numpy().astype(np.uint32), ocounts)
