@@ -449,17 +449,24 @@ void orc_dequant_mxfp4(const uint8_t *packed, const uint8_t *scales, int64_t row
 
 /* ---------------------------------------------------------------------- */
 /* The layer over a chosen container: fmt 4 = int4-grouped (the functions
- * above), 7 = MXFP4.  Expert record: gate | up | down, each in the format;
- * `scales` points to f32 scales (fmt 4) or E8M0 bytes (fmt 7), expert after
- * expert in the same order. */
+ * above), 7 = MXFP4, 8 = fp8-e4m3-b128 (below).  Expert record: gate | up | down, each in the format;
+ * `scales` points to f32 scales (fmt 4, 8) or E8M0 bytes (fmt 7), expert
+ * after expert in the same order. */
+
+int64_t orc_fp8_row_bytes(int64_t cols);
+int64_t orc_fp8_scales_per_row(int64_t cols);
+void orc_matvec_fp8b128(const uint8_t *packed, const float *scales, int64_t rows, int64_t cols,
+                        const double *x, double *y);
 
 int64_t orc_fmt_row_bytes(int fmt, int64_t cols)
 {
+    if (fmt == 8) return orc_fp8_row_bytes(cols);
     return fmt == 7 ? orc_mx_row_bytes(cols) : orc_packed_row_bytes(cols);
 }
 /* Bytes of one row's scales. */
 int64_t orc_fmt_scale_bytes(int fmt, int64_t cols)
 {
+    if (fmt == 8) return 4 * orc_fp8_scales_per_row(cols);
     return fmt == 7 ? orc_mx_scales_per_row(cols) : 4 * orc_scales_per_row(cols);
 }
 int64_t orc_fmt_expert_bytes(int fmt, int64_t H, int64_t F)
@@ -474,6 +481,10 @@ int64_t orc_fmt_expert_scale_bytes(int fmt, int64_t H, int64_t F)
 static void orc_matvec_fmt(int fmt, const uint8_t *packed, const uint8_t *scales, int64_t rows,
                            int64_t cols, const double *x, double *y)
 {
+    if (fmt == 8) {
+        orc_matvec_fp8b128(packed, (const float *)scales, rows, cols, x, y);
+        return;
+    }
     if (fmt != 7) {
         orc_matvec_i4g(packed, (const float *)scales, rows, cols, x, y);
         return;
@@ -542,4 +553,94 @@ int orc_moe_forward_fmt(int fmt, const double *x, int64_t T, int64_t H, int64_t 
     }
     free(logits);
     return nan_tokens;
+}
+
+/* ---------------------------------------------------------------------- */
+/* fp8-e4m3-b128 ([P2] §权重转换, "8 fp8-e4m3-b128" of the format registry).
+ * The page gives the name only; the reading (design notes): rows quantised in
+ * blocks of 128 consecutive columns, one f32 scale per block, s = max|w| / 448
+ * (448 = the largest finite E4M3 value; f32 division), each element the
+ * E4M3 code nearest to w / s (f32 division), ties to the even code, finite
+ * saturation at +-448.  E4M3 (OCP 8-bit floating point): 1 sign, 4 exponent
+ * (bias 7), 3 mantissa bits; exponent 0 is subnormal (m 2^-9); no infinity;
+ * exponent 15 with mantissa 7 is NaN.  Storage: one code per byte, row after
+ * row; scales f32 [rows][ceil(cols/128)].  An all-zero block stores s = 0 and
+ * codes 0; a NaN weight is ignored by the max and stored as +0. */
+
+#define ORC_FP8_BLOCK 128
+
+int64_t orc_fp8_row_bytes(int64_t cols) { return cols; }
+int64_t orc_fp8_scales_per_row(int64_t cols) { return (cols + ORC_FP8_BLOCK - 1) / ORC_FP8_BLOCK; }
+
+/* Value of an E4M3 code, from the definition. */
+double orc_e4m3_value(int code)
+{
+    const int s = (code >> 7) & 1, e = (code >> 3) & 15, m = code & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);                 /* m / 8 * 2^(1 - 7) */
+    else v = ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* Nearest finite E4M3 code of a (f32), ties to the even code, saturating:
+ * every non-negative finite code compared, plainly. */
+static int orc_e4m3_round(float a)
+{
+    const double x = fabs((double)a);
+    int best = 0;
+    for (int c = 1; c <= 0x7E; ++c) {
+        const double d_best = fabs(x - orc_e4m3_value(best));
+        const double d = fabs(x - orc_e4m3_value(c));
+        if (d < d_best || (d == d_best && (c & 1) == 0 && (best & 1) == 1)) best = c;
+    }
+    return best | (signbit(a) ? 0x80 : 0);
+}
+
+void orc_quant_fp8b128(const float *w, int64_t rows, int64_t cols, uint8_t *packed, float *scales)
+{
+    const int64_t nb = orc_fp8_scales_per_row(cols);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *wr = w + r * cols;
+        for (int64_t b = 0; b < nb; ++b) {
+            const int64_t c0 = b * ORC_FP8_BLOCK;
+            const int64_t c1 = (c0 + ORC_FP8_BLOCK < cols) ? c0 + ORC_FP8_BLOCK : cols;
+            float m = 0.0f;
+            for (int64_t c = c0; c < c1; ++c) {
+                const float a = fabsf(wr[c]);
+                if (a > m) m = a;
+            }
+            const float s = m / 448.0f;                      /* IEEE f32 division */
+            scales[r * nb + b] = s;
+            for (int64_t c = c0; c < c1; ++c)
+                packed[r * cols + c] =
+                    (uint8_t)((s == 0.0f || wr[c] != wr[c]) ? 0 : orc_e4m3_round(wr[c] / s));
+        }
+    }
+}
+
+static double orc_fp8_elem(const uint8_t *packed, const float *scales, int64_t cols, int64_t nb,
+                           int64_t r, int64_t c)
+{
+    return (double)scales[r * nb + c / ORC_FP8_BLOCK] * orc_e4m3_value(packed[r * cols + c]);
+}
+
+void orc_dequant_fp8b128(const uint8_t *packed, const float *scales, int64_t rows, int64_t cols,
+                         double *w)
+{
+    const int64_t nb = orc_fp8_scales_per_row(cols);
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) w[r * cols + c] = orc_fp8_elem(packed, scales, cols, nb, r, c);
+}
+
+void orc_matvec_fp8b128(const uint8_t *packed, const float *scales, int64_t rows, int64_t cols,
+                        const double *x, double *y)
+{
+    const int64_t nb = orc_fp8_scales_per_row(cols);
+    for (int64_t r = 0; r < rows; ++r) {
+        double acc = 0.0;
+        for (int64_t c = 0; c < cols; ++c) acc += orc_fp8_elem(packed, scales, cols, nb, r, c) * x[c];
+        y[r] = acc;
+    }
 }

@@ -14,10 +14,11 @@ __all__ = [
     "expert_scales", "quant_i4g", "dequant_i4g", "matvec_i4g", "router_logits",
     "topk", "topk_sigmoid", "expert", "moe_forward", "moe_stack_forward", "lib",
     "set_threads", "threads", "quant_mxfp4", "dequant_mxfp4", "e2m1_value", "fmt_expert_bytes",
-    "fmt_expert_scale_bytes", "moe_forward_fmt", "FMT_I4G", "FMT_MXFP4",
+    "fmt_expert_scale_bytes", "moe_forward_fmt", "FMT_I4G", "FMT_MXFP4", "FMT_FP8",
+    "quant_fp8b128", "dequant_fp8b128", "e4m3_value",
 ]
 
-FMT_I4G, FMT_MXFP4 = 4, 7
+FMT_I4G, FMT_MXFP4, FMT_FP8 = 4, 7, 8
 
 GROUP = 64
 _libs = {}
@@ -90,6 +91,12 @@ def lib():
         L.orc_moe_forward_fmt.argtypes = [C.c_int, f64p, i64, i64, i64, i64, i64, f64p, C.c_int,
                                           f64p, u8, u8, C.c_int, f64p, i32p, f64p, u32p]
         L.orc_moe_forward_fmt.restype = C.c_int
+        L.orc_quant_fp8b128.argtypes = [f32p, i64, i64, u8, f32p]
+        L.orc_quant_fp8b128.restype = None
+        L.orc_dequant_fp8b128.argtypes = [u8, f32p, i64, i64, f64p]
+        L.orc_dequant_fp8b128.restype = None
+        L.orc_e4m3_value.argtypes = [C.c_int]
+        L.orc_e4m3_value.restype = C.c_double
         _libs[key] = L
     return _libs[key]
 
@@ -299,3 +306,32 @@ def moe_forward_fmt(fmt, x, wr, packed, scales, H, F, E, n_shared, k, counts=Non
                                     _p(scales, C.c_uint8), k, _p(out, C.c_double),
                                     _p(idx, C.c_int32), _p(gates, C.c_double), cp)
     return out, idx, gates, int(nan)
+
+
+# ---------------------------------------------------------------------------
+# fp8-e4m3-b128
+
+
+def quant_fp8b128(w):
+    """w: [rows, cols] float32 -> (E4M3 codes u8 [rows, cols], f32 scales
+    [rows, ceil(cols/128)])."""
+    w = _c(w, np.float32)
+    rows, cols = w.shape
+    packed = np.zeros((rows, cols), np.uint8)
+    scales = np.zeros((rows, (cols + 127) // 128), np.float32)
+    lib().orc_quant_fp8b128(_p(w, C.c_float), rows, cols, _p(packed, C.c_uint8),
+                            _p(scales, C.c_float))
+    return packed, scales
+
+
+def dequant_fp8b128(packed, scales):
+    packed, scales = _c(packed, np.uint8), _c(scales, np.float32)
+    rows, cols = packed.shape
+    w = np.zeros((rows, cols), np.float64)
+    lib().orc_dequant_fp8b128(_p(packed, C.c_uint8), _p(scales, C.c_float), rows, cols,
+                              _p(w, C.c_double))
+    return w
+
+
+def e4m3_value(code):
+    return float(lib().orc_e4m3_value(int(code)))
