@@ -303,25 +303,31 @@ class PrefillWorkload:
     """One batched (prefill) layer resident in HBM: experts, a skewed router and
     a fresh batch of tokens per step."""
 
-    def __init__(self, shape, steps_total, dev, seed=0):
+    def __init__(self, shape, steps_total, dev, seed=0, fmt="i4g"):
         import int4_expert_ffn_gb300 as pkg
         from int4_expert_ffn_gb300 import synth
         self.coli = c = pkg.binding
         self.shape = shape
         H, F, E, S, T = shape.hidden, shape.ffn, shape.experts, shape.shared, shape.tokens
-        self.eb = c.coli_expert_packed_bytes(H, F)
-        self.es = c.coli_expert_scale_count(H, F)
+        self.fmt = {"i4g": c.COLI_FMT_I4G, "mxfp4": c.COLI_FMT_MXFP4, "fp8": c.COLI_FMT_FP8}[fmt]
+        quant, sdt = {"i4g": (c.coli_quant_i4g, torch.float32),
+                      "mxfp4": (c.coli_quant_mxfp4, torch.uint8),
+                      "fp8": (c.coli_quant_fp8b128, torch.float32)}[fmt]
+        esz = torch.tensor([], dtype=sdt).element_size()
+        self.eb = c.coli_fmt_expert_bytes(self.fmt, H, F)
+        self.es = c.coli_fmt_expert_scale_bytes(self.fmt, H, F) // esz
         n = E + S
         self.packed = torch.empty(n * self.eb, dtype=torch.uint8, device=dev)
-        self.scales = torch.empty(n * self.es, dtype=torch.float32, device=dev)
+        self.scales = torch.empty(n * self.es, dtype=sdt, device=dev)
         p0 = s0 = 0
         for e in range(n):
             for m in range(3):
                 w = synth.expert_matrix(shape, 0, e, m, seed, device=dev)
                 rows, cols = w.shape
-                nb, ns = rows * cols // 2, rows * cols // 64
-                c.coli_quant_i4g(w, self.packed[p0:p0 + nb].view(rows, -1),
-                                 self.scales[s0:s0 + ns].view(rows, -1))
+                nb = rows * c.lib.coli_fmt_row_bytes(self.fmt, cols)
+                ns = rows * c.lib.coli_fmt_scale_bytes(self.fmt, cols) // esz
+                quant(w, self.packed[p0:p0 + nb].view(rows, -1),
+                      self.scales[s0:s0 + ns].view(rows, -1))
                 p0 += nb
                 s0 += ns
         self.router = synth.router_weights(shape, 0, seed, device=dev,
@@ -331,7 +337,8 @@ class PrefillWorkload:
         self.out = torch.empty((T, H), dtype=torch.float32, device=dev)
         self.counts = torch.zeros((steps_total, E), dtype=torch.int32, device=dev)
         self.desc = c.MoEDesc(H, F, E, S, T, c.COLI_BF16 if shape.x_dtype == "bf16" else c.COLI_F32,
-                              c.COLI_BF16 if shape.router_dtype == "bf16" else c.COLI_F32)
+                              c.COLI_BF16 if shape.router_dtype == "bf16" else c.COLI_F32,
+                              weight_fmt=self.fmt)
         self.ws = c.new_workspace(self.desc, shape.top_k)
         torch.cuda.synchronize()
 
@@ -355,7 +362,7 @@ class PrefillWorkload:
 
 def run_prefill(args, shape, dev, world):
     steps, warmup = args.steps, args.warmup
-    wl = PrefillWorkload(shape, warmup + steps, dev)
+    wl = PrefillWorkload(shape, warmup + steps, dev, fmt=args.weight_fmt)
     c = wl.coli
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
@@ -711,6 +718,9 @@ def main():
     ap.add_argument("--experts", type=int, default=None,
                     help="quant workload: experts converted per step (default 256; smaller for "
                          "profiling captures)")
+    ap.add_argument("--weight-fmt", default="i4g", choices=["i4g", "mxfp4", "fp8"],
+                    help="glm_prefill: the expert weight container (int4-grouped g64, MXFP4, "
+                         "fp8-e4m3-b128)")
     ap.add_argument("--router", default="softmax", choices=["softmax", "sigmoid"],
                     help="decode workloads: softmax routing, or the GLM router (sigmoid "
                          "scores with a per-layer selection bias)")
@@ -1046,12 +1056,19 @@ def emit_prefill(args, shape, dev, world, rank, config):
     kern = res["kernels"]
     dom = max(kern, key=lambda n: kern[n]["us_per_launch"])
     kd = kern[dom]
+    fmt_name = {"i4g": "int4-grouped g64 f32 scales",
+                "mxfp4": "MXFP4 (E2M1 codes, E8M0 scale per 32)",
+                "fp8": "fp8-e4m3-b128 (E4M3 codes, f32 scale per 128)"}[args.weight_fmt]
     config = dict(config, l2="inputs larger than L2: %.2f GB of experts resident"
-                  % ((wl.packed.numel() + 4 * wl.scales.numel()) / 1e9),
+                  % ((wl.packed.nbytes + wl.scales.nbytes) / 1e9),
+                  weight_fmt=args.weight_fmt,
+                  timing="one window of %d steps (CUDA events on the launch stream)" % args.steps,
+                  workload=config["workload"].replace("int4-grouped g64 f32 scales", fmt_name),
                   routing="skewed router: the 32 most-used experts took %.1f%% of routes"
                   % (100 * res["top32_share"]))
     line = {
-        "metric": "MoE prefill tokens/s (batched grouped int4 GEMMs on tcgen05)",
+        "metric": "MoE prefill tokens/s (batched grouped GEMMs on tcgen05, %s weights)"
+                  % args.weight_fmt,
         "value": world * res["tokens_per_rank"] / sec, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"] / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

@@ -92,7 +92,7 @@ typedef struct {
 
 /*
  * Expert weight containers (the engine's format registry, [P2] §权重转换:
- * "4 int4-grouped", "7 MXFP4"; [P1] §十 "从 int4 到 MXFP4").
+ * "4 int4-grouped", "7 MXFP4", "8 fp8-e4m3-b128"; [P1] §十 "从 int4 到 MXFP4").
  *   COLI_FMT_I4G    int4-grouped, the format above: nibbles + f32 scale per 64
  *   COLI_FMT_MXFP4  OCP Microscaling MXFP4: blocks of 32 columns share one
  *                   E8M0 scale byte e (X = 2^(e - 127)); each element is an
@@ -105,8 +105,20 @@ typedef struct {
  *                   the tensor-core grouped GEMM at every token count, and
  *                   need hidden % 256 == 0 and ffn % 128 == 0; the decoded
  *                   weights must lie in the fp16 range (as the activations).
+ *   COLI_FMT_FP8    fp8-e4m3-b128 (the registry's "8 fp8-e4m3-b128"): blocks
+ *                   of 128 columns share one f32 scale s; each element is one
+ *                   OCP FP8 E4M3 byte (sign bit 7, 4 exponent bits with bias
+ *                   7, 3 mantissa bits; exponent 0 subnormal; 0x7F / 0xFF
+ *                   NaN, never written by coli_quant_fp8b128):
+ *                     packed uint8 [O][I], scales f32 [O][ceil(I/128)]
+ *                   and W[o][i] = s[o][i/128] * e4m3(code).  Record order and
+ *                   shape rules as for MXFP4 (the grouped GEMM at every token
+ *                   count).  The kernels decode e4m3(code) * 2^-8 and multiply
+ *                   by s * 256 rounded to fp16, so blocks need s * 256 inside
+ *                   the fp16 normal range (max|w| between about 1.1e-4 and
+ *                   1.1e5) for full precision; a NaN code decodes as +-480 s.
  */
-typedef enum { COLI_FMT_I4G = 4, COLI_FMT_MXFP4 = 7 } coli_weight_fmt;
+typedef enum { COLI_FMT_I4G = 4, COLI_FMT_MXFP4 = 7, COLI_FMT_FP8 = 8 } coli_weight_fmt;
 
 const char *coli_status_str(int status);
 
@@ -157,6 +169,20 @@ int coli_quant_i4g(const void *w, coli_dtype w_dtype, int64_t rows, int64_t cols
  */
 int coli_quant_mxfp4(const void *w, coli_dtype w_dtype, int64_t rows, int64_t cols,
                      uint8_t *packed, uint8_t *scales, cudaStream_t stream);
+
+/*
+ * coli_quant_fp8b128 -- quantise W[rows][cols] into fp8-e4m3-b128
+ * (COLI_FMT_FP8).  Per row and block of 128 columns: s = max|w| / 448 (f32
+ * division; 448 = the largest finite E4M3 value); code of each w = the E4M3
+ * value nearest to w / s (f32 division), ties to the even code, saturating at
+ * +-448 (finite), with w's sign.  An all-zero block stores s = 0 and codes 0;
+ * a NaN weight is ignored by the max and stored as +0.
+ *   w       [rows][cols] row-major, dtype w_dtype (COLI_BF16 or COLI_F32)
+ *   packed  [rows][cols] written;  scales f32 [rows][ceil(cols/128)] written
+ * rows >= 0, cols >= 1, any alignment.  Bit-identical to the definition.
+ */
+int coli_quant_fp8b128(const void *w, coli_dtype w_dtype, int64_t rows, int64_t cols,
+                       uint8_t *packed, float *scales, cudaStream_t stream);
 
 /*
  * Workspace: every routed call needs caller-owned device scratch of at least

@@ -92,7 +92,8 @@ int check_desc(const coli_moe_desc *d, int top_k) {
     return COLI_EINVAL;
   if (d->router_fn == COLI_ROUTER_SIGMOID_BIAS && ((uintptr_t)d->router_bias & 3u))
     return COLI_EALIGN;
-  if (d->weight_fmt != 0 && d->weight_fmt != COLI_FMT_I4G && d->weight_fmt != COLI_FMT_MXFP4)
+  if (d->weight_fmt != 0 && d->weight_fmt != COLI_FMT_I4G && d->weight_fmt != COLI_FMT_MXFP4 &&
+      d->weight_fmt != COLI_FMT_FP8)
     return COLI_EINVAL;
   return COLI_OK;
 }
@@ -105,15 +106,15 @@ int pass_tokens(int T) { return T < kDecodeMaxT ? T : kDecodeMaxT; }
 
 // Calls with many tokens take the batched path (grouped tensor-core GEMMs)
 // when its tile shapes divide the layer.
-// MXFP4 layers take it at every token count.
+// MXFP4 and fp8 layers take it at every token count.
 bool use_prefill(const coli_moe_desc *d) {
-  if (weight_fmt(d) == COLI_FMT_MXFP4) return true;
+  if (weight_fmt(d) != COLI_FMT_I4G) return true;
   return d->n_tokens >= kPrefillMinT && prefill_supported(d->hidden, d->ffn);
 }
 
 // A format the layer's shape cannot run in.
 int fmt_unsupported(const coli_moe_desc *d) {
-  return weight_fmt(d) == COLI_FMT_MXFP4 && !prefill_supported(d->hidden, d->ffn);
+  return weight_fmt(d) != COLI_FMT_I4G && !prefill_supported(d->hidden, d->ffn);
 }
 
 int map_err(cudaError_t e) { return coli::cuda_status(e); }
@@ -250,12 +251,14 @@ int64_t coli_expert_scale_count(int64_t H, int64_t F) {
 int64_t coli_fmt_row_bytes(int32_t fmt, int64_t cols) {
   if (cols < 0) return 0;
   if (fmt == 0 || fmt == COLI_FMT_I4G || fmt == COLI_FMT_MXFP4) return (cols + 1) / 2;
+  if (fmt == COLI_FMT_FP8) return cols;
   return 0;
 }
 int64_t coli_fmt_scale_bytes(int32_t fmt, int64_t cols) {
   if (cols < 0) return 0;
   if (fmt == 0 || fmt == COLI_FMT_I4G) return 4 * coli_scales_per_row(cols);
   if (fmt == COLI_FMT_MXFP4) return (cols + kMxBlock - 1) / kMxBlock;
+  if (fmt == COLI_FMT_FP8) return 4 * ((cols + kFp8Block - 1) / kFp8Block);
   return 0;
 }
 int64_t coli_fmt_expert_bytes(int32_t fmt, int64_t H, int64_t F) {
@@ -285,6 +288,15 @@ int coli_quant_mxfp4(const void *w, coli_dtype w_dtype, int64_t rows, int64_t co
   if (rows > 0 && (!w || !packed || !scales)) return COLI_EINVAL;
   if (rows > 0 && cols > INT64_MAX / rows) return COLI_EINVAL;
   return map_err(launch_quant_mxfp4(w, w_dtype, rows, cols, packed, scales, stream));
+}
+
+int coli_quant_fp8b128(const void *w, coli_dtype w_dtype, int64_t rows, int64_t cols,
+                       uint8_t *packed, float *scales, cudaStream_t stream) {
+  if (rows < 0 || cols < 1) return COLI_EINVAL;
+  if (w_dtype != COLI_F32 && w_dtype != COLI_BF16) return COLI_EINVAL;
+  if (rows > 0 && (!w || !packed || !scales)) return COLI_EINVAL;
+  if (rows > 0 && cols > INT64_MAX / rows) return COLI_EINVAL;
+  return map_err(launch_quant_fp8b128(w, w_dtype, rows, cols, packed, scales, stream));
 }
 
 size_t coli_moe_workspace_size(const coli_moe_desc *d, int top_k) {
@@ -449,8 +461,8 @@ static int prefill_run(const coli_moe_desc *d, int k, int n_layers, const void *
     a.packed = packed + l * pk_stride;
     a.scales = (const float *)((const uint8_t *)scales + l * sc_bytes);
     a.eb = coli_fmt_expert_bytes(fmt, H, F);
-    a.es = fmt == COLI_FMT_MXFP4 ? coli_fmt_expert_scale_bytes(fmt, H, F)
-                                 : coli_expert_scale_count(H, F);
+    a.es = fmt == COLI_FMT_I4G ? coli_expert_scale_count(H, F)
+                               : coli_fmt_expert_scale_bytes(fmt, H, F);
     a.residual = residual ? (l == 0 ? (const float *)x : out) : nullptr;
     a.out = out;
     a.layer_out = layer_out ? layer_out + (size_t)l * T * H : nullptr;

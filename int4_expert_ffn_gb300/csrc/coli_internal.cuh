@@ -13,6 +13,7 @@ namespace coli {
 
 constexpr int kGroup = 64;          // columns per scale
 constexpr int kMxBlock = 32;        // MXFP4: columns per E8M0 scale
+constexpr int kFp8Block = 128;      // fp8-e4m3-b128: columns per f32 scale
 constexpr int kDecodeMaxT = 16;     // tokens per call served by the GEMV path
 constexpr int kMaxTopK = 64;
 constexpr int kMaxExperts = 1024;
@@ -191,7 +192,7 @@ constexpr int kPrefillMinT = 64;      // calls with at least this many tokens ta
 constexpr int kGroupTokens = 256;     // tokens per block of the counting sort
 struct PrefillArgs {
   TierMap tier;
-  int fmt;                  // COLI_FMT_I4G or COLI_FMT_MXFP4 (then es counts scale bytes)
+  int fmt;                  // COLI_FMT_I4G, _MXFP4 or _FP8 (the last two: es counts scale bytes)
   int T, H, F, E, S, k;
   int router_fn;            // coli_router_fn
   const float *router_bias; // [E] (sigmoid router) or null
@@ -239,11 +240,13 @@ cudaError_t launch_down_multi(const Dec2Args &a, cudaStream_t s, bool pdl);
 bool plan_layer1(Dec2Args &a);
 cudaError_t launch_layer1(const Dec2Args &a, cudaStream_t s, bool pdl);
 
-// Quantisers (quant.cu, quant_mx.cu).
+// Quantisers (quant.cu, quant_fmt.cu).
 cudaError_t launch_quant_i4g(const void *w, int w_dtype, int64_t rows, int64_t cols,
                              uint8_t *packed, float *scales, cudaStream_t s);
 cudaError_t launch_quant_mxfp4(const void *w, int w_dtype, int64_t rows, int64_t cols,
                                uint8_t *packed, uint8_t *scales, cudaStream_t s);
+cudaError_t launch_quant_fp8b128(const void *w, int w_dtype, int64_t rows, int64_t cols,
+                                 uint8_t *packed, float *scales, cudaStream_t s);
 
 int num_sms();
 // The layer forward over a tiered expert store (coli_api.cu); `packed` and

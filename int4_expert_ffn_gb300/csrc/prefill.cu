@@ -36,10 +36,6 @@ namespace {
 constexpr int kBM = 128;          // m-tile rows (routes)
 constexpr int kBK = 64;           // K per k-tile: one scale group
 constexpr int kBN = 256;          // n-tile columns (gate/up: 128 gate + 128 up)
-constexpr int kNA = 5;            // A ring (fp16 activation tiles)
-constexpr int kNB = 3;            // B ring (dequantised fp16 weight tiles)
-constexpr int kNR = 4;            // raw ring (int4 rows + scales as copied)
-constexpr int kDist = 3;          // copies run this many k-tiles ahead of the dequantisation
 constexpr int kProducerWarps = 8; // two weight-row halves and four activation pieces per thread
 constexpr int kProducerThreads = 32 * kProducerWarps;
 constexpr int kMmaWarp = kProducerWarps;
@@ -48,19 +44,43 @@ constexpr int kEpilogueThreads = 32 * kEpilogueWarps;
 constexpr int kGemmThreads = 32 * (kProducerWarps + 1 + kEpilogueWarps);
 constexpr int kATileBytes = kBM * kBK * 2;     // 16 KB
 constexpr int kBTileBytes = kBN * kBK * 2;     // 32 KB
-// Raw slot: the k-tile's 32 bytes of nibbles of every weight row as 16-byte
-// halves, [2][kProducerThreads] in copy order, then one scale per half.
+// Raw slot: the k-tile's bytes of every weight row as each thread copied
+// them -- [2 rows][chunks][kProducerThreads] 16-byte chunks, a thread's
+// chunks covering columns 32 (th % 2) .. + 31 of its rows -- then one 4-byte
+// scale word per row half.
 constexpr int kRawHalves = 2 * kProducerThreads;
-constexpr int kRawNibbleBytes = kRawHalves * 16;        // 8 KB
-constexpr int kRawBytes = kRawNibbleBytes + kRawHalves * 4;   // + 2 KB scales
 constexpr int kARowPasses = kBM * 8 / kProducerThreads;        // 128-byte rows: 8 threads each
 constexpr int kTableBytes = 2 * (kMaxExperts + kMaxShared + 1) * 4;   // item_begin, offsets
-constexpr int kGemmSmem = kNA * kATileBytes + kNB * kBTileBytes + kNR * kRawBytes + kTableBytes + 2048;
-static_assert(kNR > kDist, "a raw slot is refilled only after its dequantisation");
+
+// Ring depths per weight container.  A 4-bit row brings 32 bytes per k-tile
+// (one 16-byte chunk per thread and row); an fp8 row 64 (two chunks), so its
+// raw slots are twice as large and the A and raw rings one stage shallower,
+// to stay within one block's shared memory.
+template <int FMT>
+struct Geo {
+  static constexpr int kNA = 5;      // A ring (fp16 activation tiles)
+  static constexpr int kNB = 3;      // B ring (dequantised fp16 weight tiles)
+  static constexpr int kNR = 4;      // raw ring (weight rows + scales as copied)
+  static constexpr int kDist = 3;    // copies run this many k-tiles ahead of the dequantisation
+  static constexpr int kChunks = 1;  // 16-byte chunks per thread, row and k-tile
+};
+template <>
+struct Geo<COLI_FMT_FP8> {
+  static constexpr int kNA = 4, kNB = 3, kNR = 3, kDist = 2, kChunks = 2;
+};
+template <int FMT>
+struct GeoBytes {
+  using G = Geo<FMT>;
+  static constexpr int kRawData = kRawHalves * 16 * G::kChunks;   // 8 KB (4-bit), 16 KB (fp8)
+  static constexpr int kRaw = kRawData + kRawHalves * 4;          // + 2 KB scale words
+  static constexpr int kSmem =
+      G::kNA * kATileBytes + G::kNB * kBTileBytes + G::kNR * kRaw + kTableBytes + 2048;
+  static_assert(G::kNR > G::kDist, "a raw slot is refilled only after its dequantisation");
+  static_assert(kSmem <= 232448, "shared memory of one block");
+};
 static_assert(kProducerThreads == kBN, "a thread pair per B row, two rows per pair");
 static_assert(kRawHalves == 2 * kBN && kARowPasses * kProducerThreads == 8 * kBM,
               "copy shares of the producers");
-static_assert(kGemmSmem <= 232448, "shared memory of one block");
 
 enum GemmMode : int { kModeGateUp = 0, kModeDown = 1 };
 
@@ -210,6 +230,27 @@ __device__ __forceinline__ void dequant8_mx(uint32_t w0, uint32_t w1, __half2 s2
       o[4 * i + j] = *reinterpret_cast<const uint32_t *>(&v);
     }
   }
+}
+
+// 16 fp8 E4M3 codes (one per byte, column order) -> 8 fp16x2 words of
+// e4m3(code) * X.  Moving a code's exponent and mantissa bits (6..0) to fp16
+// bits 13..7 and its sign to bit 15 gives exactly e4m3(code) * 2^-8: the
+// exponent biases differ by 8 (15 - 7), and E4M3 subnormals (exponent 0,
+// m 2^-9) land on fp16 subnormals of the same mantissa.  The caller passes
+// X = s * 256 as fp16.
+__device__ __forceinline__ void dequant16_fp8(uint4 w, __half2 s2, uint32_t (&o)[8]) {
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      // codes 2j, 2j + 1 of the word into bytes 1 and 3
+      const uint32_t t = __byte_perm(ws[i], 0, j ? 0x3424u : 0x1404u);
+      const uint32_t h = (t & 0x80008000u) | ((t >> 1) & 0x3F803F80u);
+      __half2 v = *reinterpret_cast<const __half2 *>(&h);
+      v = __hmul2(v, s2);
+      o[2 * i + j] = *reinterpret_cast<const uint32_t *>(&v);
+    }
 }
 
 // The E8M0 scale byte e as an fp16 pair: 2^(e - 127) (255: NaN).
@@ -482,11 +523,15 @@ __global__ void __launch_bounds__(256) k_gscatter(PrefillArgs p) {
 // ---------------------------------------------------------------------------
 // The grouped GEMM.
 
-// FMT: COLI_FMT_I4G (one f32 scale per row and k-tile) or COLI_FMT_MXFP4 (one
-// E8M0 byte per row and 32 columns: a thread's 16-byte half of the k-tile has
-// exactly one; the copy brings the aligned 4-byte word that holds it).
+// FMT: COLI_FMT_I4G (one f32 scale per row and k-tile), COLI_FMT_MXFP4 (one
+// E8M0 byte per row and 32 columns: a thread's half of the k-tile has exactly
+// one; the copy brings the aligned 4-byte word that holds it) or COLI_FMT_FP8
+// (one f32 scale per row and two k-tiles).
 template <int MODE, int FMT>
 __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
+  using G = Geo<FMT>;
+  constexpr int kNA = G::kNA, kNB = G::kNB, kNR = G::kNR, kDist = G::kDist, kCh = G::kChunks;
+  constexpr int kRawData = GeoBytes<FMT>::kRawData, kRawBytes = GeoBytes<FMT>::kRaw;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *a_ring = smem;                                  // kNA x 16 KB (fp16, swizzled)
@@ -575,7 +620,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
           }
           const uint8_t *pk;
           const uint8_t *sc;
-          if (FMT == COLI_FMT_MXFP4) {
+          if (FMT != COLI_FMT_I4G) {
             pk = p.packed + (int64_t)it.e * p.eb;
             sc = (const uint8_t *)p.scales + (int64_t)it.e * p.es;
           } else {
@@ -583,20 +628,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
             expert_record(p.tier, p.packed, p.scales, p.eb, p.es, it.e, &pk, &scf);
             sc = (const uint8_t *)scf;
           }
-          // bytes of one row's scales (K columns), the gate/up/down matrices' rows
-          const int64_t sh = FMT == COLI_FMT_MXFP4 ? H / kMxBlock : 4 * (H / kGroup);
-          const int64_t sf = FMT == COLI_FMT_MXFP4 ? F / kMxBlock : 4 * (F / kGroup);
+          // bytes of one row (K columns) and of its scales, for the
+          // gate/up (K = H) and down (K = F) matrices
+          const int64_t rh = FMT == COLI_FMT_FP8 ? H : H / 2;
+          const int64_t rf = FMT == COLI_FMT_FP8 ? F : F / 2;
+          const int64_t sh = FMT == COLI_FMT_MXFP4 ? H / kMxBlock
+                             : FMT == COLI_FMT_FP8 ? 4 * (H / kFp8Block) : 4 * (H / kGroup);
+          const int64_t sf = FMT == COLI_FMT_MXFP4 ? F / kMxBlock
+                             : FMT == COLI_FMT_FP8 ? 4 * (F / kFp8Block) : 4 * (F / kGroup);
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             if (MODE == kModeGateUp) {
               // B rows 0..127 are gate rows, 128..255 the up rows of the same f
               const int f = it.ni * (kBN / 2) + b_row0;
               const int64_t mat = j;
-              b_src[j] = pk + mat * (int64_t)F * (H / 2) + (int64_t)f * (H / 2);
+              b_src[j] = pk + mat * (int64_t)F * rh + (int64_t)f * rh;
               b_sc[j] = sc + mat * (int64_t)F * sh + (int64_t)f * sh;
             } else {
               const int hr = it.ni * kBN + b_row0 + 128 * j;
-              b_src[j] = pk + (int64_t)F * H + (int64_t)hr * (F / 2);
+              b_src[j] = pk + 2 * (int64_t)F * rh + (int64_t)hr * rf;
               b_sc[j] = sc + (int64_t)2 * F * sh + (int64_t)hr * sf;
             }
           }
@@ -611,10 +661,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
         uint8_t *raw = r_ring + (t % kNR) * kRawBytes;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          cp16(smem_u32(raw + (j * kProducerThreads + th) * 16), b_src[j] + k0 / 2 + 16 * b_half);
-          // int4: the k-tile's f32 scale; MXFP4: the word holding its two E8M0 bytes
-          cp4(smem_u32(raw + kRawNibbleBytes + (j * kProducerThreads + th) * 4),
-              b_sc[j] + (FMT == COLI_FMT_MXFP4 ? (kt >> 1) * 4 : kt * 4));
+#pragma unroll
+          for (int ch = 0; ch < kCh; ++ch)
+            cp16(smem_u32(raw + ((j * kCh + ch) * kProducerThreads + th) * 16),
+                 b_src[j] + (k0 + 32 * b_half) * kCh / 2 + 16 * ch);
+          // int4: the k-tile's f32 scale; MXFP4: the word holding its two E8M0
+          // bytes; fp8: the f32 scale of the 128 columns holding the k-tile
+          cp4(smem_u32(raw + kRawData + (j * kProducerThreads + th) * 4),
+              b_sc[j] + (FMT == COLI_FMT_I4G ? kt * 4 : (kt >> 1) * 4));
         }
         if (++kt == nk) { kt = 0; ++item; }
       }
@@ -630,19 +684,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int slot = j * kProducerThreads + th;
-        const uint4 w = *(const uint4 *)(raw + slot * 16);
-        const uint32_t sw = *(const uint32_t *)(raw + kRawNibbleBytes + slot * 4);
+        const uint32_t sw = *(const uint32_t *)(raw + kRawData + slot * 4);
         const __half2 s2 = FMT == COLI_FMT_MXFP4
                                ? e8m0_half2((sw >> (8 * (2 * (kt_c & 1) + b_half))) & 0xFFu)
-                               : __float2half2_rn(__uint_as_float(sw));
-        const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+                           : FMT == COLI_FMT_FP8 ? __float2half2_rn(__uint_as_float(sw) * 256.0f)
+                                                 : __float2half2_rn(__uint_as_float(sw));
         const int row = b_row0 + 128 * j;
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           // columns 32 b_half + 16 q .. + 15: 16-byte chunks 4 b_half + 2 q, + 1
           uint32_t o[8];
-          if (FMT == COLI_FMT_MXFP4) dequant8_mx(wd[2 * q], wd[2 * q + 1], s2, o);
-          else dequant8(wd[2 * q], wd[2 * q + 1], s2, o);
+          if (FMT == COLI_FMT_FP8) {
+            const uint4 w = *(const uint4 *)(raw + ((j * kCh + q) * kProducerThreads + th) * 16);
+            dequant16_fp8(w, s2, o);
+          } else {
+            const uint4 w = *(const uint4 *)(raw + slot * 16);
+            const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+            if (FMT == COLI_FMT_MXFP4) dequant8_mx(wd[2 * q], wd[2 * q + 1], s2, o);
+            else dequant8(wd[2 * q], wd[2 * q + 1], s2, o);
+          }
           st_shared16(b_dst + sw128_off(row, 4 * b_half + 2 * q), o[0], o[1], o[2], o[3]);
           st_shared16(b_dst + sw128_off(row, 4 * b_half + 2 * q + 1), o[4], o[5], o[6], o[7]);
         }
@@ -809,7 +869,25 @@ bool prefill_supported(int H, int F) {
   return H % kBN == 0 && F % (kBN / 2) == 0 && H % kBK == 0 && F % kBK == 0;
 }
 
-size_t prefill_gemm_smem() { return kGemmSmem; }
+namespace {
+// The gate/up and down GEMMs of one layer over weights in container FMT.
+template <int FMT>
+cudaError_t launch_gemms(const PrefillArgs &p, int nsm, cudaStream_t s) {
+  constexpr int smem = GeoBytes<FMT>::kSmem;
+  auto gemm_gu = k_pgemm<kModeGateUp, FMT>;
+  auto gemm_dn = k_pgemm<kModeDown, FMT>;
+  cudaError_t e;
+  if ((e = set_smem(gemm_gu, smem)) != cudaSuccess) return e;
+  if ((e = set_smem(gemm_dn, smem)) != cudaSuccess) return e;
+  size_t slot = 0;
+  if ((e = record_profile(COLI_KERNEL_PREFILL_GATEUP, s, false, &slot)) != cudaSuccess) return e;
+  gemm_gu<<<nsm, kGemmThreads, smem, s>>>(p);
+  if ((e = record_profile(COLI_KERNEL_PREFILL_GATEUP, s, true, &slot)) != cudaSuccess) return e;
+  if ((e = record_profile(COLI_KERNEL_PREFILL_DOWN, s, false, &slot)) != cudaSuccess) return e;
+  gemm_dn<<<nsm, kGemmThreads, smem, s>>>(p);
+  return record_profile(COLI_KERNEL_PREFILL_DOWN, s, true, &slot);
+}
+}  // namespace
 
 cudaError_t launch_prefill(const PrefillArgs &p, int x_dtype, int wr_dtype, cudaStream_t s) {
   cudaError_t e;
@@ -842,19 +920,10 @@ cudaError_t launch_prefill(const PrefillArgs &p, int x_dtype, int wr_dtype, cuda
   k_gscan<<<1, 1024, 0, s>>>(p, nb);
   k_gscatter<<<nb, 256, (size_t)E * 4, s>>>(p);
   // GEMMs
-  auto gemm_gu = p.fmt == COLI_FMT_MXFP4 ? k_pgemm<kModeGateUp, COLI_FMT_MXFP4>
-                                         : k_pgemm<kModeGateUp, COLI_FMT_I4G>;
-  auto gemm_dn = p.fmt == COLI_FMT_MXFP4 ? k_pgemm<kModeDown, COLI_FMT_MXFP4>
-                                         : k_pgemm<kModeDown, COLI_FMT_I4G>;
-  if ((e = set_smem(gemm_gu, kGemmSmem)) != cudaSuccess) return e;
-  if ((e = set_smem(gemm_dn, kGemmSmem)) != cudaSuccess) return e;
-  size_t slot = 0;
-  if ((e = record_profile(COLI_KERNEL_PREFILL_GATEUP, s, false, &slot)) != cudaSuccess) return e;
-  gemm_gu<<<nsm, kGemmThreads, kGemmSmem, s>>>(p);
-  if ((e = record_profile(COLI_KERNEL_PREFILL_GATEUP, s, true, &slot)) != cudaSuccess) return e;
-  if ((e = record_profile(COLI_KERNEL_PREFILL_DOWN, s, false, &slot)) != cudaSuccess) return e;
-  gemm_dn<<<nsm, kGemmThreads, kGemmSmem, s>>>(p);
-  if ((e = record_profile(COLI_KERNEL_PREFILL_DOWN, s, true, &slot)) != cudaSuccess) return e;
+  if (p.fmt == COLI_FMT_MXFP4) e = launch_gemms<COLI_FMT_MXFP4>(p, nsm, s);
+  else if (p.fmt == COLI_FMT_FP8) e = launch_gemms<COLI_FMT_FP8>(p, nsm, s);
+  else e = launch_gemms<COLI_FMT_I4G>(p, nsm, s);
+  if (e != cudaSuccess) return e;
   // combine
   const int64_t nc = (int64_t)T * (H / 4);
   const int gc = (int)((nc + 255) / 256 < 8 * nsm ? (nc + 255) / 256 : 8 * nsm);

@@ -71,6 +71,60 @@ class Layer:
         return p, s, self.wr.double().numpy()
 
 
+class FmtLayer:
+    """One MoE layer in a floating-point container (COLI_FMT_MXFP4 or
+    COLI_FMT_FP8): quantised on the GPU and, independently, by the oracle;
+    the two records must agree byte for byte."""
+
+    def __init__(self, shape, fmt, layer=0, seed=0):
+        c = coli()
+        H, F, E, S = shape.hidden, shape.ffn, shape.experts, shape.shared
+        gpu_q, orc_q, sdt = {
+            c.COLI_FMT_MXFP4: (c.coli_quant_mxfp4, orc.quant_mxfp4, torch.uint8),
+            c.COLI_FMT_FP8: (c.coli_quant_fp8b128, orc.quant_fp8b128, torch.float32),
+        }[fmt]
+        self.shape, self.fmt = shape, fmt
+        mats = [synth.expert_matrix(shape, layer, e, m, seed) for e in range(E + S)
+                for m in range(3)]
+        esz = torch.tensor([], dtype=sdt).element_size()
+        eb = c.coli_fmt_expert_bytes(fmt, H, F)
+        es = c.coli_fmt_expert_scale_bytes(fmt, H, F) // esz
+        self.packed = torch.empty((E + S) * eb, dtype=torch.uint8, device="cuda")
+        self.scales = torch.empty((E + S) * es, dtype=sdt, device="cuda")
+        p0 = s0 = 0
+        ops, oss = [], []
+        for m in mats:
+            rows, cols = m.shape
+            nb = rows * c.lib.coli_fmt_row_bytes(fmt, cols)
+            ns = rows * c.lib.coli_fmt_scale_bytes(fmt, cols) // esz
+            gpu_q(m.cuda(), self.packed[p0:p0 + nb].view(rows, -1),
+                  self.scales[s0:s0 + ns].view(rows, -1))
+            p0, s0 = p0 + nb, s0 + ns
+            a, b = orc_q(m.float().numpy())
+            ops.append(a.reshape(-1))
+            oss.append(b.reshape(-1))
+        self.o_packed, self.o_scales = np.concatenate(ops), np.concatenate(oss)
+        self.wr = synth.router_weights(shape, layer, seed)
+        torch.cuda.synchronize()
+        assert np.array_equal(self.packed.cpu().numpy(), self.o_packed)
+        assert np.array_equal(self.scales.cpu().numpy().view(np.uint8),
+                              self.o_scales.view(np.uint8))
+
+
+def fmt_desc(shape, T, fmt, bias=None, x_dtype=None):
+    """Layer descriptor for weights in container fmt (softmax router unless a
+    sigmoid-router bias is given)."""
+    c = coli()
+    args = [shape.hidden, shape.ffn, shape.experts, shape.shared, T,
+            c.COLI_F32 if (x_dtype or torch.float32) == torch.float32 else c.COLI_BF16,
+            c.COLI_F32 if shape.router_dtype == "f32" else c.COLI_BF16]
+    if bias is not None:
+        args += [c.COLI_ROUTER_SIGMOID_BIAS, bias]
+    else:
+        args += [c.COLI_ROUTER_SOFTMAX, None]
+    return c.MoEDesc(*args, weight_fmt=fmt)
+
+
 def min_topk_gap(logits, k):
     """Smallest adjacent gap among the k+1 largest logits of each row (f32 ranking)."""
     lg = np.sort(logits.astype(np.float32), axis=1)[:, ::-1]

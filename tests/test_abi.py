@@ -81,6 +81,7 @@ def test_desc_layout_matches_header(coli):
     text = open(os.path.join(ROOT, "include", "coli.h")).read()
     assert "COLI_ROUTER_SIGMOID_BIAS = 1" in text and "const float *router_bias;" in text
     assert "int32_t weight_fmt;" in text and "COLI_FMT_MXFP4 = 7" in text
+    assert "COLI_FMT_FP8 = 8" in text
 
 
 def test_workspace_size_bad_topk(coli):
@@ -162,3 +163,12 @@ def test_weight_format_rules(coli):
     assert coli.coli_fmt_expert_bytes(coli.COLI_FMT_MXFP4, 256, 128) == coli.coli_expert_packed_bytes(256, 128)
     assert coli.coli_fmt_expert_scale_bytes(coli.COLI_FMT_MXFP4, 256, 128) == 3 * 256 * 128 // 32
     assert coli.lib.coli_fmt_row_bytes(9, 64) == 0
+    # fp8-e4m3-b128: one byte per element, one f32 scale per 128 columns; same shape rules
+    d = coli.MoEDesc(256, 64, 8, 1, 4, coli.COLI_F32, coli.COLI_BF16, weight_fmt=coli.COLI_FMT_FP8)
+    assert coli.coli_moe_workspace_size(d, 2) == 0
+    d = coli.MoEDesc(256, 128, 8, 1, 4, coli.COLI_F32, coli.COLI_BF16, weight_fmt=coli.COLI_FMT_FP8)
+    assert coli.coli_moe_workspace_size(d, 2) > 0
+    assert coli.lib.coli_fmt_row_bytes(coli.COLI_FMT_FP8, 333) == 333
+    assert coli.lib.coli_fmt_scale_bytes(coli.COLI_FMT_FP8, 333) == 4 * 3
+    assert coli.coli_fmt_expert_bytes(coli.COLI_FMT_FP8, 256, 128) == 3 * 256 * 128
+    assert coli.coli_fmt_expert_scale_bytes(coli.COLI_FMT_FP8, 256, 128) == 4 * (2 * 128 * 2 + 256 * 1)

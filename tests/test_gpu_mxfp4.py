@@ -4,7 +4,6 @@ columns, NaN and zero blocks, bf16 and f32), and MXFP4 layers -- which run on
 the tensor-core grouped GEMM at every token count -- within the tolerance of
 the other tests, route counts exact, including the sigmoid router, shared
 experts and a chained stack."""
-import dataclasses
 import os
 
 import numpy as np
@@ -14,7 +13,7 @@ import torch
 import oracle as orc
 from conftest import parse_golden
 from int4_expert_ffn_gb300 import synth
-from helpers import REL_TOL, coli, rel_err, tokens_without_ties
+from helpers import REL_TOL, FmtLayer, coli, fmt_desc, rel_err, tokens_without_ties
 
 pytestmark = pytest.mark.gpu
 
@@ -54,47 +53,12 @@ def test_quant_random_with_outliers(rows, cols, dtype):
     assert bad.size == 0, "%d bytes differ, first %s" % (len(bad), bad[:3].tolist())
 
 
-class MxLayer:
-    """One MoE layer in MXFP4: quantised on the GPU and, independently, by the oracle."""
-
-    def __init__(self, shape, layer=0, seed=0):
-        c = coli()
-        H, F, E, S = shape.hidden, shape.ffn, shape.experts, shape.shared
-        self.shape = shape
-        mats = [synth.expert_matrix(shape, layer, e, m, seed) for e in range(E + S)
-                for m in range(3)]
-        eb = c.coli_fmt_expert_bytes(c.COLI_FMT_MXFP4, H, F)
-        es = c.coli_fmt_expert_scale_bytes(c.COLI_FMT_MXFP4, H, F)
-        self.packed = torch.empty((E + S) * eb, dtype=torch.uint8, device="cuda")
-        self.scales = torch.empty((E + S) * es, dtype=torch.uint8, device="cuda")
-        p0 = s0 = 0
-        ops, oss = [], []
-        for m in mats:
-            rows, cols = m.shape
-            nb, ns = rows * cols // 2, rows * cols // 32
-            c.coli_quant_mxfp4(m.cuda(), self.packed[p0:p0 + nb].view(rows, -1),
-                               self.scales[s0:s0 + ns].view(rows, -1))
-            p0, s0 = p0 + nb, s0 + ns
-            a, b = orc.quant_mxfp4(m.float().numpy())
-            ops.append(a.reshape(-1))
-            oss.append(b.reshape(-1))
-        self.o_packed, self.o_scales = np.concatenate(ops), np.concatenate(oss)
-        self.wr = synth.router_weights(shape, layer, seed)
-        torch.cuda.synchronize()
-        assert np.array_equal(self.packed.cpu().numpy(), self.o_packed)
-        assert np.array_equal(self.scales.cpu().numpy(), self.o_scales)
+def MxLayer(shape, layer=0, seed=0):
+    return FmtLayer(shape, coli().COLI_FMT_MXFP4, layer, seed)
 
 
 def desc_mx(shape, T, bias=None, x_dtype=None):
-    c = coli()
-    args = [shape.hidden, shape.ffn, shape.experts, shape.shared, T,
-            c.COLI_F32 if (x_dtype or torch.float32) == torch.float32 else c.COLI_BF16,
-            c.COLI_F32 if shape.router_dtype == "f32" else c.COLI_BF16]
-    if bias is not None:
-        args += [c.COLI_ROUTER_SIGMOID_BIAS, bias]
-    else:
-        args += [c.COLI_ROUTER_SOFTMAX, None]
-    return c.MoEDesc(*args, weight_fmt=c.COLI_FMT_MXFP4)
+    return fmt_desc(shape, T, coli().COLI_FMT_MXFP4, bias, x_dtype)
 
 
 SHAPES = [
