@@ -235,6 +235,7 @@ const char *coli_status_str(int status) {
     case COLI_EUNSUPPORTED: return "unsupported configuration";
     case COLI_EIO: return "file I/O failed";
     case COLI_EREFUSED: return "usage history of another model or format";
+    case COLI_ERANGE: return "operand outside the fp16 range of the batched path";
     default: return "unknown status";
   }
 }
@@ -597,7 +598,8 @@ int coli_moe_check(void *workspace, int clear, uint32_t *flags, cudaStream_t str
   if (e == cudaSuccess && clear && v) e = cudaMemsetAsync(dev, 0, sizeof(uint32_t), stream);
   if (e != cudaSuccess) return map_err(e);
   *flags = v;
-  return (v & COLI_FLAG_TIMEOUT) ? COLI_ETIMEOUT : COLI_OK;
+  if (v & COLI_FLAG_TIMEOUT) return COLI_ETIMEOUT;
+  return (v & COLI_FLAG_RANGE) ? COLI_ERANGE : COLI_OK;
 }
 
 }  // extern "C"

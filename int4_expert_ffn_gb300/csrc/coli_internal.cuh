@@ -46,8 +46,9 @@ enum CtrlWord : int {
   kCtrlPrefillMTiles = 2,  // m-tiles of the current batched call (written by the grouping)
   kCtrlBarArrive = 3,  // grid barrier of the one-token layer kernel: arrivals of this use
   kCtrlBarGen = 4,     //   and its generation (left as they are between calls)
-  kCtrlWaitLimit = 5,  // 0: default bounded waits; else the grid barrier's spin limit in
-                       //   clock cycles (a test hook that makes the wait run out)
+  kCtrlWaitLimit = 5,  // 0: default bounded waits; else the spin limit in clock cycles of
+                       //   the one-token kernel's grid barrier and the grouped GEMMs'
+                       //   pipeline waits (a test hook that makes the waits run out)
   kCtrlWords = 64,     // 256 bytes
 };
 static_assert(kCtrlWords * 4 <= kFxOffset, "control words precede the fixed-point region");

@@ -88,6 +88,11 @@ __device__ __forceinline__ void set_flag_p(uint32_t *ctrl, uint32_t f) {
   atomicOr(ctrl + kCtrlFlags, f);
 }
 
+// Either fp16 of the pair is +-inf (exponent all ones, mantissa zero).
+__device__ __forceinline__ bool half2_has_inf(uint32_t w) {
+  return (w & 0x7FFFu) == 0x7C00u || (w & 0x7FFF0000u) == 0x7C000000u;
+}
+
 // ---------------------------------------------------------------------------
 // tcgen05 / TMEM helpers (inline PTX)
 
@@ -310,7 +315,8 @@ __device__ __forceinline__ void load8(const float *src, float (&v)[8]) {
 }
 
 template <typename XT>
-__global__ void k_x16(const XT *x, __half *x16, int64_t n) {
+__global__ void k_x16(const XT *x, __half *x16, int64_t n, uint32_t *ctrl) {
+  bool inf = false;
   for (int64_t i = 8 * ((int64_t)blockIdx.x * blockDim.x + threadIdx.x); i < n;
        i += 8 * (int64_t)gridDim.x * blockDim.x) {
     float v[8];
@@ -320,9 +326,11 @@ __global__ void k_x16(const XT *x, __half *x16, int64_t n) {
     for (int j = 0; j < 4; ++j) {
       const __half2 h = __floats2half2_rn(v[2 * j], v[2 * j + 1]);
       o[j] = *reinterpret_cast<const uint32_t *>(&h);
+      inf |= half2_has_inf(o[j]);
     }
     *reinterpret_cast<uint4 *>(x16 + i) = make_uint4(o[0], o[1], o[2], o[3]);
   }
+  if (inf) set_flag_p(ctrl, COLI_FLAG_RANGE);
 }
 
 // ---------------------------------------------------------------------------
@@ -542,7 +550,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
   uint64_t *b_empty = a_empty + kNA;
   uint64_t *tm_full = b_empty + kNB;                       // [2]
   uint64_t *tm_empty = tm_full + 2;                        // [2]
-  uint32_t *s_taddr = (uint32_t *)(tm_empty + 2);
+  uint64_t *mma_done = tm_empty + 2;                       // the MMA thread's last commit
+  uint32_t *s_taddr = (uint32_t *)(mma_done + 1);
   int *s_abort = (int *)(s_taddr + 1);
   int *s_begin = s_abort + 4;                              // [n_groups + 1]
   int *s_off = s_begin + (kMaxExperts + kMaxShared + 1);   // [n_groups + 1]
@@ -562,6 +571,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
       mbar_init(&tm_full[b], 1);
       mbar_init(&tm_empty[b], kEpilogueThreads);
     }
+    mbar_init(mma_done, 1);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -585,6 +595,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
   const int n_items = s_begin[p.n_groups] * n_ntiles;
   const int my_items = n_items > (int)blockIdx.x ? (n_items - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
   const int n_ticks = my_items * nk;         // this CTA's k-tiles over all its items
+  const uint32_t lim_word = __ldcg(p.ctrl + kCtrlWaitLimit);
+  const long long lim = lim_word ? (long long)lim_word : kWaitCycles;   // pipeline waits
 
   if (warp < kProducerWarps) {
     // ---- producers: tick t issues the copies of k-tile t (A rows, raw B
@@ -652,7 +664,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
           }
         }
         const int sa = t % kNA;
-        if (!mbar_wait(&a_empty[sa], ((t / kNA) & 1) ^ 1)) { ok = false; break; }
+        if (!mbar_wait(&a_empty[sa], ((t / kNA) & 1) ^ 1, lim)) { ok = false; break; }
         const uint32_t a_dst = smem_u32(a_ring + sa * kATileBytes);
         const int k0 = kt * kBK;
 #pragma unroll
@@ -677,7 +689,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
       if (c < 0) continue;
       cp_wait<kDist>();            // groups of ticks <= c have landed (this thread's copies)
       const int sb = c % kNB;
-      if (!mbar_wait(&b_empty[sb], ((c / kNB) & 1) ^ 1)) { ok = false; break; }
+      if (!mbar_wait(&b_empty[sb], ((c / kNB) & 1) ^ 1, lim)) { ok = false; break; }
       const uint8_t *raw = r_ring + (c % kNR) * kRawBytes;
       const uint32_t b_dst = smem_u32(b_ring + sb * kBTileBytes);
       const int kt_c = c % nk;
@@ -722,9 +734,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
       for (int c = 0; c < n_ticks; ++c) {
         const int item = c / nk, kt = c % nk, buf = item & 1;
         const uint32_t acc = tbase + (uint32_t)(buf * kBN);
-        if (kt == 0 && !mbar_wait(&tm_empty[buf], ((item >> 1) & 1) ^ 1)) break;
         const int sb = c % kNB, sa = c % kNA;
-        if (!mbar_wait(&full[sb], (c / kNB) & 1)) break;
+        if ((kt == 0 && !mbar_wait(&tm_empty[buf], ((item >> 1) & 1) ^ 1, lim)) ||
+            !mbar_wait(&full[sb], (c / kNB) & 1, lim)) {
+          set_flag_p(p.ctrl, COLI_FLAG_TIMEOUT);
+          break;
+        }
         if (*(volatile int *)s_abort) break;
         tc_fence_after();
         const uint32_t a0 = smem_u32(a_ring + sa * kATileBytes);
@@ -737,6 +752,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
         tc_commit(&b_empty[sb]);
         if (kt == nk - 1) tc_commit(&tm_full[buf]);
       }
+      // Whether the loop ran to its end or gave up, wait until every MMA this
+      // thread issued has completed, so that none is in flight when TMEM is
+      // freed (an abandoned item's accumulator is never read).
+      tc_commit(mma_done);
+      if (!mbar_wait(mma_done, 0)) set_flag_p(p.ctrl, COLI_FLAG_TIMEOUT);
     }
     __syncwarp();
   } else {
@@ -745,7 +765,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
     for (int i = 0; i < my_items; ++i) {
       const int buf = i & 1;
-      if (!mbar_wait(&tm_full[buf], (i >> 1) & 1)) {
+      if (!mbar_wait(&tm_full[buf], (i >> 1) & 1, lim)) {
         set_flag_p(p.ctrl, COLI_FLAG_TIMEOUT);
         break;
       }
@@ -757,6 +777,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
       if (MODE == kModeGateUp) {
         const float gate = r_ok ? p.route_gate[it.p0 + r] : 0.0f;
         __half *dst = p.h16 + (int64_t)(it.p0 + r) * F + it.ni * (kBN / 2);
+        bool inf = false;
         for (int cc = 0; cc < kBN / 2; cc += 32) {
           uint32_t g[32], u[32];
           tmem_ld32(trow + cc, g);
@@ -770,6 +791,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
                 silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]) * gate;
             const __half2 hh = __floats2half2_rn(h0, h1);
             o[j] = *reinterpret_cast<const uint32_t *>(&hh);
+            inf |= half2_has_inf(o[j]);
           }
           if (r_ok) {
             uint4 *d4 = (uint4 *)(dst + cc);
@@ -778,6 +800,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
               d4[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
           }
         }
+        if (r_ok && inf) set_flag_p(p.ctrl, COLI_FLAG_RANGE);
       } else {
         float *dst = p.y + (int64_t)(it.p0 + r) * H + it.ni * kBN;
         for (int cc = 0; cc < kBN; cc += 32) {
@@ -797,7 +820,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
       mbar_arrive(&tm_empty[buf]);
     }
   }
-  // every MMA has been waited for by the epilogue (or abandoned on a timeout)
+  // every MMA has completed (the MMA thread's final commit)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -897,8 +920,9 @@ cudaError_t launch_prefill(const PrefillArgs &p, int x_dtype, int wr_dtype, cuda
   // activations -> fp16
   const int64_t nx = (int64_t)T * H;
   const int gx = (int)((nx / 8 + 255) / 256 < 4 * nsm ? (nx / 8 + 255) / 256 : 4 * nsm);
-  if (x_dtype == COLI_BF16) k_x16<__nv_bfloat16><<<gx, 256, 0, s>>>((const __nv_bfloat16 *)p.x, p.x16, nx);
-  else k_x16<float><<<gx, 256, 0, s>>>((const float *)p.x, p.x16, nx);
+  if (x_dtype == COLI_BF16)
+    k_x16<__nv_bfloat16><<<gx, 256, 0, s>>>((const __nv_bfloat16 *)p.x, p.x16, nx, p.ctrl);
+  else k_x16<float><<<gx, 256, 0, s>>>((const float *)p.x, p.x16, nx, p.ctrl);
   // router logits
   const dim3 gl((E + 63) / 64, (T + 63) / 64);
 #define COLI_LOGITS(XT, WT) \

@@ -110,3 +110,92 @@ def test_prefill_stack_two_layers():
     for l in range(2):
         assert rel_err(layer_out[l].cpu().numpy(), outs[l]).max() <= REL_TOL
     assert rel_err(xo.cpu().numpy(), xL).max() <= REL_TOL
+
+
+def _tiny_batched(seed=3):
+    H, F, E, S, k, T = 256, 128, 8, 1, 2, 64
+    shape = synth.MoEShape("pr", 1, H, F, E, S, k, T, "bf16", "f32")
+    layer = Layer(shape, 0, seed)
+    packed, scales, wr = layer.gpu()
+    x = tokens_without_ties(shape, layer.wr.double().numpy(), seed)
+    c = coli()
+    desc = c.MoEDesc(H, F, E, S, T, c.COLI_F32, c.COLI_BF16)
+    ws = c.new_workspace(desc, k)
+    return shape, layer, (packed, scales, wr), x, desc, ws
+
+
+def _check_status(ws):
+    """coli_moe_check's own status and flag word (clears the flags)."""
+    import ctypes
+    c = coli()
+    flags = ctypes.c_uint32(0)
+    st = c.lib.coli_moe_check(ctypes.c_void_p(ws.data_ptr()), 1, ctypes.byref(flags), None)
+    return st, flags.value
+
+
+def _assert_matches_oracle(shape, layer, x, out, counts):
+    op, os_, owr = layer.oracle()
+    ocounts = np.zeros(shape.experts, np.uint32)
+    ref, _, _, _ = orc.moe_forward(x.double().numpy(), owr, op, os_, shape.hidden, shape.ffn,
+                                   shape.experts, shape.shared, shape.top_k, ocounts)
+    assert np.array_equal(counts.cpu().numpy().astype(np.uint32), ocounts)
+    assert rel_err(out.cpu().numpy(), ref).max() <= REL_TOL
+
+
+def test_prefill_range_flag():
+    """Fail closed: an x value, or an h = silu(g) u gate value, that rounds to
+    +-inf in the batched path's fp16 operand copy sets COLI_FLAG_RANGE and
+    coli_moe_check returns COLI_ERANGE; in-range calls on the same workspace
+    stay clean and correct."""
+    c = coli()
+    shape, layer, (packed, scales, wr), x, desc, ws = _tiny_batched()
+    k = shape.top_k
+
+    def run(xx):
+        counts = torch.zeros(shape.experts, dtype=torch.int32, device="cuda")
+        out = c.coli_moe_forward(desc, k, xx.cuda(), wr, packed, scales, ws, route_counts=counts)
+        torch.cuda.synchronize()
+        return out, counts
+
+    out, counts = run(x)
+    assert _check_status(ws) == (c.COLI_OK, 0)
+    _assert_matches_oracle(shape, layer, x, out, counts)
+    # x itself above the fp16 range
+    xb = x.clone()
+    xb[3, 7] = 1.0e5
+    run(xb)
+    st, flags = _check_status(ws)
+    assert st == c.COLI_ERANGE and flags == c.COLI_FLAG_RANGE
+    # x inside the fp16 range (|x| < 2e4), but g and u near 1e3: h overflows
+    xs = x * 3000.0
+    assert xs.abs().max() < 65504
+    run(xs)
+    st, flags = _check_status(ws)
+    assert st == c.COLI_ERANGE and flags & c.COLI_FLAG_RANGE
+    out, counts = run(x)
+    assert _check_status(ws) == (c.COLI_OK, 0)
+    _assert_matches_oracle(shape, layer, x, out, counts)
+
+
+def test_prefill_wait_limit_runs_out_then_recovers():
+    """A workspace control word shortens the grouped GEMMs' pipeline waits to
+    one clock cycle: the waits give up, the call flags COLI_FLAG_TIMEOUT
+    (coli_moe_check returns COLI_ETIMEOUT), every MMA issued is drained before
+    the tensor memory is freed; with the word cleared the next call on the
+    same workspace is correct."""
+    c = coli()
+    shape, layer, (packed, scales, wr), x, desc, ws = _tiny_batched(4)
+    words = ws[:256].view(torch.int32)
+    WAIT_LIMIT = 5                                  # control word index (coli_internal.cuh)
+    words[WAIT_LIMIT] = 1
+    c.coli_moe_forward(desc, shape.top_k, x.cuda(), wr, packed, scales, ws)
+    torch.cuda.synchronize()
+    st, flags = _check_status(ws)
+    assert st == c.COLI_ETIMEOUT and flags & c.COLI_FLAG_TIMEOUT
+    words[WAIT_LIMIT] = 0
+    counts = torch.zeros(shape.experts, dtype=torch.int32, device="cuda")
+    out = c.coli_moe_forward(desc, shape.top_k, x.cuda(), wr, packed, scales, ws,
+                             route_counts=counts)
+    torch.cuda.synchronize()
+    assert _check_status(ws) == (c.COLI_OK, 0)
+    _assert_matches_oracle(shape, layer, x, out, counts)
