@@ -240,6 +240,11 @@ class DecodeWorkload:
         return (sh.tokens == 1 and sh.hidden % 1024 == 0 and sh.ffn % 1024 == 0
                 and per_sm <= 512 * 1024)
 
+    def gu_router(self):
+        """One token on the GEMV kernels: the first layer of each call forms
+        its router logits inside the gate/up kernel (no router launch)."""
+        return self.shape.tokens == 1 and not self.fused()
+
     def kernels_per_step(self):
         # per 16-token pass: chained, the first layer's router partials, then
         # the layer kernel(s) of every layer; else the router partials and the
@@ -249,7 +254,9 @@ class DecodeWorkload:
         # fused: one kernel; else gate/up and down (several tokens: gate/up,
         # the per-expert down GEMVs and the combine)
         per_layer = 1 if self.fused() else (2 if sh.tokens == 1 else 3)
-        return passes * ((1 + per_layer * sh.layers) if sh.chained else (1 + per_layer) * sh.layers)
+        route = 0 if self.gu_router() else 1
+        return passes * ((route + per_layer * sh.layers) if sh.chained
+                         else (route + per_layer) * sh.layers)
 
     def io_bytes_per_step(self):
         """Host <-> device bytes of one step's input and output (f32)."""
@@ -271,9 +278,12 @@ class DecodeWorkload:
         n_exp = uniq + S
         h_bytes = T * (k + S) * F * 4
         rb = sh.experts * sh.hidden * (2 if sh.router_dtype == "bf16" else 4)
+        n_route = len(steps) * (1 if sh.chained else sh.layers)
         if kernel == c.COLI_KERNEL_GATEUP:
+            # with the first layer's router inside: its router weights too
             per_exp = 2 * (F * H // 2 + 4 * F * H // 64)
-            return int((n_exp * per_exp).sum() + uniq.size * (T * H * 4 + h_bytes))
+            router = n_route * rb if self.gu_router() else 0
+            return int((n_exp * per_exp).sum() + uniq.size * (T * H * 4 + h_bytes) + router)
         if kernel == c.COLI_KERNEL_DOWN:
             per_exp = H * F // 2 + 4 * H * F // 64
             next_router = rb * (sh.layers - 1) * len(steps) if sh.chained else 0
@@ -283,7 +293,6 @@ class DecodeWorkload:
             per_exp = self.eb + 4 * self.es
             next_router = rb * (sh.layers - 1) * len(steps) if sh.chained else 0
             return int((n_exp * per_exp).sum() + uniq.size * 2 * T * H * 4 + next_router)
-        n_route = len(steps) * (1 if sh.chained else sh.layers)
         return int(n_route * (rb + T * H * 4))
 
     def algorithmic_bytes(self, steps):

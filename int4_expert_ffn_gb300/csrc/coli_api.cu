@@ -369,6 +369,10 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
   // with fixed-point logits every gate/up CTA (every fused-kernel CTA) routes
   // its own layer
   a.route_gu = fused || (a.fx && a.gu_route_fits);
+  // one token on the GEMV kernels: the first layer's gate/up CTAs form its
+  // logits themselves (no router-partials launch before them)
+  const bool gu_router = !fused && tn == 1 && a.route_gu && a.gu_rt_off >= 0;
+  a.x_bf16 = x_dtype == COLI_BF16;
   const float *bias0 = d->router_fn == COLI_ROUTER_SIGMOID_BIAS ? d->router_bias : nullptr;
   uint8_t *ws = (uint8_t *)workspace;
   for (int l = 0; l < n_layers && e == cudaSuccess; ++l) {
@@ -396,14 +400,17 @@ static int moe_pass(const coli_moe_desc *d, int k, int n_layers, int tn, const v
     // and k_gateup, layer l + 1 for the last CTA of k_down (without fixed point)
     a.router_bias = bias0 ? bias0 + (size_t)l * E : nullptr;
     if (l == 0) {
-      // router partials of layer 0
+      // router partials of layer 0 (a launch of their own, or in its gate/up CTAs)
       a.wr = router_w;
-      e = profiled(COLI_KERNEL_ROUTE, stream, [&] {
-        return launch_route_partials(a, x_dtype == COLI_BF16, wr_bf16, stream, true);
-      });
-      if (e != cudaSuccess) break;
+      if (!gu_router) {
+        e = profiled(COLI_KERNEL_ROUTE, stream, [&] {
+          return launch_route_partials(a, x_dtype == COLI_BF16, wr_bf16, stream, true);
+        });
+        if (e != cudaSuccess) break;
+      }
       if (a.route_gu) fx_buffer(a, ws, L, 1, &a.fx_acc, &a.fx_flag);
     }
+    a.gu_router = (l == 0 && gu_router) ? 1 : 0;
     if (fused) {
       // routing, gate/up, down, combine and the next layer's router partials
       const bool next = l + 1 < n_layers;

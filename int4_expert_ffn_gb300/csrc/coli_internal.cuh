@@ -47,8 +47,9 @@ enum CtrlWord : int {
   kCtrlBarArrive = 3,  // grid barrier of the one-token layer kernel: arrivals of this use
   kCtrlBarGen = 4,     //   and its generation (left as they are between calls)
   kCtrlWaitLimit = 5,  // 0: default bounded waits; else the spin limit in clock cycles of
-                       //   the one-token kernel's grid barrier and the grouped GEMMs'
-                       //   pipeline waits (a test hook that makes the waits run out)
+                       //   the grid barriers (one-token layer kernel, first-layer router
+                       //   in k_gateup) and of the grouped GEMMs' pipeline waits (a test
+                       //   hook that makes the waits run out)
   kCtrlWords = 64,     // 256 bytes
 };
 static_assert(kCtrlWords * 4 <= kFxOffset, "control words precede the fixed-point region");
@@ -74,6 +75,7 @@ struct WsLayout {
 WsLayout ws_layout(int T, int H, int F, int E, int S, int k);
 
 constexpr int kDec2MaxThreads = 512;
+constexpr int kDnMaxThreads = 640;      // k_down: up to 20 warps
 
 // Shared-memory plan of k_gateup (byte offsets into dynamic smem).
 struct GuSmem {
@@ -129,6 +131,12 @@ struct Dec2Args {
   const float *router_bias; // its selection bias [E] (sigmoid router) or null
   int route_gu;             // every gate/up CTA routes its layer from fx_rd_*
   int gu_route_fits;        // the routing scratch fits in k_gateup's pipeline ring
+  int gu_router;            // one token, first layer of the call: the k_gateup CTAs form
+                            // the logits themselves (each the whole logits of its own
+                            // experts, as floats over fx_rd_acc, then a grid barrier)
+                            // instead of a k_route launch
+  int gu_rt_off;            // byte offset of that router scratch in k_gateup's ring
+  int x_bf16;               // x (the call's input) is bf16, else f32
   const long long *fx_rd_acc;   // k_gateup: this layer's fixed-point logits
   const uint32_t *fx_rd_flag;
   long long *fx_clr_acc;    // k_down: buffer its gate/up read, cleared here

@@ -67,37 +67,6 @@ constexpr double kL1MaxBytesPerSm = 512.0 * 1024.0;
 constexpr int kL1MaxStages = 16;
 
 
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Grid barrier across the kernel's CTAs, run by one thread per CTA after the
-// CTA's own writes are ordered before it (bar.sync).  Sense by generation:
-// the last CTA to arrive resets the arrival count and advances the
-// generation; the others spin (bounded) until the generation moves.  Both
-// words stay consistent between calls.  Returns false if the wait gave up.
-__device__ bool grid_sync(uint32_t *ctrl, unsigned G) {
-  const uint32_t lim = ld_acquire(ctrl + kCtrlWaitLimit);
-  const long long limit = lim ? (long long)lim : kWaitCycles;
-  const uint32_t gen = ld_acquire(ctrl + kCtrlBarGen);
-  __threadfence();
-  const uint32_t old = atomicAdd(ctrl + kCtrlBarArrive, 1u);
-  if (old == G - 1) {
-    atomicExch(ctrl + kCtrlBarArrive, 0u);
-    __threadfence();
-    atomicAdd(ctrl + kCtrlBarGen, 1u);
-    return true;
-  }
-  const long long t0 = clock64();
-  while (ld_acquire(ctrl + kCtrlBarGen) == gen) {
-    if (clock64() - t0 > limit) return false;
-    __nanosleep(64);
-  }
-  __threadfence();
-  return true;
-}
 
 // Where the CTA's stages come from.  Gate/up work is cut into h blocks: 32
 // consecutive rows (gate and up) of one used expert, the rows whose h values

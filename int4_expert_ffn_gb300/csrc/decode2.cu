@@ -240,7 +240,7 @@ __host__ __device__ inline RouteSmem route_smem(int T, int E, int k, int S, int 
   R.idx = a16(o); o = R.idx + (size_t)T * k * 4;
   R.gates = o; o += (size_t)T * k * 4;
   R.vals = o; o += (size_t)T * k * 4;
-  R.scratch = a16(o); o = R.scratch + (size_t)kDec2MaxThreads * 4;
+  R.scratch = a16(o); o = R.scratch + (size_t)kDnMaxThreads * 4;   // one float per thread, any kernel
   R.act = o; o += (size_t)(2 + 2 * (E + S)) * 4;
   R.routes = o; o += (size_t)T * (k + S) * 4;
   R.slot_gate = o; o += (size_t)T * (k + S) * 4;
@@ -446,11 +446,30 @@ __device__ void gu_lists(const Dec2Args &a, const LayerPtrs &lp, uint8_t *scratc
   float *s_logits = (float *)(scratch + R.logits);
   int *s_idx = (int *)(scratch + R.idx);
   float *s_gates = (float *)(scratch + R.gates);
+  bool late = false;
   for (int i = threadIdx.x; i < TE; i += blockDim.x) {
-    const long long v = __ldcg(a.fx_rd_acc + i);
-    const uint32_t f = __ldcg(a.fx_rd_flag + i);
-    s_logits[i] = f ? __int_as_float(0x7FC00000) : fx_to_float(v);
+    if (a.gu_router) {
+      // published whole by the owning CTAs (gu_router_logits): wait for the
+      // word to become nonzero (bounded), then undo the sign flip
+      const uint32_t *wp = (const uint32_t *)a.fx_rd_acc + i;
+      uint32_t w = ld_acquire(wp);
+      if (w == 0u) {
+        const uint32_t lw = ld_acquire(a.ctrl + kCtrlWaitLimit);
+        const long long limit = lw ? (long long)lw : kWaitCycles;
+        const long long t0 = clock64();
+        while ((w = ld_acquire(wp)) == 0u) {
+          if (clock64() - t0 > limit) { late = true; break; }
+          __nanosleep(32);
+        }
+      }
+      s_logits[i] = __uint_as_float(w ^ 0x80000000u);
+    } else {
+      const long long v = __ldcg(a.fx_rd_acc + i);
+      const uint32_t f = __ldcg(a.fx_rd_flag + i);
+      s_logits[i] = f ? __int_as_float(0x7FC00000) : fx_to_float(v);
+    }
   }
+  if (late) set_flag(a.ctrl, COLI_FLAG_TIMEOUT);
   __syncthreads();
   COLI_TRACE_POINT(a.layer, kTpRtLogits);
   const bool sig = a.router_fn == COLI_ROUTER_SIGMOID_BIAS;
@@ -490,6 +509,109 @@ __device__ __forceinline__ void gu_bias_prefetch(const Dec2Args &a, uint8_t *scr
   for (int i = threadIdx.x; i < a.E; i += blockDim.x) s_bias[i] = __ldg(a.router_bias + i);
 }
 
+// First layer of a one-token call without a k_route launch.  CTA c of G owns
+// the experts e = c, c + G, ... and forms their logits whole,
+// l_e = sum_h Wr[e][h] x[h] in f32 (each thread its columns h = tid + i *
+// blockDim in order, four experts' sums side by side, then a fixed reduction
+// tree).  It publishes each as one 32-bit word over the layer's fixed-point
+// buffer, which holds zeros at the start of the call (its down kernel clears
+// it): the bits of l + 0 (so -0 becomes +0; a NaN becomes the quiet NaN) with
+// the sign bit flipped, a word that is never zero.  Every CTA then waits for
+// all E words to be nonzero (gu_lists), so no grid barrier is needed; the
+// gate/up warps of this layer read x directly (no replicas).
+// The owned router rows go to shared memory before the dependency wait (the
+// weights do not depend on the previous kernel); x is read after it.
+// Shared memory at `buf`: owned rows [ceil(E/G)][H] (router dtype), x f32
+// [H], 32 x 4 floats of reduction scratch.
+__device__ __forceinline__ uint32_t logit_word(float v) {
+  v = v + 0.0f;
+  return (v != v ? 0x7FC00000u : __float_as_uint(v)) ^ 0x80000000u;
+}
+
+__device__ __forceinline__ void gu_router_prefetch(const Dec2Args &a, uint8_t *buf) {
+  const int E = a.E, G = gridDim.x, c = blockIdx.x;
+  const int row16 = a.H * (a.wr_bf16 ? 2 : 4) / 16;       // H is a multiple of 64
+  const uint8_t *wr = (const uint8_t *)a.wr;
+  int n = 0;
+  for (int e = c; e < E; e += G, ++n)
+    for (int i = threadIdx.x; i < row16; i += blockDim.x)
+      cp_async16(buf + ((size_t)n * row16 + i) * 16, wr + ((size_t)e * row16 + i) * 16);
+  cp_async_commit();
+}
+
+template <typename WT>
+__device__ __forceinline__ void router_dots4(const WT *w, int H, const float *s_x, int n,
+                                             float (&sum)[4]) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  for (int i = tid; i < H; i += nthr) {
+    const float xv = s_x[i];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (q < n) sum[q] = fmaf(to_f32(w[(size_t)q * H + i]), xv, sum[q]);
+  }
+}
+
+__device__ void gu_router_logits(const Dec2Args &a, uint8_t *buf) {
+  const int E = a.E, H = a.H, G = gridDim.x, c = blockIdx.x;
+  const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5;
+  const int nw = nthr >> 5;
+  const int wsz = a.wr_bf16 ? 2 : 4;
+  const int n_max = (E + G - 1) / G;
+  const int n_own = c < E ? (E - c + G - 1) / G : 0;
+  float *s_x = (float *)(buf + al16c((size_t)n_max * H * wsz));
+  float *s_red = s_x + H;                        // [32][4]
+  // x in groups of four elements, up to four 8- or 16-byte loads per thread in
+  // flight before any is used (one memory round trip for H <= 16 blockDim)
+  const int n4 = H / 4;
+  for (int i0 = tid; i0 < n4; i0 += 4 * nthr) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * nthr;
+      if (i >= n4) break;
+      if (a.x_bf16) {
+        const uint2 q = __ldcg((const uint2 *)a.x + i);
+        v[u] = make_float4(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xFFFF0000u),
+                           __uint_as_float(q.y << 16), __uint_as_float(q.y & 0xFFFF0000u));
+      } else {
+        v[u] = __ldcg((const float4 *)a.x + i);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * nthr;
+      if (i >= n4) break;
+      ((float4 *)s_x)[i] = v[u];
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  COLI_TRACE_POINT(a.layer, kTpGuSplit);
+  uint32_t *words = (uint32_t *)const_cast<long long *>(a.fx_rd_acc);
+  for (int n0 = 0; n0 < n_own; n0 += 4) {
+    const int n = n_own - n0 < 4 ? n_own - n0 : 4;
+    float sum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (wsz == 2) router_dots4((const __nv_bfloat16 *)buf + (size_t)n0 * H, H, s_x, n, sum);
+    else router_dots4((const float *)buf + (size_t)n0 * H, H, s_x, n, sum);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sum[q] += __shfl_xor_sync(0xFFFFFFFFu, sum[q], off);
+    }
+    if (lane == 0)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) s_red[warp * 4 + q] = sum[q];
+    __syncthreads();
+    if (tid < n) {
+      float t = 0.0f;
+      for (int w = 0; w < nw; ++w) t += s_red[w * 4 + tid];
+      words[c + (n0 + tid) * G] = logit_word(t);
+    }
+    __syncthreads();
+  }
+  COLI_TRACE_POINT(a.layer, kTpGuNeed);
+}
+
 // The down kernel of a layer clears the fixed-point buffer that the layer's
 // gate/up CTAs routed from (they have all finished): CTA c its share.
 __device__ __forceinline__ void clear_fx(const Dec2Args &a) {
@@ -521,10 +643,12 @@ __global__ void __launch_bounds__(kGuOneMaxThreads) k_gateup(Dec2Args a) {
   float *s_slot_gate = (float *)(smem + L.slot_gate);
   float *red = (float *)(smem + L.red);
   gu_bias_prefetch(a, smem + L.ring);
+  if (a.gu_router) gu_router_prefetch(a, smem + L.ring + a.gu_rt_off);
   grid_dependents_launch();
   grid_dependency_wait();
   COLI_TRACE_POINT(a.layer, kTpGuDepWait);
   const LayerPtrs lp = layer_ptrs(a);
+  if (a.gu_router) gu_router_logits(a, smem + L.ring + a.gu_rt_off);
   gu_lists(a, lp, smem + L.ring, s_act, s_routes, s_slot_gate);   // ends with __syncthreads
   COLI_TRACE_POINT(a.layer, kTpGuLists);
   const int H = a.H, F = a.F;
@@ -536,6 +660,8 @@ __global__ void __launch_bounds__(kGuOneMaxThreads) k_gateup(Dec2Args a) {
   const int U = n_active * (F / 4);
   const int row0 = 4 * part_lo(c, U, G), nrows = 4 * part_lo(c + 1, U, G) - row0;
   const float *xr = lp.xrep + (size_t)(c % a.n_rep) * a.x_stride;
+  // with the router formed here (first layer), x comes from the caller's input
+  const bool x_direct = a.gu_router != 0;
   const int ncg = a.gu_ncg, S = a.gu_slots;
   const int dg = NW / ncg, dcg = NW - dg * ncg;
   const bool vec_scales = kFast || (H % 256) == 0;
@@ -582,7 +708,9 @@ __global__ void __launch_bounds__(kGuOneMaxThreads) k_gateup(Dec2Args a) {
       if (act) {
         if (cc.cg != pl_cg) {
           float xv[32];
-          load32<float>(xr + col, xv);
+          if (!x_direct) load32<float>(xr + col, xv);
+          else if (a.x_bf16) load32<__nv_bfloat16>((const __nv_bfloat16 *)a.x + col, xv);
+          else load32<float>((const float *)a.x + col, xv);
           quantize32(xv, pl);
           pl_cg = cc.cg;
         }
@@ -727,6 +855,8 @@ __global__ void __launch_bounds__(kGuMultiMaxThreads) k_gateup_multi(Dec2Args a)
   cost_split(s_act_off, n_active, gpe, c, G, (int *)(smem + L.tok) + 2 * T + 1, &u0, &u1);
   COLI_TRACE_POINT(a.layer, kTpGuSplit);
   const float *xr = lp.xrep + (size_t)(c % a.n_rep) * a.x_stride;
+  // with the router formed here (first layer), x comes from the caller's input
+  const bool x_direct = a.gu_router != 0;
   const int ncg = a.gu_ncg, nbx = H / 32;
   const bool vec_scales = kFast || (H % 256) == 0;
   const bool xpl = kXpl;   // a.gu_xpl
@@ -1029,7 +1159,7 @@ __device__ void dn_phase(const Dec2Args &a, const LayerPtrs &lp, const int *s_ac
 
 
 template <typename WT, bool kOne, bool kFast>
-__global__ void __launch_bounds__(kDec2MaxThreads) k_down(Dec2Args a) {
+__global__ void __launch_bounds__(kOne ? kDnMaxThreads : kDec2MaxThreads) k_down(Dec2Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const DnSmem &L = a.dn;
   WT *s_wr = (WT *)(smem + L.wr);
@@ -1316,6 +1446,16 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
   // routing scratch: the T = 1 kernel's ring, the several-token kernel's plane area
   a.gu_route_fits = gu_route_smem(T, E, k).total <=
                     (T == 1 ? (size_t)a.gu_nw * a.gu_slots * a.gu_slot_bytes : g.total - g.xpl);
+  // one token: room in the ring, after the routing scratch, for a CTA's owned
+  // router rows, x and the reduction scratch (the first layer's logits formed
+  // in k_gateup, gu_router_logits); -1: none
+  a.gu_rt_off = -1;
+  if (T == 1) {
+    const int n_max = (E + G - 1) / G;
+    const size_t off = al16(gu_route_smem(T, E, k).total);
+    const size_t need = off + al16((size_t)n_max * H * (a.wr_bf16 ? 2 : 4)) + (size_t)H * 4 + 512;
+    if (need <= (size_t)a.gu_nw * a.gu_slots * a.gu_slot_bytes) a.gu_rt_off = (int)off;
+  }
   // ---- down: dn_nw warps with dn_slots_pipe-deep cp.async pipelines
   a.dn_ncg = (F + kChunkCols - 1) / kChunkCols;
   a.dn_slot_bytes = slot_bytes(F);
@@ -1332,19 +1472,28 @@ cudaError_t plan_decode(Dec2Args &a, int n_part) {
   // one token: every used expert's partial sums [expert][row][chunk] at once
   const int n_exp = (E < k ? E : k) + S;
   const size_t red_bytes = (size_t)n_exp * max_nr * a.dn_ncg * 4;
-  // more warps before deeper pipelines: each warp works its tasks in order, so
-  // the down phase's latency follows the tasks per warp
-  static const int kDnNw[] = {16, 12, 8, 12, 8, 8, 4};
-  static const int kDnSl[] = {2, 3, 4, 2, 3, 2, 2};
-  bool dn_ok = false;
-  for (int c = 0; c < 7 && !dn_ok; ++c) {
+  // Each warp works its tasks (an expert's 8-row group x 1024-column chunk) in
+  // order, one in flight while it computes another, so the down phase lasts
+  // about as long as the largest number of tasks any warp has: the warp count
+  // that fits makes that number smallest, and the fewest warps among equals
+  // (measured on the GLM-like layer: 18 warps, 6 tasks each, 4 % faster than
+  // 16 warps with up to 7, and faster than 20 with up to 6).
+  static const int kDnNw[] = {4, 8, 8, 8, 12, 12, 16, 18, 20};
+  static const int kDnSl[] = {2, 2, 3, 4, 2, 3, 2, 2, 2};
+  const int n_dn_tasks = n_exp * ((max_nr + 7) / 8) * a.dn_ncg;
+  int dn_pick = -1, dn_best = 0;
+  for (int c = 0; c < 9; ++c) {
     const size_t ring = (size_t)kDnNw[c] * kDnSl[c] * a.dn_slot_bytes;
     if (al128(o) + ring + 16 + red_bytes > budget) continue;
-    a.dn_nw = kDnNw[c];
-    a.dn_slots_pipe = kDnSl[c];
-    dn_ok = true;
+    const int per_warp = (n_dn_tasks + kDnNw[c] - 1) / kDnNw[c];
+    if (dn_pick < 0 || per_warp < dn_best) {
+      dn_pick = c;
+      dn_best = per_warp;
+    }
   }
-  if (!dn_ok) return cudaErrorInvalidValue;
+  if (dn_pick < 0) return cudaErrorInvalidValue;
+  a.dn_nw = kDnNw[dn_pick];
+  a.dn_slots_pipe = kDnSl[dn_pick];
   d.ring = al128(o); o = d.ring + (size_t)a.dn_nw * a.dn_slots_pipe * a.dn_slot_bytes;
   d.red = al16(o); o = d.red + red_bytes;
   d.total = al16(o);

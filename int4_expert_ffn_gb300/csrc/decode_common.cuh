@@ -91,6 +91,19 @@ __device__ __forceinline__ void load32<float>(const float *p, float (&v)[32]) {
     v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
   }
 }
+template <>
+__device__ __forceinline__ void load32<__nv_bfloat16>(const __nv_bfloat16 *p, float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 q = __ldcg((const uint4 *)p + i);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+      v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+  }
+}
 
 // Reduce 8 values across the warp in 9 shuffles; lane l ends with the total of
 // value (l >> 2).
@@ -301,14 +314,51 @@ __device__ __forceinline__ float fx_to_float(long long v) {
   return __ll2float_rn(v) * 0x1p-32f;
 }
 
-__device__ __forceinline__ void fx_add(const Dec2Args &a, int o, float p) {
+__host__ __device__ constexpr size_t al16c(size_t v) { return (v + 15) & ~(size_t)15; }
+
+__device__ __forceinline__ void fx_add_to(long long *acc, uint32_t *flag, int o, float p) {
   if (!(fabsf(p) < 1.0e7f)) {
-    atomicOr(a.fx_flag + o, 1u);
+    atomicOr(flag + o, 1u);
     return;
   }
-  atomicAdd((unsigned long long *)(a.fx_acc + o),
-            (unsigned long long)__float2ll_rn(p * 4294967296.0f));
+  atomicAdd((unsigned long long *)(acc + o), (unsigned long long)__float2ll_rn(p * 4294967296.0f));
 }
+__device__ __forceinline__ void fx_add(const Dec2Args &a, int o, float p) {
+  fx_add_to(a.fx_acc, a.fx_flag, o, p);
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid barrier across the kernel's CTAs, run by one thread per CTA after the
+// CTA's own writes are ordered before it (bar.sync).  Sense by generation:
+// the last CTA to arrive resets the arrival count and advances the
+// generation; the others spin (bounded) until the generation moves.  Both
+// words stay consistent between calls.  Returns false if the wait gave up.
+__device__ __forceinline__ bool grid_sync(uint32_t *ctrl, unsigned G) {
+  const uint32_t lim = ld_acquire(ctrl + kCtrlWaitLimit);
+  const long long limit = lim ? (long long)lim : kWaitCycles;
+  const uint32_t gen = ld_acquire(ctrl + kCtrlBarGen);
+  __threadfence();
+  const uint32_t old = atomicAdd(ctrl + kCtrlBarArrive, 1u);
+  if (old == G - 1) {
+    atomicExch(ctrl + kCtrlBarArrive, 0u);
+    __threadfence();
+    atomicAdd(ctrl + kCtrlBarGen, 1u);
+    return true;
+  }
+  const long long t0 = clock64();
+  while (ld_acquire(ctrl + kCtrlBarGen) == gen) {
+    if (clock64() - t0 > limit) return false;
+    __nanosleep(64);
+  }
+  __threadfence();
+  return true;
+}
+
 
 
 // Shared-memory scratch of gu_route (byte offsets from its base).

@@ -10,13 +10,15 @@
 
 namespace coli {
 
-constexpr int kTraceLayers = 64, kTracePoints = 24, kTraceCtas = 160;
+constexpr int kTraceLayers = 64, kTracePoints = 25, kTraceCtas = 160;
 
 #ifdef COLI_TRACE
 // Defined here; only the decode translation unit includes this header.
 static __device__ unsigned long long g_trace[kTraceLayers][kTracePoints][kTraceCtas];
 __device__ __forceinline__ void trace_point(int layer, int pt) {
-  if (threadIdx.x != 0 || layer < 0 || layer >= kTraceLayers || blockIdx.x >= kTraceCtas) return;
+  if (threadIdx.x != 0 || layer < 0 || layer >= kTraceLayers || pt < 0 || pt >= kTracePoints ||
+      blockIdx.x >= kTraceCtas)
+    return;
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   g_trace[layer][pt][blockIdx.x] = t;
@@ -32,7 +34,7 @@ enum TracePoint : int {
   kTpDnEntry, kTpDnDepWait, kTpDnLists, kTpDnPlanes, kTpDnCompute, kTpDnCombine,
   kTpDnPartials, kTpRouteStart, kTpEnd,
   kTpRtLogits, kTpRtTopk, kTpRtPublish, kTpRtUnion, kTpDnPlaneStart, kTpDnPlaneBuilt,
-  kTpGuSplit, kTpGuNeed,
+  kTpGuSplit, kTpGuNeed, kTpGuRouter,
 };
 
 }  // namespace coli
