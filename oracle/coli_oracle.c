@@ -449,23 +449,27 @@ void orc_dequant_mxfp4(const uint8_t *packed, const uint8_t *scales, int64_t row
 
 /* ---------------------------------------------------------------------- */
 /* The layer over a chosen container: fmt 4 = int4-grouped (the functions
- * above), 7 = MXFP4, 8 = fp8-e4m3-b128 (below).  Expert record: gate | up | down, each in the format;
- * `scales` points to f32 scales (fmt 4, 8) or E8M0 bytes (fmt 7), expert
+ * above), 7 = MXFP4, 2 = int4-row and 8 = fp8-e4m3-b128 (below).  Expert record: gate | up | down, each in the format;
+ * `scales` points to f32 scales (fmt 2, 4, 8) or E8M0 bytes (fmt 7), expert
  * after expert in the same order. */
 
 int64_t orc_fp8_row_bytes(int64_t cols);
 int64_t orc_fp8_scales_per_row(int64_t cols);
 void orc_matvec_fp8b128(const uint8_t *packed, const float *scales, int64_t rows, int64_t cols,
                         const double *x, double *y);
+void orc_matvec_i4row(const uint8_t *packed, const float *scales, int64_t rows, int64_t cols,
+                      const double *x, double *y);
 
 int64_t orc_fmt_row_bytes(int fmt, int64_t cols)
 {
+    if (fmt == 2) return orc_packed_row_bytes(cols);
     if (fmt == 8) return orc_fp8_row_bytes(cols);
     return fmt == 7 ? orc_mx_row_bytes(cols) : orc_packed_row_bytes(cols);
 }
 /* Bytes of one row's scales. */
 int64_t orc_fmt_scale_bytes(int fmt, int64_t cols)
 {
+    if (fmt == 2) return 4;
     if (fmt == 8) return 4 * orc_fp8_scales_per_row(cols);
     return fmt == 7 ? orc_mx_scales_per_row(cols) : 4 * orc_scales_per_row(cols);
 }
@@ -483,6 +487,10 @@ static void orc_matvec_fmt(int fmt, const uint8_t *packed, const uint8_t *scales
 {
     if (fmt == 8) {
         orc_matvec_fp8b128(packed, (const float *)scales, rows, cols, x, y);
+        return;
+    }
+    if (fmt == 2) {
+        orc_matvec_i4row(packed, (const float *)scales, rows, cols, x, y);
         return;
     }
     if (fmt != 7) {
@@ -641,6 +649,69 @@ void orc_matvec_fp8b128(const uint8_t *packed, const float *scales, int64_t rows
     for (int64_t r = 0; r < rows; ++r) {
         double acc = 0.0;
         for (int64_t c = 0; c < cols; ++c) acc += orc_fp8_elem(packed, scales, cols, nb, r, c) * x[c];
+        y[r] = acc;
+    }
+}
+
+/* ---------------------------------------------------------------------- */
+/* int4-row ([P2] §权重转换, "2 int4-row" of the format registry).  The page
+ * gives the name only; the reading (design notes): the int4-grouped rule with
+ * one group per row -- per row s = max|w| / 7 (f32 division), q =
+ * clip(rint(w / s), -8, 7) (f32 division, ties to even), stored as u = q + 8,
+ * two per byte, even column in the low nibble; scales f32 [rows].  An all-zero
+ * row stores s = 0 and u = 8; a NaN weight is ignored by the max and stored as
+ * u = 8; with an odd column count the last high nibble is 0. */
+
+void orc_quant_i4row(const float *w, int64_t rows, int64_t cols, uint8_t *packed, float *scales)
+{
+    const int64_t rb = orc_packed_row_bytes(cols);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *wr = w + r * cols;
+        uint8_t *pr = packed + r * rb;
+        memset(pr, 0, (size_t)rb);
+        float m = 0.0f;
+        for (int64_t c = 0; c < cols; ++c) {
+            const float a = fabsf(wr[c]);
+            if (a > m) m = a;
+        }
+        const float s = m / 7.0f;
+        scales[r] = s;
+        for (int64_t c = 0; c < cols; ++c) {
+            int q = 0;
+            if (s != 0.0f) {
+                const float v = rintf(wr[c] / s);
+                q = (v != v) ? 0 : (v < -8.0f ? -8 : (v > 7.0f ? 7 : (int)v));
+            }
+            const uint8_t u = (uint8_t)(q + 8);
+            pr[c >> 1] |= (c & 1) ? (uint8_t)(u << 4) : u;
+        }
+    }
+}
+
+static double orc_i4row_elem(const uint8_t *packed, const float *scales, int64_t rb, int64_t r,
+                             int64_t c)
+{
+    const uint8_t b = packed[r * rb + (c >> 1)];
+    const int u = (c & 1) ? (b >> 4) : (b & 0x0F);
+    return (double)scales[r] * (double)(u - 8);
+}
+
+void orc_dequant_i4row(const uint8_t *packed, const float *scales, int64_t rows, int64_t cols,
+                       double *w)
+{
+    const int64_t rb = orc_packed_row_bytes(cols);
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) w[r * cols + c] = orc_i4row_elem(packed, scales, rb, r, c);
+}
+
+void orc_matvec_i4row(const uint8_t *packed, const float *scales, int64_t rows, int64_t cols,
+                      const double *x, double *y)
+{
+    const int64_t rb = orc_packed_row_bytes(cols);
+    for (int64_t r = 0; r < rows; ++r) {
+        double acc = 0.0;
+        for (int64_t c = 0; c < cols; ++c) acc += orc_i4row_elem(packed, scales, rb, r, c) * x[c];
         y[r] = acc;
     }
 }

@@ -15,10 +15,11 @@ __all__ = [
     "topk", "topk_sigmoid", "expert", "moe_forward", "moe_stack_forward", "lib",
     "set_threads", "threads", "quant_mxfp4", "dequant_mxfp4", "e2m1_value", "fmt_expert_bytes",
     "fmt_expert_scale_bytes", "moe_forward_fmt", "FMT_I4G", "FMT_MXFP4", "FMT_FP8",
-    "quant_fp8b128", "dequant_fp8b128", "e4m3_value",
+    "quant_fp8b128", "dequant_fp8b128", "e4m3_value", "FMT_I4ROW", "quant_i4row",
+    "dequant_i4row",
 ]
 
-FMT_I4G, FMT_MXFP4, FMT_FP8 = 4, 7, 8
+FMT_I4ROW, FMT_I4G, FMT_MXFP4, FMT_FP8 = 2, 4, 7, 8
 
 GROUP = 64
 _libs = {}
@@ -97,6 +98,10 @@ def lib():
         L.orc_dequant_fp8b128.restype = None
         L.orc_e4m3_value.argtypes = [C.c_int]
         L.orc_e4m3_value.restype = C.c_double
+        L.orc_quant_i4row.argtypes = [f32p, i64, i64, u8, f32p]
+        L.orc_quant_i4row.restype = None
+        L.orc_dequant_i4row.argtypes = [u8, f32p, i64, i64, f64p]
+        L.orc_dequant_i4row.restype = None
         _libs[key] = L
     return _libs[key]
 
@@ -335,3 +340,23 @@ def dequant_fp8b128(packed, scales):
 
 def e4m3_value(code):
     return float(lib().orc_e4m3_value(int(code)))
+
+
+def quant_i4row(w):
+    """w: [rows, cols] float32 -> (packed u8 [rows, ceil(cols/2)], f32 scales [rows, 1])."""
+    w = _c(w, np.float32)
+    rows, cols = w.shape
+    packed = np.zeros((rows, (cols + 1) // 2), np.uint8)
+    scales = np.zeros((rows, 1), np.float32)
+    lib().orc_quant_i4row(_p(w, C.c_float), rows, cols, _p(packed, C.c_uint8),
+                          _p(scales, C.c_float))
+    return packed, scales
+
+
+def dequant_i4row(packed, scales, cols):
+    packed, scales = _c(packed, np.uint8), _c(scales, np.float32)
+    rows = packed.shape[0]
+    w = np.zeros((rows, cols), np.float64)
+    lib().orc_dequant_i4row(_p(packed, C.c_uint8), _p(scales, C.c_float), rows, cols,
+                            _p(w, C.c_double))
+    return w
