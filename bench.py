@@ -318,10 +318,12 @@ class PrefillWorkload:
         self.coli = c = pkg.binding
         self.shape = shape
         H, F, E, S, T = shape.hidden, shape.ffn, shape.experts, shape.shared, shape.tokens
-        self.fmt = {"i4g": c.COLI_FMT_I4G, "mxfp4": c.COLI_FMT_MXFP4, "fp8": c.COLI_FMT_FP8}[fmt]
+        self.fmt = {"i4g": c.COLI_FMT_I4G, "mxfp4": c.COLI_FMT_MXFP4, "fp8": c.COLI_FMT_FP8,
+                    "i4row": c.COLI_FMT_I4ROW}[fmt]
         quant, sdt = {"i4g": (c.coli_quant_i4g, torch.float32),
                       "mxfp4": (c.coli_quant_mxfp4, torch.uint8),
-                      "fp8": (c.coli_quant_fp8b128, torch.float32)}[fmt]
+                      "fp8": (c.coli_quant_fp8b128, torch.float32),
+                      "i4row": (c.coli_quant_i4row, torch.float32)}[fmt]
         esz = torch.tensor([], dtype=sdt).element_size()
         self.eb = c.coli_fmt_expert_bytes(self.fmt, H, F)
         self.es = c.coli_fmt_expert_scale_bytes(self.fmt, H, F) // esz
@@ -727,9 +729,9 @@ def main():
     ap.add_argument("--experts", type=int, default=None,
                     help="quant workload: experts converted per step (default 256; smaller for "
                          "profiling captures)")
-    ap.add_argument("--weight-fmt", default="i4g", choices=["i4g", "mxfp4", "fp8"],
+    ap.add_argument("--weight-fmt", default="i4g", choices=["i4g", "mxfp4", "fp8", "i4row"],
                     help="glm_prefill: the expert weight container (int4-grouped g64, MXFP4, "
-                         "fp8-e4m3-b128)")
+                         "fp8-e4m3-b128, int4-row)")
     ap.add_argument("--router", default="softmax", choices=["softmax", "sigmoid"],
                     help="decode workloads: softmax routing, or the GLM router (sigmoid "
                          "scores with a per-layer selection bias)")
@@ -1067,7 +1069,8 @@ def emit_prefill(args, shape, dev, world, rank, config):
     kd = kern[dom]
     fmt_name = {"i4g": "int4-grouped g64 f32 scales",
                 "mxfp4": "MXFP4 (E2M1 codes, E8M0 scale per 32)",
-                "fp8": "fp8-e4m3-b128 (E4M3 codes, f32 scale per 128)"}[args.weight_fmt]
+                "fp8": "fp8-e4m3-b128 (E4M3 codes, f32 scale per 128)",
+                "i4row": "int4-row (nibbles, one f32 scale per row)"}[args.weight_fmt]
     config = dict(config, l2="inputs larger than L2: %.2f GB of experts resident"
                   % ((wl.packed.nbytes + wl.scales.nbytes) / 1e9),
                   weight_fmt=args.weight_fmt,

@@ -96,7 +96,12 @@ typedef struct {
 
 /*
  * Expert weight containers (the engine's format registry, [P2] §权重转换:
- * "4 int4-grouped", "7 MXFP4", "8 fp8-e4m3-b128"; [P1] §十 "从 int4 到 MXFP4").
+ * "2 int4-row", "4 int4-grouped", "7 MXFP4", "8 fp8-e4m3-b128"; [P1] §十 "从 int4 到
+ * MXFP4").
+ *   COLI_FMT_I4ROW  int4-row: the int4-grouped rule with one group per row --
+ *                   nibbles as above, one f32 scale per row:
+ *                     packed uint8 [O][ceil(I/2)], scales f32 [O]
+ *                   and W[o][i] = s[o] * (u - 8).  Runs like MXFP4 (below).
  *   COLI_FMT_I4G    int4-grouped, the format above: nibbles + f32 scale per 64
  *   COLI_FMT_MXFP4  OCP Microscaling MXFP4: blocks of 32 columns share one
  *                   E8M0 scale byte e (X = 2^(e - 127)); each element is an
@@ -122,7 +127,9 @@ typedef struct {
  *                   the fp16 normal range (max|w| between about 1.1e-4 and
  *                   1.1e5) for full precision; a NaN code decodes as +-480 s.
  */
-typedef enum { COLI_FMT_I4G = 4, COLI_FMT_MXFP4 = 7, COLI_FMT_FP8 = 8 } coli_weight_fmt;
+typedef enum {
+    COLI_FMT_I4ROW = 2, COLI_FMT_I4G = 4, COLI_FMT_MXFP4 = 7, COLI_FMT_FP8 = 8
+} coli_weight_fmt;
 
 const char *coli_status_str(int status);
 
@@ -173,6 +180,19 @@ int coli_quant_i4g(const void *w, coli_dtype w_dtype, int64_t rows, int64_t cols
  */
 int coli_quant_mxfp4(const void *w, coli_dtype w_dtype, int64_t rows, int64_t cols,
                      uint8_t *packed, uint8_t *scales, cudaStream_t stream);
+
+/*
+ * coli_quant_i4row -- quantise W[rows][cols] into int4-row (COLI_FMT_I4ROW):
+ * per row s = max|w| / 7 (f32 division), q = clip(rint(w / s), -8, 7) (f32
+ * division, ties to even), u = q + 8, byte j = u[2j] | u[2j+1] << 4.  An
+ * all-zero row stores s = 0 and u = 8; a NaN weight is ignored by the max and
+ * stored as u = 8; with an odd column count the last high nibble is 0.
+ *   w       [rows][cols] row-major, dtype w_dtype (COLI_BF16 or COLI_F32)
+ *   packed  [rows][ceil(cols/2)] written;  scales f32 [rows] written
+ * rows >= 0, cols >= 1, any alignment.  Bit-identical to the definition.
+ */
+int coli_quant_i4row(const void *w, coli_dtype w_dtype, int64_t rows, int64_t cols,
+                     uint8_t *packed, float *scales, cudaStream_t stream);
 
 /*
  * coli_quant_fp8b128 -- quantise W[rows][cols] into fp8-e4m3-b128

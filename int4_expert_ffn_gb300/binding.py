@@ -24,7 +24,7 @@ COLI_FLAG_NAN_LOGITS, COLI_FLAG_TIMEOUT, COLI_FLAG_RANGE = 0x1, 0x2, 0x4
 COLI_KERNEL_ROUTE, COLI_KERNEL_GATEUP, COLI_KERNEL_DOWN = 0, 1, 2
 COLI_KERNEL_PREFILL_GATEUP, COLI_KERNEL_PREFILL_DOWN = 3, 4
 COLI_KERNEL_LAYER = 5
-COLI_FMT_I4G, COLI_FMT_MXFP4, COLI_FMT_FP8 = 4, 7, 8
+COLI_FMT_I4ROW, COLI_FMT_I4G, COLI_FMT_MXFP4, COLI_FMT_FP8 = 2, 4, 7, 8
 GROUP = 64
 
 # every symbol include/coli.h declares
@@ -36,7 +36,7 @@ EXPORTS = (
     "coli_profile_events", "coli_moe_check", "coli_usage_engine_id", "coli_usage_save",
     "coli_usage_load", "coli_moe_forward_tiered", "coli_tier_place", "coli_tier_update",
     "coli_quant_mxfp4", "coli_fmt_row_bytes", "coli_fmt_scale_bytes", "coli_fmt_expert_bytes",
-    "coli_fmt_expert_scale_bytes", "coli_quant_fp8b128",
+    "coli_fmt_expert_scale_bytes", "coli_quant_fp8b128", "coli_quant_i4row",
 )
 
 
@@ -87,6 +87,8 @@ def _load():
     L.coli_quant_mxfp4.restype = C.c_int
     L.coli_quant_fp8b128.argtypes = [vp, C.c_int, i64, i64, vp, vp, vp]
     L.coli_quant_fp8b128.restype = C.c_int
+    L.coli_quant_i4row.argtypes = [vp, C.c_int, i64, i64, vp, vp, vp]
+    L.coli_quant_i4row.restype = C.c_int
     for f in ("coli_fmt_row_bytes", "coli_fmt_scale_bytes"):
         getattr(L, f).argtypes = [C.c_int32, i64]
         getattr(L, f).restype = i64
@@ -178,7 +180,7 @@ class MoEDesc:
     router_dtype: int = COLI_BF16
     router_fn: int = COLI_ROUTER_SOFTMAX
     router_bias: object = None    # f32 CUDA tensor [E] (or [n_layers, E]), or None
-    weight_fmt: int = 0           # COLI_FMT_I4G (0 also), COLI_FMT_MXFP4 or COLI_FMT_FP8
+    weight_fmt: int = 0           # COLI_FMT_I4G (0 also), _I4ROW, _MXFP4 or _FP8
 
     def c(self):
         b = self.router_bias
@@ -231,6 +233,21 @@ def coli_quant_mxfp4(w, packed=None, scales=None, stream=None):
         scales = torch.empty((rows, (cols + 31) // 32), dtype=torch.uint8, device=w.device)
     _cuda(packed, scales)
     _check("coli_quant_mxfp4", lib.coli_quant_mxfp4(_ptr(w), _dt(w), rows, cols, _ptr(packed),
+                                                     _ptr(scales), _stream(stream)))
+    return packed, scales
+
+
+def coli_quant_i4row(w, packed=None, scales=None, stream=None):
+    """Quantise w [rows, cols] (bf16 or f32, CUDA) to int4-row -> (packed u8
+    [rows, ceil(cols/2)], scales f32 [rows, 1])."""
+    _cuda(w)
+    rows, cols = w.shape
+    if packed is None:
+        packed = torch.empty((rows, (cols + 1) // 2), dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty((rows, 1), dtype=torch.float32, device=w.device)
+    _cuda(packed, scales)
+    _check("coli_quant_i4row", lib.coli_quant_i4row(_ptr(w), _dt(w), rows, cols, _ptr(packed),
                                                      _ptr(scales), _stream(stream)))
     return packed, scales
 

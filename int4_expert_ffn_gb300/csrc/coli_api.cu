@@ -93,7 +93,7 @@ int check_desc(const coli_moe_desc *d, int top_k) {
   if (d->router_fn == COLI_ROUTER_SIGMOID_BIAS && ((uintptr_t)d->router_bias & 3u))
     return COLI_EALIGN;
   if (d->weight_fmt != 0 && d->weight_fmt != COLI_FMT_I4G && d->weight_fmt != COLI_FMT_MXFP4 &&
-      d->weight_fmt != COLI_FMT_FP8)
+      d->weight_fmt != COLI_FMT_FP8 && d->weight_fmt != COLI_FMT_I4ROW)
     return COLI_EINVAL;
   return COLI_OK;
 }
@@ -106,7 +106,7 @@ int pass_tokens(int T) { return T < kDecodeMaxT ? T : kDecodeMaxT; }
 
 // Calls with many tokens take the batched path (grouped tensor-core GEMMs)
 // when its tile shapes divide the layer.
-// MXFP4 and fp8 layers take it at every token count.
+// The other containers (int4-row, MXFP4, fp8) take it at every token count.
 bool use_prefill(const coli_moe_desc *d) {
   if (weight_fmt(d) != COLI_FMT_I4G) return true;
   return d->n_tokens >= kPrefillMinT && prefill_supported(d->hidden, d->ffn);
@@ -251,7 +251,8 @@ int64_t coli_expert_scale_count(int64_t H, int64_t F) {
 
 int64_t coli_fmt_row_bytes(int32_t fmt, int64_t cols) {
   if (cols < 0) return 0;
-  if (fmt == 0 || fmt == COLI_FMT_I4G || fmt == COLI_FMT_MXFP4) return (cols + 1) / 2;
+  if (fmt == 0 || fmt == COLI_FMT_I4G || fmt == COLI_FMT_MXFP4 || fmt == COLI_FMT_I4ROW)
+    return (cols + 1) / 2;
   if (fmt == COLI_FMT_FP8) return cols;
   return 0;
 }
@@ -260,6 +261,7 @@ int64_t coli_fmt_scale_bytes(int32_t fmt, int64_t cols) {
   if (fmt == 0 || fmt == COLI_FMT_I4G) return 4 * coli_scales_per_row(cols);
   if (fmt == COLI_FMT_MXFP4) return (cols + kMxBlock - 1) / kMxBlock;
   if (fmt == COLI_FMT_FP8) return 4 * ((cols + kFp8Block - 1) / kFp8Block);
+  if (fmt == COLI_FMT_I4ROW) return 4;
   return 0;
 }
 int64_t coli_fmt_expert_bytes(int32_t fmt, int64_t H, int64_t F) {
@@ -289,6 +291,15 @@ int coli_quant_mxfp4(const void *w, coli_dtype w_dtype, int64_t rows, int64_t co
   if (rows > 0 && (!w || !packed || !scales)) return COLI_EINVAL;
   if (rows > 0 && cols > INT64_MAX / rows) return COLI_EINVAL;
   return map_err(launch_quant_mxfp4(w, w_dtype, rows, cols, packed, scales, stream));
+}
+
+int coli_quant_i4row(const void *w, coli_dtype w_dtype, int64_t rows, int64_t cols,
+                     uint8_t *packed, float *scales, cudaStream_t stream) {
+  if (rows < 0 || cols < 1) return COLI_EINVAL;
+  if (w_dtype != COLI_F32 && w_dtype != COLI_BF16) return COLI_EINVAL;
+  if (rows > 0 && (!w || !packed || !scales)) return COLI_EINVAL;
+  if (rows > 0 && cols > INT64_MAX / rows) return COLI_EINVAL;
+  return map_err(launch_quant_i4row(w, w_dtype, rows, cols, packed, scales, stream));
 }
 
 int coli_quant_fp8b128(const void *w, coli_dtype w_dtype, int64_t rows, int64_t cols,

@@ -201,7 +201,7 @@ constexpr int kPrefillMinT = 64;      // calls with at least this many tokens ta
 constexpr int kGroupTokens = 256;     // tokens per block of the counting sort
 struct PrefillArgs {
   TierMap tier;
-  int fmt;                  // COLI_FMT_I4G, _MXFP4 or _FP8 (the last two: es counts scale bytes)
+  int fmt;                  // COLI_FMT_I4G, _I4ROW, _MXFP4 or _FP8 (all but I4G: es counts bytes)
   int T, H, F, E, S, k;
   int router_fn;            // coli_router_fn
   const float *router_bias; // [E] (sigmoid router) or null
@@ -256,6 +256,8 @@ cudaError_t launch_quant_mxfp4(const void *w, int w_dtype, int64_t rows, int64_t
                                uint8_t *packed, uint8_t *scales, cudaStream_t s);
 cudaError_t launch_quant_fp8b128(const void *w, int w_dtype, int64_t rows, int64_t cols,
                                  uint8_t *packed, float *scales, cudaStream_t s);
+cudaError_t launch_quant_i4row(const void *w, int w_dtype, int64_t rows, int64_t cols,
+                               uint8_t *packed, float *scales, cudaStream_t s);
 
 int num_sms();
 // The layer forward over a tiered expert store (coli_api.cu); `packed` and

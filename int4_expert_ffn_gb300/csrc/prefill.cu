@@ -531,10 +531,11 @@ __global__ void __launch_bounds__(256) k_gscatter(PrefillArgs p) {
 // ---------------------------------------------------------------------------
 // The grouped GEMM.
 
-// FMT: COLI_FMT_I4G (one f32 scale per row and k-tile), COLI_FMT_MXFP4 (one
-// E8M0 byte per row and 32 columns: a thread's half of the k-tile has exactly
-// one; the copy brings the aligned 4-byte word that holds it) or COLI_FMT_FP8
-// (one f32 scale per row and two k-tiles).
+// FMT: COLI_FMT_I4G (one f32 scale per row and k-tile), COLI_FMT_I4ROW (one
+// f32 scale per row), COLI_FMT_MXFP4 (one E8M0 byte per row and 32 columns: a
+// thread's half of the k-tile has exactly one; the copy brings the aligned
+// 4-byte word that holds it) or COLI_FMT_FP8 (one f32 scale per row and two
+// k-tiles).
 template <int MODE, int FMT>
 __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
   using G = Geo<FMT>;
@@ -645,9 +646,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
           const int64_t rh = FMT == COLI_FMT_FP8 ? H : H / 2;
           const int64_t rf = FMT == COLI_FMT_FP8 ? F : F / 2;
           const int64_t sh = FMT == COLI_FMT_MXFP4 ? H / kMxBlock
-                             : FMT == COLI_FMT_FP8 ? 4 * (H / kFp8Block) : 4 * (H / kGroup);
+                             : FMT == COLI_FMT_FP8 ? 4 * (H / kFp8Block)
+                             : FMT == COLI_FMT_I4ROW ? 4 : 4 * (H / kGroup);
           const int64_t sf = FMT == COLI_FMT_MXFP4 ? F / kMxBlock
-                             : FMT == COLI_FMT_FP8 ? 4 * (F / kFp8Block) : 4 * (F / kGroup);
+                             : FMT == COLI_FMT_FP8 ? 4 * (F / kFp8Block)
+                             : FMT == COLI_FMT_I4ROW ? 4 : 4 * (F / kGroup);
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             if (MODE == kModeGateUp) {
@@ -677,10 +680,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
           for (int ch = 0; ch < kCh; ++ch)
             cp16(smem_u32(raw + ((j * kCh + ch) * kProducerThreads + th) * 16),
                  b_src[j] + (k0 + 32 * b_half) * kCh / 2 + 16 * ch);
-          // int4: the k-tile's f32 scale; MXFP4: the word holding its two E8M0
-          // bytes; fp8: the f32 scale of the 128 columns holding the k-tile
+          // int4-grouped: the k-tile's f32 scale; MXFP4: the word holding its
+          // two E8M0 bytes; fp8: the f32 scale of the 128 columns holding the
+          // k-tile; int4-row: the row's scale
           cp4(smem_u32(raw + kRawData + (j * kProducerThreads + th) * 4),
-              b_sc[j] + (FMT == COLI_FMT_I4G ? kt * 4 : (kt >> 1) * 4));
+              b_sc[j] + (FMT == COLI_FMT_I4G ? kt * 4 : FMT == COLI_FMT_I4ROW ? 0 : (kt >> 1) * 4));
         }
         if (++kt == nk) { kt = 0; ++item; }
       }
@@ -946,6 +950,7 @@ cudaError_t launch_prefill(const PrefillArgs &p, int x_dtype, int wr_dtype, cuda
   // GEMMs
   if (p.fmt == COLI_FMT_MXFP4) e = launch_gemms<COLI_FMT_MXFP4>(p, nsm, s);
   else if (p.fmt == COLI_FMT_FP8) e = launch_gemms<COLI_FMT_FP8>(p, nsm, s);
+  else if (p.fmt == COLI_FMT_I4ROW) e = launch_gemms<COLI_FMT_I4ROW>(p, nsm, s);
   else e = launch_gemms<COLI_FMT_I4G>(p, nsm, s);
   if (e != cudaSuccess) return e;
   // combine

@@ -1,7 +1,7 @@
 // Quantisers of the floating-point containers of the engine's format registry
 // (page "从源码开始colibri纯C引擎的编译、权重转换与.bin直映射实战" §权重转换:
-// "7 MXFP4", "8 fp8-e4m3-b128"; "Colibrì 深度解析" §十 "从 int4 到 MXFP4").
-// One thread per row block.
+// "2 int4-row", "7 MXFP4", "8 fp8-e4m3-b128"; "Colibrì 深度解析" §十 "从 int4 到
+// MXFP4").  MXFP4 and fp8: one thread per row block.
 //
 // MXFP4 (OCP Microscaling v1.0), blocks of 32 columns: shared exponent
 // se = floor(log2 max|w|) - 2 (2 = the largest E2M1 exponent), clamped to
@@ -12,6 +12,9 @@
 // fp8-e4m3-b128, blocks of 128 columns: f32 scale s = max|w| / 448; each
 // element becomes the OCP E4M3 code nearest to w / s, ties to the even code,
 // saturating at the largest finite value 448.
+//
+// int4-row ("2 int4-row"): the int4-grouped rule over a whole row, one CTA per
+// row (a block-wide max, then a byte per thread and step).
 #include <cuda_fp8.h>
 
 #include "coli_internal.cuh"
@@ -104,7 +107,62 @@ __global__ void k_quant_fp8(const T *__restrict__ w, int64_t rows, int64_t cols,
   }
 }
 
+constexpr int kRowThreads = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads) k_quant_i4row(const T *__restrict__ w, int64_t rows,
+                                                               int64_t cols,
+                                                               uint8_t *__restrict__ packed,
+                                                               float *__restrict__ scales) {
+  __shared__ float s_max[kRowThreads / 32];
+  const int64_t rb = (cols + 1) / 2;
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    const T *wr = w + r * cols;
+    float m = 0.0f;
+    for (int64_t c = threadIdx.x; c < cols; c += blockDim.x) m = fmaxf(m, fabsf(to_f32(wr[c])));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+    if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = 0.0f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) m = fmaxf(m, s_max[i]);   // NaN never wins
+    __syncthreads();                     // s_max is reused by the next row
+    const float s = __fdiv_rn(m, 7.0f);
+    if (threadIdx.x == 0) scales[r] = s;
+    for (int64_t j = threadIdx.x; j < rb; j += blockDim.x) {
+      int u[2] = {8, 0};
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t c = 2 * j + h;
+        if (c >= cols) break;            // odd column count: the last high nibble stays 0
+        int q = 0;
+        if (s != 0.0f) {
+          const float v = rintf(__fdiv_rn(to_f32(wr[c]), s));
+          q = (v != v) ? 0 : (v < -8.0f ? -8 : (v > 7.0f ? 7 : (int)v));
+        }
+        u[h] = q + 8;
+      }
+      packed[r * rb + j] = (uint8_t)(u[0] | (u[1] << 4));
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_quant_i4row(const void *w, int w_dtype, int64_t rows, int64_t cols,
+                               uint8_t *packed, float *scales, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  const int sms = num_sms();
+  if (sms <= 0) return cudaErrorNoDevice;
+  const int64_t blocks = rows < (int64_t)sms * 8 ? rows : (int64_t)sms * 8;
+  if (w_dtype == COLI_BF16)
+    k_quant_i4row<__nv_bfloat16><<<(unsigned)blocks, kRowThreads, 0, s>>>(
+        (const __nv_bfloat16 *)w, rows, cols, packed, scales);
+  else
+    k_quant_i4row<float><<<(unsigned)blocks, kRowThreads, 0, s>>>((const float *)w, rows, cols,
+                                                                   packed, scales);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quant_fp8b128(const void *w, int w_dtype, int64_t rows, int64_t cols,
                                  uint8_t *packed, float *scales, cudaStream_t s) {

@@ -72,8 +72,8 @@ class Layer:
 
 
 class FmtLayer:
-    """One MoE layer in a floating-point container (COLI_FMT_MXFP4 or
-    COLI_FMT_FP8): quantised on the GPU and, independently, by the oracle;
+    """One MoE layer in another container (COLI_FMT_MXFP4, COLI_FMT_FP8 or
+    COLI_FMT_I4ROW): quantised on the GPU and, independently, by the oracle;
     the two records must agree byte for byte."""
 
     def __init__(self, shape, fmt, layer=0, seed=0):
@@ -82,6 +82,7 @@ class FmtLayer:
         gpu_q, orc_q, sdt = {
             c.COLI_FMT_MXFP4: (c.coli_quant_mxfp4, orc.quant_mxfp4, torch.uint8),
             c.COLI_FMT_FP8: (c.coli_quant_fp8b128, orc.quant_fp8b128, torch.float32),
+            c.COLI_FMT_I4ROW: (c.coli_quant_i4row, orc.quant_i4row, torch.float32),
         }[fmt]
         self.shape, self.fmt = shape, fmt
         mats = [synth.expert_matrix(shape, layer, e, m, seed) for e in range(E + S)

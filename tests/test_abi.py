@@ -81,7 +81,7 @@ def test_desc_layout_matches_header(coli):
     text = open(os.path.join(ROOT, "include", "coli.h")).read()
     assert "COLI_ROUTER_SIGMOID_BIAS = 1" in text and "const float *router_bias;" in text
     assert "int32_t weight_fmt;" in text and "COLI_FMT_MXFP4 = 7" in text
-    assert "COLI_FMT_FP8 = 8" in text
+    assert "COLI_FMT_FP8 = 8" in text and "COLI_FMT_I4ROW = 2" in text
 
 
 def test_workspace_size_bad_topk(coli):
@@ -172,3 +172,9 @@ def test_weight_format_rules(coli):
     assert coli.lib.coli_fmt_scale_bytes(coli.COLI_FMT_FP8, 333) == 4 * 3
     assert coli.coli_fmt_expert_bytes(coli.COLI_FMT_FP8, 256, 128) == 3 * 256 * 128
     assert coli.coli_fmt_expert_scale_bytes(coli.COLI_FMT_FP8, 256, 128) == 4 * (2 * 128 * 2 + 256 * 1)
+    # int4-row: int4 nibbles, one f32 scale per row
+    d = coli.MoEDesc(256, 128, 8, 1, 4, coli.COLI_F32, coli.COLI_BF16, weight_fmt=coli.COLI_FMT_I4ROW)
+    assert coli.coli_moe_workspace_size(d, 2) > 0
+    assert coli.lib.coli_fmt_row_bytes(coli.COLI_FMT_I4ROW, 333) == 167
+    assert coli.lib.coli_fmt_scale_bytes(coli.COLI_FMT_I4ROW, 333) == 4
+    assert coli.coli_fmt_expert_scale_bytes(coli.COLI_FMT_I4ROW, 256, 128) == 4 * (2 * 128 + 256)
