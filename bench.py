@@ -39,7 +39,10 @@ METRIC = "MoE decode tokens/s and int4 expert-weight GB/s vs GB300 HBM peak"
 # or once the kernel has changed since.  Batch 1: the per-layer launch is the
 # same in a 1- or 2-layer capture as in the full stack.
 NCU_TRAFFIC = {
-    "olmoe_decode": {"k_gateup": 19016192, "k_down": 10036736},
+    # the one-token layer kernel (one launch per layer)
+    "olmoe_decode": {"k_layer1": 28635648},
+    # the one-token gate/up (with the first layer's router) and down kernels
+    "glm_decode_b1": {"k_gateup": 132213120, "k_down": 64369792},
     # the several-token kernel k_gateup_multi; its experts per launch vary with
     # the routing
     "glm_decode_b8": {"k_gateup": 879500288 + 7344384},
