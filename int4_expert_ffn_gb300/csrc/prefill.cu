@@ -76,6 +76,10 @@ struct GeoBytes {
   static constexpr int kSmem =
       G::kNA * kATileBytes + G::kNB * kBTileBytes + G::kNR * kRaw + kTableBytes + 2048;
   static_assert(G::kNR > G::kDist, "a raw slot is refilled only after its dequantisation");
+  // an A tile is copied kDist ticks before its dequantisation tick and is
+  // free again only after the MMA of that k-tile: a shallower ring stalls the
+  // producers until their bounded waits give up
+  static_assert(G::kNA >= G::kDist + 2, "A ring deep enough for the copy distance");
   static_assert(kSmem <= 232448, "shared memory of one block");
 };
 static_assert(kProducerThreads == kBN, "a thread pair per B row, two rows per pair");
