@@ -6,7 +6,8 @@
 // int4-grouped format the expert GEMMs dequantise).
 //
 //   k_x16       activations -> fp16 operand copy
-//   k_logits    router logits, tiled f32 SIMT GEMM (any x / router dtype)
+//   k_plogits   router logits on tcgen05 tensor cores (bf16 x and router)
+//   k_logits    router logits, tiled f32 SIMT GEMM (the other dtypes)
 //   k_ptopk     top-k, gates, NaN flag and route counts (block-parallel top-k)
 //   k_gcount / k_gscan / k_gscatter
 //               counting sort of the routes by expert (stable in (token, slot)
@@ -396,6 +397,153 @@ __global__ void __launch_bounds__(256) k_logits(const XT *x, const WT *wr, float
       const int t = t0 + ty * 4 + i, e = e0 + tx * 4 + j;
       if (t < T && e < E) logits[(size_t)t * E + e] = acc[i][j];
     }
+}
+
+// ---------------------------------------------------------------------------
+// Router logits on the tensor cores when x and the router are both bf16:
+// logits [T][E] = x [T][H] . Wr [E][H]^T with tcgen05.mma kind::f16 (bf16
+// operands, exact products, f32 accumulation in TMEM).  One CTA per 128-token
+// x 256-expert tile, K in steps of 64 (128-byte rows, the grouped GEMM's
+// swizzled layout).  Eight producer warps copy both operand tiles with
+// cp.async (kLgStages stages, kLgDist tiles ahead); one thread issues the
+// MMAs; four warps write the f32 logits.  Rows past T and experts past E are
+// not copied and never stored.  The sum order differs from k_logits' fmaf
+// chain only by rounding; token inputs keep a gap between ranked logits.
+
+constexpr int kLgStages = 4, kLgDist = 3;
+constexpr int kLgATile = kBM * kBK * 2;             // 16 KB
+constexpr int kLgBTile = kBN * kBK * 2;             // 32 KB
+constexpr int kLgSmem = kLgStages * (kLgATile + kLgBTile) + 1024 + 256;
+static_assert(kLgStages > kLgDist, "a stage is refilled only after the MMA that read it");
+static_assert(kLgSmem <= 232448, "shared memory of one block");
+
+__host__ __device__ constexpr uint32_t idesc_bf16(int n, int m) {
+  return idesc_f16(n, m) | (1u << 7) | (1u << 10);   // A and B formats: BF16
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    k_plogits(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *__restrict__ wr,
+              float *__restrict__ logits, int T, int H, int E, uint32_t *ctrl) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t *a_ring = smem;                                     // stages x 16 KB
+  uint8_t *b_ring = a_ring + kLgStages * kLgATile;            // stages x 32 KB
+  uint64_t *full = (uint64_t *)(b_ring + kLgStages * kLgBTile);
+  uint64_t *empty = full + kLgStages;
+  uint64_t *acc_full = empty + kLgStages;
+  uint64_t *mma_done = acc_full + 1;
+  uint32_t *s_taddr = (uint32_t *)(mma_done + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * kBN;
+  const int nk = H / kBK;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kLgStages; ++s) {
+      mbar_init(&full[s], kProducerThreads);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(s_taddr, kBN);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  grid_dependents_launch();
+  grid_dependency_wait();
+  const uint32_t tbase = *s_taddr;
+  const uint32_t lim_word = __ldcg(ctrl + kCtrlWaitLimit);
+  const long long lim = lim_word ? (long long)lim_word : kWaitCycles;
+
+  if (warp < kProducerWarps) {
+    // 8 threads per 128-byte row: A rows th/8 + 32 j (4 passes), B rows th/8 + 32 j (8)
+    const int th = threadIdx.x, chunk = th & 7, row0 = th >> 3;
+    bool ok = true;
+    for (int t = 0; t < nk + kLgDist && ok; ++t) {
+      if (t < nk) {
+        const int st = t % kLgStages;
+        if (!mbar_wait(&empty[st], ((t / kLgStages) & 1) ^ 1, lim)) { ok = false; break; }
+        const uint32_t a_dst = smem_u32(a_ring + st * kLgATile);
+        const uint32_t b_dst = smem_u32(b_ring + st * kLgBTile);
+        const int k0 = t * kBK + 8 * chunk;
+#pragma unroll
+        for (int j = 0; j < kBM / 32; ++j) {
+          const int r = row0 + 32 * j;
+          if (m0 + r < T) cp16(a_dst + sw128_off(r, chunk), x + (size_t)(m0 + r) * H + k0);
+        }
+#pragma unroll
+        for (int j = 0; j < kBN / 32; ++j) {
+          const int r = row0 + 32 * j;
+          if (n0 + r < E) cp16(b_dst + sw128_off(r, chunk), wr + (size_t)(n0 + r) * H + k0);
+        }
+      }
+      cp_commit();
+      const int c = t - kLgDist;
+      if (c < 0) continue;
+      cp_wait<kLgDist>();          // this thread's copies of tile c have landed
+      fence_proxy_async();         // generic-proxy writes -> tensor core reads
+      mbar_arrive(&full[c % kLgStages]);
+    }
+    cp_wait<0>();
+    if (!ok) set_flag_p(ctrl, COLI_FLAG_TIMEOUT);
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(kBN, kBM);
+      bool ok = true;
+      for (int c = 0; c < nk; ++c) {
+        const int st = c % kLgStages;
+        if (!mbar_wait(&full[st], (c / kLgStages) & 1, lim)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(a_ring + st * kLgATile);
+        const uint32_t b0 = smem_u32(b_ring + st * kLgBTile);
+#pragma unroll
+        for (int k16 = 0; k16 < kBK / 16; ++k16)
+          tc_mma(tbase, sw128_desc(a0 + 32 * k16), sw128_desc(b0 + 32 * k16), idesc,
+                 (c | k16) != 0);
+        tc_commit(&empty[st]);
+      }
+      if (ok) tc_commit(acc_full);
+      else set_flag_p(ctrl, COLI_FLAG_TIMEOUT);
+      // every MMA issued has completed before TMEM is freed
+      tc_commit(mma_done);
+      if (!mbar_wait(mma_done, 0)) set_flag_p(ctrl, COLI_FLAG_TIMEOUT);
+    }
+    __syncwarp();
+  } else {
+    // epilogue: TMEM lane quarter (warp % 4) holds tile rows 32 (warp % 4) + lane
+    const int q = warp & 3;
+    const int r = 32 * q + lane;
+    if (mbar_wait(acc_full, 0, lim)) {
+      tc_fence_after();
+      const uint32_t trow = tbase + ((uint32_t)(32 * q) << 16);
+      for (int cc = 0; cc < kBN; cc += 32) {
+        uint32_t v[32];
+        tmem_ld32(trow + cc, v);
+        tmem_ld_wait();
+        if (m0 + r < T) {
+          float *dst = logits + (size_t)(m0 + r) * E + n0 + cc;
+          if (n0 + cc + 32 <= E && (E & 3) == 0) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              ((float4 *)dst)[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                               __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          } else {
+            for (int j = 0; j < 32; ++j)
+              if (n0 + cc + j < E) dst[j] = __uint_as_float(v[j]);
+          }
+        }
+      }
+    } else {
+      set_flag_p(ctrl, COLI_FLAG_TIMEOUT);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tbase, kBN);
 }
 
 // ---------------------------------------------------------------------------
@@ -931,12 +1079,18 @@ cudaError_t launch_prefill(const PrefillArgs &p, int x_dtype, int wr_dtype, cuda
   if (x_dtype == COLI_BF16)
     k_x16<__nv_bfloat16><<<gx, 256, 0, s>>>((const __nv_bfloat16 *)p.x, p.x16, nx, p.ctrl);
   else k_x16<float><<<gx, 256, 0, s>>>((const float *)p.x, p.x16, nx, p.ctrl);
-  // router logits
+  // router logits: tensor cores when both operands are bf16 (exact products),
+  // else the f32 SIMT GEMM
   const dim3 gl((E + 63) / 64, (T + 63) / 64);
 #define COLI_LOGITS(XT, WT) \
   k_logits<XT, WT><<<gl, 256, 0, s>>>((const XT *)p.x, (const WT *)p.wr, p.logits, T, H, E)
-  if (x_dtype == COLI_BF16 && wr_dtype == COLI_BF16) COLI_LOGITS(__nv_bfloat16, __nv_bfloat16);
-  else if (x_dtype == COLI_BF16) COLI_LOGITS(__nv_bfloat16, float);
+  if (x_dtype == COLI_BF16 && wr_dtype == COLI_BF16) {
+    if ((e = set_smem(k_plogits, kLgSmem)) != cudaSuccess) return e;
+    const dim3 gp((T + kBM - 1) / kBM, (E + kBN - 1) / kBN);
+    k_plogits<<<gp, kGemmThreads, kLgSmem, s>>>((const __nv_bfloat16 *)p.x,
+                                                (const __nv_bfloat16 *)p.wr, p.logits, T, H, E,
+                                                p.ctrl);
+  } else if (x_dtype == COLI_BF16) COLI_LOGITS(__nv_bfloat16, float);
   else if (wr_dtype == COLI_BF16) COLI_LOGITS(float, __nv_bfloat16);
   else COLI_LOGITS(float, float);
 #undef COLI_LOGITS
