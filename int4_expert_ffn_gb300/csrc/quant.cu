@@ -31,13 +31,14 @@ __device__ __forceinline__ int quant_one(float w, float s, float r) {
 }
 
 // The same result with fewer instructions, for the vectorised path: eight
-// elements of one group (scale s, r = rcp(s)) into one packed word.  Adding
-// 1.5 * 2^23 to a = w * r (|a| < 2^22) leaves round-half-even(a) in the low
-// mantissa bits, so the sum's bit pattern minus the constant's is rint(a);
-// subtracting the constant back gives rint(a) as a float, and |a - rint(a)|
-// is the distance to it.  For finite weights |a| <= 7 (1 + 2^-20), so
-// rint(a) is in [-7, 7] and needs no clamp.  If any of the eight quotients
-// lies within 4e-6 of a half-integer, or is not finite (the distance is then
+// elements of one group (scale s, r = rcp(s)) into one packed word.  With
+// K = 1.5 * 2^23, t = fma(w, r, K) rounds the exact product w r to an integer
+// n (ties to even: K is even) held in t's low mantissa bits, so t's low
+// nibble is n mod 16 and (n mod 16) ^ 8 = n + 8 = u for n in [-8, 7];
+// d = fma(w, r, -n) is the product's distance to n.  For finite weights
+// |w r| <= 7 (1 + 2^-20), so n needs no clamp, and the exact quotient w / s
+// lies within 1.7e-6 of w r: whenever |d| < 0.5 - 4e-6 both round to n.  If
+// any of the eight is closer to a half-integer, or not finite (d is then
 // NaN), the word is recomputed element by element with quant_one.
 constexpr float kRoundShift = 12582912.0f;   // 1.5 * 2^23
 
@@ -48,17 +49,18 @@ __device__ __forceinline__ float rcp_approx(float x) {
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
 }
-__device__ __forceinline__ uint32_t quant_word(const float (&v)[8], float s, float r) {
+__device__ __forceinline__ uint32_t quant_word(const float *v, float s, float r) {
   uint32_t word = 0;
   bool exact = true;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float a = v[i] * r;
-    const float t = a + kRoundShift;
-    const float e = fabsf(a - (t - kRoundShift));
-    word |= (uint32_t)(__float_as_int(t) - __float_as_int(kRoundShift) + 8) << (4 * i);
-    exact = exact && (e < 0.5f - 4e-6f);
+  for (int i = 7; i >= 0; --i) {
+    const float t = fmaf(v[i], r, kRoundShift);
+    const float n = t - kRoundShift;
+    const float d = fmaf(v[i], r, -n);
+    word = (word << 4) | (__float_as_uint(t) & 0xFu);
+    exact = exact && (fabsf(d) < 0.5f - 4e-6f);
   }
+  word ^= 0x88888888u;
   if (!exact) {
     word = 0;
 #pragma unroll
@@ -98,22 +100,27 @@ struct Load8<float> {
 
 // Vectorised path: cols % 64 == 0 and 16-byte aligned w, so group g of the
 // flattened matrix is elements [64g, 64g+64), bytes [32g, 32g+32), scale g.
-// A team of 8 lanes owns one group; each lane holds 8 consecutive elements.
+// A team of 4 lanes owns one group; each lane holds 16 consecutive elements
+// (two packed words), so the per-group work (max across the team, the scale
+// division, the reciprocal, the stores) is shared by 16 elements per lane.
 template <typename T, int U>
 __global__ void __launch_bounds__(256, 4) k_quant_vec(const T *__restrict__ w, int64_t n_groups,
                                                    uint32_t *__restrict__ packed,
                                                    float *__restrict__ scales) {
   const int lane = threadIdx.x & 31;
-  const int sub = lane & 7;
-  const unsigned team_mask = 0xFFu << (lane & 24);
-  const int64_t team = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 3;
-  const int64_t n_teams = ((int64_t)gridDim.x * blockDim.x) >> 3;
+  const int sub = lane & 3;
+  const unsigned team_mask = 0xFu << (lane & 28);
+  const int64_t team = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 2;
+  const int64_t n_teams = ((int64_t)gridDim.x * blockDim.x) >> 2;
   for (int64_t g0 = team; g0 < n_groups; g0 += n_teams * U) {
-    float v[U][8];
+    float v[U][16];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t g = g0 + (int64_t)u * n_teams;
-      if (g < n_groups) Load8<T>::run(w + g * kGroup + sub * 8, v[u]);
+      if (g < n_groups) {
+        Load8<T>::run(w + g * kGroup + sub * 16, v[u]);
+        Load8<T>::run(w + g * kGroup + sub * 16 + 8, v[u] + 8);
+      }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -121,16 +128,18 @@ __global__ void __launch_bounds__(256, 4) k_quant_vec(const T *__restrict__ w, i
       if (g >= n_groups) break;  // uniform across the team
       float m = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[u][i]));
+      for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[u][i]));
       m = fmaxf(m, __shfl_xor_sync(team_mask, m, 1));
       m = fmaxf(m, __shfl_xor_sync(team_mask, m, 2));
-      m = fmaxf(m, __shfl_xor_sync(team_mask, m, 4));
       const float s = __fdiv_rn(m, 7.0f);
-      uint32_t word = 0x88888888u;
+      uint2 words = make_uint2(0x88888888u, 0x88888888u);
       if (s != 0.0f) {
-        word = quant_word(v[u], s, rcp_approx(s));
+        const float r = rcp_approx(s);
+        words.x = quant_word(v[u], s, r);
+        words.y = quant_word(v[u] + 8, s, r);
       }
-      packed[g * 8 + sub] = word;
+      packed[g * 8 + 2 * sub] = words.x;        // packed is only 4-byte aligned
+      packed[g * 8 + 2 * sub + 1] = words.y;
       if (sub == 0) scales[g] = s;
     }
   }
@@ -179,14 +188,14 @@ cudaError_t launch_quant_i4g(const void *w, int w_dtype, int64_t rows, int64_t c
   if (cols % kGroup == 0 && aligned) {
     const int64_t n_groups = rows * (cols / kGroup);
     const int64_t teams_needed = n_groups;
-    int64_t blocks = (teams_needed * 8 + 255) / 256;
+    int64_t blocks = (teams_needed * 4 + 255) / 256;
     const int64_t cap = (int64_t)sms * 4;  // 4 blocks of 256 per SM resident (64 registers)
     if (blocks > cap) blocks = cap;
     if (w_dtype == COLI_BF16)
-      k_quant_vec<__nv_bfloat16, 4><<<(unsigned)blocks, 256, 0, s>>>(
+      k_quant_vec<__nv_bfloat16, 2><<<(unsigned)blocks, 256, 0, s>>>(
           (const __nv_bfloat16 *)w, n_groups, (uint32_t *)packed, scales);
     else
-      k_quant_vec<float, 2><<<(unsigned)blocks, 256, 0, s>>>(
+      k_quant_vec<float, 1><<<(unsigned)blocks, 256, 0, s>>>(
           (const float *)w, n_groups, (uint32_t *)packed, scales);
   } else {
     const int64_t total = rows * ((cols + kGroup - 1) / kGroup);
