@@ -1,5 +1,5 @@
 // Inline-PTX helpers of the sm_103a kernels: mbarriers, 1-D bulk (TMA) copies,
-// L2 prefetch, and bounded waits.  Every wait gives up after kWaitCycles and
+// and bounded waits.  Every wait gives up after kWaitCycles and
 // reports it, so a lost completion can never hang the GPU.
 #pragma once
 
@@ -80,11 +80,6 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
           "r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
-}
-
-// Hint: bring `bytes` (multiple of 16, 16-byte aligned) of global memory into L2.
-__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // Programmatic dependent launch: wait for the preceding kernel's results /
