@@ -50,7 +50,8 @@ typedef enum {
     COLI_EUNSUPPORTED = -6,  /* valid, but outside what this build handles */
     COLI_EIO = -7,           /* a file could not be opened, written or renamed */
     COLI_EREFUSED = -8,      /* a usage history belongs to another model or format */
-    COLI_ERANGE = -9         /* an operand left the fp16 range of the batched path */
+    COLI_ERANGE = -9,        /* an operand left the fp16 range of the batched path */
+    COLI_EBOUNDS = -10       /* checked build: an index outside its buffer (COLI_FLAG_BOUNDS) */
 } coli_status;
 
 typedef enum { COLI_F32 = 0, COLI_BF16 = 1 } coli_dtype;
@@ -61,6 +62,10 @@ typedef enum { COLI_F32 = 0, COLI_BF16 = 1 } coli_dtype;
 #define COLI_FLAG_RANGE      0x4u   /* batched path: a value of x or of h = silu(g) u gate
                                        rounded to +-inf in its fp16 operand copy (|v| above
                                        65504); that call's output is not to be used */
+#define COLI_FLAG_BOUNDS     0x8u   /* diagnostic build only (-DCOLI_CHECK): an index a kernel
+                                       derived from data (expert ids, slot and route lists,
+                                       token ids) fell outside its buffer; the access was
+                                       redirected to element 0 and the output is not to be used */
 
 /*
  * Routing function ([P1] §十一 "route"; GLM layers: "per-layer n_group=1
@@ -419,9 +424,10 @@ int coli_profile_events(int kernel, const cudaEvent_t *before, const cudaEvent_t
 /*
  * coli_moe_check -- read (and optionally clear) the device-side flag word of a
  * workspace.  Synchronises `stream`.  *flags receives COLI_FLAG_* bits.
- * Returns COLI_ETIMEOUT if COLI_FLAG_TIMEOUT is set, else COLI_ERANGE if
- * COLI_FLAG_RANGE is set, else COLI_OK (COLI_FLAG_NAN_LOGITS alone is a
- * handled condition: the rule above defines that token's routing).
+ * Returns COLI_ETIMEOUT if COLI_FLAG_TIMEOUT is set, else COLI_EBOUNDS if
+ * COLI_FLAG_BOUNDS is set, else COLI_ERANGE if COLI_FLAG_RANGE is set, else
+ * COLI_OK (COLI_FLAG_NAN_LOGITS alone is a handled condition: the rule above
+ * defines that token's routing).
  */
 int coli_moe_check(void *workspace, int clear, uint32_t *flags, cudaStream_t stream);
 

@@ -13,14 +13,17 @@ from dataclasses import dataclass
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libcoli.so")
+# COLI_LIBRARY=check loads the diagnostic bounds-checked build (libcoli_check.so,
+# built by build(variant="check")); otherwise the library itself
+LIB_PATH = os.path.join(_PKG, "libcoli_check.so" if os.environ.get("COLI_LIBRARY") == "check"
+                        else "libcoli.so")
 
 COLI_OK, COLI_EINVAL, COLI_EALIGN, COLI_ECUDA, COLI_ETIMEOUT, COLI_ENOMEM, COLI_EUNSUPPORTED = (
     0, -1, -2, -3, -4, -5, -6)
-COLI_EIO, COLI_EREFUSED, COLI_ERANGE = -7, -8, -9
+COLI_EIO, COLI_EREFUSED, COLI_ERANGE, COLI_EBOUNDS = -7, -8, -9, -10
 COLI_F32, COLI_BF16 = 0, 1
 COLI_ROUTER_SOFTMAX, COLI_ROUTER_SIGMOID_BIAS = 0, 1
-COLI_FLAG_NAN_LOGITS, COLI_FLAG_TIMEOUT, COLI_FLAG_RANGE = 0x1, 0x2, 0x4
+COLI_FLAG_NAN_LOGITS, COLI_FLAG_TIMEOUT, COLI_FLAG_RANGE, COLI_FLAG_BOUNDS = 0x1, 0x2, 0x4, 0x8
 COLI_KERNEL_ROUTE, COLI_KERNEL_GATEUP, COLI_KERNEL_DOWN = 0, 1, 2
 COLI_KERNEL_PREFILL_GATEUP, COLI_KERNEL_PREFILL_DOWN = 3, 4
 COLI_KERNEL_LAYER = 5
@@ -368,7 +371,7 @@ def coli_moe_check(workspace, clear=True, stream=None):
     """Return the device-side flag word (COLI_FLAG_*) of a workspace; clears it by default."""
     flags = C.c_uint32(0)
     st = lib.coli_moe_check(_ptr(workspace), 1 if clear else 0, C.byref(flags), _stream(stream))
-    if st not in (COLI_OK, COLI_ETIMEOUT, COLI_ERANGE):
+    if st not in (COLI_OK, COLI_ETIMEOUT, COLI_ERANGE, COLI_EBOUNDS):
         raise ColiError("coli_moe_check", st)
     return flags.value
 

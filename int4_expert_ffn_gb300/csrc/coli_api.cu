@@ -236,6 +236,7 @@ const char *coli_status_str(int status) {
     case COLI_EIO: return "file I/O failed";
     case COLI_EREFUSED: return "usage history of another model or format";
     case COLI_ERANGE: return "operand outside the fp16 range of the batched path";
+    case COLI_EBOUNDS: return "index outside its buffer (checked build)";
     default: return "unknown status";
   }
 }
@@ -617,6 +618,7 @@ int coli_moe_check(void *workspace, int clear, uint32_t *flags, cudaStream_t str
   if (e != cudaSuccess) return map_err(e);
   *flags = v;
   if (v & COLI_FLAG_TIMEOUT) return COLI_ETIMEOUT;
+  if (v & COLI_FLAG_BOUNDS) return COLI_EBOUNDS;
   return (v & COLI_FLAG_RANGE) ? COLI_ERANGE : COLI_OK;
 }
 

@@ -119,6 +119,22 @@ __device__ __forceinline__ void expert_record(const TierMap &t, const uint8_t *p
   }
 }
 
+// Diagnostic build (-DCOLI_CHECK): an index that a kernel derives from data
+// (expert ids from routing, slot and route lists, token ids from the grouping)
+// is checked against the extent of the buffer it indexes; one outside sets
+// COLI_FLAG_BOUNDS and is replaced by 0, so the access stays inside the buffer.
+// Without the flag the check compiles away.
+#ifdef COLI_CHECK
+__device__ __forceinline__ int64_t chk_idx(int64_t i, int64_t n, uint32_t *ctrl) {
+  if (i >= 0 && i < n) return i;
+  atomicOr(ctrl, COLI_FLAG_BOUNDS);     // the flag word is control word 0
+  return 0;
+}
+#define COLI_CHK(i, n, ctrl) ((int)::coli::chk_idx((int64_t)(i), (int64_t)(n), (ctrl)))
+#else
+#define COLI_CHK(i, n, ctrl) ((int)(i))
+#endif
+
 // Arguments of the decode kernels (one layer, T <= kDecodeMaxT tokens).
 struct Dec2Args {
   TierMap tier;

@@ -122,7 +122,7 @@ __device__ __forceinline__ GuUnit gu_unit(const Dec2Args &a, const L1Work &w, co
   } else {
     const int x = B - bs;
     u.ai = x / bpe;
-    u.e = s_idx[u.ai];
+    u.e = COLI_CHK(s_idx[u.ai], a.E, a.ctrl);
     u.b = x - u.ai * bpe;
   }
   u.f = 32 * u.b + sub * a.l1_rg;
@@ -148,7 +148,7 @@ __device__ __forceinline__ void l1_issue(const Dec2Args &a, const L1Work &w, con
     const int d = s - w.n_gu, ai = d / w.spe;
     const int r0 = (d - ai * w.spe) * a.l1_dr;
     const int nq = w.nr - r0 < a.l1_dr ? w.nr - r0 : a.l1_dr;
-    const int e = ai < a.k ? s_idx[ai] : a.E + (ai - a.k);
+    const int e = ai < a.k ? COLI_CHK(s_idx[ai], a.E, a.ctrl) : a.E + (ai - a.k);
     const int64_t rb = a.F / 2, ngr = a.F / kGroup;
     const int64_t row = w.dh0 + r0;
     const uint8_t *pd = a.packed + (int64_t)e * a.eb + (int64_t)a.F * a.H + row * rb;
@@ -188,7 +188,7 @@ __device__ void l1_route(const Dec2Args &a, uint8_t *scratch, int *s_idx, float 
     for (int i = threadIdx.x; i < k; i += blockDim.x) {
       a.g_idx[i] = s_idx[i];
       a.g_gates[i] = s_gate[i];
-      if (a.route_counts) atomicAdd(a.route_counts + s_idx[i], 1u);
+      if (a.route_counts) atomicAdd(a.route_counts + COLI_CHK(s_idx[i], a.E, a.ctrl), 1u);
     }
   }
   __syncthreads();

@@ -218,7 +218,7 @@ __device__ void route_block(const Dec2Args &a, const LayerPtrs &lp, float *s_log
     for (int i = threadIdx.x; i < T * k; i += nthr) {
       a.g_idx[i] = s_idx[i];
       a.g_gates[i] = s_gates[i];
-      if (lp.route_counts) atomicAdd(lp.route_counts + s_idx[i], 1u);
+      if (lp.route_counts) atomicAdd(lp.route_counts + COLI_CHK(s_idx[i], a.E, a.ctrl), 1u);
     }
   }
 }
@@ -378,7 +378,7 @@ __device__ __forceinline__ void gu_copy(const Dec2Args &a, const LayerPtrs &lp,
                                         bool vec_scales) {
   const int H = a.H, F = a.F, lane = threadIdx.x & 31;
   const int64_t rb = H / 2, ngr = H / kGroup;
-  const int e = s_act_expert[k.ai];
+  const int e = COLI_CHK(s_act_expert[k.ai], a.E + a.S, a.ctrl);
   const int col = k.cg * kChunkCols + 32 * lane;
   const uint8_t *pe;
   const float *se;
@@ -490,7 +490,7 @@ __device__ void gu_lists(const Dec2Args &a, const LayerPtrs &lp, uint8_t *scratc
     for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
       a.g_idx[i] = s_idx[i];
       a.g_gates[i] = s_gates[i];
-      if (lp.route_counts) atomicAdd(lp.route_counts + s_idx[i], 1u);
+      if (lp.route_counts) atomicAdd(lp.route_counts + COLI_CHK(s_idx[i], a.E, a.ctrl), 1u);
     }
     for (int i = threadIdx.x; i < 2 + 2 * (E + S); i += blockDim.x) a.g_act[i] = s_act[i];
     for (int i = threadIdx.x; i < T * KS; i += blockDim.x) {
@@ -740,7 +740,7 @@ __global__ void __launch_bounds__(kGuOneMaxThreads) k_gateup(Dec2Args a) {
         gs += red[(i * ncg + q) * 2];
         us += red[(i * ncg + q) * 2 + 1];
       }
-      const int slot_id = s_routes[s_act_off[ai]];
+      const int slot_id = COLI_CHK(s_routes[s_act_off[ai]], a.T * (a.k + a.S), a.ctrl);
       const float hv = silu(gs) * us * s_slot_gate[slot_id];
       for (int rr = 0; rr < a.n_rep; ++rr) a.h[rr * a.h_stride + (int64_t)slot_id * F + f] = hv;
     }
@@ -869,7 +869,7 @@ __global__ void __launch_bounds__(kGuMultiMaxThreads) k_gateup_multi(Dec2Args a)
     if (warp == 0) {
       const int r0 = s_act_off[u0 / gpe], r1 = s_act_off[(u1 - 1) / gpe + 1];
       uint32_t need = 0;
-      for (int r = r0 + lane; r < r1; r += 32) need |= 1u << (s_routes[r] / KS);
+      for (int r = r0 + lane; r < r1; r += 32) need |= 1u << (COLI_CHK(s_routes[r], T * KS, a.ctrl) / KS);
       need = __reduce_or_sync(0xFFFFFFFFu, need);
       if (lane < T) {
         const bool mine = (need >> lane) & 1u;
@@ -927,7 +927,7 @@ __global__ void __launch_bounds__(kGuMultiMaxThreads) k_gateup_multi(Dec2Args a)
     gu_slot_values(slot, act, vec_scales, w, sc);
     const int j0 = s_act_off[cc.ai], nt = s_act_off[cc.ai + 1] - j0;
     for (int j = 0; j < nt; ++j) {
-      const int t = s_routes[j0 + j] / KS;
+      const int t = COLI_CHK(s_routes[j0 + j], T * KS, a.ctrl) / KS;
       float v[8];
       if (act) {
         const int key = t * ncg + cc.cg;
@@ -958,7 +958,7 @@ __global__ void __launch_bounds__(kGuMultiMaxThreads) k_gateup_multi(Dec2Args a)
       for (int it = lane; it < 4 * nt; it += 32) {
         const int j = it >> 2, r = it & 3;
         const float gs = acc[j * 8 + 2 * r], us = acc[j * 8 + 2 * r + 1];
-        const int slot_id = s_routes[j0 + j];
+        const int slot_id = COLI_CHK(s_routes[j0 + j], T * KS, a.ctrl);
         const float hv = silu(gs) * us * s_slot_gate[slot_id];
         for (int rr = 0; rr < a.n_rep; ++rr)
           a.h[rr * a.h_stride + (int64_t)slot_id * F + cc.f + r] = hv;
@@ -993,7 +993,7 @@ __device__ __forceinline__ void dn_copy(const Dec2Args &a, const LayerPtrs &lp,
                                         int dh0, int nr, bool vec_scales) {
   const int H = a.H, F = a.F, lane = threadIdx.x & 31;
   const int64_t rb = F / 2, ngr = F / kGroup;
-  const int e = s_act_expert[k.a];
+  const int e = COLI_CHK(s_act_expert[k.a], a.E + a.S, a.ctrl);
   const int col = k.cg * kChunkCols + 32 * lane;
   const int r0 = 8 * k.gi, nq = nr - r0 < 8 ? nr - r0 : 8;
   const uint8_t *pe;
@@ -1102,7 +1102,8 @@ __device__ void dn_phase(const Dec2Args &a, const LayerPtrs &lp, const int *s_ac
       if (act && key != pl_key) {
         // the h loads go out before this task's weights are waited for
         float xv[32];
-        load32<float>(h_rep + (int64_t)s_routes[s_act_off[cc.a]] * F + col, xv);
+        load32<float>(h_rep + (int64_t)COLI_CHK(s_routes[s_act_off[cc.a]], T * KS, a.ctrl) * F + col,
+                      xv);
         quantize32(xv, pl);
         pl_key = key;
       }
@@ -1251,7 +1252,7 @@ __device__ __forceinline__ void dm_loop(const Dec2Args &a, const LayerPtrs &lp,
             load_planes(s_planes, j0 + j - r0, col / 32, nbp, pl);
           } else {
             float xv[32];
-            load32<float>(h_rep + (int64_t)s_routes[j0 + j] * F + col, xv);
+            load32<float>(h_rep + (int64_t)COLI_CHK(s_routes[j0 + j], a.T * (a.k + a.S), a.ctrl) * F + col, xv);
             quantize32(xv, pl);
           }
           pl_key = key;
@@ -1272,7 +1273,7 @@ __device__ __forceinline__ void dm_loop(const Dec2Args &a, const LayerPtrs &lp,
       __syncwarp();
       for (int it = lane; it < 8 * nt; it += 32) {
         const int j = it >> 3, q = it & 7;
-        a.y[(size_t)s_routes[j0 + j] * H + row0 + q] = acc[j * 8 + q];
+        a.y[(size_t)COLI_CHK(s_routes[j0 + j], a.T * (a.k + a.S), a.ctrl) * H + row0 + q] = acc[j * 8 + q];
       }
     }
     __syncwarp();

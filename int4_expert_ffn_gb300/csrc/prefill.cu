@@ -574,7 +574,7 @@ __global__ void __launch_bounds__(256) k_ptopk(PrefillArgs p) {
   for (int i = threadIdx.x; i < TB * k; i += blockDim.x) {
     p.idx[(size_t)t0 * k + i] = s_idx[i];
     p.gates[(size_t)t0 * k + i] = s_gates[i];
-    if (p.route_counts) atomicAdd(p.route_counts + s_idx[i], 1u);
+    if (p.route_counts) atomicAdd(p.route_counts + COLI_CHK(s_idx[i], p.E, p.ctrl), 1u);
   }
 }
 
@@ -666,7 +666,7 @@ __global__ void __launch_bounds__(256) k_gscatter(PrefillArgs p) {
     }
     first = __shfl_sync(~0u, first, leader);
     if (e >= 0) {
-      const int pos = first + __popc(same & lower);
+      const int pos = COLI_CHK(first + __popc(same & lower), T * (k + p.S), p.ctrl);
       p.route_tok[pos] = g / k;
       p.route_gate[pos] = p.gates[g];
       p.inv[g] = pos;
@@ -713,6 +713,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
   const int K = MODE == kModeGateUp ? H : F;
   const int nk = K / kBK;
   const int n_ntiles = MODE == kModeGateUp ? F / (kBN / 2) : H / kBN;
+  const int P_routes = p.T * (p.k + p.S);    // rows of h16 / y, entries of route_tok
+  (void)P_routes;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNB; ++s) {
@@ -774,14 +776,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
       if (t < n_ticks) {
         if (kt == 0) {
           it = decode_item(s_begin, s_off, p.n_groups, blockIdx.x + item * gridDim.x, n_ntiles);
+          it.e = COLI_CHK(it.e, p.n_groups, p.ctrl);
 #pragma unroll
           for (int j = 0; j < kARowPasses; ++j) {
             const int r = a_row0 + 32 * j;
             a_ok[j] = r < it.rows;
             a_src[j] = nullptr;
             if (a_ok[j])
-              a_src[j] = MODE == kModeGateUp ? p.x16 + (int64_t)p.route_tok[it.p0 + r] * H
-                                             : p.h16 + (int64_t)(it.p0 + r) * F;
+              a_src[j] = MODE == kModeGateUp
+                             ? p.x16 + (int64_t)COLI_CHK(p.route_tok[COLI_CHK(it.p0 + r, P_routes, p.ctrl)],
+                                                         p.T, p.ctrl) * H
+                             : p.h16 + (int64_t)COLI_CHK(it.p0 + r, P_routes, p.ctrl) * F;
           }
           const uint8_t *pk;
           const uint8_t *sc;
@@ -928,7 +933,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(PrefillArgs p) {
       tc_fence_after();
       const Item it = decode_item(s_begin, s_off, p.n_groups, blockIdx.x + i * gridDim.x, n_ntiles);
       const int r = 32 * q + lane;
-      const bool r_ok = r < it.rows;
+      // (a checked build also drops a row outside the route arrays)
+      const bool r_ok = r < it.rows && COLI_CHK(it.p0 + r, P_routes, p.ctrl) == it.p0 + r;
       const uint32_t trow = tbase + lane_off + (uint32_t)(buf * kBN);
       if (MODE == kModeGateUp) {
         const float gate = r_ok ? p.route_gate[it.p0 + r] : 0.0f;
@@ -995,7 +1001,7 @@ __global__ void k_pcombine(PrefillArgs p) {
     const int t = (int)(i / H4), c = (int)(i - (int64_t)t * H4);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; ++j) {
-      const float4 v = ((const float4 *)(p.y + (int64_t)p.inv[t * k + j] * H))[c];
+      const float4 v = ((const float4 *)(p.y + (int64_t)COLI_CHK(p.inv[t * k + j], T * k, p.ctrl) * H))[c];
       acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
     for (int s = 0; s < S; ++s) {

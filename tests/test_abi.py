@@ -34,7 +34,7 @@ def test_library_exports_every_declared_symbol(coli):
 
 
 def test_status_strings(coli):
-    for st in range(0, -10, -1):
+    for st in range(0, -11, -1):
         assert coli.lib.coli_status_str(st) != b"unknown status", st
     assert coli.lib.coli_status_str(-99) == b"unknown status"
 
