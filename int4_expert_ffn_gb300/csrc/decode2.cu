@@ -8,16 +8,20 @@
 //
 // Per layer, kernels chained with programmatic dependent launch inside one
 // CUDA graph per step:
-//   k_route (first layer of a pass): the router partial logits of each CTA's
-//     slice of the hidden dimension, added as fixed-point integers.
+//   k_route (first layer of a several-token pass): the router partial logits
+//     of each CTA's slice of the hidden dimension, added as fixed-point
+//     integers.  With one token the first layer's gate/up CTAs form the
+//     logits themselves instead (gu_router_logits: each CTA the whole logits
+//     of its own experts, published as never-zero words every CTA waits for).
 //   k_gateup (one token) / k_gateup_multi (several): every CTA routes the
-//     layer itself from the fixed-point logits (top-k, union lists; CTA 0
-//     publishes them and the route counts), then streams its share of the
-//     used experts' gate/up rows through per-warp cp.async rings in shared
-//     memory and writes h = silu(g) * u * gate.
+//     layer itself from the logits (top-k, union lists; CTA 0 publishes them
+//     and the route counts), then streams its share of the used experts'
+//     gate/up rows through per-warp cp.async rings in shared memory and
+//     writes h = silu(g) * u * gate.
 //   k_down (one token): each CTA owns a block of output rows of every used
 //     expert's down matrix, sums the experts in a fixed order, adds the
-//     residual, and adds its rows' share of the next layer's router logits.
+//     residual, and adds its rows' share of the next layer's router logits;
+//     its warp count makes the largest number of tasks per warp smallest.
 //   k_down_multi + k_down (several tokens): the down GEMVs split by expert
 //     and cost into per-slot outputs, then k_down adds each token's slots.
 //
