@@ -45,17 +45,18 @@ namespace coli {
 namespace {
 
 // Phase trace of k_layer1, compiled in only with -DCOLI_TRACE (a diagnostic
-// build): one %globaltimer stamp per (point, CTA), read by coli_trace1_read_raw.
+// build): one %globaltimer stamp per (layer, point, CTA) for the first
+// kT1Layers layers of a call, read by coli_trace1_read_raw.
 #ifdef COLI_TRACE
-constexpr int kT1Points = 12, kT1Ctas = 160;
-static __device__ unsigned long long g_trace1[kT1Points][kT1Ctas];
-__device__ __forceinline__ void t1_point(int pt) {
-  if (blockIdx.x >= kT1Ctas) return;
+constexpr int kT1Layers = 4, kT1Points = 12, kT1Ctas = 160;
+static __device__ unsigned long long g_trace1[kT1Layers][kT1Points][kT1Ctas];
+__device__ __forceinline__ void t1_point(int layer, int pt) {
+  if (blockIdx.x >= kT1Ctas || layer < 0 || layer >= kT1Layers) return;
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  g_trace1[pt][blockIdx.x] = t;
+  g_trace1[layer][pt][blockIdx.x] = t;
 }
-#define T1(pt, who) do { if (threadIdx.x == (who)) t1_point(pt); } while (0)
+#define T1(pt, who) do { if (threadIdx.x == (who)) t1_point(a.layer, pt); } while (0)
 #else
 #define T1(pt, who) do {} while (0)
 #endif
@@ -287,6 +288,30 @@ __device__ __forceinline__ void l1_down_stage(const Dec2Args &a, const L1Work &w
   }
 }
 
+// The next layer's router-row slice ([E][nr] values of type WT, this CTA's
+// columns dh0 .. dh0 + nr) into shared memory by cp.async, 8 bytes per copy,
+// so the kernel does not wait for it at its start; the partials at the end
+// wait for the group.  dh0 and nr are multiples of 4 and the rows whole
+// multiples of 1024 values, so with an 8-byte aligned base every piece is
+// aligned.  Returns false (nothing issued) for a misaligned base.
+template <typename WT>
+__device__ __forceinline__ bool l1_router_rows_async(const Dec2Args &a, const WT *wr, WT *s_wr) {
+  if (((uintptr_t)wr & 7) != 0) return false;
+  const int H = a.H, E = a.E, G = gridDim.x, c = blockIdx.x, UH = H / 4;
+  const int dh0 = 4 * part_lo(c, UH, G), nr = 4 * part_lo(c + 1, UH, G) - dh0;
+  constexpr int kPer = 8 / (int)sizeof(WT);     // values per 8-byte piece
+  const int ppr = nr / kPer;                    // pieces per row
+  for (int i = threadIdx.x; i < E * ppr; i += blockDim.x) {
+    const int e = i / ppr, q = i - e * ppr;
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(
+                     smem_u32(s_wr + (size_t)e * nr + q * kPer)),
+                 "l"(wr + (size_t)e * H + dh0 + q * kPer)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  return true;
+}
+
 template <typename WT>
 __global__ void __launch_bounds__(kL1Threads, 1) k_layer1(Dec2Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -334,7 +359,8 @@ __global__ void __launch_bounds__(kL1Threads, 1) k_layer1(Dec2Args a) {
     l1_issue(a, w, s_idx, ring, full, slot_of(0), warp);
     issued = 1;
   }
-  if (a.wr) load_router_rows<WT>(a, (const WT *)a.wr, s_wr);
+  if (a.wr && !l1_router_rows_async<WT>(a, (const WT *)a.wr, s_wr))
+    load_router_rows<WT>(a, (const WT *)a.wr, s_wr);
   if (a.router_fn == COLI_ROUTER_SIGMOID_BIAS && a.router_bias) {
     float *s_bias = (float *)(U + gu_route_smem(1, a.E, a.k).bias);
     for (int i = tid; i < a.E; i += blockDim.x) s_bias[i] = __ldg(a.router_bias + i);
@@ -462,8 +488,13 @@ __global__ void __launch_bounds__(kL1Threads, 1) k_layer1(Dec2Args a) {
     if (a.xrep)
       for (int rr = 0; rr < a.n_rep; ++rr) a.xrep[rr * a.x_stride + o] = xn;
   }
+  // this thread's router-row pieces (if any) have landed; the barrier makes
+  // every thread's visible
+  asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
+  T1(10, 0);
   if (a.wr) dn_partials_fx<WT>(a, s_wr, s_xn);
+  T1(11, 0);
 }
 
 }  // namespace
@@ -474,7 +505,7 @@ extern "C" int coli_trace1_reset() {
   if (cudaGetSymbolAddress(&p, g_trace1) != cudaSuccess) return -1;
   return cudaMemset(p, 0, sizeof(g_trace1)) == cudaSuccess ? 0 : -1;
 }
-// [point][cta] timestamps in ns (0: not reached).
+// [layer][point][cta] timestamps in ns (0: not reached).
 extern "C" int coli_trace1_read_raw(void *buf) {
   return cudaMemcpyFromSymbol(buf, g_trace1, sizeof(g_trace1)) == cudaSuccess ? 0 : -1;
 }
