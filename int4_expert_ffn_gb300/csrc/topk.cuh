@@ -38,6 +38,24 @@ __device__ __forceinline__ void block_gates(const float *vals, int T, int k, flo
   }
 }
 
+// The same gates for k <= 32: a warp per token, lane j holds pick j, one
+// exponential per lane; the denominator is a butterfly sum, which leaves the
+// identical value in every lane (a + b == b + a at every level).
+__device__ __forceinline__ void warp_gates(const float *vals, int T, int k, float *gates) {
+  const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  for (int t = threadIdx.x >> 5; t < T; t += nw) {
+    const float *vt = vals + t * k;
+    const float l0 = vt[0];
+    const float v = lane < k ? vt[lane] : __int_as_float(0x7FC00000);   // no term
+    const float e = (v != v) ? 0.0f : expf(v - l0);
+    float den = e;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xFFFFFFFFu, den, off);
+    if (lane < k)
+      gates[t * k + lane] = (l0 != l0) ? 1.0f / (float)k : ((v != v) ? 0.0f : e / den);
+  }
+}
+
 // Order key of a logit: the float order mapped onto unsigned integers, NaN
 // lowest and -0 folded into +0.  ranks_before(a, ia, b, ib) is exactly
 // key(a) > key(b) || (key(a) == key(b) && ia < ib).
@@ -163,9 +181,9 @@ __device__ __forceinline__ bool warp_topk(const float *lg, int T, int E, int k, 
 // token with a shuffle bitonic network on 64-bit keys (order key, then the
 // complement of the expert id, so keys are distinct and larger ranks first;
 // padding is 0, below every logit) and keeps its k best; one thread per
-// candidate then counts the token's larger candidates.  s_cand: T *
-// ceil(E/32) * k 64-bit words.  Returns true (on every thread) if any logit
-// is NaN.
+// candidate then counts the token's larger candidates (a quad of lanes per
+// candidate, each over every fourth entry).  s_cand: T * ceil(E/32) * k 64-bit
+// words.  Returns true (on every thread) if any logit is NaN.
 __device__ __forceinline__ bool tournament_topk(const float *lg, int T, int E, int k, int *idx,
                                                 float *gates, float *vals,
                                                 unsigned long long *s_cand, int *s_flag) {
@@ -193,21 +211,26 @@ __device__ __forceinline__ bool tournament_topk(const float *lg, int T, int E, i
     if (lane < k) s_cand[(size_t)t * C + ch * k + lane] = key;
   }
   __syncthreads();
-  for (int i = tid; i < T * C; i += blockDim.x) {
+  // blockDim is a multiple of 32, so a quad's four lanes share i in every
+  // iteration and leave the loop together
+  const unsigned qmask = 0xFu << (lane & 28);
+  for (int i4 = tid; i4 < 4 * T * C; i4 += blockDim.x) {
+    const int i = i4 >> 2, q = i4 & 3;
     const int t = i / C;
     const unsigned long long c = s_cand[i];
-    if (c == 0ull) continue;
     const unsigned long long *row = s_cand + (size_t)t * C;
     int r = 0;
-    for (int j = 0; j < C; ++j) r += row[j] > c;
-    if (r < k) {
+    for (int j = q; j < C; j += 4) r += row[j] > c;
+    r += __shfl_xor_sync(qmask, r, 1);
+    r += __shfl_xor_sync(qmask, r, 2);
+    if (q == 0 && c != 0ull && r < k) {    // c == 0: padding of a short chunk
       const int e = (int)(0xFFFFFFFFu - (uint32_t)c);
       idx[t * k + r] = e;
       vals[t * k + r] = lg[(size_t)t * E + e];
     }
   }
   __syncthreads();
-  block_gates(vals, T, k, gates);
+  warp_gates(vals, T, k, gates);
   const bool nan = *(volatile int *)s_flag != 0;
   __syncthreads();
   return nan;
