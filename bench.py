@@ -38,7 +38,12 @@ METRIC = "MoE decode tokens/s and int4 expert-weight GB/s vs GB300 HBM peak"
 # workload and kernel; absent (null in the line) until such a capture exists
 # or once the kernel has changed since.  Batch 1: the per-layer launch is the
 # same in a 1- or 2-layer capture as in the full stack.
-NCU_TRAFFIC = {
+NCU_TRAFFIC = {}
+
+# Captures of earlier builds of kernels that have changed since (the top-k
+# inside the decode kernels' routing; the quantiser's lane teams).  The line
+# reports them beside a null traffic, labelled as such, not as the traffic.
+NCU_TRAFFIC_EARLIER = {
     # the one-token layer kernel (one launch per layer; mean of two captured launches)
     "olmoe_decode": {"k_layer1": 28637184},
     # the one-token gate/up (with the first layer's router) and down kernels
@@ -46,7 +51,11 @@ NCU_TRAFFIC = {
     # the several-token kernel k_gateup_multi; its experts per launch vary with
     # the routing
     "glm_decode_b8": {"k_gateup": 879500288 + 7344384},
+    # one launch over 16 experts' matrices: 402.7 MB read, 55.8 MB written
+    "quant16": {"k_quant_vec": 402740480 + 55846144},
 }
+EARLIER_NOTE = ("traffic is null: the kernel changed after its last ncu capture; "
+                "traffic_earlier_build is that capture")
 
 
 def read_peaks():
@@ -820,6 +829,7 @@ def main():
     kd = kern[dom]
     k_gbs = kd["alg_bytes_per_launch"] / (kd["us_per_launch"] * 1e-6) / 1e9
     traffic = NCU_TRAFFIC.get(args.workload, {}).get(dom)
+    earlier = NCU_TRAFFIC_EARLIER.get(args.workload, {}).get(dom) if traffic is None else None
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"] / args.steps,
@@ -832,6 +842,8 @@ def main():
                      "unit": "GB/s", "frac": k_gbs / hbm_peak,
                      "peak_kind": "%s (hbm_gbs, burst copy)" % peak_kind,
                      "traffic": traffic,
+                     **({"traffic_earlier_build": earlier, "traffic_note": EARLIER_NOTE}
+                        if earlier is not None else {}),
                      "alg_bytes_per_launch": kd["alg_bytes_per_launch"],
                      "us_per_launch": kd["us_per_launch"]},
         "step_roofline": {"achieved": gbs, "unit": "GB/s", "frac": gbs / hbm_peak,
@@ -904,13 +916,13 @@ def emit_quant(args, dev, world, rank):
         "config": {"workload": "quantiser: %d experts x {gate, up [2048,6144], down [6144,2048]}" % E,
                    "elements": elems, "bytes_per_step": nbytes,
                    "l2": "inputs larger than L2 (%.1f GB)" % (nbytes / 1e9)},
-        # traffic per launch: an ncu capture of one launch over 16 experts' matrices
-        # read 402.7 MB and wrote 55.8 MB; a launch here covers E experts'
-        # matrices of the same shape, so scaled by E / 16
+        # a launch here covers E experts' matrices of the 16-expert capture's
+        # shape, so a capture scales by E / 16
         "roofline": {"bound": "hbm", "kernel": "k_quant_vec", "achieved": gbs, "peak": hbm_peak,
                      "unit": "GB/s", "frac": gbs / hbm_peak, "peak_kind": peak_kind,
-                     "traffic": (402740480 + 55846144) * E / 16,
-                     "traffic_note": "from a 16-expert capture, scaled by experts"},
+                     "traffic": None,
+                     "traffic_earlier_build": NCU_TRAFFIC_EARLIER["quant16"]["k_quant_vec"] * E / 16,
+                     "traffic_note": EARLIER_NOTE + " (a 16-expert capture, scaled by experts)"},
         "clocks": sampler.summary(t0, t1), "gpu_launches": 3 * args.steps,
     }
     if rank == 0:
