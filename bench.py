@@ -40,9 +40,10 @@ METRIC = "MoE decode tokens/s and int4 expert-weight GB/s vs GB300 HBM peak"
 # same in a 1- or 2-layer capture as in the full stack.
 NCU_TRAFFIC = {}
 
-# Captures of earlier builds of kernels that have changed since (the top-k
-# inside the decode kernels' routing; the quantiser's lane teams).  The line
-# reports them beside a null traffic, labelled as such, not as the traffic.
+# Captures of earlier builds of kernels that have changed since (the decode
+# kernels' routing code, and for batch 8 also the expert-record lookup of the
+# tiered store; the quantiser's lane teams).  The line reports them beside a
+# null traffic, labelled as such, not as the traffic.
 NCU_TRAFFIC_EARLIER = {
     # the one-token layer kernel (one launch per layer; mean of two captured launches)
     "olmoe_decode": {"k_layer1": 28637184},
